@@ -1,0 +1,236 @@
+"""CPU oracle for the FP8 linear-layer hot path (test infrastructure only).
+
+This package wraps ``fp8_oracle.c`` -- a plain, slow, scalar C restatement of
+what the path computes -- through ctypes and numpy.  Only the tests, the smoke
+check and the benchmark's CPU-baseline leg may import it; the CUDA library and
+its Python binding never do, and this package imports nothing from them.
+
+Sources of each definition are cited in ``fp8_oracle.c``:
+  * "FP8 training for Flux models" (Configuration > Key FP8 Parameters): the
+    recipe knobs -- format, recipe, margin, amax history length, amax compute
+    algorithm.
+  * "FP8 Training on MI300X" ("Discovered AMD FP8 dtype difference", "Patched
+    nanochat/fp8.py"): E4M3 forward / E5M2 backward, e4m3fn max 448 against
+    e4m3fnuz max 240.
+  * "How PyTorch FP8 Optimizations on AMD GPUs ..." (What Happened) and "FP8
+    Training on AMD GPUs with TorchTitan and TorchAO": rowwise scaling,
+    colwise scales with a transposed layout, grouped GEMM for MoE.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+E4M3FN, E5M2, E4M3FNUZ = 0, 1, 2
+DELAYED, TENSORWISE, ROWWISE = 0, 1, 2
+MOST_RECENT, MAX = 0, 1
+LAYOUT_ROW, LAYOUT_COLT = 1, 2
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "fp8_oracle.c")
+_LIB_DIR = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_LIB_DIR, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (ISO C11, no FMA contraction, OpenMP)."""
+    os.makedirs(_LIB_DIR, exist_ok=True)
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fopenmp",
+               "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            i64, i32, f32, f64 = ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_double
+            lib.orc_fp8_decode.restype = f64
+            lib.orc_fp8_decode.argtypes = [i32, i32]
+            lib.orc_fp8_encode.restype = i32
+            lib.orc_fp8_encode.argtypes = [f64, i32]
+            lib.orc_fp8_max_code.restype = i32
+            lib.orc_fp8_max_code.argtypes = [i32]
+            lib.orc_fp8_nan_code.restype = i32
+            lib.orc_fp8_nan_code.argtypes = [i32]
+            lib.orc_fp8_max_value.restype = f64
+            lib.orc_fp8_max_value.argtypes = [i32]
+            lib.orc_current_scale.restype = None
+            lib.orc_current_scale.argtypes = [f32, i32, i32, P, P]
+            lib.orc_padded_offsets.restype = i64
+            lib.orc_padded_offsets.argtypes = [P, i32, P]
+            lib.orc_quantize.restype = i32
+            lib.orc_quantize.argtypes = [P, i64, i64, i64, i32, i32, i32, i32, P, P, P, P, P, P, P, i32]
+            lib.orc_amax_bf16.restype = f32
+            lib.orc_amax_bf16.argtypes = [P, i64, i64, i64]
+            lib.orc_cast_points.restype = None
+            lib.orc_cast_points.argtypes = [P, P, i64, i32, P]
+            lib.orc_update_amax_history.restype = None
+            lib.orc_update_amax_history.argtypes = [P, P, P, P, i32, i32, i32, i32, P]
+            lib.orc_gemm.restype = None
+            lib.orc_gemm.argtypes = [P, i32, i64, P, i32, i64, i64, i64, i64, P, i32, P, i32,
+                                     P, P, i64, P, P]
+            lib.orc_grouped_gemm.restype = None
+            lib.orc_grouped_gemm.argtypes = [i32, P, i32, P, i32, P, i32, i64, i64, i64, P, i32,
+                                             P, i32, P, P, P, i64, P, P]
+            _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else ctypes.c_void_p(a.ctypes.data)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+# --- codec ---------------------------------------------------------------
+
+def fp8_decode(code: int, fmt: int) -> float:
+    return _load().orc_fp8_decode(int(code), int(fmt))
+
+
+def fp8_encode(v: float, fmt: int) -> int:
+    """Round an fp32 value (given as a Python float) to the nearest code."""
+    return _load().orc_fp8_encode(float(np.float32(v)), int(fmt))
+
+
+def fp8_max_code(fmt: int) -> int:
+    return _load().orc_fp8_max_code(int(fmt))
+
+
+def fp8_nan_code(fmt: int) -> int:
+    return _load().orc_fp8_nan_code(int(fmt))
+
+
+def fp8_max_value(fmt: int) -> float:
+    return _load().orc_fp8_max_value(int(fmt))
+
+
+def decode_table(fmt: int) -> np.ndarray:
+    return np.array([fp8_decode(c, fmt) for c in range(256)], dtype=np.float64)
+
+
+def current_scale(amax: float, fmt: int, margin: int = 0):
+    s, si = ctypes.c_float(), ctypes.c_float()
+    _load().orc_current_scale(float(np.float32(amax)), fmt, margin, ctypes.byref(s), ctypes.byref(si))
+    return np.float32(s.value), np.float32(si.value)
+
+
+# --- quantize ------------------------------------------------------------
+
+def padded_offsets(offsets) -> np.ndarray:
+    off = _c(offsets, np.int32)
+    G = off.size - 1
+    poff = np.zeros(G + 1, dtype=np.int64)
+    _load().orc_padded_offsets(_ptr(off), G, _ptr(poff))
+    return poff
+
+
+def quantize(x_bits, fmt, kind, margin=0, layouts=LAYOUT_ROW | LAYOUT_COLT, scale_in=None,
+             amax_io=None, offsets=None):
+    """Quantize a bf16 matrix given as its uint16 bit patterns [rows, cols].
+
+    Returns a dict with q_row [rows, cols] u8, scale_inv_row, q_colT
+    [cols, ldT] u8, scale_inv_col, amax (the value left in amax_io).
+    """
+    x = _c(x_bits, np.uint16)
+    rows, cols = x.shape
+    G = 0 if offsets is None else len(offsets) - 1
+    off = None if offsets is None else _c(offsets, np.int32)
+    ldT = rows if off is None else int(padded_offsets(off)[-1])
+    q_row = np.zeros((rows, cols), np.uint8) if layouts & LAYOUT_ROW else None
+    q_colT = np.zeros((cols, ldT), np.uint8) if layouts & LAYOUT_COLT else None
+    if kind == ROWWISE:
+        sr = np.zeros(rows, np.float32)
+        sc = np.zeros((G, cols) if off is not None else cols, np.float32)
+    else:
+        sr = np.zeros(1, np.float32)
+        sc = np.zeros(1, np.float32)
+    sin = None if scale_in is None else _c(np.atleast_1d(scale_in), np.float32)
+    amax = np.array([0.0 if amax_io is None else amax_io], np.float32)
+    _load().orc_quantize(_ptr(x), rows, cols, cols, fmt, kind, margin, layouts, _ptr(sin), _ptr(amax),
+                         _ptr(q_row), _ptr(sr), _ptr(q_colT), _ptr(sc), _ptr(off), G)
+    return dict(q_row=q_row, scale_inv_row=sr, q_colT=q_colT, scale_inv_col=sc, amax=np.float32(amax[0]))
+
+
+def amax_bf16(x_bits) -> np.float32:
+    x = _c(x_bits, np.uint16)
+    if x.ndim == 1:
+        x = x.reshape(1, -1)
+    return np.float32(_load().orc_amax_bf16(_ptr(x), x.shape[0], x.shape[1], x.shape[1]))
+
+
+def cast_points(x_bits, scales, fmt) -> np.ndarray:
+    """encode(fp32(x[i]) * scales[i]) for selected elements."""
+    x = _c(x_bits, np.uint16).ravel()
+    s = _c(np.broadcast_to(np.asarray(scales, np.float32), x.shape), np.float32)
+    out = np.zeros(x.size, np.uint8)
+    _load().orc_cast_points(_ptr(x), _ptr(s), x.size, fmt, _ptr(out))
+    return out
+
+
+# --- history update ------------------------------------------------------
+
+def update_amax_history(hist, scale, scale_inv, fmt, algo, margin, nonfinite=None):
+    """In-place update of numpy arrays hist [n, L], scale [n], scale_inv [n]."""
+    assert hist.dtype == np.float32 and hist.flags.c_contiguous
+    n, L = hist.shape
+    fm = _c(np.broadcast_to(np.asarray(fmt, np.uint8), (n,)), np.uint8)
+    _load().orc_update_amax_history(_ptr(hist), _ptr(scale), _ptr(scale_inv), _ptr(fm), n, L, algo, margin,
+                                    _ptr(nonfinite))
+
+
+# --- GEMM ------------------------------------------------------------------
+
+def gemm(A, fa, B, fb, sa, sb, points=None):
+    """Dequantised TN GEMM in double.  A [M, K] u8, B [N, K] u8.
+
+    sa / sb: scalar (one scale) or vector [M] / [N].  points: optional
+    (pm, pn) int arrays.  Returns (ref, bound) as float64 arrays ([M, N] or
+    [npts]).
+    """
+    A = _c(A, np.uint8)
+    B = _c(B, np.uint8)
+    M, K = A.shape
+    N = B.shape[0]
+    sa_a = _c(np.atleast_1d(sa), np.float32)
+    sb_a = _c(np.atleast_1d(sb), np.float32)
+    if points is None:
+        ref = np.zeros((M, N)); bound = np.zeros((M, N)); pm = pn = None; npts = 0
+    else:
+        pm = _c(points[0], np.int64); pn = _c(points[1], np.int64); npts = pm.size
+        ref = np.zeros(npts); bound = np.zeros(npts)
+    _load().orc_gemm(_ptr(A), fa, K, _ptr(B), fb, K, M, N, K, _ptr(sa_a), int(sa_a.size > 1),
+                     _ptr(sb_a), int(sb_a.size > 1), _ptr(pm), _ptr(pn), npts, _ptr(ref), _ptr(bound))
+    return ref, bound
+
+
+def grouped_gemm(mode, A, fa, B, fb, offsets, N, K, sa, sb, pg, pm, pn):
+    """Sampled grouped GEMM (see orc_grouped_gemm).  Returns (ref, bound)."""
+    A = _c(A, np.uint8)
+    B = _c(B, np.uint8)
+    off = _c(offsets, np.int32)
+    G = off.size - 1
+    sa_a = _c(np.atleast_1d(sa), np.float32)
+    sb_a = _c(np.atleast_1d(sb), np.float32)
+    pm = _c(pm, np.int64); pn = _c(pn, np.int64)
+    pg = _c(pg if pg is not None else np.zeros_like(pm), np.int64)
+    ref = np.zeros(pm.size); bound = np.zeros(pm.size)
+    _load().orc_grouped_gemm(mode, _ptr(A), fa, _ptr(B), fb, _ptr(off), G, int(off[-1]), N, K,
+                             _ptr(sa_a), int(sa_a.size > 1), _ptr(sb_a), int(sb_a.size > 1),
+                             _ptr(pg), _ptr(pm), _ptr(pn), pm.size, _ptr(ref), _ptr(bound))
+    return ref, bound

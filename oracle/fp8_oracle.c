@@ -1,0 +1,498 @@
+/*
+ * fp8_oracle.c -- plain CPU restatement of the FP8 linear-layer hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the oracle that the CUDA library is
+ * checked against.  Only the test-suite, the smoke check and the CPU-baseline
+ * leg of the benchmark may load it; the product path never calls it.  It
+ * shares no source, header, table or helper with the CUDA library.
+ *
+ * What it computes, and where that comes from:
+ *
+ *  - FP8 formats e4m3fn (max 448), e5m2 (max 57344) and e4m3fnuz (max 240,
+ *    one NaN code, no infinities, no negative zero).  The maxima and the fnuz
+ *    conventions are stated on "FP8 Training on MI300X" (section "Discovered
+ *    AMD FP8 dtype difference") and on "FP8 Training on AMD GPUs with
+ *    TorchTitan and TorchAO" (the question "Why does FP8 training on AMD GPUs
+ *    give silently wrong results ...").  The bit layouts (sign, exponent,
+ *    mantissa, bias) are the public OCP 8-bit float definitions.
+ *  - The scaling recipe knobs (format, recipe, margin, amax history length,
+ *    amax compute algorithm) are the ones listed on "FP8 training for Flux
+ *    models" (section Configuration > Key FP8 Parameters).  The scale formula
+ *    is scale = fp8_max / amax / 2^margin; the quantised value is
+ *    sat_rne_fp8(fp32(x) * scale) and the dequantisation multiplier is
+ *    scale_inv = 1 / scale.
+ *  - Forward tensors in E4M3 and gradients in E5M2 ("hybrid") follow "FP8
+ *    Training on MI300X" (section "Patched nanochat/fp8.py").
+ *  - Rowwise scales and colwise scales with a transposed layout follow "How
+ *    PyTorch FP8 Optimizations on AMD GPUs ..." (section What Happened) and
+ *    the TorchTitan/TorchAO post (the colwise-scales kernel).
+ *  - The grouped GEMM over expert groups follows the same two pages (grouped
+ *    GEMM for Mixture-of-Experts).
+ *
+ * Readings where the pages are silent (each is repeated in the design notes):
+ *  - NaN input encodes to the format's NaN code; |x| above the format maximum
+ *    (or +-Inf) saturates to +-max; ties round to the even code.
+ *  - Current scaling: amax == 0 or non-finite gives scale 1; a scale that
+ *    overflows fp32 becomes FLT_MAX.
+ *  - Delayed update: a non-finite or zero window amax keeps the previous
+ *    scale; a non-finite one also bumps a per-tensor counter.  The history
+ *    row is shifted one slot towards the end (oldest dropped) and slot 0,
+ *    which collects the current step's amax, is zeroed.
+ *  - Grouped colwise layout: group e's columns start at the padded offset
+ *    sum_{e'<e} roundup(m_e', 32); padding bytes are zero.
+ *
+ * Arithmetic: scalar C, fp32 where the method is fp32 (the x*scale product,
+ * the scale divide), exact double for the FP8 rounding decision and for the
+ * dequantised GEMM.  Compile with -ffp-contract=off (no fused multiply-add).
+ * OpenMP only distributes independent outer iterations; every result is
+ * independent of the thread count.
+ */
+#include <float.h>
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_E4M3FN 0
+#define ORC_E5M2 1
+#define ORC_E4M3FNUZ 2
+
+#define ORC_DELAYED 0
+#define ORC_TENSORWISE 1
+#define ORC_ROWWISE 2
+
+#define ORC_MOST_RECENT 0
+#define ORC_MAX 1
+
+#define ORC_LAYOUT_ROW 1
+#define ORC_LAYOUT_COLT 2
+
+/* ------------------------------------------------------------------------ */
+/* FP8 codec                                                                 */
+/* ------------------------------------------------------------------------ */
+
+static int fmt_exp_bits(int fmt) { return fmt == ORC_E5M2 ? 5 : 4; }
+static int fmt_man_bits(int fmt) { return fmt == ORC_E5M2 ? 2 : 3; }
+static int fmt_bias(int fmt)
+{
+    if (fmt == ORC_E5M2) return 15;
+    if (fmt == ORC_E4M3FNUZ) return 8;
+    return 7;
+}
+
+/* Largest finite positive code of each format. */
+int orc_fp8_max_code(int fmt)
+{
+    if (fmt == ORC_E5M2) return 0x7B;     /* 0 11110 11 = 1.75 * 2^15 */
+    if (fmt == ORC_E4M3FNUZ) return 0x7F; /* 0 1111 111 = 1.875 * 2^7 (bias 8) */
+    return 0x7E;                          /* 0 1111 110 = 1.75 * 2^8 */
+}
+
+int orc_fp8_nan_code(int fmt)
+{
+    if (fmt == ORC_E5M2) return 0x7E;
+    if (fmt == ORC_E4M3FNUZ) return 0x80;
+    return 0x7F;
+}
+
+/* Exact value of an 8-bit code, from the sign / exponent / mantissa fields. */
+double orc_fp8_decode(int code, int fmt)
+{
+    int eb = fmt_exp_bits(fmt), mb = fmt_man_bits(fmt), bias = fmt_bias(fmt);
+    int sign = (code >> 7) & 1;
+    int e = (code >> mb) & ((1 << eb) - 1);
+    int m = code & ((1 << mb) - 1);
+    double mag;
+
+    if (fmt == ORC_E4M3FNUZ) {
+        if (code == 0x80) return NAN; /* the only NaN; there is no -0 */
+    } else if (fmt == ORC_E4M3FN) {
+        if (e == 15 && m == 7) return NAN; /* 0x7F / 0xFF */
+    } else {                               /* e5m2: IEEE-style top exponent */
+        if (e == 31) {
+            if (m != 0) return NAN;
+            return sign ? -INFINITY : INFINITY;
+        }
+    }
+    if (e == 0) /* subnormal: m * 2^(1 - bias - mb) */
+        mag = ldexp((double)m, 1 - bias - mb);
+    else /* normal: (2^mb + m) * 2^(e - bias - mb) */
+        mag = ldexp((double)((1 << mb) + m), e - bias - mb);
+    return sign ? -mag : mag;
+}
+
+/* Magnitudes of codes 0 .. max_code, strictly increasing with the code. */
+static double g_mag[3][128];
+static int g_mag_ready = 0;
+
+static void init_tables(void)
+{
+    if (g_mag_ready) return;
+    for (int f = 0; f < 3; f++)
+        for (int c = 0; c <= orc_fp8_max_code(f); c++) g_mag[f][c] = orc_fp8_decode(c, f);
+    g_mag_ready = 1;
+}
+
+/*
+ * Round v to the nearest FP8 value, ties to the even code (= even mantissa),
+ * saturating to +-max (a saturating cast: anything above max, or +-Inf, maps
+ * to +-max).  v is an fp32 value carried exactly in a double, so every
+ * comparison below is exact.
+ */
+int orc_fp8_encode(double v, int fmt)
+{
+    int top = orc_fp8_max_code(fmt);
+    int neg, lo, hi, mag;
+    double a;
+
+    init_tables();
+    if (isnan(v)) return orc_fp8_nan_code(fmt);
+    neg = signbit(v) ? 1 : 0;
+    a = fabs(v);
+    if (a >= g_mag[fmt][top]) {
+        mag = top;
+    } else {
+        /* bracket a: g_mag[lo] <= a < g_mag[hi], hi = lo + 1 */
+        lo = 0;
+        hi = top;
+        while (hi - lo > 1) {
+            int mid = (lo + hi) / 2;
+            if (g_mag[fmt][mid] <= a)
+                lo = mid;
+            else
+                hi = mid;
+        }
+        {
+            double dlo = a - g_mag[fmt][lo], dhi = g_mag[fmt][hi] - a;
+            if (dlo < dhi)
+                mag = lo;
+            else if (dhi < dlo)
+                mag = hi;
+            else
+                mag = (lo % 2 == 0) ? lo : hi;
+        }
+    }
+    if (fmt == ORC_E4M3FNUZ && mag == 0) return 0x00; /* unsigned zero */
+    return (neg << 7) | mag;
+}
+
+double orc_fp8_max_value(int fmt) { return orc_fp8_decode(orc_fp8_max_code(fmt), fmt); }
+
+/* ------------------------------------------------------------------------ */
+/* Scales                                                                    */
+/* ------------------------------------------------------------------------ */
+
+static float bf16_to_float(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+/* scale = fp8_max / amax, then * 2^-margin; overflow becomes FLT_MAX. */
+static float scale_formula(float amax, int fmt, int margin)
+{
+    float fmax = (float)orc_fp8_max_value(fmt);
+    float s = fmax / amax;
+    s = s * ldexpf(1.0f, -margin);
+    if (isinf(s)) s = FLT_MAX;
+    return s;
+}
+
+/* Current scaling (tensorwise / rowwise / colwise). */
+void orc_current_scale(float amax, int fmt, int margin, float *scale, float *scale_inv)
+{
+    float s;
+    if (!(amax > 0.0f) || !isfinite(amax))
+        s = 1.0f;
+    else
+        s = scale_formula(amax, fmt, margin);
+    *scale = s;
+    *scale_inv = 1.0f / s;
+}
+
+/* max with NaN propagation */
+static float amax_acc(float acc, float v)
+{
+    float a = fabsf(v);
+    if (isnan(acc) || isnan(a)) return NAN;
+    return a > acc ? a : acc;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Quantize                                                                  */
+/* ------------------------------------------------------------------------ */
+
+static int64_t roundup32(int64_t m) { return (m + 31) / 32 * 32; }
+
+/* Padded column offsets of the grouped colwise layout; returns the total. */
+int64_t orc_padded_offsets(const int32_t *off, int G, int64_t *poff)
+{
+    int64_t acc = 0;
+    for (int e = 0; e < G; e++) {
+        poff[e] = acc;
+        acc += roundup32((int64_t)off[e + 1] - off[e]);
+    }
+    poff[G] = acc;
+    return acc;
+}
+
+/*
+ * Full quantize of a bf16 matrix x[rows][cols] (row stride ld_x elements).
+ *
+ * kind DELAYED   : cast with the stored scale scale_in[0]; both layouts share
+ *                  it; scale_inv = 1/scale_in[0]; amax_io[0] = max(amax_io[0],
+ *                  amax(x)) (the history slot of the current step).
+ * kind TENSORWISE: scale from the whole tensor's amax (current scaling);
+ *                  amax_io[0] (optional) receives that amax.
+ * kind ROWWISE   : q_row uses one scale per row, q_colT one per column (per
+ *                  group and column when offsets != NULL); amax_io[0]
+ *                  (optional) receives the whole-tensor amax.
+ *
+ * q_row  : [rows][cols] bytes, scale_inv_row: [1] or [rows].
+ * q_colT : [cols][ldT] bytes, ldT = rows (ungrouped) or the padded total
+ *          (grouped); scale_inv_col: [1], [cols] or [G][cols].
+ * offsets: NULL for an ungrouped tensor, else int32 [G+1] with offsets[0] = 0
+ *          and offsets[G] = rows (the row range of each group).
+ */
+int orc_quantize(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, int fmt, int kind,
+                 int margin, int layouts, const float *scale_in, float *amax_io, uint8_t *q_row,
+                 float *scale_inv_row, uint8_t *q_colT, float *scale_inv_col,
+                 const int32_t *offsets, int G)
+{
+    int ngroups = offsets ? G : 1;
+    int64_t *poff = (int64_t *)malloc(sizeof(int64_t) * (ngroups + 1));
+    int64_t ldT;
+    float tensor_amax = 0.0f;
+
+    init_tables();
+    if (offsets) {
+        ldT = orc_padded_offsets(offsets, G, poff);
+    } else {
+        poff[0] = 0;
+        poff[1] = rows;
+        ldT = rows;
+    }
+
+    /* whole-tensor amax */
+    for (int64_t r = 0; r < rows; r++)
+        for (int64_t c = 0; c < cols; c++) tensor_amax = amax_acc(tensor_amax, bf16_to_float(x[r * ld_x + c]));
+
+    if (kind == ORC_DELAYED || kind == ORC_TENSORWISE) {
+        float s, sinv;
+        if (kind == ORC_DELAYED) {
+            s = scale_in[0];
+            sinv = 1.0f / s;
+            if (amax_io) {
+                float prev = amax_io[0];
+                amax_io[0] = (isnan(prev) || isnan(tensor_amax)) ? NAN
+                             : (tensor_amax > prev ? tensor_amax : prev);
+            }
+        } else {
+            orc_current_scale(tensor_amax, fmt, margin, &s, &sinv);
+            if (amax_io) amax_io[0] = tensor_amax;
+        }
+        if (layouts & ORC_LAYOUT_ROW) {
+#pragma omp parallel for schedule(static)
+            for (int64_t r = 0; r < rows; r++)
+                for (int64_t c = 0; c < cols; c++) {
+                    float p = bf16_to_float(x[r * ld_x + c]) * s;
+                    q_row[r * cols + c] = (uint8_t)orc_fp8_encode((double)p, fmt);
+                }
+            scale_inv_row[0] = sinv;
+        }
+        if (layouts & ORC_LAYOUT_COLT) {
+            memset(q_colT, 0, (size_t)(cols * ldT));
+#pragma omp parallel for schedule(static)
+            for (int64_t c = 0; c < cols; c++)
+                for (int e = 0; e < ngroups; e++) {
+                    int64_t r0 = offsets ? offsets[e] : 0, r1 = offsets ? offsets[e + 1] : rows;
+                    for (int64_t r = r0; r < r1; r++) {
+                        float p = bf16_to_float(x[r * ld_x + c]) * s;
+                        q_colT[c * ldT + poff[e] + (r - r0)] = (uint8_t)orc_fp8_encode((double)p, fmt);
+                    }
+                }
+            scale_inv_col[0] = sinv;
+        }
+    } else { /* ROWWISE (current scaling per row, per column / group column) */
+        if (amax_io) amax_io[0] = tensor_amax;
+        if (layouts & ORC_LAYOUT_ROW) {
+#pragma omp parallel for schedule(static)
+            for (int64_t r = 0; r < rows; r++) {
+                float am = 0.0f, s, sinv;
+                for (int64_t c = 0; c < cols; c++) am = amax_acc(am, bf16_to_float(x[r * ld_x + c]));
+                orc_current_scale(am, fmt, margin, &s, &sinv);
+                for (int64_t c = 0; c < cols; c++) {
+                    float p = bf16_to_float(x[r * ld_x + c]) * s;
+                    q_row[r * cols + c] = (uint8_t)orc_fp8_encode((double)p, fmt);
+                }
+                scale_inv_row[r] = sinv;
+            }
+        }
+        if (layouts & ORC_LAYOUT_COLT) {
+            memset(q_colT, 0, (size_t)(cols * ldT));
+#pragma omp parallel for schedule(static)
+            for (int64_t c = 0; c < cols; c++)
+                for (int e = 0; e < ngroups; e++) {
+                    int64_t r0 = offsets ? offsets[e] : 0, r1 = offsets ? offsets[e + 1] : rows;
+                    float am = 0.0f, s, sinv;
+                    for (int64_t r = r0; r < r1; r++) am = amax_acc(am, bf16_to_float(x[r * ld_x + c]));
+                    orc_current_scale(am, fmt, margin, &s, &sinv);
+                    for (int64_t r = r0; r < r1; r++) {
+                        float p = bf16_to_float(x[r * ld_x + c]) * s;
+                        q_colT[c * ldT + poff[e] + (r - r0)] = (uint8_t)orc_fp8_encode((double)p, fmt);
+                    }
+                    scale_inv_col[(int64_t)e * cols + c] = sinv;
+                }
+        }
+    }
+    free(poff);
+    return 0;
+}
+
+/* Whole-tensor amax of a bf16 matrix (NaN propagates). */
+float orc_amax_bf16(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x)
+{
+    float acc = 0.0f;
+    for (int64_t r = 0; r < rows; r++)
+        for (int64_t c = 0; c < cols; c++) acc = amax_acc(acc, bf16_to_float(x[r * ld_x + c]));
+    return acc;
+}
+
+/*
+ * Encode selected elements only: out[i] = encode(fp32(x[i]) * scale[i]).
+ * Lets tests check sampled bytes of full-size tensors one element at a time.
+ */
+void orc_cast_points(const uint16_t *xv, const float *scale, int64_t n, int fmt, uint8_t *out)
+{
+    init_tables();
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; i++) {
+        float p = bf16_to_float(xv[i]) * scale[i];
+        out[i] = (uint8_t)orc_fp8_encode((double)p, fmt);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Amax history and the delayed scale update                                 */
+/* ------------------------------------------------------------------------ */
+
+void orc_update_amax_history(float *hist, float *scale, float *scale_inv, const uint8_t *fmt, int n,
+                             int L, int algo, int margin, int32_t *nonfinite_count)
+{
+    init_tables();
+    for (int i = 0; i < n; i++) {
+        float *H = hist + (int64_t)i * L;
+        float a = H[0];
+        if (algo == ORC_MAX)
+            for (int j = 1; j < L; j++) {
+                if (isnan(a) || isnan(H[j]))
+                    a = NAN;
+                else if (H[j] > a)
+                    a = H[j];
+            }
+        if (isfinite(a) && a > 0.0f) {
+            float s = scale_formula(a, fmt[i], margin);
+            scale[i] = s;
+            scale_inv[i] = 1.0f / s;
+        } else if (!isfinite(a) && nonfinite_count) {
+            nonfinite_count[i] += 1;
+        }
+        for (int j = L - 1; j >= 1; j--) H[j] = H[j - 1];
+        H[0] = 0.0f;
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Dequantised GEMM in double                                                */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * C[m][n] = sum_k dec(A[m][k]) * dec(B[n][k]) * sa(m) * sb(n), A and B both
+ * K-contiguous ("TN").  sa_mode/sb_mode: 0 = one scale, 1 = one per row of
+ * the operand.  bound[m][n] = the same sum of absolute values.
+ * pm/pn: if non-NULL, only the npts points (pm[i], pn[i]) are computed and
+ * written to ref[i], bound[i]; else the full M x N result, row-major.
+ */
+void orc_gemm(const uint8_t *A, int fa, int64_t lda, const uint8_t *B, int fb, int64_t ldb, int64_t M,
+              int64_t N, int64_t K, const float *sa, int sa_mode, const float *sb, int sb_mode,
+              const int64_t *pm, const int64_t *pn, int64_t npts, double *ref, double *bound)
+{
+    double da[256], db[256];
+    int64_t total = pm ? npts : M * N;
+    for (int c = 0; c < 256; c++) {
+        da[c] = orc_fp8_decode(c, fa);
+        db[c] = orc_fp8_decode(c, fb);
+    }
+#pragma omp parallel for schedule(dynamic, 64)
+    for (int64_t i = 0; i < total; i++) {
+        int64_t m = pm ? pm[i] : i / N, n = pm ? pn[i] : i % N;
+        const uint8_t *a = A + m * lda, *b = B + n * ldb;
+        double s = 0.0, t = 0.0, scl;
+        for (int64_t k = 0; k < K; k++) {
+            double p = da[a[k]] * db[b[k]];
+            s += p;
+            t += fabs(p);
+        }
+        scl = (double)sa[sa_mode ? m : 0] * (double)sb[sb_mode ? n : 0];
+        ref[i] = s * scl;
+        bound[i] = t * fabs(scl);
+    }
+}
+
+/*
+ * Grouped GEMM over expert groups; offsets int32 [G+1] (row ranges).
+ *
+ * mode 0 (M_GROUPED): A [M_total][K] rows of all groups, B [G][N][K];
+ *   C[m][n] = sum_k A[m][k] B[e(m)][n][k] sa(m) sb(e(m), n), with
+ *   sa_mode 1 -> sa[m], sb_mode 1 -> sb[e*N + n] (0 -> scalar).
+ *   Points: (pm[i], pn[i]); pg ignored.
+ * mode 1 (K_GROUPED): A [N][ldT], B [K][ldT] in the padded grouped colwise
+ *   layout; C[e][n][k] = sum_{r < m_e} A[n][poff_e + r] B[k][poff_e + r]
+ *   sa(e, n) sb(e, k); an empty group gives 0.  sa_mode 1 -> sa[e*N + n],
+ *   sb_mode 1 -> sb[e*K + k].  Points: (pg[i], pm[i] = n, pn[i] = k).
+ */
+void orc_grouped_gemm(int mode, const uint8_t *A, int fa, const uint8_t *B, int fb, const int32_t *offsets,
+                      int G, int64_t M_total, int64_t N, int64_t K, const float *sa, int sa_mode,
+                      const float *sb, int sb_mode, const int64_t *pg, const int64_t *pm,
+                      const int64_t *pn, int64_t npts, double *ref, double *bound)
+{
+    double da[256], db[256];
+    int64_t *poff = (int64_t *)malloc(sizeof(int64_t) * (G + 1));
+    int64_t ldT = orc_padded_offsets(offsets, G, poff);
+    (void)M_total;
+    for (int c = 0; c < 256; c++) {
+        da[c] = orc_fp8_decode(c, fa);
+        db[c] = orc_fp8_decode(c, fb);
+    }
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t i = 0; i < npts; i++) {
+        double s = 0.0, t = 0.0, scl;
+        if (mode == 0) {
+            int64_t m = pm[i], n = pn[i];
+            int e = 0;
+            while (e < G - 1 && m >= offsets[e + 1]) e++;
+            const uint8_t *a = A + m * K, *b = B + ((int64_t)e * N + n) * K;
+            for (int64_t k = 0; k < K; k++) {
+                double p = da[a[k]] * db[b[k]];
+                s += p;
+                t += fabs(p);
+            }
+            scl = (double)sa[sa_mode ? m : 0] * (double)sb[sb_mode ? (int64_t)e * N + n : 0];
+        } else {
+            int64_t e = pg[i], n = pm[i], k = pn[i];
+            int64_t me = (int64_t)offsets[e + 1] - offsets[e];
+            const uint8_t *a = A + n * ldT + poff[e], *b = B + k * ldT + poff[e];
+            for (int64_t r = 0; r < me; r++) {
+                double p = da[a[r]] * db[b[r]];
+                s += p;
+                t += fabs(p);
+            }
+            scl = (double)sa[sa_mode ? e * N + n : 0] * (double)sb[sb_mode ? e * K + k : 0];
+        }
+        ref[i] = s * scl;
+        bound[i] = t * fabs(scl);
+    }
+    free(poff);
+}
