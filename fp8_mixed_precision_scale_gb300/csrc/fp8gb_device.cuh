@@ -1,0 +1,268 @@
+// fp8gb_device.cuh -- device helpers shared by the library's kernels:
+// the scale formula, FP8 conversions, the device error word, bounded
+// mbarrier waits, and thin inline-PTX wrappers for TMA and tcgen05.
+//
+// Target: sm_103a only (tcgen05 / TMEM / TMA).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "fp8gb.h"
+
+namespace fp8gb {
+
+// ---------------------------------------------------------------------------
+// Device error word (one per device, defined in api.cu; kernels receive its
+// address): set by a bounded wait that gave up or by malformed device-side
+// arguments; read and cleared by fp8_sync_status().
+// ---------------------------------------------------------------------------
+enum : unsigned int {
+    ERR_PRODUCER_WAIT = 1u,
+    ERR_MMA_WAIT = 2u,
+    ERR_EPILOGUE_WAIT = 4u,
+    ERR_TEARDOWN_WAIT = 8u,
+    ERR_SELFTEST_WAIT = 16u,
+    ERR_BAD_OFFSETS = 32u,
+};
+
+__device__ __forceinline__ void record_error(unsigned int *err, unsigned int bits)
+{
+    if (err) atomicOr(err, bits);
+}
+
+// ---------------------------------------------------------------------------
+// Scale arithmetic ("FP8 training for Flux models", Key FP8 Parameters:
+// scale = fp8_max / amax / 2^margin).  IEEE fp32 operations, no contraction.
+// ---------------------------------------------------------------------------
+__host__ __device__ __forceinline__ float fp8_max_of(int fmt)
+{
+    return fmt == FP8_E5M2 ? 57344.0f : (fmt == FP8_E4M3FNUZ ? 240.0f : 448.0f);
+}
+
+__device__ __forceinline__ float pow2_neg(int margin)  // 2^-margin, 0 <= margin <= 126
+{
+    return __int_as_float((127 - margin) << 23);
+}
+
+// Current scaling: amax == 0 or non-finite -> 1; overflow -> FLT_MAX.
+__device__ __forceinline__ float scale_from_amax(float amax, float fmax, int margin)
+{
+    if (!(amax > 0.0f) || !isfinite(amax)) return 1.0f;
+    float s = __fdiv_rn(fmax, amax);
+    s = __fmul_rn(s, pow2_neg(margin));
+    if (isinf(s)) s = 3.402823466e38f;
+    return s;
+}
+
+__device__ __forceinline__ float recip_rn(float s) { return __fdiv_rn(1.0f, s); }
+
+// ---------------------------------------------------------------------------
+// FP8 conversion: saturating, round-to-nearest-even, two fp32 at a time.
+// Result: low byte = lo, high byte = hi.
+// ---------------------------------------------------------------------------
+template <int FMT>
+__device__ __forceinline__ uint32_t cvt2(float lo, float hi)
+{
+    unsigned short r;
+    if constexpr (FMT == FP8_E5M2)
+        asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    else
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return (uint32_t)r;
+}
+
+// bf16 pair (one 32-bit word: element 0 in the low half) -> two fp32.
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// |x| bit patterns of a bf16 pair, max'ed per half: NaN patterns (0x7F81..)
+// are above Inf (0x7F80) so NaN propagates through an unsigned max.
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t acc, uint32_t w)
+{
+    return __vmaxu2(acc, w & 0x7FFF7FFFu);
+}
+
+// Fold the two halves of a packed |bf16| max into the fp32 bit pattern of
+// the larger one (bf16 -> fp32 is exact, so the order is preserved).
+__device__ __forceinline__ uint32_t fold_absmax(uint32_t acc)
+{
+    uint32_t a = acc & 0xFFFFu, b = acc >> 16;
+    return (a > b ? a : b) << 16;
+}
+
+// ---------------------------------------------------------------------------
+// Shared-memory addresses and mbarriers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait for the phase of `parity` to complete.  Gives up after about
+// limit_ns of wall time (checked every 256 polls), records `err_bits` and
+// returns false.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, uint64_t limit_ns,
+                                                  unsigned int *err, unsigned int err_bits)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 255u) == 0 && global_timer_ns() - t0 > limit_ns) {
+            record_error(err, err_bits);
+            return false;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// TMA (cp.async.bulk.tensor) -- 2D tile load into shared memory, completing
+// on an mbarrier by transaction bytes.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *map, int32_t x, int32_t y,
+                                            uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(smem_u32(smem_dst)), "l"((uint64_t)map), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)map) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// tcgen05 (5th-generation tensor cores, accumulators in TMEM)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t *slot_smem, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot_smem)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor of a K-major operand tile stored as rows of
+// 128 bytes with the 128-byte swizzle (the layout TMA writes with
+// CU_TENSOR_MAP_SWIZZLE_128B): 8-row groups are 1024 bytes apart (SBO),
+// LBO unused for this layout, descriptor version 1, layout type 2 (128B).
+__device__ __forceinline__ uint64_t smem_desc_k128_sw128(uint32_t smem_addr)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((smem_addr & 0x3FFFFu) >> 4);  // start address, bits 0-13
+    d |= (uint64_t)1 << 16;                        // leading byte offset (unused), bits 16-29
+    d |= (uint64_t)(1024 >> 4) << 32;              // stride byte offset, bits 32-45
+    d |= (uint64_t)1 << 46;                        // version, bits 46-47
+    d |= (uint64_t)2 << 61;                        // swizzle 128B, bits 61-63
+    return d;
+}
+
+// Instruction descriptor of tcgen05.mma kind::f8f6f4, fp32 accumulate,
+// both operands K-major, dense.  fa / fb: 0 = E4M3, 1 = E5M2.
+__host__ __device__ constexpr uint32_t idesc_f8f6f4(int fa, int fb, int M, int N)
+{
+    return (1u << 4)                         // D format f32
+           | ((uint32_t)fa << 7)             // A format
+           | ((uint32_t)fb << 10)            // B format
+           | ((uint32_t)(N >> 3) << 17)      // N / 8
+           | ((uint32_t)(M >> 4) << 24);     // M / 16
+}
+
+__device__ __forceinline__ void mma_f8f6f4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive on `bar` once every tcgen05 operation issued so far by this thread
+// has completed.
+__device__ __forceinline__ void mma_commit(uint64_t *bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+
+// 32 lanes x 32 consecutive fp32 columns: thread i of the warp receives lane
+// (quarter*32 + i), columns col .. col+31.
+__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
+          "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+          "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Two fp32 -> packed bf16x2 (round to nearest even); lo in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+}  // namespace fp8gb

@@ -1,0 +1,574 @@
+// gemm.cu -- FP8 scaled GEMM and grouped GEMM on the tcgen05 tensor cores.
+//
+// C[m][n] = bf16( sum_k A[m][k] B[n][k] * sa(m) * sb(n) ), FP8 E4M3 / E5M2
+// operands, fp32 accumulation in tensor memory, per-tensor or per-row /
+// per-column scales applied in the epilogue.  The grouped variants run the
+// per-expert GEMMs of a Mixture-of-Experts layer over variable-size row
+// groups in one launch.
+//
+// Method: FP8 for the linear layers' forward and backward GEMMs ("FP8
+// Training on MI300X", Patched nanochat/fp8.py; "FP8 training for Flux
+// models", fp8_wgrad); per-row / per-column scales ("How PyTorch FP8
+// Optimizations on AMD GPUs ...", rowwise FP8); grouped GEMM for MoE (same
+// page and "FP8 Training on AMD GPUs with TorchTitan and TorchAO").
+//
+// Design (GB300, sm_103a): persistent, warp-specialised kernel, one CTA per
+// SM, 192 threads.
+//   warp 0     TMA producer: 128x128-byte A and 256x128-byte B tiles into a
+//              4-stage shared-memory ring (128-byte swizzle), completion by
+//              mbarrier transaction counts.
+//   warp 1     MMA issuer: one thread issues tcgen05.mma kind::f8f6f4
+//              (M=128, N=256, K=32) into a TMEM accumulator; tcgen05.commit
+//              frees ring stages and hands finished accumulators over.
+//   warps 2-5  epilogue: tcgen05.ld 32 columns at a time, scale, convert to
+//              bf16, store.  Two 256-column accumulators (all 512 TMEM
+//              columns) let the epilogue of one tile overlap the main loop of
+//              the next.
+// Every mbarrier wait is bounded (about 2 s of wall time); a wait that gives
+// up records the device error word, drains in-flight copies, releases TMEM
+// and returns.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "fp8gb.h"
+#include "fp8gb_device.cuh"
+#include "fp8gb_host.h"
+
+namespace fp8gb {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 128;  // bytes = FP8 elements per k-block (one 128B swizzle row)
+constexpr int UMMA_K = 32;
+constexpr int STAGES = 4;
+constexpr int A_STAGE_BYTES = BM * BK;
+constexpr int B_STAGE_BYTES = BN * BK;
+constexpr int GEMM_THREADS = 192;
+constexpr uint32_t TMEM_COLS = 2 * BN;
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
+constexpr int MAX_GROUPS = 4096;
+
+enum { MODE_DENSE = 0, MODE_MGROUP = 1, MODE_KGROUP = 2 };
+
+struct GemmParams {
+    int64_t M, N, K;  // dense / M-grouped: A [M][K], B [N][K]; K-grouped: C[e] is [M=N][N=K]
+    const float *sa;
+    const float *sb;
+    int sa_per_row, sb_per_row;
+    uint16_t *C;
+    int64_t ldc;
+    int num_m_blk, num_n_blk, num_k_blk;
+    int m_fastest;
+    int64_t total_tiles;  // dense
+    const int32_t *offsets;
+    int G;
+    int64_t ld_T;  // K-grouped: padded width of A and B
+    unsigned int *err;
+};
+
+struct TileInfo {
+    int32_t a_y, b_y, k_x0;
+    int nkb, last_steps;
+    int64_t row0, row_end, col0, col_end;
+    int64_t c_base;
+    int64_t sa_base, sb_base;
+};
+
+struct SmemLayout {
+    static constexpr int a_off = 0;
+    static constexpr int b_off = STAGES * A_STAGE_BYTES;
+    static constexpr int bar_off = b_off + STAGES * B_STAGE_BYTES;
+    static constexpr int n_bars = 2 * STAGES + 2 + 2 + 1;
+    static constexpr int slot_off = bar_off + n_bars * 8;
+    static constexpr int misc_off = slot_off + 16;  // int32 group tables start here
+    static constexpr int base_bytes = misc_off;
+};
+
+// Group tables in shared memory: tile prefix [G+1] then padded offsets [G+1].
+__device__ bool build_group_tables(const GemmParams &p, int MODE, int32_t *tile_prefix, int32_t *poff,
+                                   int64_t *total_tiles)
+{
+    // executed by one warp
+    const int lane = threadIdx.x & 31;
+    const int G = p.G;
+    const int per = (G + 31) / 32;
+    const int g0 = min(G, lane * per), g1 = min(G, g0 + per);
+    int64_t lt = 0, lp = 0;
+    int bad = 0;
+    for (int e = g0; e < g1; e++) {
+        const int m = p.offsets[e + 1] - p.offsets[e];
+        if (m < 0) bad = 1;
+        const int mm = max(m, 0);
+        lt += MODE == MODE_MGROUP ? (int64_t)((mm + BM - 1) / BM) * p.num_n_blk : (int64_t)p.num_m_blk * p.num_n_blk;
+        lp += (int64_t)((mm + 31) / 32) * 32;
+    }
+    int64_t it = lt, ip = lp;
+    for (int d = 1; d < 32; d <<= 1) {
+        const int64_t vt = __shfl_up_sync(0xffffffffu, it, d), vp = __shfl_up_sync(0xffffffffu, ip, d);
+        if (lane >= d) {
+            it += vt;
+            ip += vp;
+        }
+    }
+    int64_t rt = it - lt, rp = ip - lp;
+    for (int e = g0; e < g1; e++) {
+        tile_prefix[e] = (int32_t)rt;
+        poff[e] = (int32_t)rp;
+        const int mm = max(p.offsets[e + 1] - p.offsets[e], 0);
+        rt += MODE == MODE_MGROUP ? (int64_t)((mm + BM - 1) / BM) * p.num_n_blk : (int64_t)p.num_m_blk * p.num_n_blk;
+        rp += (int64_t)((mm + 31) / 32) * 32;
+    }
+    const int64_t tt = __shfl_sync(0xffffffffu, it, 31), tp = __shfl_sync(0xffffffffu, ip, 31);
+    bad = __any_sync(0xffffffffu, bad);
+    if (lane == 0) {
+        tile_prefix[G] = (int32_t)tt;
+        poff[G] = (int32_t)tp;
+    }
+    *total_tiles = tt;
+    const bool ok = !bad && p.offsets[0] == 0 && (int64_t)p.offsets[G] == p.M &&
+                    (MODE != MODE_KGROUP || tp <= p.ld_T) && tt < (int64_t)1 << 31;
+    return ok;
+}
+
+template <int MODE>
+__device__ __forceinline__ TileInfo tile_info(const GemmParams &p, int64_t t, const int32_t *tile_prefix,
+                                              const int32_t *poff)
+{
+    TileInfo ti;
+    if constexpr (MODE == MODE_DENSE) {
+        int mb, nb;
+        if (p.m_fastest) {
+            mb = (int)(t % p.num_m_blk);
+            nb = (int)(t / p.num_m_blk);
+        } else {
+            nb = (int)(t % p.num_n_blk);
+            mb = (int)(t / p.num_n_blk);
+        }
+        ti.a_y = mb * BM;
+        ti.b_y = nb * BN;
+        ti.k_x0 = 0;
+        ti.nkb = p.num_k_blk;
+        ti.last_steps = BK / UMMA_K;
+        ti.row0 = (int64_t)mb * BM;
+        ti.row_end = p.M;
+        ti.col0 = (int64_t)nb * BN;
+        ti.col_end = p.N;
+        ti.c_base = 0;
+        ti.sa_base = 0;
+        ti.sb_base = 0;
+    } else {
+        // group e: last with tile_prefix[e] <= t
+        int lo = 0, hi = p.G;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (tile_prefix[mid] <= t)
+                lo = mid;
+            else
+                hi = mid;
+        }
+        const int e = lo;
+        const int64_t local = t - tile_prefix[e];
+        const int64_t m_e = (int64_t)p.offsets[e + 1] - p.offsets[e];
+        if constexpr (MODE == MODE_MGROUP) {
+            const int64_t mt = (m_e + BM - 1) / BM;
+            const int64_t mb = local % mt, nb = local / mt;  // rows fastest: the expert's weight tile stays in L2
+            ti.a_y = (int32_t)(p.offsets[e] + mb * BM);
+            ti.b_y = (int32_t)((int64_t)e * p.N + nb * BN);
+            ti.k_x0 = 0;
+            ti.nkb = p.num_k_blk;
+            ti.last_steps = BK / UMMA_K;
+            ti.row0 = p.offsets[e] + mb * BM;
+            ti.row_end = p.offsets[e + 1];
+            ti.col0 = nb * BN;
+            ti.col_end = p.N;
+            ti.c_base = 0;
+            ti.sa_base = 0;
+            ti.sb_base = (int64_t)e * p.N;
+        } else {
+            // K-grouped: output block e is [N][K]; contraction over the group's padded columns
+            const int64_t nb = local % p.num_n_blk, mb = local / p.num_n_blk;
+            const int64_t pad = (m_e + 31) / 32 * 32;
+            ti.a_y = (int32_t)(mb * BM);
+            ti.b_y = (int32_t)(nb * BN);
+            ti.k_x0 = poff[e];
+            ti.nkb = (int)((pad + BK - 1) / BK);
+            ti.last_steps = ti.nkb > 0 ? (int)((pad - (int64_t)(ti.nkb - 1) * BK) / UMMA_K) : 0;
+            ti.row0 = mb * BM;
+            ti.row_end = p.N;  // rows of C[e]
+            ti.col0 = nb * BN;
+            ti.col_end = p.K;
+            ti.c_base = (int64_t)e * p.N * p.K;
+            ti.sa_base = (int64_t)e * p.N;
+            ti.sb_base = (int64_t)e * p.K;
+        }
+    }
+    return ti;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
+    fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmParams p,
+                    uint32_t idesc)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sA = smem + SmemLayout::a_off;
+    uint8_t *sB = smem + SmemLayout::b_off;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + SmemLayout::bar_off);
+    uint64_t *full = bars;
+    uint64_t *empty = bars + STAGES;
+    uint64_t *tfull = bars + 2 * STAGES;
+    uint64_t *tempty = tfull + 2;
+    uint64_t *done = tempty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + SmemLayout::slot_off);
+    int32_t *tile_prefix = reinterpret_cast<int32_t *>(smem + SmemLayout::misc_off);
+    int32_t *poff = tile_prefix + (p.G + 1);
+    __shared__ int64_t s_total;
+    __shared__ int s_ok;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < STAGES; s++) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; b++) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 4);
+        }
+        mbar_init(done, 1);
+        fence_barrier_init();
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB);
+    }
+    if constexpr (MODE != MODE_DENSE) {
+        if (warp == 2) {
+            int64_t tt = 0;
+            const bool ok = build_group_tables(p, MODE, tile_prefix, poff, &tt);
+            if (lane == 0) {
+                s_total = tt;
+                s_ok = ok;
+                if (!ok) record_error(p.err, ERR_BAD_OFFSETS);
+            }
+        }
+    } else {
+        if (threadIdx.x == 0) {
+            s_total = p.total_tiles;
+            s_ok = 1;
+        }
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int64_t total = s_ok ? s_total : 0;
+
+    if (warp == 0 && lane == 0) {
+        // ---------------- TMA producer ----------------
+        int stage = 0;
+        uint32_t phase = 0;
+        int issued_parity[STAGES];
+        for (int s = 0; s < STAGES; s++) issued_parity[s] = -1;
+        bool ok = true;
+        for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            const TileInfo ti = tile_info<MODE>(p, t, tile_prefix, poff);
+            for (int kb = 0; kb < ti.nkb; kb++) {
+                if (!mbar_wait_bounded(&empty[stage], phase ^ 1, WAIT_LIMIT_NS, p.err, ERR_PRODUCER_WAIT)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&full[stage], A_STAGE_BYTES + B_STAGE_BYTES);
+                const int32_t kx = ti.k_x0 + kb * BK;
+                tma_load_2d(sA + stage * A_STAGE_BYTES, &tmA, kx, ti.a_y, &full[stage]);
+                tma_load_2d(sB + stage * B_STAGE_BYTES, &tmB, kx, ti.b_y, &full[stage]);
+                issued_parity[stage] = (int)phase;
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+        }
+        // drain: every issued copy must have landed before the CTA exits
+        for (int s = 0; s < STAGES; s++)
+            if (issued_parity[s] >= 0)
+                mbar_wait_bounded(&full[s], (uint32_t)issued_parity[s], WAIT_LIMIT_NS, p.err, ERR_TEARDOWN_WAIT);
+    } else if (warp == 1 && lane == 0) {
+        // ---------------- MMA issuer ----------------
+        int stage = 0;
+        uint32_t phase = 0;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool ok = true;
+        for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            const TileInfo ti = tile_info<MODE>(p, t, tile_prefix, poff);
+            if (ti.nkb == 0) continue;  // empty K-grouped block: the epilogue writes zeros
+            if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1, WAIT_LIMIT_NS, p.err, ERR_MMA_WAIT)) break;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+            for (int kb = 0; kb < ti.nkb; kb++) {
+                if (!mbar_wait_bounded(&full[stage], phase, WAIT_LIMIT_NS, p.err, ERR_MMA_WAIT)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a_addr = smem_u32(sA + stage * A_STAGE_BYTES);
+                const uint32_t b_addr = smem_u32(sB + stage * B_STAGE_BYTES);
+                const int steps = kb == ti.nkb - 1 ? ti.last_steps : BK / UMMA_K;
+                for (int k = 0; k < steps; k++) {
+                    const uint64_t ad = smem_desc_k128_sw128(a_addr + k * UMMA_K);
+                    const uint64_t bd = smem_desc_k128_sw128(b_addr + k * UMMA_K);
+                    mma_f8f6f4(d_tmem, ad, bd, idesc, (kb | k) != 0);
+                }
+                mma_commit(&empty[stage]);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+            if (!ok) break;
+            mma_commit(&tfull[acc]);
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1;
+            }
+        }
+        // all issued MMAs complete before TMEM is released
+        mma_commit(done);
+        mbar_wait_bounded(done, 0, WAIT_LIMIT_NS, p.err, ERR_TEARDOWN_WAIT);
+    } else if (warp >= 2) {
+        // ---------------- epilogue ----------------
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
+            const TileInfo ti = tile_info<MODE>(p, t, tile_prefix, poff);
+            const int64_t gr = ti.row0 + q * 32 + lane;
+            const bool row_ok = gr < ti.row_end;
+            uint16_t *crow = p.C + ti.c_base + gr * p.ldc;
+            if (ti.nkb == 0) {
+                if (row_ok)
+                    for (int64_t c = ti.col0; c < ti.col0 + BN && c < ti.col_end; c += 8) {
+                        if (c + 8 <= ti.col_end)
+                            *reinterpret_cast<uint4 *>(crow + c) = make_uint4(0, 0, 0, 0);
+                        else
+                            for (int64_t j = c; j < ti.col_end; j++) crow[j] = 0;
+                    }
+                continue;
+            }
+            if (!mbar_wait_bounded(&tfull[acc], acc_phase, WAIT_LIMIT_NS, p.err, ERR_EPILOGUE_WAIT)) break;
+            tc_fence_after();
+            const float sa_v = row_ok ? (p.sa_per_row ? __ldg(p.sa + ti.sa_base + gr) : __ldg(p.sa)) : 0.0f;
+            const float sb0 = p.sb_per_row ? 0.0f : __ldg(p.sb);
+            for (int ch = 0; ch < BN / 32; ch++) {
+                const int64_t c0 = ti.col0 + ch * 32;
+                if (c0 >= ti.col_end) break;  // warp-uniform
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + ch * 32), r);
+                tmem_ld_wait();
+                if (!row_ok) continue;
+                uint32_t packed[16];
+#pragma unroll
+                for (int j = 0; j < 16; j++) {
+                    float sb_lo = sb0, sb_hi = sb0;
+                    if (p.sb_per_row) {
+                        const int64_t cl = c0 + 2 * j;
+                        sb_lo = cl < ti.col_end ? __ldg(p.sb + ti.sb_base + cl) : 0.0f;
+                        sb_hi = cl + 1 < ti.col_end ? __ldg(p.sb + ti.sb_base + cl + 1) : 0.0f;
+                    }
+                    const float lo = __uint_as_float(r[2 * j]) * sa_v * sb_lo;
+                    const float hi = __uint_as_float(r[2 * j + 1]) * sa_v * sb_hi;
+                    packed[j] = pack_bf16x2(lo, hi);
+                }
+#pragma unroll
+                for (int g = 0; g < 4; g++) {
+                    const int64_t c = c0 + g * 8;
+                    if (c + 8 <= ti.col_end) {
+                        *reinterpret_cast<uint4 *>(crow + c) =
+                            make_uint4(packed[4 * g], packed[4 * g + 1], packed[4 * g + 2], packed[4 * g + 3]);
+                    } else {
+                        for (int j = 0; j < 8 && c + j < ti.col_end; j++)
+                            crow[c + j] = (uint16_t)(packed[4 * g + j / 2] >> (16 * (j & 1)));
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[acc]);
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host side: tensor maps via the driver entry point (no link-time libcuda).
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encode_fn()
+{
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// 2D map over a row-major u8 matrix [rows][ld] (inner extent `cols`), box
+// {128 bytes, box_rows}, 128-byte swizzle, zero fill out of bounds.
+static bool make_map(CUtensorMap *map, const void *base, int64_t rows, int64_t cols, int64_t ld, int box_rows)
+{
+    EncodeTiledFn enc = get_encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)ld};
+    cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+static size_t gemm_smem_bytes(int G) { return 1024 + SmemLayout::base_bytes + (G > 0 ? 8 * (size_t)(G + 1) : 0); }
+
+template <int MODE>
+static fp8_status_t launch_gemm(const CUtensorMap &ma, const CUtensorMap &mb, const GemmParams &p, int fa, int fb,
+                                int64_t grid, cudaStream_t st)
+{
+    const size_t smem = gemm_smem_bytes(MODE == MODE_DENSE ? 0 : p.G);
+    cudaError_t e = cudaFuncSetAttribute(fp8_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return cuda_fail_with(e);
+    const uint32_t idesc = idesc_f8f6f4(fa, fb, BM, BN);
+    fp8_gemm_kernel<MODE><<<(unsigned)grid, GEMM_THREADS, smem, st>>>(ma, mb, p, idesc);
+    return check_launch();
+}
+
+static bool gemm_format_ok(int f) { return f == FP8_E4M3FN || f == FP8_E5M2; }
+
+}  // namespace fp8gb
+
+using namespace fp8gb;
+
+extern "C" fp8_status_t fp8_scaled_gemm(const uint8_t *A, int fa, int64_t lda, const uint8_t *B, int fb, int64_t ldb,
+                                        int64_t M, int64_t N, int64_t K, const float *sa, int sa_mode,
+                                        const float *sb, int sb_mode, void *C_bf16, int64_t ldc, void *stream)
+{
+    if (!A || !B || !sa || !sb || !C_bf16) return FP8_ERR_INVALID_ARG;
+    if (fa == FP8_E4M3FNUZ || fb == FP8_E4M3FNUZ) return FP8_ERR_UNSUPPORTED;
+    if (!gemm_format_ok(fa) || !gemm_format_ok(fb)) return FP8_ERR_INVALID_ARG;
+    if (M < 1 || N < 1 || K < 1 || lda < K || ldb < K || ldc < N) return FP8_ERR_INVALID_ARG;
+    if ((sa_mode != FP8_SCALE_TENSOR && sa_mode != FP8_SCALE_PER_ROW) ||
+        (sb_mode != FP8_SCALE_TENSOR && sb_mode != FP8_SCALE_PER_ROW))
+        return FP8_ERR_INVALID_ARG;
+    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return FP8_ERR_INVALID_ARG;
+    if (K % 16 != 0 || lda % 16 != 0 || ldb % 16 != 0 || ldc % 8 != 0) return FP8_ERR_ALIGNMENT;
+    if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C_bf16, 16) || !aligned(sa, 4) || !aligned(sb, 4))
+        return FP8_ERR_ALIGNMENT;
+
+    GemmParams p{};
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.sa = sa;
+    p.sb = sb;
+    p.sa_per_row = sa_mode == FP8_SCALE_PER_ROW;
+    p.sb_per_row = sb_mode == FP8_SCALE_PER_ROW;
+    p.C = static_cast<uint16_t *>(C_bf16);
+    p.ldc = ldc;
+    p.num_m_blk = (int)((M + BM - 1) / BM);
+    p.num_n_blk = (int)((N + BN - 1) / BN);
+    p.num_k_blk = (int)((K + BK - 1) / BK);
+    // sweep the dimension whose operand is smaller fastest, so that operand
+    // stays resident in L2 while the other streams through once
+    p.m_fastest = M <= N;
+    p.total_tiles = (int64_t)p.num_m_blk * p.num_n_blk;
+    p.err = device_error_word();
+    p.offsets = nullptr;
+    p.G = 0;
+
+    CUtensorMap ma, mb;
+    if (!make_map(&ma, A, M, K, lda, BM) || !make_map(&mb, B, N, K, ldb, BN)) return FP8_ERR_CUDA;
+    const int64_t grid = p.total_tiles < num_sms() ? p.total_tiles : num_sms();
+    return launch_gemm<MODE_DENSE>(ma, mb, p, fa, fb, grid, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" fp8_status_t fp8_grouped_gemm(int mode, const uint8_t *A, int fa, const uint8_t *B, int fb,
+                                         const int32_t *group_offsets, int G, int64_t M_total, int64_t N, int64_t K,
+                                         const float *sa, int sa_mode, const float *sb, int sb_mode, void *C_bf16,
+                                         int64_t ld_T, void *stream)
+{
+    if (!A || !B || !sa || !sb || !C_bf16 || !group_offsets) return FP8_ERR_INVALID_ARG;
+    if (fa == FP8_E4M3FNUZ || fb == FP8_E4M3FNUZ) return FP8_ERR_UNSUPPORTED;
+    if (!gemm_format_ok(fa) || !gemm_format_ok(fb)) return FP8_ERR_INVALID_ARG;
+    if (mode != FP8_GROUPED_M && mode != FP8_GROUPED_K) return FP8_ERR_INVALID_ARG;
+    if (G < 1 || G > MAX_GROUPS || M_total < 0 || N < 1 || K < 1) return FP8_ERR_INVALID_ARG;
+    if ((sa_mode != FP8_SCALE_TENSOR && sa_mode != FP8_SCALE_PER_ROW) ||
+        (sb_mode != FP8_SCALE_TENSOR && sb_mode != FP8_SCALE_PER_ROW))
+        return FP8_ERR_INVALID_ARG;
+    if (M_total > INT32_MAX || N > INT32_MAX || K > INT32_MAX || (int64_t)G * N > INT32_MAX)
+        return FP8_ERR_INVALID_ARG;
+    if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C_bf16, 16) || !aligned(sa, 4) || !aligned(sb, 4))
+        return FP8_ERR_ALIGNMENT;
+
+    GemmParams p{};
+    p.M = M_total;
+    p.N = N;
+    p.K = K;
+    p.sa = sa;
+    p.sb = sb;
+    p.sa_per_row = sa_mode == FP8_SCALE_PER_ROW;
+    p.sb_per_row = sb_mode == FP8_SCALE_PER_ROW;
+    p.C = static_cast<uint16_t *>(C_bf16);
+    p.offsets = group_offsets;
+    p.G = G;
+    p.err = device_error_word();
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    CUtensorMap ma, mb;
+    const int64_t grid = num_sms();
+
+    if (mode == FP8_GROUPED_M) {
+        if (K % 16 != 0 || N % 8 != 0) return FP8_ERR_ALIGNMENT;
+        p.ldc = N;
+        p.num_m_blk = 0;
+        p.num_n_blk = (int)((N + BN - 1) / BN);
+        p.num_k_blk = (int)((K + BK - 1) / BK);
+        if (M_total == 0) return FP8_OK;
+        if (!make_map(&ma, A, M_total, K, K, BM) || !make_map(&mb, B, (int64_t)G * N, K, K, BN)) return FP8_ERR_CUDA;
+        return launch_gemm<MODE_MGROUP>(ma, mb, p, fa, fb, grid, st);
+    }
+    // K-grouped (wgrad): C[e] = A_e [N][m_e] . B_e [K][m_e]^T
+    if (ld_T < 16 || ld_T % 16 != 0 || N % 8 != 0 || K % 8 != 0) return FP8_ERR_ALIGNMENT;
+    p.ldc = K;
+    p.ld_T = ld_T;
+    p.num_m_blk = (int)((N + BM - 1) / BM);
+    p.num_n_blk = (int)((K + BN - 1) / BN);
+    p.num_k_blk = 0;
+    if (!make_map(&ma, A, N, ld_T, ld_T, BM) || !make_map(&mb, B, K, ld_T, ld_T, BN)) return FP8_ERR_CUDA;
+    return launch_gemm<MODE_KGROUP>(ma, mb, p, fa, fb, grid, st);
+}

@@ -1,0 +1,577 @@
+// quantize.cu -- fused amax + scale + saturating cast of bf16 matrices to FP8,
+// emitting the row layout and the colwise-transposed layout from one read.
+//
+// Method: "FP8 training for Flux models" (Configuration > Key FP8 Parameters:
+// delayed / tensorwise recipes, fp8_margin); rowwise and colwise scales with
+// the transposed layout and fused quantize kernels: "How PyTorch FP8
+// Optimizations on AMD GPUs ..." (What Happened) and "FP8 Training on AMD
+// GPUs with TorchTitan and TorchAO" (the colwise-scales kernel whose
+// non-coalesced writes were the bottleneck; the five-kernel chain fused into
+// one; relaxed atomics).
+//
+// Design (GB300): persistent thread blocks of 256 threads walk tiles of
+// RB rows x 128 columns.  Each thread issues all of its 16-byte loads for a
+// tile before touching the data, converts 8 elements at a time with
+// cvt.rn.satfinite.{e4m3,e5m2}x2, stores the row layout directly (8-byte
+// coalesced stores) and stages the bytes in shared memory; the transposed
+// layout is then read back as 8x4 byte blocks, transposed in registers with
+// byte permutes and written as 8-byte runs along the token dimension, so both
+// layouts are written with coalesced stores.  Amax reductions use packed
+// |bf16| maxima, warp shuffles and one relaxed atomic per block (tensor
+// amax) or per tile row / column (rowwise / colwise amax).
+//
+// Kernels and passes:
+//   DELAYED    : cast (stored scale) + fused amax            -> 1 launch
+//   TENSORWISE : amax pass, cast pass                        -> 2 launches
+//   ROWWISE    : amax pass (row + column amax), cast pass,
+//                scale finalise                              -> 3 launches
+// The rowwise / colwise amax values are accumulated in the scale_inv output
+// buffers themselves (as fp32 bit patterns) and turned into scale_inv by the
+// finalise kernel, so no scratch memory is needed.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "fp8gb.h"
+#include "fp8gb_device.cuh"
+#include "fp8gb_host.h"
+
+namespace fp8gb {
+
+constexpr int QT_THREADS = 256;
+constexpr int QT_COLS = 128;          // columns per tile
+constexpr int QT_PITCH = QT_COLS + 4; // shared tile row pitch in bytes
+constexpr int QT_MAX_GROUPS = 4096;
+
+struct QArgs {
+    const uint16_t *x;
+    int64_t rows, cols, ld_x;
+    uint8_t *q_row;
+    uint8_t *q_colT;
+    int64_t ld_colT;
+    float *sinv_row;  // ROWWISE: amax bits during the passes
+    float *sinv_col;
+    const float *scale_in;
+    float *amax_out;
+    const int32_t *offsets;
+    unsigned int *err;
+    int G;
+    int margin;
+    int64_t n_row_blocks;
+    int64_t n_col_chunks;
+};
+
+// Row-block geometry: which input rows a tile covers and where they land in
+// the transposed layout.
+struct RowBlock {
+    bool skip;         // block lies beyond the padded total (grouped)
+    int64_t in_row0;   // first input row
+    int64_t out_col0;  // first column of q_colT
+    int valid;         // number of real rows (<= RB)
+    int group;         // expert group (0 when ungrouped)
+};
+
+// Exclusive prefix of roundup(m_e, 32) over groups, computed by warp 0 into
+// shared memory.  Flags malformed offsets (negative group sizes, total
+// beyond `rows`, padded total beyond ld_colT).
+__device__ void compute_padded_offsets(const int32_t *off, int G, int64_t rows, int64_t ld_colT, int32_t *poff,
+                                       int *bad, unsigned int *err)
+{
+    if (threadIdx.x >= 32) return;
+    const int lane = threadIdx.x;
+    const int per = (G + 31) / 32;
+    const int g0 = min(G, lane * per), g1 = min(G, g0 + per);
+    int64_t local = 0;
+    int badl = 0;
+    for (int e = g0; e < g1; e++) {
+        int m = off[e + 1] - off[e];
+        if (m < 0) badl = 1;
+        local += (int64_t)((max(m, 0) + 31) / 32) * 32;
+    }
+    int64_t incl = local;
+    for (int d = 1; d < 32; d <<= 1) {
+        int64_t v = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += v;
+    }
+    int64_t run = incl - local;
+    for (int e = g0; e < g1; e++) {
+        poff[e] = (int32_t)run;
+        int m = off[e + 1] - off[e];
+        run += (int64_t)((max(m, 0) + 31) / 32) * 32;
+    }
+    int64_t total = __shfl_sync(0xffffffffu, incl, 31);
+    badl = __any_sync(0xffffffffu, badl);
+    if (lane == 0) {
+        poff[G] = (int32_t)total;
+        int b = badl || off[0] != 0 || (int64_t)off[G] != rows || (ld_colT > 0 && total > ld_colT);
+        *bad = b;
+        if (b) record_error(err, ERR_BAD_OFFSETS);
+    }
+}
+
+template <int RB>
+__device__ __forceinline__ RowBlock row_block(const QArgs &a, int64_t b, const int32_t *poff)
+{
+    RowBlock rb;
+    rb.skip = false;
+    if (a.offsets == nullptr) {
+        rb.in_row0 = b * RB;
+        rb.out_col0 = b * RB;
+        rb.valid = (int)(a.rows - rb.in_row0 < RB ? a.rows - rb.in_row0 : RB);
+        rb.group = 0;
+    } else {
+        // padded block start p = b * RB (RB == 32): last group with poff <= p
+        const int64_t p = b * RB;
+        if (p >= poff[a.G]) {
+            rb.skip = true;
+            rb.in_row0 = rb.out_col0 = 0;
+            rb.valid = 0;
+            rb.group = 0;
+            return rb;
+        }
+        int lo = 0, hi = a.G;  // invariant: poff[lo] <= p < poff[hi]
+        while (hi - lo > 1) {
+            int mid = (lo + hi) >> 1;
+            if (poff[mid] <= p)
+                lo = mid;
+            else
+                hi = mid;
+        }
+        const int e = lo;
+        const int64_t within = p - poff[e];
+        const int64_t m = (int64_t)a.offsets[e + 1] - a.offsets[e];
+        rb.in_row0 = a.offsets[e] + within;
+        rb.out_col0 = p;
+        rb.valid = (int)(m - within < RB ? (m - within > 0 ? m - within : 0) : RB);
+        rb.group = e;
+    }
+    return rb;
+}
+
+__device__ __forceinline__ uint32_t warp_max_u32(uint32_t v)
+{
+    for (int d = 16; d > 0; d >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, d));
+    return v;
+}
+
+// Block-wide max of a u32, then one relaxed atomic into `dst` (fp32 bits of a
+// non-negative value or NaN).
+__device__ __forceinline__ void block_amax_atomic(uint32_t v, float *dst, uint32_t *red)
+{
+    v = warp_max_u32(v);
+    const int w = threadIdx.x >> 5;
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[w] = v;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t m = 0;
+        for (int i = 0; i < QT_THREADS / 32; i++) m = max(m, red[i]);
+        atomicMax(reinterpret_cast<unsigned int *>(dst), m);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Pass 1 (TENSORWISE and ROWWISE): amax only.
+//   MODE 0: whole-tensor amax into amax_out.
+//   MODE 1: per-row amax into sinv_row, per-(group, column) amax into
+//           sinv_col (both as fp32 bits, buffers zeroed by the host), plus
+//           the whole-tensor amax into amax_out when given.
+// ---------------------------------------------------------------------------
+template <int RB, int MODE>
+__global__ void __launch_bounds__(QT_THREADS) amax_kernel(QArgs a)
+{
+    extern __shared__ __align__(16) unsigned char dsm[];
+    int32_t *poff = reinterpret_cast<int32_t *>(dsm);
+    __shared__ uint32_t red[QT_THREADS / 32];
+    __shared__ uint32_t colw[QT_THREADS / 32][16][4];  // per warp: 16 column groups x 4 packed words
+    __shared__ int bad;
+    if (a.offsets) {
+        compute_padded_offsets(a.offsets, a.G, a.rows, 0, poff, &bad, a.err);
+        __syncthreads();
+        if (bad) return;
+    }
+    const int t = threadIdx.x, cg = t & 15, roff = t >> 4;
+    const int64_t n_tiles = a.n_row_blocks * a.n_col_chunks;
+    uint32_t tensor_acc = 0;
+    for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+        const int64_t b = tile / a.n_col_chunks;
+        const int64_t c0 = (tile % a.n_col_chunks) * QT_COLS;
+        const RowBlock rb = row_block<RB>(a, b, poff);
+        if (rb.skip) continue;
+        const int64_t col = c0 + cg * 8;
+        const bool col_ok = col < a.cols;
+        uint4 v[RB / 16];
+#pragma unroll
+        for (int i = 0; i < RB / 16; i++) {
+            const int r = i * 16 + roff;
+            if (col_ok && r < rb.valid)
+                v[i] = __ldg(reinterpret_cast<const uint4 *>(a.x + (rb.in_row0 + r) * a.ld_x + col));
+            else
+                v[i] = make_uint4(0, 0, 0, 0);
+        }
+        uint32_t cacc[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int i = 0; i < RB / 16; i++) {
+            uint32_t racc = 0;
+            racc = absmax_bf16x2(racc, v[i].x);
+            racc = absmax_bf16x2(racc, v[i].y);
+            racc = absmax_bf16x2(racc, v[i].z);
+            racc = absmax_bf16x2(racc, v[i].w);
+            if constexpr (MODE == 1) {
+                cacc[0] = absmax_bf16x2(cacc[0], v[i].x);
+                cacc[1] = absmax_bf16x2(cacc[1], v[i].y);
+                cacc[2] = absmax_bf16x2(cacc[2], v[i].z);
+                cacc[3] = absmax_bf16x2(cacc[3], v[i].w);
+                // row amax: reduce over the 16 threads sharing this row
+                uint32_t rm = fold_absmax(racc);
+                for (int d = 8; d > 0; d >>= 1) rm = max(rm, __shfl_xor_sync(0xffffffffu, rm, d));
+                const int r = i * 16 + roff;
+                if (cg == 0 && r < rb.valid && a.sinv_row)
+                    atomicMax(reinterpret_cast<unsigned int *>(a.sinv_row) + rb.in_row0 + r, rm);
+            }
+            tensor_acc = max(tensor_acc, fold_absmax(racc));
+        }
+        if constexpr (MODE == 1) {
+            if (a.sinv_col) {
+                // column amax over the tile's rows: lanes t and t^16 share columns
+#pragma unroll
+                for (int k = 0; k < 4; k++) cacc[k] = __vmaxu2(cacc[k], __shfl_xor_sync(0xffffffffu, cacc[k], 16));
+                const int w = t >> 5;
+                if ((t & 31) < 16) {
+#pragma unroll
+                    for (int k = 0; k < 4; k++) colw[w][cg][k] = cacc[k];
+                }
+                __syncthreads();
+                if (t < QT_COLS) {
+                    const int g = t >> 3, j = t & 7;  // column c0 + 8g + j
+                    uint32_t m = 0;
+                    for (int ww = 0; ww < QT_THREADS / 32; ww++) {
+                        const uint32_t word = colw[ww][g][j >> 1];
+                        m = max(m, (j & 1) ? (word >> 16) : (word & 0xFFFFu));
+                    }
+                    const int64_t c = c0 + t;
+                    if (c < a.cols && rb.valid > 0)
+                        atomicMax(reinterpret_cast<unsigned int *>(a.sinv_col) + (int64_t)rb.group * a.cols + c,
+                                  m << 16);
+                }
+                __syncthreads();
+            }
+        }
+    }
+    if (MODE == 0 || a.amax_out) block_amax_atomic(tensor_acc, a.amax_out, red);
+}
+
+// ---------------------------------------------------------------------------
+// Cast pass.
+//   SMODE 0: one scale for the tensor (DELAYED: scale_in[0]; TENSORWISE:
+//            from amax_out[0]).  DELAYED also max-accumulates the amax.
+//   SMODE 1: ROWWISE -- row scales from the row amax, column scales from the
+//            (group, column) amax.
+// ---------------------------------------------------------------------------
+template <int FMT, int RB, int SMODE, bool DELAYED, bool DO_ROW, bool DO_COLT>
+__global__ void __launch_bounds__(QT_THREADS) cast_kernel(QArgs a)
+{
+    extern __shared__ __align__(16) unsigned char dsm[];
+    uint8_t *tileT = dsm;                                                    // [RB][QT_PITCH]
+    int32_t *poff = reinterpret_cast<int32_t *>(dsm + RB * QT_PITCH);       // grouped only
+    __shared__ float srow[RB];
+    __shared__ float scol[QT_COLS];
+    __shared__ uint32_t red[QT_THREADS / 32];
+    __shared__ int bad;
+    const float fmax = fp8_max_of(FMT);
+    if (a.offsets) {
+        compute_padded_offsets(a.offsets, a.G, a.rows, DO_COLT ? a.ld_colT : 0, poff, &bad, a.err);
+        __syncthreads();
+        if (bad) return;
+    }
+
+    float s_tensor = 1.0f;
+    if constexpr (SMODE == 0) {
+        if constexpr (DELAYED)
+            s_tensor = a.scale_in[0];
+        else
+            s_tensor = scale_from_amax(a.amax_out[0], fmax, a.margin);
+        if (blockIdx.x == 0 && threadIdx.x == 0) {
+            const float sinv = recip_rn(s_tensor);
+            if (DO_ROW) a.sinv_row[0] = sinv;
+            if (DO_COLT) a.sinv_col[0] = sinv;
+        }
+    }
+
+    const int t = threadIdx.x, cg = t & 15, roff = t >> 4;
+    const int64_t n_tiles = a.n_row_blocks * a.n_col_chunks;
+    uint32_t amax_acc = 0;
+    for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+        const int64_t b = tile / a.n_col_chunks;
+        const int64_t c0 = (tile % a.n_col_chunks) * QT_COLS;
+        const RowBlock rb = row_block<RB>(a, b, poff);
+        if (rb.skip) continue;
+        const int64_t col = c0 + cg * 8;
+        const bool col_ok = col < a.cols;
+
+        uint4 v[RB / 16];
+#pragma unroll
+        for (int i = 0; i < RB / 16; i++) {
+            const int r = i * 16 + roff;
+            if (col_ok && r < rb.valid)
+                v[i] = __ldg(reinterpret_cast<const uint4 *>(a.x + (rb.in_row0 + r) * a.ld_x + col));
+            else
+                v[i] = make_uint4(0, 0, 0, 0);
+        }
+        if constexpr (SMODE == 1) {
+            // per-tile scales from the amax accumulated by pass 1
+            if (DO_ROW && t < RB) {
+                float am = 0.0f;
+                if (t < rb.valid) am = a.sinv_row[rb.in_row0 + t];
+                srow[t] = scale_from_amax(am, fmax, a.margin);
+            }
+            if (DO_COLT && t >= QT_THREADS - QT_COLS) {
+                const int j = t - (QT_THREADS - QT_COLS);
+                float am = 0.0f;
+                if (c0 + j < a.cols) am = a.sinv_col[(int64_t)rb.group * a.cols + c0 + j];
+                scol[j] = scale_from_amax(am, fmax, a.margin);
+            }
+            __syncthreads();
+        }
+
+#pragma unroll
+        for (int i = 0; i < RB / 16; i++) {
+            const int r = i * 16 + roff;
+            const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+            if constexpr (DELAYED) {
+#pragma unroll
+                for (int k = 0; k < 4; k++) amax_acc = absmax_bf16x2(amax_acc, w[k]);
+            }
+            uint32_t rowb0, rowb1, colb0, colb1;
+            if constexpr (SMODE == 0) {
+                const float s = s_tensor;
+                rowb0 = cvt2<FMT>(__fmul_rn(bf16lo(w[0]), s), __fmul_rn(bf16hi(w[0]), s)) |
+                        (cvt2<FMT>(__fmul_rn(bf16lo(w[1]), s), __fmul_rn(bf16hi(w[1]), s)) << 16);
+                rowb1 = cvt2<FMT>(__fmul_rn(bf16lo(w[2]), s), __fmul_rn(bf16hi(w[2]), s)) |
+                        (cvt2<FMT>(__fmul_rn(bf16lo(w[3]), s), __fmul_rn(bf16hi(w[3]), s)) << 16);
+                colb0 = rowb0;
+                colb1 = rowb1;
+            } else {
+                if constexpr (DO_ROW) {
+                    const float s = srow[r];
+                    rowb0 = cvt2<FMT>(__fmul_rn(bf16lo(w[0]), s), __fmul_rn(bf16hi(w[0]), s)) |
+                            (cvt2<FMT>(__fmul_rn(bf16lo(w[1]), s), __fmul_rn(bf16hi(w[1]), s)) << 16);
+                    rowb1 = cvt2<FMT>(__fmul_rn(bf16lo(w[2]), s), __fmul_rn(bf16hi(w[2]), s)) |
+                            (cvt2<FMT>(__fmul_rn(bf16lo(w[3]), s), __fmul_rn(bf16hi(w[3]), s)) << 16);
+                }
+                if constexpr (DO_COLT) {
+                    const float *sc = scol + cg * 8;
+                    colb0 = cvt2<FMT>(__fmul_rn(bf16lo(w[0]), sc[0]), __fmul_rn(bf16hi(w[0]), sc[1])) |
+                            (cvt2<FMT>(__fmul_rn(bf16lo(w[1]), sc[2]), __fmul_rn(bf16hi(w[1]), sc[3])) << 16);
+                    colb1 = cvt2<FMT>(__fmul_rn(bf16lo(w[2]), sc[4]), __fmul_rn(bf16hi(w[2]), sc[5])) |
+                            (cvt2<FMT>(__fmul_rn(bf16lo(w[3]), sc[6]), __fmul_rn(bf16hi(w[3]), sc[7])) << 16);
+                }
+            }
+            const bool ok = col_ok && r < rb.valid;
+            if constexpr (DO_ROW) {
+                if (ok)
+                    *reinterpret_cast<uint2 *>(a.q_row + (rb.in_row0 + r) * a.cols + col) = make_uint2(rowb0, rowb1);
+            }
+            if constexpr (DO_COLT) {
+                uint32_t *dst = reinterpret_cast<uint32_t *>(tileT + r * QT_PITCH + cg * 8);
+                dst[0] = ok ? colb0 : 0u;  // rows past the block's end become zero padding
+                dst[1] = ok ? colb1 : 0u;
+            }
+        }
+
+        if constexpr (DO_COLT) {
+            __syncthreads();
+            // transposed write-out: item = (column quad qa, 8-row chunk q)
+            constexpr int NQ = RB / 8;
+            for (int item = t; item < 32 * NQ; item += QT_THREADS) {
+                const int q = item % NQ, qa = item / NQ;
+                uint32_t wv[8];
+#pragma unroll
+                for (int i = 0; i < 8; i++) wv[i] = *reinterpret_cast<const uint32_t *>(tileT + (q * 8 + i) * QT_PITCH + qa * 4);
+                // 8 rows x 4 columns of bytes -> 4 columns x 8 rows
+                const uint32_t a01l = __byte_perm(wv[0], wv[1], 0x5140), a01h = __byte_perm(wv[0], wv[1], 0x7362);
+                const uint32_t a23l = __byte_perm(wv[2], wv[3], 0x5140), a23h = __byte_perm(wv[2], wv[3], 0x7362);
+                const uint32_t a45l = __byte_perm(wv[4], wv[5], 0x5140), a45h = __byte_perm(wv[4], wv[5], 0x7362);
+                const uint32_t a67l = __byte_perm(wv[6], wv[7], 0x5140), a67h = __byte_perm(wv[6], wv[7], 0x7362);
+                uint2 o[4];
+                o[0] = make_uint2(__byte_perm(a01l, a23l, 0x5410), __byte_perm(a45l, a67l, 0x5410));
+                o[1] = make_uint2(__byte_perm(a01l, a23l, 0x7632), __byte_perm(a45l, a67l, 0x7632));
+                o[2] = make_uint2(__byte_perm(a01h, a23h, 0x5410), __byte_perm(a45h, a67h, 0x5410));
+                o[3] = make_uint2(__byte_perm(a01h, a23h, 0x7632), __byte_perm(a45h, a67h, 0x7632));
+                const int r0 = q * 8;
+                // grouped blocks always write the full 32-byte padded extent
+                const int lim = a.offsets ? RB : rb.valid;
+                if (r0 >= lim) continue;
+#pragma unroll
+                for (int jj = 0; jj < 4; jj++) {
+                    const int64_t c = c0 + qa * 4 + jj;
+                    if (c >= a.cols) break;
+                    uint8_t *dst = a.q_colT + c * a.ld_colT + rb.out_col0 + r0;
+                    if (r0 + 8 <= lim) {
+                        *reinterpret_cast<uint2 *>(dst) = o[jj];
+                    } else {
+                        const uint64_t bits = ((uint64_t)o[jj].y << 32) | o[jj].x;
+                        for (int k = 0; k < lim - r0; k++) dst[k] = (uint8_t)(bits >> (8 * k));
+                    }
+                }
+            }
+            __syncthreads();
+        } else if constexpr (SMODE == 1) {
+            __syncthreads();
+        }
+    }
+    if constexpr (DELAYED) block_amax_atomic(fold_absmax(amax_acc), a.amax_out, red);
+}
+
+// ROWWISE finalise: amax bits -> scale_inv, in place.
+__global__ void finalize_rowwise_kernel(float *sinv_row, int64_t n_row, float *sinv_col, int64_t n_col, float fmax,
+                                        int margin)
+{
+    const int64_t total = n_row + n_col;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        float *p = i < n_row ? sinv_row + i : sinv_col + (i - n_row);
+        *p = recip_rn(scale_from_amax(*p, fmax, margin));
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+template <typename K>
+static int blocks_for(K kernel, size_t dyn_smem, int64_t n_tiles)
+{
+    int per_sm = 0;
+    if (dyn_smem > 48 * 1024) cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn_smem);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, QT_THREADS, dyn_smem);
+    if (per_sm < 1) per_sm = 1;
+    int64_t g = (int64_t)num_sms() * per_sm;
+    if (n_tiles < g) g = n_tiles;
+    if (g < 1) g = 1;
+    return (int)g;
+}
+
+template <int FMT, int RB, int SMODE, bool DELAYED>
+static fp8_status_t launch_cast(const QArgs &a, int layouts, size_t group_smem, cudaStream_t st)
+{
+    const int64_t n_tiles = a.n_row_blocks * a.n_col_chunks;
+    const size_t smem = (size_t)RB * QT_PITCH + group_smem;
+    if (layouts == (FP8_LAYOUT_ROW | FP8_LAYOUT_COLT)) {
+        auto k = cast_kernel<FMT, RB, SMODE, DELAYED, true, true>;
+        k<<<blocks_for(k, smem, n_tiles), QT_THREADS, smem, st>>>(a);
+    } else if (layouts == FP8_LAYOUT_ROW) {
+        auto k = cast_kernel<FMT, RB, SMODE, DELAYED, true, false>;
+        k<<<blocks_for(k, smem, n_tiles), QT_THREADS, smem, st>>>(a);
+    } else {
+        auto k = cast_kernel<FMT, RB, SMODE, DELAYED, false, true>;
+        k<<<blocks_for(k, smem, n_tiles), QT_THREADS, smem, st>>>(a);
+    }
+    return check_launch();
+}
+
+template <int FMT, int RB>
+static fp8_status_t run_quantize(QArgs a, int kind, int layouts, cudaStream_t st)
+{
+    const size_t group_smem = a.offsets ? sizeof(int32_t) * (size_t)(a.G + 1) : 0;
+    const int64_t n_tiles = a.n_row_blocks * a.n_col_chunks;
+    fp8_status_t s;
+    if (kind == FP8_RECIPE_DELAYED) {
+        return launch_cast<FMT, RB, 0, true>(a, layouts, group_smem, st);
+    }
+    if (kind == FP8_RECIPE_TENSORWISE) {
+        if (cudaMemsetAsync(a.amax_out, 0, sizeof(float), st) != cudaSuccess) return cuda_fail();
+        auto k = amax_kernel<RB, 0>;
+        k<<<blocks_for(k, group_smem, n_tiles), QT_THREADS, group_smem, st>>>(a);
+        if ((s = check_launch()) != FP8_OK) return s;
+        return launch_cast<FMT, RB, 0, false>(a, layouts, group_smem, st);
+    }
+    // ROWWISE
+    const int64_t n_row = (layouts & FP8_LAYOUT_ROW) ? a.rows : 0;
+    const int64_t n_col = (layouts & FP8_LAYOUT_COLT) ? a.cols * (a.offsets ? a.G : 1) : 0;
+    if (!(layouts & FP8_LAYOUT_ROW)) a.sinv_row = nullptr;
+    if (!(layouts & FP8_LAYOUT_COLT)) a.sinv_col = nullptr;
+    if (n_row && cudaMemsetAsync(a.sinv_row, 0, sizeof(float) * n_row, st) != cudaSuccess) return cuda_fail();
+    if (n_col && cudaMemsetAsync(a.sinv_col, 0, sizeof(float) * n_col, st) != cudaSuccess) return cuda_fail();
+    if (a.amax_out && cudaMemsetAsync(a.amax_out, 0, sizeof(float), st) != cudaSuccess) return cuda_fail();
+    {
+        auto k = amax_kernel<RB, 1>;
+        k<<<blocks_for(k, group_smem, n_tiles), QT_THREADS, group_smem, st>>>(a);
+        if ((s = check_launch()) != FP8_OK) return s;
+    }
+    if ((s = launch_cast<FMT, RB, 1, false>(a, layouts, group_smem, st)) != FP8_OK) return s;
+    const int64_t total = n_row + n_col;
+    if (total > 0) {
+        const int grid = (int)((total + 255) / 256 < 4096 ? (total + 255) / 256 : 4096);
+        finalize_rowwise_kernel<<<grid, 256, 0, st>>>(a.sinv_row, n_row, a.sinv_col, n_col, fp8_max_of(FMT), a.margin);
+        return check_launch();
+    }
+    return FP8_OK;
+}
+
+}  // namespace fp8gb
+
+using namespace fp8gb;
+
+extern "C" fp8_status_t fp8_quantize(const void *x_bf16, int64_t rows, int64_t cols, int64_t ld_x, int fmt,
+                                     const fp8_recipe_t *recipe, int layouts, const float *scale_in,
+                                     float *amax_out, uint8_t *q_row, float *scale_inv_row, uint8_t *q_colT,
+                                     int64_t ld_colT, float *scale_inv_col, const int32_t *group_offsets,
+                                     int num_groups, void *stream)
+{
+    // ---- validation (host only; nothing is launched on failure) ----
+    if (!recipe || (!x_bf16 && rows > 0)) return FP8_ERR_INVALID_ARG;
+    if (rows < 0 || cols < 1 || ld_x < cols) return FP8_ERR_INVALID_ARG;
+    if (fmt == FP8_E4M3FNUZ) return FP8_ERR_UNSUPPORTED;
+    if (fmt != FP8_E4M3FN && fmt != FP8_E5M2) return FP8_ERR_INVALID_ARG;
+    if (recipe->kind < FP8_RECIPE_DELAYED || recipe->kind > FP8_RECIPE_ROWWISE) return FP8_ERR_INVALID_ARG;
+    if (recipe->margin < 0 || recipe->margin > 64) return FP8_ERR_INVALID_ARG;
+    if (layouts < 1 || layouts > 3) return FP8_ERR_INVALID_ARG;
+    // an empty tensor may come with empty (NULL) row-layout buffers
+    if ((layouts & FP8_LAYOUT_ROW) && rows > 0 && (!q_row || !scale_inv_row)) return FP8_ERR_INVALID_ARG;
+    if ((layouts & FP8_LAYOUT_ROW) && recipe->kind != FP8_RECIPE_ROWWISE && !scale_inv_row)
+        return FP8_ERR_INVALID_ARG;
+    if ((layouts & FP8_LAYOUT_COLT) && (!q_colT || !scale_inv_col)) return FP8_ERR_INVALID_ARG;
+    if (recipe->kind == FP8_RECIPE_DELAYED && (!scale_in || !amax_out)) return FP8_ERR_INVALID_ARG;
+    if (recipe->kind == FP8_RECIPE_TENSORWISE && !amax_out) return FP8_ERR_INVALID_ARG;
+    if (group_offsets && (num_groups < 1 || num_groups > QT_MAX_GROUPS)) return FP8_ERR_INVALID_ARG;
+    if (!group_offsets && num_groups != 0) return FP8_ERR_INVALID_ARG;
+    if (cols % 8 != 0 || ld_x % 8 != 0 || !aligned(x_bf16, 16)) return FP8_ERR_ALIGNMENT;
+    if ((layouts & FP8_LAYOUT_ROW) && !aligned(q_row, 8)) return FP8_ERR_ALIGNMENT;
+    if (layouts & FP8_LAYOUT_COLT) {
+        if (!aligned(q_colT, 16) || ld_colT % 16 != 0) return FP8_ERR_ALIGNMENT;
+        if (!group_offsets && ld_colT < rows) return FP8_ERR_INVALID_ARG;
+        if (group_offsets && ld_colT < rows) return FP8_ERR_INVALID_ARG;  // padded width is >= rows
+    }
+    if (rows > ((int64_t)1 << 40) || cols > ((int64_t)1 << 31)) return FP8_ERR_INVALID_ARG;
+    // grouped padded offsets are int32 on the device
+    if (group_offsets && (rows + 32LL * num_groups > INT32_MAX || ld_colT > INT32_MAX)) return FP8_ERR_INVALID_ARG;
+
+    QArgs a;
+    a.x = static_cast<const uint16_t *>(x_bf16);
+    a.rows = rows;
+    a.cols = cols;
+    a.ld_x = ld_x;
+    a.q_row = q_row;
+    a.q_colT = q_colT;
+    a.ld_colT = (layouts & FP8_LAYOUT_COLT) ? ld_colT : 0;
+    a.sinv_row = scale_inv_row;
+    a.sinv_col = scale_inv_col;
+    a.scale_in = scale_in;
+    a.amax_out = amax_out;
+    a.offsets = group_offsets;
+    a.err = device_error_word();
+    a.G = group_offsets ? num_groups : 0;
+    a.margin = recipe->margin;
+    a.n_col_chunks = (cols + QT_COLS - 1) / QT_COLS;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    if (group_offsets) {
+        // padded space: rows + at most 31 padding rows per group
+        const int64_t padded_max = ld_colT > 0 && (layouts & FP8_LAYOUT_COLT) ? ld_colT : rows + 32LL * num_groups;
+        a.n_row_blocks = (padded_max + 31) / 32;
+        return fmt == FP8_E5M2 ? run_quantize<FP8_E5M2, 32>(a, recipe->kind, layouts, st)
+                               : run_quantize<FP8_E4M3FN, 32>(a, recipe->kind, layouts, st);
+    }
+    a.n_row_blocks = (rows + 127) / 128;
+    return fmt == FP8_E5M2 ? run_quantize<FP8_E5M2, 128>(a, recipe->kind, layouts, st)
+                           : run_quantize<FP8_E4M3FN, 128>(a, recipe->kind, layouts, st);
+}

@@ -1,0 +1,244 @@
+/*
+ * fp8gb.h -- C ABI of the GB300 (sm_103a) FP8 linear-layer library.
+ *
+ * The library implements the hot path of FP8 mixed-precision training of a
+ * linear layer:
+ *   1. fp8_quantize            fused amax + scale + saturating cast of a bf16
+ *                              matrix to FP8, rowwise and colwise-transposed
+ *                              layouts from one kernel pass;
+ *   2. fp8_update_amax_history the delayed-scaling history roll and scale
+ *                              update for many tensors in one launch;
+ *   3. fp8_scaled_gemm         FP8 x FP8 -> bf16 GEMM with per-tensor or
+ *                              per-row / per-column scales in the epilogue
+ *                              (fprop, dgrad and wgrad are all this call);
+ *   4. fp8_grouped_gemm        the same over variable-size expert groups of a
+ *                              Mixture-of-Experts layer.
+ *
+ * Method sources (page title, section):
+ *   - "FP8 training for Flux models" (AMD Primus guide), Configuration >
+ *     Key FP8 Parameters: fp8 format "e4m3" or "hybrid", fp8_recipe
+ *     ("delayed", "tensorwise", ...), fp8_margin, fp8_amax_history_len,
+ *     fp8_amax_compute_algo ("most_recent" or "max"), fp8_wgrad.
+ *   - "FP8 Training on MI300X", "Discovered AMD FP8 dtype difference" and
+ *     "Patched nanochat/fp8.py": E4M3 forward / E5M2 backward, e4m3fn max
+ *     448, e4m3fnuz max 240.
+ *   - "How PyTorch FP8 Optimizations on AMD GPUs Reduce LLM Cost ...", What
+ *     Happened; "FP8 Training on AMD GPUs with TorchTitan and TorchAO":
+ *     rowwise FP8, the colwise-scales kernel (transposed layout), grouped
+ *     GEMM for MoE, fused quantize kernels, relaxed atomics.
+ *
+ * Conventions shared by every entry point
+ *   - All pointers are caller-owned DEVICE memory unless the argument name
+ *     starts with host_.  The library allocates nothing.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the
+ *     legacy default stream) and never synchronises.
+ *   - Arguments are validated on the host before anything is launched; a
+ *     failed check returns its status and launches nothing.
+ *   - FP8_ERR_CUDA: a CUDA launch or runtime call failed (see
+ *     fp8_last_cuda_error()).
+ *   - Device-side waits are bounded.  A wait that gives up records an error
+ *     word on the device; fp8_sync_status() synchronises the stream and
+ *     returns FP8_ERR_TIMEOUT (clearing the word) if that happened.
+ *   - Formats are explicit enums.  Nothing is auto-detected.
+ */
+#ifndef FP8GB_H
+#define FP8GB_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FP8GB_API __attribute__((visibility("default")))
+#else
+#define FP8GB_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* FP8 formats.  e4m3fn: bias 7, max 448, NaN 0x7F/0xFF, no Inf.  e5m2: bias
+ * 15, max 57344, IEEE-style Inf/NaN.  e4m3fnuz: bias 8, max 240, single NaN
+ * 0x80, no Inf, no negative zero (decoded by the oracle; not produced by the
+ * GPU kernels, which return FP8_ERR_UNSUPPORTED for it). */
+typedef enum { FP8_E4M3FN = 0, FP8_E5M2 = 1, FP8_E4M3FNUZ = 2 } fp8_format_t;
+
+/* Scaling recipes ("FP8 training for Flux models", fp8_recipe):
+ *   DELAYED    cast with the stored per-tensor scale (from the amax history);
+ *              the current amax is max-accumulated into the history slot.
+ *   TENSORWISE one scale per tensor from the current amax.
+ *   ROWWISE    current scaling with one scale per row for the row layout and
+ *              one per column (per expert group and column when grouped) for
+ *              the colwise-transposed layout. */
+typedef enum { FP8_RECIPE_DELAYED = 0, FP8_RECIPE_TENSORWISE = 1, FP8_RECIPE_ROWWISE = 2 } fp8_recipe_kind_t;
+
+/* fp8_amax_compute_algo: most_recent uses the current amax; max uses the
+ * maximum over the history window. */
+typedef enum { FP8_AMAX_MOST_RECENT = 0, FP8_AMAX_MAX = 1 } fp8_amax_algo_t;
+
+/* The recipe knobs.  kind and margin drive fp8_quantize; history_len and
+ * algo drive fp8_update_amax_history (they are carried here so a caller can
+ * hold one struct per layer). */
+typedef struct {
+    int kind;        /* fp8_recipe_kind_t */
+    int margin;      /* fp8_margin: scale = fp8_max / amax / 2^margin, 0..64 */
+    int history_len; /* fp8_amax_history_len */
+    int algo;        /* fp8_amax_algo_t */
+} fp8_recipe_t;
+
+typedef enum {
+    FP8_OK = 0,
+    FP8_ERR_INVALID_ARG = 1,
+    FP8_ERR_UNSUPPORTED = 2,
+    FP8_ERR_ALIGNMENT = 3,
+    FP8_ERR_CUDA = 4,
+    FP8_ERR_TIMEOUT = 5
+} fp8_status_t;
+
+enum { FP8_LAYOUT_ROW = 1, FP8_LAYOUT_COLT = 2 };      /* bitmask of layouts to emit */
+enum { FP8_SCALE_TENSOR = 0, FP8_SCALE_PER_ROW = 1 };  /* GEMM operand scale granularity */
+enum { FP8_GROUPED_M = 0, FP8_GROUPED_K = 1 };         /* grouped GEMM modes */
+
+/*
+ * fp8_quantize -- fused amax + scale + saturating round-to-nearest-even cast
+ * of a bf16 matrix, emitting the row layout, the colwise-transposed layout,
+ * or both from one read of x.
+ *
+ *   x_bf16        [rows][ld_x] bf16, row-major; 16-byte aligned, ld_x % 8 == 0.
+ *   rows, cols    rows >= 0, cols >= 1, cols % 8 == 0.
+ *   fmt           FP8_E4M3FN or FP8_E5M2.
+ *   recipe        kind and margin are used (see fp8_recipe_t).
+ *   layouts       FP8_LAYOUT_ROW | FP8_LAYOUT_COLT (at least one).
+ *   scale_in      DELAYED only: device fp32 [1], the stored scale used for the
+ *                 cast (NULL otherwise).
+ *   amax_out      DELAYED: device fp32 [1] receiving max(amax_out, amax(x))
+ *                 by one relaxed atomic per thread block -- pass the history
+ *                 slot &hist[i*L + 0].  TENSORWISE: required, receives
+ *                 amax(x) (it carries the amax between the reduction and the
+ *                 cast).  ROWWISE: optional (NULL or [1]), receives amax(x).
+ *   q_row         [rows][cols] u8 (if LAYOUT_ROW); q[r][c] = fp8(x[r][c] *
+ *                 s_row(r)).  8-byte aligned.
+ *   scale_inv_row [1] (DELAYED, TENSORWISE) or [rows] (ROWWISE): 1 / scale.
+ *   q_colT        [cols][ld_colT] u8 (if LAYOUT_COLT); q_colT[c][j] =
+ *                 fp8(x[r][c] * s_col(c)) with j = r when ungrouped.  Grouped:
+ *                 group e's rows land at columns poff_e .. poff_e + m_e - 1,
+ *                 poff_e = sum_{e'<e} roundup(m_e', 32); the padding columns up
+ *                 to poff_{e+1} are written as 0.  ld_colT % 16 == 0 and
+ *                 ld_colT >= rows (ungrouped) or >= poff_G (grouped).
+ *   scale_inv_col [1] (DELAYED, TENSORWISE), [cols] (ROWWISE ungrouped) or
+ *                 [num_groups][cols] (ROWWISE grouped).  An empty group, an
+ *                 all-zero column or a non-finite amax gives scale 1.
+ *   group_offsets NULL, or device int32 [num_groups + 1]: offsets[0] = 0,
+ *                 non-decreasing, offsets[num_groups] = rows (the row range
+ *                 of each expert group).  Not validated on the device beyond
+ *                 bounds: rows outside [0, rows) are skipped.
+ *   Scale arithmetic (fp32, IEEE): s = fp8_max / amax, s *= 2^-margin, an
+ *   overflow to Inf becomes FLT_MAX, amax == 0 or non-finite gives s = 1;
+ *   scale_inv = 1 / s.  NaN in x propagates into the amax.
+ */
+FP8GB_API fp8_status_t fp8_quantize(const void *x_bf16, int64_t rows, int64_t cols, int64_t ld_x, int fmt,
+                          const fp8_recipe_t *recipe, int layouts, const float *scale_in, float *amax_out,
+                          uint8_t *q_row, float *scale_inv_row, uint8_t *q_colT, int64_t ld_colT,
+                          float *scale_inv_col, const int32_t *group_offsets, int num_groups, void *stream);
+
+/*
+ * fp8_update_amax_history -- delayed-scaling update for n tensors in one
+ * launch ("FP8 training for Flux models": fp8_amax_history_len,
+ * fp8_amax_compute_algo, fp8_margin; its verification list names a "fused
+ * delayed-scale update").
+ *
+ *   hist            fp32 [n][L] in place; hist[i][0] is the current step's
+ *                   amax (filled by fp8_quantize with DELAYED).
+ *   scale, scale_inv fp32 [n] in place.
+ *   fmt             u8 [n] (fp8_format_t of each tensor; decides fp8_max).
+ *   algo            most_recent: a = hist[i][0]; max: a = max_j hist[i][j]
+ *                   (NaN anywhere in the window gives NaN).
+ *   margin          0..64.
+ *   nonfinite_count int32 [n] or NULL; incremented when a is not finite.
+ *   Per tensor: if a is finite and > 0, scale = fp8_max / a * 2^-margin (Inf
+ *   -> FLT_MAX) and scale_inv = 1 / scale; otherwise both are kept.  Then the
+ *   row is shifted one slot towards the end (hist[j] = hist[j-1], the oldest
+ *   value dropped) and hist[i][0] = 0.
+ *   Limits: n >= 1, 1 <= L <= 32768.
+ */
+FP8GB_API fp8_status_t fp8_update_amax_history(float *hist, float *scale, float *scale_inv, const uint8_t *fmt, int n,
+                                     int L, int algo, int margin, int32_t *nonfinite_count, void *stream);
+
+/*
+ * fp8_scaled_gemm -- C[m][n] = bf16( sum_k A[m][k] * B[n][k] * sa(m) * sb(n) )
+ * with fp32 accumulation on the tcgen05 tensor cores ("TN": both operands
+ * K-contiguous).
+ *
+ *   A  u8 [M][lda], format fa;  B  u8 [N][ldb], format fb  (E4M3FN or E5M2).
+ *   M, N >= 1; K >= 16, K % 16 == 0; lda, ldb >= K, % 16 == 0; A, B 16-byte
+ *   aligned.
+ *   sa, sa_mode   FP8_SCALE_TENSOR: sa[0]; FP8_SCALE_PER_ROW: sa[m], [M].
+ *   sb, sb_mode   FP8_SCALE_TENSOR: sb[0]; FP8_SCALE_PER_ROW: sb[n], [N].
+ *   C_bf16        [M][ldc] bf16, ldc >= N, ldc % 8 == 0, 16-byte aligned.
+ *   The scales are the scale_inv outputs of fp8_quantize.  fprop Y = X W^T
+ *   takes A = X row layout, B = W row layout; dgrad dX = dY W takes A = dY
+ *   row layout, B = W colwise-transposed; wgrad dW = dY^T X takes A = dY
+ *   colwise-transposed, B = X colwise-transposed.
+ */
+FP8GB_API fp8_status_t fp8_scaled_gemm(const uint8_t *A, int fa, int64_t lda, const uint8_t *B, int fb, int64_t ldb,
+                             int64_t M, int64_t N, int64_t K, const float *sa, int sa_mode, const float *sb,
+                             int sb_mode, void *C_bf16, int64_t ldc, void *stream);
+
+/*
+ * fp8_grouped_gemm -- per-expert GEMMs over variable-size row groups in one
+ * launch (grouped GEMM for Mixture-of-Experts, "How PyTorch FP8
+ * Optimizations on AMD GPUs ..." What Happened).
+ *
+ * group_offsets: device int32 [G+1] row ranges (offsets[0] = 0,
+ * non-decreasing, offsets[G] = M_total).  Empty groups are allowed.
+ *
+ * FP8_GROUPED_M (fprop, dgrad): A u8 [M_total][K] (group rows stacked), B u8
+ *   [G][N][K]; C[m][n] = sum_k A[m][k] B[e][n][k] sa(m) sb(e, n) for m in
+ *   group e; C bf16 [M_total][N].  sa: [1] or [M_total]; sb: [1] or [G][N].
+ * FP8_GROUPED_K (wgrad): A u8 [N][ld_T], B u8 [K][ld_T] in the padded
+ *   grouped colwise layout of fp8_quantize (ld_T = that call's ld_colT);
+ *   C[e][n][k] = sum_{r < m_e} A[n][poff_e + r] B[k][poff_e + r] sa(e, n)
+ *   sb(e, k); C bf16 [G][N][K]; an empty group's block is written as 0.
+ *   sa: [1] or [G][N]; sb: [1] or [G][K].
+ * Limits: K % 16 == 0 (M mode), N % 8 == 0 and K % 8 == 0 (K mode),
+ * ld_T % 16 == 0, 1 <= G <= 4096; 16-byte aligned A, B, C.
+ */
+FP8GB_API fp8_status_t fp8_grouped_gemm(int mode, const uint8_t *A, int fa, const uint8_t *B, int fb,
+                              const int32_t *group_offsets, int G, int64_t M_total, int64_t N, int64_t K,
+                              const float *sa, int sa_mode, const float *sb, int sb_mode, void *C_bf16,
+                              int64_t ld_T, void *stream);
+
+/*
+ * fp8_group_padded_offsets -- host helper for the grouped colwise layout.
+ * host_offsets int32 [G+1] -> host_padded_out int64 [G+1] (may be NULL) with
+ * poff_e = sum_{e'<e} roundup(m_e', align); returns poff_G (the ld_colT /
+ * ld_T to allocate), or -1 for bad arguments (align must be a positive
+ * multiple of 16; offsets non-decreasing).
+ */
+FP8GB_API int64_t fp8_group_padded_offsets(const int32_t *host_offsets, int G, int align, int64_t *host_padded_out);
+
+/* Synchronise `stream`, then report and clear a device-side timeout word:
+ * FP8_OK, FP8_ERR_TIMEOUT, or FP8_ERR_CUDA. */
+FP8GB_API fp8_status_t fp8_sync_status(void *stream);
+
+/* Test support for the bounded-wait machinery: launches one thread block
+ * that waits on a shared-memory barrier nothing will complete, giving up
+ * after about `wait_ns` nanoseconds (1e3 .. 1e10).  The wait gives up,
+ * records the device error word and the kernel returns; fp8_sync_status()
+ * then reports FP8_ERR_TIMEOUT. */
+FP8GB_API fp8_status_t fp8_selftest_bounded_wait(int64_t wait_ns, void *stream);
+
+/* Human-readable name of a status; never NULL. */
+FP8GB_API const char *fp8_status_string(fp8_status_t s);
+
+/* Message of the last CUDA error seen by this library in this thread. */
+FP8GB_API const char *fp8_last_cuda_error(void);
+
+/* Library version, e.g. "fp8gb 0.1 sm_103a". */
+FP8GB_API const char *fp8_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8GB_H */

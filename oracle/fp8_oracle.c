@@ -224,6 +224,8 @@ static float amax_acc(float acc, float v)
 /* Quantize                                                                  */
 /* ------------------------------------------------------------------------ */
 
+float orc_amax_bf16(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x);
+
 static int64_t roundup32(int64_t m) { return (m + 31) / 32 * 32; }
 
 /* Padded column offsets of the grouped colwise layout; returns the total. */
@@ -276,8 +278,7 @@ int orc_quantize(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, in
     }
 
     /* whole-tensor amax */
-    for (int64_t r = 0; r < rows; r++)
-        for (int64_t c = 0; c < cols; c++) tensor_amax = amax_acc(tensor_amax, bf16_to_float(x[r * ld_x + c]));
+    tensor_amax = orc_amax_bf16(x, rows, cols, ld_x);
 
     if (kind == ORC_DELAYED || kind == ORC_TENSORWISE) {
         float s, sinv;
@@ -351,12 +352,20 @@ int orc_quantize(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, in
     return 0;
 }
 
-/* Whole-tensor amax of a bf16 matrix (NaN propagates). */
+/* Whole-tensor amax of a bf16 matrix (NaN propagates): per-row maxima in
+ * parallel, then their maximum (max is independent of the order). */
 float orc_amax_bf16(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x)
 {
     float acc = 0.0f;
-    for (int64_t r = 0; r < rows; r++)
-        for (int64_t c = 0; c < cols; c++) acc = amax_acc(acc, bf16_to_float(x[r * ld_x + c]));
+    float *rowmax = (float *)malloc(sizeof(float) * (rows > 0 ? rows : 1));
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; r++) {
+        float m = 0.0f;
+        for (int64_t c = 0; c < cols; c++) m = amax_acc(m, bf16_to_float(x[r * ld_x + c]));
+        rowmax[r] = m;
+    }
+    for (int64_t r = 0; r < rows; r++) acc = (isnan(acc) || isnan(rowmax[r])) ? NAN : (rowmax[r] > acc ? rowmax[r] : acc);
+    free(rowmax);
     return acc;
 }
 

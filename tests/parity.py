@@ -1,0 +1,92 @@
+"""Helpers shared by the GPU parity tests: comparisons against the oracle."""
+import numpy as np
+import torch
+
+import synth
+
+TOL_REL = 2e-3   # |out - ref| <= TOL_REL * sum_k |a_k b_k| * |sa sb| + TOL_ABS
+TOL_ABS = 1e-5
+
+
+def nan_mask(codes: np.ndarray, fmt: int) -> np.ndarray:
+    c = codes.astype(np.int32)
+    if fmt == 2:
+        return c == 0x80
+    if fmt == 0:
+        return (c & 0x7F) == 0x7F
+    return (c & 0x7F) > 0x7C
+
+
+def assert_codes_equal(gpu: np.ndarray, ref: np.ndarray, fmt: int, what: str = ""):
+    """Bit-exact byte comparison; NaN outputs are compared by class."""
+    assert gpu.shape == ref.shape, (what, gpu.shape, ref.shape)
+    ng, nr = nan_mask(gpu, fmt), nan_mask(ref, fmt)
+    bad = (ng != nr) | ((gpu != ref) & ~nr)
+    if bad.any():
+        idx = np.argwhere(bad)[:8]
+        raise AssertionError(f"{what}: {int(bad.sum())} byte mismatches, first at {idx.tolist()}: "
+                             f"gpu {[hex(int(gpu[tuple(i)])) for i in idx]} ref {[hex(int(ref[tuple(i)])) for i in idx]}")
+
+
+def assert_f32_bits_equal(gpu: np.ndarray, ref: np.ndarray, what: str = ""):
+    g = np.ascontiguousarray(gpu, np.float32)
+    r = np.ascontiguousarray(ref, np.float32)
+    assert g.shape == r.shape, (what, g.shape, r.shape)
+    same = (g.view(np.uint32) == r.view(np.uint32)) | (np.isnan(g) & np.isnan(r))
+    if not same.all():
+        idx = np.argwhere(~same)[:8]
+        raise AssertionError(f"{what}: {int((~same).sum())} fp32 mismatches at {idx.tolist()}: "
+                             f"gpu {g[~same][:8]} ref {r[~same][:8]}")
+
+
+def bf16_to_f64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def check_gemm(out, ref, bound, what=""):
+    """GEMM tolerance: |out - ref| <= 2e-3 * bound + 1e-5, elementwise."""
+    out = np.asarray(out, np.float64)
+    err = np.abs(out - ref)
+    lim = TOL_REL * bound + TOL_ABS
+    bad = ~(err <= lim)
+    if bad.any():
+        i = np.argwhere(bad)[:6]
+        raise AssertionError(f"{what}: {int(bad.sum())}/{bad.size} outside tolerance; first {i.tolist()}: "
+                             f"out {out[bad][:6]} ref {ref[bad][:6]} bound {bound[bad][:6]}")
+    denom = np.where(bound > 0, bound, 1.0)
+    return float((err / denom).max()) if err.size else 0.0
+
+
+def finite_codes(gen: torch.Generator, shape, fmt: int) -> torch.Tensor:
+    """Random FP8 codes with NaN / Inf codes replaced (CPU uint8)."""
+    c = torch.randint(0, 256, shape, generator=gen, dtype=torch.int32)
+    if fmt == 0:
+        bad = (c & 0x7F) == 0x7F
+    else:
+        bad = (c & 0x7F) >= 0x7C
+    c[bad] = 0x30
+    return c.to(torch.uint8)
+
+
+def realistic_codes(gen: torch.Generator, shape, fmt: int) -> torch.Tensor:
+    """Codes of N(0,1) values scaled so the max lands near the format max."""
+    x = torch.randn(shape, generator=gen)
+    s = (448.0 if fmt == 0 else 57344.0) / float(x.abs().max())
+    dt = torch.float8_e4m3fn if fmt == 0 else torch.float8_e5m2
+    return (x * s).to(dt).view(torch.uint8)
+
+
+def sample_points(gen: torch.Generator, M: int, N: int, n_rows=64, n_cols=64, n_rand=4096):
+    """64 full rows + 64 full columns + random points (numpy int64 pm, pn)."""
+    rows = torch.randperm(M, generator=gen)[:min(n_rows, M)].numpy()
+    cols = torch.randperm(N, generator=gen)[:min(n_cols, N)].numpy()
+    pm = [np.repeat(rows, N), np.tile(np.arange(N), len(rows)).astype(np.int64)]
+    pc = [np.tile(np.arange(M), len(cols)).astype(np.int64), np.repeat(cols, M)]
+    rm = torch.randint(0, M, (n_rand,), generator=gen).numpy()
+    rn = torch.randint(0, N, (n_rand,), generator=gen).numpy()
+    return (np.concatenate([pm[0], pc[0], rm]).astype(np.int64),
+            np.concatenate([pm[1], pc[1], rn]).astype(np.int64))
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    return synth.bf16_bits(t)

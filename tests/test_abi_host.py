@@ -1,0 +1,183 @@
+"""Host-only checks of the C ABI (no GPU needed, no kernel launched).
+
+  * libfp8gb.so loads and exports every function that include/fp8gb.h
+    declares;
+  * argument validation rejects bad calls with the documented status before
+    anything touches the device;
+  * the grouped-layout helper computes the padded offsets.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+import fp8_mixed_precision_scale_gb300 as fp8
+from fp8_mixed_precision_scale_gb300 import build as fp8build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fp8gb.h")
+
+OK, INVALID, UNSUPPORTED, ALIGN = 0, 1, 2, 3
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fp8build.build()
+    return fp8.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fp8_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_four_entry_points():
+    names = declared_functions()
+    for n in ("fp8_quantize", "fp8_update_amax_history", "fp8_scaled_gemm", "fp8_grouped_gemm"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", fp8.LIB_PATH], capture_output=True, text=True, check=True)
+    exported = set(re.findall(r"\sT\s+(\w+)", out.stdout))
+    for name in declared_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+    assert set(fp8.EXPORTED) <= set(declared_functions())
+
+
+def test_library_has_no_torch_dependency():
+    out = subprocess.run(["ldd", fp8.LIB_PATH], capture_output=True, text=True)
+    assert "torch" not in out.stdout and "c10" not in out.stdout
+
+
+def test_status_strings(lib):
+    assert lib.fp8_status_string(0) == b"FP8_OK"
+    assert lib.fp8_status_string(5) == b"FP8_ERR_TIMEOUT"
+    assert lib.fp8_status_string(99) == b"FP8_ERR_UNKNOWN"
+    assert lib.fp8_version().startswith(b"fp8gb")
+
+
+FAKE = 0x10000  # a 16-byte-aligned non-null address: validation never dereferences it
+
+
+def q_call(lib, **kw):
+    args = dict(x=FAKE, rows=64, cols=64, ld_x=64, fmt=0, kind=0, margin=0, layouts=3, scale_in=FAKE,
+                amax_out=FAKE, q_row=FAKE, sinv_row=FAKE, q_colT=FAKE, ld_colT=64, sinv_col=FAKE, offsets=None,
+                G=0)
+    args.update(kw)
+    rec = fp8.fp8_recipe_t(args["kind"], args["margin"], 1024, 0)
+    P = ctypes.c_void_p
+    return lib.fp8_quantize(P(args["x"]), args["rows"], args["cols"], args["ld_x"], args["fmt"], ctypes.byref(rec),
+                            args["layouts"], P(args["scale_in"]), P(args["amax_out"]), P(args["q_row"]),
+                            P(args["sinv_row"]), P(args["q_colT"]), args["ld_colT"], P(args["sinv_col"]),
+                            P(args["offsets"]), args["G"], None)
+
+
+def test_quantize_validation(lib):
+    assert q_call(lib, x=None) == INVALID
+    assert q_call(lib, rows=-1) == INVALID
+    assert q_call(lib, cols=0) == INVALID
+    assert q_call(lib, ld_x=32) == INVALID
+    assert q_call(lib, fmt=2) == UNSUPPORTED          # e4m3fnuz is oracle-only
+    assert q_call(lib, fmt=7) == INVALID
+    assert q_call(lib, kind=3) == INVALID
+    assert q_call(lib, margin=-1) == INVALID
+    assert q_call(lib, margin=65) == INVALID
+    assert q_call(lib, layouts=0) == INVALID
+    assert q_call(lib, layouts=4) == INVALID
+    assert q_call(lib, q_row=None) == INVALID
+    assert q_call(lib, sinv_col=None) == INVALID
+    assert q_call(lib, scale_in=None) == INVALID      # delayed needs the stored scale
+    assert q_call(lib, amax_out=None) == INVALID      # ... and the history slot
+    assert q_call(lib, kind=1, amax_out=None) == INVALID
+    assert q_call(lib, cols=60, ld_x=64) == ALIGN
+    assert q_call(lib, ld_x=68) == ALIGN
+    assert q_call(lib, x=FAKE + 8) == ALIGN
+    assert q_call(lib, ld_colT=72) == ALIGN
+    assert q_call(lib, ld_colT=48) == INVALID         # shorter than rows
+    assert q_call(lib, offsets=FAKE, G=0) == INVALID
+    assert q_call(lib, G=3) == INVALID
+
+
+def g_call(lib, **kw):
+    a = dict(A=FAKE, fa=0, lda=128, B=FAKE, fb=0, ldb=128, M=128, N=256, K=128, sa=FAKE, sam=0, sb=FAKE, sbm=0,
+             C=FAKE, ldc=256)
+    a.update(kw)
+    P = ctypes.c_void_p
+    return lib.fp8_scaled_gemm(P(a["A"]), a["fa"], a["lda"], P(a["B"]), a["fb"], a["ldb"], a["M"], a["N"], a["K"],
+                               P(a["sa"]), a["sam"], P(a["sb"]), a["sbm"], P(a["C"]), a["ldc"], None)
+
+
+def test_gemm_validation(lib):
+    assert g_call(lib, A=None) == INVALID
+    assert g_call(lib, C=None) == INVALID
+    assert g_call(lib, fa=2) == UNSUPPORTED
+    assert g_call(lib, fb=5) == INVALID
+    assert g_call(lib, M=0) == INVALID
+    assert g_call(lib, K=0) == INVALID
+    assert g_call(lib, lda=64) == INVALID
+    assert g_call(lib, ldc=128) == INVALID
+    assert g_call(lib, sam=2) == INVALID
+    assert g_call(lib, K=120, lda=128) == ALIGN
+    assert g_call(lib, lda=136) == ALIGN
+    assert g_call(lib, ldc=260) == ALIGN
+    assert g_call(lib, A=FAKE + 4) == ALIGN
+    assert g_call(lib, C=FAKE + 2) == ALIGN
+
+
+def gg_call(lib, **kw):
+    a = dict(mode=0, A=FAKE, fa=0, B=FAKE, fb=0, off=FAKE, G=4, Mt=100, N=256, K=128, sa=FAKE, sam=1, sb=FAKE,
+             sbm=1, C=FAKE, ldT=0)
+    a.update(kw)
+    P = ctypes.c_void_p
+    return lib.fp8_grouped_gemm(a["mode"], P(a["A"]), a["fa"], P(a["B"]), a["fb"], P(a["off"]), a["G"], a["Mt"],
+                                a["N"], a["K"], P(a["sa"]), a["sam"], P(a["sb"]), a["sbm"], P(a["C"]), a["ldT"], None)
+
+
+def test_grouped_gemm_validation(lib):
+    assert gg_call(lib, off=None) == INVALID
+    assert gg_call(lib, mode=2) == INVALID
+    assert gg_call(lib, G=0) == INVALID
+    assert gg_call(lib, G=5000) == INVALID
+    assert gg_call(lib, fa=2) == UNSUPPORTED
+    assert gg_call(lib, K=120) == ALIGN
+    assert gg_call(lib, N=100) == ALIGN
+    assert gg_call(lib, mode=1, ldT=40) == ALIGN
+    assert gg_call(lib, mode=1, ldT=0) == ALIGN
+
+
+def test_update_validation(lib):
+    P = ctypes.c_void_p
+    call = lambda **kw: lib.fp8_update_amax_history(  # noqa: E731
+        P(kw.get("h", FAKE)), P(FAKE), P(FAKE), P(FAKE), kw.get("n", 4), kw.get("L", 16), kw.get("algo", 0),
+        kw.get("margin", 0), None, None)
+    assert call(h=None) == INVALID
+    assert call(n=0) == INVALID
+    assert call(L=0) == INVALID
+    assert call(L=40000) == INVALID
+    assert call(algo=2) == INVALID
+    assert call(margin=70) == INVALID
+    assert call(h=FAKE + 2) == ALIGN
+
+
+def test_padded_offsets_helper(lib):
+    total, poff = fp8.fp8_group_padded_offsets([0, 5, 5, 38, 39, 39, 79])
+    assert total == 192
+    assert list(poff.numpy()) == [0, 32, 32, 96, 128, 128, 192]
+    total64, _ = fp8.fp8_group_padded_offsets([0, 5, 5, 38], align=64)
+    assert total64 == 128
+    with pytest.raises(fp8.Fp8Error):
+        fp8.fp8_group_padded_offsets([0, 5, 3])
+    off = np.array([0, 1], np.int32)
+    assert lib.fp8_group_padded_offsets(ctypes.c_void_p(off.ctypes.data), 1, 24, None) == -1
+
+
+def test_format_roles():
+    assert fp8.format_for("e4m3", "grad") == fp8.E4M3FN
+    assert fp8.format_for("hybrid", "grad") == fp8.E5M2
+    assert fp8.format_for("hybrid", "weight") == fp8.E4M3FN
