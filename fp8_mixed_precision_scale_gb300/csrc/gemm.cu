@@ -60,6 +60,7 @@ struct GemmParams {
     int sa_per_row, sb_per_row;
     uint16_t *C;
     int64_t ldc;
+    int c_vec16;  // every row of C starts 16-byte aligned: 8-wide vector stores
     int num_m_blk, num_n_blk, num_k_blk;
     int m_fastest;
     int64_t total_tiles;  // dense
@@ -353,7 +354,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             if (ti.nkb == 0) {
                 if (row_ok)
                     for (int64_t c = ti.col0; c < ti.col0 + BN && c < ti.col_end; c += 8) {
-                        if (c + 8 <= ti.col_end)
+                        if (p.c_vec16 && c + 8 <= ti.col_end)
                             *reinterpret_cast<uint4 *>(crow + c) = make_uint4(0, 0, 0, 0);
                         else
                             for (int64_t j = c; j < ti.col_end; j++) crow[j] = 0;
@@ -387,7 +388,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 #pragma unroll
                 for (int g = 0; g < 4; g++) {
                     const int64_t c = c0 + g * 8;
-                    if (c + 8 <= ti.col_end) {
+                    if (p.c_vec16 && c + 8 <= ti.col_end) {
                         *reinterpret_cast<uint4 *>(crow + c) =
                             make_uint4(packed[4 * g], packed[4 * g + 1], packed[4 * g + 2], packed[4 * g + 3]);
                     } else {
@@ -487,8 +488,8 @@ extern "C" fp8_status_t fp8_scaled_gemm(const uint8_t *A, int fa, int64_t lda, c
         (sb_mode != FP8_SCALE_TENSOR && sb_mode != FP8_SCALE_PER_ROW))
         return FP8_ERR_INVALID_ARG;
     if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return FP8_ERR_INVALID_ARG;
-    if (K % 16 != 0 || lda % 16 != 0 || ldb % 16 != 0 || ldc % 8 != 0) return FP8_ERR_ALIGNMENT;
-    if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C_bf16, 16) || !aligned(sa, 4) || !aligned(sb, 4))
+    if (K % 16 != 0 || lda % 16 != 0 || ldb % 16 != 0) return FP8_ERR_ALIGNMENT;
+    if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C_bf16, 2) || !aligned(sa, 4) || !aligned(sb, 4))
         return FP8_ERR_ALIGNMENT;
 
     GemmParams p{};
@@ -501,6 +502,7 @@ extern "C" fp8_status_t fp8_scaled_gemm(const uint8_t *A, int fa, int64_t lda, c
     p.sb_per_row = sb_mode == FP8_SCALE_PER_ROW;
     p.C = static_cast<uint16_t *>(C_bf16);
     p.ldc = ldc;
+    p.c_vec16 = ldc % 8 == 0 && aligned(C_bf16, 16);
     p.num_m_blk = (int)((M + BM - 1) / BM);
     p.num_n_blk = (int)((N + BN - 1) / BN);
     p.num_k_blk = (int)((K + BK - 1) / BK);
@@ -533,7 +535,7 @@ extern "C" fp8_status_t fp8_grouped_gemm(int mode, const uint8_t *A, int fa, con
         return FP8_ERR_INVALID_ARG;
     if (M_total > INT32_MAX || N > INT32_MAX || K > INT32_MAX || (int64_t)G * N > INT32_MAX)
         return FP8_ERR_INVALID_ARG;
-    if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C_bf16, 16) || !aligned(sa, 4) || !aligned(sb, 4))
+    if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C_bf16, 2) || !aligned(sa, 4) || !aligned(sb, 4))
         return FP8_ERR_ALIGNMENT;
 
     GemmParams p{};
@@ -553,8 +555,9 @@ extern "C" fp8_status_t fp8_grouped_gemm(int mode, const uint8_t *A, int fa, con
     const int64_t grid = num_sms();
 
     if (mode == FP8_GROUPED_M) {
-        if (K % 16 != 0 || N % 8 != 0) return FP8_ERR_ALIGNMENT;
+        if (K % 16 != 0) return FP8_ERR_ALIGNMENT;
         p.ldc = N;
+        p.c_vec16 = N % 8 == 0 && aligned(C_bf16, 16);
         p.num_m_blk = 0;
         p.num_n_blk = (int)((N + BN - 1) / BN);
         p.num_k_blk = (int)((K + BK - 1) / BK);
@@ -563,8 +566,9 @@ extern "C" fp8_status_t fp8_grouped_gemm(int mode, const uint8_t *A, int fa, con
         return launch_gemm<MODE_MGROUP>(ma, mb, p, fa, fb, grid, st);
     }
     // K-grouped (wgrad): C[e] = A_e [N][m_e] . B_e [K][m_e]^T
-    if (ld_T < 16 || ld_T % 16 != 0 || N % 8 != 0 || K % 8 != 0) return FP8_ERR_ALIGNMENT;
+    if (ld_T < 16 || ld_T % 16 != 0) return FP8_ERR_ALIGNMENT;
     p.ldc = K;
+    p.c_vec16 = K % 8 == 0 && aligned(C_bf16, 16);  // then N*K % 8 == 0 too
     p.ld_T = ld_T;
     p.num_m_blk = (int)((N + BM - 1) / BM);
     p.num_n_blk = (int)((K + BN - 1) / BN);

@@ -174,7 +174,8 @@ FP8GB_API fp8_status_t fp8_update_amax_history(float *hist, float *scale, float 
  *   aligned.
  *   sa, sa_mode   FP8_SCALE_TENSOR: sa[0]; FP8_SCALE_PER_ROW: sa[m], [M].
  *   sb, sb_mode   FP8_SCALE_TENSOR: sb[0]; FP8_SCALE_PER_ROW: sb[n], [N].
- *   C_bf16        [M][ldc] bf16, ldc >= N, ldc % 8 == 0, 16-byte aligned.
+ *   C_bf16        [M][ldc] bf16, ldc >= N, 2-byte aligned (16-byte vector
+ *                 stores are used when C is 16-byte aligned and ldc % 8 == 0).
  *   The scales are the scale_inv outputs of fp8_quantize.  fprop Y = X W^T
  *   takes A = X row layout, B = W row layout; dgrad dX = dY W takes A = dY
  *   row layout, B = W colwise-transposed; wgrad dW = dY^T X takes A = dY
@@ -200,8 +201,8 @@ FP8GB_API fp8_status_t fp8_scaled_gemm(const uint8_t *A, int fa, int64_t lda, co
  *   C[e][n][k] = sum_{r < m_e} A[n][poff_e + r] B[k][poff_e + r] sa(e, n)
  *   sb(e, k); C bf16 [G][N][K]; an empty group's block is written as 0.
  *   sa: [1] or [G][N]; sb: [1] or [G][K].
- * Limits: K % 16 == 0 (M mode), N % 8 == 0 and K % 8 == 0 (K mode),
- * ld_T % 16 == 0, 1 <= G <= 4096; 16-byte aligned A, B, C.
+ * Limits: K % 16 == 0 (M mode), ld_T % 16 == 0 (K mode), 1 <= G <= 4096;
+ * 16-byte aligned A and B; C 2-byte aligned.
  */
 FP8GB_API fp8_status_t fp8_grouped_gemm(int mode, const uint8_t *A, int fa, const uint8_t *B, int fb,
                               const int32_t *group_offsets, int G, int64_t M_total, int64_t N, int64_t K,

@@ -238,7 +238,8 @@ def test_deterministic_repeats():
     rec = fp8.Recipe(kind=fp8.ROWWISE)
     a = fp8.quantize(x, 0, rec, 3)
     b = fp8.quantize(x, 0, rec, 3)
-    assert torch.equal(a.q_row, b.q_row) and torch.equal(a.q_colT, b.q_colT)
+    # columns past `rows` of the transposed layout are padding the kernel never writes
+    assert torch.equal(a.q_row, b.q_row) and torch.equal(a.q_colT[:, :700], b.q_colT[:, :700])
     assert torch.equal(a.scale_inv_col, b.scale_inv_col)
 
 
