@@ -111,8 +111,9 @@ def _sampled(orc, M, N, K, fa, fb, seed, per_row=True):
     xb = torch.randn((N, K), generator=gd, device=DEV)
     dta = torch.float8_e4m3fn if fa == 0 else torch.float8_e5m2
     dtb = torch.float8_e4m3fn if fb == 0 else torch.float8_e5m2
-    A = (xa * 100).to(dta).view(torch.uint8)
-    B = (xb * 100).to(dtb).view(torch.uint8)
+    # torch's cast is not saturating: clamp to the format range first
+    A = (xa * 100).clamp(-448, 448).to(dta).view(torch.uint8)
+    B = (xb * 100).clamp(-448, 448).to(dtb).view(torch.uint8)
     del xa, xb
     g = torch.Generator().manual_seed(seed)
     sa, sb = scales(g, M, per_row), scales(g, N, per_row)
@@ -197,8 +198,10 @@ def test_grouped_m_moe_shape_sampled(orc):
     off = offsets_of(sizes)
     G, Mt, N, K = len(sizes), int(off[-1]), 2048, 7168
     gd = torch.Generator(device=DEV).manual_seed(9)
-    A = (torch.randn((Mt, K), generator=gd, device=DEV) * 100).to(torch.float8_e4m3fn).view(torch.uint8)
-    B = (torch.randn((G, N, K), generator=gd, device=DEV) * 100).to(torch.float8_e4m3fn).view(torch.uint8)
+    A = (torch.randn((Mt, K), generator=gd, device=DEV) * 100).clamp(-448, 448).to(torch.float8_e4m3fn)
+    A = A.view(torch.uint8)
+    B = (torch.randn((G, N, K), generator=gd, device=DEV) * 100).clamp(-448, 448).to(torch.float8_e4m3fn)
+    B = B.view(torch.uint8)
     g = torch.Generator().manual_seed(9)
     sa = scales(g, Mt, True)
     sb = scales(g, G * N, True)
