@@ -52,7 +52,8 @@ def peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms; only the
+    samples taken inside the timed window are kept."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -60,12 +61,12 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.lines = []
+        self.lines = []  # (host time, csv line)
 
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                                          "-lms", "200", "-i", str(self.index)], stdout=subprocess.PIPE,
+                                          "-lms", "100", "-i", str(self.index)], stdout=subprocess.PIPE,
                                          stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -74,9 +75,9 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
 
-    def stop(self):
+    def stop(self, window=None):
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -87,7 +88,9 @@ class ClockSampler:
         self.thread.join(timeout=2)
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ts, ln in self.lines:
+            if window is not None and not (window[0] <= ts <= window[1]):
+                continue
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) != 6:
                 continue
@@ -112,7 +115,14 @@ class ClockSampler:
 class MlpStep:
     """Buffers and the launch sequence of one FP8 fwd+bwd step of the MLP block."""
 
-    def __init__(self, dev, seed: int):
+    SHAPES = {"x": ((T_, H_), 1.0), "w_gate": ((F_, H_), 0.02), "w_up": ((F_, H_), 0.02),
+              "w_down": ((H_, F_), 0.02), "h": ((T_, F_), 1.0), "dy_down": ((T_, H_), 1e-4),
+              "dy_gate": ((T_, F_), 1e-4), "dy_up": ((T_, F_), 1e-4)}
+    OUTS = {"gate": (T_, F_), "up": (T_, F_), "y": (T_, H_), "dh": (T_, F_), "dx_gate": (T_, H_),
+            "dx_up": (T_, H_), "dw_down": (H_, F_), "dw_gate": (F_, H_), "dw_up": (F_, H_)}
+
+    def __init__(self, dev, seed: int, keys=None, outs=None):
+        """keys / outs restrict the tensors allocated (single-kernel workloads)."""
         import fp8_mixed_precision_scale_gb300 as fp8
         self.fp8 = fp8
         g = torch.Generator(device=dev)
@@ -121,17 +131,8 @@ class MlpStep:
         def normal(shape, std):
             return (torch.randn(shape, generator=g, device=dev) * std).to(torch.bfloat16)
 
-        self.inp = {
-            "x": normal((T_, H_), 1.0),
-            "w_gate": normal((F_, H_), 0.02),
-            "w_up": normal((F_, H_), 0.02),
-            "w_down": normal((H_, F_), 0.02),
-            "h": normal((T_, F_), 1.0),
-            "dy_down": normal((T_, H_), 1e-4),
-            "dy_gate": normal((T_, F_), 1e-4),
-            "dy_up": normal((T_, F_), 1e-4),
-        }
-        self.order = list(self.inp.keys())
+        self.order = list(self.SHAPES.keys())
+        self.inp = {k: normal(*self.SHAPES[k]) for k in self.order if keys is None or k in keys}
         self.fmt = {k: (fp8.E5M2 if k.startswith("dy") else fp8.E4M3FN) for k in self.order}
         n = len(self.order)
         self.hist = torch.zeros((n, L_HIST), dtype=torch.float32, device=dev)
@@ -145,9 +146,8 @@ class MlpStep:
                              colT=torch.empty((c, r), dtype=torch.uint8, device=dev),
                              srow=torch.empty(1, dtype=torch.float32, device=dev),
                              scol=torch.empty(1, dtype=torch.float32, device=dev))
-        e = lambda r, c: torch.empty((r, c), dtype=torch.bfloat16, device=dev)  # noqa: E731
-        self.out = dict(gate=e(T_, F_), up=e(T_, F_), y=e(T_, H_), dh=e(T_, F_), dx_gate=e(T_, H_),
-                        dx_up=e(T_, H_), dw_down=e(H_, F_), dw_gate=e(F_, H_), dw_up=e(F_, H_))
+        self.out = {k: torch.empty(shape, dtype=torch.bfloat16, device=dev) for k, shape in self.OUTS.items()
+                    if outs is None or k in outs}
         self.recipe = fp8.Recipe(kind=fp8.DELAYED, margin=0, history_len=L_HIST, algo=fp8.MOST_RECENT)
         # launches per step: 8 quantize (1 kernel each, delayed) + 9 GEMMs + 1 update
         self.launches_per_step = 8 + 9 + 1
@@ -262,6 +262,12 @@ def run_gpu(args, rank, world, local_rank):
     hbm_gbs, bf16_burst, bf16_sust, peak_src = peaks()
     fp8_peak = 2.0 * bf16_sust               # FP8 dense = 2x bf16 dense (nominal 4.5 vs 2.25 PFLOP/s)
 
+    if args.workload == "gemm":
+        run_single_kernel(args, MlpStep(dev, seed=1 + rank, keys=("x", "w_gate"), outs=("gate",)), rank, world)
+        return
+    if args.workload == "quantize":
+        run_single_kernel(args, MlpStep(dev, seed=1 + rank, keys=("dy_gate",), outs=()), rank, world)
+        return
     step = MlpStep(dev, seed=1 + rank)
     for _ in range(max(3, args.warmup)):
         step.run(world=world)
@@ -277,15 +283,17 @@ def run_gpu(args, rank, world, local_rank):
     ev = {"q": [], "g": [], "u": []}
     barrier()
     sampler.start()
-    time.sleep(0.25)
+    time.sleep(0.3)
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
+    w0 = time.time()
     t_start.record()
     for _ in range(args.steps):
         step.run(ev, world=world)
     t_end.record()
     barrier()
-    clocks = sampler.stop()
+    w1 = time.time()
+    clocks = sampler.stop((w0, w1))
     st = fp8.fp8_sync_status()
     assert st == 0, f"device status {st}"
     total_ms = t_start.elapsed_time(t_end)
@@ -377,6 +385,34 @@ def run_gpu(args, rank, world, local_rank):
         print(json.dumps(out), flush=True)
 
 
+def run_single_kernel(args, step, rank, world):
+    """Time one kernel of the step in isolation (profiling aid)."""
+    import fp8_mixed_precision_scale_gb300 as fp8
+    if args.workload == "gemm":
+        for k in ("x", "w_gate"):   # real FP8 operands for the GEMM
+            step.quantize(k, step.order.index(k))
+        fn = lambda: step.gemm(*MlpStep.GEMMS[0])  # noqa: E731
+        work, unit = GEMM_FLOP / 1e12, "TFLOP/s"
+    else:
+        fn = lambda: step.quantize("dy_gate", step.order.index("dy_gate"))  # noqa: E731
+        work, unit = QUANT_ELEMS["dy_gate"] * QUANT_BYTES_PER_ELEM / 1e9, "GB/s"
+    for _ in range(max(3, args.warmup)):
+        fn()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.steps):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    assert fp8.fp8_sync_status() == 0
+    ms = a.elapsed_time(b) / args.steps
+    if rank == 0:
+        print(json.dumps({"workload": args.workload, "ms_per_launch": round(ms, 4),
+                          "value": round(work / (ms * 1e-3), 1), "unit": unit, "launches": args.steps}), flush=True)
+
+
 def run_reference(args, rank, world):
     """The oracle as it stands, timed on the host cores (rank 0 only)."""
     if rank != 0:
@@ -408,10 +444,14 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="llama_mlp", choices=["llama_mlp", "gemm", "quantize"],
+                    help="llama_mlp: the whole fwd+bwd FP8 step (default); gemm / quantize: one kernel of it "
+                         "(the gate-projection GEMM 8192x14336x4096, the delayed quantize of a [8192, 14336] "
+                         "tensor), for profiling")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
