@@ -40,6 +40,22 @@ QUANT_BYTES_PER_ELEM = 4                  # 2 B read + 1 B per layout, two layou
 WORKLOAD = ("llama3-8b-mlp fwd+bwd, delayed scaling: tokens 8192, hidden 4096, ffn 14336, "
             "hybrid e4m3 fwd / e5m2 grads, amax history 1024 most_recent, margin 0")
 
+# DRAM bytes (read + write) of one dense GEMM launch, the gate projection
+# 8192x14336x4096, from one ncu capture (profiles/fp8_gemm_kernel_llama_gate_8192x14336x4096.md).
+# Reported only while the profiled sources are unchanged.
+GEMM_TRAFFIC = {"bytes": 291.5e6,
+                "sources": {"gemm.cu": "bdce445243241ecb", "fp8gb_device.cuh": "ea559f4d3db429bb"}}
+
+
+def gemm_traffic():
+    import hashlib
+    csrc = os.path.join(ROOT, "fp8_mixed_precision_scale_gb300", "csrc")
+    for name, want in GEMM_TRAFFIC["sources"].items():
+        with open(os.path.join(csrc, name), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest()[:16] != want:
+                return None
+    return GEMM_TRAFFIC["bytes"]
+
 
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -372,7 +388,7 @@ def run_gpu(args, rank, world, local_rank):
                      "frac_of_hbm": round(q_gbs / hbm_gbs, 4), "bytes_per_elem": QUANT_BYTES_PER_ELEM},
         "update_us": round(1e3 * sum(u_ms) / len(u_ms), 2),
         "roofline": {"bound": "tensor", "achieved": round(gemm_tflops, 1), "peak": round(fp8_peak, 1),
-                     "unit": "TFLOP/s", "frac": round(gemm_tflops / fp8_peak, 4), "traffic": None,
+                     "unit": "TFLOP/s", "frac": round(gemm_tflops / fp8_peak, 4), "traffic": gemm_traffic(),
                      "peak_source": f"{peak_src}: 2 x sustained bf16 {bf16_sust} TFLOP/s (fp8/bf16 nominal ratio 2)"},
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
