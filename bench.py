@@ -211,10 +211,8 @@ class MlpStep:
         for g in self.GEMMS[3:]:
             self._timed(ev, "g", lambda g=g: self.gemm(*g))
         if world > 1:
-            import torch.distributed as dist
-            cur = self.hist[:, 0].contiguous()
-            dist.all_reduce(cur, op=dist.ReduceOp.MAX)
-            self.hist[:, 0].copy_(cur)
+            from fp8_mixed_precision_scale_gb300 import dp
+            dp.reduce_current_amax(self.hist)
         self._timed(ev, "u", lambda: self.fp8.fp8_update_amax_history(
             self.hist, self.scale, self.scale_inv, self.fmt_dev, len(self.order), L_HIST, self.fp8.MOST_RECENT, 0))
 

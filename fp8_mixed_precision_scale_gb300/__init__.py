@@ -31,7 +31,7 @@ DELAYED, TENSORWISE, ROWWISE = 0, 1, 2
 MOST_RECENT, MAX = 0, 1
 LAYOUT_ROW, LAYOUT_COLT = 1, 2
 SCALE_TENSOR, SCALE_PER_ROW = 0, 1
-GROUPED_M, GROUPED_K = 0, 1
+GROUPED_M, GROUPED_K, GROUPED_M_BT = 0, 1, 2
 STATUS = {0: "FP8_OK", 1: "FP8_ERR_INVALID_ARG", 2: "FP8_ERR_UNSUPPORTED", 3: "FP8_ERR_ALIGNMENT",
           4: "FP8_ERR_CUDA", 5: "FP8_ERR_TIMEOUT"}
 
@@ -255,7 +255,7 @@ def scaled_gemm(A: torch.Tensor, fa: int, B: torch.Tensor, fb: int, sa: torch.Te
 def grouped_gemm(mode: int, A, fa, B, fb, group_offsets, M_total, N, K, sa, sb, ld_T=0, out=None, stream=None):
     G = group_offsets.numel() - 1
     if out is None:
-        shape = (M_total, N) if mode == GROUPED_M else (G, N, K)
+        shape = (G, N, K) if mode == GROUPED_K else (M_total, N)
         out = torch.empty(shape, dtype=torch.bfloat16, device=A.device)
     fp8_grouped_gemm(mode, A, fa, B, fb, group_offsets, G, M_total, N, K, sa, int(sa.numel() > 1), sb,
                      int(sb.numel() > 1), out, ld_T, stream)

@@ -67,6 +67,8 @@ struct GemmParams {
     const int32_t *offsets;
     int G;
     int64_t ld_T;  // K-grouped: padded width of A and B
+    int b_trans;   // M-grouped with B in the grouped colwise layout [N][G * kpad]
+    int64_t kpad;  // roundup(K, 32): column stride between experts when b_trans
     unsigned int *err;
 };
 
@@ -177,10 +179,18 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams &p, int64_t t, co
             const int64_t mt = (m_e + BM - 1) / BM;
             const int64_t mb = local % mt, nb = local / mt;  // rows fastest: the expert's weight tile stays in L2
             ti.a_y = (int32_t)(p.offsets[e] + mb * BM);
-            ti.b_y = (int32_t)((int64_t)e * p.N + nb * BN);
-            ti.k_x0 = 0;
             ti.nkb = p.num_k_blk;
-            ti.last_steps = BK / UMMA_K;
+            if (p.b_trans) {
+                // expert e's K columns start at e * kpad; only the MMA steps
+                // up to kpad are issued so the next expert's columns are unused
+                ti.b_y = (int32_t)(nb * BN);
+                ti.k_x0 = (int32_t)(e * p.kpad);
+                ti.last_steps = (int)((p.kpad - (int64_t)(ti.nkb - 1) * BK) / UMMA_K);
+            } else {
+                ti.b_y = (int32_t)((int64_t)e * p.N + nb * BN);
+                ti.k_x0 = 0;
+                ti.last_steps = BK / UMMA_K;
+            }
             ti.row0 = p.offsets[e] + mb * BM;
             ti.row_end = p.offsets[e + 1];
             ti.col0 = nb * BN;
@@ -528,7 +538,7 @@ extern "C" fp8_status_t fp8_grouped_gemm(int mode, const uint8_t *A, int fa, con
     if (!A || !B || !sa || !sb || !C_bf16 || !group_offsets) return FP8_ERR_INVALID_ARG;
     if (fa == FP8_E4M3FNUZ || fb == FP8_E4M3FNUZ) return FP8_ERR_UNSUPPORTED;
     if (!gemm_format_ok(fa) || !gemm_format_ok(fb)) return FP8_ERR_INVALID_ARG;
-    if (mode != FP8_GROUPED_M && mode != FP8_GROUPED_K) return FP8_ERR_INVALID_ARG;
+    if (mode != FP8_GROUPED_M && mode != FP8_GROUPED_K && mode != FP8_GROUPED_M_BT) return FP8_ERR_INVALID_ARG;
     if (G < 1 || G > MAX_GROUPS || M_total < 0 || N < 1 || K < 1) return FP8_ERR_INVALID_ARG;
     if ((sa_mode != FP8_SCALE_TENSOR && sa_mode != FP8_SCALE_PER_ROW) ||
         (sb_mode != FP8_SCALE_TENSOR && sb_mode != FP8_SCALE_PER_ROW))
@@ -554,15 +564,24 @@ extern "C" fp8_status_t fp8_grouped_gemm(int mode, const uint8_t *A, int fa, con
     CUtensorMap ma, mb;
     const int64_t grid = num_sms();
 
-    if (mode == FP8_GROUPED_M) {
+    if (mode == FP8_GROUPED_M || mode == FP8_GROUPED_M_BT) {
         if (K % 16 != 0) return FP8_ERR_ALIGNMENT;
         p.ldc = N;
         p.c_vec16 = N % 8 == 0 && aligned(C_bf16, 16);
         p.num_m_blk = 0;
         p.num_n_blk = (int)((N + BN - 1) / BN);
         p.num_k_blk = (int)((K + BK - 1) / BK);
+        p.kpad = (K + 31) / 32 * 32;
+        if (mode == FP8_GROUPED_M_BT) {
+            if (ld_T % 16 != 0) return FP8_ERR_ALIGNMENT;
+            if (ld_T < (int64_t)G * p.kpad || ld_T > INT32_MAX) return FP8_ERR_INVALID_ARG;
+            p.b_trans = 1;
+        }
         if (M_total == 0) return FP8_OK;
-        if (!make_map(&ma, A, M_total, K, K, BM) || !make_map(&mb, B, (int64_t)G * N, K, K, BN)) return FP8_ERR_CUDA;
+        if (!make_map(&ma, A, M_total, K, K, BM)) return FP8_ERR_CUDA;
+        if (p.b_trans ? !make_map(&mb, B, N, (int64_t)G * p.kpad, ld_T, BN)
+                      : !make_map(&mb, B, (int64_t)G * N, K, K, BN))
+            return FP8_ERR_CUDA;
         return launch_gemm<MODE_MGROUP>(ma, mb, p, fa, fb, grid, st);
     }
     // K-grouped (wgrad): C[e] = A_e [N][m_e] . B_e [K][m_e]^T

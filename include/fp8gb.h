@@ -97,7 +97,7 @@ typedef enum {
 
 enum { FP8_LAYOUT_ROW = 1, FP8_LAYOUT_COLT = 2 };      /* bitmask of layouts to emit */
 enum { FP8_SCALE_TENSOR = 0, FP8_SCALE_PER_ROW = 1 };  /* GEMM operand scale granularity */
-enum { FP8_GROUPED_M = 0, FP8_GROUPED_K = 1 };         /* grouped GEMM modes */
+enum { FP8_GROUPED_M = 0, FP8_GROUPED_K = 1, FP8_GROUPED_M_BT = 2 };  /* grouped GEMM modes */
 
 /*
  * fp8_quantize -- fused amax + scale + saturating round-to-nearest-even cast
@@ -196,6 +196,13 @@ FP8GB_API fp8_status_t fp8_scaled_gemm(const uint8_t *A, int fa, int64_t lda, co
  * FP8_GROUPED_M (fprop, dgrad): A u8 [M_total][K] (group rows stacked), B u8
  *   [G][N][K]; C[m][n] = sum_k A[m][k] B[e][n][k] sa(m) sb(e, n) for m in
  *   group e; C bf16 [M_total][N].  sa: [1] or [M_total]; sb: [1] or [G][N].
+ * FP8_GROUPED_M_BT (dgrad with the weights' colwise-transposed layout): as
+ *   FP8_GROUPED_M, but B u8 [N][ld_T] is the grouped colwise layout that
+ *   fp8_quantize emits for a weight tensor [G*K][N] quantized with G equal
+ *   groups of K rows: expert e's [N][K] matrix starts at column e * kpad,
+ *   kpad = roundup(K, 32) (its padding columns are zero).  Requires
+ *   ld_T >= G * kpad, ld_T % 16 == 0.  sb: [1] or [G][N] (that call's
+ *   per-group column scales).
  * FP8_GROUPED_K (wgrad): A u8 [N][ld_T], B u8 [K][ld_T] in the padded
  *   grouped colwise layout of fp8_quantize (ld_T = that call's ld_colT);
  *   C[e][n][k] = sum_{r < m_e} A[n][poff_e + r] B[k][poff_e + r] sa(e, n)

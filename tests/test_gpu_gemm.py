@@ -226,3 +226,28 @@ def test_grouped_m_moe_shape_sampled(orc):
                                       sb.numpy()[e * N:(e + 1) * N], None, pm - r0, pn)
         out = C[torch.from_numpy(pm).to(DEV), torch.from_numpy(pn).to(DEV)].float().cpu().numpy()
         check_gemm(out, ref, bound, f"expert {e}")
+
+
+@pytest.mark.parametrize("sizes,K", [([5, 0, 33, 1, 0, 140, 128, 300], 272), ([64, 0, 200], 80), ([1], 48)])
+def test_grouped_m_bt_small(orc, sizes, K):
+    """M-grouped with B in the grouped colwise layout of a weight tensor (dgrad)."""
+    off = offsets_of(sizes)
+    G, Mt, N = len(sizes), int(off[-1]), 264
+    kpad = (K + 31) // 32 * 32
+    ldT = (G * kpad + 15) // 16 * 16 + 16          # a little wider than needed
+    g = torch.Generator().manual_seed(sum(sizes) + K)
+    A = finite_codes(g, (Mt, K), 1)
+    Bexp = finite_codes(g, (G, N, K), 0)            # expert e: [N][K]
+    BT = torch.full((N, ldT), 0x7F, dtype=torch.uint8)   # NaN bytes where no expert data lives
+    for e in range(G):
+        BT[:, e * kpad:e * kpad + K] = Bexp[e]
+        BT[:, e * kpad + K:(e + 1) * kpad] = 0          # zero padding, as fp8_quantize writes it
+    sa = scales(g, Mt, True)
+    sb = scales(g, G * N, True)
+    C = fp8.grouped_gemm(fp8.GROUPED_M_BT, A.to(DEV), 1, BT.to(DEV), 0, torch.from_numpy(off).to(DEV), Mt, N, K,
+                         sa.to(DEV), sb.to(DEV), ld_T=ldT)
+    assert fp8.fp8_sync_status() == 0
+    pm, pn = np.meshgrid(np.arange(Mt), np.arange(N), indexing="ij")
+    ref, bound = orc.grouped_gemm(0, A.numpy(), 1, Bexp.numpy(), 0, off, N, K, sa.numpy(), sb.numpy(), None,
+                                  pm.ravel(), pn.ravel())
+    check_gemm(C.float().cpu().numpy().ravel(), ref, bound, f"grouped M^T {sizes}")
