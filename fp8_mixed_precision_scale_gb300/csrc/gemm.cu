@@ -73,7 +73,8 @@ struct GemmParams {
 };
 
 struct TileInfo {
-    int32_t a_y, b_y, k_x0;
+    int32_t a_y, b_y;
+    int32_t a_x0, b_x0;  // first K column (bytes) of the A and B tiles
     int nkb, last_steps;
     int64_t row0, row_end, col0, col_end;
     int64_t c_base;
@@ -152,7 +153,7 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams &p, int64_t t, co
         }
         ti.a_y = mb * BM;
         ti.b_y = nb * BN;
-        ti.k_x0 = 0;
+        ti.a_x0 = ti.b_x0 = 0;
         ti.nkb = p.num_k_blk;
         ti.last_steps = BK / UMMA_K;
         ti.row0 = (int64_t)mb * BM;
@@ -184,11 +185,12 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams &p, int64_t t, co
                 // expert e's K columns start at e * kpad; only the MMA steps
                 // up to kpad are issued so the next expert's columns are unused
                 ti.b_y = (int32_t)(nb * BN);
-                ti.k_x0 = (int32_t)(e * p.kpad);
+                ti.a_x0 = 0;
+                ti.b_x0 = (int32_t)(e * p.kpad);
                 ti.last_steps = (int)((p.kpad - (int64_t)(ti.nkb - 1) * BK) / UMMA_K);
             } else {
                 ti.b_y = (int32_t)((int64_t)e * p.N + nb * BN);
-                ti.k_x0 = 0;
+                ti.a_x0 = ti.b_x0 = 0;
                 ti.last_steps = BK / UMMA_K;
             }
             ti.row0 = p.offsets[e] + mb * BM;
@@ -204,7 +206,7 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams &p, int64_t t, co
             const int64_t pad = (m_e + 31) / 32 * 32;
             ti.a_y = (int32_t)(mb * BM);
             ti.b_y = (int32_t)(nb * BN);
-            ti.k_x0 = poff[e];
+            ti.a_x0 = ti.b_x0 = poff[e];
             ti.nkb = (int)((pad + BK - 1) / BK);
             ti.last_steps = ti.nkb > 0 ? (int)((pad - (int64_t)(ti.nkb - 1) * BK) / UMMA_K) : 0;
             ti.row0 = mb * BM;
@@ -294,9 +296,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     break;
                 }
                 mbar_arrive_expect_tx(&full[stage], A_STAGE_BYTES + B_STAGE_BYTES);
-                const int32_t kx = ti.k_x0 + kb * BK;
-                tma_load_2d(sA + stage * A_STAGE_BYTES, &tmA, kx, ti.a_y, &full[stage]);
-                tma_load_2d(sB + stage * B_STAGE_BYTES, &tmB, kx, ti.b_y, &full[stage]);
+                tma_load_2d(sA + stage * A_STAGE_BYTES, &tmA, ti.a_x0 + kb * BK, ti.a_y, &full[stage]);
+                tma_load_2d(sB + stage * B_STAGE_BYTES, &tmB, ti.b_x0 + kb * BK, ti.b_y, &full[stage]);
                 issued_parity[stage] = (int)phase;
                 if (++stage == STAGES) {
                     stage = 0;

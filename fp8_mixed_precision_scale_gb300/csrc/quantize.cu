@@ -9,8 +9,9 @@
 // non-coalesced writes were the bottleneck; the five-kernel chain fused into
 // one; relaxed atomics).
 //
-// Design (GB300): persistent thread blocks of 256 threads walk tiles of
-// RB rows x 128 columns.  Each thread issues all of its 16-byte loads for a
+// Design (GB300): thread blocks of 256 threads work on tiles of RB rows x 128
+// columns (RB = 64 for plain tensors, one tile per block; RB = 32 for
+// expert-grouped tensors, persistent blocks).  Each thread issues all of its 16-byte loads for a
 // tile before touching the data, converts 8 elements at a time with
 // cvt.rn.satfinite.{e4m3,e5m2}x2, stores the row layout directly (8-byte
 // coalesced stores) and stages the bytes in shared memory; the transposed
@@ -437,9 +438,15 @@ __global__ void finalize_rowwise_kernel(float *sinv_row, int64_t n_row, float *s
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
+// Grid size.  Ungrouped tensors get one thread block per tile, so the
+// hardware block scheduler balances the tail at tile granularity (measured
+// faster on GB300 than a persistent grid of a few blocks per SM, which leaves
+// a partial last round).  Grouped tensors keep a persistent grid because
+// every block first builds the padded-offset table of all groups.
 template <typename K>
-static int blocks_for(K kernel, size_t dyn_smem, int64_t n_tiles)
+static int blocks_for(K kernel, size_t dyn_smem, int64_t n_tiles, bool persistent)
 {
+    if (!persistent) return (int)(n_tiles < 1 ? 1 : (n_tiles < INT32_MAX ? n_tiles : INT32_MAX));
     int per_sm = 0;
     if (dyn_smem > 48 * 1024) cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn_smem);
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, QT_THREADS, dyn_smem);
@@ -457,13 +464,13 @@ static fp8_status_t launch_cast(const QArgs &a, int layouts, size_t group_smem, 
     const size_t smem = (size_t)RB * QT_PITCH + group_smem;
     if (layouts == (FP8_LAYOUT_ROW | FP8_LAYOUT_COLT)) {
         auto k = cast_kernel<FMT, RB, SMODE, DELAYED, true, true>;
-        k<<<blocks_for(k, smem, n_tiles), QT_THREADS, smem, st>>>(a);
+        k<<<blocks_for(k, smem, n_tiles, a.offsets != nullptr), QT_THREADS, smem, st>>>(a);
     } else if (layouts == FP8_LAYOUT_ROW) {
         auto k = cast_kernel<FMT, RB, SMODE, DELAYED, true, false>;
-        k<<<blocks_for(k, smem, n_tiles), QT_THREADS, smem, st>>>(a);
+        k<<<blocks_for(k, smem, n_tiles, a.offsets != nullptr), QT_THREADS, smem, st>>>(a);
     } else {
         auto k = cast_kernel<FMT, RB, SMODE, DELAYED, false, true>;
-        k<<<blocks_for(k, smem, n_tiles), QT_THREADS, smem, st>>>(a);
+        k<<<blocks_for(k, smem, n_tiles, a.offsets != nullptr), QT_THREADS, smem, st>>>(a);
     }
     return check_launch();
 }
@@ -480,7 +487,7 @@ static fp8_status_t run_quantize(QArgs a, int kind, int layouts, cudaStream_t st
     if (kind == FP8_RECIPE_TENSORWISE) {
         if (cudaMemsetAsync(a.amax_out, 0, sizeof(float), st) != cudaSuccess) return cuda_fail();
         auto k = amax_kernel<RB, 0>;
-        k<<<blocks_for(k, group_smem, n_tiles), QT_THREADS, group_smem, st>>>(a);
+        k<<<blocks_for(k, group_smem, n_tiles, a.offsets != nullptr), QT_THREADS, group_smem, st>>>(a);
         if ((s = check_launch()) != FP8_OK) return s;
         return launch_cast<FMT, RB, 0, false>(a, layouts, group_smem, st);
     }
@@ -494,7 +501,7 @@ static fp8_status_t run_quantize(QArgs a, int kind, int layouts, cudaStream_t st
     if (a.amax_out && cudaMemsetAsync(a.amax_out, 0, sizeof(float), st) != cudaSuccess) return cuda_fail();
     {
         auto k = amax_kernel<RB, 1>;
-        k<<<blocks_for(k, group_smem, n_tiles), QT_THREADS, group_smem, st>>>(a);
+        k<<<blocks_for(k, group_smem, n_tiles, a.offsets != nullptr), QT_THREADS, group_smem, st>>>(a);
         if ((s = check_launch()) != FP8_OK) return s;
     }
     if ((s = launch_cast<FMT, RB, 1, false>(a, layouts, group_smem, st)) != FP8_OK) return s;
@@ -571,7 +578,7 @@ extern "C" fp8_status_t fp8_quantize(const void *x_bf16, int64_t rows, int64_t c
         return fmt == FP8_E5M2 ? run_quantize<FP8_E5M2, 32>(a, recipe->kind, layouts, st)
                                : run_quantize<FP8_E4M3FN, 32>(a, recipe->kind, layouts, st);
     }
-    a.n_row_blocks = (rows + 127) / 128;
-    return fmt == FP8_E5M2 ? run_quantize<FP8_E5M2, 128>(a, recipe->kind, layouts, st)
-                           : run_quantize<FP8_E4M3FN, 128>(a, recipe->kind, layouts, st);
+    a.n_row_blocks = (rows + 63) / 64;
+    return fmt == FP8_E5M2 ? run_quantize<FP8_E5M2, 64>(a, recipe->kind, layouts, st)
+                           : run_quantize<FP8_E4M3FN, 64>(a, recipe->kind, layouts, st);
 }
