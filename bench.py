@@ -1,14 +1,27 @@
 """Benchmark of the FP8 linear hot path on one GB300 (or N, one process each).
 
-One step = the whole FP8 path of the Llama-3-8B MLP block (tokens 8192,
-hidden 4096, ffn 14336) under delayed scaling with the hybrid format:
+Default workload (`--workload llama_mlp`): one step = the whole FP8 path of
+the Llama-3-8B MLP block (tokens 8192, hidden 4096, ffn 14336) under delayed
+scaling with the hybrid format:
   8 fused quantizes (X, W_gate, W_up, W_down, H, dY_down, dY_gate, dY_up;
     E4M3 forward / E5M2 gradients; rowwise + colwise-transposed layouts),
   9 FP8 GEMMs (fprop, dgrad, wgrad of gate, up and down; 962 GFLOP each),
   1 fused amax-history update (8 histories of length 1024, most_recent).
 Under torchrun each rank runs its own batch (data parallel, weak scaling);
-the one exchange of the path -- a MAX all-reduce of the 8 current amaxes
-before the update -- goes over NCCL.
+the one exchange of the path -- a MAX all-reduce of the current amaxes before
+the update -- goes over NCCL.
+
+Other workloads (same JSON line, their own config):
+  llama_rowwise  Llama-3-8B attention projections + MLP, rowwise recipe,
+                 Student-t activations (15 GEMMs, 11.13 TFLOP per step)
+  moe            DeepSeek-V3-shaped MoE layer: 32768 routed rows, 256 experts,
+                 hidden 7168, ffn 2048; rowwise tokens with per-expert colwise
+                 scales, rowwise / per-expert colwise weights, 9 grouped GEMMs
+  flux           Flux-12B linears (tokens 9216, hidden 3072, MLP 12288, QKV
+                 9216), delayed scaling, all E4M3, amax algo max
+  sweep          the delayed quantize (E4M3, both layouts) of 2^20 .. 2^30
+                 elements, GB/s against size
+  gemm, quantize single kernels of the default step, for profiling
 
 Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle on a
 bounded sample of the same workload instead.
@@ -30,15 +43,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "FP8 linear fwd+bwd TFLOPS & quantize GB/s per GB300, as % of roofline"
-T_, H_, F_ = 8192, 4096, 14336
 L_HIST = 1024
-GEMM_FLOP = 2.0 * T_ * H_ * F_            # every GEMM of the block has the same M*N*K
-N_GEMM = 9
-QUANT_ELEMS = {"x": T_ * H_, "w_gate": F_ * H_, "w_up": F_ * H_, "w_down": H_ * F_, "h": T_ * F_,
-               "dy_down": T_ * H_, "dy_gate": T_ * F_, "dy_up": T_ * F_}
 QUANT_BYTES_PER_ELEM = 4                  # 2 B read + 1 B per layout, two layouts
-WORKLOAD = ("llama3-8b-mlp fwd+bwd, delayed scaling: tokens 8192, hidden 4096, ffn 14336, "
-            "hybrid e4m3 fwd / e5m2 grads, amax history 1024 most_recent, margin 0")
 
 # DRAM bytes (read + write) of one dense GEMM launch, the gate projection
 # 8192x14336x4096, from one ncu capture (profiles/fp8_gemm_kernel_llama_gate_8192x14336x4096.md).
@@ -125,36 +131,53 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------------------------
-# the GPU arm
+# workloads
 # --------------------------------------------------------------------------------------------
 
-class MlpStep:
-    """Buffers and the launch sequence of one FP8 fwd+bwd step of the MLP block."""
+def _timed(ev, kind, fn, work=None):
+    """Run fn; with ev, bracket it with CUDA events on the current stream and
+    record (start, end, work) under `kind`."""
+    if ev is None:
+        fn()
+        return
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    fn()
+    b.record()
+    ev.setdefault(kind, []).append((a, b, work))
 
-    SHAPES = {"x": ((T_, H_), 1.0), "w_gate": ((F_, H_), 0.02), "w_up": ((F_, H_), 0.02),
-              "w_down": ((H_, F_), 0.02), "h": ((T_, F_), 1.0), "dy_down": ((T_, H_), 1e-4),
-              "dy_gate": ((T_, F_), 1e-4), "dy_up": ((T_, F_), 1e-4)}
-    OUTS = {"gate": (T_, F_), "up": (T_, F_), "y": (T_, H_), "dh": (T_, F_), "dx_gate": (T_, H_),
-            "dx_up": (T_, H_), "dw_down": (H_, F_), "dw_gate": (F_, H_), "dw_up": (F_, H_)}
 
-    def __init__(self, dev, seed: int, keys=None, outs=None):
-        """keys / outs restrict the tensors allocated (single-kernel workloads)."""
+def _normal(g, dev, shape, std):
+    return (torch.randn(shape, generator=g, device=dev) * std).to(torch.bfloat16)
+
+
+def quantize_bytes(shape, layouts=3):
+    """Algorithmic bytes of one quantize: 2 B read + 1 B per emitted layout per element."""
+    r, c = shape
+    return r * c * (2 + (1 if layouts & 1 else 0) + (1 if layouts & 2 else 0))
+
+
+class DelayedStep:
+    """A block of Linears under delayed scaling: quantize (stored scale,
+    amax into the history slot), GEMMs with per-tensor scales, one update."""
+
+    def __init__(self, dev, seed, shapes, fmts, gemms, fwd_q, bwd_q, n_fwd_gemm, algo, tokens, name, desc,
+                 keys=None, outs=None):
         import fp8_mixed_precision_scale_gb300 as fp8
         self.fp8 = fp8
+        self.name, self.desc, self.tokens, self.algo = name, desc, tokens, algo
         g = torch.Generator(device=dev)
         g.manual_seed(seed)
-
-        def normal(shape, std):
-            return (torch.randn(shape, generator=g, device=dev) * std).to(torch.bfloat16)
-
-        self.order = list(self.SHAPES.keys())
-        self.inp = {k: normal(*self.SHAPES[k]) for k in self.order if keys is None or k in keys}
-        self.fmt = {k: (fp8.E5M2 if k.startswith("dy") else fp8.E4M3FN) for k in self.order}
+        self.order = list(shapes)
+        self.inp = {k: _normal(g, dev, *shapes[k]) for k in self.order if keys is None or k in keys}
+        self.fmt = fmts
+        self.gemms, self.fwd_q, self.bwd_q, self.n_fwd_gemm = gemms, fwd_q, bwd_q, n_fwd_gemm
         n = len(self.order)
         self.hist = torch.zeros((n, L_HIST), dtype=torch.float32, device=dev)
         self.scale = torch.ones(n, dtype=torch.float32, device=dev)
         self.scale_inv = torch.ones(n, dtype=torch.float32, device=dev)
-        self.fmt_dev = torch.tensor([self.fmt[k] for k in self.order], dtype=torch.uint8, device=dev)
+        self.fmt_dev = torch.tensor([fmts[k] for k in self.order], dtype=torch.uint8, device=dev)
         self.q = {}
         for k, t in self.inp.items():
             r, c = t.shape
@@ -162,13 +185,22 @@ class MlpStep:
                              colT=torch.empty((c, r), dtype=torch.uint8, device=dev),
                              srow=torch.empty(1, dtype=torch.float32, device=dev),
                              scol=torch.empty(1, dtype=torch.float32, device=dev))
-        self.out = {k: torch.empty(shape, dtype=torch.bfloat16, device=dev) for k, shape in self.OUTS.items()
-                    if outs is None or k in outs}
-        self.recipe = fp8.Recipe(kind=fp8.DELAYED, margin=0, history_len=L_HIST, algo=fp8.MOST_RECENT)
-        # launches per step: 8 quantize (1 kernel each, delayed) + 9 GEMMs + 1 update
-        self.launches_per_step = 8 + 9 + 1
+        self.out, self.gemm_work = {}, {}
+        self.flops = 0.0
+        for (a, al, b, bl, o) in gemms:
+            M, K = shapes[a][0] if al == "row" else shapes[a][0][::-1]
+            N = shapes[b][0][0] if bl == "row" else shapes[b][0][1]
+            self.gemm_work[o] = (2.0 * M * N * K, M * K + N * K + 2.0 * M * N)
+            self.flops += 2.0 * M * N * K
+            if outs is None or o in outs:
+                self.out[o] = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        self.recipe = fp8.Recipe(kind=fp8.DELAYED, margin=0, history_len=L_HIST, algo=algo)
+        self.q_bytes = sum(quantize_bytes(shapes[k][0]) for k in self.order)
+        self.launches_per_step = len(self.order) + len(gemms) + 1
+        self.d2h = [self.out[gemms[self.n_fwd_gemm - 1][4]]] if outs is None else []
 
-    def quantize(self, k, i):
+    def quantize(self, k):
+        i = self.order.index(k)
         t, q = self.inp[k], self.q[k]
         r, c = t.shape
         self.fp8.fp8_quantize(t, r, c, c, self.fmt[k], self.recipe, 3, self.scale[i:i + 1],
@@ -185,52 +217,277 @@ class MlpStep:
         N = B.shape[0]
         self.fp8.fp8_scaled_gemm(A, self.fmt[a], K, B, self.fmt[b], K, M, N, K, sa, 0, sb, 0, C, N)
 
-    GEMMS = [  # (A, A layout, B, B layout, output)
-        ("x", "row", "w_gate", "row", "gate"),          # fprop gate
-        ("x", "row", "w_up", "row", "up"),              # fprop up
-        ("h", "row", "w_down", "row", "y"),             # fprop down
-        ("dy_down", "row", "w_down", "colT", "dh"),     # dgrad down
-        ("dy_gate", "row", "w_gate", "colT", "dx_gate"),  # dgrad gate
-        ("dy_up", "row", "w_up", "colT", "dx_up"),      # dgrad up
-        ("dy_down", "colT", "h", "colT", "dw_down"),    # wgrad down
-        ("dy_gate", "colT", "x", "colT", "dw_gate"),    # wgrad gate
-        ("dy_up", "colT", "x", "colT", "dw_up"),        # wgrad up
-    ]
-
     def run(self, ev=None, world=1):
-        """One step.  ev: optional dict of event lists to time the quantize and GEMM launches."""
-        idx = {k: i for i, k in enumerate(self.order)}
-        fwd_q = ["x", "w_gate", "w_up", "w_down", "h"]
-        bwd_q = ["dy_down", "dy_gate", "dy_up"]
-        for k in fwd_q:
-            self._timed(ev, "q", lambda k=k: self.quantize(k, idx[k]))
-        for g in self.GEMMS[:3]:
-            self._timed(ev, "g", lambda g=g: self.gemm(*g))
-        for k in bwd_q:
-            self._timed(ev, "q", lambda k=k: self.quantize(k, idx[k]))
-        for g in self.GEMMS[3:]:
-            self._timed(ev, "g", lambda g=g: self.gemm(*g))
+        for k in self.fwd_q:
+            _timed(ev, "q", lambda k=k: self.quantize(k), quantize_bytes(self.inp[k].shape))
+        for g in self.gemms[:self.n_fwd_gemm]:
+            _timed(ev, "g", lambda g=g: self.gemm(*g), self.gemm_work[g[4]])
+        for k in self.bwd_q:
+            _timed(ev, "q", lambda k=k: self.quantize(k), quantize_bytes(self.inp[k].shape))
+        for g in self.gemms[self.n_fwd_gemm:]:
+            _timed(ev, "g", lambda g=g: self.gemm(*g), self.gemm_work[g[4]])
         if world > 1:
             from fp8_mixed_precision_scale_gb300 import dp
             dp.reduce_current_amax(self.hist)
-        self._timed(ev, "u", lambda: self.fp8.fp8_update_amax_history(
-            self.hist, self.scale, self.scale_inv, self.fmt_dev, len(self.order), L_HIST, self.fp8.MOST_RECENT, 0))
+        _timed(ev, "u", lambda: self.fp8.fp8_update_amax_history(
+            self.hist, self.scale, self.scale_inv, self.fmt_dev, len(self.order), L_HIST, self.algo, 0),
+            len(self.order) * (8.0 * L_HIST + 8))
 
-    @staticmethod
-    def _timed(ev, kind, fn):
-        if ev is None:
-            fn()
-            return
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record()
-        fn()
-        b.record()
-        ev[kind].append((a, b))
+
+T_, H_, F_ = 8192, 4096, 14336
+LLAMA_MLP_SHAPES = {"x": ((T_, H_), 1.0), "w_gate": ((F_, H_), 0.02), "w_up": ((F_, H_), 0.02),
+                    "w_down": ((H_, F_), 0.02), "h": ((T_, F_), 1.0), "dy_down": ((T_, H_), 1e-4),
+                    "dy_gate": ((T_, F_), 1e-4), "dy_up": ((T_, F_), 1e-4)}
+MLP_GEMMS = [  # (A, A layout, B, B layout, output)
+    ("x", "row", "w_gate", "row", "gate"),             # fprop gate
+    ("x", "row", "w_up", "row", "up"),                 # fprop up
+    ("h", "row", "w_down", "row", "y"),                # fprop down
+    ("dy_down", "row", "w_down", "colT", "dh"),        # dgrad down
+    ("dy_gate", "row", "w_gate", "colT", "dx_gate"),   # dgrad gate
+    ("dy_up", "row", "w_up", "colT", "dx_up"),         # dgrad up
+    ("dy_down", "colT", "h", "colT", "dw_down"),       # wgrad down
+    ("dy_gate", "colT", "x", "colT", "dw_gate"),       # wgrad gate
+    ("dy_up", "colT", "x", "colT", "dw_up"),           # wgrad up
+]
+LLAMA_MLP_DESC = ("llama3-8b-mlp fwd+bwd, delayed scaling: tokens 8192, hidden 4096, ffn 14336, "
+                  "hybrid e4m3 fwd / e5m2 grads, amax history 1024 most_recent, margin 0")
+
+
+def llama_mlp_step(dev, seed, keys=None, outs=None):
+    import fp8_mixed_precision_scale_gb300 as fp8
+    fmts = {k: (fp8.E5M2 if k.startswith("dy") else fp8.E4M3FN) for k in LLAMA_MLP_SHAPES}
+    return DelayedStep(dev, seed, LLAMA_MLP_SHAPES, fmts, MLP_GEMMS, ["x", "w_gate", "w_up", "w_down", "h"],
+                       ["dy_down", "dy_gate", "dy_up"], 3, fp8.MOST_RECENT, T_, "llama_mlp", LLAMA_MLP_DESC,
+                       keys, outs)
+
+
+FT, FH, FF, FQ = 9216, 3072, 12288, 9216
+FLUX_SHAPES = {"x": ((FT, FH), 1.0), "w_qkv": ((FQ, FH), 0.02), "w_up": ((FF, FH), 0.02),
+               "w_down": ((FH, FF), 0.02), "h": ((FT, FF), 1.0), "dy_qkv": ((FT, FQ), 1e-4),
+               "dy_up": ((FT, FF), 1e-4), "dy_down": ((FT, FH), 1e-4)}
+FLUX_GEMMS = [("x", "row", "w_qkv", "row", "qkv"), ("x", "row", "w_up", "row", "up"),
+              ("h", "row", "w_down", "row", "y"), ("dy_qkv", "row", "w_qkv", "colT", "dx_qkv"),
+              ("dy_up", "row", "w_up", "colT", "dx_up"), ("dy_down", "row", "w_down", "colT", "dh"),
+              ("dy_qkv", "colT", "x", "colT", "dw_qkv"), ("dy_up", "colT", "x", "colT", "dw_up"),
+              ("dy_down", "colT", "h", "colT", "dw_down")]
+
+
+def flux_step(dev, seed):
+    import fp8_mixed_precision_scale_gb300 as fp8
+    fmts = {k: fp8.E4M3FN for k in FLUX_SHAPES}
+    desc = ("flux-12b linears fwd+bwd (QKV 3072->9216, MLP 3072->12288->3072), tokens 2 x (4096 + 512) = 9216, "
+            "delayed scaling, all e4m3, amax history 1024, algo max, margin 0")
+    return DelayedStep(dev, seed, FLUX_SHAPES, fmts, FLUX_GEMMS, ["x", "w_qkv", "w_up", "w_down", "h"],
+                       ["dy_qkv", "dy_up", "dy_down"], 3, fp8.MAX, FT, "flux", desc)
+
+
+class RowwiseStep:
+    """Llama-3-8B attention projections + MLP with the rowwise recipe: every
+    tensor quantized with per-row scales (row layout) and per-column scales
+    (transposed layout); GEMMs with per-row / per-column scales."""
+
+    SHAPES = {  # name: (shape, distribution, fmt)
+        "x": ((T_, H_), "t", 0), "w_qkv": ((6144, H_), 0.02, 0), "o_in": ((T_, 6144), "t", 0),
+        "w_o": ((H_, 6144), 0.02, 0), "x2": ((T_, H_), "t", 0), "w_gate": ((F_, H_), 0.02, 0),
+        "w_up": ((F_, H_), 0.02, 0), "w_down": ((H_, F_), 0.02, 0), "h": ((T_, F_), "t", 0),
+        "dy_qkv": ((T_, 6144), 1e-4, 1), "dy_o": ((T_, H_), 1e-4, 1), "dy_gate": ((T_, F_), 1e-4, 1),
+        "dy_up": ((T_, F_), 1e-4, 1), "dy_down": ((T_, H_), 1e-4, 1)}
+    GEMMS = [("x", "row", "w_qkv", "row", "qkv"), ("o_in", "row", "w_o", "row", "o"),
+             ("x2", "row", "w_gate", "row", "gate"), ("x2", "row", "w_up", "row", "up"),
+             ("h", "row", "w_down", "row", "y"),
+             ("dy_down", "row", "w_down", "colT", "dh"), ("dy_gate", "row", "w_gate", "colT", "dx_gate"),
+             ("dy_up", "row", "w_up", "colT", "dx_up"), ("dy_o", "row", "w_o", "colT", "do_in"),
+             ("dy_qkv", "row", "w_qkv", "colT", "dx"),
+             ("dy_down", "colT", "h", "colT", "dw_down"), ("dy_gate", "colT", "x2", "colT", "dw_gate"),
+             ("dy_up", "colT", "x2", "colT", "dw_up"), ("dy_o", "colT", "o_in", "colT", "dw_o"),
+             ("dy_qkv", "colT", "x", "colT", "dw_qkv")]
+    FWD_Q = ["x", "w_qkv", "o_in", "w_o", "x2", "w_gate", "w_up", "w_down", "h"]
+    BWD_Q = ["dy_down", "dy_gate", "dy_up", "dy_o", "dy_qkv"]
+
+    def __init__(self, dev, seed):
+        import fp8_mixed_precision_scale_gb300 as fp8
+        import synth
+        self.fp8 = fp8
+        self.name = "llama_rowwise"
+        self.desc = ("llama3-8b attention projections (QKV 4096->6144, O 6144->4096) + MLP (4096->14336->4096) "
+                     "fwd+bwd, rowwise recipe: per-row scales for the row layout, per-column scales for the "
+                     "transposed layout; tokens 8192; Student-t (nu=4) activations; hybrid e4m3 / e5m2")
+        self.tokens = T_
+        g = torch.Generator(device=dev)
+        g.manual_seed(seed)
+        self.inp, self.fmt = {}, {}
+        for k, (shape, dist, f) in self.SHAPES.items():
+            self.inp[k] = synth.student_t(shape, 4, g, dev) if dist == "t" else _normal(g, dev, shape, dist)
+            self.fmt[k] = f
+        self.q = {}
+        for k, t in self.inp.items():
+            r, c = t.shape
+            self.q[k] = dict(row=torch.empty((r, c), dtype=torch.uint8, device=dev),
+                             colT=torch.empty((c, r), dtype=torch.uint8, device=dev),
+                             srow=torch.empty(r, dtype=torch.float32, device=dev),
+                             scol=torch.empty(c, dtype=torch.float32, device=dev))
+        self.out, self.gemm_work = {}, {}
+        self.flops = 0.0
+        for (a, al, b, bl, o) in self.GEMMS:
+            M, K = self.inp[a].shape if al == "row" else self.inp[a].shape[::-1]
+            N = self.inp[b].shape[0] if bl == "row" else self.inp[b].shape[1]
+            self.out[o] = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            self.gemm_work[o] = (2.0 * M * N * K, M * K + N * K + 2.0 * M * N)
+            self.flops += 2.0 * M * N * K
+        self.recipe = fp8.Recipe(kind=fp8.ROWWISE)
+        self.q_bytes = sum(quantize_bytes(t.shape) for t in self.inp.values())
+        self.launches_per_step = 3 * len(self.inp) + len(self.GEMMS)   # amax, cast, finalise per tensor
+        self.d2h = [self.out["y"]]
+
+    def quantize(self, k):
+        t, q = self.inp[k], self.q[k]
+        r, c = t.shape
+        self.fp8.fp8_quantize(t, r, c, c, self.fmt[k], self.recipe, 3, None, None, q["row"], q["srow"],
+                              q["colT"], r, q["scol"])
+
+    def gemm(self, a, al, b, bl, out):
+        qa, qb = self.q[a], self.q[b]
+        A = qa["row"] if al == "row" else qa["colT"]
+        B = qb["row"] if bl == "row" else qb["colT"]
+        sa = qa["srow"] if al == "row" else qa["scol"]
+        sb = qb["srow"] if bl == "row" else qb["scol"]
+        M, K = A.shape
+        N = B.shape[0]
+        self.fp8.fp8_scaled_gemm(A, self.fmt[a], K, B, self.fmt[b], K, M, N, K, sa, 1, sb, 1, self.out[out], N)
+
+    def run(self, ev=None, world=1):
+        for k in self.FWD_Q:
+            _timed(ev, "q", lambda k=k: self.quantize(k), quantize_bytes(self.inp[k].shape))
+        for g in self.GEMMS[:5]:
+            _timed(ev, "g", lambda g=g: self.gemm(*g), self.gemm_work[g[4]])
+        for k in self.BWD_Q:
+            _timed(ev, "q", lambda k=k: self.quantize(k), quantize_bytes(self.inp[k].shape))
+        for g in self.GEMMS[5:]:
+            _timed(ev, "g", lambda g=g: self.gemm(*g), self.gemm_work[g[4]])
+
+
+class MoeStep:
+    """DeepSeek-V3-shaped MoE layer fwd+bwd on one GPU: routed token rows
+    grouped by expert, rowwise scales per token plus per-expert column scales;
+    expert weights with per-row scales and per-expert column scales; the
+    nine grouped GEMMs (M-grouped fprop, M-grouped dgrad on the weights'
+    transposed layout, K-grouped wgrad)."""
+
+    def __init__(self, dev, seed):
+        import numpy as np
+
+        import fp8_mixed_precision_scale_gb300 as fp8
+        import synth
+        self.fp8 = fp8
+        E, H, F = synth.DSV3["E"], synth.DSV3["H"], synth.DSV3["F"]
+        self.E, self.H, self.F = E, H, F
+        sizes = synth.moe_group_sizes().numpy()
+        self.sizes = sizes
+        self.off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+        self.off_d = torch.from_numpy(self.off).to(dev)
+        self.M = M = int(self.off[-1])
+        self.tokens = synth.DSV3["tokens"]
+        self.name = "moe"
+        self.desc = ("deepseek-v3 moe layer fwd+bwd: 4096 tokens x top-8 = 32768 routed rows, hidden 7168, "
+                     "256 experts of ffn 2048 (gate/up/down), group sizes multinomial over zipf(1.1) with 8 empty "
+                     "experts; rowwise + per-expert colwise scales; 9 grouped GEMMs")
+        g = torch.Generator(device=dev)
+        g.manual_seed(seed)
+        self.tok = {"xp": _normal(g, dev, (M, H), 1.0), "hp": _normal(g, dev, (M, F), 1.0),
+                    "dy_down": _normal(g, dev, (M, H), 1e-4), "dy_gate": _normal(g, dev, (M, F), 1e-4),
+                    "dy_up": _normal(g, dev, (M, F), 1e-4)}
+        self.tfmt = {"xp": 0, "hp": 0, "dy_down": 1, "dy_gate": 1, "dy_up": 1}
+        self.w = {"w_gate": _normal(g, dev, (E * F, H), 0.02), "w_up": _normal(g, dev, (E * F, H), 0.02),
+                  "w_down": _normal(g, dev, (E * H, F), 0.02)}
+        self.inp = dict(self.tok, **self.w)
+        rows_per_expert = {"w_gate": F, "w_up": F, "w_down": H}
+        self.woff_d = {k: torch.from_numpy(np.arange(E + 1, dtype=np.int32) * r).to(dev)
+                       for k, r in rows_per_expert.items()}
+        self.recipe = fp8.Recipe(kind=fp8.ROWWISE)
+        ldT = fp8.fp8_group_padded_offsets(self.off)[0]
+        self.ldT_tok = max(16, (ldT + 15) // 16 * 16)
+        self.q = {}
+        for k, t in self.inp.items():
+            r, c = t.shape
+            ld = r if k in self.w else self.ldT_tok
+            self.q[k] = dict(row=torch.empty((r, c), dtype=torch.uint8, device=dev),
+                             colT=torch.empty((c, ld), dtype=torch.uint8, device=dev), ldT=ld,
+                             srow=torch.empty(r, dtype=torch.float32, device=dev),
+                             scol=torch.empty(E * c, dtype=torch.float32, device=dev))
+        e = lambda *s: torch.empty(s, dtype=torch.bfloat16, device=dev)  # noqa: E731
+        self.out = {"gate": e(M, F), "up": e(M, F), "y": e(M, H), "dh": e(M, F), "dx_gate": e(M, H),
+                    "dx_up": e(M, H), "dw_down": e(E, H, F), "dw_gate": e(E, F, H), "dw_up": e(E, F, H)}
+        nz = int((sizes > 0).sum())
+        fl = 2.0 * M * F * H
+        wbytes = nz * F * H
+        self.gemm_work = {  # (flops, algorithmic bytes: A + non-empty experts' weights + C)
+            "fprop": (fl, M * H + wbytes + 2.0 * M * F), "fprop_down": (fl, M * F + wbytes + 2.0 * M * H),
+            "dgrad_down": (fl, M * H + wbytes + 2.0 * M * F), "dgrad": (fl, M * F + wbytes + 2.0 * M * H),
+            "wgrad": (fl, M * (F + H) + 2.0 * E * F * H)}
+        self.flops = 9 * fl
+        self.q_bytes = sum(quantize_bytes(t.shape) for t in self.inp.values())
+        self.launches_per_step = 3 * len(self.inp) + 9
+        self.d2h = [self.out["y"]]
+
+    def quantize(self, k):
+        t, q = self.inp[k], self.q[k]
+        r, c = t.shape
+        off_d = self.woff_d[k] if k in self.w else self.off_d
+        f = 0 if k in self.w else self.tfmt[k]
+        self.fp8.fp8_quantize(t, r, c, c, f, self.recipe, 3, None, None, q["row"], q["srow"], q["colT"],
+                              q["ldT"], q["scol"], off_d, self.E)
+
+    def run(self, ev=None, world=1):
+        fp8, q, o, E, H, F, M = self.fp8, self.q, self.out, self.E, self.H, self.F, self.M
+        GM, GK, GMT = fp8.GROUPED_M, fp8.GROUPED_K, fp8.GROUPED_M_BT
+        off = self.off_d
+
+        def gg(mode, a, al, fa, b, bl, fb, N, K, out, ldT=0):
+            A = q[a]["row"] if al == "row" else q[a]["colT"]
+            B = q[b]["row"] if bl == "row" else q[b]["colT"]
+            sa = q[a]["srow"] if al == "row" else q[a]["scol"]
+            sb = q[b]["srow"] if bl == "row" else q[b]["scol"]
+            fp8.fp8_grouped_gemm(mode, A, fa, B, fb, off, E, M, N, K, sa, 1, sb, 1, o[out], ldT)
+
+        W = self.gemm_work
+        for k in ("xp", "w_gate", "w_up", "w_down", "hp"):
+            _timed(ev, "q", lambda k=k: self.quantize(k), quantize_bytes(self.inp[k].shape))
+        _timed(ev, "g", lambda: gg(GM, "xp", "row", 0, "w_gate", "row", 0, F, H, "gate"), W["fprop"])
+        _timed(ev, "g", lambda: gg(GM, "xp", "row", 0, "w_up", "row", 0, F, H, "up"), W["fprop"])
+        _timed(ev, "g", lambda: gg(GM, "hp", "row", 0, "w_down", "row", 0, H, F, "y"), W["fprop_down"])
+        for k in ("dy_down", "dy_gate", "dy_up"):
+            _timed(ev, "q", lambda k=k: self.quantize(k), quantize_bytes(self.inp[k].shape))
+        _timed(ev, "g", lambda: gg(GMT, "dy_down", "row", 1, "w_down", "colT", 0, F, H, "dh",
+                                   q["w_down"]["ldT"]), W["dgrad_down"])
+        _timed(ev, "g", lambda: gg(GMT, "dy_gate", "row", 1, "w_gate", "colT", 0, H, F, "dx_gate",
+                                   q["w_gate"]["ldT"]), W["dgrad"])
+        _timed(ev, "g", lambda: gg(GMT, "dy_up", "row", 1, "w_up", "colT", 0, H, F, "dx_up",
+                                   q["w_up"]["ldT"]), W["dgrad"])
+        _timed(ev, "g", lambda: gg(GK, "dy_down", "colT", 1, "hp", "colT", 0, H, F, "dw_down", self.ldT_tok),
+               W["wgrad"])
+        _timed(ev, "g", lambda: gg(GK, "dy_gate", "colT", 1, "xp", "colT", 0, F, H, "dw_gate", self.ldT_tok),
+               W["wgrad"])
+        _timed(ev, "g", lambda: gg(GK, "dy_up", "colT", 1, "xp", "colT", 0, F, H, "dw_up", self.ldT_tok),
+               W["wgrad"])
+
+
+# --------------------------------------------------------------------------------------------
+# CPU baseline (the oracle)
+# --------------------------------------------------------------------------------------------
+
+def llama_mlp_work():
+    """FLOPs and algorithmic quantize bytes of one default step."""
+    flops = 0.0
+    for (a, al, b, bl, o) in MLP_GEMMS:
+        M, K = LLAMA_MLP_SHAPES[a][0] if al == "row" else LLAMA_MLP_SHAPES[a][0][::-1]
+        N = LLAMA_MLP_SHAPES[b][0][0] if bl == "row" else LLAMA_MLP_SHAPES[b][0][1]
+        flops += 2.0 * M * N * K
+    q_bytes = sum(quantize_bytes(shape) for shape, _ in LLAMA_MLP_SHAPES.values())
+    return {"flops": flops, "q_bytes": q_bytes}
 
 
 def cpu_baseline_sample():
-    """The oracle on a bounded sample of the same workload, on the host cores."""
+    """The oracle on a bounded sample of the default workload, on the host cores."""
     import numpy as np
 
     import oracle
@@ -250,16 +507,40 @@ def cpu_baseline_sample():
     t0 = time.perf_counter()
     oracle.gemm(A, 0, B, 0, np.float32(1.0), np.float32(1.0))
     tg = time.perf_counter() - t0
-    flops = 2.0 * 8 * F_ * H_
-    g_tflops = flops / tg / 1e12
-    # the step-time model of the oracle: 9 GEMMs at its GEMM rate + 8 quantizes at its quantize rate
-    step_s = N_GEMM * GEMM_FLOP / (g_tflops * 1e12) + sum(QUANT_ELEMS.values()) * QUANT_BYTES_PER_ELEM / (q_gbs * 1e9)
-    value = N_GEMM * GEMM_FLOP / step_s / 1e12
-    return {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+    g_tflops = 2.0 * 8 * F_ * H_ / tg / 1e12
+    w = llama_mlp_work()
+    # the oracle's step time: its GEMM rate over the step's FLOPs + its quantize rate over the step's bytes
+    step_s = w["flops"] / (g_tflops * 1e12) + w["q_bytes"] / (q_gbs * 1e9)
+    return {"value": w["flops"] / step_s / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "sample": (f"oracle delayed quantize (both layouts) of X rows 0..2047 [2048x4096] "
                        f"({q_gbs:.3f} GB/s) and the fp64 gate GEMM for 8 output rows [8x14336x4096] "
                        f"({g_tflops * 1e3:.4f} GFLOP/s), extrapolated to one whole step"),
             "quantize_gbs": q_gbs, "gemm_tflops": g_tflops, "seconds": tq + tg}
+
+
+# --------------------------------------------------------------------------------------------
+# the GPU arm
+# --------------------------------------------------------------------------------------------
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+
+
+def _max_over_ranks(v, world, dev):
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], device=dev, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t)
+
+
+def _category(ev, kind):
+    items = ev.get(kind, [])
+    return [a.elapsed_time(b) for a, b, _ in items], [w for _, _, w in items]
 
 
 def run_gpu(args, rank, world, local_rank):
@@ -276,26 +557,21 @@ def run_gpu(args, rank, world, local_rank):
     hbm_gbs, bf16_burst, bf16_sust, peak_src = peaks()
     fp8_peak = 2.0 * bf16_sust               # FP8 dense = 2x bf16 dense (nominal 4.5 vs 2.25 PFLOP/s)
 
-    if args.workload == "gemm":
-        run_single_kernel(args, MlpStep(dev, seed=1 + rank, keys=("x", "w_gate"), outs=("gate",)), rank, world)
+    if args.workload in ("gemm", "quantize"):
+        run_single_kernel(args, dev, rank)
         return
-    if args.workload == "quantize":
-        run_single_kernel(args, MlpStep(dev, seed=1 + rank, keys=("dy_gate",), outs=()), rank, world)
+    if args.workload == "sweep":
+        run_sweep(args, dev, rank, hbm_gbs)
         return
-    step = MlpStep(dev, seed=1 + rank)
+    make = {"llama_mlp": llama_mlp_step, "flux": flux_step, "llama_rowwise": RowwiseStep, "moe": MoeStep}
+    step = make[args.workload](dev, 1 + rank)
     for _ in range(max(3, args.warmup)):
         step.run(world=world)
     assert fp8.fp8_sync_status() == 0
 
-    def barrier():
-        if world > 1:
-            import torch.distributed as dist
-            dist.barrier()
-        torch.cuda.synchronize()
-
     sampler = ClockSampler(local_rank)
-    ev = {"q": [], "g": [], "u": []}
-    barrier()
+    ev = {}
+    _barrier(world)
     sampler.start()
     time.sleep(0.3)
     t_start = torch.cuda.Event(enable_timing=True)
@@ -305,64 +581,43 @@ def run_gpu(args, rank, world, local_rank):
     for _ in range(args.steps):
         step.run(ev, world=world)
     t_end.record()
-    barrier()
+    _barrier(world)
     w1 = time.time()
     clocks = sampler.stop((w0, w1))
     st = fp8.fp8_sync_status()
     assert st == 0, f"device status {st}"
-    total_ms = t_start.elapsed_time(t_end)
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt)
-    ms_step = total_ms / args.steps
-    g_ms = [a.elapsed_time(b) for a, b in ev["g"]]
-    q_ms = [a.elapsed_time(b) for a, b in ev["q"]]
-    u_ms = [a.elapsed_time(b) for a, b in ev["u"]]
-    gemm_avg_ms = sum(g_ms) / len(g_ms)
-    gemm_tflops = GEMM_FLOP / (gemm_avg_ms * 1e-3) / 1e12
-    q_bytes = sum(QUANT_ELEMS.values()) * QUANT_BYTES_PER_ELEM
-    q_ms_step = sum(q_ms) / args.steps
-    q_gbs = q_bytes / (q_ms_step * 1e-3) / 1e9
+    ms_step = _max_over_ranks(t_start.elapsed_time(t_end), world, dev) / args.steps
 
-    # end to end through the public API with host buffers: H2D of the step's
-    # inputs from pinned memory, the step, D2H of the block output and dX
-    pinned = {k: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for k, t in step.inp.items()}
-    for k in pinned:
-        pinned[k].copy_(step.inp[k])
-    host_y = torch.empty(step.out["y"].shape, dtype=torch.bfloat16, pin_memory=True)
-    host_dx = torch.empty(step.out["dx_gate"].shape, dtype=torch.bfloat16, pin_memory=True)
-    host_scale = torch.empty(len(step.order), dtype=torch.float32, pin_memory=True)
-    h2d = sum(t.numel() * t.element_size() for t in pinned.values())
-    d2h = host_y.numel() * 2 + host_dx.numel() * 2 + host_scale.numel() * 4
-    e2e_steps = max(2, min(args.steps, 5))
+    g_ms, g_work = _category(ev, "g")
+    q_ms, q_work = _category(ev, "q")
+    u_ms, _ = _category(ev, "u")
+    gemm_tflops = sum(f for f, _ in g_work) / (sum(g_ms) * 1e-3) / 1e12
+    # roofline time of every GEMM launch: max(flops / tensor peak, bytes / HBM)
+    g_roof_ms = sum(max(f / (fp8_peak * 1e12), b / (hbm_gbs * 1e9)) * 1e3 for f, b in g_work)
+    g_tensor_ms = sum(f / (fp8_peak * 1e12) * 1e3 for f, _ in g_work)
+    g_frac = g_roof_ms / sum(g_ms)
+    q_gbs = sum(q_work) / (sum(q_ms) * 1e-3) / 1e9 if q_ms else 0.0
 
-    def e2e_step():
-        for k in pinned:
-            step.inp[k].copy_(pinned[k], non_blocking=True)
-        step.run(world=world)
-        host_y.copy_(step.out["y"], non_blocking=True)
-        host_dx.copy_(step.out["dx_gate"], non_blocking=True)
-        host_scale.copy_(step.scale, non_blocking=True)
-    e2e_step()
-    barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record()
-    barrier()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt)
+    # the dominant kernel category of the step gives the roofline object
+    if sum(g_ms) >= sum(q_ms):
+        if g_roof_ms <= g_tensor_ms * 1.0001:      # tensor-bound GEMMs
+            roof = {"bound": "tensor", "achieved": round(gemm_tflops, 1), "peak": round(fp8_peak, 1),
+                    "unit": "TFLOP/s", "frac": round(gemm_tflops / fp8_peak, 4), "kernel": "fp8_gemm_kernel",
+                    "traffic": gemm_traffic() if step.name == "llama_mlp" else None,
+                    "peak_source": f"{peak_src}: 2 x sustained bf16 {bf16_sust} TFLOP/s (fp8/bf16 nominal ratio 2)"}
+        else:                                      # HBM-bound (grouped GEMMs at the MoE shape)
+            gbs = sum(b for _, b in g_work) / (sum(g_ms) * 1e-3) / 1e9
+            roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_gbs, "unit": "GB/s",
+                    "frac": round(g_frac, 4), "traffic": None, "kernel": "fp8_gemm_kernel (grouped)",
+                    "peak_source": f"{peak_src} HBM copy bandwidth; frac = roofline time max(flops / fp8 peak, "
+                                   f"bytes / HBM) over the measured time"}
+    else:
+        roof = {"bound": "hbm", "achieved": round(q_gbs, 1), "peak": hbm_gbs, "unit": "GB/s",
+                "frac": round(q_gbs / hbm_gbs, 4), "traffic": None, "kernel": "quantize (amax + cast)",
+                "peak_source": f"{peak_src} HBM copy bandwidth"}
 
-    value = world * N_GEMM * GEMM_FLOP / (ms_step * 1e-3) / 1e12
-    e2e_value = world * N_GEMM * GEMM_FLOP / (e2e_ms * 1e-3) / 1e12
+    e2e = run_e2e(step, args, world, dev)
+    value = world * step.flops / (ms_step * 1e-3) / 1e12
     out = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -376,40 +631,125 @@ def run_gpu(args, rank, world, local_rank):
         "vs_baseline": None,
         "dtype": "fp8 e4m3/e5m2 operands, fp32 accumulate, bf16 out",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "tokens_per_rank": T_, "parallelism": f"dp{world}",
-                   "l2": "inputs larger than L2 (about 2.4 GB of operands touched per step)",
+        "config": {"workload": step.desc, "name": step.name, "tokens_per_rank": step.tokens,
+                   "parallelism": f"dp{world}",
+                   "l2": "inputs larger than L2 (GBs of operands touched per step), no flush needed",
                    "timing": "CUDA events on the launching stream, max over ranks"},
-        "tokens_per_s": round(world * T_ / (ms_step * 1e-3), 1),
-        "gemm": {"avg_ms": round(gemm_avg_ms, 4), "tflops": round(gemm_tflops, 1),
-                 "frac_of_fp8_peak": round(gemm_tflops / fp8_peak, 4)},
-        "quantize": {"ms_per_step": round(q_ms_step, 4), "gbs": round(q_gbs, 1),
-                     "frac_of_hbm": round(q_gbs / hbm_gbs, 4), "bytes_per_elem": QUANT_BYTES_PER_ELEM},
-        "update_us": round(1e3 * sum(u_ms) / len(u_ms), 2),
-        "roofline": {"bound": "tensor", "achieved": round(gemm_tflops, 1), "peak": round(fp8_peak, 1),
-                     "unit": "TFLOP/s", "frac": round(gemm_tflops / fp8_peak, 4), "traffic": gemm_traffic(),
-                     "peak_source": f"{peak_src}: 2 x sustained bf16 {bf16_sust} TFLOP/s (fp8/bf16 nominal ratio 2)"},
-        "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+        "tokens_per_s": round(world * step.tokens / (ms_step * 1e-3), 1),
+        "gemm": {"ms_per_step": round(sum(g_ms) / args.steps, 4), "tflops": round(gemm_tflops, 1),
+                 "frac_of_fp8_peak": round(gemm_tflops / fp8_peak, 4), "frac_of_roofline": round(g_frac, 4),
+                 "launches_per_step": len(g_ms) // args.steps},
+        "quantize": {"ms_per_step": round(sum(q_ms) / args.steps, 4), "gbs": round(q_gbs, 1),
+                     "frac_of_hbm": round(q_gbs / hbm_gbs, 4), "bytes_per_step": step.q_bytes,
+                     "calls_per_step": len(q_ms) // args.steps},
+        "update_us": round(1e3 * sum(u_ms) / len(u_ms), 2) if u_ms else None,
+        "roofline": roof,
+        "e2e": e2e,
         "gpu_launches": step.launches_per_step * args.steps,
         "clocks": clocks,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if step.name == "llama_mlp" and rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline_sample()
     if rank == 0:
         print(json.dumps(out), flush=True)
 
 
-def run_single_kernel(args, step, rank, world):
-    """Time one kernel of the step in isolation (profiling aid)."""
+def run_e2e(step, args, world, dev):
+    """The same metric through the public API with host buffers: every step
+    copies the step's bf16 inputs from pinned host memory and reads back the
+    forward output, inside the timed region."""
+    pinned = {k: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for k, t in step.inp.items()}
+    for k in pinned:
+        pinned[k].copy_(step.inp[k])
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in step.d2h]
+    h2d = sum(t.numel() * t.element_size() for t in pinned.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    n = 2 if step.name == "moe" else max(2, min(args.steps, 5))
+
+    def one():
+        for k in pinned:
+            step.inp[k].copy_(pinned[k], non_blocking=True)
+        step.run(world=world)
+        for h, d in zip(host_out, step.d2h):
+            h.copy_(d, non_blocking=True)
+    one()
+    _barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(n):
+        one()
+    e1.record()
+    _barrier(world)
+    ms = _max_over_ranks(e0.elapsed_time(e1) / n, world, dev)
+    return {"value": round(world * step.flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n}
+
+
+def run_sweep(args, dev, rank, hbm_gbs):
+    """Delayed quantize (E4M3, both layouts) of 2^20 .. 2^30 elements."""
+    import fp8_mixed_precision_scale_gb300 as fp8
+    import synth
+    rec = fp8.Recipe(kind=fp8.DELAYED)
+    scale = torch.full((1,), 64.0, device=dev)
+    amax = torch.zeros(1, device=dev)
+    points = []
+    for p in range(20, 31):
+        n = 1 << p
+        rows, cols = n // 4096, 4096
+        # rotate over enough buffers that one round touches more than 3 x L2
+        nbuf = max(1, -(-(400 << 20) // (4 * n)))
+        base = synth.sweep_tensor(n, dev)
+        bufs = []
+        for i in range(nbuf):
+            bufs.append((base if i == 0 else base.clone(), torch.empty((rows, cols), dtype=torch.uint8, device=dev),
+                         torch.empty((cols, rows), dtype=torch.uint8, device=dev),
+                         torch.empty(1, device=dev), torch.empty(1, device=dev)))
+        reps = max(nbuf, min(200, (64 << 30) // (4 * n)))
+
+        def launch(i):
+            x, qr, qc, sr, sc = bufs[i % nbuf]
+            fp8.fp8_quantize(x, rows, cols, cols, 0, rec, 3, scale, amax, qr, sr, qc, rows, sc)
+        for i in range(nbuf + 3):
+            launch(i)
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        for i in range(reps):
+            launch(i)
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / reps
+        gbs = 4.0 * n / (ms * 1e-3) / 1e9
+        points.append({"elements": n, "us_per_launch": round(ms * 1e3, 2), "gbs": round(gbs, 1),
+                       "frac_of_hbm": round(gbs / hbm_gbs, 4), "buffers": nbuf, "launches": reps})
+        del bufs, base
+        torch.cuda.empty_cache()
+    assert fp8.fp8_sync_status() == 0
+    knee = next((pt["elements"] for pt in points if pt["frac_of_hbm"] >= 0.8), None)
+    best = max(points, key=lambda pt: pt["gbs"])
+    if rank == 0:
+        print(json.dumps({"metric": METRIC, "workload": "sweep", "value": best["gbs"], "unit": "GB/s",
+                          "config": {"workload": "delayed quantize e4m3fn, both layouts, x ~ N(0,1) shaped "
+                                                 "[n/4096, 4096], n = 2^20..2^30; buffers rotated so each round "
+                                                 "exceeds L2", "algorithmic_bytes_per_element": 4},
+                          "knee_elements_at_80pct": knee, "points": points}), flush=True)
+
+
+def run_single_kernel(args, dev, rank):
+    """Time one kernel of the default step in isolation (profiling aid)."""
     import fp8_mixed_precision_scale_gb300 as fp8
     if args.workload == "gemm":
+        step = llama_mlp_step(dev, 1, keys=("x", "w_gate"), outs=("gate",))
         for k in ("x", "w_gate"):   # real FP8 operands for the GEMM
-            step.quantize(k, step.order.index(k))
-        fn = lambda: step.gemm(*MlpStep.GEMMS[0])  # noqa: E731
-        work, unit = GEMM_FLOP / 1e12, "TFLOP/s"
+            step.quantize(k)
+        fn = lambda: step.gemm(*MLP_GEMMS[0])  # noqa: E731
+        work, unit = step.gemm_work["gate"][0] / 1e12, "TFLOP/s"
     else:
-        fn = lambda: step.quantize("dy_gate", step.order.index("dy_gate"))  # noqa: E731
-        work, unit = QUANT_ELEMS["dy_gate"] * QUANT_BYTES_PER_ELEM / 1e9, "GB/s"
+        step = llama_mlp_step(dev, 1, keys=("dy_gate",), outs=())
+        fn = lambda: step.quantize("dy_gate")  # noqa: E731
+        work, unit = quantize_bytes(step.inp["dy_gate"].shape) / 1e9, "GB/s"
     for _ in range(max(3, args.warmup)):
         fn()
     torch.cuda.synchronize()
@@ -441,12 +781,13 @@ def run_reference(args, rank, world):
         base = b
     value = statistics.mean(vals)
     wall = time.perf_counter() - t0
+    work = llama_mlp_work()
     out = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": 1e3 * N_GEMM * GEMM_FLOP / (value * 1e12),
+        "warmup": args.warmup, "ms_per_step": 1e3 * work["flops"] / (value * 1e12),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
         "data": "synthetic", "impl": "reference",
-        "config": {"workload": WORKLOAD, "parallelism": "host cores"},
+        "config": {"workload": LLAMA_MLP_DESC, "parallelism": "host cores"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": base["cores"], "kind": "oracle",
                          "sample": base["sample"]},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -462,10 +803,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", default="llama_mlp", choices=["llama_mlp", "gemm", "quantize"],
-                    help="llama_mlp: the whole fwd+bwd FP8 step (default); gemm / quantize: one kernel of it "
-                         "(the gate-projection GEMM 8192x14336x4096, the delayed quantize of a [8192, 14336] "
-                         "tensor), for profiling")
+    ap.add_argument("--workload", default="llama_mlp",
+                    choices=["llama_mlp", "llama_rowwise", "moe", "flux", "sweep", "gemm", "quantize"],
+                    help="llama_mlp: the whole fwd+bwd FP8 step of the Llama-3-8B MLP (default); see the "
+                         "module docstring for the others")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
