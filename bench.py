@@ -22,6 +22,8 @@ Other workloads (same JSON line, their own config):
   sweep          the delayed quantize (E4M3, both layouts) of 2^20 .. 2^30
                  elements, GB/s against size
   gemm, quantize single kernels of the default step, for profiling
+  grouped_m, grouped_k  one M-grouped / K-grouped expert GEMM of a reduced
+                 MoE layer (64 experts, 8192 routed rows), for profiling
 
 Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle on a
 bounded sample of the same workload instead.
@@ -557,7 +559,7 @@ def run_gpu(args, rank, world, local_rank):
     hbm_gbs, bf16_burst, bf16_sust, peak_src = peaks()
     fp8_peak = 2.0 * bf16_sust               # FP8 dense = 2x bf16 dense (nominal 4.5 vs 2.25 PFLOP/s)
 
-    if args.workload in ("gemm", "quantize"):
+    if args.workload in ("gemm", "quantize", "grouped_m", "grouped_k"):
         run_single_kernel(args, dev, rank)
         return
     if args.workload == "sweep":
@@ -737,10 +739,45 @@ def run_sweep(args, dev, rank, hbm_gbs):
                           "knee_elements_at_80pct": knee, "points": points}), flush=True)
 
 
+def grouped_case(kind, dev, E=64, rows=8192):
+    """A reduced DeepSeek-V3 expert GEMM for profiling: 64 experts (2 empty),
+    8192 routed rows, hidden 7168, ffn 2048; random FP8 operands."""
+    import numpy as np
+
+    import fp8_mixed_precision_scale_gb300 as fp8
+    import synth
+    H, F = synth.DSV3["H"], synth.DSV3["F"]
+    sizes = synth.moe_group_sizes(total_rows=rows, E=E, n_forced_empty=2).numpy()
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    off_d = torch.from_numpy(off).to(dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+
+    def codes(*shape):
+        return (torch.randn(shape, generator=g, device=dev) * 64).clamp(-448, 448).to(
+            torch.float8_e4m3fn).view(torch.uint8)
+    s_rows, s_ef, s_eh = (torch.ones(n, device=dev) for n in (rows, E * F, E * H))
+    if kind == "grouped_m":       # fprop of the gate projection
+        A, B, C = codes(rows, H), codes(E, F, H), torch.empty((rows, F), dtype=torch.bfloat16, device=dev)
+        fn = lambda: fp8.fp8_grouped_gemm(fp8.GROUPED_M, A, 0, B, 0, off_d, E, rows, F, H, s_rows, 1,  # noqa
+                                          s_ef, 1, C, 0)
+        wbytes = int((sizes > 0).sum()) * F * H
+        return fn, (rows * H + wbytes + 2.0 * rows * F) / 1e9, "GB/s (algorithmic)"
+    ldT = int(fp8.fp8_group_padded_offsets(off)[0])
+    ldT = (ldT + 15) // 16 * 16
+    A, B = codes(F, ldT), codes(H, ldT)   # wgrad of the gate projection: dW_e = dY_e^T X_e
+    C = torch.empty((E, F, H), dtype=torch.bfloat16, device=dev)
+    fn = lambda: fp8.fp8_grouped_gemm(fp8.GROUPED_K, A, 1, B, 0, off_d, E, rows, F, H, s_ef, 1,  # noqa
+                                      s_eh, 1, C, ldT)
+    return fn, (rows * (F + H) + 2.0 * E * F * H) / 1e9, "GB/s (algorithmic)"
+
+
 def run_single_kernel(args, dev, rank):
     """Time one kernel of the default step in isolation (profiling aid)."""
     import fp8_mixed_precision_scale_gb300 as fp8
-    if args.workload == "gemm":
+    if args.workload in ("grouped_m", "grouped_k"):
+        fn, work, unit = grouped_case(args.workload, dev)
+    elif args.workload == "gemm":
         step = llama_mlp_step(dev, 1, keys=("x", "w_gate"), outs=("gate",))
         for k in ("x", "w_gate"):   # real FP8 operands for the GEMM
             step.quantize(k)
@@ -804,7 +841,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="llama_mlp",
-                    choices=["llama_mlp", "llama_rowwise", "moe", "flux", "sweep", "gemm", "quantize"],
+                    choices=["llama_mlp", "llama_rowwise", "moe", "flux", "sweep", "gemm", "quantize", "grouped_m",
+                             "grouped_k"],
                     help="llama_mlp: the whole fwd+bwd FP8 step of the Llama-3-8B MLP (default); see the "
                          "module docstring for the others")
     args = ap.parse_args()

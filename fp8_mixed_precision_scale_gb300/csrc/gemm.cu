@@ -13,14 +13,15 @@
 // page and "FP8 Training on AMD GPUs with TorchTitan and TorchAO").
 //
 // Design (GB300, sm_103a): persistent, warp-specialised kernel, one CTA per
-// SM, 192 threads.
+// SM, 320 threads.
 //   warp 0     TMA producer: 128x128-byte A and 256x128-byte B tiles into a
 //              4-stage shared-memory ring (128-byte swizzle), completion by
 //              mbarrier transaction counts.
 //   warp 1     MMA issuer: one thread issues tcgen05.mma kind::f8f6f4
 //              (M=128, N=256, K=32) into a TMEM accumulator; tcgen05.commit
 //              frees ring stages and hands finished accumulators over.
-//   warps 2-5  epilogue: tcgen05.ld 32 columns at a time, scale, convert to
+//   warps 2-9  epilogue: tcgen05.ld 32 columns at a time (each warp one TMEM
+//              lane quarter and half of the columns), scale, convert to
 //              bf16, store.  Two 256-column accumulators (all 512 TMEM
 //              columns) let the epilogue of one tile overlap the main loop of
 //              the next.
@@ -46,10 +47,10 @@ constexpr int UMMA_K = 32;
 constexpr int STAGES = 4;
 constexpr int A_STAGE_BYTES = BM * BK;
 constexpr int B_STAGE_BYTES = BN * BK;
-constexpr int GEMM_THREADS = 192;
+constexpr int GEMM_THREADS = 320;   // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
-constexpr int MAX_GROUPS = 4096;
+constexpr int MAX_GROUPS = 1024;  // group tables share shared memory with the ring
 
 enum { MODE_DENSE = 0, MODE_MGROUP = 1, MODE_KGROUP = 2 };
 
@@ -87,7 +88,12 @@ struct SmemLayout {
     static constexpr int bar_off = b_off + STAGES * B_STAGE_BYTES;
     static constexpr int n_bars = 2 * STAGES + 2 + 2 + 1;
     static constexpr int slot_off = bar_off + n_bars * 8;
-    static constexpr int misc_off = slot_off + 16;  // int32 group tables start here
+    // epilogue staging: per epilogue warp a 32-row x 32-column bf16 block,
+    // rows padded to 80 bytes (conflict-free 16-byte accesses both ways)
+    static constexpr int stage_pitch = 80;
+    static constexpr int stage_warp_bytes = 32 * stage_pitch;
+    static constexpr int stage_off = (slot_off + 16 + 127) / 128 * 128;
+    static constexpr int misc_off = stage_off + 8 * stage_warp_bytes;  // int32 group tables start here
     static constexpr int base_bytes = misc_off;
 };
 
@@ -251,7 +257,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
         for (int b = 0; b < 2; b++) {
             mbar_init(&tfull[b], 1);
-            mbar_init(&tempty[b], 4);
+            mbar_init(&tempty[b], 8);  // one arrive per epilogue warp
         }
         mbar_init(done, 1);
         fence_barrier_init();
@@ -354,7 +360,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         mbar_wait_bounded(done, 0, WAIT_LIMIT_NS, p.err, ERR_TEARDOWN_WAIT);
     } else if (warp >= 2) {
         // ---------------- epilogue ----------------
-        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        // 8 warps: warp w reads TMEM lane quarter (w % 4) -- the hardware rule
+        // for tcgen05.ld -- and one half of the tile's 256 columns.
+        const int q = warp & 3;
+        const int half = (warp - 2) >> 2;
+        uint8_t *stage = smem + SmemLayout::stage_off + (warp - 2) * SmemLayout::stage_warp_bytes;
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
@@ -362,13 +372,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             const int64_t gr = ti.row0 + q * 32 + lane;
             const bool row_ok = gr < ti.row_end;
             uint16_t *crow = p.C + ti.c_base + gr * p.ldc;
+            const int64_t cbeg = ti.col0 + half * (BN / 2);
+            const int64_t cend = min(cbeg + BN / 2, ti.col_end);
             if (ti.nkb == 0) {
                 if (row_ok)
-                    for (int64_t c = ti.col0; c < ti.col0 + BN && c < ti.col_end; c += 8) {
-                        if (p.c_vec16 && c + 8 <= ti.col_end)
+                    for (int64_t c = cbeg; c < cend; c += 8) {
+                        if (p.c_vec16 && c + 8 <= cend)
                             *reinterpret_cast<uint4 *>(crow + c) = make_uint4(0, 0, 0, 0);
                         else
-                            for (int64_t j = c; j < ti.col_end; j++) crow[j] = 0;
+                            for (int64_t j = c; j < cend; j++) crow[j] = 0;
                     }
                 continue;
             }
@@ -376,36 +388,67 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             tc_fence_after();
             const float sa_v = row_ok ? (p.sa_per_row ? __ldg(p.sa + ti.sa_base + gr) : __ldg(p.sa)) : 0.0f;
             const float sb0 = p.sb_per_row ? 0.0f : __ldg(p.sb);
-            for (int ch = 0; ch < BN / 32; ch++) {
-                const int64_t c0 = ti.col0 + ch * 32;
-                if (c0 >= ti.col_end) break;  // warp-uniform
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + ch * 32), r);
-                tmem_ld_wait();
-                if (!row_ok) continue;
-                uint32_t packed[16];
+            // two 32-column chunks per round: both TMEM loads are in flight
+            // before the first wait
+            for (int ch = 0; ch < BN / 64; ch += 2) {
+                const int64_t c0 = cbeg + ch * 32;
+                if (c0 >= cend) break;  // warp-uniform
+                uint32_t r[2][32];
+                const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) +
+                                       (uint32_t)(acc * BN + half * (BN / 2) + ch * 32);
+                tmem_ld_32x32b_x32(taddr, r[0]);
+                tmem_ld_32x32b_x32(taddr + 32, r[1]);
+                // column scales: lane j holds the scale of column c + j; the
+                // other lanes read it by shuffle (one coalesced load per chunk)
+                float sbl[2] = {sb0, sb0};
+                if (p.sb_per_row) {
 #pragma unroll
-                for (int j = 0; j < 16; j++) {
-                    float sb_lo = sb0, sb_hi = sb0;
-                    if (p.sb_per_row) {
-                        const int64_t cl = c0 + 2 * j;
-                        sb_lo = cl < ti.col_end ? __ldg(p.sb + ti.sb_base + cl) : 0.0f;
-                        sb_hi = cl + 1 < ti.col_end ? __ldg(p.sb + ti.sb_base + cl + 1) : 0.0f;
+                    for (int u = 0; u < 2; u++) {
+                        const int64_t cc = c0 + u * 32 + lane;
+                        sbl[u] = cc < cend ? __ldg(p.sb + ti.sb_base + cc) : 0.0f;
                     }
-                    const float lo = __uint_as_float(r[2 * j]) * sa_v * sb_lo;
-                    const float hi = __uint_as_float(r[2 * j + 1]) * sa_v * sb_hi;
-                    packed[j] = pack_bf16x2(lo, hi);
                 }
+                tmem_ld_wait();
 #pragma unroll
-                for (int g = 0; g < 4; g++) {
-                    const int64_t c = c0 + g * 8;
-                    if (p.c_vec16 && c + 8 <= ti.col_end) {
-                        *reinterpret_cast<uint4 *>(crow + c) =
-                            make_uint4(packed[4 * g], packed[4 * g + 1], packed[4 * g + 2], packed[4 * g + 3]);
-                    } else {
-                        for (int j = 0; j < 8 && c + j < ti.col_end; j++)
-                            crow[c + j] = (uint16_t)(packed[4 * g + j / 2] >> (16 * (j & 1)));
+                for (int u = 0; u < 2; u++) {
+                    const int64_t cu = c0 + u * 32;
+                    if (cu >= cend) break;  // warp-uniform
+                    uint32_t packed[16];
+#pragma unroll
+                    for (int j = 0; j < 16; j++) {
+                        const float sb_lo = __shfl_sync(0xffffffffu, sbl[u], 2 * j);
+                        const float sb_hi = __shfl_sync(0xffffffffu, sbl[u], 2 * j + 1);
+                        const float lo = __uint_as_float(r[u][2 * j]) * sa_v * sb_lo;
+                        const float hi = __uint_as_float(r[u][2 * j + 1]) * sa_v * sb_hi;
+                        packed[j] = pack_bf16x2(lo, hi);
                     }
+                    // transpose through shared memory so that each store
+                    // instruction writes 8 rows x 64 contiguous bytes (whole
+                    // sectors) instead of 32 rows x 16 bytes
+#pragma unroll
+                    for (int g = 0; g < 4; g++)
+                        *reinterpret_cast<uint4 *>(stage + lane * SmemLayout::stage_pitch + g * 16) =
+                            make_uint4(packed[4 * g], packed[4 * g + 1], packed[4 * g + 2], packed[4 * g + 3]);
+                    __syncwarp();
+#pragma unroll
+                    for (int i = 0; i < 4; i++) {
+                        const int rr = i * 8 + (lane >> 2), seg = lane & 3;
+                        const uint4 v =
+                            *reinterpret_cast<const uint4 *>(stage + rr * SmemLayout::stage_pitch + seg * 16);
+                        const int64_t row = ti.row0 + q * 32 + rr;
+                        const int64_t c = cu + seg * 8;
+                        if (row < ti.row_end && c < cend) {
+                            uint16_t *dst = p.C + ti.c_base + row * p.ldc + c;
+                            if (p.c_vec16 && c + 8 <= cend) {
+                                *reinterpret_cast<uint4 *>(dst) = v;
+                            } else {
+                                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                                for (int j = 0; j < 8 && c + j < cend; j++)
+                                    dst[j] = (uint16_t)(w[j / 2] >> (16 * (j & 1)));
+                            }
+                        }
+                    }
+                    __syncwarp();
                 }
             }
             tc_fence_before();

@@ -208,7 +208,7 @@ FP8GB_API fp8_status_t fp8_scaled_gemm(const uint8_t *A, int fa, int64_t lda, co
  *   C[e][n][k] = sum_{r < m_e} A[n][poff_e + r] B[k][poff_e + r] sa(e, n)
  *   sb(e, k); C bf16 [G][N][K]; an empty group's block is written as 0.
  *   sa: [1] or [G][N]; sb: [1] or [G][K].
- * Limits: K % 16 == 0 (M mode), ld_T % 16 == 0 (K mode), 1 <= G <= 4096;
+ * Limits: K % 16 == 0 (M mode), ld_T % 16 == 0 (K mode), 1 <= G <= 1024;
  * 16-byte aligned A and B; C 2-byte aligned.
  */
 FP8GB_API fp8_status_t fp8_grouped_gemm(int mode, const uint8_t *A, int fa, const uint8_t *B, int fb,
