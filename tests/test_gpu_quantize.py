@@ -307,3 +307,15 @@ def test_full_moe_tokens_grouped_sampled(orc):
             assert_codes_equal(seg[:, :r1 - r0], ref["q_colT"], 0, f"group {e} col {c0}")
             assert not seg[:, r1 - r0:].any()
             assert_f32_bits_equal(sc[e, c0:c0 + 8].cpu().numpy(), ref["scale_inv_col"], f"scol {e} {c0}")
+
+
+def test_quantize_grouped_large(orc):
+    """A large grouped tensor (20000 x 4096, 40 groups incl. empty ones), every byte."""
+    g = torch.Generator().manual_seed(41)
+    sizes = torch.randint(0, 900, (40,), generator=g).numpy()
+    sizes[[3, 17]] = 0
+    sizes[-1] = 20000 - sizes[:-1].sum()
+    assert sizes[-1] > 0
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    x = gen_x((int(off[-1]), 4096), seed=42)
+    compare(orc, x, 0, 2, offsets=off, what="grouped multi-chunk")
