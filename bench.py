@@ -24,6 +24,8 @@ Other workloads (same JSON line, their own config):
   gemm, quantize single kernels of the default step, for profiling
   grouped_m, grouped_k  one M-grouped / K-grouped expert GEMM of a reduced
                  MoE layer (64 experts, 8192 routed rows), for profiling
+  quantize_grouped  the rowwise quantize of one reduced MoE weight (64
+                 experts x 2048 rows x 7168), for profiling
 
 Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle on a
 bounded sample of the same workload instead.
@@ -559,7 +561,7 @@ def run_gpu(args, rank, world, local_rank):
     hbm_gbs, bf16_burst, bf16_sust, peak_src = peaks()
     fp8_peak = 2.0 * bf16_sust               # FP8 dense = 2x bf16 dense (nominal 4.5 vs 2.25 PFLOP/s)
 
-    if args.workload in ("gemm", "quantize", "grouped_m", "grouped_k"):
+    if args.workload in ("gemm", "quantize", "grouped_m", "grouped_k", "quantize_grouped"):
         run_single_kernel(args, dev, rank)
         return
     if args.workload == "sweep":
@@ -772,11 +774,36 @@ def grouped_case(kind, dev, E=64, rows=8192):
     return fn, (rows * (F + H) + 2.0 * E * F * H) / 1e9, "GB/s (algorithmic)"
 
 
+def grouped_weight_quantize_case(dev, E=64):
+    """Rowwise quantize of one reduced MoE gate weight [64 * 2048, 7168] with
+    per-expert column scales (64 equal groups), for profiling."""
+    import numpy as np
+
+    import fp8_mixed_precision_scale_gb300 as fp8
+    import synth
+    H, F = synth.DSV3["H"], synth.DSV3["F"]
+    g = torch.Generator(device=dev)
+    g.manual_seed(3)
+    w = _normal(g, dev, (E * F, H), 0.02)
+    off = torch.from_numpy(np.arange(E + 1, dtype=np.int32) * F).to(dev)
+    rows = E * F
+    q_row = torch.empty((rows, H), dtype=torch.uint8, device=dev)
+    q_colT = torch.empty((H, rows), dtype=torch.uint8, device=dev)
+    sr = torch.empty(rows, device=dev)
+    sc = torch.empty(E * H, device=dev)
+    rec = fp8.Recipe(kind=fp8.ROWWISE)
+    fn = lambda: fp8.fp8_quantize(w, rows, H, H, 0, rec, 3, None, None, q_row, sr, q_colT, rows, sc,  # noqa: E731
+                                  off, E)
+    return fn, quantize_bytes((rows, H)) / 1e9, "GB/s (algorithmic)"
+
+
 def run_single_kernel(args, dev, rank):
     """Time one kernel of the default step in isolation (profiling aid)."""
     import fp8_mixed_precision_scale_gb300 as fp8
     if args.workload in ("grouped_m", "grouped_k"):
         fn, work, unit = grouped_case(args.workload, dev)
+    elif args.workload == "quantize_grouped":
+        fn, work, unit = grouped_weight_quantize_case(dev)
     elif args.workload == "gemm":
         step = llama_mlp_step(dev, 1, keys=("x", "w_gate"), outs=("gate",))
         for k in ("x", "w_gate"):   # real FP8 operands for the GEMM
@@ -842,7 +869,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="llama_mlp",
                     choices=["llama_mlp", "llama_rowwise", "moe", "flux", "sweep", "gemm", "quantize", "grouped_m",
-                             "grouped_k"],
+                             "grouped_k", "quantize_grouped"],
                     help="llama_mlp: the whole fwd+bwd FP8 step of the Llama-3-8B MLP (default); see the "
                          "module docstring for the others")
     args = ap.parse_args()
