@@ -24,11 +24,11 @@
 // Kernels and passes:
 //   DELAYED    : cast (stored scale) + fused amax            -> 1 launch
 //   TENSORWISE : amax pass, cast pass                        -> 2 launches
-//   ROWWISE    : amax pass (row + column amax), cast pass,
-//                scale finalise                              -> 3 launches
+//   ROWWISE    : amax pass (row + column amax), cast pass, scale_inv
+//                (+ amax -> scale before the cast when grouped) -> 3 or 4 launches
 // The rowwise / colwise amax values are accumulated in the scale_inv output
-// buffers themselves (as fp32 bit patterns) and turned into scale_inv by the
-// finalise kernel, so no scratch memory is needed.
+// buffers themselves (as fp32 bit patterns), turned into the scales before
+// the cast pass and into scale_inv after it, so no scratch memory is needed.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -60,6 +60,9 @@ struct QArgs {
     int margin;
     int64_t n_row_blocks;
     int64_t n_col_chunks;
+    int scales_ready;  // rowwise cast pass: the scale buffers already hold scales (else amaxes)
+    int sup_blocks;  // rowwise amax pass: 32-row blocks per super tile (1..8)
+    int sup_chunks;  // rowwise amax pass: 128-column chunks per super tile (1..8)
 };
 
 // Row-block geometry: which input rows a tile covers and where they land in
@@ -263,6 +266,150 @@ __global__ void __launch_bounds__(QT_THREADS) amax_kernel(QArgs a)
 }
 
 // ---------------------------------------------------------------------------
+// Pass 1 of the ROWWISE recipe: row amax and (group, column) amax.
+//
+// A thread block covers a super tile of up to 8 row blocks of 32 rows x up
+// to 8 column chunks of 128 columns (smaller super tiles for smaller tensors,
+// so that the grid still fills the GPU).  Column maxima are kept in registers
+// across the row blocks of one group and reduced / flushed (one relaxed
+// atomic per column) when the group changes or the chunk ends; row maxima are
+// kept across the column chunks and flushed once per row per super tile.
+// Both amaxes are accumulated as fp32 bit patterns in the scale_inv output
+// buffers (zeroed by the host).
+// ---------------------------------------------------------------------------
+constexpr int SUP_BLOCKS = 8;   // at most 32-row blocks per super tile
+constexpr int SUP_CHUNKS = 8;   // at most 128-column chunks per super tile
+
+__device__ __forceinline__ void flush_col_amax(const QArgs &a, uint32_t (&cacc)[4], int group, int64_t c0,
+                                               uint32_t (*colw)[16][4])
+{
+    const int t = threadIdx.x, cg = t & 15, w = t >> 5;
+#pragma unroll
+    for (int k = 0; k < 4; k++) cacc[k] = __vmaxu2(cacc[k], __shfl_xor_sync(0xffffffffu, cacc[k], 16));
+    if ((t & 31) < 16) {
+#pragma unroll
+        for (int k = 0; k < 4; k++) colw[w][cg][k] = cacc[k];
+    }
+    __syncthreads();
+    if (t < QT_COLS) {
+        const int g = t >> 3, j = t & 7;  // column c0 + 8g + j
+        uint32_t m = 0;
+#pragma unroll
+        for (int ww = 0; ww < QT_THREADS / 32; ww++) {
+            const uint32_t word = colw[ww][g][j >> 1];
+            m = max(m, (j & 1) ? (word >> 16) : (word & 0xFFFFu));
+        }
+        const int64_t c = c0 + t;
+        if (c < a.cols && m != 0)
+            atomicMax(reinterpret_cast<unsigned int *>(a.sinv_col) + (int64_t)group * a.cols + c, m << 16);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < 4; k++) cacc[k] = 0;
+}
+
+__global__ void __launch_bounds__(QT_THREADS) rowcol_amax_kernel(QArgs a)
+{
+    extern __shared__ __align__(16) unsigned char dsm[];
+    int32_t *poff = reinterpret_cast<int32_t *>(dsm);
+    __shared__ uint32_t red[QT_THREADS / 32];
+    __shared__ uint32_t colw[QT_THREADS / 32][16][4];
+    __shared__ RowBlock srb[SUP_BLOCKS];
+    __shared__ int bad;
+    if (a.offsets) {
+        compute_padded_offsets(a.offsets, a.G, a.rows, 0, poff, &bad, a.err);
+        __syncthreads();
+        if (bad) return;
+    }
+    const int t = threadIdx.x, cg = t & 15, roff = t >> 4;
+    const int SB = a.sup_blocks, SC = a.sup_chunks;
+    const int64_t n_sr = (a.n_row_blocks + SB - 1) / SB;
+    const int64_t n_sc = (a.n_col_chunks + SC - 1) / SC;
+    uint32_t tensor_acc = 0;
+    for (int64_t st = blockIdx.x; st < n_sr * n_sc; st += gridDim.x) {
+        const int64_t sr = st / n_sc, sc = st % n_sc;
+        __syncthreads();
+        if (t < SUP_BLOCKS) {
+            const int64_t b = sr * SB + t;
+            if (t < SB && b < a.n_row_blocks) {
+                srb[t] = row_block<32>(a, b, poff);
+            } else {
+                srb[t].skip = true;
+                srb[t].valid = 0;
+            }
+        }
+        __syncthreads();
+        uint32_t rmax[SUP_BLOCKS][2];
+#pragma unroll
+        for (int kb = 0; kb < SUP_BLOCKS; kb++) rmax[kb][0] = rmax[kb][1] = 0;
+        for (int j = 0; j < SC; j++) {
+            const int64_t c0 = (sc * SC + j) * QT_COLS;
+            if (c0 >= a.cols) break;  // uniform
+            const int64_t col = c0 + cg * 8;
+            const bool col_ok = col < a.cols;
+            uint32_t cacc[4] = {0, 0, 0, 0};
+            int cur_group = -1;
+#pragma unroll
+            for (int half = 0; half < 2; half++) {
+                if (half * (SUP_BLOCKS / 2) >= SB) break;  // uniform
+                uint4 v[SUP_BLOCKS / 2][2];
+#pragma unroll
+                for (int kk = 0; kk < SUP_BLOCKS / 2; kk++) {
+                    const RowBlock &rb = srb[half * (SUP_BLOCKS / 2) + kk];
+#pragma unroll
+                    for (int h = 0; h < 2; h++) {
+                        const int r = h * 16 + roff;
+                        if (!rb.skip && col_ok && r < rb.valid)
+                            v[kk][h] = __ldg(reinterpret_cast<const uint4 *>(a.x + (rb.in_row0 + r) * a.ld_x + col));
+                        else
+                            v[kk][h] = make_uint4(0, 0, 0, 0);
+                    }
+                }
+#pragma unroll
+                for (int kk = 0; kk < SUP_BLOCKS / 2; kk++) {
+                    const int kb = half * (SUP_BLOCKS / 2) + kk;
+                    const RowBlock &rb = srb[kb];
+                    if (rb.skip) continue;  // uniform
+                    if (a.sinv_col && cur_group >= 0 && rb.group != cur_group)
+                        flush_col_amax(a, cacc, cur_group, c0, colw);
+                    cur_group = rb.group;
+#pragma unroll
+                    for (int h = 0; h < 2; h++) {
+                        const uint4 w4 = v[kk][h];
+                        uint32_t racc = 0;
+                        racc = absmax_bf16x2(racc, w4.x);
+                        racc = absmax_bf16x2(racc, w4.y);
+                        racc = absmax_bf16x2(racc, w4.z);
+                        racc = absmax_bf16x2(racc, w4.w);
+                        cacc[0] = absmax_bf16x2(cacc[0], w4.x);
+                        cacc[1] = absmax_bf16x2(cacc[1], w4.y);
+                        cacc[2] = absmax_bf16x2(cacc[2], w4.z);
+                        cacc[3] = absmax_bf16x2(cacc[3], w4.w);
+                        rmax[kb][h] = max(rmax[kb][h], fold_absmax(racc));
+                    }
+                }
+            }
+            if (a.sinv_col && cur_group >= 0) flush_col_amax(a, cacc, cur_group, c0, colw);
+        }
+        // row maxima: reduce over the 16 threads sharing a row, one atomic per row
+#pragma unroll
+        for (int kb = 0; kb < SUP_BLOCKS; kb++) {
+#pragma unroll
+            for (int h = 0; h < 2; h++) {
+                uint32_t m = rmax[kb][h];
+                for (int d = 8; d > 0; d >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, d));
+                tensor_acc = max(tensor_acc, m);
+                const RowBlock &rb = srb[kb];
+                const int r = h * 16 + roff;
+                if (cg == 0 && !rb.skip && r < rb.valid && a.sinv_row && m != 0)
+                    atomicMax(reinterpret_cast<unsigned int *>(a.sinv_row) + rb.in_row0 + r, m);
+            }
+        }
+    }
+    if (a.amax_out) block_amax_atomic(tensor_acc, a.amax_out, red);
+}
+
+// ---------------------------------------------------------------------------
 // Cast pass.
 //   SMODE 0: one scale for the tensor (DELAYED: scale_in[0]; TENSORWISE:
 //            from amax_out[0]).  DELAYED also max-accumulates the amax.
@@ -321,16 +468,16 @@ __global__ void __launch_bounds__(QT_THREADS) cast_kernel(QArgs a)
         }
         if constexpr (SMODE == 1) {
             // per-tile scales from the amax accumulated by pass 1
+            // the scale buffers hold either the amaxes of pass 1 (turned into
+            // scales here) or, when scales_ready, the scales themselves
             if (DO_ROW && t < RB) {
-                float am = 0.0f;
-                if (t < rb.valid) am = a.sinv_row[rb.in_row0 + t];
-                srow[t] = scale_from_amax(am, fmax, a.margin);
+                const float v = t < rb.valid ? a.sinv_row[rb.in_row0 + t] : 0.0f;
+                srow[t] = a.scales_ready ? (t < rb.valid ? v : 1.0f) : scale_from_amax(v, fmax, a.margin);
             }
             if (DO_COLT && t >= QT_THREADS - QT_COLS) {
                 const int j = t - (QT_THREADS - QT_COLS);
-                float am = 0.0f;
-                if (c0 + j < a.cols) am = a.sinv_col[(int64_t)rb.group * a.cols + c0 + j];
-                scol[j] = scale_from_amax(am, fmax, a.margin);
+                const float v = c0 + j < a.cols ? a.sinv_col[(int64_t)rb.group * a.cols + c0 + j] : 0.0f;
+                scol[j] = a.scales_ready ? (c0 + j < a.cols ? v : 1.0f) : scale_from_amax(v, fmax, a.margin);
             }
             __syncthreads();
         }
@@ -424,14 +571,18 @@ __global__ void __launch_bounds__(QT_THREADS) cast_kernel(QArgs a)
     if constexpr (DELAYED) block_amax_atomic(fold_absmax(amax_acc), a.amax_out, red);
 }
 
-// ROWWISE finalise: amax bits -> scale_inv, in place.
-__global__ void finalize_rowwise_kernel(float *sinv_row, int64_t n_row, float *sinv_col, int64_t n_col, float fmax,
-                                        int margin)
+// ROWWISE scale buffers, in place: mode 0 turns the accumulated amax into
+// the scale (before the cast pass), mode 1 turns the scale into scale_inv =
+// 1 / scale (after it), mode 2 turns the amax into scale_inv directly.
+__global__ void scales_kernel(float *sinv_row, int64_t n_row, float *sinv_col, int64_t n_col, float fmax, int margin,
+                              int mode)
 {
     const int64_t total = n_row + n_col;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
         float *p = i < n_row ? sinv_row + i : sinv_col + (i - n_row);
-        *p = recip_rn(scale_from_amax(*p, fmax, margin));
+        const float v = *p;
+        *p = mode == 0 ? scale_from_amax(v, fmax, margin)
+                       : (mode == 1 ? recip_rn(v) : recip_rn(scale_from_amax(v, fmax, margin)));
     }
 }
 
@@ -499,16 +650,47 @@ static fp8_status_t run_quantize(QArgs a, int kind, int layouts, cudaStream_t st
     if (n_row && cudaMemsetAsync(a.sinv_row, 0, sizeof(float) * n_row, st) != cudaSuccess) return cuda_fail();
     if (n_col && cudaMemsetAsync(a.sinv_col, 0, sizeof(float) * n_col, st) != cudaSuccess) return cuda_fail();
     if (a.amax_out && cudaMemsetAsync(a.amax_out, 0, sizeof(float), st) != cudaSuccess) return cuda_fail();
-    {
+    if (!a.offsets) {
         auto k = amax_kernel<RB, 1>;
-        k<<<blocks_for(k, group_smem, n_tiles, a.offsets != nullptr), QT_THREADS, group_smem, st>>>(a);
+        k<<<blocks_for(k, group_smem, n_tiles, false), QT_THREADS, group_smem, st>>>(a);
+        if ((s = check_launch()) != FP8_OK) return s;
+    } else {
+        // pass 1 works on 32-row blocks for both layouts of the row space
+        QArgs b = a;
+        b.n_row_blocks = a.offsets ? a.n_row_blocks * RB / 32 : (a.rows + 31) / 32;
+        // the largest super tile that still gives about 6 blocks per SM
+        const int64_t target = 6LL * num_sms();
+        b.sup_blocks = SUP_BLOCKS;
+        b.sup_chunks = SUP_CHUNKS;
+        auto n_super_of = [&](const QArgs &q) {
+            return ((q.n_row_blocks + q.sup_blocks - 1) / q.sup_blocks) *
+                   ((q.n_col_chunks + q.sup_chunks - 1) / q.sup_chunks);
+        };
+        while (n_super_of(b) < target && (b.sup_blocks > 1 || b.sup_chunks > 1)) {
+            if (b.sup_chunks > 2 || b.sup_blocks == 1)
+                b.sup_chunks /= 2;
+            else
+                b.sup_blocks /= 2;
+        }
+        const int64_t n_super = n_super_of(b);
+        rowcol_amax_kernel<<<(unsigned)(n_super < 1 ? 1 : (n_super < INT32_MAX ? n_super : INT32_MAX)), QT_THREADS,
+                             group_smem, st>>>(b);
+        if ((s = check_launch()) != FP8_OK) return s;
+    }
+    const int64_t total = n_row + n_col;
+    const int sgrid = (int)((total + 255) / 256 < 4096 ? ((total + 255) / 256 > 0 ? (total + 255) / 256 : 1) : 4096);
+    // grouped tensors: turn the amaxes into scales once (a grouped tile is
+    // small, so per-tile divisions would cost more than one extra launch);
+    // plain tensors: the cast pass divides per tile and saves the launch
+    a.scales_ready = a.offsets != nullptr;
+    if (a.scales_ready && total > 0) {
+        scales_kernel<<<sgrid, 256, 0, st>>>(a.sinv_row, n_row, a.sinv_col, n_col, fp8_max_of(FMT), a.margin, 0);
         if ((s = check_launch()) != FP8_OK) return s;
     }
     if ((s = launch_cast<FMT, RB, 1, false>(a, layouts, group_smem, st)) != FP8_OK) return s;
-    const int64_t total = n_row + n_col;
     if (total > 0) {
-        const int grid = (int)((total + 255) / 256 < 4096 ? (total + 255) / 256 : 4096);
-        finalize_rowwise_kernel<<<grid, 256, 0, st>>>(a.sinv_row, n_row, a.sinv_col, n_col, fp8_max_of(FMT), a.margin);
+        scales_kernel<<<sgrid, 256, 0, st>>>(a.sinv_row, n_row, a.sinv_col, n_col, fp8_max_of(FMT), a.margin,
+                                             a.scales_ready ? 1 : 2);
         return check_launch();
     }
     return FP8_OK;
@@ -569,6 +751,9 @@ extern "C" fp8_status_t fp8_quantize(const void *x_bf16, int64_t rows, int64_t c
     a.G = group_offsets ? num_groups : 0;
     a.margin = recipe->margin;
     a.n_col_chunks = (cols + QT_COLS - 1) / QT_COLS;
+    a.scales_ready = 0;
+    a.sup_blocks = SUP_BLOCKS;
+    a.sup_chunks = SUP_CHUNKS;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
     if (group_offsets) {
