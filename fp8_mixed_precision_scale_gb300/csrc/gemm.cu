@@ -227,6 +227,84 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams &p, int64_t t, co
     return ti;
 }
 
+// Epilogue of one finished tile for one warp: TMEM lane quarter q (rows
+// q*32 .. q*32+31 of the tile), column half `half` (128 columns).  Reads the
+// accumulator at TMEM column `acc_col`, applies the row / column scales,
+// converts to bf16 and stores through the warp's shared staging block.
+__device__ __forceinline__ void epilogue_tile(const GemmParams &p, const TileInfo &ti, uint32_t tmem_base,
+                                              uint32_t acc_col, int q, int half, int lane, uint8_t *stage)
+{
+    const int64_t gr = ti.row0 + q * 32 + lane;
+    const bool row_ok = gr < ti.row_end;
+    const int64_t cbeg = ti.col0 + half * (BN / 2);
+    const int64_t cend = min(cbeg + BN / 2, ti.col_end);
+    const float sa_v = row_ok ? (p.sa_per_row ? __ldg(p.sa + ti.sa_base + gr) : __ldg(p.sa)) : 0.0f;
+    const float sb0 = p.sb_per_row ? 0.0f : __ldg(p.sb);
+    // two 32-column chunks per round: both TMEM loads are in flight
+    // before the first wait
+    for (int ch = 0; ch < BN / 64; ch += 2) {
+        const int64_t c0 = cbeg + ch * 32;
+        if (c0 >= cend) break;  // warp-uniform
+        uint32_t r[2][32];
+        const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) +
+                               acc_col + (uint32_t)(half * (BN / 2) + ch * 32);
+        tmem_ld_32x32b_x32(taddr, r[0]);
+        tmem_ld_32x32b_x32(taddr + 32, r[1]);
+        // column scales: lane j holds the scale of column c + j; the
+        // other lanes read it by shuffle (one coalesced load per chunk)
+        float sbl[2] = {sb0, sb0};
+        if (p.sb_per_row) {
+#pragma unroll
+            for (int u = 0; u < 2; u++) {
+                const int64_t cc = c0 + u * 32 + lane;
+                sbl[u] = cc < cend ? __ldg(p.sb + ti.sb_base + cc) : 0.0f;
+            }
+        }
+        tmem_ld_wait();
+#pragma unroll
+        for (int u = 0; u < 2; u++) {
+            const int64_t cu = c0 + u * 32;
+            if (cu >= cend) break;  // warp-uniform
+            uint32_t packed[16];
+#pragma unroll
+            for (int j = 0; j < 16; j++) {
+                const float sb_lo = __shfl_sync(0xffffffffu, sbl[u], 2 * j);
+                const float sb_hi = __shfl_sync(0xffffffffu, sbl[u], 2 * j + 1);
+                const float lo = __uint_as_float(r[u][2 * j]) * sa_v * sb_lo;
+                const float hi = __uint_as_float(r[u][2 * j + 1]) * sa_v * sb_hi;
+                packed[j] = pack_bf16x2(lo, hi);
+            }
+            // transpose through shared memory so that each store
+            // instruction writes 8 rows x 64 contiguous bytes (whole
+            // sectors) instead of 32 rows x 16 bytes
+#pragma unroll
+            for (int g = 0; g < 4; g++)
+                *reinterpret_cast<uint4 *>(stage + lane * SmemLayout::stage_pitch + g * 16) =
+                    make_uint4(packed[4 * g], packed[4 * g + 1], packed[4 * g + 2], packed[4 * g + 3]);
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                const int rr = i * 8 + (lane >> 2), seg = lane & 3;
+                const uint4 v =
+                    *reinterpret_cast<const uint4 *>(stage + rr * SmemLayout::stage_pitch + seg * 16);
+                const int64_t row = ti.row0 + q * 32 + rr;
+                const int64_t c = cu + seg * 8;
+                if (row < ti.row_end && c < cend) {
+                    uint16_t *dst = p.C + ti.c_base + row * p.ldc + c;
+                    if (p.c_vec16 && c + 8 <= cend) {
+                        *reinterpret_cast<uint4 *>(dst) = v;
+                    } else {
+                        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                        for (int j = 0; j < 8 && c + j < cend; j++)
+                            dst[j] = (uint16_t)(w[j / 2] >> (16 * (j & 1)));
+                    }
+                }
+            }
+            __syncwarp();
+        }
+    }
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmParams p,
@@ -386,71 +464,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             }
             if (!mbar_wait_bounded(&tfull[acc], acc_phase, WAIT_LIMIT_NS, p.err, ERR_EPILOGUE_WAIT)) break;
             tc_fence_after();
-            const float sa_v = row_ok ? (p.sa_per_row ? __ldg(p.sa + ti.sa_base + gr) : __ldg(p.sa)) : 0.0f;
-            const float sb0 = p.sb_per_row ? 0.0f : __ldg(p.sb);
-            // two 32-column chunks per round: both TMEM loads are in flight
-            // before the first wait
-            for (int ch = 0; ch < BN / 64; ch += 2) {
-                const int64_t c0 = cbeg + ch * 32;
-                if (c0 >= cend) break;  // warp-uniform
-                uint32_t r[2][32];
-                const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) +
-                                       (uint32_t)(acc * BN + half * (BN / 2) + ch * 32);
-                tmem_ld_32x32b_x32(taddr, r[0]);
-                tmem_ld_32x32b_x32(taddr + 32, r[1]);
-                // column scales: lane j holds the scale of column c + j; the
-                // other lanes read it by shuffle (one coalesced load per chunk)
-                float sbl[2] = {sb0, sb0};
-                if (p.sb_per_row) {
-#pragma unroll
-                    for (int u = 0; u < 2; u++) {
-                        const int64_t cc = c0 + u * 32 + lane;
-                        sbl[u] = cc < cend ? __ldg(p.sb + ti.sb_base + cc) : 0.0f;
-                    }
-                }
-                tmem_ld_wait();
-#pragma unroll
-                for (int u = 0; u < 2; u++) {
-                    const int64_t cu = c0 + u * 32;
-                    if (cu >= cend) break;  // warp-uniform
-                    uint32_t packed[16];
-#pragma unroll
-                    for (int j = 0; j < 16; j++) {
-                        const float sb_lo = __shfl_sync(0xffffffffu, sbl[u], 2 * j);
-                        const float sb_hi = __shfl_sync(0xffffffffu, sbl[u], 2 * j + 1);
-                        const float lo = __uint_as_float(r[u][2 * j]) * sa_v * sb_lo;
-                        const float hi = __uint_as_float(r[u][2 * j + 1]) * sa_v * sb_hi;
-                        packed[j] = pack_bf16x2(lo, hi);
-                    }
-                    // transpose through shared memory so that each store
-                    // instruction writes 8 rows x 64 contiguous bytes (whole
-                    // sectors) instead of 32 rows x 16 bytes
-#pragma unroll
-                    for (int g = 0; g < 4; g++)
-                        *reinterpret_cast<uint4 *>(stage + lane * SmemLayout::stage_pitch + g * 16) =
-                            make_uint4(packed[4 * g], packed[4 * g + 1], packed[4 * g + 2], packed[4 * g + 3]);
-                    __syncwarp();
-#pragma unroll
-                    for (int i = 0; i < 4; i++) {
-                        const int rr = i * 8 + (lane >> 2), seg = lane & 3;
-                        const uint4 v =
-                            *reinterpret_cast<const uint4 *>(stage + rr * SmemLayout::stage_pitch + seg * 16);
-                        const int64_t row = ti.row0 + q * 32 + rr;
-                        const int64_t c = cu + seg * 8;
-                        if (row < ti.row_end && c < cend) {
-                            uint16_t *dst = p.C + ti.c_base + row * p.ldc + c;
-                            if (p.c_vec16 && c + 8 <= cend) {
-                                *reinterpret_cast<uint4 *>(dst) = v;
-                            } else {
-                                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-                                for (int j = 0; j < 8 && c + j < cend; j++)
-                                    dst[j] = (uint16_t)(w[j / 2] >> (16 * (j & 1)));
-                            }
-                        }
-                    }
-                    __syncwarp();
-                }
-            }
+            epilogue_tile(p, ti, tmem_base, (uint32_t)(acc * BN), q, half, lane, stage);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[acc]);
@@ -467,6 +481,198 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Dense GEMM on CTA pairs: 256 x 256 tiles computed by 2-SM tcgen05 MMAs.
+//
+// The two CTAs of a cluster each stage half of the A tile (128 rows) and
+// half of the B tile (128 rows) at the same shared-memory offsets; the even
+// CTA's single MMA thread issues tcgen05.mma.cta_group::2 (M = 256, N = 256),
+// which reads both CTAs' halves and leaves each CTA's 128 rows of D in its
+// own TMEM.  Per SM this halves the shared-memory footprint of B, so a stage
+// is 32 KB and the ring holds 6 stages.  Both CTAs' TMA loads count on the
+// even CTA's "full" barrier; the MMA thread's commits are multicast to both
+// CTAs ("empty" frees a stage in both, "tmem full" starts both epilogues);
+// both CTAs' epilogue warps arrive on the even CTA's "tmem empty".
+// ---------------------------------------------------------------------------
+constexpr int STAGES2 = 6;
+constexpr int A2_STAGE_BYTES = 128 * BK;
+constexpr int B2_STAGE_BYTES = 128 * BK;
+
+struct SmemLayout2 {
+    static constexpr int a_off = 0;
+    static constexpr int b_off = STAGES2 * A2_STAGE_BYTES;
+    static constexpr int bar_off = b_off + STAGES2 * B2_STAGE_BYTES;
+    static constexpr int n_bars = 2 * STAGES2 + 2 + 2 + 1;
+    static constexpr int slot_off = bar_off + n_bars * 8;
+    static constexpr int stage_off = (slot_off + 16 + 127) / 128 * 128;
+    static constexpr int total = stage_off + 8 * SmemLayout::stage_warp_bytes;
+};
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
+    fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                         GemmParams p, uint32_t idesc)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sA = smem + SmemLayout2::a_off;
+    uint8_t *sB = smem + SmemLayout2::b_off;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + SmemLayout2::bar_off);
+    uint64_t *full = bars;
+    uint64_t *empty = bars + STAGES2;
+    uint64_t *tfull = bars + 2 * STAGES2;
+    uint64_t *tempty = tfull + 2;
+    uint64_t *done = tempty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + SmemLayout2::slot_off);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int64_t cluster = blockIdx.x >> 1, n_clusters = gridDim.x >> 1;
+
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < STAGES2; s++) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; b++) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 16);  // 8 epilogue warps in each of the two CTAs
+        }
+        mbar_init(done, 1);
+        fence_barrier_init();
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB);
+    }
+    if (warp == 1) tmem_alloc_pair(tmem_slot, TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // both CTAs' barriers are initialised before any remote use
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int64_t total = p.total_tiles;
+    const int num_m2 = (int)((p.M + 255) / 256);
+
+    auto coords = [&](int64_t t, int &mb, int &nb) {
+        if (p.m_fastest) {
+            mb = (int)(t % num_m2);
+            nb = (int)(t / num_m2);
+        } else {
+            nb = (int)(t % p.num_n_blk);
+            mb = (int)(t / p.num_n_blk);
+        }
+    };
+
+    if (warp == 0 && lane == 0) {
+        // ---------------- TMA producer (both CTAs) ----------------
+        int stage = 0;
+        uint32_t phase = 0;
+        int issued_parity[STAGES2];
+        for (int s = 0; s < STAGES2; s++) issued_parity[s] = -1;
+        bool ok = true;
+        for (int64_t t = cluster; t < total && ok; t += n_clusters) {
+            int mb, nb;
+            coords(t, mb, nb);
+            for (int kb = 0; kb < p.num_k_blk; kb++) {
+                if (!mbar_wait_bounded(&empty[stage], phase ^ 1, WAIT_LIMIT_NS, p.err, ERR_PRODUCER_WAIT)) {
+                    ok = false;
+                    break;
+                }
+                if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (A2_STAGE_BYTES + B2_STAGE_BYTES));
+                const uint32_t full_leader = mapa_shared(smem_u32(&full[stage]), 0);
+                tma_load_2d_pair(sA + stage * A2_STAGE_BYTES, &tmA, kb * BK, mb * 256 + (int)rank * 128, full_leader);
+                tma_load_2d_pair(sB + stage * B2_STAGE_BYTES, &tmB, kb * BK, nb * 256 + (int)rank * 128, full_leader);
+                issued_parity[stage] = (int)phase;
+                if (++stage == STAGES2) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+        }
+        // the even CTA's full barriers count both CTAs' copies: draining them
+        // there covers the pair (the odd CTA waits at the final cluster barrier)
+        if (leader)
+            for (int s = 0; s < STAGES2; s++)
+                if (issued_parity[s] >= 0)
+                    mbar_wait_bounded(&full[s], (uint32_t)issued_parity[s], WAIT_LIMIT_NS, p.err, ERR_TEARDOWN_WAIT);
+    } else if (warp == 1 && lane == 0 && leader) {
+        // ---------------- MMA issuer (even CTA) ----------------
+        int stage = 0;
+        uint32_t phase = 0;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool ok = true;
+        for (int64_t t = cluster; t < total && ok; t += n_clusters) {
+            if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1, WAIT_LIMIT_NS, p.err, ERR_MMA_WAIT)) break;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+            for (int kb = 0; kb < p.num_k_blk; kb++) {
+                if (!mbar_wait_bounded(&full[stage], phase, WAIT_LIMIT_NS, p.err, ERR_MMA_WAIT)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a_addr = smem_u32(sA + stage * A2_STAGE_BYTES);
+                const uint32_t b_addr = smem_u32(sB + stage * B2_STAGE_BYTES);
+#pragma unroll
+                for (int k = 0; k < BK / UMMA_K; k++)
+                    mma_f8f6f4_pair(d_tmem, smem_desc_k128_sw128(a_addr + k * UMMA_K),
+                                    smem_desc_k128_sw128(b_addr + k * UMMA_K), idesc, (kb | k) != 0);
+                mma_commit_pair(&empty[stage], 0x3);
+                if (++stage == STAGES2) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+            if (!ok) break;
+            mma_commit_pair(&tfull[acc], 0x3);
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1;
+            }
+        }
+        mma_commit_pair_local(done);
+        mbar_wait_bounded(done, 0, WAIT_LIMIT_NS, p.err, ERR_TEARDOWN_WAIT);
+    } else if (warp >= 2) {
+        // ---------------- epilogue (both CTAs) ----------------
+        const int q = warp & 3;
+        const int half = (warp - 2) >> 2;
+        uint8_t *stage = smem + SmemLayout2::stage_off + (warp - 2) * SmemLayout::stage_warp_bytes;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int64_t t = cluster; t < total; t += n_clusters) {
+            int mb, nb;
+            coords(t, mb, nb);
+            TileInfo ti;
+            ti.row0 = (int64_t)mb * 256 + rank * 128;
+            ti.row_end = p.M;
+            ti.col0 = (int64_t)nb * BN;
+            ti.col_end = p.N;
+            ti.c_base = 0;
+            ti.sa_base = 0;
+            ti.sb_base = 0;
+            if (!mbar_wait_bounded(&tfull[acc], acc_phase, WAIT_LIMIT_NS, p.err, ERR_EPILOGUE_WAIT)) break;
+            tc_fence_after();
+            epilogue_tile(p, ti, tmem_base, (uint32_t)(acc * BN), q, half, lane, stage);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // no CTA leaves while its peer may still touch its shared memory or TMEM
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, TMEM_COLS);
     }
 }
 
@@ -524,6 +730,43 @@ static fp8_status_t launch_gemm(const CUtensorMap &ma, const CUtensorMap &mb, co
     return check_launch();
 }
 
+static fp8_status_t launch_gemm_pair(const CUtensorMap &ma, const CUtensorMap &mb, const GemmParams &p, int fa,
+                                     int fb, cudaStream_t st)
+{
+    const size_t smem = 1024 + SmemLayout2::total;
+    cudaError_t e = cudaFuncSetAttribute(fp8_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return cuda_fail_with(e);
+    // as many pairs as can be resident at once, never more than tiles
+    static int max_pairs[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && max_pairs[dev] == 0) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * (num_sms() / 2));
+        cfg.blockDim = dim3(GEMM_THREADS);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = 2;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, fp8_gemm_pair_kernel, &cfg) != cudaSuccess || n < 1) {
+            cudaGetLastError();
+            n = num_sms() / 2;
+        }
+        max_pairs[dev] = n;
+    }
+    int64_t pairs = (dev >= 0 && dev < 64) ? max_pairs[dev] : num_sms() / 2;
+    if (pairs > p.total_tiles) pairs = p.total_tiles;
+    if (pairs < 1) pairs = 1;
+    const uint32_t idesc = idesc_f8f6f4(fa, fb, 256, BN);
+    fp8_gemm_pair_kernel<<<(unsigned)(2 * pairs), GEMM_THREADS, smem, st>>>(ma, mb, p, idesc);
+    return check_launch();
+}
+
 static bool gemm_format_ok(int f) { return f == FP8_E4M3FN || f == FP8_E5M2; }
 
 }  // namespace fp8gb
@@ -569,9 +812,18 @@ extern "C" fp8_status_t fp8_scaled_gemm(const uint8_t *A, int fa, int64_t lda, c
     p.G = 0;
 
     CUtensorMap ma, mb;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (M > 128) {
+        // CTA pairs with 256 x 256 tiles
+        const int64_t num_m2 = (M + 255) / 256;
+        p.total_tiles = num_m2 * p.num_n_blk;
+        p.m_fastest = M <= N;
+        if (!make_map(&ma, A, M, K, lda, 128) || !make_map(&mb, B, N, K, ldb, 128)) return FP8_ERR_CUDA;
+        return launch_gemm_pair(ma, mb, p, fa, fb, st);
+    }
     if (!make_map(&ma, A, M, K, lda, BM) || !make_map(&mb, B, N, K, ldb, BN)) return FP8_ERR_CUDA;
     const int64_t grid = p.total_tiles < num_sms() ? p.total_tiles : num_sms();
-    return launch_gemm<MODE_DENSE>(ma, mb, p, fa, fb, grid, static_cast<cudaStream_t>(stream));
+    return launch_gemm<MODE_DENSE>(ma, mb, p, fa, fb, grid, st);
 }
 
 extern "C" fp8_status_t fp8_grouped_gemm(int mode, const uint8_t *A, int fa, const uint8_t *B, int fb,
