@@ -62,14 +62,31 @@ __device__ __forceinline__ float recip_rn(float s) { return __fdiv_rn(1.0f, s); 
 // FP8 conversion: saturating, round-to-nearest-even, two fp32 at a time.
 // Result: low byte = lo, high byte = hi.
 // ---------------------------------------------------------------------------
+// e4m3fnuz (bias 8) from the e4m3fn conversion: fnuz code c is worth half
+// of e4m3fn code c for every finite code, so fnuz(v) = e4m3fn(2 v) (doubling
+// is exact and preserves the rounding decision) with the format's own rules
+// on top: |v| above 232 (the tie between 224 and 240 rounds to the even code
+// 0x7E) gives +-240 = 0x7F / 0xFF, which e4m3fn reserves for NaN; NaN gives
+// the single fnuz NaN 0x80; and a negative zero becomes the unsigned zero.
+__device__ __forceinline__ uint32_t fnuz_fix(uint32_t code, float v)
+{
+    if (v != v) return 0x80u;
+    if (fabsf(v) > 232.0f) return v < 0.0f ? 0xFFu : 0x7Fu;
+    return code == 0x80u ? 0x00u : code;
+}
+
 template <int FMT>
 __device__ __forceinline__ uint32_t cvt2(float lo, float hi)
 {
     unsigned short r;
-    if constexpr (FMT == FP8_E5M2)
+    if constexpr (FMT == FP8_E5M2) {
         asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-    else
+    } else if constexpr (FMT == FP8_E4M3FNUZ) {
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi * 2.0f), "f"(lo * 2.0f));
+        return fnuz_fix(r & 0xFFu, lo) | (fnuz_fix(r >> 8, hi) << 8);
+    } else {
         asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    }
     return (uint32_t)r;
 }
 

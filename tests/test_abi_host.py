@@ -83,7 +83,7 @@ def test_quantize_validation(lib):
     assert q_call(lib, rows=-1) == INVALID
     assert q_call(lib, cols=0) == INVALID
     assert q_call(lib, ld_x=32) == INVALID
-    assert q_call(lib, fmt=2) == UNSUPPORTED          # e4m3fnuz is oracle-only
+    assert q_call(lib, fmt=3) == INVALID
     assert q_call(lib, fmt=7) == INVALID
     assert q_call(lib, kind=3) == INVALID
     assert q_call(lib, margin=-1) == INVALID

@@ -319,3 +319,34 @@ def test_quantize_grouped_large(orc):
     off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
     x = gen_x((int(off[-1]), 4096), seed=42)
     compare(orc, x, 0, 2, offsets=off, what="grouped multi-chunk")
+
+
+@pytest.mark.parametrize("fmt", [0, 1, 2])
+@pytest.mark.parametrize("scale", [1.0, 3.5, 2.0 ** -20, 448.0 / 3.0, 1e30])
+def test_cast_every_bf16_pattern(orc, fmt, scale):
+    """Every bf16 bit pattern (NaN, Inf, subnormals, both zeros included),
+    cast with a stored scale, against the oracle's element-wise encoder."""
+    pats = torch.arange(65536, dtype=torch.int32).to(torch.int16).view(torch.bfloat16).reshape(512, 128)
+    q, _ = run_gpu(pats, fmt, 0, scale=scale)
+    exp = orc.cast_points(bits(pats), np.float32(scale), fmt).reshape(512, 128)
+    assert_codes_equal(q.q_row.cpu().numpy(), exp, fmt, f"patterns f{fmt} s{scale}")
+    assert_codes_equal(q.q_colT.cpu().numpy()[:, :512], exp.T, fmt, f"patterns colT f{fmt} s{scale}")
+
+
+@pytest.mark.parametrize("kind", [0, 1, 2])
+@pytest.mark.parametrize("shape", [(37, 136), (300, 520)])
+def test_quantize_fnuz(orc, kind, shape):
+    """e4m3fnuz (max 240, no negative zero, single NaN) for every recipe."""
+    x = gen_x(shape, seed=shape[0] + kind, scale=0.5)
+    compare(orc, x, 2, kind, scale=100.0, amax0=0.1, what=f"fnuz {shape} k{kind}")
+
+
+def test_quantize_fnuz_grouped_and_special(orc):
+    g = torch.Generator().manual_seed(8)
+    x = synth.randomize_special(gen_x((120, 136), seed=10), g, frac=0.03)
+    x[3, 5] = float("nan")
+    for kind in (0, 1, 2):
+        compare(orc, x, 2, kind, scale=7.0, what=f"fnuz special k{kind}")
+    sizes = [5, 0, 33, 1, 0, 40]
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    compare(orc, gen_x((int(off[-1]), 136), seed=12), 2, 2, offsets=off, what="fnuz grouped")
