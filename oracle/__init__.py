@@ -11,7 +11,7 @@ Sources of each definition are cited in ``fp8_oracle.c``:
     algorithm.
   * "FP8 Training on MI300X" ("Discovered AMD FP8 dtype difference", "Patched
     nanochat/fp8.py"): E4M3 forward / E5M2 backward, e4m3fn max 448 against
-    e4m3fnuz max 240.
+    e4m3fnuz max 240; float8_e5m2fnuz as AMD's backward format.
   * "How PyTorch FP8 Optimizations on AMD GPUs ..." (What Happened) and "FP8
     Training on AMD GPUs with TorchTitan and TorchAO": rowwise scaling,
     colwise scales with a transposed layout, grouped GEMM for MoE.
@@ -25,7 +25,7 @@ import threading
 
 import numpy as np
 
-E4M3FN, E5M2, E4M3FNUZ = 0, 1, 2
+E4M3FN, E5M2, E4M3FNUZ, E5M2FNUZ = 0, 1, 2, 3
 DELAYED, TENSORWISE, ROWWISE = 0, 1, 2
 MOST_RECENT, MAX = 0, 1
 LAYOUT_ROW, LAYOUT_COLT = 1, 2

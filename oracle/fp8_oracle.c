@@ -8,13 +8,16 @@
  *
  * What it computes, and where that comes from:
  *
- *  - FP8 formats e4m3fn (max 448), e5m2 (max 57344) and e4m3fnuz (max 240,
- *    one NaN code, no infinities, no negative zero).  The maxima and the fnuz
- *    conventions are stated on "FP8 Training on MI300X" (section "Discovered
- *    AMD FP8 dtype difference") and on "FP8 Training on AMD GPUs with
- *    TorchTitan and TorchAO" (the question "Why does FP8 training on AMD GPUs
- *    give silently wrong results ...").  The bit layouts (sign, exponent,
- *    mantissa, bias) are the public OCP 8-bit float definitions.
+ *  - FP8 formats e4m3fn (max 448), e5m2 (max 57344), e4m3fnuz (max 240) and
+ *    e5m2fnuz (max 57344); the two fnuz formats have one NaN code (0x80), no
+ *    infinities and no negative zero, and an exponent bias one above their fn
+ *    counterparts.  The maxima and the fnuz conventions are stated on "FP8
+ *    Training on MI300X" (section "Discovered AMD FP8 dtype difference", which
+ *    also names float8_e5m2fnuz as AMD's backward format) and on "FP8 Training
+ *    on AMD GPUs with TorchTitan and TorchAO" (the question "Why does FP8
+ *    training on AMD GPUs give silently wrong results ...").  The bit layouts
+ *    (sign, exponent, mantissa, bias) are the public OCP 8-bit float
+ *    definitions.
  *  - The scaling recipe knobs (format, recipe, margin, amax history length,
  *    amax compute algorithm) are the ones listed on "FP8 training for Flux
  *    models" (section Configuration > Key FP8 Parameters).  The scale formula
@@ -56,6 +59,8 @@
 #define ORC_E4M3FN 0
 #define ORC_E5M2 1
 #define ORC_E4M3FNUZ 2
+#define ORC_E5M2FNUZ 3
+#define ORC_NUM_FMT 4
 
 #define ORC_DELAYED 0
 #define ORC_TENSORWISE 1
@@ -71,11 +76,13 @@
 /* FP8 codec                                                                 */
 /* ------------------------------------------------------------------------ */
 
-static int fmt_exp_bits(int fmt) { return fmt == ORC_E5M2 ? 5 : 4; }
-static int fmt_man_bits(int fmt) { return fmt == ORC_E5M2 ? 2 : 3; }
+static int fmt_is_fnuz(int fmt) { return fmt == ORC_E4M3FNUZ || fmt == ORC_E5M2FNUZ; }
+static int fmt_exp_bits(int fmt) { return (fmt == ORC_E5M2 || fmt == ORC_E5M2FNUZ) ? 5 : 4; }
+static int fmt_man_bits(int fmt) { return (fmt == ORC_E5M2 || fmt == ORC_E5M2FNUZ) ? 2 : 3; }
 static int fmt_bias(int fmt)
 {
     if (fmt == ORC_E5M2) return 15;
+    if (fmt == ORC_E5M2FNUZ) return 16;
     if (fmt == ORC_E4M3FNUZ) return 8;
     return 7;
 }
@@ -85,13 +92,14 @@ int orc_fp8_max_code(int fmt)
 {
     if (fmt == ORC_E5M2) return 0x7B;     /* 0 11110 11 = 1.75 * 2^15 */
     if (fmt == ORC_E4M3FNUZ) return 0x7F; /* 0 1111 111 = 1.875 * 2^7 (bias 8) */
+    if (fmt == ORC_E5M2FNUZ) return 0x7F; /* 0 11111 11 = 1.75 * 2^15 (bias 16) */
     return 0x7E;                          /* 0 1111 110 = 1.75 * 2^8 */
 }
 
 int orc_fp8_nan_code(int fmt)
 {
     if (fmt == ORC_E5M2) return 0x7E;
-    if (fmt == ORC_E4M3FNUZ) return 0x80;
+    if (fmt_is_fnuz(fmt)) return 0x80;
     return 0x7F;
 }
 
@@ -104,7 +112,7 @@ double orc_fp8_decode(int code, int fmt)
     int m = code & ((1 << mb) - 1);
     double mag;
 
-    if (fmt == ORC_E4M3FNUZ) {
+    if (fmt_is_fnuz(fmt)) {
         if (code == 0x80) return NAN; /* the only NaN; there is no -0 */
     } else if (fmt == ORC_E4M3FN) {
         if (e == 15 && m == 7) return NAN; /* 0x7F / 0xFF */
@@ -122,13 +130,13 @@ double orc_fp8_decode(int code, int fmt)
 }
 
 /* Magnitudes of codes 0 .. max_code, strictly increasing with the code. */
-static double g_mag[3][128];
+static double g_mag[ORC_NUM_FMT][128];
 static int g_mag_ready = 0;
 
 static void init_tables(void)
 {
     if (g_mag_ready) return;
-    for (int f = 0; f < 3; f++)
+    for (int f = 0; f < ORC_NUM_FMT; f++)
         for (int c = 0; c <= orc_fp8_max_code(f); c++) g_mag[f][c] = orc_fp8_decode(c, f);
     g_mag_ready = 1;
 }
@@ -172,7 +180,7 @@ int orc_fp8_encode(double v, int fmt)
                 mag = (lo % 2 == 0) ? lo : hi;
         }
     }
-    if (fmt == ORC_E4M3FNUZ && mag == 0) return 0x00; /* unsigned zero */
+    if (fmt_is_fnuz(fmt) && mag == 0) return 0x00; /* unsigned zero */
     return (neg << 7) | mag;
 }
 

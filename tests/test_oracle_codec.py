@@ -17,8 +17,10 @@ import torch
 from conftest import parse_value, read_golden
 from fp8_ref import PARAMS, is_inf_code, is_nan_code, ref_encode
 
-FMT = {"e4m3fn": 0, "e5m2": 1, "e4m3fnuz": 2}
-TORCH_DT = {0: torch.float8_e4m3fn, 1: torch.float8_e5m2, 2: torch.float8_e4m3fnuz}
+FMT = {"e4m3fn": 0, "e5m2": 1, "e4m3fnuz": 2, "e5m2fnuz": 3}
+TORCH_DT = {0: torch.float8_e4m3fn, 1: torch.float8_e5m2, 2: torch.float8_e4m3fnuz,
+            3: torch.float8_e5m2fnuz}
+ALL_FMTS = [0, 1, 2, 3]
 # --- tests -------------------------------------------------------------------
 
 def test_maxima_match_pages(orc):
@@ -37,7 +39,7 @@ def test_worked_codes(orc):
         assert orc.fp8_encode(parse_value(val), f) == int(code, 16), (name, val)
 
 
-@pytest.mark.parametrize("fmt", [0, 1, 2])
+@pytest.mark.parametrize("fmt", ALL_FMTS)
 def test_roundtrip_all_codes(orc, fmt):
     n_checked = 0
     for c in range(256):
@@ -53,10 +55,10 @@ def test_roundtrip_all_codes(orc, fmt):
             continue
         assert orc.fp8_encode(v, fmt) == c, hex(c)
         n_checked += 1
-    assert n_checked == {0: 254, 1: 248, 2: 255}[fmt]
+    assert n_checked == {0: 254, 1: 248, 2: 255, 3: 255}[fmt]
 
 
-@pytest.mark.parametrize("fmt", [0, 1, 2])
+@pytest.mark.parametrize("fmt", ALL_FMTS)
 def test_decode_strictly_monotone(orc, fmt):
     vals = [orc.fp8_decode(c, fmt) for c in range(orc.fp8_max_code(fmt) + 1)]
     assert vals[0] == 0.0
@@ -66,7 +68,7 @@ def test_decode_strictly_monotone(orc, fmt):
         assert orc.fp8_decode(0x80 | c, fmt) == -vals[c]
 
 
-@pytest.mark.parametrize("fmt", [0, 1, 2])
+@pytest.mark.parametrize("fmt", ALL_FMTS)
 def test_decode_matches_torch(orc, fmt):
     codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
     tv = codes.view(TORCH_DT[fmt]).to(torch.float64).numpy()
@@ -92,7 +94,7 @@ def _sweep_values():
     return np.concatenate(vals)
 
 
-@pytest.mark.parametrize("fmt", [0, 1, 2])
+@pytest.mark.parametrize("fmt", ALL_FMTS)
 def test_encode_matches_torch_cast(orc, fmt):
     """torch's fp8 cast of clamp(v, -max, max) equals the saturating encode."""
     v = _sweep_values()
@@ -106,13 +108,13 @@ def test_encode_matches_torch_cast(orc, fmt):
     idx = rng.choice(v.size, size=60_000, replace=False)
     for i in idx:
         oc = orc.fp8_encode(float(v[i]), fmt)
-        if fmt == 2 and oc == 0:
+        if fmt in (2, 3) and oc == 0:
             assert tc[i] in (0x00,), (v[i], tc[i])
         else:
             assert oc == tc[i], (fmt, float(v[i]), hex(oc), hex(tc[i]))
 
 
-@pytest.mark.parametrize("fmt", [0, 1, 2])
+@pytest.mark.parametrize("fmt", ALL_FMTS)
 def test_encode_matches_independent_encoder(orc, fmt):
     v = _sweep_values()
     rng = np.random.default_rng(100 + fmt)
@@ -122,7 +124,7 @@ def test_encode_matches_independent_encoder(orc, fmt):
         assert orc.fp8_encode(x, fmt) == ref_encode(x, fmt), (fmt, x)
 
 
-@pytest.mark.parametrize("fmt", [0, 1, 2])
+@pytest.mark.parametrize("fmt", ALL_FMTS)
 def test_all_bf16_cast_points_match_independent(orc, fmt):
     """Every bf16 pattern through the element-wise cast (bf16 -> fp32 -> * scale)."""
     bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
@@ -141,10 +143,11 @@ def test_all_bf16_cast_points_match_independent(orc, fmt):
 
 
 def test_nan_and_inf_inputs(orc):
-    for fmt in (0, 1, 2):
+    for fmt in ALL_FMTS:
         assert is_nan_code(orc.fp8_encode(float("nan"), fmt), fmt)
         assert orc.fp8_encode(float("inf"), fmt) == orc.fp8_max_code(fmt)
         assert orc.fp8_encode(float("-inf"), fmt) == 0x80 | orc.fp8_max_code(fmt)
     assert orc.fp8_encode(-0.0, 0) == 0x80
     assert orc.fp8_encode(-0.0, 1) == 0x80
     assert orc.fp8_encode(-0.0, 2) == 0x00
+    assert orc.fp8_encode(-0.0, 3) == 0x00
