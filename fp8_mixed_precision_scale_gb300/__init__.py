@@ -26,7 +26,7 @@ from dataclasses import dataclass
 
 import torch
 
-E4M3FN, E5M2, E4M3FNUZ = 0, 1, 2
+E4M3FN, E5M2, E4M3FNUZ, E5M2FNUZ = 0, 1, 2, 3
 DELAYED, TENSORWISE, ROWWISE = 0, 1, 2
 MOST_RECENT, MAX = 0, 1
 LAYOUT_ROW, LAYOUT_COLT = 1, 2

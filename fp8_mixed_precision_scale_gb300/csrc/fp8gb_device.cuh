@@ -38,7 +38,7 @@ __device__ __forceinline__ void record_error(unsigned int *err, unsigned int bit
 // ---------------------------------------------------------------------------
 __host__ __device__ __forceinline__ float fp8_max_of(int fmt)
 {
-    return fmt == FP8_E5M2 ? 57344.0f : (fmt == FP8_E4M3FNUZ ? 240.0f : 448.0f);
+    return (fmt == FP8_E5M2 || fmt == FP8_E5M2FNUZ) ? 57344.0f : (fmt == FP8_E4M3FNUZ ? 240.0f : 448.0f);
 }
 
 __device__ __forceinline__ float pow2_neg(int margin)  // 2^-margin, 0 <= margin <= 126
@@ -75,6 +75,29 @@ __device__ __forceinline__ uint32_t fnuz_fix(uint32_t code, float v)
     return code == 0x80u ? 0x00u : code;
 }
 
+// e5m2fnuz (bias 16) likewise: fnuz code c is worth half of e5m2 code c, so
+// fnuz(v) = e5m2(2 v) while 2 v stays inside e5m2's finite range.  The top
+// fnuz binade [2^15, 57344] has no finite e5m2 counterpart at 2 v, so for
+// |v| >= 2^14 the code comes from e5m2(v / 2) two binades up (+8: two steps
+// of the 2-bit mantissa field); v / 2 is normal there, so the rounding is
+// the same.  Above 57344 (and +-Inf) it saturates; NaN gives 0x80; a
+// negative zero becomes the unsigned zero.
+__device__ __forceinline__ uint32_t e5m2_code(float v)
+{
+    unsigned short r;
+    asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(v));
+    return r & 0xFFu;
+}
+
+__device__ __forceinline__ uint32_t e5m2fnuz_fix(uint32_t code, float v)
+{
+    if (v != v) return 0x80u;
+    const float a = fabsf(v);
+    if (a > 57344.0f) return v < 0.0f ? 0xFFu : 0x7Fu;
+    if (a >= 16384.0f) return e5m2_code(v * 0.5f) + 8u;
+    return code == 0x80u ? 0x00u : code;
+}
+
 template <int FMT>
 __device__ __forceinline__ uint32_t cvt2(float lo, float hi)
 {
@@ -84,6 +107,9 @@ __device__ __forceinline__ uint32_t cvt2(float lo, float hi)
     } else if constexpr (FMT == FP8_E4M3FNUZ) {
         asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi * 2.0f), "f"(lo * 2.0f));
         return fnuz_fix(r & 0xFFu, lo) | (fnuz_fix(r >> 8, hi) << 8);
+    } else if constexpr (FMT == FP8_E5M2FNUZ) {
+        asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi * 2.0f), "f"(lo * 2.0f));
+        return e5m2fnuz_fix(r & 0xFFu, lo) | (e5m2fnuz_fix(r >> 8, hi) << 8);
     } else {
         asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
     }

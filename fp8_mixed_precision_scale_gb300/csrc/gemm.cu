@@ -778,7 +778,8 @@ extern "C" fp8_status_t fp8_scaled_gemm(const uint8_t *A, int fa, int64_t lda, c
                                         const float *sb, int sb_mode, void *C_bf16, int64_t ldc, void *stream)
 {
     if (!A || !B || !sa || !sb || !C_bf16) return FP8_ERR_INVALID_ARG;
-    if (fa == FP8_E4M3FNUZ || fb == FP8_E4M3FNUZ) return FP8_ERR_UNSUPPORTED;
+    if (fa == FP8_E4M3FNUZ || fb == FP8_E4M3FNUZ || fa == FP8_E5M2FNUZ || fb == FP8_E5M2FNUZ)
+        return FP8_ERR_UNSUPPORTED;
     if (!gemm_format_ok(fa) || !gemm_format_ok(fb)) return FP8_ERR_INVALID_ARG;
     if (M < 1 || N < 1 || K < 1 || lda < K || ldb < K || ldc < N) return FP8_ERR_INVALID_ARG;
     if ((sa_mode != FP8_SCALE_TENSOR && sa_mode != FP8_SCALE_PER_ROW) ||
@@ -832,7 +833,8 @@ extern "C" fp8_status_t fp8_grouped_gemm(int mode, const uint8_t *A, int fa, con
                                          int64_t ld_T, void *stream)
 {
     if (!A || !B || !sa || !sb || !C_bf16 || !group_offsets) return FP8_ERR_INVALID_ARG;
-    if (fa == FP8_E4M3FNUZ || fb == FP8_E4M3FNUZ) return FP8_ERR_UNSUPPORTED;
+    if (fa == FP8_E4M3FNUZ || fb == FP8_E4M3FNUZ || fa == FP8_E5M2FNUZ || fb == FP8_E5M2FNUZ)
+        return FP8_ERR_UNSUPPORTED;
     if (!gemm_format_ok(fa) || !gemm_format_ok(fb)) return FP8_ERR_INVALID_ARG;
     if (mode != FP8_GROUPED_M && mode != FP8_GROUPED_K && mode != FP8_GROUPED_M_BT) return FP8_ERR_INVALID_ARG;
     if (G < 1 || G > MAX_GROUPS || M_total < 0 || N < 1 || K < 1) return FP8_ERR_INVALID_ARG;

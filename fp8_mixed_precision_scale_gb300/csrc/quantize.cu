@@ -709,7 +709,8 @@ extern "C" fp8_status_t fp8_quantize(const void *x_bf16, int64_t rows, int64_t c
     // ---- validation (host only; nothing is launched on failure) ----
     if (!recipe || (!x_bf16 && rows > 0)) return FP8_ERR_INVALID_ARG;
     if (rows < 0 || cols < 1 || ld_x < cols) return FP8_ERR_INVALID_ARG;
-    if (fmt != FP8_E4M3FN && fmt != FP8_E5M2 && fmt != FP8_E4M3FNUZ) return FP8_ERR_INVALID_ARG;
+    if (fmt != FP8_E4M3FN && fmt != FP8_E5M2 && fmt != FP8_E4M3FNUZ && fmt != FP8_E5M2FNUZ)
+        return FP8_ERR_INVALID_ARG;
     if (recipe->kind < FP8_RECIPE_DELAYED || recipe->kind > FP8_RECIPE_ROWWISE) return FP8_ERR_INVALID_ARG;
     if (recipe->margin < 0 || recipe->margin > 64) return FP8_ERR_INVALID_ARG;
     if (layouts < 1 || layouts > 3) return FP8_ERR_INVALID_ARG;
@@ -761,10 +762,12 @@ extern "C" fp8_status_t fp8_quantize(const void *x_bf16, int64_t rows, int64_t c
         a.n_row_blocks = (padded_max + 31) / 32;
         if (fmt == FP8_E5M2) return run_quantize<FP8_E5M2, 32>(a, recipe->kind, layouts, st);
         if (fmt == FP8_E4M3FNUZ) return run_quantize<FP8_E4M3FNUZ, 32>(a, recipe->kind, layouts, st);
+        if (fmt == FP8_E5M2FNUZ) return run_quantize<FP8_E5M2FNUZ, 32>(a, recipe->kind, layouts, st);
         return run_quantize<FP8_E4M3FN, 32>(a, recipe->kind, layouts, st);
     }
     a.n_row_blocks = (rows + 63) / 64;
     if (fmt == FP8_E5M2) return run_quantize<FP8_E5M2, 64>(a, recipe->kind, layouts, st);
     if (fmt == FP8_E4M3FNUZ) return run_quantize<FP8_E4M3FNUZ, 64>(a, recipe->kind, layouts, st);
+    if (fmt == FP8_E5M2FNUZ) return run_quantize<FP8_E5M2FNUZ, 64>(a, recipe->kind, layouts, st);
     return run_quantize<FP8_E4M3FN, 64>(a, recipe->kind, layouts, st);
 }

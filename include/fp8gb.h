@@ -58,12 +58,13 @@ extern "C" {
 #endif
 
 /* FP8 formats.  e4m3fn: bias 7, max 448, NaN 0x7F/0xFF, no Inf.  e5m2: bias
- * 15, max 57344, IEEE-style Inf/NaN.  e4m3fnuz: bias 8, max 240, single NaN
- * 0x80, no Inf, no negative zero -- the AMD format ("FP8 Training on MI300X",
- * "Discovered AMD FP8 dtype difference").  fp8_quantize and
- * fp8_update_amax_history accept all three; the GEMMs take e4m3fn / e5m2
- * operands (FP8_ERR_UNSUPPORTED for fnuz). */
-typedef enum { FP8_E4M3FN = 0, FP8_E5M2 = 1, FP8_E4M3FNUZ = 2 } fp8_format_t;
+ * 15, max 57344, IEEE-style Inf/NaN.  e4m3fnuz: bias 8, max 240; e5m2fnuz:
+ * bias 16, max 57344; both fnuz formats have the single NaN 0x80, no Inf and
+ * no negative zero -- the AMD formats ("FP8 Training on MI300X", "Discovered
+ * AMD FP8 dtype difference": e4m3fnuz forward, e5m2fnuz backward).
+ * fp8_quantize and fp8_update_amax_history accept all four; the GEMMs take
+ * e4m3fn / e5m2 operands (FP8_ERR_UNSUPPORTED for fnuz). */
+typedef enum { FP8_E4M3FN = 0, FP8_E5M2 = 1, FP8_E4M3FNUZ = 2, FP8_E5M2FNUZ = 3 } fp8_format_t;
 
 /* Scaling recipes ("FP8 training for Flux models", fp8_recipe):
  *   DELAYED    cast with the stored per-tensor scale (from the amax history);
@@ -108,7 +109,7 @@ enum { FP8_GROUPED_M = 0, FP8_GROUPED_K = 1, FP8_GROUPED_M_BT = 2 };  /* grouped
  *
  *   x_bf16        [rows][ld_x] bf16, row-major; 16-byte aligned, ld_x % 8 == 0.
  *   rows, cols    rows >= 0, cols >= 1, cols % 8 == 0.
- *   fmt           FP8_E4M3FN, FP8_E5M2 or FP8_E4M3FNUZ.
+ *   fmt           FP8_E4M3FN, FP8_E5M2, FP8_E4M3FNUZ or FP8_E5M2FNUZ.
  *   recipe        kind and margin are used (see fp8_recipe_t).
  *   layouts       FP8_LAYOUT_ROW | FP8_LAYOUT_COLT (at least one).
  *   scale_in      DELAYED only: device fp32 [1], the stored scale used for the

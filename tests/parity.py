@@ -11,7 +11,7 @@ BF16_HALF_ULP_REL = 2.0 ** -8   # round-to-nearest into bf16 moves a value by at
 
 def nan_mask(codes: np.ndarray, fmt: int) -> np.ndarray:
     c = codes.astype(np.int32)
-    if fmt == 2:
+    if fmt in (2, 3):  # fnuz: the single NaN code
         return c == 0x80
     if fmt == 0:
         return (c & 0x7F) == 0x7F

@@ -182,7 +182,7 @@ def test_update_matches_oracle(orc, L, algo):
     hist[3, 0] = np.nan
     hist[4, :] = 0.0
     hist[5, 0] = 1e-44                       # scale overflows -> FLT_MAX
-    fmt = np.array([0, 1, 0, 1, 0, 0, 1, 2, 0], np.uint8)
+    fmt = np.array([0, 1, 0, 1, 0, 3, 1, 2, 3], np.uint8)
     scale = rng.uniform(0.5, 2, n).astype(np.float32)
     sinv = (1 / scale).astype(np.float32)
     cnt = np.zeros(n, np.int32)
@@ -321,7 +321,7 @@ def test_quantize_grouped_large(orc):
     compare(orc, x, 0, 2, offsets=off, what="grouped multi-chunk")
 
 
-@pytest.mark.parametrize("fmt", [0, 1, 2])
+@pytest.mark.parametrize("fmt", [0, 1, 2, 3])
 @pytest.mark.parametrize("scale", [1.0, 3.5, 2.0 ** -20, 448.0 / 3.0, 1e30])
 def test_cast_every_bf16_pattern(orc, fmt, scale):
     """Every bf16 bit pattern (NaN, Inf, subnormals, both zeros included),
@@ -333,20 +333,35 @@ def test_cast_every_bf16_pattern(orc, fmt, scale):
     assert_codes_equal(q.q_colT.cpu().numpy()[:, :512], exp.T, fmt, f"patterns colT f{fmt} s{scale}")
 
 
+@pytest.mark.parametrize("fmt", [2, 3])
 @pytest.mark.parametrize("kind", [0, 1, 2])
 @pytest.mark.parametrize("shape", [(37, 136), (300, 520)])
-def test_quantize_fnuz(orc, kind, shape):
-    """e4m3fnuz (max 240, no negative zero, single NaN) for every recipe."""
+def test_quantize_fnuz(orc, fmt, kind, shape):
+    """e4m3fnuz (max 240) and e5m2fnuz (max 57344): no negative zero, single
+    NaN, for every recipe."""
     x = gen_x(shape, seed=shape[0] + kind, scale=0.5)
-    compare(orc, x, 2, kind, scale=100.0, amax0=0.1, what=f"fnuz {shape} k{kind}")
+    compare(orc, x, fmt, kind, scale=100.0, amax0=0.1, what=f"fnuz{fmt} {shape} k{kind}")
 
 
-def test_quantize_fnuz_grouped_and_special(orc):
+@pytest.mark.parametrize("fmt", [2, 3])
+def test_quantize_fnuz_grouped_and_special(orc, fmt):
     g = torch.Generator().manual_seed(8)
     x = synth.randomize_special(gen_x((120, 136), seed=10), g, frac=0.03)
     x[3, 5] = float("nan")
     for kind in (0, 1, 2):
-        compare(orc, x, 2, kind, scale=7.0, what=f"fnuz special k{kind}")
+        compare(orc, x, fmt, kind, scale=7.0, what=f"fnuz{fmt} special k{kind}")
     sizes = [5, 0, 33, 1, 0, 40]
     off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
-    compare(orc, gen_x((int(off[-1]), 136), seed=12), 2, 2, offsets=off, what="fnuz grouped")
+    compare(orc, gen_x((int(off[-1]), 136), seed=12), fmt, 2, offsets=off, what=f"fnuz{fmt} grouped")
+
+
+def test_e5m2fnuz_top_binade(orc):
+    """Every bf16 value of e5m2fnuz's top binades (|v| in [2^13, 2^17)), the
+    range where the GPU encoder switches from e5m2(2v) to e5m2(v/2), plus the
+    saturation band above 57344."""
+    mags = torch.arange(0x4600, 0x4800, dtype=torch.int32)          # bf16 patterns 2^13 .. 2^17
+    pats = torch.cat([mags, mags | 0x8000]).to(torch.int16).view(torch.bfloat16).reshape(8, 128)
+    for scale in (1.0, 0.5, 2.0):
+        q, _ = run_gpu(pats, 3, 0, scale=scale)
+        exp = orc.cast_points(bits(pats), np.float32(scale), 3).reshape(8, 128)
+        assert_codes_equal(q.q_row.cpu().numpy(), exp, 3, f"top binade s{scale}")
