@@ -15,6 +15,9 @@ Sources of each definition are cited in ``fp8_oracle.c``:
   * "How PyTorch FP8 Optimizations on AMD GPUs ..." (What Happened) and "FP8
     Training on AMD GPUs with TorchTitan and TorchAO": rowwise scaling,
     colwise scales with a transposed layout, grouped GEMM for MoE.
+  * MXFP8 (the "mxfp8" recipe of the Flux page; MXFP8 grouped GEMM on the
+    TorchTitan/TorchAO page): the OCP Microscaling v1.0 definition -- blocks
+    of 32, E8M0 scale 2^(floor(log2 amax) - emax_elem).
 """
 from __future__ import annotations
 
@@ -85,6 +88,19 @@ def _load():
             lib.orc_grouped_gemm.restype = None
             lib.orc_grouped_gemm.argtypes = [i32, P, i32, P, i32, P, i32, i64, i64, i64, P, i32,
                                              P, i32, P, P, P, i64, P, P]
+            lib.orc_mx_emax.restype = i32
+            lib.orc_mx_emax.argtypes = [i32]
+            lib.orc_mx_scale_code.restype = i32
+            lib.orc_mx_scale_code.argtypes = [f64, i32]
+            lib.orc_e8m0_decode.restype = f64
+            lib.orc_e8m0_decode.argtypes = [i32]
+            lib.orc_padded_offsets_align.restype = i64
+            lib.orc_padded_offsets_align.argtypes = [P, i32, i64, P]
+            lib.orc_mx_quantize.restype = i32
+            lib.orc_mx_quantize.argtypes = [P, i64, i64, i64, i32, i32, P, i32, i64, P, P, P, i64, P]
+            lib.orc_mx_gemm.restype = None
+            lib.orc_mx_gemm.argtypes = [P, i32, i64, P, i64, P, i32, i64, P, i64, i64, i64, i64, P, P, i64,
+                                        P, P]
             _lib = lib
     return _lib
 
@@ -233,4 +249,68 @@ def grouped_gemm(mode, A, fa, B, fb, offsets, N, K, sa, sb, pg, pm, pn):
     _load().orc_grouped_gemm(mode, _ptr(A), fa, _ptr(B), fb, _ptr(off), G, int(off[-1]), N, K,
                              _ptr(sa_a), int(sa_a.size > 1), _ptr(sb_a), int(sb_a.size > 1),
                              _ptr(pg), _ptr(pm), _ptr(pn), pm.size, _ptr(ref), _ptr(bound))
+    return ref, bound
+
+
+# --- MXFP8 -------------------------------------------------------------------
+
+MX_BLOCK = 32
+
+
+def mx_emax(fmt: int) -> int:
+    return _load().orc_mx_emax(int(fmt))
+
+
+def mx_scale_code(amax: float, fmt: int) -> int:
+    """E8M0 code of a block whose largest magnitude is amax."""
+    return _load().orc_mx_scale_code(float(amax), int(fmt))
+
+
+def e8m0_decode(code: int) -> float:
+    return _load().orc_e8m0_decode(int(code))
+
+
+def padded_offsets_align(offsets, align: int) -> np.ndarray:
+    off = _c(offsets, np.int32)
+    G = off.size - 1
+    poff = np.zeros(G + 1, dtype=np.int64)
+    _load().orc_padded_offsets_align(_ptr(off), G, int(align), _ptr(poff))
+    return poff
+
+
+def mx_quantize(x_bits, fmt, layouts=LAYOUT_ROW | LAYOUT_COLT, offsets=None, align=128):
+    """MX quantize of a bf16 matrix given as uint16 bits [rows, cols].
+
+    Returns dict(q_row [rows, cols], s_row [SR, cols/32], q_colT [cols, P],
+    s_col [cols, P/32]) with plain row-major E8M0 scale matrices; SR = P =
+    rows (ungrouped) or the total of the group sizes padded to `align`.
+    """
+    x = _c(x_bits, np.uint16)
+    rows, cols = x.shape
+    G = 0 if offsets is None else len(offsets) - 1
+    off = None if offsets is None else _c(offsets, np.int32)
+    P = rows if off is None else int(padded_offsets_align(off, align)[-1])
+    q_row = np.zeros((rows, cols), np.uint8) if layouts & LAYOUT_ROW else None
+    s_row = np.zeros((P, cols // MX_BLOCK), np.uint8) if layouts & LAYOUT_ROW else None
+    q_colT = np.zeros((cols, P), np.uint8) if layouts & LAYOUT_COLT else None
+    s_col = np.zeros((cols, P // MX_BLOCK), np.uint8) if layouts & LAYOUT_COLT else None
+    _load().orc_mx_quantize(_ptr(x), rows, cols, cols, fmt, layouts, _ptr(off), G, int(align), _ptr(q_row),
+                            _ptr(s_row), _ptr(q_colT), P, _ptr(s_col))
+    return dict(q_row=q_row, s_row=s_row, q_colT=q_colT, s_col=s_col)
+
+
+def mx_gemm(A, fa, sA, B, fb, sB, points=None):
+    """MX GEMM in double: A [M, K] u8 with E8M0 codes sA [M, K/32], B [N, K]
+    with sB [N, K/32].  Returns (ref, bound) ([M, N] or [npts])."""
+    A = _c(A, np.uint8); B = _c(B, np.uint8)
+    sA = _c(sA, np.uint8); sB = _c(sB, np.uint8)
+    M, K = A.shape
+    N = B.shape[0]
+    if points is None:
+        ref = np.zeros((M, N)); bound = np.zeros((M, N)); pm = pn = None; npts = 0
+    else:
+        pm = _c(points[0], np.int64); pn = _c(points[1], np.int64); npts = pm.size
+        ref = np.zeros(npts); bound = np.zeros(npts)
+    _load().orc_mx_gemm(_ptr(A), fa, K, _ptr(sA), sA.shape[1], _ptr(B), fb, K, _ptr(sB), sB.shape[1], M, N, K,
+                        _ptr(pm), _ptr(pn), npts, _ptr(ref), _ptr(bound))
     return ref, bound

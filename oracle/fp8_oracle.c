@@ -513,3 +513,180 @@ void orc_grouped_gemm(int mode, const uint8_t *A, int fa, const uint8_t *B, int 
     }
     free(poff);
 }
+
+/* ------------------------------------------------------------------------ */
+/* MXFP8: blocks of 32 elements sharing one power-of-two (E8M0) scale         */
+/* ------------------------------------------------------------------------ */
+/*
+ * "FP8 training for Flux models" (Configuration > Key FP8 Parameters) lists
+ * "mxfp8" among the fp8_recipe values, and "FP8 Training on AMD GPUs with
+ * TorchTitan and TorchAO" names an MXFP8 grouped GEMM as next work; neither
+ * page defines it.  The definition followed here is the public OCP
+ * Microscaling Formats (MX) v1.0 specification:
+ *   - a block is 32 consecutive elements along the contraction dimension
+ *     (rowwise: along a row; colwise: along a column);
+ *   - its shared scale is X = 2^e, stored as E8M0 code e + 127 (0 .. 254;
+ *     255 is NaN), with e = floor(log2(max_i |V_i|)) - emax_elem, where
+ *     emax_elem is the exponent of the element format's largest normal
+ *     (8 for E4M3: 448 = 1.75 * 2^8; 15 for E5M2: 57344 = 1.75 * 2^15),
+ *     clamped to [-127, 127];
+ *   - each element is P_i = sat_rne_fp8(V_i / X) (ties to even, saturating).
+ * Readings where the specification leaves a choice: an all-zero block gets
+ * code 0; a block holding a NaN or an Inf gets code 255 and every element
+ * of it the format's NaN code.  V_i / X is exact in double (X is a power of
+ * two), so the element rounding is the single RNE of the encoder.
+ *
+ * Scales are returned as plain row-major matrices of codes: s[r][b] is the
+ * scale of block b of row r (rowwise) or of column r (colwise).
+ */
+#define ORC_MX_BLOCK 32
+
+int orc_mx_emax(int fmt) { return fmt == ORC_E5M2 ? 15 : 8; }
+
+int orc_mx_scale_code(double amax, int fmt)
+{
+    int e;
+    if (isnan(amax) || isinf(amax)) return 255;
+    if (amax == 0.0) return 0;
+    (void)frexp(amax, &e); /* amax = f * 2^e with f in [0.5, 1): floor(log2 amax) = e - 1 */
+    e = (e - 1) - orc_mx_emax(fmt);
+    if (e < -127) e = -127;
+    if (e > 127) e = 127;
+    return e + 127;
+}
+
+double orc_e8m0_decode(int code) { return code == 255 ? NAN : ldexp(1.0, code - 127); }
+
+/* One block: v[0..31] (missing elements are passed as 0), codes to
+ * out[i * stride], the scale code returned. */
+static int mx_block(const double *v, int fmt, uint8_t *out, int64_t stride)
+{
+    double amax = 0.0;
+    int nonfinite = 0, code;
+    for (int i = 0; i < ORC_MX_BLOCK; i++) {
+        if (!isfinite(v[i])) nonfinite = 1;
+        else if (fabs(v[i]) > amax) amax = fabs(v[i]);
+    }
+    code = nonfinite ? 255 : orc_mx_scale_code(amax, fmt);
+    for (int i = 0; i < ORC_MX_BLOCK; i++) {
+        int q = code == 255 ? orc_fp8_nan_code(fmt) : orc_fp8_encode(ldexp(v[i], 127 - code), fmt);
+        out[(int64_t)i * stride] = (uint8_t)q;
+    }
+    return code;
+}
+
+/* Group offsets padded to a multiple of `align`; returns the padded total. */
+int64_t orc_padded_offsets_align(const int32_t *off, int G, int64_t align, int64_t *poff)
+{
+    int64_t acc = 0;
+    for (int e = 0; e < G; e++) {
+        poff[e] = acc;
+        acc += ((int64_t)off[e + 1] - off[e] + align - 1) / align * align;
+    }
+    poff[G] = acc;
+    return acc;
+}
+
+/*
+ * MX quantize of a bf16 matrix x[rows][cols] (cols % 32 == 0).
+ *
+ * Row layout (layouts & 1): q_row [rows][cols]; s_row [SR][cols / 32] with
+ *   SR = rows (ungrouped) or the padded total (grouped): row r of group e is
+ *   scale row poff[e] + (r - offsets[e]); scale rows in a group's padding are
+ *   all-zero blocks (code 0).
+ * Transposed layout (layouts & 2): q_colT [cols][ldT], column c holding the
+ *   rows of x (ungrouped: rows % 32 == 0) or group e's rows at poff[e]
+ *   followed by zero padding up to poff[e + 1]; blocks run along the rows
+ *   of each group (a group's last block is completed with zeros), s_col
+ *   [cols][P / 32], P = rows or the padded total.
+ * offsets: NULL or int32 [G + 1]; align: the group padding (a multiple of 32).
+ */
+int orc_mx_quantize(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, int fmt, int layouts,
+                    const int32_t *offsets, int G, int64_t align, uint8_t *q_row, uint8_t *s_row,
+                    uint8_t *q_colT, int64_t ldT, uint8_t *s_col)
+{
+    int ngroups = offsets ? G : 1;
+    int64_t *poff = (int64_t *)malloc(sizeof(int64_t) * (ngroups + 1));
+    int64_t P, nb = cols / ORC_MX_BLOCK;
+
+    init_tables();
+    if (offsets) {
+        P = orc_padded_offsets_align(offsets, G, align, poff);
+    } else {
+        poff[0] = 0;
+        poff[1] = rows;
+        P = rows;
+    }
+    if (layouts & ORC_LAYOUT_ROW) {
+        if (offsets) memset(s_row, 0, (size_t)(P * nb));
+#pragma omp parallel for schedule(static)
+        for (int64_t r = 0; r < rows; r++) {
+            int64_t sr = r;
+            double v[ORC_MX_BLOCK];
+            if (offsets) {
+                int e = 0;
+                while (e < G - 1 && r >= offsets[e + 1]) e++;
+                sr = poff[e] + (r - offsets[e]);
+            }
+            for (int64_t b = 0; b < nb; b++) {
+                for (int i = 0; i < ORC_MX_BLOCK; i++) v[i] = bf16_to_float(x[r * ld_x + b * ORC_MX_BLOCK + i]);
+                s_row[sr * nb + b] = (uint8_t)mx_block(v, fmt, q_row + r * cols + b * ORC_MX_BLOCK, 1);
+            }
+        }
+    }
+    if (layouts & ORC_LAYOUT_COLT) {
+        int64_t pb = P / ORC_MX_BLOCK;
+        memset(q_colT, 0, (size_t)(cols * ldT));
+        memset(s_col, 0, (size_t)(cols * pb));
+#pragma omp parallel for schedule(static)
+        for (int64_t c = 0; c < cols; c++) {
+            double v[ORC_MX_BLOCK];
+            for (int e = 0; e < ngroups; e++) {
+                int64_t r0 = offsets ? offsets[e] : 0, r1 = offsets ? offsets[e + 1] : rows;
+                for (int64_t b = 0; r0 + b * ORC_MX_BLOCK < r1; b++) {
+                    for (int i = 0; i < ORC_MX_BLOCK; i++) {
+                        int64_t r = r0 + b * ORC_MX_BLOCK + i;
+                        v[i] = r < r1 ? bf16_to_float(x[r * ld_x + c]) : 0.0;
+                    }
+                    s_col[c * pb + poff[e] / ORC_MX_BLOCK + b] =
+                        (uint8_t)mx_block(v, fmt, q_colT + c * ldT + poff[e] + b * ORC_MX_BLOCK, 1);
+                }
+            }
+        }
+    }
+    free(poff);
+    return 0;
+}
+
+/*
+ * MX GEMM in double: C[m][n] = sum_k dec(A[m][k]) X_A(m, k / 32)
+ * dec(B[n][k]) X_B(n, k / 32), both operands K-contiguous; sA [M][lds_a],
+ * sB [N][lds_b] are the E8M0 codes of each row's blocks.  bound = the sum of
+ * absolute values.  pm/pn: as orc_gemm (NULL = the full M x N result).
+ */
+void orc_mx_gemm(const uint8_t *A, int fa, int64_t lda, const uint8_t *sA, int64_t lds_a, const uint8_t *B,
+                 int fb, int64_t ldb, const uint8_t *sB, int64_t lds_b, int64_t M, int64_t N, int64_t K,
+                 const int64_t *pm, const int64_t *pn, int64_t npts, double *ref, double *bound)
+{
+    double da[256], db[256];
+    int64_t total = pm ? npts : M * N;
+    for (int c = 0; c < 256; c++) {
+        da[c] = orc_fp8_decode(c, fa);
+        db[c] = orc_fp8_decode(c, fb);
+    }
+#pragma omp parallel for schedule(dynamic, 64)
+    for (int64_t i = 0; i < total; i++) {
+        int64_t m = pm ? pm[i] : i / N, n = pm ? pn[i] : i % N;
+        const uint8_t *a = A + m * lda, *b = B + n * ldb;
+        double s = 0.0, t = 0.0;
+        for (int64_t k = 0; k < K; k++) {
+            double x = orc_e8m0_decode(sA[m * lds_a + k / ORC_MX_BLOCK]) *
+                       orc_e8m0_decode(sB[n * lds_b + k / ORC_MX_BLOCK]);
+            double p = da[a[k]] * db[b[k]] * x;
+            s += p;
+            t += fabs(p);
+        }
+        ref[i] = s;
+        bound[i] = t;
+    }
+}
