@@ -19,6 +19,8 @@ Other workloads (same JSON line, their own config):
                  scales, rowwise / per-expert colwise weights, 9 grouped GEMMs
   flux           Flux-12B linears (tokens 9216, hidden 3072, MLP 12288, QKV
                  9216), delayed scaling, all E4M3, amax algo max
+  llama_mxfp8    the Llama-3-8B MLP step under the MXFP8 recipe (blocks of 32
+                 with E8M0 scales, both layouts per tensor, block-scaled GEMMs)
   sweep          the delayed quantize (E4M3, both layouts) of 2^20 .. 2^30
                  elements, GB/s against size
   gemm, quantize single kernels of the default step, for profiling
@@ -26,6 +28,7 @@ Other workloads (same JSON line, their own config):
                  MoE layer (64 experts, 8192 routed rows), for profiling
   quantize_grouped  the rowwise quantize of one reduced MoE weight (64
                  experts x 2048 rows x 7168), for profiling
+  mx_gemm, mx_quantize  the MXFP8 gate GEMM / the MX quantize of dY_gate
 
 Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle on a
 bounded sample of the same workload instead.
@@ -370,6 +373,76 @@ class RowwiseStep:
             _timed(ev, "g", lambda g=g: self.gemm(*g), self.gemm_work[g[4]])
 
 
+def mx_quantize_bytes(shape):
+    """Algorithmic bytes of one MX quantize with both layouts: 2 B read, 1 B
+    per layout per element, one E8M0 byte per 32 elements per layout."""
+    r, c = shape
+    return r * c * 4 + 2 * (r * c // 32)
+
+
+class MxStep:
+    """The Llama-3-8B MLP block fwd+bwd under the MXFP8 recipe: every tensor
+    MX-quantized once into both layouts (blocks of 32 along rows for the row
+    layout, along columns for the transposed one, E8M0 scales); the nine
+    GEMMs on the block-scaled tensor cores.  No history, no update."""
+
+    def __init__(self, dev, seed, keys=None, outs=None):
+        import fp8_mixed_precision_scale_gb300 as fp8
+        self.fp8 = fp8
+        self.name = "llama_mxfp8"
+        self.desc = ("llama3-8b-mlp fwd+bwd, mxfp8 recipe (OCP MX: 32-element blocks, E8M0 scales): tokens 8192, "
+                     "hidden 4096, ffn 14336, e4m3 fwd / e5m2 grads")
+        self.tokens = T_
+        g = torch.Generator(device=dev)
+        g.manual_seed(seed)
+        self.inp = {k: _normal(g, dev, *LLAMA_MLP_SHAPES[k]) for k in LLAMA_MLP_SHAPES if keys is None or k in keys}
+        self.fmt = {k: (fp8.E5M2 if k.startswith("dy") else fp8.E4M3FN) for k in LLAMA_MLP_SHAPES}
+        self.q = {}
+        for k, t in self.inp.items():
+            r, c = t.shape
+            self.q[k] = dict(row=torch.empty((r, c), dtype=torch.uint8, device=dev),
+                             colT=torch.empty((c, r), dtype=torch.uint8, device=dev),
+                             srow=torch.empty(fp8.fp8_mx_scale_bytes(r, c // 32), dtype=torch.uint8, device=dev),
+                             scol=torch.empty(fp8.fp8_mx_scale_bytes(c, r // 32), dtype=torch.uint8, device=dev))
+        self.out, self.gemm_work = {}, {}
+        self.flops = 0.0
+        for (a, al, b, bl, o) in MLP_GEMMS:
+            M, K = LLAMA_MLP_SHAPES[a][0] if al == "row" else LLAMA_MLP_SHAPES[a][0][::-1]
+            N = LLAMA_MLP_SHAPES[b][0][0] if bl == "row" else LLAMA_MLP_SHAPES[b][0][1]
+            self.gemm_work[o] = (2.0 * M * N * K, M * K + N * K + 2.0 * M * N + (M + N) * K / 32)
+            self.flops += 2.0 * M * N * K
+            if outs is None or o in outs:
+                self.out[o] = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        self.q_bytes = sum(mx_quantize_bytes(LLAMA_MLP_SHAPES[k][0]) for k in LLAMA_MLP_SHAPES)
+        self.launches_per_step = len(LLAMA_MLP_SHAPES) + len(MLP_GEMMS)
+        self.d2h = [self.out["y"]] if outs is None else []
+
+    def quantize(self, k):
+        t, q = self.inp[k], self.q[k]
+        r, c = t.shape
+        self.fp8.fp8_mx_quantize(t, r, c, c, self.fmt[k], 3, q["row"], q["srow"], q["colT"], r, q["scol"])
+
+    def gemm(self, a, al, b, bl, out):
+        qa, qb = self.q[a], self.q[b]
+        A = qa["row"] if al == "row" else qa["colT"]
+        B = qb["row"] if bl == "row" else qb["colT"]
+        sA = qa["srow"] if al == "row" else qa["scol"]
+        sB = qb["srow"] if bl == "row" else qb["scol"]
+        M, K = A.shape
+        N = B.shape[0]
+        self.fp8.fp8_mx_gemm(A, self.fmt[a], K, sA, B, self.fmt[b], K, sB, M, N, K, self.out[out], N)
+
+    def run(self, ev=None, world=1):
+        for k in ["x", "w_gate", "w_up", "w_down", "h"]:
+            _timed(ev, "q", lambda k=k: self.quantize(k), mx_quantize_bytes(self.inp[k].shape))
+        for g in MLP_GEMMS[:3]:
+            _timed(ev, "g", lambda g=g: self.gemm(*g), self.gemm_work[g[4]])
+        for k in ["dy_down", "dy_gate", "dy_up"]:
+            _timed(ev, "q", lambda k=k: self.quantize(k), mx_quantize_bytes(self.inp[k].shape))
+        for g in MLP_GEMMS[3:]:
+            _timed(ev, "g", lambda g=g: self.gemm(*g), self.gemm_work[g[4]])
+
+
 class MoeStep:
     """DeepSeek-V3-shaped MoE layer fwd+bwd on one GPU: routed token rows
     grouped by expert, rowwise scales per token plus per-expert column scales;
@@ -561,13 +634,14 @@ def run_gpu(args, rank, world, local_rank):
     hbm_gbs, bf16_burst, bf16_sust, peak_src = peaks()
     fp8_peak = 2.0 * bf16_sust               # FP8 dense = 2x bf16 dense (nominal 4.5 vs 2.25 PFLOP/s)
 
-    if args.workload in ("gemm", "quantize", "grouped_m", "grouped_k", "quantize_grouped"):
+    if args.workload in ("gemm", "quantize", "grouped_m", "grouped_k", "quantize_grouped", "mx_gemm", "mx_quantize"):
         run_single_kernel(args, dev, rank)
         return
     if args.workload == "sweep":
         run_sweep(args, dev, rank, hbm_gbs)
         return
-    make = {"llama_mlp": llama_mlp_step, "flux": flux_step, "llama_rowwise": RowwiseStep, "moe": MoeStep}
+    make = {"llama_mlp": llama_mlp_step, "flux": flux_step, "llama_rowwise": RowwiseStep, "moe": MoeStep,
+            "llama_mxfp8": MxStep}
     step = make[args.workload](dev, 1 + rank)
     for _ in range(max(3, args.warmup)):
         step.run(world=world)
@@ -606,7 +680,8 @@ def run_gpu(args, rank, world, local_rank):
     if sum(g_ms) >= sum(q_ms):
         if g_roof_ms <= g_tensor_ms * 1.0001:      # tensor-bound GEMMs
             roof = {"bound": "tensor", "achieved": round(gemm_tflops, 1), "peak": round(fp8_peak, 1),
-                    "unit": "TFLOP/s", "frac": round(gemm_tflops / fp8_peak, 4), "kernel": "fp8_gemm_kernel",
+                    "unit": "TFLOP/s", "frac": round(gemm_tflops / fp8_peak, 4),
+                    "kernel": "mx_gemm_kernel" if step.name == "llama_mxfp8" else "fp8_gemm_kernel",
                     "traffic": gemm_traffic() if step.name == "llama_mlp" else None,
                     "peak_source": f"{peak_src}: 2 x sustained bf16 {bf16_sust} TFLOP/s (fp8/bf16 nominal ratio 2)"}
         else:                                      # HBM-bound (grouped GEMMs at the MoE shape)
@@ -832,6 +907,16 @@ def run_single_kernel(args, dev, rank):
         fn, work, unit = grouped_case(args.workload, dev)
     elif args.workload == "quantize_grouped":
         fn, work, unit = grouped_weight_quantize_case(dev)
+    elif args.workload == "mx_gemm":
+        step = MxStep(dev, 1, keys=("x", "w_gate"), outs=("gate",))
+        for k in ("x", "w_gate"):
+            step.quantize(k)
+        fn = lambda: step.gemm(*MLP_GEMMS[0])  # noqa: E731
+        work, unit = step.gemm_work["gate"][0] / 1e12, "TFLOP/s"
+    elif args.workload == "mx_quantize":
+        step = MxStep(dev, 1, keys=("dy_gate",), outs=())
+        fn = lambda: step.quantize("dy_gate")  # noqa: E731
+        work, unit = mx_quantize_bytes(step.inp["dy_gate"].shape) / 1e9, "GB/s"
     elif args.workload == "gemm":
         step = llama_mlp_step(dev, 1, keys=("x", "w_gate"), outs=("gate",))
         for k in ("x", "w_gate"):   # real FP8 operands for the GEMM
@@ -896,8 +981,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="llama_mlp",
-                    choices=["llama_mlp", "llama_rowwise", "moe", "flux", "sweep", "gemm", "quantize", "grouped_m",
-                             "grouped_k", "quantize_grouped"],
+                    choices=["llama_mlp", "llama_rowwise", "llama_mxfp8", "moe", "flux", "sweep", "gemm", "quantize",
+                             "grouped_m", "grouped_k", "quantize_grouped", "mx_gemm", "mx_quantize"],
                     help="llama_mlp: the whole fwd+bwd FP8 step of the Llama-3-8B MLP (default); see the "
                          "module docstring for the others")
     args = ap.parse_args()

@@ -39,7 +39,10 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libfp8gb.so")
 EXPORTED = ("fp8_quantize", "fp8_update_amax_history", "fp8_scaled_gemm", "fp8_grouped_gemm",
             "fp8_group_padded_offsets", "fp8_sync_status", "fp8_selftest_bounded_wait", "fp8_status_string",
-            "fp8_last_cuda_error", "fp8_version")
+            "fp8_last_cuda_error", "fp8_version", "fp8_mx_scale_bytes", "fp8_mx_quantize", "fp8_mx_gemm",
+            "fp8_mx_grouped_gemm")
+MX_BLOCK = 32
+MX_GROUP_ALIGN = 128
 
 _lock = threading.Lock()
 _lib = None
@@ -112,6 +115,14 @@ def load_library():
             lib.fp8_last_cuda_error.argtypes = []
             lib.fp8_version.restype = ctypes.c_char_p
             lib.fp8_version.argtypes = []
+            lib.fp8_mx_scale_bytes.restype = i64
+            lib.fp8_mx_scale_bytes.argtypes = [i64, i64]
+            lib.fp8_mx_quantize.restype = i32
+            lib.fp8_mx_quantize.argtypes = [P, i64, i64, i64, i32, i32, P, P, P, i64, P, P, i32, P]
+            lib.fp8_mx_gemm.restype = i32
+            lib.fp8_mx_gemm.argtypes = [P, i32, i64, P, P, i32, i64, P, i64, i64, i64, P, i64, P]
+            lib.fp8_mx_grouped_gemm.restype = i32
+            lib.fp8_mx_grouped_gemm.argtypes = [i32, P, i32, P, P, i32, P, P, i32, i64, i64, i64, P, i64, P]
             _lib = lib
     return _lib
 
@@ -187,6 +198,36 @@ def fp8_group_padded_offsets(host_offsets, align: int = 32):
     return int(total), out
 
 
+def fp8_mx_scale_bytes(scale_rows: int, blocks: int) -> int:
+    return int(load_library().fp8_mx_scale_bytes(scale_rows, blocks))
+
+
+def fp8_mx_quantize(x, rows, cols, ld_x, fmt, layouts, q_row, s_row, q_colT, ld_colT, s_col, group_offsets=None,
+                    num_groups=0, stream=None, check=True):
+    rc = load_library().fp8_mx_quantize(_p(x), rows, cols, ld_x, fmt, layouts, _p(q_row), _p(s_row), _p(q_colT),
+                                        ld_colT, _p(s_col), _p(group_offsets), num_groups, _stream(stream))
+    if check:
+        _check(rc, "fp8_mx_quantize")
+    return rc
+
+
+def fp8_mx_gemm(A, fa, lda, sA, B, fb, ldb, sB, M, N, K, C, ldc, stream=None, check=True):
+    rc = load_library().fp8_mx_gemm(_p(A), fa, lda, _p(sA), _p(B), fb, ldb, _p(sB), M, N, K, _p(C), ldc,
+                                    _stream(stream))
+    if check:
+        _check(rc, "fp8_mx_gemm")
+    return rc
+
+
+def fp8_mx_grouped_gemm(mode, A, fa, sA, B, fb, sB, group_offsets, G, M_total, N, K, C, ld_T=0, stream=None,
+                        check=True):
+    rc = load_library().fp8_mx_grouped_gemm(mode, _p(A), fa, _p(sA), _p(B), fb, _p(sB), _p(group_offsets), G,
+                                            M_total, N, K, _p(C), ld_T, _stream(stream))
+    if check:
+        _check(rc, "fp8_mx_grouped_gemm")
+    return rc
+
+
 def fp8_sync_status(stream=None) -> int:
     return load_library().fp8_sync_status(_stream(stream))
 
@@ -259,4 +300,66 @@ def grouped_gemm(mode: int, A, fa, B, fb, group_offsets, M_total, N, K, sa, sb, 
         out = torch.empty(shape, dtype=torch.bfloat16, device=A.device)
     fp8_grouped_gemm(mode, A, fa, B, fb, group_offsets, G, M_total, N, K, sa, int(sa.numel() > 1), sb,
                      int(sb.numel() > 1), out, ld_T, stream)
+    return out
+
+
+@dataclass
+class MxQuantized:
+    q_row: torch.Tensor | None     # [rows, cols] u8
+    s_row: torch.Tensor | None     # MX scale layout, R = rows (grouped: padded total)
+    q_colT: torch.Tensor | None    # [cols, ld_colT] u8
+    s_col: torch.Tensor | None     # MX scale layout, R = cols, KB = ld_colT / 32
+    ld_colT: int
+    scale_rows: int                # R of s_row
+
+
+def mx_quantize(x: torch.Tensor, fmt: int, layouts: int = LAYOUT_ROW | LAYOUT_COLT, group_offsets=None,
+                host_offsets=None, stream=None) -> MxQuantized:
+    """MX quantize of a CUDA bf16 [rows, cols] tensor (cols % 32 == 0).
+
+    Grouped (MoE) tensors pass the device offsets and their CPU copy; every
+    group is padded to MX_GROUP_ALIGN rows in the padded layouts.
+    """
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    rows, cols = x.shape
+    dev = x.device
+    G = 0
+    if group_offsets is not None:
+        G = group_offsets.numel() - 1
+        P, _ = fp8_group_padded_offsets(host_offsets, MX_GROUP_ALIGN)
+    else:
+        P = rows
+    ld_colT = max(16, (P + 15) // 16 * 16)
+    def buf(n):  # never a zero-byte (null) allocation
+        return torch.empty(max(16, n), dtype=torch.uint8, device=dev)
+
+    q_row = s_row = q_colT = s_col = None
+    if layouts & LAYOUT_ROW:
+        q_row = buf(rows * cols)[:rows * cols].view(rows, cols)
+        s_row = buf(fp8_mx_scale_bytes(P, cols // MX_BLOCK))
+    if layouts & LAYOUT_COLT:
+        q_colT = buf(cols * ld_colT)[:cols * ld_colT].view(cols, ld_colT)
+        s_col = buf(fp8_mx_scale_bytes(cols, P // MX_BLOCK))
+    fp8_mx_quantize(x, rows, cols, x.stride(0), fmt, layouts, q_row, s_row, q_colT, ld_colT, s_col, group_offsets,
+                    G, stream)
+    return MxQuantized(q_row, s_row, q_colT, s_col, ld_colT, P)
+
+
+def mx_gemm(A: torch.Tensor, fa: int, sA: torch.Tensor, B: torch.Tensor, fb: int, sB: torch.Tensor, K=None,
+            out=None, stream=None) -> torch.Tensor:
+    """C = bf16(MX-scaled A[:, :K] . B[:, :K]^T)."""
+    M, lda = A.shape
+    N, ldb = B.shape
+    K = lda if K is None else K
+    C = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    fp8_mx_gemm(A, fa, A.stride(0), sA, B, fb, B.stride(0), sB, M, N, K, C, C.stride(0), stream)
+    return C
+
+
+def mx_grouped_gemm(mode: int, A, fa, sA, B, fb, sB, group_offsets, M_total, N, K, ld_T=0, out=None, stream=None):
+    G = group_offsets.numel() - 1
+    if out is None:
+        shape = (G, N, K) if mode == GROUPED_K else (M_total, N)
+        out = torch.empty(shape, dtype=torch.bfloat16, device=A.device)
+    fp8_mx_grouped_gemm(mode, A, fa, sA, B, fb, sB, group_offsets, G, M_total, N, K, out, ld_T, stream)
     return out

@@ -384,6 +384,66 @@ __device__ __forceinline__ void tma_load_2d_pair(void *smem_dst, const CUtensorM
         : "memory");
 }
 
+// ---------------------------------------------------------------------------
+// Block-scaled MMA (tcgen05.mma kind::mxf8f6f4, E8M0 scales in TMEM)
+// ---------------------------------------------------------------------------
+// Plain bulk copy global -> shared (no tensor map), completing on an mbarrier
+// by transaction bytes; both addresses 16-byte aligned, bytes % 16 == 0.
+__device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(smem_u32(smem_dst)), "l"((uint64_t)gsrc), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+// Shared-memory descriptor of a 32-row x 16-byte block without swizzle
+// (8-row core matrices of 128 contiguous bytes, 128 bytes apart): the source
+// of tcgen05.cp 32x128b.
+__device__ __forceinline__ uint64_t smem_desc_sf(uint32_t smem_addr)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((smem_addr & 0x3FFFFu) >> 4);  // start address
+    d |= (uint64_t)(128 >> 4) << 32;               // stride byte offset: next 8 rows
+    d |= (uint64_t)1 << 46;                        // version; layout type 0 (no swizzle)
+    return d;
+}
+
+// Copy 32 lanes x 128 bits from shared memory into TMEM columns
+// taddr .. taddr+3, replicated into all four lane quarters (warpx4).
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc)
+{
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// Instruction descriptor of kind::mxf8f6f4 with E8M0 block scales, fp32
+// accumulate, K-major operands: formats at bits 7 / 10, N/8 at bit 17, the
+// scale type (E8M0 = 1) at bit 23, M/16 at bit 24; the byte of the scale word
+// used by an MMA (its 32-element block within a 128-element K tile) is
+// selected by the scale-factor ids, B's at bit 4 and A's at bit 29.
+__host__ __device__ constexpr uint32_t idesc_mxf8f6f4(int fa, int fb, int M, int N)
+{
+    return ((uint32_t)fa << 7) | ((uint32_t)fb << 10) | ((uint32_t)(N >> 3) << 17) | (1u << 23) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
+__host__ __device__ constexpr uint32_t idesc_sf_ids(uint32_t idesc, uint32_t a_id, uint32_t b_id)
+{
+    return idesc | (b_id << 4) | (a_id << 29);
+}
+
+// Scale factors for A row m: TMEM lane m, column sfa + m / 32; for B row n:
+// column sfb + n / 32 in every lane quarter (lane 32q + n % 32).
+__device__ __forceinline__ void mma_mxf8f6f4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+        : "memory");
+}
+
 // Two fp32 -> packed bf16x2 (round to nearest even); lo in the low half.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {

@@ -1,0 +1,683 @@
+// mxgemm.cu -- MXFP8 GEMM and grouped GEMM on the block-scaled tcgen05
+// tensor cores.
+//
+// C[m][n] = bf16( sum_k A[m][k] X_A(m, k/32) B[n][k] X_B(n, k/32) ): FP8
+// E4M3 / E5M2 operands, one E8M0 scale per 32 elements along K for every row
+// of A and of B, fp32 accumulation in tensor memory.  The scales are applied
+// by the MMA itself (tcgen05.mma kind::mxf8f6f4 block_scale), which reads
+// them from tensor memory, so the epilogue only converts to bf16.
+//
+// Method: the "mxfp8" recipe ("FP8 training for Flux models", Key FP8
+// Parameters) and MXFP8 grouped GEMM for MoE ("FP8 Training on AMD GPUs with
+// TorchTitan and TorchAO"), with the OCP Microscaling block rule.
+//
+// Design (GB300, sm_103a): the persistent warp-specialised structure of the
+// tensor-scaled GEMM plus a scale warp, 352 threads per CTA, one CTA per SM.
+//   warp 0     producer: TMA tiles of A (128 x 128 bytes) and B (224 x 128
+//              bytes), plus one bulk copy each of the tiles' scale words
+//              (one 32-bit word per row and 128-element K tile), all counted
+//              on one mbarrier per stage of a 4-stage ring.
+//   warp 10    scales: rearranges each stage's scale words into the 32-lane
+//              x 16-byte blocks that tcgen05.cp 32x128b.warpx4 copies into
+//              tensor memory (word of row 32j + L at lane L, column j,
+//              replicated into every lane quarter: the column and lane the
+//              block-scaled MMA reads for that row), issues the three copies
+//              into the stage's own scale columns and commits them to a
+//              per-stage barrier -- off the MMA thread's critical path.
+//   warp 1     MMA: one thread waits for a stage's scales and issues its four
+//              K=32 MMAs, each selecting its byte of the scale words by the
+//              scale-factor ids of the instruction descriptor.
+//   warps 2-9  epilogue: tcgen05.ld, bf16, shared-memory transpose, whole-
+//              sector stores.
+// Tiles are 128 x 224: two 224-column accumulators (columns 0 and 256) and
+// one set of scale columns per ring stage (224 .. 239 for A, 480 .. 511 for
+// B) fit the 512 TMEM columns, so the epilogue of one tile overlaps the main
+// loop of the next and a stage's scale copies never wait for the MMAs of the
+// stage before.  Every wait is
+// bounded as in the tensor-scaled GEMM.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "fp8gb.h"
+#include "fp8gb_device.cuh"
+#include "fp8gb_host.h"
+
+namespace fp8gb {
+namespace mx {
+
+constexpr int BM = 128;
+constexpr int BN = 224;
+constexpr int BK = 128;
+constexpr int UMMA_K = 32;
+constexpr int STAGES = 4;
+constexpr int THREADS = 352;  // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue, warp 10 scales
+constexpr int A_BYTES = BM * BK;
+constexpr int B_BYTES = BN * BK;
+constexpr int SFA_RAW = BM * 4;   // one scale word per A row
+constexpr int SFB_RAW = 256 * 4;  // BN words used; room for two 128-row blocks
+constexpr int SFA_CP = 512;       // [32 lanes][4 words]
+constexpr int SFB_CP = 1024;      // two such blocks (rows 0-127, 128-255)
+constexpr uint32_t TMEM_COLS = 512;
+// scale columns, one set per ring stage so a stage's copies never overwrite
+// scales that MMAs of an earlier stage may still be reading: A's 4 columns
+// per stage in 224 .. 239, B's 8 per stage in 480 .. 511
+constexpr uint32_t SFA_COL = 224;
+constexpr uint32_t SFB_COL = 480;
+static_assert(SFA_COL + 4 * STAGES <= 256 && SFB_COL + 8 * STAGES <= TMEM_COLS, "scale columns");
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
+constexpr int MAX_GROUPS = 1024;
+
+__host__ __device__ constexpr uint32_t acc_col(int acc) { return acc ? 256u : 0u; }
+
+enum { MODE_DENSE = 0, MODE_MGROUP = 1, MODE_KGROUP = 2 };
+
+struct Params {
+    int64_t M, N, K;
+    const uint8_t *sA, *sB;
+    int64_t rsA, rsB;  // scale rows of the A / B scale layouts (multiples of 4)
+    uint16_t *C;
+    int64_t ldc;
+    int c_vec16;
+    int num_m_blk, num_n_blk, num_k_blk;
+    int m_fastest;
+    int64_t total_tiles;  // dense
+    const int32_t *offsets;
+    int G;
+    int64_t ld_T;
+    unsigned int *err;
+};
+
+struct Tile {
+    int32_t a_y, b_y;        // first TMA row of the A / B tile
+    int32_t x0;              // first K column (bytes) of both tiles
+    int64_t sa_row, sb_row;  // first scale row of the A / B tile
+    int64_t kt0;             // first K tile in the scale layouts
+    int nkb, last_steps;
+    int64_t row0, row_end, col0, col_end, c_base;
+};
+
+struct Smem {
+    static constexpr int a_off = 0;
+    static constexpr int b_off = STAGES * A_BYTES;
+    static constexpr int sfa_raw_off = b_off + STAGES * B_BYTES;
+    static constexpr int sfb_raw_off = sfa_raw_off + STAGES * SFA_RAW;
+    static constexpr int sfa_cp_off = sfb_raw_off + STAGES * SFB_RAW;
+    static constexpr int sfb_cp_off = sfa_cp_off + STAGES * SFA_CP;
+    static constexpr int bar_off = sfb_cp_off + STAGES * SFB_CP;
+    static constexpr int n_bars = 3 * STAGES + 2 + 2 + 2;
+    static constexpr int slot_off = bar_off + n_bars * 8;
+    static constexpr int stage_pitch = 80;
+    static constexpr int stage_warp_bytes = 32 * stage_pitch;
+    static constexpr int stage_off = (slot_off + 16 + 127) / 128 * 128;
+    static constexpr int misc_off = stage_off + 8 * stage_warp_bytes;  // group tables
+};
+
+// Tile prefix [G+1] and offsets padded to FP8_MX_GROUP_ALIGN [G+1]; one warp.
+__device__ bool build_group_tables(const Params &p, int MODE, int32_t *tile_prefix, int32_t *poff,
+                                   int64_t *total_tiles)
+{
+    constexpr int AL = FP8_MX_GROUP_ALIGN;
+    const int lane = threadIdx.x & 31;
+    const int G = p.G;
+    const int per = (G + 31) / 32;
+    const int g0 = min(G, lane * per), g1 = min(G, g0 + per);
+    int64_t lt = 0, lp = 0;
+    int bad = 0;
+    for (int e = g0; e < g1; e++) {
+        const int m = p.offsets[e + 1] - p.offsets[e];
+        if (m < 0) bad = 1;
+        const int mm = max(m, 0);
+        lt += MODE == MODE_MGROUP ? (int64_t)((mm + BM - 1) / BM) * p.num_n_blk : (int64_t)p.num_m_blk * p.num_n_blk;
+        lp += (int64_t)((mm + AL - 1) / AL) * AL;
+    }
+    int64_t it = lt, ip = lp;
+    for (int d = 1; d < 32; d <<= 1) {
+        const int64_t vt = __shfl_up_sync(0xffffffffu, it, d), vp = __shfl_up_sync(0xffffffffu, ip, d);
+        if (lane >= d) {
+            it += vt;
+            ip += vp;
+        }
+    }
+    int64_t rt = it - lt, rp = ip - lp;
+    for (int e = g0; e < g1; e++) {
+        tile_prefix[e] = (int32_t)rt;
+        poff[e] = (int32_t)rp;
+        const int mm = max(p.offsets[e + 1] - p.offsets[e], 0);
+        rt += MODE == MODE_MGROUP ? (int64_t)((mm + BM - 1) / BM) * p.num_n_blk : (int64_t)p.num_m_blk * p.num_n_blk;
+        rp += (int64_t)((mm + AL - 1) / AL) * AL;
+    }
+    const int64_t tt = __shfl_sync(0xffffffffu, it, 31), tp = __shfl_sync(0xffffffffu, ip, 31);
+    bad = __any_sync(0xffffffffu, bad);
+    if (lane == 0) {
+        tile_prefix[G] = (int32_t)tt;
+        poff[G] = (int32_t)tp;
+    }
+    *total_tiles = tt;
+    const bool ok = !bad && p.offsets[0] == 0 && (int64_t)p.offsets[G] == p.M &&
+                    (MODE != MODE_KGROUP || tp <= p.ld_T) && tp <= INT32_MAX && tt < (int64_t)1 << 31;
+    return ok;
+}
+
+template <int MODE>
+__device__ __forceinline__ Tile tile_info(const Params &p, int64_t t, const int32_t *tile_prefix, const int32_t *poff)
+{
+    Tile ti;
+    if constexpr (MODE == MODE_DENSE) {
+        int mb, nb;
+        if (p.m_fastest) {
+            mb = (int)(t % p.num_m_blk);
+            nb = (int)(t / p.num_m_blk);
+        } else {
+            nb = (int)(t % p.num_n_blk);
+            mb = (int)(t / p.num_n_blk);
+        }
+        ti.a_y = mb * BM;
+        ti.b_y = nb * BN;
+        ti.x0 = 0;
+        ti.sa_row = (int64_t)mb * BM;
+        ti.sb_row = (int64_t)nb * BN;
+        ti.kt0 = 0;
+        ti.nkb = p.num_k_blk;
+        ti.last_steps = (int)((p.K - (int64_t)(ti.nkb - 1) * BK) / UMMA_K);
+        ti.row0 = (int64_t)mb * BM;
+        ti.row_end = p.M;
+        ti.col0 = (int64_t)nb * BN;
+        ti.col_end = p.N;
+        ti.c_base = 0;
+    } else {
+        int lo = 0, hi = p.G;  // group e: last with tile_prefix[e] <= t
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (tile_prefix[mid] <= t)
+                lo = mid;
+            else
+                hi = mid;
+        }
+        const int e = lo;
+        const int64_t local = t - tile_prefix[e];
+        const int64_t m_e = (int64_t)p.offsets[e + 1] - p.offsets[e];
+        if constexpr (MODE == MODE_MGROUP) {
+            const int64_t mt = (m_e + BM - 1) / BM;
+            const int64_t mb = local % mt, nb = local / mt;  // rows fastest: the expert's weight tile stays in L2
+            ti.a_y = (int32_t)(p.offsets[e] + mb * BM);
+            ti.b_y = (int32_t)((int64_t)e * p.N + nb * BN);
+            ti.x0 = 0;
+            ti.sa_row = poff[e] + mb * BM;
+            ti.sb_row = (int64_t)e * p.N + nb * BN;
+            ti.kt0 = 0;
+            ti.nkb = p.num_k_blk;
+            ti.last_steps = (int)((p.K - (int64_t)(ti.nkb - 1) * BK) / UMMA_K);
+            ti.row0 = p.offsets[e] + mb * BM;
+            ti.row_end = p.offsets[e + 1];
+            ti.col0 = nb * BN;
+            ti.col_end = p.N;
+            ti.c_base = 0;
+        } else {
+            // K-grouped: output block e is [N][K]; the contraction runs over
+            // group e's columns, which start at poff[e] (a multiple of 128)
+            const int64_t nb = local % p.num_n_blk, mb = local / p.num_n_blk;
+            ti.a_y = (int32_t)(mb * BM);
+            ti.b_y = (int32_t)(nb * BN);
+            ti.x0 = poff[e];
+            ti.sa_row = mb * BM;
+            ti.sb_row = nb * BN;
+            ti.kt0 = poff[e] / BK;
+            ti.nkb = (int)((m_e + BK - 1) / BK);
+            ti.last_steps = ti.nkb > 0 ? (int)((m_e - (int64_t)(ti.nkb - 1) * BK + UMMA_K - 1) / UMMA_K) : 0;
+            ti.row0 = mb * BM;
+            ti.row_end = p.N;
+            ti.col0 = nb * BN;
+            ti.col_end = p.K;
+            ti.c_base = (int64_t)e * p.N * p.K;
+        }
+    }
+    return ti;
+}
+
+// One finished tile for one epilogue warp: TMEM lane quarter q, columns
+// [cb, ce) of the tile (a multiple of 32 wide except at the tile's end).
+__device__ __forceinline__ void epilogue_tile(const Params &p, const Tile &ti, uint32_t tmem_base, uint32_t acc,
+                                              int q, int cb, int ce, int lane, uint8_t *stage)
+{
+    for (int ch = cb; ch < ce; ch += 64) {
+        const int64_t c0 = ti.col0 + ch;
+        if (c0 >= ti.col_end) break;  // warp-uniform
+        const bool two = ch + 32 < ce && c0 + 32 < ti.col_end;
+        uint32_t r[2][32];
+        const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc + (uint32_t)ch;
+        tmem_ld_32x32b_x32(taddr, r[0]);
+        if (two) tmem_ld_32x32b_x32(taddr + 32, r[1]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int u = 0; u < 2; u++) {
+            if (u == 1 && !two) break;  // warp-uniform
+            const int64_t cu = c0 + u * 32;
+            uint32_t packed[16];
+#pragma unroll
+            for (int j = 0; j < 16; j++)
+                packed[j] = pack_bf16x2(__uint_as_float(r[u][2 * j]), __uint_as_float(r[u][2 * j + 1]));
+#pragma unroll
+            for (int g = 0; g < 4; g++)
+                *reinterpret_cast<uint4 *>(stage + lane * Smem::stage_pitch + g * 16) =
+                    make_uint4(packed[4 * g], packed[4 * g + 1], packed[4 * g + 2], packed[4 * g + 3]);
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                const int rr = i * 8 + (lane >> 2), seg = lane & 3;
+                const uint4 v = *reinterpret_cast<const uint4 *>(stage + rr * Smem::stage_pitch + seg * 16);
+                const int64_t row = ti.row0 + q * 32 + rr;
+                const int64_t c = cu + seg * 8;
+                if (row < ti.row_end && c < ti.col_end) {
+                    uint16_t *dst = p.C + ti.c_base + row * p.ldc + c;
+                    if (p.c_vec16 && c + 8 <= ti.col_end) {
+                        *reinterpret_cast<uint4 *>(dst) = v;
+                    } else {
+                        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                        for (int j = 0; j < 8 && c + j < ti.col_end; j++)
+                            dst[j] = (uint16_t)(w[j / 2] >> (16 * (j & 1)));
+                    }
+                }
+            }
+            __syncwarp();
+        }
+    }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(THREADS, 1)
+    mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, Params p,
+                   uint32_t idesc)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sA = smem + Smem::a_off;
+    uint8_t *sB = smem + Smem::b_off;
+    uint8_t *sfa_raw = smem + Smem::sfa_raw_off;
+    uint8_t *sfb_raw = smem + Smem::sfb_raw_off;
+    uint8_t *sfa_cp = smem + Smem::sfa_cp_off;
+    uint8_t *sfb_cp = smem + Smem::sfb_cp_off;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Smem::bar_off);
+    uint64_t *full = bars;
+    uint64_t *empty = bars + STAGES;
+    uint64_t *tfull = bars + 2 * STAGES;
+    uint64_t *tempty = tfull + 2;
+    uint64_t *done = tempty + 2;
+    uint64_t *sf_done = done + 1;
+    uint64_t *sf_full = sf_done + 1;  // [STAGES]: the stage's scales are in TMEM
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Smem::slot_off);
+    int32_t *tile_prefix = reinterpret_cast<int32_t *>(smem + Smem::misc_off);
+    int32_t *poff = tile_prefix + (p.G + 1);
+    __shared__ int64_t s_total;
+    __shared__ int s_ok;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < STAGES; s++) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+            mbar_init(&sf_full[s], 1);
+        }
+        mbar_init(sf_done, 1);
+        for (int b = 0; b < 2; b++) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 8);  // one arrive per epilogue warp
+        }
+        mbar_init(done, 1);
+        fence_barrier_init();
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB);
+    }
+    if constexpr (MODE != MODE_DENSE) {
+        if (warp == 2) {
+            int64_t tt = 0;
+            const bool ok = build_group_tables(p, MODE, tile_prefix, poff, &tt);
+            if (lane == 0) {
+                s_total = tt;
+                s_ok = ok;
+                if (!ok) record_error(p.err, ERR_BAD_OFFSETS);
+            }
+        }
+    } else {
+        if (threadIdx.x == 0) {
+            s_total = p.total_tiles;
+            s_ok = 1;
+        }
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int64_t total = s_ok ? s_total : 0;
+
+    if (warp == 0 && lane == 0) {
+        // ---------------- producer ----------------
+        int stage = 0;
+        uint32_t phase = 0;
+        int issued_parity[STAGES];
+        for (int s = 0; s < STAGES; s++) issued_parity[s] = -1;
+        bool ok = true;
+        // M-grouped: A's scale layout has one row per padded row (the padded total)
+        const int64_t rsA = MODE == MODE_MGROUP ? (int64_t)poff[p.G] : p.rsA;
+        for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            const Tile ti = tile_info<MODE>(p, t, tile_prefix, poff);
+            const int64_t na = rsA - ti.sa_row, nb = p.rsB - ti.sb_row;
+            const uint32_t sfa_bytes = (uint32_t)((na < BM ? na : BM) * 4);
+            const uint32_t sfb_bytes = (uint32_t)((nb < BN ? nb : BN) * 4);
+            for (int kb = 0; kb < ti.nkb; kb++) {
+                if (!mbar_wait_bounded(&empty[stage], phase ^ 1, WAIT_LIMIT_NS, p.err, ERR_PRODUCER_WAIT)) {
+                    ok = false;
+                    break;
+                }
+                const int64_t kt = ti.kt0 + kb;
+                mbar_arrive_expect_tx(&full[stage], A_BYTES + B_BYTES + sfa_bytes + sfb_bytes);
+                tma_load_2d(sA + stage * A_BYTES, &tmA, ti.x0 + kb * BK, ti.a_y, &full[stage]);
+                tma_load_2d(sB + stage * B_BYTES, &tmB, ti.x0 + kb * BK, ti.b_y, &full[stage]);
+                bulk_load(sfa_raw + stage * SFA_RAW, p.sA + (kt * rsA + ti.sa_row) * 4, sfa_bytes, &full[stage]);
+                bulk_load(sfb_raw + stage * SFB_RAW, p.sB + (kt * p.rsB + ti.sb_row) * 4, sfb_bytes, &full[stage]);
+                issued_parity[stage] = (int)phase;
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+        }
+        for (int s = 0; s < STAGES; s++)
+            if (issued_parity[s] >= 0)
+                mbar_wait_bounded(&full[s], (uint32_t)issued_parity[s], WAIT_LIMIT_NS, p.err, ERR_TEARDOWN_WAIT);
+    } else if (warp == 1 && lane == 0) {
+        // ---------------- MMA issuer ----------------
+        int stage = 0;
+        uint32_t phase = 0;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool ok = true;
+        for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            const Tile ti = tile_info<MODE>(p, t, tile_prefix, poff);
+            if (ti.nkb == 0) continue;  // empty K-grouped block: the epilogue writes zeros
+            if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1, WAIT_LIMIT_NS, p.err, ERR_MMA_WAIT)) break;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + acc_col(acc);
+            for (int kb = 0; kb < ti.nkb; kb++) {
+                // the scale warp's copies of this stage completed (so did its TMA loads)
+                if (!mbar_wait_bounded(&sf_full[stage], phase, WAIT_LIMIT_NS, p.err, ERR_MMA_WAIT)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t sfa = tmem_base + SFA_COL + 4 * stage, sfb = tmem_base + SFB_COL + 8 * stage;
+                const uint32_t a_addr = smem_u32(sA + stage * A_BYTES);
+                const uint32_t b_addr = smem_u32(sB + stage * B_BYTES);
+                const int steps = kb == ti.nkb - 1 ? ti.last_steps : BK / UMMA_K;
+                for (int k = 0; k < steps; k++) {
+                    const uint64_t ad = smem_desc_k128_sw128(a_addr + k * UMMA_K);
+                    const uint64_t bd = smem_desc_k128_sw128(b_addr + k * UMMA_K);
+                    mma_mxf8f6f4(d_tmem, ad, bd, idesc_sf_ids(idesc, (uint32_t)k, (uint32_t)k), sfa, sfb,
+                                 (kb | k) != 0);
+                }
+                mma_commit(&empty[stage]);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+            if (!ok) break;
+            mma_commit(&tfull[acc]);
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1;
+            }
+        }
+        // all issued MMAs complete before TMEM is released
+        mma_commit(done);
+        mbar_wait_bounded(done, 0, WAIT_LIMIT_NS, p.err, ERR_TEARDOWN_WAIT);
+    } else if (warp == 10) {
+        // ---------------- scale factors ----------------
+        // For every stage: rearrange the scale words (row r's word at r) into
+        // the copy blocks (row 32j + L at lane L, word j), copy them into the
+        // stage's TMEM scale columns, and signal sf_full[stage] when the
+        // copies have landed.  Runs ahead of the MMA thread by up to the ring.
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            const Tile ti = tile_info<MODE>(p, t, tile_prefix, poff);
+            for (int kb = 0; kb < ti.nkb; kb++) {
+                if (!mbar_wait_bounded(&full[stage], phase, WAIT_LIMIT_NS, p.err, ERR_MMA_WAIT)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t *ra = reinterpret_cast<const uint32_t *>(sfa_raw + stage * SFA_RAW);
+                const uint32_t *rb = reinterpret_cast<const uint32_t *>(sfb_raw + stage * SFB_RAW);
+                uint8_t *ca = sfa_cp + stage * SFA_CP;
+                uint8_t *cb = sfb_cp + stage * SFB_CP;
+                *reinterpret_cast<uint4 *>(ca + lane * 16) =
+                    make_uint4(ra[lane], ra[32 + lane], ra[64 + lane], ra[96 + lane]);
+                *reinterpret_cast<uint4 *>(cb + lane * 16) =
+                    make_uint4(rb[lane], rb[32 + lane], rb[64 + lane], rb[96 + lane]);
+                *reinterpret_cast<uint4 *>(cb + 512 + lane * 16) =
+                    make_uint4(rb[128 + lane], rb[160 + lane], rb[192 + lane], rb[224 + lane]);
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) {
+                    tc_fence_after();
+                    const uint32_t sfa = tmem_base + SFA_COL + 4 * stage, sfb = tmem_base + SFB_COL + 8 * stage;
+                    tmem_cp_32x128b_x4(sfa, smem_desc_sf(smem_u32(ca)));
+                    tmem_cp_32x128b_x4(sfb, smem_desc_sf(smem_u32(cb)));
+                    tmem_cp_32x128b_x4(sfb + 4, smem_desc_sf(smem_u32(cb + 512)));
+                    mma_commit(&sf_full[stage]);
+                }
+                __syncwarp();
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+        }
+        // every issued copy lands before TMEM is released
+        if (lane == 0) {
+            mma_commit(sf_done);
+            mbar_wait_bounded(sf_done, 0, WAIT_LIMIT_NS, p.err, ERR_TEARDOWN_WAIT);
+        }
+        __syncwarp();
+    } else if (warp >= 2 && warp < 10) {
+        // ---------------- epilogue ----------------
+        // warp w reads TMEM lane quarter w % 4; the two warps of a quarter
+        // split the 224 columns 128 + 96
+        const int q = warp & 3;
+        const int half = (warp - 2) >> 2;
+        const int cb = half ? 128 : 0, ce = half ? BN : 128;
+        uint8_t *stage = smem + Smem::stage_off + (warp - 2) * Smem::stage_warp_bytes;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
+            const Tile ti = tile_info<MODE>(p, t, tile_prefix, poff);
+            if (ti.nkb == 0) {
+                const int64_t gr = ti.row0 + q * 32 + lane;
+                if (gr < ti.row_end) {
+                    uint16_t *crow = p.C + ti.c_base + gr * p.ldc;
+                    const int64_t c1 = ti.col0 + ce < ti.col_end ? ti.col0 + ce : ti.col_end;
+                    for (int64_t c = ti.col0 + cb; c < c1; c++) crow[c] = 0;
+                }
+                continue;
+            }
+            if (!mbar_wait_bounded(&tfull[acc], acc_phase, WAIT_LIMIT_NS, p.err, ERR_EPILOGUE_WAIT)) break;
+            tc_fence_after();
+            epilogue_tile(p, ti, tmem_base, acc_col(acc), q, cb, ce, lane, stage);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[acc]);
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// 2D map over a row-major u8 matrix [rows][ld] (inner extent `cols`), box
+// {128 bytes, box_rows}, 128-byte swizzle, zero fill out of bounds.
+static bool make_map(CUtensorMap *map, const void *base, int64_t rows, int64_t cols, int64_t ld, int box_rows)
+{
+    EncodeTiledFn enc = get_encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)ld};
+    cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+static size_t smem_bytes(int G) { return 1024 + Smem::misc_off + (G > 0 ? 8 * (size_t)(G + 1) : 0); }
+
+template <int MODE>
+static fp8_status_t launch(const CUtensorMap &ma, const CUtensorMap &mb, const Params &p, int fa, int fb,
+                           int64_t grid, cudaStream_t st)
+{
+    const size_t smem = smem_bytes(MODE == MODE_DENSE ? 0 : p.G);
+    cudaError_t e = cudaFuncSetAttribute(mx_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return cuda_fail_with(e);
+    const uint32_t idesc = idesc_mxf8f6f4(fa, fb, BM, BN);
+    mx_gemm_kernel<MODE><<<(unsigned)grid, THREADS, smem, st>>>(ma, mb, p, idesc);
+    return check_launch();
+}
+
+static bool format_ok(int f) { return f == FP8_E4M3FN || f == FP8_E5M2; }
+
+}  // namespace mx
+}  // namespace fp8gb
+
+using namespace fp8gb;
+
+extern "C" fp8_status_t fp8_mx_gemm(const uint8_t *A, int fa, int64_t lda, const uint8_t *sA, const uint8_t *B,
+                                    int fb, int64_t ldb, const uint8_t *sB, int64_t M, int64_t N, int64_t K,
+                                    void *C_bf16, int64_t ldc, void *stream)
+{
+    if (!A || !B || !sA || !sB || !C_bf16) return FP8_ERR_INVALID_ARG;
+    if (fa == FP8_E4M3FNUZ || fb == FP8_E4M3FNUZ || fa == FP8_E5M2FNUZ || fb == FP8_E5M2FNUZ)
+        return FP8_ERR_UNSUPPORTED;
+    if (!mx::format_ok(fa) || !mx::format_ok(fb)) return FP8_ERR_INVALID_ARG;
+    if (M < 1 || N < 1 || K < 1 || lda < K || ldb < K || ldc < N) return FP8_ERR_INVALID_ARG;
+    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return FP8_ERR_INVALID_ARG;
+    if (K % FP8_MX_BLOCK != 0 || lda % 16 != 0 || ldb % 16 != 0) return FP8_ERR_ALIGNMENT;
+    if (!aligned(A, 16) || !aligned(B, 16) || !aligned(sA, 16) || !aligned(sB, 16) || !aligned(C_bf16, 2))
+        return FP8_ERR_ALIGNMENT;
+
+    mx::Params p{};
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.sA = sA;
+    p.sB = sB;
+    p.rsA = (M + 3) / 4 * 4;
+    p.rsB = (N + 3) / 4 * 4;
+    p.C = static_cast<uint16_t *>(C_bf16);
+    p.ldc = ldc;
+    p.c_vec16 = ldc % 8 == 0 && aligned(C_bf16, 16);
+    p.num_m_blk = (int)((M + mx::BM - 1) / mx::BM);
+    p.num_n_blk = (int)((N + mx::BN - 1) / mx::BN);
+    p.num_k_blk = (int)((K + mx::BK - 1) / mx::BK);
+    p.m_fastest = M <= N;
+    p.total_tiles = (int64_t)p.num_m_blk * p.num_n_blk;
+    p.err = device_error_word();
+
+    CUtensorMap ma, mb;
+    if (!mx::make_map(&ma, A, M, K, lda, mx::BM) || !mx::make_map(&mb, B, N, K, ldb, mx::BN)) return FP8_ERR_CUDA;
+    const int64_t grid = p.total_tiles < num_sms() ? p.total_tiles : num_sms();
+    return mx::launch<mx::MODE_DENSE>(ma, mb, p, fa, fb, grid, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" fp8_status_t fp8_mx_grouped_gemm(int mode, const uint8_t *A, int fa, const uint8_t *sA,
+                                            const uint8_t *B, int fb, const uint8_t *sB,
+                                            const int32_t *group_offsets, int G, int64_t M_total, int64_t N,
+                                            int64_t K, void *C_bf16, int64_t ld_T, void *stream)
+{
+    if (!A || !B || !sA || !sB || !C_bf16 || !group_offsets) return FP8_ERR_INVALID_ARG;
+    if (fa == FP8_E4M3FNUZ || fb == FP8_E4M3FNUZ || fa == FP8_E5M2FNUZ || fb == FP8_E5M2FNUZ)
+        return FP8_ERR_UNSUPPORTED;
+    if (!mx::format_ok(fa) || !mx::format_ok(fb)) return FP8_ERR_INVALID_ARG;
+    if (mode != FP8_GROUPED_M && mode != FP8_GROUPED_K) return FP8_ERR_INVALID_ARG;
+    if (G < 1 || G > mx::MAX_GROUPS || M_total < 0 || N < 1 || K < 1) return FP8_ERR_INVALID_ARG;
+    if (M_total > INT32_MAX || N > INT32_MAX || K > INT32_MAX || (int64_t)G * N > INT32_MAX)
+        return FP8_ERR_INVALID_ARG;
+    if (!aligned(A, 16) || !aligned(B, 16) || !aligned(sA, 16) || !aligned(sB, 16) || !aligned(C_bf16, 2))
+        return FP8_ERR_ALIGNMENT;
+
+    mx::Params p{};
+    p.M = M_total;
+    p.N = N;
+    p.K = K;
+    p.sA = sA;
+    p.sB = sB;
+    p.C = static_cast<uint16_t *>(C_bf16);
+    p.offsets = group_offsets;
+    p.G = G;
+    p.err = device_error_word();
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    CUtensorMap ma, mb;
+    const int64_t grid = num_sms();
+
+    if (mode == FP8_GROUPED_M) {
+        if (K % FP8_MX_BLOCK != 0 || N % 4 != 0) return FP8_ERR_ALIGNMENT;
+        p.rsA = 0;  // the padded total, known on the device from the offsets
+        p.rsB = (int64_t)G * N;
+        p.ldc = N;
+        p.c_vec16 = N % 8 == 0 && aligned(C_bf16, 16);
+        p.num_m_blk = 0;
+        p.num_n_blk = (int)((N + mx::BN - 1) / mx::BN);
+        p.num_k_blk = (int)((K + mx::BK - 1) / mx::BK);
+        if (M_total == 0) return FP8_OK;
+        if (!mx::make_map(&ma, A, M_total, K, K, mx::BM) || !mx::make_map(&mb, B, (int64_t)G * N, K, K, mx::BN))
+            return FP8_ERR_CUDA;
+        return mx::launch<mx::MODE_MGROUP>(ma, mb, p, fa, fb, grid, st);
+    }
+    // K-grouped (wgrad): C[e] = A_e [N][m_e] . B_e [K][m_e]^T
+    if (ld_T < 128 || ld_T % 128 != 0 || N % 4 != 0 || K % 4 != 0) return FP8_ERR_ALIGNMENT;
+    p.rsA = N;
+    p.rsB = K;
+    p.ldc = K;
+    p.c_vec16 = K % 8 == 0 && aligned(C_bf16, 16);
+    p.ld_T = ld_T;
+    p.num_m_blk = (int)((N + mx::BM - 1) / mx::BM);
+    p.num_n_blk = (int)((K + mx::BN - 1) / mx::BN);
+    p.num_k_blk = 0;
+    if (!mx::make_map(&ma, A, N, ld_T, ld_T, mx::BM) || !mx::make_map(&mb, B, K, ld_T, ld_T, mx::BN))
+        return FP8_ERR_CUDA;
+    return mx::launch<mx::MODE_KGROUP>(ma, mb, p, fa, fb, grid, st);
+}

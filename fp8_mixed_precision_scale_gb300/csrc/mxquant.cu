@@ -1,0 +1,342 @@
+// mxquant.cu -- MXFP8 quantize: blocks of 32 elements that share one E8M0
+// (power-of-two) scale, emitting the row layout (blocks along rows) and the
+// transposed layout (blocks along columns) from one read of the bf16 input.
+//
+// Method: the "mxfp8" recipe of "FP8 training for Flux models" (Configuration
+// > Key FP8 Parameters) and the MXFP8 grouped GEMM of "FP8 Training on AMD
+// GPUs with TorchTitan and TorchAO"; the block rule is the OCP Microscaling
+// v1.0 one: X = 2^(floor(log2 amax) - emax_elem), element = sat_rne(v / X).
+//
+// Design (GB300): 256-thread blocks on tiles of 64 rows x 128 columns.
+//   Row layout: thread (row, block) loads its 32 bf16 (4 x 16-byte loads),
+//     takes the packed |bf16| maximum, derives the E8M0 code from the fp32
+//     exponent bits, multiplies by 2^(127 - code) (exact) and converts with
+//     cvt.rn.satfinite; the four blocks of a row combine their codes into one
+//     32-bit word of the scale layout by two shuffles.
+//   Transposed layout: the tile is staged in shared memory; thread (column,
+//     half) reads its 32 rows, computes that block's code and writes 32
+//     contiguous bytes of q_colT (one sector) and one scale byte.
+// One launch, no atomics, no scratch memory: every block's scale depends
+// only on its own 32 elements.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "fp8gb.h"
+#include "fp8gb_device.cuh"
+#include "fp8gb_host.h"
+
+namespace fp8gb {
+
+constexpr int MX_THREADS = 256;
+constexpr int MX_ROWS = 64;             // rows per tile
+constexpr int MX_COLS = 128;            // columns per tile: four blocks of a row
+constexpr int MX_PITCH = MX_COLS + 8;   // bf16 per shared-memory row (16-byte pad)
+constexpr int MX_MAX_GROUPS = 4096;
+
+struct MxArgs {
+    const uint16_t *x;
+    int64_t rows, cols, ld_x;
+    uint8_t *q_row, *s_row, *q_colT, *s_col;
+    int64_t ld_colT;
+    int64_t rs_row;       // scale rows of s_row rounded up to 4 (ungrouped)
+    int64_t n_row_tiles;  // grouped: an upper bound (tiles past the padded total exit)
+    int64_t n_col_tiles;
+    const int32_t *offsets;
+    int G;
+    int do_row, do_col;
+    unsigned int *err;
+};
+
+// E8M0 code of a block from the fp32 bit pattern of its largest magnitude:
+// floor(log2 amax) is the exponent field (normal) or the position of the top
+// mantissa bit (subnormal), minus emax_elem, clamped to [-127, 127].
+template <int FMT>
+__device__ __forceinline__ uint32_t mx_code(uint32_t amax_bits)
+{
+    constexpr int emax = FMT == FP8_E5M2 ? 15 : 8;
+    if (amax_bits >= 0x7F800000u) return 255u;  // Inf or NaN in the block
+    if (amax_bits == 0u) return 0u;
+    const int ex = (int)(amax_bits >> 23);
+    const int fl = ex > 0 ? ex - 127 : (31 - __clz((int)amax_bits)) - 149;
+    int e = fl - emax;
+    e = e < -127 ? -127 : (e > 127 ? 127 : e);
+    return (uint32_t)(e + 127);
+}
+
+// 1 / X = 2^(127 - code) as an fp32 (a normal number for every code a bf16
+// block can produce); NaN for the NaN scale, so the block's elements are NaN.
+__device__ __forceinline__ float mx_inv_scale(uint32_t code)
+{
+    if (code == 255u) return __uint_as_float(0x7FC00000u);
+    return code <= 253u ? __uint_as_float((254u - code) << 23) : __uint_as_float(0x00400000u);
+}
+
+// Exclusive prefix of roundup(m_e, FP8_MX_GROUP_ALIGN) over the groups, by
+// warp 0 into shared memory; flags malformed offsets and a padded total that
+// does not fit ld_colT.
+__device__ void mx_padded_offsets(const MxArgs &a, int32_t *poff, int *bad)
+{
+    if (threadIdx.x >= 32) return;
+    constexpr int AL = FP8_MX_GROUP_ALIGN;
+    const int lane = threadIdx.x;
+    const int G = a.G;
+    const int per = (G + 31) / 32;
+    const int g0 = min(G, lane * per), g1 = min(G, g0 + per);
+    int64_t local = 0;
+    int badl = 0;
+    for (int e = g0; e < g1; e++) {
+        const int m = a.offsets[e + 1] - a.offsets[e];
+        if (m < 0) badl = 1;
+        local += (int64_t)((max(m, 0) + AL - 1) / AL) * AL;
+    }
+    int64_t incl = local;
+    for (int d = 1; d < 32; d <<= 1) {
+        const int64_t v = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += v;
+    }
+    int64_t run = incl - local;
+    for (int e = g0; e < g1; e++) {
+        poff[e] = (int32_t)run;
+        run += (int64_t)((max(a.offsets[e + 1] - a.offsets[e], 0) + AL - 1) / AL) * AL;
+    }
+    const int64_t total = __shfl_sync(0xffffffffu, incl, 31);
+    badl = __any_sync(0xffffffffu, badl);
+    if (lane == 0) {
+        poff[G] = (int32_t)total;
+        const int b = badl || a.offsets[0] != 0 || (int64_t)a.offsets[G] != a.rows ||
+                      (a.do_col && total > a.ld_colT) || total > INT32_MAX;
+        *bad = b;
+        if (b) record_error(a.err, ERR_BAD_OFFSETS);
+    }
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(MX_THREADS)
+    mx_quantize_kernel(MxArgs a)
+{
+    __shared__ __align__(16) uint16_t tile[MX_ROWS * MX_PITCH];
+    extern __shared__ int32_t poff[];  // grouped: [G + 1]
+    __shared__ int s_bad;
+
+    const int tid = threadIdx.x;
+    int64_t prows = a.rows;  // rows of the (padded) row space
+    if (a.offsets) {
+        mx_padded_offsets(a, poff, &s_bad);
+        __syncthreads();
+        if (s_bad) return;
+        prows = poff[a.G];
+    }
+    const int64_t total = a.n_row_tiles * a.n_col_tiles;
+    const int64_t last_rt = prows > 0 ? (prows - 1) / MX_ROWS : -1;
+
+    for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
+        const int64_t rt = t / a.n_col_tiles, ct = t % a.n_col_tiles;
+        const int64_t pr0 = rt * MX_ROWS;  // first row of the tile in the padded row space
+        if (pr0 >= prows) {
+            if (!a.offsets) break;
+            continue;  // grouped: beyond the padded total
+        }
+        const int64_t c0 = ct * MX_COLS;
+
+        // map the tile's rows to input rows: ungrouped identity; grouped, the
+        // tile lies inside one group (groups are padded to 128 rows)
+        int64_t src0 = pr0, nreal = a.rows - pr0 < MX_ROWS ? a.rows - pr0 : MX_ROWS;
+        if (a.offsets) {
+            int lo = 0, hi = a.G;  // poff[lo] <= pr0 < poff[hi]
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (poff[mid] <= pr0)
+                    lo = mid;
+                else
+                    hi = mid;
+            }
+            const int64_t local0 = pr0 - poff[lo];
+            const int64_t m_e = (int64_t)a.offsets[lo + 1] - a.offsets[lo];
+            src0 = a.offsets[lo] + local0;
+            nreal = m_e - local0 < MX_ROWS ? m_e - local0 : MX_ROWS;
+            if (nreal < 0) nreal = 0;
+        }
+
+        // ---- load: thread (lr, blk) takes 32 bf16 of one row ----
+        const int lr = tid >> 2, blk = tid & 3;
+        const bool row_real = lr < nreal;
+        const bool blk_ok = c0 + 32 * blk < a.cols;
+        uint4 v[4];
+        if (row_real && blk_ok) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(a.x + (src0 + lr) * a.ld_x + c0 + 32 * blk);
+#pragma unroll
+            for (int j = 0; j < 4; j++) v[j] = __ldg(src + j);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; j++) v[j] = make_uint4(0, 0, 0, 0);
+        }
+
+        // ---- row layout ----
+        if (a.do_row) {
+            uint32_t am = 0;
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                am = absmax_bf16x2(am, v[j].x);
+                am = absmax_bf16x2(am, v[j].y);
+                am = absmax_bf16x2(am, v[j].z);
+                am = absmax_bf16x2(am, v[j].w);
+            }
+            const uint32_t code = blk_ok ? mx_code<FMT>(fold_absmax(am)) : 0u;
+            if (row_real && blk_ok) {
+                const float inv = mx_inv_scale(code);
+                uint32_t out[8];
+#pragma unroll
+                for (int j = 0; j < 4; j++) {
+                    const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+                    const uint32_t b01 = cvt2<FMT>(bf16lo(w[0]) * inv, bf16hi(w[0]) * inv);
+                    const uint32_t b23 = cvt2<FMT>(bf16lo(w[1]) * inv, bf16hi(w[1]) * inv);
+                    const uint32_t b45 = cvt2<FMT>(bf16lo(w[2]) * inv, bf16hi(w[2]) * inv);
+                    const uint32_t b67 = cvt2<FMT>(bf16lo(w[3]) * inv, bf16hi(w[3]) * inv);
+                    out[2 * j] = b01 | (b23 << 16);
+                    out[2 * j + 1] = b45 | (b67 << 16);
+                }
+                uint4 *dst = reinterpret_cast<uint4 *>(a.q_row + (src0 + lr) * a.cols + c0 + 32 * blk);
+                dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
+                dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
+            }
+            // the four blocks of the row (lanes 4i .. 4i+3) form one scale word
+            uint32_t word = code << (8 * blk);
+            word |= __shfl_xor_sync(0xffffffffu, word, 1);
+            word |= __shfl_xor_sync(0xffffffffu, word, 2);
+            const int64_t srow = pr0 + lr;  // scale row (padded row space)
+            const int64_t srows = a.offsets ? prows : a.rs_row;
+            if (blk == 0 && srow < srows)
+                *reinterpret_cast<uint32_t *>(a.s_row + (ct * srows + srow) * 4) = word;
+        }
+
+        // ---- transposed layout ----
+        if (a.do_col) {
+#pragma unroll
+            for (int j = 0; j < 4; j++)
+                *reinterpret_cast<uint4 *>(&tile[lr * MX_PITCH + 32 * blk + 8 * j]) = v[j];
+            __syncthreads();
+            const int cl = tid & 127, h = tid >> 7;
+            const int64_t c = c0 + cl;
+            const int64_t kb = (pr0 >> 5) + h;  // block index along the rows
+            const bool blk_valid = pr0 + 32 * h < prows;
+            if (c < a.cols) {
+                uint32_t e[32];
+                uint32_t am = 0;
+#pragma unroll
+                for (int i = 0; i < 32; i++) {
+                    e[i] = tile[(32 * h + i) * MX_PITCH + cl];
+                    const uint32_t m = e[i] & 0x7FFFu;
+                    am = m > am ? m : am;
+                }
+                const uint32_t code = blk_valid ? mx_code<FMT>(am << 16) : 0u;
+                uint8_t *sc = a.s_col + ((kb >> 2) * a.cols + c) * 4 + (kb & 3);
+                if (blk_valid) {
+                    const float inv = mx_inv_scale(code);
+                    uint32_t out[8];
+#pragma unroll
+                    for (int i = 0; i < 8; i++) {
+                        const uint32_t b01 = cvt2<FMT>(__uint_as_float(e[4 * i] << 16) * inv,
+                                                       __uint_as_float(e[4 * i + 1] << 16) * inv);
+                        const uint32_t b23 = cvt2<FMT>(__uint_as_float(e[4 * i + 2] << 16) * inv,
+                                                       __uint_as_float(e[4 * i + 3] << 16) * inv);
+                        out[i] = b01 | (b23 << 16);
+                    }
+                    uint4 *dst = reinterpret_cast<uint4 *>(a.q_colT + c * a.ld_colT + pr0 + 32 * h);
+                    dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
+                    dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
+                }
+                *sc = (uint8_t)code;
+                // the last word's blocks past the data are written as 0
+                if (rt == last_rt && (kb & 3) < 2) sc[2] = 0;
+            }
+            __syncthreads();  // the tile is rewritten by the next iteration
+        }
+    }
+}
+
+template <int FMT>
+static fp8_status_t launch_mx(const MxArgs &a, cudaStream_t st)
+{
+    const size_t dyn = a.offsets ? (size_t)(a.G + 1) * sizeof(int32_t) : 0;
+    const int64_t total = a.n_row_tiles * a.n_col_tiles;
+    int64_t grid = total;
+    if (a.offsets) {
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mx_quantize_kernel<FMT>, MX_THREADS, dyn) !=
+            cudaSuccess)
+            return cuda_fail();
+        const int64_t cap = (int64_t)num_sms() * (per_sm > 0 ? per_sm : 1);
+        grid = total < cap ? total : cap;
+    }
+    if (grid > INT32_MAX) grid = INT32_MAX;
+    if (grid < 1) return FP8_OK;
+    mx_quantize_kernel<FMT><<<(unsigned)grid, MX_THREADS, dyn, st>>>(a);
+    return check_launch();
+}
+
+}  // namespace fp8gb
+
+using namespace fp8gb;
+
+extern "C" int64_t fp8_mx_scale_bytes(int64_t scale_rows, int64_t blocks)
+{
+    if (scale_rows < 0 || blocks < 0) return -1;
+    return (blocks + 3) / 4 * ((scale_rows + 3) / 4 * 4) * 4;
+}
+
+extern "C" fp8_status_t fp8_mx_quantize(const void *x_bf16, int64_t rows, int64_t cols, int64_t ld_x, int fmt,
+                                        int layouts, uint8_t *q_row, uint8_t *s_row, uint8_t *q_colT,
+                                        int64_t ld_colT, uint8_t *s_col, const int32_t *group_offsets,
+                                        int num_groups, void *stream)
+{
+    if (rows < 0 || cols < 1 || ld_x < cols) return FP8_ERR_INVALID_ARG;
+    if (fmt == FP8_E4M3FNUZ || fmt == FP8_E5M2FNUZ) return FP8_ERR_UNSUPPORTED;
+    if (fmt != FP8_E4M3FN && fmt != FP8_E5M2) return FP8_ERR_INVALID_ARG;
+    if (layouts < 1 || layouts > 3) return FP8_ERR_INVALID_ARG;
+    if (rows == 0) return FP8_OK;  // nothing to read or write (an all-empty grouped tensor has P = 0)
+    if (!x_bf16) return FP8_ERR_INVALID_ARG;
+    const bool do_row = layouts & FP8_LAYOUT_ROW, do_col = layouts & FP8_LAYOUT_COLT;
+    if (do_row && (!q_row || !s_row)) return FP8_ERR_INVALID_ARG;
+    if (do_col && (!q_colT || !s_col)) return FP8_ERR_INVALID_ARG;
+    if (group_offsets && (num_groups < 1 || num_groups > MX_MAX_GROUPS)) return FP8_ERR_INVALID_ARG;
+    if (!group_offsets && num_groups != 0) return FP8_ERR_INVALID_ARG;
+    if (rows > INT32_MAX || cols > INT32_MAX) return FP8_ERR_INVALID_ARG;
+    if (cols % FP8_MX_BLOCK != 0 || ld_x % 8 != 0 || !aligned(x_bf16, 16)) return FP8_ERR_ALIGNMENT;
+    if (do_row && (!aligned(q_row, 16) || !aligned(s_row, 4))) return FP8_ERR_ALIGNMENT;
+    if (do_col) {
+        if (ld_colT < 16 || ld_colT % 16 != 0 || !aligned(q_colT, 16)) return FP8_ERR_ALIGNMENT;
+        if (!group_offsets) {
+            if (rows % FP8_MX_BLOCK != 0) return FP8_ERR_ALIGNMENT;
+            if (ld_colT < rows) return FP8_ERR_INVALID_ARG;
+        }
+    }
+    MxArgs a{};
+    a.x = static_cast<const uint16_t *>(x_bf16);
+    a.rows = rows;
+    a.cols = cols;
+    a.ld_x = ld_x;
+    a.q_row = q_row;
+    a.s_row = s_row;
+    a.q_colT = q_colT;
+    a.s_col = s_col;
+    a.ld_colT = ld_colT;
+    a.rs_row = (rows + 3) / 4 * 4;
+    a.n_col_tiles = (cols + MX_COLS - 1) / MX_COLS;
+    a.offsets = group_offsets;
+    a.G = group_offsets ? num_groups : 0;
+    a.do_row = do_row;
+    a.do_col = do_col;
+    a.err = device_error_word();
+    if (group_offsets) {
+        // padded row space: at most 127 padding rows per group, and within ld_colT
+        int64_t bound = rows + (int64_t)(FP8_MX_GROUP_ALIGN - 1) * num_groups;
+        if (do_col && ld_colT < bound) bound = ld_colT;
+        a.n_row_tiles = (bound + MX_ROWS - 1) / MX_ROWS;
+    } else {
+        a.n_row_tiles = (a.rs_row + MX_ROWS - 1) / MX_ROWS;
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (fmt == FP8_E5M2) return launch_mx<FP8_E5M2>(a, st);
+    return launch_mx<FP8_E4M3FN>(a, st);
+}

@@ -228,6 +228,108 @@ FP8GB_API fp8_status_t fp8_grouped_gemm(int mode, const uint8_t *A, int fa, cons
  */
 FP8GB_API int64_t fp8_group_padded_offsets(const int32_t *host_offsets, int G, int align, int64_t *host_padded_out);
 
+/* ------------------------------------------------------------------------
+ * MXFP8 -- the "mxfp8" recipe ("FP8 training for Flux models", Key FP8
+ * Parameters, fp8_recipe) and the MXFP8 grouped GEMM ("FP8 Training on AMD
+ * GPUs with TorchTitan and TorchAO", next work).  The pages name it without
+ * a definition; this library follows the OCP Microscaling (MX) v1.0
+ * specification: blocks of 32 consecutive elements along the contraction
+ * dimension share one power-of-two scale X = 2^e stored as an E8M0 byte
+ * (code e + 127; 255 = NaN), e = floor(log2(block amax)) - emax_elem
+ * (emax_elem = 8 for E4M3, 15 for E5M2) clamped to [-127, 127], and each
+ * element is sat_rne_fp8(v / X).  An all-zero block has code 0; a block
+ * holding a NaN or Inf has code 255 and NaN elements.
+ *
+ * MX scale layout.  The E8M0 codes of an operand with R scale rows and KB
+ * blocks per row are bytes [ceil(KB / 4)][roundup(R, 4)][4]: the scale of
+ * block b of row r is at byte ((b / 4) * roundup(R, 4) + r) * 4 + b % 4.  A
+ * row's four blocks of one 128-element K tile form one 32-bit word and the
+ * words of consecutive rows are contiguous, so the scales of a GEMM tile are
+ * a single contiguous copy.  Bytes of blocks past KB and of rows past R are
+ * written as 0.  Grouped MX layouts pad every group to FP8_MX_GROUP_ALIGN
+ * rows (fp8_group_padded_offsets with that align gives the padded offsets
+ * and the total P).
+ * ------------------------------------------------------------------------ */
+#define FP8_MX_BLOCK 32
+#define FP8_MX_GROUP_ALIGN 128
+
+/* Bytes of an MX scale buffer for R scale rows and KB blocks per row. */
+FP8GB_API int64_t fp8_mx_scale_bytes(int64_t scale_rows, int64_t blocks);
+
+/*
+ * fp8_mx_quantize -- MX quantize of a bf16 matrix, emitting the row layout
+ * (blocks along each row), the transposed layout (blocks along each column,
+ * stored column-major), or both, from one read of x.  The two layouts have
+ * their own blocks, so q_colT is not the transpose of q_row.
+ *
+ *   x_bf16     [rows][ld_x] bf16; 16-byte aligned, ld_x % 8 == 0, ld_x >= cols.
+ *              rows == 0 returns FP8_OK without touching any buffer.
+ *   rows >= 0; cols >= 32, cols % 32 == 0.
+ *   fmt        FP8_E4M3FN or FP8_E5M2 (FP8_ERR_UNSUPPORTED for the fnuz
+ *              formats, which MX does not define).
+ *   layouts    FP8_LAYOUT_ROW | FP8_LAYOUT_COLT (at least one).
+ *   q_row      [rows][cols] u8, 16-byte aligned  (FP8_LAYOUT_ROW).
+ *   s_row      MX scale layout, R = rows (grouped: the padded total P),
+ *              KB = cols / 32; 4-byte aligned.  Grouped: row r of group e
+ *              has scale row poff_e + (r - offsets[e]); padding rows are
+ *              all-zero blocks (code 0).
+ *   q_colT     [cols][ld_colT] u8, 16-byte aligned, ld_colT % 16 == 0
+ *              (FP8_LAYOUT_COLT).  Ungrouped: rows % 32 == 0, ld_colT >=
+ *              rows, column c holds x[0..rows)[c]; bytes past rows are left
+ *              untouched.  Grouped: ld_colT >= P; group e's rows start at
+ *              column poff_e and are followed by zero bytes up to poff_(e+1).
+ *   s_col      MX scale layout, R = cols, KB = rows / 32 (grouped: P / 32).
+ *   group_offsets  NULL, or device int32 [num_groups + 1] row ranges as for
+ *              fp8_quantize (1 <= num_groups <= 4096).  Malformed offsets,
+ *              or P > ld_colT, set the device error word (fp8_sync_status
+ *              reports FP8_ERR_INVALID_ARG) and nothing is written.
+ * Ownership: every buffer is caller-owned device memory; nothing is
+ * allocated.  Errors: FP8_ERR_INVALID_ARG / FP8_ERR_UNSUPPORTED /
+ * FP8_ERR_ALIGNMENT before any launch, FP8_ERR_CUDA on a launch failure.
+ */
+FP8GB_API fp8_status_t fp8_mx_quantize(const void *x_bf16, int64_t rows, int64_t cols, int64_t ld_x, int fmt,
+                                       int layouts, uint8_t *q_row, uint8_t *s_row, uint8_t *q_colT,
+                                       int64_t ld_colT, uint8_t *s_col, const int32_t *group_offsets,
+                                       int num_groups, void *stream);
+
+/*
+ * fp8_mx_gemm -- C[m][n] = bf16( sum_k A[m][k] X_A(m, k/32) B[n][k] X_B(n, k/32) )
+ * on the tcgen05 block-scaled tensor cores (kind::mxf8f6f4, scales read by
+ * the MMA from tensor memory), fp32 accumulation, "TN" operands.
+ *
+ *   A  u8 [M][lda] format fa, sA its MX scales (R = M, KB = K / 32);
+ *   B  u8 [N][ldb] format fb, sB its MX scales (R = N, KB = K / 32);
+ *   fa, fb: FP8_E4M3FN or FP8_E5M2.  M, N >= 1; K >= 32, K % 32 == 0;
+ *   lda, ldb >= K, % 16 == 0; A, B 16-byte aligned; sA, sB 16-byte aligned.
+ *   C_bf16 [M][ldc], ldc >= N, 2-byte aligned.
+ * fprop takes A = X row layout, B = W row layout; dgrad A = dY row layout,
+ * B = W transposed layout; wgrad A = dY transposed, B = X transposed, each
+ * with the scales fp8_mx_quantize wrote beside it.
+ */
+FP8GB_API fp8_status_t fp8_mx_gemm(const uint8_t *A, int fa, int64_t lda, const uint8_t *sA, const uint8_t *B,
+                                   int fb, int64_t ldb, const uint8_t *sB, int64_t M, int64_t N, int64_t K,
+                                   void *C_bf16, int64_t ldc, void *stream);
+
+/*
+ * fp8_mx_grouped_gemm -- the MX counterpart of fp8_grouped_gemm (groups
+ * padded to FP8_MX_GROUP_ALIGN in every padded layout).
+ *
+ * FP8_GROUPED_M: A u8 [M_total][K] (group rows stacked), sA the row-layout
+ *   scales of a grouped fp8_mx_quantize (R = P, KB = K / 32); B u8 [G][N][K],
+ *   sB its scales as one [G*N][K] operand (R = G * N); C bf16 [M_total][N].
+ * FP8_GROUPED_K: A u8 [N][ld_T], B u8 [K][ld_T] the transposed layouts of
+ *   grouped fp8_mx_quantize calls (ld_T their ld_colT), sA / sB their scales
+ *   (R = N / K, KB = P / 32 with P the padded total); C[e] = A_e . B_e^T
+ *   over group e's padded columns, C bf16 [G][N][K]; an empty group's block
+ *   is 0.
+ * Limits: K % 32 == 0 (M mode); N % 4 == 0 (M mode); ld_T % 128 == 0
+ * (K mode); 1 <= G <= 1024; A, B, sA, sB 16-byte aligned.
+ */
+FP8GB_API fp8_status_t fp8_mx_grouped_gemm(int mode, const uint8_t *A, int fa, const uint8_t *sA,
+                                           const uint8_t *B, int fb, const uint8_t *sB,
+                                           const int32_t *group_offsets, int G, int64_t M_total, int64_t N,
+                                           int64_t K, void *C_bf16, int64_t ld_T, void *stream);
+
 /* Synchronise `stream`, then report and clear a device-side timeout word:
  * FP8_OK, FP8_ERR_TIMEOUT, or FP8_ERR_CUDA. */
 FP8GB_API fp8_status_t fp8_sync_status(void *stream);

@@ -100,3 +100,15 @@ def sample_points(gen: torch.Generator, M: int, N: int, n_rows=64, n_cols=64, n_
 
 def bits(t: torch.Tensor) -> np.ndarray:
     return synth.bf16_bits(t)
+
+
+def mx_tiled(plain: np.ndarray) -> np.ndarray:
+    """Plain E8M0 codes [R][KB] -> the bytes of the MX scale layout
+    [ceil(KB/4)][roundup(R, 4)][4] (scale of block b of row r at
+    ((b // 4) * roundup(R, 4) + r) * 4 + b % 4; pad bytes 0)."""
+    R, KB = plain.shape
+    KT = -(-KB // 4)
+    Rs = -(-R // 4) * 4
+    padded = np.zeros((Rs, KT * 4), np.uint8)
+    padded[:R, :KB] = plain
+    return np.ascontiguousarray(padded.reshape(Rs, KT, 4).transpose(1, 0, 2)).reshape(-1)

@@ -181,3 +181,78 @@ def test_format_roles():
     assert fp8.format_for("e4m3", "grad") == fp8.E4M3FN
     assert fp8.format_for("hybrid", "grad") == fp8.E5M2
     assert fp8.format_for("hybrid", "weight") == fp8.E4M3FN
+
+
+def test_mx_scale_bytes(lib):
+    assert lib.fp8_mx_scale_bytes(5, 5) == 2 * 8 * 4      # ceil(5/4) K tiles x roundup(5,4) rows x 4
+    assert lib.fp8_mx_scale_bytes(128, 128) == 32 * 128 * 4
+    assert lib.fp8_mx_scale_bytes(0, 4) == 0
+    assert lib.fp8_mx_scale_bytes(-1, 4) == -1
+
+
+def mxq_call(lib, **kw):
+    a = dict(x=FAKE, rows=64, cols=64, ld_x=64, fmt=0, layouts=3, q_row=FAKE, s_row=FAKE, q_colT=FAKE, ld_colT=64,
+             s_col=FAKE, off=None, G=0)
+    a.update(kw)
+    P = ctypes.c_void_p
+    return lib.fp8_mx_quantize(P(a["x"]), a["rows"], a["cols"], a["ld_x"], a["fmt"], a["layouts"], P(a["q_row"]),
+                               P(a["s_row"]), P(a["q_colT"]), a["ld_colT"], P(a["s_col"]), P(a["off"]), a["G"],
+                               None)
+
+
+def test_mx_quantize_validation(lib):
+    assert mxq_call(lib, x=None) == INVALID
+    assert mxq_call(lib, fmt=2) == UNSUPPORTED
+    assert mxq_call(lib, fmt=3) == UNSUPPORTED
+    assert mxq_call(lib, fmt=4) == INVALID
+    assert mxq_call(lib, layouts=0) == INVALID
+    assert mxq_call(lib, q_row=None) == INVALID
+    assert mxq_call(lib, s_col=None) == INVALID
+    assert mxq_call(lib, cols=48, ld_x=64) == ALIGN        # blocks of 32 along the row
+    assert mxq_call(lib, rows=40) == ALIGN                 # transposed layout: blocks of 32 rows
+    assert mxq_call(lib, ld_colT=48) == INVALID            # shorter than rows
+    assert mxq_call(lib, ld_colT=72) == ALIGN
+    assert mxq_call(lib, x=FAKE + 8) == ALIGN
+    assert mxq_call(lib, s_row=FAKE + 2) == ALIGN
+    assert mxq_call(lib, off=FAKE, G=0) == INVALID
+    assert mxq_call(lib, G=2) == INVALID
+    assert mxq_call(lib, rows=0, x=None) == OK             # nothing to do
+
+
+def mxg_call(lib, **kw):
+    a = dict(A=FAKE, fa=0, lda=128, sA=FAKE, B=FAKE, fb=0, ldb=128, sB=FAKE, M=128, N=224, K=128, C=FAKE, ldc=224)
+    a.update(kw)
+    P = ctypes.c_void_p
+    return lib.fp8_mx_gemm(P(a["A"]), a["fa"], a["lda"], P(a["sA"]), P(a["B"]), a["fb"], a["ldb"], P(a["sB"]),
+                           a["M"], a["N"], a["K"], P(a["C"]), a["ldc"], None)
+
+
+def test_mx_gemm_validation(lib):
+    assert mxg_call(lib, sA=None) == INVALID
+    assert mxg_call(lib, fa=2) == UNSUPPORTED
+    assert mxg_call(lib, fb=6) == INVALID
+    assert mxg_call(lib, K=0) == INVALID
+    assert mxg_call(lib, K=112) == ALIGN                   # K must be whole 32-element blocks
+    assert mxg_call(lib, sB=FAKE + 4) == ALIGN             # scale tiles are bulk copies
+    assert mxg_call(lib, lda=136) == ALIGN
+    assert mxg_call(lib, ldc=100) == INVALID
+
+
+def mxgg_call(lib, **kw):
+    a = dict(mode=0, A=FAKE, fa=0, sA=FAKE, B=FAKE, fb=0, sB=FAKE, off=FAKE, G=4, Mt=100, N=256, K=128, C=FAKE,
+             ldT=0)
+    a.update(kw)
+    P = ctypes.c_void_p
+    return lib.fp8_mx_grouped_gemm(a["mode"], P(a["A"]), a["fa"], P(a["sA"]), P(a["B"]), a["fb"], P(a["sB"]),
+                                   P(a["off"]), a["G"], a["Mt"], a["N"], a["K"], P(a["C"]), a["ldT"], None)
+
+
+def test_mx_grouped_gemm_validation(lib):
+    assert mxgg_call(lib, off=None) == INVALID
+    assert mxgg_call(lib, mode=2) == INVALID               # no transposed-B mode for MX
+    assert mxgg_call(lib, G=2000) == INVALID
+    assert mxgg_call(lib, fa=3) == UNSUPPORTED
+    assert mxgg_call(lib, K=96 + 16) == ALIGN
+    assert mxgg_call(lib, N=254) == ALIGN                  # scale rows of a tile start on a word boundary
+    assert mxgg_call(lib, mode=1, ldT=192) == ALIGN        # groups padded to 128 columns
+    assert mxgg_call(lib, mode=1, ldT=256, K=130) == ALIGN

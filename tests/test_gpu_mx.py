@@ -1,0 +1,278 @@
+"""GPU parity of the MXFP8 path (fp8_mx_quantize, fp8_mx_gemm,
+fp8_mx_grouped_gemm) against the oracle.
+
+Quantize: bit-exact element bytes (NaN compared by class) and E8M0 scale
+bytes over the whole scale buffers (pad bytes included), for both layouts,
+ragged shapes, special values, every bf16 pattern, grouped tensors with
+empty groups and a full-size Llama-3-8B activation.
+
+GEMM: operands are produced by the oracle's MX quantize of seeded inputs
+(never by the GPU), uploaded in the MX scale layout, and the bf16 result is
+compared with the oracle's fp64 block-scaled product under the GEMM
+tolerance |out - ref| <= 2e-3 * bound + 1e-5 + 2^-8 * max(|ref|, |out|).
+"""
+import numpy as np
+import pytest
+import torch
+
+import fp8_mixed_precision_scale_gb300 as fp8
+import synth
+from parity import assert_codes_equal, bits, check_gemm, mx_tiled, sample_points
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    assert torch.cuda.is_available()
+    fp8.load_library()
+
+
+def gen_x(shape, seed, scale=1.0, spread=6):
+    """bf16 values N(0, 1) times a per-row power-of-two spread (exercises
+    many block scales)."""
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(shape, generator=g) * scale
+    if shape[0] > 0:
+        x = x * torch.exp2(torch.randint(-spread, spread + 1, (shape[0], 1), generator=g).float())
+    return x.to(torch.bfloat16)
+
+
+def compare_mx(orc, x, fmt, layouts=3, offsets=None, what=""):
+    xb = bits(x)
+    ref = orc.mx_quantize(xb, fmt, layouts, offsets=offsets, align=fp8.MX_GROUP_ALIGN)
+    dev_off = None if offsets is None else torch.as_tensor(np.asarray(offsets, np.int32), device=DEV)
+    q = fp8.mx_quantize(x.to(DEV), fmt, layouts, group_offsets=dev_off,
+                        host_offsets=None if offsets is None else torch.as_tensor(np.asarray(offsets, np.int32)))
+    torch.cuda.synchronize()
+    assert fp8.fp8_sync_status() == 0
+    P = q.scale_rows
+    if layouts & fp8.LAYOUT_ROW:
+        assert_codes_equal(q.q_row.cpu().numpy(), ref["q_row"], fmt, f"{what} q_row")
+        exp = mx_tiled(ref["s_row"])
+        got = q.s_row.cpu().numpy()
+        assert got.size >= exp.size and np.array_equal(got[:exp.size], exp), f"{what} s_row"
+    if layouts & fp8.LAYOUT_COLT:
+        assert_codes_equal(q.q_colT.cpu().numpy()[:, :P], ref["q_colT"], fmt, f"{what} q_colT")
+        exp = mx_tiled(ref["s_col"])
+        got = q.s_col.cpu().numpy()
+        assert got.size >= exp.size and np.array_equal(got[:exp.size], exp), f"{what} s_col"
+    return q, ref
+
+
+# --- quantize ----------------------------------------------------------------
+
+SHAPES = [(64, 128), (96, 160), (32, 32), (128, 4096), (320, 544), (1024, 96)]
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_mx_quantize_both_layouts(orc, shape, fmt):
+    compare_mx(orc, gen_x(shape, seed=shape[0] + shape[1] + fmt), fmt, 3, what=f"{shape} f{fmt}")
+
+
+@pytest.mark.parametrize("rows", [1, 37, 62, 65, 130])
+def test_mx_quantize_row_only_ragged_rows(orc, rows):
+    """Row layout alone allows any row count; the scale rows are padded to 4."""
+    compare_mx(orc, gen_x((rows, 224), seed=rows), 0, fp8.LAYOUT_ROW, what=f"rows {rows}")
+
+
+@pytest.mark.parametrize("layouts", [1, 2])
+def test_mx_quantize_single_layout(orc, layouts):
+    compare_mx(orc, gen_x((192, 384), seed=3), 1, layouts, what=f"layouts {layouts}")
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_mx_quantize_special_values(orc, fmt):
+    g = torch.Generator().manual_seed(8 + fmt)
+    x = synth.randomize_special(gen_x((128, 256), seed=10), g, frac=0.02)
+    x[3, 5] = float("nan")
+    x[40, 70] = float("inf")
+    x[64:96, 128:160] = 0.0                 # all-zero blocks in both directions
+    x[100, 200:232] = 1e38                  # huge block
+    x[101, 0:32] = 2.0 ** -133              # bf16 subnormals
+    compare_mx(orc, x, fmt, 3, what=f"special f{fmt}")
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_mx_every_bf16_pattern(orc, fmt):
+    """All 65536 bf16 patterns, laid out so each row block and each column
+    block mixes magnitudes."""
+    pats = torch.arange(65536, dtype=torch.int32).to(torch.int16).view(torch.bfloat16)
+    perm = torch.randperm(65536, generator=torch.Generator().manual_seed(1))
+    compare_mx(orc, pats[perm].reshape(256, 256), fmt, 3, what=f"patterns f{fmt}")
+    compare_mx(orc, pats.reshape(512, 128), fmt, 3, what=f"patterns sorted f{fmt}")
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_mx_quantize_grouped(orc, fmt):
+    sizes = [5, 0, 70, 1, 0, 129, 32, 300]
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    x = gen_x((int(off[-1]), 160), seed=12 + fmt)
+    q, _ = compare_mx(orc, x, fmt, 3, offsets=off, what=f"grouped f{fmt}")
+    assert q.scale_rows == sum(-(-m // 128) * 128 for m in sizes)
+
+
+def test_mx_quantize_grouped_row_only_and_all_empty(orc):
+    sizes = [0, 3, 0]
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    compare_mx(orc, gen_x((3, 64), seed=2), 0, fp8.LAYOUT_ROW, offsets=off, what="tiny grouped")
+    off0 = np.zeros(4, np.int32)
+    x = torch.zeros((0, 64), dtype=torch.bfloat16)
+    q = fp8.mx_quantize(x.to(DEV), 1, 3, group_offsets=torch.as_tensor(off0, device=DEV),
+                        host_offsets=torch.as_tensor(off0))
+    torch.cuda.synchronize()
+    assert fp8.fp8_sync_status() == 0 and q.scale_rows == 0
+
+
+def test_mx_quantize_bad_offsets_flagged():
+    x = gen_x((64, 64), seed=1).to(DEV)
+    off = torch.tensor([0, 40, 30, 64], dtype=torch.int32)      # decreasing
+    q_row = torch.empty((64, 64), dtype=torch.uint8, device=DEV)
+    s_row = torch.full((fp8.fp8_mx_scale_bytes(512, 2),), 7, dtype=torch.uint8, device=DEV)
+    fp8.fp8_mx_quantize(x, 64, 64, 64, 0, fp8.LAYOUT_ROW, q_row, s_row, None, 0, None, off.to(DEV), 3)
+    assert fp8.fp8_sync_status() == 1                            # FP8_ERR_INVALID_ARG
+    assert (s_row.cpu() == 7).all()                             # nothing written
+    assert fp8.fp8_sync_status() == 0
+
+
+def test_mx_quantize_llama_activation_full(orc):
+    """Llama-3-8B MLP input [8192, 4096], both layouts, compared in full."""
+    g = torch.Generator().manual_seed(1)
+    x = torch.randn((8192, 4096), generator=g).to(torch.bfloat16)
+    compare_mx(orc, x, 0, 3, what="llama X")
+
+
+def test_mx_quantize_deterministic():
+    x = gen_x((256, 512), seed=5).to(DEV)
+    a = fp8.mx_quantize(x, 0)
+    b = fp8.mx_quantize(x, 0)
+    torch.cuda.synchronize()
+    assert torch.equal(a.q_row, b.q_row) and torch.equal(a.s_row, b.s_row)
+    assert torch.equal(a.q_colT[:, :256], b.q_colT[:, :256]) and torch.equal(a.s_col, b.s_col)
+
+
+# --- GEMM --------------------------------------------------------------------
+
+def mx_operand(orc, rows, K, fmt, seed, spread=4):
+    ref = orc.mx_quantize(bits(gen_x((rows, K), seed, spread=spread)), fmt, fp8.LAYOUT_ROW)
+    return ref["q_row"], ref["s_row"]
+
+
+def up(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+MX_SMALL = [(128, 224, 128), (1, 1, 32), (100, 40, 64), (130, 300, 160), (256, 448, 512), (300, 520, 1056),
+            (129, 257, 4096)]
+
+
+@pytest.mark.parametrize("shape", MX_SMALL)
+@pytest.mark.parametrize("fa,fb", [(0, 0), (1, 0), (0, 1)])
+def test_mx_gemm_small_full(orc, shape, fa, fb):
+    M, N, K = shape
+    A, sA = mx_operand(orc, M, K, fa, seed=M + K + fa)
+    B, sB = mx_operand(orc, N, K, fb, seed=N + 2 * K + fb)
+    C = fp8.mx_gemm(up(A), fa, up(mx_tiled(sA)), up(B), fb, up(mx_tiled(sB)))
+    assert fp8.fp8_sync_status() == 0
+    ref, bound = orc.mx_gemm(A, fa, sA, B, fb, sB)
+    check_gemm(C.float().cpu().numpy(), ref, bound, f"mx {shape} {fa}{fb}")
+
+
+def test_mx_gemm_wide_scale_spread(orc):
+    """Block scales spread over 2^-40 .. 2^40 between rows and K blocks."""
+    M, N, K = 256, 448, 1024
+    A, sA = mx_operand(orc, M, K, 0, seed=1, spread=20)
+    B, sB = mx_operand(orc, N, K, 0, seed=2, spread=20)
+    C = fp8.mx_gemm(up(A), 0, up(mx_tiled(sA)), up(B), 0, up(mx_tiled(sB)))
+    assert fp8.fp8_sync_status() == 0
+    ref, bound = orc.mx_gemm(A, 0, sA, B, 0, sB)
+    check_gemm(C.float().cpu().numpy(), ref, bound, "spread")
+
+
+def test_mx_gemm_padded_ld_and_deterministic(orc):
+    M, N, K = 200, 300, 256
+    A, sA = mx_operand(orc, M, K, 0, seed=3)
+    B, sB = mx_operand(orc, N, K, 1, seed=4)
+    Ap = np.zeros((M, K + 64), np.uint8)
+    Ap[:, :K] = A
+    Cp = torch.zeros((M, N + 5), dtype=torch.bfloat16, device=DEV)
+    fp8.mx_gemm(up(Ap), 0, up(mx_tiled(sA)), up(B), 1, up(mx_tiled(sB)), K=K, out=Cp[:, :N])
+    C2 = fp8.mx_gemm(up(A), 0, up(mx_tiled(sA)), up(B), 1, up(mx_tiled(sB)))
+    assert fp8.fp8_sync_status() == 0
+    ref, bound = orc.mx_gemm(A, 0, sA, B, 1, sB)
+    check_gemm(Cp[:, :N].float().cpu().numpy(), ref, bound, "padded ld")
+    assert torch.equal(Cp[:, :N], C2)
+    assert (Cp[:, N:] == 0).all()
+
+
+def test_mx_gemm_llama_gate_sampled(orc):
+    """Llama-3-8B gate projection fprop, M=8192 N=14336 K=4096, sampled."""
+    M, N, K = 8192, 14336, 4096
+    A, sA = mx_operand(orc, M, K, 0, seed=21, spread=1)
+    B, sB = mx_operand(orc, N, K, 0, seed=22, spread=1)
+    C = fp8.mx_gemm(up(A), 0, up(mx_tiled(sA)), up(B), 0, up(mx_tiled(sB)))
+    assert fp8.fp8_sync_status() == 0
+    g = torch.Generator().manual_seed(5)
+    pm, pn = sample_points(g, M, N, n_rows=16, n_cols=16, n_rand=4096)
+    ref, bound = orc.mx_gemm(A, 0, sA, B, 0, sB, points=(pm, pn))
+    check_gemm(C.float().cpu().numpy()[pm, pn], ref, bound, "llama gate")
+
+
+# --- grouped GEMM ------------------------------------------------------------
+
+def test_mx_grouped_m_small(orc):
+    sizes = [5, 0, 200, 1, 0, 129, 64]
+    G = len(sizes)
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    Mt, N, K = int(off[-1]), 300, 256
+    xa = gen_x((Mt, K), seed=31)
+    qa = orc.mx_quantize(bits(xa), 0, fp8.LAYOUT_ROW, offsets=off, align=128)
+    B, sB = mx_operand(orc, G * N, K, 0, seed=32)
+    C = fp8.mx_grouped_gemm(fp8.GROUPED_M, up(qa["q_row"]), 0, up(mx_tiled(qa["s_row"])), up(B), 0,
+                            up(mx_tiled(sB)), up(off), Mt, N, K)
+    assert fp8.fp8_sync_status() == 0
+    poff = orc.padded_offsets_align(off, 128)
+    out = C.float().cpu().numpy()
+    for e in range(G):
+        if sizes[e] == 0:
+            continue
+        r0, r1 = off[e], off[e + 1]
+        ref, bound = orc.mx_gemm(qa["q_row"][r0:r1], 0, qa["s_row"][poff[e]:poff[e] + sizes[e]],
+                                 B[e * N:(e + 1) * N], 0, sB[e * N:(e + 1) * N])
+        check_gemm(out[r0:r1], ref, bound, f"mgroup e{e}")
+
+
+def test_mx_grouped_k_small(orc):
+    sizes = [5, 0, 200, 1, 0, 129, 64]
+    G = len(sizes)
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    Mt, N, K = int(off[-1]), 200, 300
+    qd = orc.mx_quantize(bits(gen_x((Mt, N), seed=41)), 1, fp8.LAYOUT_COLT, offsets=off, align=128)
+    qx = orc.mx_quantize(bits(gen_x((Mt, K), seed=42)), 0, fp8.LAYOUT_COLT, offsets=off, align=128)
+    P = qd["q_colT"].shape[1]
+    C = fp8.mx_grouped_gemm(fp8.GROUPED_K, up(qd["q_colT"]), 1, up(mx_tiled(qd["s_col"])), up(qx["q_colT"]), 0,
+                            up(mx_tiled(qx["s_col"])), up(off), Mt, N, K, ld_T=P)
+    assert fp8.fp8_sync_status() == 0
+    poff = orc.padded_offsets_align(off, 128)
+    out = C.float().cpu().numpy()
+    for e in range(G):
+        if sizes[e] == 0:
+            assert (out[e] == 0).all()
+            continue
+        a, b = int(poff[e]), int(poff[e + 1])
+        ref, bound = orc.mx_gemm(qd["q_colT"][:, a:b], 1, qd["s_col"][:, a // 32:b // 32],
+                                 qx["q_colT"][:, a:b], 0, qx["s_col"][:, a // 32:b // 32])
+        check_gemm(out[e], ref, bound, f"kgroup e{e}")
+
+
+def test_mx_grouped_bad_offsets_flagged():
+    off = torch.tensor([0, 50, 20, 64], dtype=torch.int32, device=DEV)
+    A = torch.zeros((64, 128), dtype=torch.uint8, device=DEV)
+    B = torch.zeros((3 * 224, 128), dtype=torch.uint8, device=DEV)
+    s = torch.zeros(1 << 16, dtype=torch.uint8, device=DEV)
+    C = torch.full((64, 224), 3.0, dtype=torch.bfloat16, device=DEV)
+    fp8.fp8_mx_grouped_gemm(fp8.GROUPED_M, A, 0, s, B, 0, s, off, 3, 64, 224, 128, C)
+    assert fp8.fp8_sync_status() == 1
+    assert (C == 3.0).all()
