@@ -49,10 +49,11 @@ namespace fp8gb {
 namespace mx {
 
 constexpr int BM = 128;
-constexpr int BN = 224;
+constexpr int BN = 256;
 constexpr int BK = 128;
 constexpr int UMMA_K = 32;
-constexpr int STAGES = 4;
+constexpr int STAGES = 4;         // dense; grouped kernels keep 3 (room for the group tables)
+constexpr int STAGES_GROUPED = 3;
 constexpr int THREADS = 352;  // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue, warp 10 scales
 constexpr int A_BYTES = BM * BK;
 constexpr int B_BYTES = BN * BK;
@@ -61,16 +62,16 @@ constexpr int SFB_RAW = 256 * 4;  // BN words used; room for two 128-row blocks
 constexpr int SFA_CP = 512;       // [32 lanes][4 words]
 constexpr int SFB_CP = 1024;      // two such blocks (rows 0-127, 128-255)
 constexpr uint32_t TMEM_COLS = 512;
-// scale columns, one set per ring stage so a stage's copies never overwrite
-// scales that MMAs of an earlier stage may still be reading: A's 4 columns
-// per stage in 224 .. 239, B's 8 per stage in 480 .. 511
-constexpr uint32_t SFA_COL = 224;
-constexpr uint32_t SFB_COL = 480;
-static_assert(SFA_COL + 4 * STAGES <= 256 && SFB_COL + 8 * STAGES <= TMEM_COLS, "scale columns");
+// one 256-column accumulator at column 0; scale columns, one set per ring
+// stage so a stage's copies never overwrite scales that MMAs of an earlier
+// stage may still be reading: A's 4 columns per stage from 256, B's 8 per
+// stage from 288
+constexpr uint32_t SFA_COL = 256;
+constexpr uint32_t SFB_COL = 288;
+static_assert(SFA_COL + 4 * STAGES <= SFB_COL && SFB_COL + 8 * STAGES <= TMEM_COLS, "scale columns");
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 constexpr int MAX_GROUPS = 1024;
 
-__host__ __device__ constexpr uint32_t acc_col(int acc) { return acc ? 256u : 0u; }
 
 enum { MODE_DENSE = 0, MODE_MGROUP = 1, MODE_KGROUP = 2 };
 
@@ -99,21 +100,23 @@ struct Tile {
     int64_t row0, row_end, col0, col_end, c_base;
 };
 
+template <int NS>
 struct Smem {
     static constexpr int a_off = 0;
-    static constexpr int b_off = STAGES * A_BYTES;
-    static constexpr int sfa_raw_off = b_off + STAGES * B_BYTES;
-    static constexpr int sfb_raw_off = sfa_raw_off + STAGES * SFA_RAW;
-    static constexpr int sfa_cp_off = sfb_raw_off + STAGES * SFB_RAW;
-    static constexpr int sfb_cp_off = sfa_cp_off + STAGES * SFA_CP;
-    static constexpr int bar_off = sfb_cp_off + STAGES * SFB_CP;
-    static constexpr int n_bars = 3 * STAGES + 2 + 2 + 2;
+    static constexpr int b_off = NS * A_BYTES;
+    static constexpr int sfa_raw_off = b_off + NS * B_BYTES;
+    static constexpr int sfb_raw_off = sfa_raw_off + NS * SFA_RAW;
+    static constexpr int sfa_cp_off = sfb_raw_off + NS * SFB_RAW;
+    static constexpr int sfb_cp_off = sfa_cp_off + NS * SFA_CP;
+    static constexpr int bar_off = sfb_cp_off + NS * SFB_CP;
+    static constexpr int n_bars = 3 * NS + 2 + 2 + 2;
     static constexpr int slot_off = bar_off + n_bars * 8;
-    static constexpr int stage_pitch = 80;
-    static constexpr int stage_warp_bytes = 32 * stage_pitch;
     static constexpr int stage_off = (slot_off + 16 + 127) / 128 * 128;
-    static constexpr int misc_off = stage_off + 8 * stage_warp_bytes;  // group tables
+    static constexpr int misc_off = stage_off + 8 * 32 * 80;  // group tables
 };
+constexpr int STAGE_PITCH = 80;  // epilogue staging: 32 rows x 32 bf16 per warp, rows padded to 80 bytes
+constexpr int STAGE_WARP_BYTES = 32 * STAGE_PITCH;
+__host__ __device__ constexpr int ring_stages(int mode) { return mode == 0 ? STAGES : STAGES_GROUPED; }
 
 // Tile prefix [G+1] and offsets padded to FP8_MX_GROUP_ALIGN [G+1]; one warp.
 __device__ bool build_group_tables(const Params &p, int MODE, int32_t *tile_prefix, int32_t *poff,
@@ -237,52 +240,53 @@ __device__ __forceinline__ Tile tile_info(const Params &p, int64_t t, const int3
     return ti;
 }
 
-// One finished tile for one epilogue warp: TMEM lane quarter q, columns
-// [cb, ce) of the tile (a multiple of 32 wide except at the tile's end).
-__device__ __forceinline__ void epilogue_tile(const Params &p, const Tile &ti, uint32_t tmem_base, uint32_t acc,
-                                              int q, int cb, int ce, int lane, uint8_t *stage)
+// One finished tile for one epilogue warp: TMEM lane quarter q (rows q*32 ..
+// q*32+31 of the tile), columns [cb, cb + 128).  The warp first copies its
+// 32 x 128 accumulator block into registers and releases the accumulator
+// (one arrive on `tempty`), so the next tile's MMAs start while this warp
+// converts to bf16 and stores through its shared staging block.
+__device__ __forceinline__ void epilogue_tile(const Params &p, const Tile &ti, uint32_t tmem_base, int q, int cb,
+                                              int lane, uint8_t *stage, uint64_t *tempty)
 {
-    for (int ch = cb; ch < ce; ch += 64) {
-        const int64_t c0 = ti.col0 + ch;
-        if (c0 >= ti.col_end) break;  // warp-uniform
-        const bool two = ch + 32 < ce && c0 + 32 < ti.col_end;
-        uint32_t r[2][32];
-        const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc + (uint32_t)ch;
-        tmem_ld_32x32b_x32(taddr, r[0]);
-        if (two) tmem_ld_32x32b_x32(taddr + 32, r[1]);
-        tmem_ld_wait();
+    uint32_t r[4][32];
+    const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)cb;
 #pragma unroll
-        for (int u = 0; u < 2; u++) {
-            if (u == 1 && !two) break;  // warp-uniform
-            const int64_t cu = c0 + u * 32;
-            uint32_t packed[16];
+    for (int u = 0; u < 4; u++) tmem_ld_32x32b_x32(taddr + 32 * u, r[u]);
+    tmem_ld_wait();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(tempty);
 #pragma unroll
-            for (int j = 0; j < 16; j++)
-                packed[j] = pack_bf16x2(__uint_as_float(r[u][2 * j]), __uint_as_float(r[u][2 * j + 1]));
+    for (int u = 0; u < 4; u++) {
+        const int64_t cu = ti.col0 + cb + u * 32;
+        if (cu >= ti.col_end) break;  // warp-uniform
+        uint32_t packed[16];
 #pragma unroll
-            for (int g = 0; g < 4; g++)
-                *reinterpret_cast<uint4 *>(stage + lane * Smem::stage_pitch + g * 16) =
-                    make_uint4(packed[4 * g], packed[4 * g + 1], packed[4 * g + 2], packed[4 * g + 3]);
-            __syncwarp();
+        for (int j = 0; j < 16; j++)
+            packed[j] = pack_bf16x2(__uint_as_float(r[u][2 * j]), __uint_as_float(r[u][2 * j + 1]));
 #pragma unroll
-            for (int i = 0; i < 4; i++) {
-                const int rr = i * 8 + (lane >> 2), seg = lane & 3;
-                const uint4 v = *reinterpret_cast<const uint4 *>(stage + rr * Smem::stage_pitch + seg * 16);
-                const int64_t row = ti.row0 + q * 32 + rr;
-                const int64_t c = cu + seg * 8;
-                if (row < ti.row_end && c < ti.col_end) {
-                    uint16_t *dst = p.C + ti.c_base + row * p.ldc + c;
-                    if (p.c_vec16 && c + 8 <= ti.col_end) {
-                        *reinterpret_cast<uint4 *>(dst) = v;
-                    } else {
-                        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-                        for (int j = 0; j < 8 && c + j < ti.col_end; j++)
-                            dst[j] = (uint16_t)(w[j / 2] >> (16 * (j & 1)));
-                    }
+        for (int g = 0; g < 4; g++)
+            *reinterpret_cast<uint4 *>(stage + lane * STAGE_PITCH + g * 16) =
+                make_uint4(packed[4 * g], packed[4 * g + 1], packed[4 * g + 2], packed[4 * g + 3]);
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const int rr = i * 8 + (lane >> 2), seg = lane & 3;
+            const uint4 v = *reinterpret_cast<const uint4 *>(stage + rr * STAGE_PITCH + seg * 16);
+            const int64_t row = ti.row0 + q * 32 + rr;
+            const int64_t c = cu + seg * 8;
+            if (row < ti.row_end && c < ti.col_end) {
+                uint16_t *dst = p.C + ti.c_base + row * p.ldc + c;
+                if (p.c_vec16 && c + 8 <= ti.col_end) {
+                    *reinterpret_cast<uint4 *>(dst) = v;
+                } else {
+                    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                    for (int j = 0; j < 8 && c + j < ti.col_end; j++)
+                        dst[j] = (uint16_t)(w[j / 2] >> (16 * (j & 1)));
                 }
             }
-            __syncwarp();
         }
+        __syncwarp();
     }
 }
 
@@ -291,24 +295,26 @@ __global__ void __launch_bounds__(THREADS, 1)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, Params p,
                    uint32_t idesc)
 {
+    constexpr int NS = ring_stages(MODE);
+    using L = Smem<NS>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *sA = smem + Smem::a_off;
-    uint8_t *sB = smem + Smem::b_off;
-    uint8_t *sfa_raw = smem + Smem::sfa_raw_off;
-    uint8_t *sfb_raw = smem + Smem::sfb_raw_off;
-    uint8_t *sfa_cp = smem + Smem::sfa_cp_off;
-    uint8_t *sfb_cp = smem + Smem::sfb_cp_off;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Smem::bar_off);
+    uint8_t *sA = smem + L::a_off;
+    uint8_t *sB = smem + L::b_off;
+    uint8_t *sfa_raw = smem + L::sfa_raw_off;
+    uint8_t *sfb_raw = smem + L::sfb_raw_off;
+    uint8_t *sfa_cp = smem + L::sfa_cp_off;
+    uint8_t *sfb_cp = smem + L::sfb_cp_off;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::bar_off);
     uint64_t *full = bars;
-    uint64_t *empty = bars + STAGES;
-    uint64_t *tfull = bars + 2 * STAGES;
+    uint64_t *empty = bars + NS;
+    uint64_t *tfull = bars + 2 * NS;
     uint64_t *tempty = tfull + 2;
     uint64_t *done = tempty + 2;
     uint64_t *sf_done = done + 1;
-    uint64_t *sf_full = sf_done + 1;  // [STAGES]: the stage's scales are in TMEM
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Smem::slot_off);
-    int32_t *tile_prefix = reinterpret_cast<int32_t *>(smem + Smem::misc_off);
+    uint64_t *sf_full = sf_done + 1;  // [NS]: the stage's scales are in TMEM
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::slot_off);
+    int32_t *tile_prefix = reinterpret_cast<int32_t *>(smem + L::misc_off);
     int32_t *poff = tile_prefix + (p.G + 1);
     __shared__ int64_t s_total;
     __shared__ int s_ok;
@@ -316,7 +322,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (warp == 0 && lane == 0) {
-        for (int s = 0; s < STAGES; s++) {
+        for (int s = 0; s < NS; s++) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
             mbar_init(&sf_full[s], 1);
@@ -358,8 +364,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ---------------- producer ----------------
         int stage = 0;
         uint32_t phase = 0;
-        int issued_parity[STAGES];
-        for (int s = 0; s < STAGES; s++) issued_parity[s] = -1;
+        int issued_parity[NS];
+        for (int s = 0; s < NS; s++) issued_parity[s] = -1;
         bool ok = true;
         // M-grouped: A's scale layout has one row per padded row (the padded total)
         const int64_t rsA = MODE == MODE_MGROUP ? (int64_t)poff[p.G] : p.rsA;
@@ -380,28 +386,27 @@ __global__ void __launch_bounds__(THREADS, 1)
                 bulk_load(sfa_raw + stage * SFA_RAW, p.sA + (kt * rsA + ti.sa_row) * 4, sfa_bytes, &full[stage]);
                 bulk_load(sfb_raw + stage * SFB_RAW, p.sB + (kt * p.rsB + ti.sb_row) * 4, sfb_bytes, &full[stage]);
                 issued_parity[stage] = (int)phase;
-                if (++stage == STAGES) {
+                if (++stage == NS) {
                     stage = 0;
                     phase ^= 1;
                 }
             }
         }
-        for (int s = 0; s < STAGES; s++)
+        for (int s = 0; s < NS; s++)
             if (issued_parity[s] >= 0)
                 mbar_wait_bounded(&full[s], (uint32_t)issued_parity[s], WAIT_LIMIT_NS, p.err, ERR_TEARDOWN_WAIT);
     } else if (warp == 1 && lane == 0) {
         // ---------------- MMA issuer ----------------
         int stage = 0;
         uint32_t phase = 0;
-        int acc = 0;
         uint32_t acc_phase = 0;
         bool ok = true;
         for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
             const Tile ti = tile_info<MODE>(p, t, tile_prefix, poff);
             if (ti.nkb == 0) continue;  // empty K-grouped block: the epilogue writes zeros
-            if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1, WAIT_LIMIT_NS, p.err, ERR_MMA_WAIT)) break;
+            if (!mbar_wait_bounded(&tempty[0], acc_phase ^ 1, WAIT_LIMIT_NS, p.err, ERR_MMA_WAIT)) break;
             tc_fence_after();
-            const uint32_t d_tmem = tmem_base + acc_col(acc);
+            const uint32_t d_tmem = tmem_base;
             for (int kb = 0; kb < ti.nkb; kb++) {
                 // the scale warp's copies of this stage completed (so did its TMA loads)
                 if (!mbar_wait_bounded(&sf_full[stage], phase, WAIT_LIMIT_NS, p.err, ERR_MMA_WAIT)) {
@@ -420,17 +425,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                                  (kb | k) != 0);
                 }
                 mma_commit(&empty[stage]);
-                if (++stage == STAGES) {
+                if (++stage == NS) {
                     stage = 0;
                     phase ^= 1;
                 }
             }
             if (!ok) break;
-            mma_commit(&tfull[acc]);
-            if (++acc == 2) {
-                acc = 0;
-                acc_phase ^= 1;
-            }
+            mma_commit(&tfull[0]);
+            acc_phase ^= 1;
         }
         // all issued MMAs complete before TMEM is released
         mma_commit(done);
@@ -472,7 +474,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     mma_commit(&sf_full[stage]);
                 }
                 __syncwarp();
-                if (++stage == STAGES) {
+                if (++stage == NS) {
                     stage = 0;
                     phase ^= 1;
                 }
@@ -486,13 +488,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         __syncwarp();
     } else if (warp >= 2 && warp < 10) {
         // ---------------- epilogue ----------------
-        // warp w reads TMEM lane quarter w % 4; the two warps of a quarter
-        // split the 224 columns 128 + 96
+        // warp w reads TMEM lane quarter w % 4 and one half (128 columns) of
+        // the tile
         const int q = warp & 3;
-        const int half = (warp - 2) >> 2;
-        const int cb = half ? 128 : 0, ce = half ? BN : 128;
-        uint8_t *stage = smem + Smem::stage_off + (warp - 2) * Smem::stage_warp_bytes;
-        int acc = 0;
+        const int cb = ((warp - 2) >> 2) * 128;
+        uint8_t *stage = smem + L::stage_off + (warp - 2) * STAGE_WARP_BYTES;
         uint32_t acc_phase = 0;
         for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
             const Tile ti = tile_info<MODE>(p, t, tile_prefix, poff);
@@ -500,21 +500,15 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int64_t gr = ti.row0 + q * 32 + lane;
                 if (gr < ti.row_end) {
                     uint16_t *crow = p.C + ti.c_base + gr * p.ldc;
-                    const int64_t c1 = ti.col0 + ce < ti.col_end ? ti.col0 + ce : ti.col_end;
+                    const int64_t c1 = ti.col0 + cb + 128 < ti.col_end ? ti.col0 + cb + 128 : ti.col_end;
                     for (int64_t c = ti.col0 + cb; c < c1; c++) crow[c] = 0;
                 }
                 continue;
             }
-            if (!mbar_wait_bounded(&tfull[acc], acc_phase, WAIT_LIMIT_NS, p.err, ERR_EPILOGUE_WAIT)) break;
+            if (!mbar_wait_bounded(&tfull[0], acc_phase, WAIT_LIMIT_NS, p.err, ERR_EPILOGUE_WAIT)) break;
             tc_fence_after();
-            epilogue_tile(p, ti, tmem_base, acc_col(acc), q, cb, ce, lane, stage);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[acc]);
-            if (++acc == 2) {
-                acc = 0;
-                acc_phase ^= 1;
-            }
+            epilogue_tile(p, ti, tmem_base, q, cb, lane, stage, &tempty[0]);
+            acc_phase ^= 1;
         }
     }
 
@@ -564,13 +558,17 @@ static bool make_map(CUtensorMap *map, const void *base, int64_t rows, int64_t c
     return r == CUDA_SUCCESS;
 }
 
-static size_t smem_bytes(int G) { return 1024 + Smem::misc_off + (G > 0 ? 8 * (size_t)(G + 1) : 0); }
+template <int MODE>
+static size_t smem_bytes(int G)
+{
+    return 1024 + Smem<ring_stages(MODE)>::misc_off + (G > 0 ? 8 * (size_t)(G + 1) : 0);
+}
 
 template <int MODE>
 static fp8_status_t launch(const CUtensorMap &ma, const CUtensorMap &mb, const Params &p, int fa, int fb,
                            int64_t grid, cudaStream_t st)
 {
-    const size_t smem = smem_bytes(MODE == MODE_DENSE ? 0 : p.G);
+    const size_t smem = smem_bytes<MODE>(MODE == MODE_DENSE ? 0 : p.G);
     cudaError_t e = cudaFuncSetAttribute(mx_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return cuda_fail_with(e);
     const uint32_t idesc = idesc_mxf8f6f4(fa, fb, BM, BN);

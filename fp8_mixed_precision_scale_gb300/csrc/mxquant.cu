@@ -7,15 +7,18 @@
 // GPUs with TorchTitan and TorchAO"; the block rule is the OCP Microscaling
 // v1.0 one: X = 2^(floor(log2 amax) - emax_elem), element = sat_rne(v / X).
 //
-// Design (GB300): 256-thread blocks on tiles of 64 rows x 128 columns.
+// Design (GB300): persistent 256-thread blocks looping over tiles of 64 rows
+// x 128 columns; each block issues the next tile's loads before working on
+// the current one.
 //   Row layout: thread (row, block) loads its 32 bf16 (4 x 16-byte loads),
 //     takes the packed |bf16| maximum, derives the E8M0 code from the fp32
 //     exponent bits, multiplies by 2^(127 - code) (exact) and converts with
 //     cvt.rn.satfinite; the four blocks of a row combine their codes into one
 //     32-bit word of the scale layout by two shuffles.
-//   Transposed layout: the tile is staged in shared memory; thread (column,
-//     half) reads its 32 rows, computes that block's code and writes 32
-//     contiguous bytes of q_colT (one sector) and one scale byte.
+//   Transposed layout: the tile is staged in shared memory (column pairs as
+//     32-bit words, swizzled); a thread reads two columns x 16 rows, takes
+//     the block maximum with its partner thread (the other 16 rows) and
+//     writes 16 contiguous bytes per column of q_colT.
 // One launch, no atomics, no scratch memory: every block's scale depends
 // only on its own 32 elements.
 #include <cuda.h>
@@ -111,11 +114,67 @@ __device__ void mx_padded_offsets(const MxArgs &a, int32_t *poff, int *bad)
     }
 }
 
+// Geometry of tile t: its first row in the (padded) row space, first column,
+// first input row and number of real rows.
+struct MxTile {
+    bool live;  // inside the (padded) row space
+    int64_t rt, ct, pr0, c0, src0, nreal;
+};
+
+__device__ __forceinline__ MxTile mx_tile(const MxArgs &a, int64_t t, int64_t prows, const int32_t *poff)
+{
+    MxTile g;
+    g.rt = t / a.n_col_tiles;
+    g.ct = t % a.n_col_tiles;
+    g.pr0 = g.rt * MX_ROWS;
+    g.c0 = g.ct * MX_COLS;
+    g.live = g.pr0 < prows;
+    g.src0 = g.pr0;
+    g.nreal = a.rows - g.pr0 < MX_ROWS ? a.rows - g.pr0 : MX_ROWS;
+    if (a.offsets && g.live) {
+        // the tile lies inside one group (groups are padded to 128 rows)
+        int lo = 0, hi = a.G;  // poff[lo] <= pr0 < poff[hi]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (poff[mid] <= g.pr0)
+                lo = mid;
+            else
+                hi = mid;
+        }
+        const int64_t local0 = g.pr0 - poff[lo];
+        const int64_t m_e = (int64_t)a.offsets[lo + 1] - a.offsets[lo];
+        g.src0 = a.offsets[lo] + local0;
+        g.nreal = m_e - local0 < MX_ROWS ? m_e - local0 : MX_ROWS;
+    }
+    if (g.nreal < 0) g.nreal = 0;
+    return g;
+}
+
+// Thread (lr, blk) = (tid / 4, tid % 4) loads the 32 bf16 of row lr, block
+// blk of the tile (zeros outside the data).
+__device__ __forceinline__ void mx_load(const MxArgs &a, const MxTile &g, int tid, uint4 (&v)[4])
+{
+    const int lr = tid >> 2, blk = tid & 3;
+    if (g.live && lr < g.nreal && g.c0 + 32 * blk < a.cols) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(a.x + (g.src0 + lr) * a.ld_x + g.c0 + 32 * blk);
+#pragma unroll
+        for (int j = 0; j < 4; j++) v[j] = __ldg(src + j);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; j++) v[j] = make_uint4(0, 0, 0, 0);
+    }
+}
+
+// Shared tile: 64 rows of MX_PITCH / 2 words; the 32-bit word (column pair)
+// index is XOR-swizzled by 16 in rows 16-31 of every 32, so the transposed
+// phase's column-pair reads (rows r and r + 16 in one warp) hit all 32 banks.
+__device__ __forceinline__ int mx_word(int row, int pair) { return row * (MX_PITCH / 2) + (pair ^ ((row & 16))); }
+
 template <int FMT>
 __global__ void __launch_bounds__(MX_THREADS)
     mx_quantize_kernel(MxArgs a)
 {
-    __shared__ __align__(16) uint16_t tile[MX_ROWS * MX_PITCH];
+    __shared__ __align__(16) uint32_t tile[MX_ROWS * MX_PITCH / 2];
     extern __shared__ int32_t poff[];  // grouped: [G + 1]
     __shared__ int s_bad;
 
@@ -129,51 +188,28 @@ __global__ void __launch_bounds__(MX_THREADS)
     }
     const int64_t total = a.n_row_tiles * a.n_col_tiles;
     const int64_t last_rt = prows > 0 ? (prows - 1) / MX_ROWS : -1;
+    const int lr = tid >> 2, blk = tid & 3;
 
-    for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
-        const int64_t rt = t / a.n_col_tiles, ct = t % a.n_col_tiles;
-        const int64_t pr0 = rt * MX_ROWS;  // first row of the tile in the padded row space
-        if (pr0 >= prows) {
-            if (!a.offsets) break;
-            continue;  // grouped: beyond the padded total
-        }
-        const int64_t c0 = ct * MX_COLS;
-
-        // map the tile's rows to input rows: ungrouped identity; grouped, the
-        // tile lies inside one group (groups are padded to 128 rows)
-        int64_t src0 = pr0, nreal = a.rows - pr0 < MX_ROWS ? a.rows - pr0 : MX_ROWS;
-        if (a.offsets) {
-            int lo = 0, hi = a.G;  // poff[lo] <= pr0 < poff[hi]
-            while (hi - lo > 1) {
-                const int mid = (lo + hi) >> 1;
-                if (poff[mid] <= pr0)
-                    lo = mid;
-                else
-                    hi = mid;
-            }
-            const int64_t local0 = pr0 - poff[lo];
-            const int64_t m_e = (int64_t)a.offsets[lo + 1] - a.offsets[lo];
-            src0 = a.offsets[lo] + local0;
-            nreal = m_e - local0 < MX_ROWS ? m_e - local0 : MX_ROWS;
-            if (nreal < 0) nreal = 0;
-        }
-
-        // ---- load: thread (lr, blk) takes 32 bf16 of one row ----
-        const int lr = tid >> 2, blk = tid & 3;
-        const bool row_real = lr < nreal;
-        const bool blk_ok = c0 + 32 * blk < a.cols;
+    // persistent loop; the next tile's loads are issued before this tile's work
+    int64_t t = blockIdx.x;
+    MxTile g = mx_tile(a, t, prows, poff);
+    uint4 nv[4];
+    mx_load(a, g, tid, nv);
+    for (; t < total; t += gridDim.x) {
+        const MxTile cur = g;
         uint4 v[4];
-        if (row_real && blk_ok) {
-            const uint4 *src = reinterpret_cast<const uint4 *>(a.x + (src0 + lr) * a.ld_x + c0 + 32 * blk);
 #pragma unroll
-            for (int j = 0; j < 4; j++) v[j] = __ldg(src + j);
-        } else {
-#pragma unroll
-            for (int j = 0; j < 4; j++) v[j] = make_uint4(0, 0, 0, 0);
+        for (int j = 0; j < 4; j++) v[j] = nv[j];
+        if (t + gridDim.x < total) {
+            g = mx_tile(a, t + gridDim.x, prows, poff);
+            mx_load(a, g, tid, nv);
         }
+        if (!cur.live) continue;  // grouped: beyond the padded total (block-uniform)
 
         // ---- row layout ----
         if (a.do_row) {
+            const bool row_real = lr < cur.nreal;
+            const bool blk_ok = cur.c0 + 32 * blk < a.cols;
             uint32_t am = 0;
 #pragma unroll
             for (int j = 0; j < 4; j++) {
@@ -196,7 +232,7 @@ __global__ void __launch_bounds__(MX_THREADS)
                     out[2 * j] = b01 | (b23 << 16);
                     out[2 * j + 1] = b45 | (b67 << 16);
                 }
-                uint4 *dst = reinterpret_cast<uint4 *>(a.q_row + (src0 + lr) * a.cols + c0 + 32 * blk);
+                uint4 *dst = reinterpret_cast<uint4 *>(a.q_row + (cur.src0 + lr) * a.cols + cur.c0 + 32 * blk);
                 dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
                 dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
             }
@@ -204,51 +240,61 @@ __global__ void __launch_bounds__(MX_THREADS)
             uint32_t word = code << (8 * blk);
             word |= __shfl_xor_sync(0xffffffffu, word, 1);
             word |= __shfl_xor_sync(0xffffffffu, word, 2);
-            const int64_t srow = pr0 + lr;  // scale row (padded row space)
+            const int64_t srow = cur.pr0 + lr;  // scale row (padded row space)
             const int64_t srows = a.offsets ? prows : a.rs_row;
             if (blk == 0 && srow < srows)
-                *reinterpret_cast<uint32_t *>(a.s_row + (ct * srows + srow) * 4) = word;
+                *reinterpret_cast<uint32_t *>(a.s_row + (cur.ct * srows + srow) * 4) = word;
         }
 
         // ---- transposed layout ----
         if (a.do_col) {
 #pragma unroll
             for (int j = 0; j < 4; j++)
-                *reinterpret_cast<uint4 *>(&tile[lr * MX_PITCH + 32 * blk + 8 * j]) = v[j];
+                *reinterpret_cast<uint4 *>(&tile[mx_word(lr, 16 * blk + 4 * j)]) = v[j];
             __syncthreads();
-            const int cl = tid & 127, h = tid >> 7;
-            const int64_t c = c0 + cl;
-            const int64_t kb = (pr0 >> 5) + h;  // block index along the rows
-            const bool blk_valid = pr0 + 32 * h < prows;
+            // thread: column pair `pair`, 32-row block h, rows 16 s .. 16 s + 15
+            // of it; the partner holding the other 16 rows is lane ^ 1
+            const int s = tid & 1, pair = (tid >> 1) & 63, h = tid >> 7;
+            const int64_t c = cur.c0 + 2 * pair;
+            const int64_t kb = (cur.pr0 >> 5) + h;  // block index along the rows
+            const bool blk_valid = cur.pr0 + 32 * h < prows;
+            uint32_t w[16];
+            uint32_t am = 0;
+#pragma unroll
+            for (int i = 0; i < 16; i++) {
+                w[i] = tile[mx_word(32 * h + 16 * s + i, pair)];
+                am = absmax_bf16x2(am, w[i]);
+            }
+            am = __vmaxu2(am, __shfl_xor_sync(0xffffffffu, am, 1));
             if (c < a.cols) {
-                uint32_t e[32];
-                uint32_t am = 0;
-#pragma unroll
-                for (int i = 0; i < 32; i++) {
-                    e[i] = tile[(32 * h + i) * MX_PITCH + cl];
-                    const uint32_t m = e[i] & 0x7FFFu;
-                    am = m > am ? m : am;
-                }
-                const uint32_t code = blk_valid ? mx_code<FMT>(am << 16) : 0u;
-                uint8_t *sc = a.s_col + ((kb >> 2) * a.cols + c) * 4 + (kb & 3);
+                const uint32_t code0 = blk_valid ? mx_code<FMT>(am << 16) : 0u;
+                const uint32_t code1 = blk_valid ? mx_code<FMT>(am & 0xFFFF0000u) : 0u;
                 if (blk_valid) {
-                    const float inv = mx_inv_scale(code);
-                    uint32_t out[8];
+                    const float inv0 = mx_inv_scale(code0), inv1 = mx_inv_scale(code1);
+                    uint32_t o0[4], o1[4];
 #pragma unroll
-                    for (int i = 0; i < 8; i++) {
-                        const uint32_t b01 = cvt2<FMT>(__uint_as_float(e[4 * i] << 16) * inv,
-                                                       __uint_as_float(e[4 * i + 1] << 16) * inv);
-                        const uint32_t b23 = cvt2<FMT>(__uint_as_float(e[4 * i + 2] << 16) * inv,
-                                                       __uint_as_float(e[4 * i + 3] << 16) * inv);
-                        out[i] = b01 | (b23 << 16);
+                    for (int i = 0; i < 4; i++) {
+                        const uint32_t x0 = w[4 * i], x1 = w[4 * i + 1], x2 = w[4 * i + 2], x3 = w[4 * i + 3];
+                        o0[i] = cvt2<FMT>(bf16lo(x0) * inv0, bf16lo(x1) * inv0) |
+                                (cvt2<FMT>(bf16lo(x2) * inv0, bf16lo(x3) * inv0) << 16);
+                        o1[i] = cvt2<FMT>(bf16hi(x0) * inv1, bf16hi(x1) * inv1) |
+                                (cvt2<FMT>(bf16hi(x2) * inv1, bf16hi(x3) * inv1) << 16);
                     }
-                    uint4 *dst = reinterpret_cast<uint4 *>(a.q_colT + c * a.ld_colT + pr0 + 32 * h);
-                    dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
-                    dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
+                    const int64_t r0 = cur.pr0 + 32 * h + 16 * s;
+                    *reinterpret_cast<uint4 *>(a.q_colT + c * a.ld_colT + r0) = make_uint4(o0[0], o0[1], o0[2], o0[3]);
+                    *reinterpret_cast<uint4 *>(a.q_colT + (c + 1) * a.ld_colT + r0) =
+                        make_uint4(o1[0], o1[1], o1[2], o1[3]);
                 }
-                *sc = (uint8_t)code;
-                // the last word's blocks past the data are written as 0
-                if (rt == last_rt && (kb & 3) < 2) sc[2] = 0;
+                if (s == 0) {
+                    uint8_t *sc = a.s_col + ((kb >> 2) * a.cols + c) * 4 + (kb & 3);
+                    sc[0] = (uint8_t)code0;
+                    sc[4] = (uint8_t)code1;
+                    // the last word's blocks past the data are written as 0
+                    if (cur.rt == last_rt && (kb & 3) < 2) {
+                        sc[2] = 0;
+                        sc[6] = 0;
+                    }
+                }
             }
             __syncthreads();  // the tile is rewritten by the next iteration
         }
@@ -260,15 +306,13 @@ static fp8_status_t launch_mx(const MxArgs &a, cudaStream_t st)
 {
     const size_t dyn = a.offsets ? (size_t)(a.G + 1) * sizeof(int32_t) : 0;
     const int64_t total = a.n_row_tiles * a.n_col_tiles;
-    int64_t grid = total;
-    if (a.offsets) {
-        int per_sm = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mx_quantize_kernel<FMT>, MX_THREADS, dyn) !=
-            cudaSuccess)
-            return cuda_fail();
-        const int64_t cap = (int64_t)num_sms() * (per_sm > 0 ? per_sm : 1);
-        grid = total < cap ? total : cap;
-    }
+    // persistent: as many blocks as fit at once, each looping over tiles
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mx_quantize_kernel<FMT>, MX_THREADS, dyn) !=
+        cudaSuccess)
+        return cuda_fail();
+    const int64_t cap = (int64_t)num_sms() * (per_sm > 0 ? per_sm : 1);
+    int64_t grid = total < cap ? total : cap;
     if (grid > INT32_MAX) grid = INT32_MAX;
     if (grid < 1) return FP8_OK;
     mx_quantize_kernel<FMT><<<(unsigned)grid, MX_THREADS, dyn, st>>>(a);
