@@ -56,18 +56,27 @@ QUANT_BYTES_PER_ELEM = 4                  # 2 B read + 1 B per layout, two layou
 # DRAM bytes (read + write) of one dense GEMM launch, the gate projection
 # 8192x14336x4096, from one ncu capture (profiles/fp8_gemm_pair_kernel_llama_gate_8192x14336x4096.md).
 # Reported only while the profiled sources are unchanged.
-GEMM_TRAFFIC = {"bytes": 317.0e6,
-                "sources": {"gemm.cu": "2a147c6746c0ea15", "fp8gb_device.cuh": "fecdad5f55743ee8"}}
+# DRAM bytes (read + write) of one launch of the step's dominant kernel, from
+# an ncu capture of the gate GEMM; valid only for the sources it was taken on
+GEMM_TRAFFIC = {
+    "llama_mlp": {"bytes": 320.3e6, "kernel": "fp8_gemm_pair_kernel",
+                  "sources": {"gemm.cu": "7e6d296a4f9d9232", "fp8gb_device.cuh": "b761586718523e93"}},
+    "llama_mxfp8": {"bytes": 316.1e6, "kernel": "mx_gemm_kernel",
+                    "sources": {"mxgemm.cu": "3ac2abf63f54ff71", "fp8gb_device.cuh": "b761586718523e93"}},
+}
 
 
-def gemm_traffic():
+def gemm_traffic(name):
     import hashlib
+    entry = GEMM_TRAFFIC.get(name)
+    if entry is None:
+        return None
     csrc = os.path.join(ROOT, "fp8_mixed_precision_scale_gb300", "csrc")
-    for name, want in GEMM_TRAFFIC["sources"].items():
-        with open(os.path.join(csrc, name), "rb") as f:
+    for fname, want in entry["sources"].items():
+        with open(os.path.join(csrc, fname), "rb") as f:
             if hashlib.sha256(f.read()).hexdigest()[:16] != want:
                 return None
-    return GEMM_TRAFFIC["bytes"]
+    return entry["bytes"]
 
 
 def peaks():
@@ -681,8 +690,8 @@ def run_gpu(args, rank, world, local_rank):
         if g_roof_ms <= g_tensor_ms * 1.0001:      # tensor-bound GEMMs
             roof = {"bound": "tensor", "achieved": round(gemm_tflops, 1), "peak": round(fp8_peak, 1),
                     "unit": "TFLOP/s", "frac": round(gemm_tflops / fp8_peak, 4),
-                    "kernel": "mx_gemm_kernel" if step.name == "llama_mxfp8" else "fp8_gemm_kernel",
-                    "traffic": gemm_traffic() if step.name == "llama_mlp" else None,
+                    "kernel": GEMM_TRAFFIC[step.name]["kernel"] if step.name in GEMM_TRAFFIC else "fp8_gemm_kernel",
+                    "traffic": gemm_traffic(step.name),
                     "peak_source": f"{peak_src}: 2 x sustained bf16 {bf16_sust} TFLOP/s (fp8/bf16 nominal ratio 2)"}
         else:                                      # HBM-bound (grouped GEMMs at the MoE shape)
             gbs = sum(b for _, b in g_work) / (sum(g_ms) * 1e-3) / 1e9
