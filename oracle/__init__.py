@@ -101,6 +101,12 @@ def _load():
             lib.orc_mx_gemm.restype = None
             lib.orc_mx_gemm.argtypes = [P, i32, i64, P, i64, P, i32, i64, P, i64, i64, i64, i64, P, P, i64,
                                         P, P]
+            lib.orc_exp_f32.restype = f32
+            lib.orc_exp_f32.argtypes = [f32]
+            lib.orc_bf16_rne.restype = ctypes.c_uint16
+            lib.orc_bf16_rne.argtypes = [f32]
+            lib.orc_swiglu_bf16.restype = None
+            lib.orc_swiglu_bf16.argtypes = [P, P, i64, P]
             _lib = lib
     return _lib
 
@@ -314,3 +320,43 @@ def mx_gemm(A, fa, sA, B, fb, sB, points=None):
     _load().orc_mx_gemm(_ptr(A), fa, K, _ptr(sA), sA.shape[1], _ptr(B), fb, K, _ptr(sB), sB.shape[1], M, N, K,
                         _ptr(pm), _ptr(pn), npts, _ptr(ref), _ptr(bound))
     return ref, bound
+
+
+# --- MoE prologues: gather (permute) and SwiGLU ------------------------------
+
+def exp_f32(x: float) -> np.float32:
+    """The fixed fp32 exp (Cody-Waite reduction, degree-6 Taylor) of the
+    SwiGLU definition."""
+    return np.float32(_load().orc_exp_f32(float(np.float32(x))))
+
+
+def bf16_rne(x: float) -> int:
+    return int(_load().orc_bf16_rne(float(np.float32(x))))
+
+
+def swiglu_bf16(g_bits, u_bits) -> np.ndarray:
+    """h = bf16(silu(g) * u) element-wise on bf16 bit patterns."""
+    g = _c(g_bits, np.uint16)
+    u = _c(u_bits, np.uint16)
+    assert g.shape == u.shape
+    h = np.zeros(g.shape, np.uint16)
+    _load().orc_swiglu_bf16(_ptr(g), _ptr(u), g.size, _ptr(h))
+    return h
+
+
+def mx_permute_quantize(x_bits, src_rows, fmt, layouts=LAYOUT_ROW | LAYOUT_COLT, offsets=None, align=128):
+    """Gather rows x[src_rows] (the permutation of token rows into expert
+    order), then MX-quantize them (see mx_quantize)."""
+    x = _c(x_bits, np.uint16)
+    return mx_quantize(x[np.asarray(src_rows, np.int64)], fmt, layouts, offsets=offsets, align=align)
+
+
+def mx_swiglu_quantize(gate_up_bits, fmt, layouts=LAYOUT_ROW | LAYOUT_COLT, offsets=None, align=128):
+    """h = SwiGLU of a [rows, 2F] gate|up tensor (gate in columns [0, F), up
+    in [F, 2F)), then MX quantize of h.  Returns the mx_quantize dict plus h."""
+    gu = _c(gate_up_bits, np.uint16)
+    F = gu.shape[1] // 2
+    h = swiglu_bf16(gu[:, :F], gu[:, F:])
+    out = mx_quantize(h, fmt, layouts, offsets=offsets, align=align)
+    out["h"] = h
+    return out

@@ -690,3 +690,91 @@ void orc_mx_gemm(const uint8_t *A, int fa, int64_t lda, const uint8_t *sA, int64
         bound[i] = t;
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* MoE prologues fused ahead of the quantize: gather (permute) and SwiGLU     */
+/* ------------------------------------------------------------------------ */
+/*
+ * "FP8 Training on AMD GPUs with TorchTitan and TorchAO" (the fused Triton
+ * kernels question) replaces a five-kernel eager chain in front of the MoE
+ * grouped GEMMs by one fused kernel.  The two element-wise steps that sit
+ * in front of the expert GEMMs of a MoE layer are the permutation of token
+ * rows into expert order (a gather by routing index) and, between the
+ * gate/up and down projections, SwiGLU.  Their definitions here:
+ *
+ *   gather : row i of the output is row src[i] of the input.
+ *   SwiGLU : h = bf16_rne(silu(g) * u), silu(g) = g / (1 + exp(-g)), with
+ *            every operation an IEEE fp32 operation (round to nearest even,
+ *            no fused multiply-add) and exp evaluated by the fixed fp32
+ *            algorithm below, so that a kernel evaluating the same steps in
+ *            the same order produces the same bf16 value.
+ *
+ * exp_f32 (Cody-Waite argument reduction and a Taylor polynomial):
+ *   n = rint(x * log2(e)), r = (x - n * C1) - n * C2, where C1 is ln 2
+ *   rounded to 16 significant bits (so n * C1 is exact) and C2 = fp32(ln 2 -
+ *   C1); e^r ~ 1 + r + r^2/2! + ... + r^6/6! by Horner's rule (|r| <= 0.35,
+ *   truncation below 2e-7 relative); the result is scaled by 2^n in two
+ *   exact power-of-two multiplies.  x > 88 gives +Inf, x < -104 gives +0,
+ *   NaN gives NaN.
+ */
+static float f32_mul(float a, float b) { volatile float r = a * b; return r; }
+static float f32_add(float a, float b) { volatile float r = a + b; return r; }
+static float f32_sub(float a, float b) { volatile float r = a - b; return r; }
+static float f32_div(float a, float b) { volatile float r = a / b; return r; }
+
+static float pow2_f32(int n) /* 2^n for -126 <= n <= 127 */
+{
+    uint32_t u = (uint32_t)(n + 127) << 23;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+float orc_exp_f32(float x)
+{
+    const float LOG2E = 1.44269502f;            /* fp32(1 / ln 2) */
+    const float C1 = 0.693145751953125f;        /* ln 2 to 16 significant bits */
+    const float C2 = 1.42860677e-06f;           /* fp32(ln 2 - C1) */
+    float n, r, p;
+    int ni;
+    if (isnan(x)) return x;
+    if (x > 88.0f) return INFINITY;
+    if (x < -104.0f) return 0.0f;
+    n = rintf(f32_mul(x, LOG2E));
+    ni = (int)n;
+    r = f32_sub(f32_sub(x, f32_mul(n, C1)), f32_mul(n, C2));
+    /* Horner: 1 + r(1 + r(1/2 + r(1/6 + r(1/24 + r(1/120 + r/720))))) */
+    p = f32_add(1.0f / 120.0f, f32_mul(r, 1.0f / 720.0f));
+    p = f32_add(1.0f / 24.0f, f32_mul(r, p));
+    p = f32_add(1.0f / 6.0f, f32_mul(r, p));
+    p = f32_add(0.5f, f32_mul(r, p));
+    p = f32_add(1.0f, f32_mul(r, p));
+    p = f32_add(1.0f, f32_mul(r, p));
+    /* 2^n in two power-of-two multiplies (n in [-150, 127]: each factor is
+     * a normal fp32 power of two) */
+    p = f32_mul(p, pow2_f32(ni / 2));
+    p = f32_mul(p, pow2_f32(ni - ni / 2));
+    return p;
+}
+
+/* bf16 bit pattern of an fp32 value, round to nearest even (NaN stays NaN). */
+uint16_t orc_bf16_rne(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    if ((u & 0x7FFFFFFFu) > 0x7F800000u) return (uint16_t)((u >> 16) | 0x40u);
+    u += 0x7FFFu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+
+/* h = bf16(silu(g) * u) for n pairs; g, u and h are bf16 bit patterns. */
+void orc_swiglu_bf16(const uint16_t *g, const uint16_t *u, int64_t n, uint16_t *h)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; i++) {
+        float gf = bf16_to_float(g[i]), uf = bf16_to_float(u[i]);
+        float e = orc_exp_f32(-gf);
+        float s = f32_div(gf, f32_add(1.0f, e));
+        h[i] = orc_bf16_rne(f32_mul(s, uf));
+    }
+}
