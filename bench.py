@@ -29,6 +29,9 @@ Other workloads (same JSON line, their own config):
   quantize_grouped  the rowwise quantize of one reduced MoE weight (64
                  experts x 2048 rows x 7168), for profiling
   mx_gemm, mx_quantize  the MXFP8 gate GEMM / the MX quantize of dY_gate
+  mx_permute, mx_swiglu  fused MoE prologue + MX quantize at DeepSeek-V3
+                 shapes (gather of 4096 x top-8 routed rows of 7168; SwiGLU
+                 of [32768, 2 x 2048]), also timed against the unfused chain
 
 Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle on a
 bounded sample of the same workload instead.
@@ -643,7 +646,8 @@ def run_gpu(args, rank, world, local_rank):
     hbm_gbs, bf16_burst, bf16_sust, peak_src = peaks()
     fp8_peak = 2.0 * bf16_sust               # FP8 dense = 2x bf16 dense (nominal 4.5 vs 2.25 PFLOP/s)
 
-    if args.workload in ("gemm", "quantize", "grouped_m", "grouped_k", "quantize_grouped", "mx_gemm", "mx_quantize"):
+    if args.workload in ("gemm", "quantize", "grouped_m", "grouped_k", "quantize_grouped", "mx_gemm", "mx_quantize",
+                         "mx_permute", "mx_swiglu"):
         run_single_kernel(args, dev, rank)
         return
     if args.workload == "sweep":
@@ -909,10 +913,52 @@ def grouped_weight_quantize_case(dev, E=64):
     return fn, quantize_bytes((rows, H)) / 1e9, "GB/s (algorithmic)"
 
 
+def moe_fused_case(kind, dev, T=4096, topk=8, E=256):
+    """DeepSeek-V3-shaped fused MoE prologue + MX quantize (both layouts,
+    per-expert grouping): `mx_permute` gathers 4096 tokens x top-8 routed
+    rows of hidden 7168 into expert order; `mx_swiglu` applies SwiGLU to the
+    [32768, 2 x 2048] gate|up output.  Returns (fused fn, unfused-chain fn,
+    algorithmic GB per call)."""
+    import numpy as np
+
+    import fp8_mixed_precision_scale_gb300 as fp8
+    import synth
+    H, F = synth.DSV3["H"], synth.DSV3["F"]
+    rng = np.random.default_rng(5)
+    experts = np.argsort(rng.random((T, E)), axis=1)[:, :topk]
+    tok = np.repeat(np.arange(T), topk)
+    order = np.argsort(experts.reshape(-1), kind="stable")
+    src = torch.from_numpy(tok[order].astype(np.int32)).to(dev)
+    off_h = torch.from_numpy(np.concatenate([[0], np.cumsum(np.bincount(experts.reshape(-1), minlength=E))])
+                             .astype(np.int32))
+    off = off_h.to(dev)
+    rows = T * topk
+    g = torch.Generator(device=dev)
+    g.manual_seed(9)
+    if kind == "mx_permute":
+        x = _normal(g, dev, (T, H), 1.0)
+        fused = lambda: fp8.mx_permute_quantize(x, src, 0, 3, group_offsets=off, host_offsets=off_h)  # noqa: E731
+        src64 = src.long()
+        unfused = lambda: fp8.mx_quantize(x.index_select(0, src64), 0, 3, group_offsets=off,  # noqa: E731
+                                          host_offsets=off_h)
+        return fused, unfused, rows * H * (2 + 2 + 2 / 32) / 1e9
+    gu = _normal(g, dev, (rows, 2 * F), 2.0)
+    fused = lambda: fp8.mx_swiglu_quantize(gu, 0, 3, group_offsets=off, host_offsets=off_h)  # noqa: E731
+
+    def unfused():
+        h = (torch.nn.functional.silu(gu[:, :F].float()) * gu[:, F:].float()).to(torch.bfloat16)
+        return fp8.mx_quantize(h, 0, 3, group_offsets=off, host_offsets=off_h)
+    return fused, unfused, rows * F * (4 + 2 + 2 / 32) / 1e9
+
+
 def run_single_kernel(args, dev, rank):
     """Time one kernel of the default step in isolation (profiling aid)."""
     import fp8_mixed_precision_scale_gb300 as fp8
-    if args.workload in ("grouped_m", "grouped_k"):
+    unfused = None
+    if args.workload in ("mx_permute", "mx_swiglu"):
+        fn, unfused, work = moe_fused_case(args.workload, dev)
+        unit = "GB/s (algorithmic)"
+    elif args.workload in ("grouped_m", "grouped_k"):
         fn, work, unit = grouped_case(args.workload, dev)
     elif args.workload == "quantize_grouped":
         fn, work, unit = grouped_weight_quantize_case(dev)
@@ -948,9 +994,21 @@ def run_single_kernel(args, dev, rank):
     torch.cuda.synchronize()
     assert fp8.fp8_sync_status() == 0
     ms = a.elapsed_time(b) / args.steps
+    line = {"workload": args.workload, "ms_per_launch": round(ms, 4), "value": round(work / (ms * 1e-3), 1),
+            "unit": unit, "launches": args.steps}
+    if unfused is not None:   # the same result through the unfused chain (torch prologue, then the quantize)
+        for _ in range(3):
+            unfused()
+        torch.cuda.synchronize()
+        a.record()
+        for _ in range(args.steps):
+            unfused()
+        b.record()
+        torch.cuda.synchronize()
+        line["unfused_chain_ms"] = round(a.elapsed_time(b) / args.steps, 4)
+        line["speedup_vs_chain"] = round(line["unfused_chain_ms"] / ms, 2)
     if rank == 0:
-        print(json.dumps({"workload": args.workload, "ms_per_launch": round(ms, 4),
-                          "value": round(work / (ms * 1e-3), 1), "unit": unit, "launches": args.steps}), flush=True)
+        print(json.dumps(line), flush=True)
 
 
 def run_reference(args, rank, world):
@@ -991,7 +1049,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="llama_mlp",
                     choices=["llama_mlp", "llama_rowwise", "llama_mxfp8", "moe", "flux", "sweep", "gemm", "quantize",
-                             "grouped_m", "grouped_k", "quantize_grouped", "mx_gemm", "mx_quantize"],
+                             "grouped_m", "grouped_k", "quantize_grouped", "mx_gemm", "mx_quantize", "mx_permute",
+                             "mx_swiglu"],
                     help="llama_mlp: the whole fwd+bwd FP8 step of the Llama-3-8B MLP (default); see the "
                          "module docstring for the others")
     args = ap.parse_args()

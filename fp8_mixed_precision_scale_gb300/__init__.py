@@ -40,7 +40,7 @@ LIB_PATH = os.path.join(_HERE, "libfp8gb.so")
 EXPORTED = ("fp8_quantize", "fp8_update_amax_history", "fp8_scaled_gemm", "fp8_grouped_gemm",
             "fp8_group_padded_offsets", "fp8_sync_status", "fp8_selftest_bounded_wait", "fp8_status_string",
             "fp8_last_cuda_error", "fp8_version", "fp8_mx_scale_bytes", "fp8_mx_quantize", "fp8_mx_gemm",
-            "fp8_mx_grouped_gemm")
+            "fp8_mx_grouped_gemm", "fp8_mx_permute_quantize", "fp8_mx_swiglu_quantize")
 MX_BLOCK = 32
 MX_GROUP_ALIGN = 128
 
@@ -119,6 +119,10 @@ def load_library():
             lib.fp8_mx_scale_bytes.argtypes = [i64, i64]
             lib.fp8_mx_quantize.restype = i32
             lib.fp8_mx_quantize.argtypes = [P, i64, i64, i64, i32, i32, P, P, P, i64, P, P, i32, P]
+            lib.fp8_mx_permute_quantize.restype = i32
+            lib.fp8_mx_permute_quantize.argtypes = [P, i64, i64, i64, P, i64, i32, i32, P, P, P, i64, P, P, i32, P]
+            lib.fp8_mx_swiglu_quantize.restype = i32
+            lib.fp8_mx_swiglu_quantize.argtypes = [P, i64, i64, i64, i32, i32, P, i64, P, P, P, i64, P, P, i32, P]
             lib.fp8_mx_gemm.restype = i32
             lib.fp8_mx_gemm.argtypes = [P, i32, i64, P, P, i32, i64, P, i64, i64, i64, P, i64, P]
             lib.fp8_mx_grouped_gemm.restype = i32
@@ -208,6 +212,26 @@ def fp8_mx_quantize(x, rows, cols, ld_x, fmt, layouts, q_row, s_row, q_colT, ld_
                                         ld_colT, _p(s_col), _p(group_offsets), num_groups, _stream(stream))
     if check:
         _check(rc, "fp8_mx_quantize")
+    return rc
+
+
+def fp8_mx_permute_quantize(x, x_rows, cols, ld_x, src_rows, rows, fmt, layouts, q_row, s_row, q_colT, ld_colT,
+                            s_col, group_offsets=None, num_groups=0, stream=None, check=True):
+    rc = load_library().fp8_mx_permute_quantize(_p(x), x_rows, cols, ld_x, _p(src_rows), rows, fmt, layouts,
+                                                _p(q_row), _p(s_row), _p(q_colT), ld_colT, _p(s_col),
+                                                _p(group_offsets), num_groups, _stream(stream))
+    if check:
+        _check(rc, "fp8_mx_permute_quantize")
+    return rc
+
+
+def fp8_mx_swiglu_quantize(gate_up, rows, F, ld, fmt, layouts, h, ld_h, q_row, s_row, q_colT, ld_colT, s_col,
+                           group_offsets=None, num_groups=0, stream=None, check=True):
+    rc = load_library().fp8_mx_swiglu_quantize(_p(gate_up), rows, F, ld, fmt, layouts, _p(h), ld_h, _p(q_row),
+                                               _p(s_row), _p(q_colT), ld_colT, _p(s_col), _p(group_offsets),
+                                               num_groups, _stream(stream))
+    if check:
+        _check(rc, "fp8_mx_swiglu_quantize")
     return rc
 
 
@@ -343,6 +367,50 @@ def mx_quantize(x: torch.Tensor, fmt: int, layouts: int = LAYOUT_ROW | LAYOUT_CO
     fp8_mx_quantize(x, rows, cols, x.stride(0), fmt, layouts, q_row, s_row, q_colT, ld_colT, s_col, group_offsets,
                     G, stream)
     return MxQuantized(q_row, s_row, q_colT, s_col, ld_colT, P)
+
+
+def _mx_outputs(rows, cols, dev, layouts, host_offsets):
+    P = fp8_group_padded_offsets(host_offsets, MX_GROUP_ALIGN)[0] if host_offsets is not None else rows
+    ld_colT = max(16, (P + 15) // 16 * 16)
+
+    def buf(n):  # never a zero-byte (null) allocation
+        return torch.empty(max(16, n), dtype=torch.uint8, device=dev)
+
+    q_row = s_row = q_colT = s_col = None
+    if layouts & LAYOUT_ROW:
+        q_row = buf(rows * cols)[:rows * cols].view(rows, cols)
+        s_row = buf(fp8_mx_scale_bytes(P, cols // MX_BLOCK))
+    if layouts & LAYOUT_COLT:
+        q_colT = buf(cols * ld_colT)[:cols * ld_colT].view(cols, ld_colT)
+        s_col = buf(fp8_mx_scale_bytes(cols, P // MX_BLOCK))
+    return MxQuantized(q_row, s_row, q_colT, s_col, ld_colT, P)
+
+
+def mx_permute_quantize(x: torch.Tensor, src_rows: torch.Tensor, fmt: int, layouts: int = LAYOUT_ROW | LAYOUT_COLT,
+                        group_offsets=None, host_offsets=None, stream=None) -> MxQuantized:
+    """Gather x[src_rows] (routed token rows in expert order) and MX-quantize
+    them in one pass."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1 and src_rows.dtype == torch.int32
+    rows, cols = src_rows.numel(), x.shape[1]
+    q = _mx_outputs(rows, cols, x.device, layouts, host_offsets)
+    G = 0 if group_offsets is None else group_offsets.numel() - 1
+    fp8_mx_permute_quantize(x, x.shape[0], cols, x.stride(0), src_rows, rows, fmt, layouts, q.q_row, q.s_row,
+                            q.q_colT, q.ld_colT, q.s_col, group_offsets, G, stream)
+    return q
+
+
+def mx_swiglu_quantize(gate_up: torch.Tensor, fmt: int, layouts: int = LAYOUT_ROW | LAYOUT_COLT, h_out=None,
+                       group_offsets=None, host_offsets=None, stream=None) -> MxQuantized:
+    """h = bf16(silu(gate) * up) of a [rows, 2F] gate|up tensor, MX-quantized
+    in one pass (h also written to h_out when given)."""
+    assert gate_up.dtype == torch.bfloat16 and gate_up.dim() == 2 and gate_up.stride(1) == 1
+    rows, F = gate_up.shape[0], gate_up.shape[1] // 2
+    q = _mx_outputs(rows, F, gate_up.device, layouts, host_offsets)
+    G = 0 if group_offsets is None else group_offsets.numel() - 1
+    fp8_mx_swiglu_quantize(gate_up, rows, F, gate_up.stride(0), fmt, layouts, h_out,
+                           h_out.stride(0) if h_out is not None else 0, q.q_row, q.s_row, q.q_colT, q.ld_colT,
+                           q.s_col, group_offsets, G, stream)
+    return q
 
 
 def mx_gemm(A: torch.Tensor, fa: int, sA: torch.Tensor, B: torch.Tensor, fb: int, sB: torch.Tensor, K=None,

@@ -118,7 +118,7 @@ extern "C" fp8_status_t fp8_sync_status(void *stream)
         e = cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero));
         if (e != cudaSuccess) return cuda_fail_with(e);
         // a wait that gave up outranks malformed device-side offsets
-        return (word & ~ERR_BAD_OFFSETS) ? FP8_ERR_TIMEOUT : FP8_ERR_INVALID_ARG;
+        return (word & ~(ERR_BAD_OFFSETS | ERR_BAD_INDEX)) ? FP8_ERR_TIMEOUT : FP8_ERR_INVALID_ARG;
     }
     return FP8_OK;
 }

@@ -25,6 +25,7 @@ enum : unsigned int {
     ERR_TEARDOWN_WAIT = 8u,
     ERR_SELFTEST_WAIT = 16u,
     ERR_BAD_OFFSETS = 32u,
+    ERR_BAD_INDEX = 64u,  // a gather index outside the source rows
 };
 
 __device__ __forceinline__ void record_error(unsigned int *err, unsigned int bits)

@@ -49,7 +49,15 @@ struct MxArgs {
     int G;
     int do_row, do_col;
     unsigned int *err;
+    // prologues (template parameter PRO of the kernel)
+    const int32_t *src_rows;  // PRO_GATHER: output row r reads input row src_rows[r]
+    int64_t x_rows;           // PRO_GATHER: rows of the input
+    int64_t up_off;           // PRO_SWIGLU: column offset of `up` in each input row (= cols)
+    uint16_t *h_out;          // PRO_SWIGLU: optional bf16 [rows][ld_h] copy of h
+    int64_t ld_h;
 };
+
+enum { PRO_NONE = 0, PRO_GATHER = 1, PRO_SWIGLU = 2 };
 
 // E8M0 code of a block from the fp32 bit pattern of its largest magnitude:
 // floor(log2 amax) is the exponent field (normal) or the position of the top
@@ -150,18 +158,112 @@ __device__ __forceinline__ MxTile mx_tile(const MxArgs &a, int64_t t, int64_t pr
     return g;
 }
 
-// Thread (lr, blk) = (tid / 4, tid % 4) loads the 32 bf16 of row lr, block
-// blk of the tile (zeros outside the data).
-__device__ __forceinline__ void mx_load(const MxArgs &a, const MxTile &g, int tid, uint4 (&v)[4])
+// Raw input registers of one thread for one tile: the 32 bf16 of its row
+// block, and for SwiGLU the 32 gate and 32 up values.
+template <int PRO>
+struct MxRaw {
+    uint4 v[PRO == PRO_SWIGLU ? 8 : 4];
+};
+
+// Thread (lr, blk) = (tid / 4, tid % 4) loads row lr, block blk of the tile
+// (zeros outside the data).  Gather reads input row src_rows[r] for output
+// row r (an index outside the input is reported and read as zeros); SwiGLU
+// reads the gate block and the up block `up_off` columns further.
+template <int PRO>
+__device__ __forceinline__ void mx_load(const MxArgs &a, const MxTile &g, int tid, MxRaw<PRO> &raw)
 {
+    constexpr int NV = PRO == PRO_SWIGLU ? 8 : 4;
     const int lr = tid >> 2, blk = tid & 3;
+    const uint16_t *row = nullptr;
     if (g.live && lr < g.nreal && g.c0 + 32 * blk < a.cols) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(a.x + (g.src0 + lr) * a.ld_x + g.c0 + 32 * blk);
+        int64_t r = g.src0 + lr;
+        if constexpr (PRO == PRO_GATHER) {
+            r = __ldg(a.src_rows + r);
+            if (r < 0 || r >= a.x_rows) {
+                record_error(a.err, ERR_BAD_INDEX);
+                r = -1;
+            }
+        }
+        if (r >= 0) row = a.x + r * a.ld_x + g.c0 + 32 * blk;
+    }
+    if (row) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(row);
 #pragma unroll
-        for (int j = 0; j < 4; j++) v[j] = __ldg(src + j);
+        for (int j = 0; j < 4; j++) raw.v[j] = __ldg(src + j);
+        if constexpr (PRO == PRO_SWIGLU) {
+            const uint4 *up = reinterpret_cast<const uint4 *>(row + a.up_off);
+#pragma unroll
+            for (int j = 0; j < 4; j++) raw.v[4 + j] = __ldg(up + j);
+        }
     } else {
 #pragma unroll
-        for (int j = 0; j < 4; j++) v[j] = make_uint4(0, 0, 0, 0);
+        for (int j = 0; j < NV; j++) raw.v[j] = make_uint4(0, 0, 0, 0);
+    }
+}
+
+// exp in IEEE fp32 by a fixed algorithm (Cody-Waite argument reduction with
+// ln 2 split into a 16-significant-bit part and its fp32 remainder, then the
+// degree-6 Taylor polynomial of e^r by Horner's rule, then two exact
+// power-of-two scalings), every operation rounded to nearest without fused
+// multiply-add, so the result is reproducible bit for bit on any IEEE fp32
+// implementation that takes the same steps.  x > 88 -> +Inf, x < -104 -> +0.
+__device__ __forceinline__ float exp_fixed(float x)
+{
+    if (x != x) return x;
+    if (x > 88.0f) return __int_as_float(0x7F800000);
+    if (x < -104.0f) return 0.0f;
+    const float n = rintf(__fmul_rn(x, 1.44269502f));
+    const int ni = (int)n;
+    const float r = __fsub_rn(__fsub_rn(x, __fmul_rn(n, 0.693145751953125f)), __fmul_rn(n, 1.42860677e-06f));
+    float p = __fadd_rn(1.0f / 120.0f, __fmul_rn(r, 1.0f / 720.0f));
+    p = __fadd_rn(1.0f / 24.0f, __fmul_rn(r, p));
+    p = __fadd_rn(1.0f / 6.0f, __fmul_rn(r, p));
+    p = __fadd_rn(0.5f, __fmul_rn(r, p));
+    p = __fadd_rn(1.0f, __fmul_rn(r, p));
+    p = __fadd_rn(1.0f, __fmul_rn(r, p));
+    p = __fmul_rn(p, __int_as_float((ni / 2 + 127) << 23));
+    return __fmul_rn(p, __int_as_float((ni - ni / 2 + 127) << 23));
+}
+
+// fp32 -> bf16 bits, round to nearest even; NaN stays a quiet NaN.
+__device__ __forceinline__ uint32_t bf16_bits_rne(float f)
+{
+    uint32_t u = __float_as_uint(f);
+    if ((u & 0x7FFFFFFFu) > 0x7F800000u) return (u >> 16) | 0x40u;
+    u += 0x7FFFu + ((u >> 16) & 1u);
+    return u >> 16;
+}
+
+// h = bf16(silu(g) * u), silu(g) = g / (1 + exp(-g)), for a packed pair.
+__device__ __forceinline__ uint32_t swiglu2(uint32_t g2, uint32_t u2)
+{
+    const float g0 = bf16lo(g2), g1 = bf16hi(g2);
+    const float s0 = __fdiv_rn(g0, __fadd_rn(1.0f, exp_fixed(-g0)));
+    const float s1 = __fdiv_rn(g1, __fadd_rn(1.0f, exp_fixed(-g1)));
+    return bf16_bits_rne(__fmul_rn(s0, bf16lo(u2))) | (bf16_bits_rne(__fmul_rn(s1, bf16hi(u2))) << 16);
+}
+
+// The 32 bf16 the quantize sees: the raw values, or SwiGLU of gate and up
+// (then also stored to h_out when requested).
+template <int PRO>
+__device__ __forceinline__ void mx_prologue(const MxArgs &a, const MxTile &g, int tid, const MxRaw<PRO> &raw,
+                                            uint4 (&v)[4])
+{
+    if constexpr (PRO == PRO_SWIGLU) {
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            const uint4 gg = raw.v[j], uu = raw.v[4 + j];
+            v[j] = make_uint4(swiglu2(gg.x, uu.x), swiglu2(gg.y, uu.y), swiglu2(gg.z, uu.z), swiglu2(gg.w, uu.w));
+        }
+        const int lr = tid >> 2, blk = tid & 3;
+        if (a.h_out && g.live && lr < g.nreal && g.c0 + 32 * blk < a.cols) {
+            uint4 *dst = reinterpret_cast<uint4 *>(a.h_out + (g.src0 + lr) * a.ld_h + g.c0 + 32 * blk);
+#pragma unroll
+            for (int j = 0; j < 4; j++) dst[j] = v[j];
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; j++) v[j] = raw.v[j];
     }
 }
 
@@ -170,7 +272,7 @@ __device__ __forceinline__ void mx_load(const MxArgs &a, const MxTile &g, int ti
 // phase's column-pair reads (rows r and r + 16 in one warp) hit all 32 banks.
 __device__ __forceinline__ int mx_word(int row, int pair) { return row * (MX_PITCH / 2) + (pair ^ ((row & 16))); }
 
-template <int FMT>
+template <int FMT, int PRO>
 __global__ void __launch_bounds__(MX_THREADS)
     mx_quantize_kernel(MxArgs a)
 {
@@ -193,18 +295,18 @@ __global__ void __launch_bounds__(MX_THREADS)
     // persistent loop; the next tile's loads are issued before this tile's work
     int64_t t = blockIdx.x;
     MxTile g = mx_tile(a, t, prows, poff);
-    uint4 nv[4];
-    mx_load(a, g, tid, nv);
+    MxRaw<PRO> nraw;
+    mx_load<PRO>(a, g, tid, nraw);
     for (; t < total; t += gridDim.x) {
         const MxTile cur = g;
-        uint4 v[4];
-#pragma unroll
-        for (int j = 0; j < 4; j++) v[j] = nv[j];
+        const MxRaw<PRO> raw = nraw;
         if (t + gridDim.x < total) {
             g = mx_tile(a, t + gridDim.x, prows, poff);
-            mx_load(a, g, tid, nv);
+            mx_load<PRO>(a, g, tid, nraw);
         }
         if (!cur.live) continue;  // grouped: beyond the padded total (block-uniform)
+        uint4 v[4];
+        mx_prologue<PRO>(a, cur, tid, raw, v);
 
         // ---- row layout ----
         if (a.do_row) {
@@ -301,22 +403,86 @@ __global__ void __launch_bounds__(MX_THREADS)
     }
 }
 
-template <int FMT>
+template <int FMT, int PRO>
 static fp8_status_t launch_mx(const MxArgs &a, cudaStream_t st)
 {
     const size_t dyn = a.offsets ? (size_t)(a.G + 1) * sizeof(int32_t) : 0;
     const int64_t total = a.n_row_tiles * a.n_col_tiles;
     // persistent: as many blocks as fit at once, each looping over tiles
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mx_quantize_kernel<FMT>, MX_THREADS, dyn) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mx_quantize_kernel<FMT, PRO>, MX_THREADS, dyn) !=
         cudaSuccess)
         return cuda_fail();
     const int64_t cap = (int64_t)num_sms() * (per_sm > 0 ? per_sm : 1);
     int64_t grid = total < cap ? total : cap;
     if (grid > INT32_MAX) grid = INT32_MAX;
     if (grid < 1) return FP8_OK;
-    mx_quantize_kernel<FMT><<<(unsigned)grid, MX_THREADS, dyn, st>>>(a);
+    mx_quantize_kernel<FMT, PRO><<<(unsigned)grid, MX_THREADS, dyn, st>>>(a);
     return check_launch();
+}
+
+// Validation and launch shared by the three entry points: `rows` output rows
+// of `cols` columns read from `x` (row stride ld_x) through the prologue.
+static fp8_status_t mx_run(MxArgs a, int fmt, int layouts, int pro, cudaStream_t st)
+{
+    const int64_t rows = a.rows, cols = a.cols;
+    if (rows < 0 || cols < 1 || a.ld_x < 1) return FP8_ERR_INVALID_ARG;
+    if (fmt == FP8_E4M3FNUZ || fmt == FP8_E5M2FNUZ) return FP8_ERR_UNSUPPORTED;
+    if (fmt != FP8_E4M3FN && fmt != FP8_E5M2) return FP8_ERR_INVALID_ARG;
+    if (layouts < 1 || layouts > 3) return FP8_ERR_INVALID_ARG;
+    if (rows == 0) return FP8_OK;  // nothing to read or write (an all-empty grouped tensor has P = 0)
+    if (!a.x) return FP8_ERR_INVALID_ARG;
+    const bool do_row = layouts & FP8_LAYOUT_ROW, do_col = layouts & FP8_LAYOUT_COLT;
+    if (do_row && (!a.q_row || !a.s_row)) return FP8_ERR_INVALID_ARG;
+    if (do_col && (!a.q_colT || !a.s_col)) return FP8_ERR_INVALID_ARG;
+    if (a.offsets && (a.G < 1 || a.G > MX_MAX_GROUPS)) return FP8_ERR_INVALID_ARG;
+    if (!a.offsets && a.G != 0) return FP8_ERR_INVALID_ARG;
+    if (rows > INT32_MAX || cols > INT32_MAX) return FP8_ERR_INVALID_ARG;
+    if (cols % FP8_MX_BLOCK != 0 || a.ld_x % 8 != 0 || !aligned(a.x, 16)) return FP8_ERR_ALIGNMENT;
+    if (do_row && (!aligned(a.q_row, 16) || !aligned(a.s_row, 4))) return FP8_ERR_ALIGNMENT;
+    if (do_col) {
+        if (a.ld_colT < 16 || a.ld_colT % 16 != 0 || !aligned(a.q_colT, 16)) return FP8_ERR_ALIGNMENT;
+        if (!a.offsets) {
+            if (rows % FP8_MX_BLOCK != 0) return FP8_ERR_ALIGNMENT;
+            if (a.ld_colT < rows) return FP8_ERR_INVALID_ARG;
+        }
+    }
+    a.do_row = do_row;
+    a.do_col = do_col;
+    a.rs_row = (rows + 3) / 4 * 4;
+    a.n_col_tiles = (cols + MX_COLS - 1) / MX_COLS;
+    a.err = device_error_word();
+    if (a.offsets) {
+        // padded row space: at most 127 padding rows per group, and within ld_colT
+        int64_t bound = rows + (int64_t)(FP8_MX_GROUP_ALIGN - 1) * a.G;
+        if (do_col && a.ld_colT < bound) bound = a.ld_colT;
+        a.n_row_tiles = (bound + MX_ROWS - 1) / MX_ROWS;
+    } else {
+        a.n_row_tiles = (a.rs_row + MX_ROWS - 1) / MX_ROWS;
+    }
+    if (pro == PRO_GATHER) return fmt == FP8_E5M2 ? launch_mx<FP8_E5M2, PRO_GATHER>(a, st)
+                                                  : launch_mx<FP8_E4M3FN, PRO_GATHER>(a, st);
+    if (pro == PRO_SWIGLU) return fmt == FP8_E5M2 ? launch_mx<FP8_E5M2, PRO_SWIGLU>(a, st)
+                                                  : launch_mx<FP8_E4M3FN, PRO_SWIGLU>(a, st);
+    return fmt == FP8_E5M2 ? launch_mx<FP8_E5M2, PRO_NONE>(a, st) : launch_mx<FP8_E4M3FN, PRO_NONE>(a, st);
+}
+
+static MxArgs mx_args(const void *x, int64_t rows, int64_t cols, int64_t ld_x, uint8_t *q_row, uint8_t *s_row,
+                      uint8_t *q_colT, int64_t ld_colT, uint8_t *s_col, const int32_t *group_offsets, int num_groups)
+{
+    MxArgs a{};
+    a.x = static_cast<const uint16_t *>(x);
+    a.rows = rows;
+    a.cols = cols;
+    a.ld_x = ld_x;
+    a.q_row = q_row;
+    a.s_row = s_row;
+    a.q_colT = q_colT;
+    a.ld_colT = ld_colT;
+    a.s_col = s_col;
+    a.offsets = group_offsets;
+    a.G = num_groups;
+    return a;
 }
 
 }  // namespace fp8gb
@@ -334,53 +500,36 @@ extern "C" fp8_status_t fp8_mx_quantize(const void *x_bf16, int64_t rows, int64_
                                         int64_t ld_colT, uint8_t *s_col, const int32_t *group_offsets,
                                         int num_groups, void *stream)
 {
-    if (rows < 0 || cols < 1 || ld_x < cols) return FP8_ERR_INVALID_ARG;
-    if (fmt == FP8_E4M3FNUZ || fmt == FP8_E5M2FNUZ) return FP8_ERR_UNSUPPORTED;
-    if (fmt != FP8_E4M3FN && fmt != FP8_E5M2) return FP8_ERR_INVALID_ARG;
-    if (layouts < 1 || layouts > 3) return FP8_ERR_INVALID_ARG;
-    if (rows == 0) return FP8_OK;  // nothing to read or write (an all-empty grouped tensor has P = 0)
-    if (!x_bf16) return FP8_ERR_INVALID_ARG;
-    const bool do_row = layouts & FP8_LAYOUT_ROW, do_col = layouts & FP8_LAYOUT_COLT;
-    if (do_row && (!q_row || !s_row)) return FP8_ERR_INVALID_ARG;
-    if (do_col && (!q_colT || !s_col)) return FP8_ERR_INVALID_ARG;
-    if (group_offsets && (num_groups < 1 || num_groups > MX_MAX_GROUPS)) return FP8_ERR_INVALID_ARG;
-    if (!group_offsets && num_groups != 0) return FP8_ERR_INVALID_ARG;
-    if (rows > INT32_MAX || cols > INT32_MAX) return FP8_ERR_INVALID_ARG;
-    if (cols % FP8_MX_BLOCK != 0 || ld_x % 8 != 0 || !aligned(x_bf16, 16)) return FP8_ERR_ALIGNMENT;
-    if (do_row && (!aligned(q_row, 16) || !aligned(s_row, 4))) return FP8_ERR_ALIGNMENT;
-    if (do_col) {
-        if (ld_colT < 16 || ld_colT % 16 != 0 || !aligned(q_colT, 16)) return FP8_ERR_ALIGNMENT;
-        if (!group_offsets) {
-            if (rows % FP8_MX_BLOCK != 0) return FP8_ERR_ALIGNMENT;
-            if (ld_colT < rows) return FP8_ERR_INVALID_ARG;
-        }
-    }
-    MxArgs a{};
-    a.x = static_cast<const uint16_t *>(x_bf16);
-    a.rows = rows;
-    a.cols = cols;
-    a.ld_x = ld_x;
-    a.q_row = q_row;
-    a.s_row = s_row;
-    a.q_colT = q_colT;
-    a.s_col = s_col;
-    a.ld_colT = ld_colT;
-    a.rs_row = (rows + 3) / 4 * 4;
-    a.n_col_tiles = (cols + MX_COLS - 1) / MX_COLS;
-    a.offsets = group_offsets;
-    a.G = group_offsets ? num_groups : 0;
-    a.do_row = do_row;
-    a.do_col = do_col;
-    a.err = device_error_word();
-    if (group_offsets) {
-        // padded row space: at most 127 padding rows per group, and within ld_colT
-        int64_t bound = rows + (int64_t)(FP8_MX_GROUP_ALIGN - 1) * num_groups;
-        if (do_col && ld_colT < bound) bound = ld_colT;
-        a.n_row_tiles = (bound + MX_ROWS - 1) / MX_ROWS;
-    } else {
-        a.n_row_tiles = (a.rs_row + MX_ROWS - 1) / MX_ROWS;
-    }
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (fmt == FP8_E5M2) return launch_mx<FP8_E5M2>(a, st);
-    return launch_mx<FP8_E4M3FN>(a, st);
+    if (ld_x < cols) return FP8_ERR_INVALID_ARG;
+    MxArgs a = mx_args(x_bf16, rows, cols, ld_x, q_row, s_row, q_colT, ld_colT, s_col, group_offsets, num_groups);
+    return mx_run(a, fmt, layouts, PRO_NONE, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" fp8_status_t fp8_mx_permute_quantize(const void *x_bf16, int64_t x_rows, int64_t cols, int64_t ld_x,
+                                                const int32_t *src_rows, int64_t rows, int fmt, int layouts,
+                                                uint8_t *q_row, uint8_t *s_row, uint8_t *q_colT, int64_t ld_colT,
+                                                uint8_t *s_col, const int32_t *group_offsets, int num_groups,
+                                                void *stream)
+{
+    if (x_rows < 0 || ld_x < cols) return FP8_ERR_INVALID_ARG;
+    if (rows > 0 && (!src_rows || x_rows < 1)) return FP8_ERR_INVALID_ARG;
+    MxArgs a = mx_args(x_bf16, rows, cols, ld_x, q_row, s_row, q_colT, ld_colT, s_col, group_offsets, num_groups);
+    a.src_rows = src_rows;
+    a.x_rows = x_rows;
+    return mx_run(a, fmt, layouts, PRO_GATHER, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" fp8_status_t fp8_mx_swiglu_quantize(const void *gate_up_bf16, int64_t rows, int64_t F, int64_t ld,
+                                               int fmt, int layouts, void *h_bf16, int64_t ld_h, uint8_t *q_row,
+                                               uint8_t *s_row, uint8_t *q_colT, int64_t ld_colT, uint8_t *s_col,
+                                               const int32_t *group_offsets, int num_groups, void *stream)
+{
+    if (F < 1 || ld < 2 * F) return FP8_ERR_INVALID_ARG;
+    if (h_bf16 && (ld_h < F)) return FP8_ERR_INVALID_ARG;
+    if (h_bf16 && (ld_h % 8 != 0 || !aligned(h_bf16, 16))) return FP8_ERR_ALIGNMENT;
+    MxArgs a = mx_args(gate_up_bf16, rows, F, ld, q_row, s_row, q_colT, ld_colT, s_col, group_offsets, num_groups);
+    a.up_off = F;
+    a.h_out = static_cast<uint16_t *>(h_bf16);
+    a.ld_h = ld_h;
+    return mx_run(a, fmt, layouts, PRO_SWIGLU, static_cast<cudaStream_t>(stream));
 }

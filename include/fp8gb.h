@@ -293,6 +293,45 @@ FP8GB_API fp8_status_t fp8_mx_quantize(const void *x_bf16, int64_t rows, int64_t
                                        int num_groups, void *stream);
 
 /*
+ * Fused MoE prologues ("FP8 Training on AMD GPUs with TorchTitan and TorchAO":
+ * a five-kernel eager chain in front of the MoE grouped GEMMs replaced by one
+ * fused kernel).  Each reads its bf16 input once and writes exactly what
+ * fp8_mx_quantize would write for the tensor the prologue defines; same
+ * layouts, grouping, limits and errors as fp8_mx_quantize.
+ *
+ * fp8_mx_permute_quantize -- gather, then MX quantize: output row r is input
+ *   row src_rows[r] (the permutation of routed token rows into expert order;
+ *   a token routed to k experts appears k times).
+ *     x_bf16    [x_rows][ld_x] bf16 token rows; cols % 32 == 0.
+ *     src_rows  device int32 [rows]; an index outside [0, x_rows) is read as a
+ *               zero row and reported (fp8_sync_status: FP8_ERR_INVALID_ARG).
+ *     rows      output rows (the routed rows, grouped by expert when
+ *               group_offsets is given).
+ *
+ * fp8_mx_swiglu_quantize -- h = bf16(silu(g) * u), then MX quantize of h.
+ *     gate_up_bf16  [rows][ld] bf16: gate in columns [0, F), up in [F, 2F);
+ *                   ld >= 2F, ld % 8 == 0; F % 32 == 0.
+ *     h_bf16        optional [rows][ld_h] bf16 copy of h (NULL: not written).
+ *   silu(g) = g / (1 + exp(-g)) is evaluated in IEEE fp32 (round to nearest,
+ *   no fused multiply-add) with exp computed by a fixed algorithm:
+ *   n = rint(x log2 e), r = (x - n C1) - n C2 (C1 = ln 2 to 16 significant
+ *   bits, C2 = fp32(ln 2 - C1)), e^r by the degree-6 Taylor polynomial in
+ *   Horner form, scaled by 2^n in two exact steps; x > 88 -> Inf, x < -104 ->
+ *   0.  h is that fp32 product rounded to bf16 (nearest even), so the
+ *   quantized bytes are reproducible from the definition.
+ */
+FP8GB_API fp8_status_t fp8_mx_permute_quantize(const void *x_bf16, int64_t x_rows, int64_t cols, int64_t ld_x,
+                                               const int32_t *src_rows, int64_t rows, int fmt, int layouts,
+                                               uint8_t *q_row, uint8_t *s_row, uint8_t *q_colT, int64_t ld_colT,
+                                               uint8_t *s_col, const int32_t *group_offsets, int num_groups,
+                                               void *stream);
+
+FP8GB_API fp8_status_t fp8_mx_swiglu_quantize(const void *gate_up_bf16, int64_t rows, int64_t F, int64_t ld,
+                                              int fmt, int layouts, void *h_bf16, int64_t ld_h, uint8_t *q_row,
+                                              uint8_t *s_row, uint8_t *q_colT, int64_t ld_colT, uint8_t *s_col,
+                                              const int32_t *group_offsets, int num_groups, void *stream);
+
+/*
  * fp8_mx_gemm -- C[m][n] = bf16( sum_k A[m][k] X_A(m, k/32) B[n][k] X_B(n, k/32) )
  * on the tcgen05 block-scaled tensor cores (kind::mxf8f6f4, scales read by
  * the MMA from tensor memory), fp32 accumulation, "TN" operands.

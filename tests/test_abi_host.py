@@ -256,3 +256,22 @@ def test_mx_grouped_gemm_validation(lib):
     assert mxgg_call(lib, N=254) == ALIGN                  # scale rows of a tile start on a word boundary
     assert mxgg_call(lib, mode=1, ldT=192) == ALIGN        # groups padded to 128 columns
     assert mxgg_call(lib, mode=1, ldT=256, K=130) == ALIGN
+
+
+def test_mx_fused_validation(lib):
+    P = ctypes.c_void_p
+    perm = lambda **kw: lib.fp8_mx_permute_quantize(  # noqa: E731
+        P(kw.get("x", FAKE)), kw.get("x_rows", 64), kw.get("cols", 64), 64, P(kw.get("src", FAKE)),
+        kw.get("rows", 64), kw.get("fmt", 0), 1, P(FAKE), P(FAKE), None, 0, None, None, 0, None)
+    assert perm(src=None) == INVALID
+    assert perm(x_rows=0) == INVALID
+    assert perm(cols=48) == ALIGN                          # 48 columns are not whole 32-element blocks
+    assert perm(fmt=2) == UNSUPPORTED
+    assert perm(rows=0, src=None) == OK
+    swi = lambda **kw: lib.fp8_mx_swiglu_quantize(  # noqa: E731
+        P(FAKE), 64, kw.get("F", 64), kw.get("ld", 128), 0, 1, P(kw.get("h", None)), kw.get("ld_h", 0),
+        P(FAKE), P(FAKE), None, 0, None, None, 0, None)
+    assert swi(ld=100) == INVALID                          # shorter than 2F
+    assert swi(F=48, ld=96) == ALIGN
+    assert swi(h=FAKE, ld_h=32) == INVALID
+    assert swi(h=FAKE + 8, ld_h=64) == ALIGN
