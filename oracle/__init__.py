@@ -107,6 +107,10 @@ def _load():
             lib.orc_bf16_rne.argtypes = [f32]
             lib.orc_swiglu_bf16.restype = None
             lib.orc_swiglu_bf16.argtypes = [P, P, i64, P]
+            lib.orc_blockwise_code.restype = i32
+            lib.orc_blockwise_code.argtypes = [f64, i32]
+            lib.orc_blockwise_quantize.restype = i32
+            lib.orc_blockwise_quantize.argtypes = [P, i64, i64, i64, i32, i32, i32, P, P, P, P]
             _lib = lib
     return _lib
 
@@ -360,3 +364,25 @@ def mx_swiglu_quantize(gate_up_bits, fmt, layouts=LAYOUT_ROW | LAYOUT_COLT, offs
     out = mx_quantize(h, fmt, layouts, offsets=offsets, align=align)
     out["h"] = h
     return out
+
+
+# --- blockwise (1 x 128 / 128 x 128 blocks, power-of-two scales) -------------
+
+def blockwise_code(amax: float, fmt: int) -> int:
+    """E8M0 code of 1/s, s = the largest power of two with amax * s <= fp8_max."""
+    return _load().orc_blockwise_code(float(amax), int(fmt))
+
+
+def blockwise_quantize(x_bits, fmt, block_rows, layouts=LAYOUT_ROW | LAYOUT_COLT):
+    """Blockwise quantize (block_rows 1: 1 x 128 activation blocks, 128:
+    128 x 128 weight blocks).  Returns q_row, s_row [rows, cols/32], q_colT
+    [cols, rows], s_col [cols, rows/32] with per-32-block E8M0 codes."""
+    x = _c(x_bits, np.uint16)
+    rows, cols = x.shape
+    q_row = np.zeros((rows, cols), np.uint8) if layouts & LAYOUT_ROW else None
+    s_row = np.zeros((rows, cols // 32), np.uint8) if layouts & LAYOUT_ROW else None
+    q_colT = np.zeros((cols, rows), np.uint8) if layouts & LAYOUT_COLT else None
+    s_col = np.zeros((cols, rows // 32), np.uint8) if layouts & LAYOUT_COLT else None
+    _load().orc_blockwise_quantize(_ptr(x), rows, cols, cols, fmt, block_rows, layouts, _ptr(q_row), _ptr(s_row),
+                                   _ptr(q_colT), _ptr(s_col))
+    return dict(q_row=q_row, s_row=s_row, q_colT=q_colT, s_col=s_col)
