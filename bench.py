@@ -21,6 +21,9 @@ Other workloads (same JSON line, their own config):
                  9216), delayed scaling, all E4M3, amax algo max
   llama_mxfp8    the Llama-3-8B MLP step under the MXFP8 recipe (blocks of 32
                  with E8M0 scales, both layouts per tensor, block-scaled GEMMs)
+  llama_blockwise  the same step under the blockwise recipe (1x128 activation
+                 and gradient blocks, 128x128 weight blocks, power-of-two scales)
+  bw_quantize    the blockwise quantize of dY_gate (1x128 blocks)
   sweep          the delayed quantize (E4M3, both layouts) of 2^20 .. 2^30
                  elements, GB/s against size
   gemm, quantize single kernels of the default step, for profiling
@@ -398,12 +401,18 @@ class MxStep:
     layout, along columns for the transposed one, E8M0 scales); the nine
     GEMMs on the block-scaled tensor cores.  No history, no update."""
 
-    def __init__(self, dev, seed, keys=None, outs=None):
+    def __init__(self, dev, seed, keys=None, outs=None, recipe="mxfp8"):
         import fp8_mixed_precision_scale_gb300 as fp8
         self.fp8 = fp8
-        self.name = "llama_mxfp8"
-        self.desc = ("llama3-8b-mlp fwd+bwd, mxfp8 recipe (OCP MX: 32-element blocks, E8M0 scales): tokens 8192, "
-                     "hidden 4096, ffn 14336, e4m3 fwd / e5m2 grads")
+        self.recipe = recipe
+        self.name = "llama_" + recipe
+        if recipe == "mxfp8":
+            self.desc = ("llama3-8b-mlp fwd+bwd, mxfp8 recipe (OCP MX: 32-element blocks, E8M0 scales): tokens 8192, "
+                         "hidden 4096, ffn 14336, e4m3 fwd / e5m2 grads")
+        else:
+            self.desc = ("llama3-8b-mlp fwd+bwd, blockwise recipe (1x128 activation / gradient blocks, 128x128 weight "
+                         "blocks, power-of-two scales, block-scaled GEMMs): tokens 8192, hidden 4096, ffn 14336, "
+                         "e4m3 fwd / e5m2 grads")
         self.tokens = T_
         g = torch.Generator(device=dev)
         g.manual_seed(seed)
@@ -432,7 +441,11 @@ class MxStep:
     def quantize(self, k):
         t, q = self.inp[k], self.q[k]
         r, c = t.shape
-        self.fp8.fp8_mx_quantize(t, r, c, c, self.fmt[k], 3, q["row"], q["srow"], q["colT"], r, q["scol"])
+        if self.recipe == "blockwise":
+            self.fp8.fp8_blockwise_quantize(t, r, c, c, self.fmt[k], 128 if k.startswith("w_") else 1, 3, q["row"],
+                                            q["srow"], q["colT"], r, q["scol"])
+        else:
+            self.fp8.fp8_mx_quantize(t, r, c, c, self.fmt[k], 3, q["row"], q["srow"], q["colT"], r, q["scol"])
 
     def gemm(self, a, al, b, bl, out):
         qa, qb = self.q[a], self.q[b]
@@ -647,14 +660,14 @@ def run_gpu(args, rank, world, local_rank):
     fp8_peak = 2.0 * bf16_sust               # FP8 dense = 2x bf16 dense (nominal 4.5 vs 2.25 PFLOP/s)
 
     if args.workload in ("gemm", "quantize", "grouped_m", "grouped_k", "quantize_grouped", "mx_gemm", "mx_quantize",
-                         "mx_permute", "mx_swiglu"):
+                         "mx_permute", "mx_swiglu", "bw_quantize"):
         run_single_kernel(args, dev, rank)
         return
     if args.workload == "sweep":
         run_sweep(args, dev, rank, hbm_gbs)
         return
     make = {"llama_mlp": llama_mlp_step, "flux": flux_step, "llama_rowwise": RowwiseStep, "moe": MoeStep,
-            "llama_mxfp8": MxStep}
+            "llama_mxfp8": MxStep, "llama_blockwise": lambda dev, seed: MxStep(dev, seed, recipe="blockwise")}
     step = make[args.workload](dev, 1 + rank)
     for _ in range(max(3, args.warmup)):
         step.run(world=world)
@@ -694,7 +707,7 @@ def run_gpu(args, rank, world, local_rank):
         if g_roof_ms <= g_tensor_ms * 1.0001:      # tensor-bound GEMMs
             roof = {"bound": "tensor", "achieved": round(gemm_tflops, 1), "peak": round(fp8_peak, 1),
                     "unit": "TFLOP/s", "frac": round(gemm_tflops / fp8_peak, 4),
-                    "kernel": GEMM_TRAFFIC[step.name]["kernel"] if step.name in GEMM_TRAFFIC else "fp8_gemm_kernel",
+                    "kernel": "mx_gemm_kernel" if isinstance(step, MxStep) else "fp8_gemm_pair_kernel",
                     "traffic": gemm_traffic(step.name),
                     "peak_source": f"{peak_src}: 2 x sustained bf16 {bf16_sust} TFLOP/s (fp8/bf16 nominal ratio 2)"}
         else:                                      # HBM-bound (grouped GEMMs at the MoE shape)
@@ -968,8 +981,8 @@ def run_single_kernel(args, dev, rank):
             step.quantize(k)
         fn = lambda: step.gemm(*MLP_GEMMS[0])  # noqa: E731
         work, unit = step.gemm_work["gate"][0] / 1e12, "TFLOP/s"
-    elif args.workload == "mx_quantize":
-        step = MxStep(dev, 1, keys=("dy_gate",), outs=())
+    elif args.workload in ("mx_quantize", "bw_quantize"):
+        step = MxStep(dev, 1, keys=("dy_gate",), outs=(), recipe="mxfp8" if args.workload == "mx_quantize" else "blockwise")
         fn = lambda: step.quantize("dy_gate")  # noqa: E731
         work, unit = mx_quantize_bytes(step.inp["dy_gate"].shape) / 1e9, "GB/s"
     elif args.workload == "gemm":
@@ -1048,7 +1061,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="llama_mlp",
-                    choices=["llama_mlp", "llama_rowwise", "llama_mxfp8", "moe", "flux", "sweep", "gemm", "quantize",
+                    choices=["llama_mlp", "llama_rowwise", "llama_mxfp8", "llama_blockwise", "moe", "flux", "sweep",
+                             "gemm", "quantize", "bw_quantize",
                              "grouped_m", "grouped_k", "quantize_grouped", "mx_gemm", "mx_quantize", "mx_permute",
                              "mx_swiglu"],
                     help="llama_mlp: the whole fwd+bwd FP8 step of the Llama-3-8B MLP (default); see the "

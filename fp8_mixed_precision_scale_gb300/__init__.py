@@ -40,7 +40,7 @@ LIB_PATH = os.path.join(_HERE, "libfp8gb.so")
 EXPORTED = ("fp8_quantize", "fp8_update_amax_history", "fp8_scaled_gemm", "fp8_grouped_gemm",
             "fp8_group_padded_offsets", "fp8_sync_status", "fp8_selftest_bounded_wait", "fp8_status_string",
             "fp8_last_cuda_error", "fp8_version", "fp8_mx_scale_bytes", "fp8_mx_quantize", "fp8_mx_gemm",
-            "fp8_mx_grouped_gemm", "fp8_mx_permute_quantize", "fp8_mx_swiglu_quantize")
+            "fp8_mx_grouped_gemm", "fp8_mx_permute_quantize", "fp8_mx_swiglu_quantize", "fp8_blockwise_quantize")
 MX_BLOCK = 32
 MX_GROUP_ALIGN = 128
 
@@ -123,6 +123,8 @@ def load_library():
             lib.fp8_mx_permute_quantize.argtypes = [P, i64, i64, i64, P, i64, i32, i32, P, P, P, i64, P, P, i32, P]
             lib.fp8_mx_swiglu_quantize.restype = i32
             lib.fp8_mx_swiglu_quantize.argtypes = [P, i64, i64, i64, i32, i32, P, i64, P, P, P, i64, P, P, i32, P]
+            lib.fp8_blockwise_quantize.restype = i32
+            lib.fp8_blockwise_quantize.argtypes = [P, i64, i64, i64, i32, i32, i32, P, P, P, i64, P, P]
             lib.fp8_mx_gemm.restype = i32
             lib.fp8_mx_gemm.argtypes = [P, i32, i64, P, P, i32, i64, P, i64, i64, i64, P, i64, P]
             lib.fp8_mx_grouped_gemm.restype = i32
@@ -232,6 +234,15 @@ def fp8_mx_swiglu_quantize(gate_up, rows, F, ld, fmt, layouts, h, ld_h, q_row, s
                                                num_groups, _stream(stream))
     if check:
         _check(rc, "fp8_mx_swiglu_quantize")
+    return rc
+
+
+def fp8_blockwise_quantize(x, rows, cols, ld_x, fmt, block_rows, layouts, q_row, s_row, q_colT, ld_colT, s_col,
+                           stream=None, check=True):
+    rc = load_library().fp8_blockwise_quantize(_p(x), rows, cols, ld_x, fmt, block_rows, layouts, _p(q_row),
+                                               _p(s_row), _p(q_colT), ld_colT, _p(s_col), _stream(stream))
+    if check:
+        _check(rc, "fp8_blockwise_quantize")
     return rc
 
 
@@ -431,3 +442,16 @@ def mx_grouped_gemm(mode: int, A, fa, sA, B, fb, sB, group_offsets, M_total, N, 
         out = torch.empty(shape, dtype=torch.bfloat16, device=A.device)
     fp8_mx_grouped_gemm(mode, A, fa, sA, B, fb, sB, group_offsets, G, M_total, N, K, out, ld_T, stream)
     return out
+
+
+def blockwise_quantize(x: torch.Tensor, fmt: int, block_rows: int, layouts: int = LAYOUT_ROW | LAYOUT_COLT,
+                       stream=None) -> MxQuantized:
+    """Blockwise quantize of a CUDA bf16 [rows, cols] tensor: block_rows 1 for
+    activations / gradients (1 x 128 blocks), 128 for weights (128 x 128).
+    The scales are in the MX scale layout, ready for mx_gemm."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    rows, cols = x.shape
+    q = _mx_outputs(rows, cols, x.device, layouts, None)
+    fp8_blockwise_quantize(x, rows, cols, x.stride(0), fmt, block_rows, layouts, q.q_row, q.s_row, q.q_colT,
+                           q.ld_colT, q.s_col, stream)
+    return q

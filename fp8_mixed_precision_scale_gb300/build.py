@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libfp8gb.so")
-SOURCES = ["api.cu", "quantize.cu", "update.cu", "gemm.cu", "mxquant.cu", "mxgemm.cu"]
+SOURCES = ["api.cu", "quantize.cu", "update.cu", "gemm.cu", "mxquant.cu", "mxgemm.cu", "blockwise.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
               "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

@@ -1,0 +1,235 @@
+// blockwise.cu -- blockwise FP8 quantize: 1 x 128 blocks along the
+// contraction for activations and gradients, 128 x 128 blocks for weights,
+// one power-of-two scale per block, row and transposed layouts from one read.
+//
+// Method: the "blockwise" recipe listed on "FP8 training for Flux models"
+// (Configuration > Key FP8 Parameters), which the page names without a
+// definition.  Each block takes the largest power-of-two scale s with
+// amax * s <= fp8_max (amax 0 or non-finite: s = 1), q = sat_rne(v * s); the
+// dequantisation factor 1/s is an exact E8M0 value, written into the MX
+// scale layout (each 128-block's code in its four 32-element slots), so the
+// block-scaled tensor-core GEMM (fp8_mx_gemm) applies it unchanged.
+//
+// Design (GB300): one 256-thread block per 128 x 128 tile.  Thread pairs own
+// a row (64 columns each: eight 16-byte loads issued before use); the row
+// block's maximum is shared by one shuffle, weights reduce the whole tile
+// through shared memory.  The tile is staged in shared memory as swizzled
+// column-pair words; for the transposed layout four adjacent lanes own a
+// column pair's four 32-row quarters, combine their maxima by shuffles and
+// write 32 contiguous bytes per column.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "fp8gb.h"
+#include "fp8gb_device.cuh"
+#include "fp8gb_host.h"
+
+namespace fp8gb {
+
+constexpr int BW_THREADS = 256;
+constexpr int BW_TILE = 128;
+constexpr int BW_PITCH_W = BW_TILE / 2 + 4;  // 32-bit words (column pairs) per shared row, padded
+
+struct BwArgs {
+    const uint16_t *x;
+    int64_t rows, cols, ld_x;
+    uint8_t *q_row, *s_row, *q_colT, *s_col;
+    int64_t ld_colT;
+    int64_t rs_row;  // scale rows of s_row (rows rounded up to 4)
+    int64_t n_col_tiles;
+    int do_row, do_col;
+};
+
+// E8M0 code of 1/s for a block whose largest magnitude has fp32 bits
+// amax_bits: s = 2^e with e the largest integer such that amax * 2^e <=
+// fp8_max = 1.75 * 2^EF.  For a normal amax = m * 2^E (1 <= m < 2) that is
+// e = EF - E, one less when m > 1.75; subnormal maxima clamp to e = 127.
+template <int FMT>
+__device__ __forceinline__ uint32_t bw_code(uint32_t amax_bits)
+{
+    constexpr int EF = FMT == FP8_E5M2 ? 15 : 8;
+    if (amax_bits >= 0x7F800000u || amax_bits == 0u) return 127u;  // non-finite or zero block: s = 1
+    if (amax_bits < 0x00800000u) return 0u;                        // subnormal maximum: e clamps to 127
+    int e = EF - ((int)(amax_bits >> 23) - 127) - ((amax_bits & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+    e = e < -127 ? -127 : (e > 127 ? 127 : e);
+    return (uint32_t)(127 - e);
+}
+
+__device__ __forceinline__ float bw_scale(uint32_t code)  // s = 2^(127 - code), code <= 254
+{
+    return __uint_as_float((254u - code) << 23);
+}
+
+// shared tile word of (row, column pair): XOR-swizzled by the row's 32-row
+// quarter so the four quarters read in one warp hit different banks
+__device__ __forceinline__ int bw_word(int row, int pair) { return row * BW_PITCH_W + (pair ^ (((row >> 5) & 3) << 3)); }
+
+template <int FMT, bool WEIGHT>
+__global__ void __launch_bounds__(BW_THREADS)
+    bw_quantize_kernel(BwArgs a)
+{
+    __shared__ __align__(16) uint32_t tile[BW_TILE * BW_PITCH_W];
+    __shared__ uint32_t warp_max[BW_THREADS / 32];
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t rt = blockIdx.x / a.n_col_tiles, ct = blockIdx.x % a.n_col_tiles;
+    const int64_t r0 = rt * BW_TILE, c0 = ct * BW_TILE;
+
+    // ---- load: thread pair (r, half) owns 64 columns of row r ----
+    const int r = tid >> 1, half = tid & 1;
+    const bool row_real = r0 + r < a.rows;
+    uint4 v[8];
+    if (row_real) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(a.x + (r0 + r) * a.ld_x + c0 + 64 * half);
+#pragma unroll
+        for (int j = 0; j < 8; j++) v[j] = __ldg(src + j);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 8; j++) v[j] = make_uint4(0, 0, 0, 0);
+    }
+    uint32_t am = 0;
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+        am = absmax_bf16x2(am, v[j].x);
+        am = absmax_bf16x2(am, v[j].y);
+        am = absmax_bf16x2(am, v[j].z);
+        am = absmax_bf16x2(am, v[j].w);
+    }
+    uint32_t row_bits = fold_absmax(am);
+    row_bits = max(row_bits, __shfl_xor_sync(0xffffffffu, row_bits, 1));  // the row's two halves
+
+    uint32_t block_code = 0;
+    if constexpr (WEIGHT) {
+        uint32_t m = row_bits;
+#pragma unroll
+        for (int d = 2; d < 32; d <<= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, d));
+        if (lane == 0) warp_max[warp] = m;
+    }
+    if (a.do_col || WEIGHT) {
+#pragma unroll
+        for (int j = 0; j < 8; j++)
+            *reinterpret_cast<uint4 *>(&tile[bw_word(r, 32 * half + 4 * j)]) = v[j];
+    }
+    if (a.do_col || WEIGHT) __syncthreads();
+    if constexpr (WEIGHT) {
+        uint32_t m = warp_max[0];
+#pragma unroll
+        for (int w = 1; w < BW_THREADS / 32; w++) m = max(m, warp_max[w]);
+        block_code = bw_code<FMT>(m);
+    }
+
+    // ---- row layout ----
+    if (a.do_row) {
+        const uint32_t code = WEIGHT ? block_code : bw_code<FMT>(row_bits);
+        if (row_real) {
+            const float s = bw_scale(code);
+            uint32_t out[16];
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+                out[2 * j] = cvt2<FMT>(bf16lo(w[0]) * s, bf16hi(w[0]) * s) |
+                             (cvt2<FMT>(bf16lo(w[1]) * s, bf16hi(w[1]) * s) << 16);
+                out[2 * j + 1] = cvt2<FMT>(bf16lo(w[2]) * s, bf16hi(w[2]) * s) |
+                                 (cvt2<FMT>(bf16lo(w[3]) * s, bf16hi(w[3]) * s) << 16);
+            }
+            uint4 *dst = reinterpret_cast<uint4 *>(a.q_row + (r0 + r) * a.cols + c0 + 64 * half);
+#pragma unroll
+            for (int j = 0; j < 4; j++) dst[j] = make_uint4(out[4 * j], out[4 * j + 1], out[4 * j + 2], out[4 * j + 3]);
+        }
+        // one scale word per row and 128-column tile: the code in all four slots
+        if (half == 0 && r0 + r < a.rs_row)
+            *reinterpret_cast<uint32_t *>(a.s_row + (ct * a.rs_row + r0 + r) * 4) =
+                row_real ? code * 0x01010101u : 0u;
+    }
+
+    // ---- transposed layout ----
+    if (a.do_col) {
+        // lanes 4p .. 4p+3 of the block own column pair p's four 32-row quarters
+        const int p = tid >> 2, qq = tid & 3;
+        uint32_t w[32];
+        uint32_t cm = 0;
+#pragma unroll
+        for (int i = 0; i < 32; i++) {
+            w[i] = tile[bw_word(32 * qq + i, p)];
+            cm = absmax_bf16x2(cm, w[i]);
+        }
+        cm = __vmaxu2(cm, __shfl_xor_sync(0xffffffffu, cm, 1));
+        cm = __vmaxu2(cm, __shfl_xor_sync(0xffffffffu, cm, 2));
+        const uint32_t code0 = WEIGHT ? block_code : bw_code<FMT>(cm << 16);
+        const uint32_t code1 = WEIGHT ? block_code : bw_code<FMT>(cm & 0xFFFF0000u);
+        const float s0 = bw_scale(code0), s1 = bw_scale(code1);
+        uint32_t o0[8], o1[8];
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            const uint32_t x0 = w[4 * i], x1 = w[4 * i + 1], x2 = w[4 * i + 2], x3 = w[4 * i + 3];
+            o0[i] = cvt2<FMT>(bf16lo(x0) * s0, bf16lo(x1) * s0) | (cvt2<FMT>(bf16lo(x2) * s0, bf16lo(x3) * s0) << 16);
+            o1[i] = cvt2<FMT>(bf16hi(x0) * s1, bf16hi(x1) * s1) | (cvt2<FMT>(bf16hi(x2) * s1, bf16hi(x3) * s1) << 16);
+        }
+        const int64_t c = c0 + 2 * p;
+        uint4 *d0 = reinterpret_cast<uint4 *>(a.q_colT + c * a.ld_colT + r0 + 32 * qq);
+        uint4 *d1 = reinterpret_cast<uint4 *>(a.q_colT + (c + 1) * a.ld_colT + r0 + 32 * qq);
+        d0[0] = make_uint4(o0[0], o0[1], o0[2], o0[3]);
+        d0[1] = make_uint4(o0[4], o0[5], o0[6], o0[7]);
+        d1[0] = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+        d1[1] = make_uint4(o1[4], o1[5], o1[6], o1[7]);
+        if (qq == 0) {
+            uint32_t *sc = reinterpret_cast<uint32_t *>(a.s_col + (rt * a.cols + c) * 4);
+            sc[0] = code0 * 0x01010101u;
+            sc[1] = code1 * 0x01010101u;
+        }
+    }
+}
+
+template <int FMT, bool WEIGHT>
+static fp8_status_t launch_bw(const BwArgs &a, int64_t n_tiles, cudaStream_t st)
+{
+    bw_quantize_kernel<FMT, WEIGHT><<<(unsigned)n_tiles, BW_THREADS, 0, st>>>(a);
+    return check_launch();
+}
+
+}  // namespace fp8gb
+
+using namespace fp8gb;
+
+extern "C" fp8_status_t fp8_blockwise_quantize(const void *x_bf16, int64_t rows, int64_t cols, int64_t ld_x, int fmt,
+                                               int block_rows, int layouts, uint8_t *q_row, uint8_t *s_row,
+                                               uint8_t *q_colT, int64_t ld_colT, uint8_t *s_col, void *stream)
+{
+    if (rows < 0 || cols < 1 || ld_x < cols) return FP8_ERR_INVALID_ARG;
+    if (fmt == FP8_E4M3FNUZ || fmt == FP8_E5M2FNUZ) return FP8_ERR_UNSUPPORTED;
+    if (fmt != FP8_E4M3FN && fmt != FP8_E5M2) return FP8_ERR_INVALID_ARG;
+    if (block_rows != 1 && block_rows != BW_TILE) return FP8_ERR_INVALID_ARG;
+    if (layouts < 1 || layouts > 3) return FP8_ERR_INVALID_ARG;
+    if (rows == 0) return FP8_OK;
+    const bool do_row = layouts & FP8_LAYOUT_ROW, do_col = layouts & FP8_LAYOUT_COLT;
+    if (!x_bf16 || (do_row && (!q_row || !s_row)) || (do_col && (!q_colT || !s_col))) return FP8_ERR_INVALID_ARG;
+    if (rows > INT32_MAX || cols > INT32_MAX) return FP8_ERR_INVALID_ARG;
+    if (cols % BW_TILE != 0 || ld_x % 8 != 0 || !aligned(x_bf16, 16)) return FP8_ERR_ALIGNMENT;
+    if ((do_col || block_rows == BW_TILE) && rows % BW_TILE != 0) return FP8_ERR_ALIGNMENT;
+    if (do_row && (!aligned(q_row, 16) || !aligned(s_row, 4))) return FP8_ERR_ALIGNMENT;
+    if (do_col) {
+        if (ld_colT % 16 != 0 || !aligned(q_colT, 16) || !aligned(s_col, 8)) return FP8_ERR_ALIGNMENT;
+        if (ld_colT < rows) return FP8_ERR_INVALID_ARG;
+    }
+    BwArgs a{};
+    a.x = static_cast<const uint16_t *>(x_bf16);
+    a.rows = rows;
+    a.cols = cols;
+    a.ld_x = ld_x;
+    a.q_row = q_row;
+    a.s_row = s_row;
+    a.q_colT = q_colT;
+    a.s_col = s_col;
+    a.ld_colT = ld_colT;
+    a.rs_row = (rows + 3) / 4 * 4;
+    a.n_col_tiles = cols / BW_TILE;
+    a.do_row = do_row;
+    a.do_col = do_col;
+    const int64_t n_tiles = (a.rs_row + BW_TILE - 1) / BW_TILE * a.n_col_tiles;
+    if (n_tiles > INT32_MAX) return FP8_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const bool w = block_rows == BW_TILE;
+    if (fmt == FP8_E5M2) return w ? launch_bw<FP8_E5M2, true>(a, n_tiles, st) : launch_bw<FP8_E5M2, false>(a, n_tiles, st);
+    return w ? launch_bw<FP8_E4M3FN, true>(a, n_tiles, st) : launch_bw<FP8_E4M3FN, false>(a, n_tiles, st);
+}

@@ -293,6 +293,30 @@ FP8GB_API fp8_status_t fp8_mx_quantize(const void *x_bf16, int64_t rows, int64_t
                                        int num_groups, void *stream);
 
 /*
+ * fp8_blockwise_quantize -- the "blockwise" recipe ("FP8 training for Flux
+ * models", Key FP8 Parameters; named there without a definition).  Blocks of
+ * 128 elements along the contraction: block_rows = 1 gives 1 x 128 blocks
+ * (activations, gradients; the transposed layout's blocks are 128 rows of one
+ * column), block_rows = 128 gives 128 x 128 blocks (weights; one scale per
+ * block serves both layouts).  Each block takes the largest power-of-two
+ * scale s with amax * s <= fp8_max (amax 0 or non-finite: s = 1), q =
+ * sat_rne(v * s) -- no finite element saturates -- and 1/s is stored as its
+ * E8M0 code in the MX scale layout (the code in all four 32-element slots of
+ * the block), so fp8_mx_gemm multiplies blockwise operands directly.
+ *
+ *   x_bf16   [rows][ld_x] bf16, 16-byte aligned, ld_x % 8 == 0; cols % 128 == 0;
+ *            rows % 128 == 0 for the transposed layout or 128 x 128 blocks.
+ *   fmt      FP8_E4M3FN or FP8_E5M2.
+ *   q_row, s_row    [rows][cols] u8 and its scales (R = rows, KB = cols / 32).
+ *   q_colT, s_col   [cols][ld_colT] u8 (ld_colT >= rows, % 16 == 0) and its
+ *                   scales (R = cols, KB = rows / 32); s_col 8-byte aligned.
+ * Errors as fp8_mx_quantize; nothing is allocated.
+ */
+FP8GB_API fp8_status_t fp8_blockwise_quantize(const void *x_bf16, int64_t rows, int64_t cols, int64_t ld_x, int fmt,
+                                              int block_rows, int layouts, uint8_t *q_row, uint8_t *s_row,
+                                              uint8_t *q_colT, int64_t ld_colT, uint8_t *s_col, void *stream);
+
+/*
  * Fused MoE prologues ("FP8 Training on AMD GPUs with TorchTitan and TorchAO":
  * a five-kernel eager chain in front of the MoE grouped GEMMs replaced by one
  * fused kernel).  Each reads its bf16 input once and writes exactly what

@@ -275,3 +275,17 @@ def test_mx_fused_validation(lib):
     assert swi(F=48, ld=96) == ALIGN
     assert swi(h=FAKE, ld_h=32) == INVALID
     assert swi(h=FAKE + 8, ld_h=64) == ALIGN
+
+
+def test_blockwise_validation(lib):
+    P = ctypes.c_void_p
+    bw = lambda **kw: lib.fp8_blockwise_quantize(  # noqa: E731
+        P(kw.get("x", FAKE)), kw.get("rows", 128), kw.get("cols", 128), kw.get("ld", 128), kw.get("fmt", 0),
+        kw.get("br", 1), kw.get("lay", 3), P(FAKE), P(FAKE), P(FAKE), kw.get("ldT", 128), P(FAKE), None)
+    assert bw(br=64) == INVALID
+    assert bw(fmt=2) == UNSUPPORTED
+    assert bw(cols=96, ld=128) == ALIGN                     # whole 128-column blocks
+    assert bw(rows=96, ldT=128) == ALIGN                    # transposed layout: whole 128-row blocks
+    assert bw(rows=96, lay=1, br=128) == ALIGN              # weights: 128 x 128 blocks
+    assert bw(ldT=136) == ALIGN                            # not a multiple of 16
+    assert bw(rows=256, ldT=128) == INVALID                 # ld_colT shorter than rows
