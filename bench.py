@@ -24,6 +24,7 @@ Other workloads (same JSON line, their own config):
   llama_blockwise  the same step under the blockwise recipe (1x128 activation
                  and gradient blocks, 128x128 weight blocks, power-of-two scales)
   bw_quantize    the blockwise quantize of dY_gate (1x128 blocks)
+  rowwise_quantize  the rowwise (current scaling) quantize of dY_gate
   sweep          the delayed quantize (E4M3, both layouts) of 2^20 .. 2^30
                  elements, GB/s against size
   gemm, quantize single kernels of the default step, for profiling
@@ -326,7 +327,7 @@ class RowwiseStep:
     FWD_Q = ["x", "w_qkv", "o_in", "w_o", "x2", "w_gate", "w_up", "w_down", "h"]
     BWD_Q = ["dy_down", "dy_gate", "dy_up", "dy_o", "dy_qkv"]
 
-    def __init__(self, dev, seed):
+    def __init__(self, dev, seed, keys=None):
         import fp8_mixed_precision_scale_gb300 as fp8
         import synth
         self.fp8 = fp8
@@ -339,6 +340,8 @@ class RowwiseStep:
         g.manual_seed(seed)
         self.inp, self.fmt = {}, {}
         for k, (shape, dist, f) in self.SHAPES.items():
+            if keys is not None and k not in keys:
+                continue
             self.inp[k] = synth.student_t(shape, 4, g, dev) if dist == "t" else _normal(g, dev, shape, dist)
             self.fmt[k] = f
         self.q = {}
@@ -351,6 +354,8 @@ class RowwiseStep:
         self.out, self.gemm_work = {}, {}
         self.flops = 0.0
         for (a, al, b, bl, o) in self.GEMMS:
+            if a not in self.inp or b not in self.inp:
+                continue
             M, K = self.inp[a].shape if al == "row" else self.inp[a].shape[::-1]
             N = self.inp[b].shape[0] if bl == "row" else self.inp[b].shape[1]
             self.out[o] = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
@@ -359,7 +364,7 @@ class RowwiseStep:
         self.recipe = fp8.Recipe(kind=fp8.ROWWISE)
         self.q_bytes = sum(quantize_bytes(t.shape) for t in self.inp.values())
         self.launches_per_step = 3 * len(self.inp) + len(self.GEMMS)   # amax, cast, finalise per tensor
-        self.d2h = [self.out["y"]]
+        self.d2h = [self.out["y"]] if "y" in self.out else []
 
     def quantize(self, k):
         t, q = self.inp[k], self.q[k]
@@ -660,7 +665,7 @@ def run_gpu(args, rank, world, local_rank):
     fp8_peak = 2.0 * bf16_sust               # FP8 dense = 2x bf16 dense (nominal 4.5 vs 2.25 PFLOP/s)
 
     if args.workload in ("gemm", "quantize", "grouped_m", "grouped_k", "quantize_grouped", "mx_gemm", "mx_quantize",
-                         "mx_permute", "mx_swiglu", "bw_quantize"):
+                         "mx_permute", "mx_swiglu", "bw_quantize", "rowwise_quantize"):
         run_single_kernel(args, dev, rank)
         return
     if args.workload == "sweep":
@@ -981,6 +986,10 @@ def run_single_kernel(args, dev, rank):
             step.quantize(k)
         fn = lambda: step.gemm(*MLP_GEMMS[0])  # noqa: E731
         work, unit = step.gemm_work["gate"][0] / 1e12, "TFLOP/s"
+    elif args.workload == "rowwise_quantize":
+        step = RowwiseStep(dev, 1, keys=("dy_gate",))
+        fn = lambda: step.quantize("dy_gate")  # noqa: E731
+        work, unit = quantize_bytes(step.inp["dy_gate"].shape) / 1e9, "GB/s (algorithmic)"
     elif args.workload in ("mx_quantize", "bw_quantize"):
         step = MxStep(dev, 1, keys=("dy_gate",), outs=(), recipe="mxfp8" if args.workload == "mx_quantize" else "blockwise")
         fn = lambda: step.quantize("dy_gate")  # noqa: E731
@@ -1062,7 +1071,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="llama_mlp",
                     choices=["llama_mlp", "llama_rowwise", "llama_mxfp8", "llama_blockwise", "moe", "flux", "sweep",
-                             "gemm", "quantize", "bw_quantize",
+                             "gemm", "quantize", "bw_quantize", "rowwise_quantize",
                              "grouped_m", "grouped_k", "quantize_grouped", "mx_gemm", "mx_quantize", "mx_permute",
                              "mx_swiglu"],
                     help="llama_mlp: the whole fwd+bwd FP8 step of the Llama-3-8B MLP (default); see the "

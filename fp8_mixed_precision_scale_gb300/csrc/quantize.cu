@@ -266,6 +266,119 @@ __global__ void __launch_bounds__(QT_THREADS) amax_kernel(QArgs a)
 }
 
 // ---------------------------------------------------------------------------
+// Pass 1 of the ROWWISE recipe on a plain (ungrouped) tensor: row amax and
+// column amax in one read.
+//
+// Persistent blocks, each owning a contiguous run of tiles in row-major tile
+// order, so consecutive tiles mostly belong to the same row block: the row
+// maxima stay in registers across the run and are flushed (one relaxed
+// atomic per row) only when the row block changes or the run ends.  The next
+// tile's 16-byte loads are issued before the current tile is reduced, so
+// every thread keeps loads in flight while it reduces.  Column maxima are
+// reduced per tile (shuffles, then shared memory across the 8 warps) and
+// flushed with one relaxed atomic per column per tile.
+// ---------------------------------------------------------------------------
+template <int RB>
+__device__ __forceinline__ void dense_tile_load(const QArgs &a, int64_t tile, int cg, int roff, uint4 (&v)[RB / 16])
+{
+    const int64_t b = tile / a.n_col_chunks;
+    const int64_t col = (tile % a.n_col_chunks) * QT_COLS + cg * 8;
+    const int64_t row0 = b * RB;
+#pragma unroll
+    for (int i = 0; i < RB / 16; i++) {
+        const int64_t r = row0 + i * 16 + roff;
+        if (col < a.cols && r < a.rows)
+            v[i] = __ldg(reinterpret_cast<const uint4 *>(a.x + r * a.ld_x + col));
+        else
+            v[i] = make_uint4(0, 0, 0, 0);
+    }
+}
+
+template <int RB>
+__global__ void __launch_bounds__(QT_THREADS) dense_rowcol_amax_kernel(QArgs a, int64_t tiles_per_block)
+{
+    __shared__ uint32_t red[QT_THREADS / 32];
+    __shared__ uint32_t colw[QT_THREADS / 32][16][4];  // per warp: 16 column groups x 4 packed words
+    const int t = threadIdx.x, cg = t & 15, roff = t >> 4;
+    const int64_t n_tiles = a.n_row_blocks * a.n_col_chunks;
+    const int64_t first = (int64_t)blockIdx.x * tiles_per_block;
+    const int64_t last = first + tiles_per_block < n_tiles ? first + tiles_per_block : n_tiles;
+    uint32_t tensor_acc = 0;
+    uint32_t racc[RB / 16];
+#pragma unroll
+    for (int i = 0; i < RB / 16; i++) racc[i] = 0;
+    int64_t cur_b = first < last ? first / a.n_col_chunks : -1;
+
+    // row maxima of row block b: 16 threads share a row; one atomic per row
+    auto flush_rows = [&](int64_t b) {
+#pragma unroll
+        for (int i = 0; i < RB / 16; i++) {
+            uint32_t rm = racc[i];
+            for (int d = 8; d > 0; d >>= 1) rm = max(rm, __shfl_xor_sync(0xffffffffu, rm, d));
+            const int64_t r = b * RB + i * 16 + roff;
+            if (cg == 0 && r < a.rows && a.sinv_row)
+                atomicMax(reinterpret_cast<unsigned int *>(a.sinv_row) + r, rm);
+            racc[i] = 0;
+        }
+    };
+
+    uint4 nv[RB / 16];
+    if (first < last) dense_tile_load<RB>(a, first, cg, roff, nv);
+    for (int64_t tile = first; tile < last; tile++) {
+        uint4 v[RB / 16];
+#pragma unroll
+        for (int i = 0; i < RB / 16; i++) v[i] = nv[i];
+        if (tile + 1 < last) dense_tile_load<RB>(a, tile + 1, cg, roff, nv);
+        const int64_t b = tile / a.n_col_chunks;
+        const int64_t c0 = (tile % a.n_col_chunks) * QT_COLS;
+        if (b != cur_b) {  // warp-uniform: the whole block moves to the next row block
+            flush_rows(cur_b);
+            cur_b = b;
+        }
+        uint32_t cacc[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int i = 0; i < RB / 16; i++) {
+            uint32_t rr = 0;
+            rr = absmax_bf16x2(rr, v[i].x);
+            rr = absmax_bf16x2(rr, v[i].y);
+            rr = absmax_bf16x2(rr, v[i].z);
+            rr = absmax_bf16x2(rr, v[i].w);
+            cacc[0] = absmax_bf16x2(cacc[0], v[i].x);
+            cacc[1] = absmax_bf16x2(cacc[1], v[i].y);
+            cacc[2] = absmax_bf16x2(cacc[2], v[i].z);
+            cacc[3] = absmax_bf16x2(cacc[3], v[i].w);
+            const uint32_t f = fold_absmax(rr);
+            racc[i] = max(racc[i], f);
+            tensor_acc = max(tensor_acc, f);
+        }
+        if (a.sinv_col) {
+            // column maxima over the tile's rows: lanes t and t^16 share columns
+#pragma unroll
+            for (int k = 0; k < 4; k++) cacc[k] = __vmaxu2(cacc[k], __shfl_xor_sync(0xffffffffu, cacc[k], 16));
+            const int w = t >> 5;
+            if ((t & 31) < 16) {
+#pragma unroll
+                for (int k = 0; k < 4; k++) colw[w][cg][k] = cacc[k];
+            }
+            __syncthreads();
+            if (t < QT_COLS) {
+                const int g = t >> 3, j = t & 7;  // column c0 + 8g + j
+                uint32_t m = 0;
+                for (int ww = 0; ww < QT_THREADS / 32; ww++) {
+                    const uint32_t word = colw[ww][g][j >> 1];
+                    m = max(m, (j & 1) ? (word >> 16) : (word & 0xFFFFu));
+                }
+                const int64_t c = c0 + t;
+                if (c < a.cols) atomicMax(reinterpret_cast<unsigned int *>(a.sinv_col) + c, m << 16);
+            }
+            __syncthreads();
+        }
+    }
+    if (cur_b >= 0) flush_rows(cur_b);
+    if (a.amax_out) block_amax_atomic(tensor_acc, a.amax_out, red);
+}
+
+// ---------------------------------------------------------------------------
 // Pass 1 of the ROWWISE recipe: row amax and (group, column) amax.
 //
 // A thread block covers a super tile of up to 8 row blocks of 32 rows x up
@@ -651,8 +764,9 @@ static fp8_status_t run_quantize(QArgs a, int kind, int layouts, cudaStream_t st
     if (n_col && cudaMemsetAsync(a.sinv_col, 0, sizeof(float) * n_col, st) != cudaSuccess) return cuda_fail();
     if (a.amax_out && cudaMemsetAsync(a.amax_out, 0, sizeof(float), st) != cudaSuccess) return cuda_fail();
     if (!a.offsets) {
-        auto k = amax_kernel<RB, 1>;
-        k<<<blocks_for(k, group_smem, n_tiles, false), QT_THREADS, group_smem, st>>>(a);
+        auto k = dense_rowcol_amax_kernel<RB>;
+        const int64_t grid = blocks_for(k, 0, n_tiles, true);
+        k<<<(unsigned)grid, QT_THREADS, 0, st>>>(a, (n_tiles + grid - 1) / grid);
         if ((s = check_launch()) != FP8_OK) return s;
     } else {
         // pass 1 works on 32-row blocks for both layouts of the row space
