@@ -485,6 +485,254 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 }
 
 // ---------------------------------------------------------------------------
+// K-grouped GEMM (MoE wgrad) with a TMA-store epilogue.
+//
+// Each output tile of dW_e is written once and its contraction is short (one
+// expert's tokens), so the kernel is bound by writing C.  Here each epilogue
+// warp converts its 32 x 128 block to bf16 into two 32-row x 64-column boxes
+// in shared memory (128-byte swizzle: conflict-free 16-byte writes) and
+// issues their TMA stores itself; the copy drains asynchronously while the
+// warp reads the next accumulator, and the warp only waits for its previous
+// stores to finish reading shared memory before refilling its boxes.  A
+// 3-stage operand ring leaves room for the 64 KB of boxes.  Used when N is a
+// multiple of 32 (a 32-row quarter never straddles two experts' blocks), K
+// a multiple of 8 and C 16-byte aligned.
+// ---------------------------------------------------------------------------
+constexpr int KT_STAGES = 3;
+constexpr int KT_BOX_BYTES = 32 * 128;  // 32 rows x 64 bf16
+
+struct SmemLayoutKT {
+    static constexpr int a_off = 0;
+    static constexpr int b_off = KT_STAGES * A_STAGE_BYTES;
+    static constexpr int box_off = b_off + KT_STAGES * B_STAGE_BYTES;      // 1024-aligned
+    static constexpr int bar_off = box_off + 8 * 2 * KT_BOX_BYTES;
+    static constexpr int n_bars = 2 * KT_STAGES + 2 + 2 + 1;
+    static constexpr int slot_off = bar_off + n_bars * 8;
+    static constexpr int misc_off = (slot_off + 16 + 127) / 128 * 128;    // group tables
+};
+
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
+    fp8_gemm_kgroup_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                               const __grid_constant__ CUtensorMap tmC, GemmParams p, uint32_t idesc)
+{
+    constexpr int MODE = MODE_KGROUP;
+    using L = SmemLayoutKT;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sA = smem + L::a_off;
+    uint8_t *sB = smem + L::b_off;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::bar_off);
+    uint64_t *full = bars;
+    uint64_t *empty = bars + KT_STAGES;
+    uint64_t *tfull = bars + 2 * KT_STAGES;
+    uint64_t *tempty = tfull + 2;
+    uint64_t *done = tempty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::slot_off);
+    int32_t *tile_prefix = reinterpret_cast<int32_t *>(smem + L::misc_off);
+    int32_t *poff = tile_prefix + (p.G + 1);
+    __shared__ int64_t s_total;
+    __shared__ int s_ok;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < KT_STAGES; s++) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; b++) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 8);
+        }
+        mbar_init(done, 1);
+        fence_barrier_init();
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB);
+        prefetch_tensormap(&tmC);
+    }
+    if (warp == 2) {
+        int64_t tt = 0;
+        const bool ok = build_group_tables(p, MODE, tile_prefix, poff, &tt);
+        if (lane == 0) {
+            s_total = tt;
+            s_ok = ok;
+            if (!ok) record_error(p.err, ERR_BAD_OFFSETS);
+        }
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int64_t total = s_ok ? s_total : 0;
+
+    if (warp == 0 && lane == 0) {
+        // ---------------- TMA producer ----------------
+        int stage = 0;
+        uint32_t phase = 0;
+        int issued_parity[KT_STAGES];
+        for (int s = 0; s < KT_STAGES; s++) issued_parity[s] = -1;
+        bool ok = true;
+        for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            const TileInfo ti = tile_info<MODE>(p, t, tile_prefix, poff);
+            for (int kb = 0; kb < ti.nkb; kb++) {
+                if (!mbar_wait_bounded(&empty[stage], phase ^ 1, WAIT_LIMIT_NS, p.err, ERR_PRODUCER_WAIT)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&full[stage], A_STAGE_BYTES + B_STAGE_BYTES);
+                tma_load_2d(sA + stage * A_STAGE_BYTES, &tmA, ti.a_x0 + kb * BK, ti.a_y, &full[stage]);
+                tma_load_2d(sB + stage * B_STAGE_BYTES, &tmB, ti.b_x0 + kb * BK, ti.b_y, &full[stage]);
+                issued_parity[stage] = (int)phase;
+                if (++stage == KT_STAGES) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+        }
+        for (int s = 0; s < KT_STAGES; s++)
+            if (issued_parity[s] >= 0)
+                mbar_wait_bounded(&full[s], (uint32_t)issued_parity[s], WAIT_LIMIT_NS, p.err, ERR_TEARDOWN_WAIT);
+    } else if (warp == 1 && lane == 0) {
+        // ---------------- MMA issuer ----------------
+        int stage = 0;
+        uint32_t phase = 0;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool ok = true;
+        for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            const TileInfo ti = tile_info<MODE>(p, t, tile_prefix, poff);
+            if (ti.nkb == 0) continue;
+            if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1, WAIT_LIMIT_NS, p.err, ERR_MMA_WAIT)) break;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+            for (int kb = 0; kb < ti.nkb; kb++) {
+                if (!mbar_wait_bounded(&full[stage], phase, WAIT_LIMIT_NS, p.err, ERR_MMA_WAIT)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a_addr = smem_u32(sA + stage * A_STAGE_BYTES);
+                const uint32_t b_addr = smem_u32(sB + stage * B_STAGE_BYTES);
+                const int steps = kb == ti.nkb - 1 ? ti.last_steps : BK / UMMA_K;
+                for (int k = 0; k < steps; k++)
+                    mma_f8f6f4(d_tmem, smem_desc_k128_sw128(a_addr + k * UMMA_K),
+                               smem_desc_k128_sw128(b_addr + k * UMMA_K), idesc, (kb | k) != 0);
+                mma_commit(&empty[stage]);
+                if (++stage == KT_STAGES) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+            if (!ok) break;
+            mma_commit(&tfull[acc]);
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1;
+            }
+        }
+        mma_commit(done);
+        mbar_wait_bounded(done, 0, WAIT_LIMIT_NS, p.err, ERR_TEARDOWN_WAIT);
+    } else if (warp >= 2) {
+        // ---------------- epilogue: TMEM -> bf16 boxes -> TMA stores ----------------
+        const int q = warp & 3;
+        const int half = (warp - 2) >> 2;
+        uint8_t *box = smem + L::box_off + (warp - 2) * 2 * KT_BOX_BYTES;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
+            const TileInfo ti = tile_info<MODE>(p, t, tile_prefix, poff);
+            const int64_t qrow0 = ti.row0 + q * 32;  // this warp's first row of C[e]
+            const bool live = qrow0 < ti.row_end;    // N % 32 == 0: the quarter is all in or all out
+            const int64_t cbeg = ti.col0 + half * (BN / 2);
+            if (ti.nkb == 0) {
+                // empty group: its block of C is zero
+                const int64_t cend = min(cbeg + BN / 2, ti.col_end);
+                if (live) {
+                    uint16_t *crow = p.C + ti.c_base + (qrow0 + lane) * p.ldc;
+                    for (int64_t c = cbeg; c < cend; c += 8) *reinterpret_cast<uint4 *>(crow + c) = make_uint4(0, 0, 0, 0);
+                }
+                continue;
+            }
+            if (!mbar_wait_bounded(&tfull[acc], acc_phase, WAIT_LIMIT_NS, p.err, ERR_EPILOGUE_WAIT)) break;
+            tc_fence_after();
+            const float sa_v = live ? (p.sa_per_row ? __ldg(p.sa + ti.sa_base + qrow0 + lane) : __ldg(p.sa)) : 0.0f;
+            const float sb0 = p.sb_per_row ? 0.0f : __ldg(p.sb);
+            // the previous tile's stores must have read the boxes before they are refilled
+            if (lane == 0) bulk_wait_group_read0();
+            __syncwarp();
+#pragma unroll
+            for (int ch = 0; ch < 4; ch += 2) {
+                uint32_t r[2][32];
+                const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN) +
+                                       (uint32_t)(half * (BN / 2) + ch * 32);
+                tmem_ld_32x32b_x32(taddr, r[0]);
+                tmem_ld_32x32b_x32(taddr + 32, r[1]);
+                float sbl[2] = {sb0, sb0};
+                if (p.sb_per_row) {
+#pragma unroll
+                    for (int u = 0; u < 2; u++) {
+                        const int64_t cc = cbeg + (ch + u) * 32 + lane;
+                        sbl[u] = cc < ti.col_end ? __ldg(p.sb + ti.sb_base + cc) : 0.0f;
+                    }
+                }
+                tmem_ld_wait();
+#pragma unroll
+                for (int u = 0; u < 2; u++) {
+                    const int cu = ch + u;  // 32-column chunk 0..3 of this warp's 128 columns
+                    uint32_t packed[16];
+#pragma unroll
+                    for (int j = 0; j < 16; j++) {
+                        const float lo = __uint_as_float(r[u][2 * j]) * sa_v * __shfl_sync(0xffffffffu, sbl[u], 2 * j);
+                        const float hi =
+                            __uint_as_float(r[u][2 * j + 1]) * sa_v * __shfl_sync(0xffffffffu, sbl[u], 2 * j + 1);
+                        packed[j] = pack_bf16x2(lo, hi);
+                    }
+                    // box cu / 2, 16-byte chunks 4 (cu % 2) .. +3 of this lane's 128-byte row,
+                    // 128-byte swizzle: chunk index XOR (row % 8)
+                    uint8_t *brow = box + (cu >> 1) * KT_BOX_BYTES + lane * 128;
+#pragma unroll
+                    for (int g = 0; g < 4; g++) {
+                        const int chunk = ((cu & 1) * 4 + g) ^ (lane & 7);
+                        *reinterpret_cast<uint4 *>(brow + chunk * 16) =
+                            make_uint4(packed[4 * g], packed[4 * g + 1], packed[4 * g + 2], packed[4 * g + 3]);
+                    }
+                }
+            }
+            // accumulator read: release it to the MMA warp
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[acc]);
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0 && live) {
+                const int32_t y = (int32_t)(ti.c_base / p.ldc + qrow0);  // row of the [G*N][K] view
+#pragma unroll
+                for (int b = 0; b < 2; b++) {
+                    const int64_t x = cbeg + 64 * b;
+                    if (x < ti.col_end) tma_store_2d(&tmC, (int32_t)x, y, box + b * KT_BOX_BYTES);
+                }
+                bulk_commit_group();
+            }
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1;
+            }
+        }
+        if (lane == 0) bulk_wait_group0();
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Dense GEMM on CTA pairs: 256 x 256 tiles computed by 2-SM tcgen05 MMAs.
 //
 // The two CTAs of a cluster each stage half of the A tile (128 rows) and
@@ -716,6 +964,34 @@ static bool make_map(CUtensorMap *map, const void *base, int64_t rows, int64_t c
     return r == CUDA_SUCCESS;
 }
 
+// 2D map over a row-major bf16 matrix [rows][cols] (row stride cols), box
+// {64 elements, 32 rows}, 128-byte swizzle: the K-grouped epilogue's stores.
+static bool make_map_c(CUtensorMap *map, void *base, int64_t rows, int64_t cols)
+{
+    EncodeTiledFn enc = get_encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {64, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+static fp8_status_t launch_kgroup_tma(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &mc,
+                                      const GemmParams &p, int fa, int fb, int64_t grid, cudaStream_t st)
+{
+    const size_t smem = 1024 + SmemLayoutKT::misc_off + 8 * (size_t)(p.G + 1);
+    cudaError_t e = cudaFuncSetAttribute(fp8_gemm_kgroup_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return cuda_fail_with(e);
+    const uint32_t idesc = idesc_f8f6f4(fa, fb, BM, BN);
+    fp8_gemm_kgroup_tma_kernel<<<(unsigned)grid, GEMM_THREADS, smem, st>>>(ma, mb, mc, p, idesc);
+    return check_launch();
+}
+
 static size_t gemm_smem_bytes(int G) { return 1024 + SmemLayout::base_bytes + (G > 0 ? 8 * (size_t)(G + 1) : 0); }
 
 template <int MODE>
@@ -891,5 +1167,10 @@ extern "C" fp8_status_t fp8_grouped_gemm(int mode, const uint8_t *A, int fa, con
     p.num_n_blk = (int)((K + BN - 1) / BN);
     p.num_k_blk = 0;
     if (!make_map(&ma, A, N, ld_T, ld_T, BM) || !make_map(&mb, B, K, ld_T, ld_T, BN)) return FP8_ERR_CUDA;
+    if (N % 32 == 0 && K % 8 == 0 && aligned(C_bf16, 16) && (int64_t)G * N <= INT32_MAX) {
+        CUtensorMap mc;
+        if (!make_map_c(&mc, C_bf16, (int64_t)G * N, K)) return FP8_ERR_CUDA;
+        return launch_kgroup_tma(ma, mb, mc, p, fa, fb, grid, st);
+    }
     return launch_gemm<MODE_KGROUP>(ma, mb, p, fa, fb, grid, st);
 }

@@ -166,11 +166,14 @@ def test_grouped_m_small(orc, sizes, per_row):
 
 
 @pytest.mark.parametrize("sizes", [[5, 0, 33, 1, 0, 140, 128, 300], [0, 0, 256], [1], [200, 0]])
-def test_grouped_k_small(orc, sizes):
+@pytest.mark.parametrize("NK", [(136, 264), (160, 296), (96, 520)])
+def test_grouped_k_small(orc, sizes, NK):
+    """(136, 264) takes the direct-store epilogue; N % 32 == 0 and K % 8 == 0
+    take the TMA-store epilogue (partial 128-row tiles, K ending inside a box)."""
     off = offsets_of(sizes)
     poff = orc.padded_offsets(off)
     ldT = max(16, int(poff[-1]))
-    G, N, K = len(sizes), 136, 264
+    G, (N, K) = len(sizes), NK
     g = torch.Generator().manual_seed(len(sizes) * 13)
     AT = torch.zeros((N, ldT), dtype=torch.uint8)
     BT = torch.zeros((K, ldT), dtype=torch.uint8)
