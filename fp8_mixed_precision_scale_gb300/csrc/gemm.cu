@@ -654,55 +654,52 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 }
                 continue;
             }
+            // this tile's scales, loaded before the accumulator wait so their
+            // latency hides behind it: the lane's row scale and, for each of
+            // the four 32-column chunks, the scale of column (chunk, lane)
+            const float sa_v = live ? (p.sa_per_row ? __ldg(p.sa + ti.sa_base + qrow0 + lane) : __ldg(p.sa)) : 0.0f;
+            float sbl4[4];
+#pragma unroll
+            for (int u = 0; u < 4; u++) {
+                const int64_t cc = cbeg + u * 32 + lane;
+                sbl4[u] = p.sb_per_row ? (cc < ti.col_end ? __ldg(p.sb + ti.sb_base + cc) : 0.0f) : __ldg(p.sb);
+            }
             if (!mbar_wait_bounded(&tfull[acc], acc_phase, WAIT_LIMIT_NS, p.err, ERR_EPILOGUE_WAIT)) break;
             tc_fence_after();
-            const float sa_v = live ? (p.sa_per_row ? __ldg(p.sa + ti.sa_base + qrow0 + lane) : __ldg(p.sa)) : 0.0f;
-            const float sb0 = p.sb_per_row ? 0.0f : __ldg(p.sb);
             // the previous tile's stores must have read the boxes before they are refilled
             if (lane == 0) bulk_wait_group_read0();
             __syncwarp();
+            // the warp's whole 32 x 128 block in one round trip: four loads, one wait
+            uint32_t r[4][32];
+            const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN) +
+                                   (uint32_t)(half * (BN / 2));
 #pragma unroll
-            for (int ch = 0; ch < 4; ch += 2) {
-                uint32_t r[2][32];
-                const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN) +
-                                       (uint32_t)(half * (BN / 2) + ch * 32);
-                tmem_ld_32x32b_x32(taddr, r[0]);
-                tmem_ld_32x32b_x32(taddr + 32, r[1]);
-                float sbl[2] = {sb0, sb0};
-                if (p.sb_per_row) {
-#pragma unroll
-                    for (int u = 0; u < 2; u++) {
-                        const int64_t cc = cbeg + (ch + u) * 32 + lane;
-                        sbl[u] = cc < ti.col_end ? __ldg(p.sb + ti.sb_base + cc) : 0.0f;
-                    }
-                }
-                tmem_ld_wait();
-#pragma unroll
-                for (int u = 0; u < 2; u++) {
-                    const int cu = ch + u;  // 32-column chunk 0..3 of this warp's 128 columns
-                    uint32_t packed[16];
-#pragma unroll
-                    for (int j = 0; j < 16; j++) {
-                        const float lo = __uint_as_float(r[u][2 * j]) * sa_v * __shfl_sync(0xffffffffu, sbl[u], 2 * j);
-                        const float hi =
-                            __uint_as_float(r[u][2 * j + 1]) * sa_v * __shfl_sync(0xffffffffu, sbl[u], 2 * j + 1);
-                        packed[j] = pack_bf16x2(lo, hi);
-                    }
-                    // box cu / 2, 16-byte chunks 4 (cu % 2) .. +3 of this lane's 128-byte row,
-                    // 128-byte swizzle: chunk index XOR (row % 8)
-                    uint8_t *brow = box + (cu >> 1) * KT_BOX_BYTES + lane * 128;
-#pragma unroll
-                    for (int g = 0; g < 4; g++) {
-                        const int chunk = ((cu & 1) * 4 + g) ^ (lane & 7);
-                        *reinterpret_cast<uint4 *>(brow + chunk * 16) =
-                            make_uint4(packed[4 * g], packed[4 * g + 1], packed[4 * g + 2], packed[4 * g + 3]);
-                    }
-                }
-            }
-            // accumulator read: release it to the MMA warp
+            for (int u = 0; u < 4; u++) tmem_ld_32x32b_x32(taddr + 32 * u, r[u]);
+            tmem_ld_wait();
+            // accumulator read: release it to the MMA warp before converting
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[acc]);
+#pragma unroll
+            for (int cu = 0; cu < 4; cu++) {  // 32-column chunk 0..3 of this warp's 128 columns
+                uint32_t packed[16];
+#pragma unroll
+                for (int j = 0; j < 16; j++) {
+                    const float lo = __uint_as_float(r[cu][2 * j]) * sa_v * __shfl_sync(0xffffffffu, sbl4[cu], 2 * j);
+                    const float hi =
+                        __uint_as_float(r[cu][2 * j + 1]) * sa_v * __shfl_sync(0xffffffffu, sbl4[cu], 2 * j + 1);
+                    packed[j] = pack_bf16x2(lo, hi);
+                }
+                // box cu / 2, 16-byte chunks 4 (cu % 2) .. +3 of this lane's 128-byte row,
+                // 128-byte swizzle: chunk index XOR (row % 8)
+                uint8_t *brow = box + (cu >> 1) * KT_BOX_BYTES + lane * 128;
+#pragma unroll
+                for (int g = 0; g < 4; g++) {
+                    const int chunk = ((cu & 1) * 4 + g) ^ (lane & 7);
+                    *reinterpret_cast<uint4 *>(brow + chunk * 16) =
+                        make_uint4(packed[4 * g], packed[4 * g + 1], packed[4 * g + 2], packed[4 * g + 3]);
+                }
+            }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
             if (lane == 0 && live) {
