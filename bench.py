@@ -21,6 +21,8 @@ Other workloads (same JSON line, their own config):
                  9216), delayed scaling, all E4M3, amax algo max
   llama_mxfp8    the Llama-3-8B MLP step under the MXFP8 recipe (blocks of 32
                  with E8M0 scales, both layouts per tensor, block-scaled GEMMs)
+  moe_mxfp8      the DeepSeek-V3 MoE layer under the MXFP8 recipe with the
+                 fused permute / SwiGLU prologues and MX grouped GEMMs
   llama_blockwise  the same step under the blockwise recipe (1x128 activation
                  and gradient blocks, 128x128 weight blocks, power-of-two scales)
   bw_quantize    the blockwise quantize of dY_gate (1x128 blocks)
@@ -578,6 +580,122 @@ class MoeStep:
                W["wgrad"])
 
 
+class MoeMxStep:
+    """The DeepSeek-V3-shaped MoE layer fwd+bwd under the MXFP8 recipe, with
+    the fused prologues: the token rows are gathered into expert order inside
+    their quantize (fp8_mx_permute_quantize), SwiGLU of the fused gate|up
+    projection's output is applied inside the quantize of the down
+    projection's input (fp8_mx_swiglu_quantize); the expert weights are MX
+    quantized as grouped stacks (gate and up fused per expert); six grouped
+    MX GEMMs with the FLOPs of the nine unfused ones: M-grouped fprop (gate|up,
+    down), M-grouped dgrad on the weights' transposed layouts, K-grouped
+    wgrad."""
+
+    def __init__(self, dev, seed):
+        import numpy as np
+
+        import fp8_mixed_precision_scale_gb300 as fp8
+        import synth
+        self.fp8 = fp8
+        E, H, F, T = synth.DSV3["E"], synth.DSV3["H"], synth.DSV3["F"], synth.DSV3["tokens"]
+        self.E, self.H, self.F = E, H, F
+        sizes = synth.moe_group_sizes().numpy()
+        self.off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+        self.off_h = torch.from_numpy(self.off)
+        self.off_d = self.off_h.to(dev)
+        self.M = M = int(self.off[-1])
+        self.tokens = T
+        self.name = "moe_mxfp8"
+        self.desc = ("deepseek-v3 moe layer fwd+bwd, mxfp8 recipe: 4096 tokens x top-8 = 32768 routed rows gathered "
+                     "into expert order inside their quantize, hidden 7168, 256 experts of ffn 2048 (gate|up fused, "
+                     "down), SwiGLU fused into the quantize of the down projection's input, group sizes multinomial "
+                     "over zipf(1.1) with 8 empty experts; 6 grouped MX GEMMs (the FLOPs of 9)")
+        rng = np.random.default_rng(seed)
+        self.src = torch.from_numpy(rng.integers(0, T, size=M).astype(np.int32)).to(dev)   # routed row -> token
+        g = torch.Generator(device=dev)
+        g.manual_seed(seed)
+        self.inp = {"x": _normal(g, dev, (T, H), 1.0), "w_gu": _normal(g, dev, (E * 2 * F, H), 0.02),
+                    "w_down": _normal(g, dev, (E * H, F), 0.02), "dy": _normal(g, dev, (M, H), 1e-4),
+                    "dgu": _normal(g, dev, (M, 2 * F), 1e-4)}
+        self.P, _ = fp8.fp8_group_padded_offsets(self.off_h, fp8.MX_GROUP_ALIGN)   # padded routed rows
+        woff = {"w_gu": 2 * F, "w_down": H}
+        self.woff_d = {k: torch.from_numpy(np.arange(E + 1, dtype=np.int32) * r).to(dev) for k, r in woff.items()}
+
+        def bufs(rows, cols, srows):
+            return dict(row=torch.empty((rows, cols), dtype=torch.uint8, device=dev),
+                        colT=torch.empty((cols, srows), dtype=torch.uint8, device=dev),
+                        srow=torch.empty(fp8.fp8_mx_scale_bytes(srows, cols // 32), dtype=torch.uint8, device=dev),
+                        scol=torch.empty(fp8.fp8_mx_scale_bytes(cols, srows // 32), dtype=torch.uint8, device=dev),
+                        ldT=srows)
+        self.q = {"xp": bufs(M, H, self.P), "hp": bufs(M, F, self.P), "dy": bufs(M, H, self.P),
+                  "dgu": bufs(M, 2 * F, self.P), "w_gu": bufs(E * 2 * F, H, E * 2 * F),
+                  "w_down": bufs(E * H, F, E * H)}
+        e = lambda *shape: torch.empty(shape, dtype=torch.bfloat16, device=dev)  # noqa: E731
+        self.out = {"gu": e(M, 2 * F), "y": e(M, H), "dh": e(M, F), "dx": e(M, H), "dw_down": e(E, H, F),
+                    "dw_gu": e(E, 2 * F, H)}
+        nz = int((sizes > 0).sum())
+        fl = 2.0 * M * F * H
+        self.gemm_work = {  # (flops, algorithmic bytes: A + non-empty experts' weights + C + scales)
+            "fprop_gu": (2 * fl, M * H + 2 * nz * F * H + 4.0 * M * F + (M + 2 * nz * F) * H / 32),
+            "fprop_down": (fl, M * F + nz * F * H + 2.0 * M * H + (M + nz * H) * F / 32),
+            "dgrad_down": (fl, M * H + nz * F * H + 2.0 * M * F + (M + F) * H / 32),
+            "dgrad_gu": (2 * fl, 2 * M * F + 2 * nz * F * H + 2.0 * M * H + (M + H) * 2 * F / 32),
+            "wgrad_down": (fl, M * (F + H) + 2.0 * E * F * H + M * (F + H) / 32),
+            "wgrad_gu": (2 * fl, M * (2 * F + H) + 4.0 * E * F * H + M * (2 * F + H) / 32)}
+        self.flops = 9 * fl
+        self.q_shapes = {"xp": (M, H), "w_gu": (E * 2 * F, H), "w_down": (E * H, F), "hp": (M, F), "dy": (M, H),
+                         "dgu": (M, 2 * F)}
+        self.q_bytes = sum(mx_quantize_bytes(sh) for sh in self.q_shapes.values()) + 2 * M * F
+        self.launches_per_step = 6 + 6
+        self.d2h = [self.out["y"]]
+
+    def quantize(self, k):
+        fp8, q = self.fp8, self.q[k]
+        E = self.E
+        if k == "xp":
+            x = self.inp["x"]
+            fp8.fp8_mx_permute_quantize(x, x.shape[0], x.shape[1], x.stride(0), self.src, self.M, 0, 3, q["row"],
+                                        q["srow"], q["colT"], q["ldT"], q["scol"], self.off_d, E)
+        elif k == "hp":
+            gu = self.out["gu"]
+            fp8.fp8_mx_swiglu_quantize(gu, self.M, self.F, gu.stride(0), 0, 3, None, 0, q["row"], q["srow"],
+                                       q["colT"], q["ldT"], q["scol"], self.off_d, E)
+        else:
+            t = self.inp[k]
+            r, c = t.shape
+            off = self.woff_d[k] if k.startswith("w_") else self.off_d
+            f = 1 if k in ("dy", "dgu") else 0
+            fp8.fp8_mx_quantize(t, r, c, c, f, 3, q["row"], q["srow"], q["colT"], q["ldT"], q["scol"], off, E)
+
+    def run(self, ev=None, world=1):
+        fp8, q, o, E, H, F, M = self.fp8, self.q, self.out, self.E, self.H, self.F, self.M
+        GM, GK, GMT = fp8.GROUPED_M, fp8.GROUPED_K, fp8.GROUPED_M_BT
+        off = self.off_d
+
+        def gg(mode, a, al, fa, b, bl, fb, N, K, out, ldT=0):
+            A = q[a]["row"] if al == "row" else q[a]["colT"]
+            B = q[b]["row"] if bl == "row" else q[b]["colT"]
+            sA = q[a]["srow"] if al == "row" else q[a]["scol"]
+            sB = q[b]["srow"] if bl == "row" else q[b]["scol"]
+            fp8.fp8_mx_grouped_gemm(mode, A, fa, sA, B, fb, sB, off, E, M, N, K, o[out], ldT)
+
+        W = self.gemm_work
+        for k in ("xp", "w_gu", "w_down"):
+            _timed(ev, "q", lambda k=k: self.quantize(k), mx_quantize_bytes(self.q_shapes[k]))
+        _timed(ev, "g", lambda: gg(GM, "xp", "row", 0, "w_gu", "row", 0, 2 * F, H, "gu"), W["fprop_gu"])
+        _timed(ev, "q", lambda: self.quantize("hp"), mx_quantize_bytes(self.q_shapes["hp"]) + 2 * M * F)
+        _timed(ev, "g", lambda: gg(GM, "hp", "row", 0, "w_down", "row", 0, H, F, "y"), W["fprop_down"])
+        for k in ("dy", "dgu"):
+            _timed(ev, "q", lambda k=k: self.quantize(k), mx_quantize_bytes(self.q_shapes[k]))
+        _timed(ev, "g", lambda: gg(GMT, "dy", "row", 1, "w_down", "colT", 0, F, H, "dh", q["w_down"]["ldT"]),
+               W["dgrad_down"])
+        _timed(ev, "g", lambda: gg(GMT, "dgu", "row", 1, "w_gu", "colT", 0, H, 2 * F, "dx", q["w_gu"]["ldT"]),
+               W["dgrad_gu"])
+        _timed(ev, "g", lambda: gg(GK, "dy", "colT", 1, "hp", "colT", 0, H, F, "dw_down", self.P), W["wgrad_down"])
+        _timed(ev, "g", lambda: gg(GK, "dgu", "colT", 1, "xp", "colT", 0, 2 * F, H, "dw_gu", self.P),
+               W["wgrad_gu"])
+
+
 # --------------------------------------------------------------------------------------------
 # CPU baseline (the oracle)
 # --------------------------------------------------------------------------------------------
@@ -672,7 +790,8 @@ def run_gpu(args, rank, world, local_rank):
         run_sweep(args, dev, rank, hbm_gbs)
         return
     make = {"llama_mlp": llama_mlp_step, "flux": flux_step, "llama_rowwise": RowwiseStep, "moe": MoeStep,
-            "llama_mxfp8": MxStep, "llama_blockwise": lambda dev, seed: MxStep(dev, seed, recipe="blockwise")}
+            "llama_mxfp8": MxStep, "llama_blockwise": lambda dev, seed: MxStep(dev, seed, recipe="blockwise"),
+            "moe_mxfp8": MoeMxStep}
     step = make[args.workload](dev, 1 + rank)
     for _ in range(max(3, args.warmup)):
         step.run(world=world)
@@ -712,13 +831,14 @@ def run_gpu(args, rank, world, local_rank):
         if g_roof_ms <= g_tensor_ms * 1.0001:      # tensor-bound GEMMs
             roof = {"bound": "tensor", "achieved": round(gemm_tflops, 1), "peak": round(fp8_peak, 1),
                     "unit": "TFLOP/s", "frac": round(gemm_tflops / fp8_peak, 4),
-                    "kernel": "mx_gemm_kernel" if isinstance(step, MxStep) else "fp8_gemm_pair_kernel",
+                    "kernel": "mx_gemm_kernel" if isinstance(step, (MxStep, MoeMxStep)) else "fp8_gemm_pair_kernel",
                     "traffic": gemm_traffic(step.name),
                     "peak_source": f"{peak_src}: 2 x sustained bf16 {bf16_sust} TFLOP/s (fp8/bf16 nominal ratio 2)"}
         else:                                      # HBM-bound (grouped GEMMs at the MoE shape)
             gbs = sum(b for _, b in g_work) / (sum(g_ms) * 1e-3) / 1e9
             roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_gbs, "unit": "GB/s",
-                    "frac": round(g_frac, 4), "traffic": None, "kernel": "fp8_gemm_kernel (grouped)",
+                    "frac": round(g_frac, 4), "traffic": None,
+                    "kernel": "mx_gemm_kernel (grouped)" if isinstance(step, MoeMxStep) else "fp8_gemm_kernel (grouped)",
                     "peak_source": f"{peak_src} HBM copy bandwidth; frac = roofline time max(flops / fp8 peak, "
                                    f"bytes / HBM) over the measured time"}
     else:
@@ -777,7 +897,7 @@ def run_e2e(step, args, world, dev):
     host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in step.d2h]
     h2d = sum(t.numel() * t.element_size() for t in pinned.values())
     d2h = sum(t.numel() * t.element_size() for t in host_out)
-    n = 2 if step.name == "moe" else max(3, min(args.steps, 10))
+    n = 2 if step.name.startswith("moe") else max(3, min(args.steps, 10))
     sets = [dict(step.inp), {k: torch.empty_like(t) for k, t in step.inp.items()}]
     comp = torch.cuda.current_stream()
     copy_s = torch.cuda.Stream()
@@ -1070,7 +1190,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="llama_mlp",
-                    choices=["llama_mlp", "llama_rowwise", "llama_mxfp8", "llama_blockwise", "moe", "flux", "sweep",
+                    choices=["llama_mlp", "llama_rowwise", "llama_mxfp8", "llama_blockwise", "moe", "moe_mxfp8", "flux",
+                             "sweep",
                              "gemm", "quantize", "bw_quantize", "rowwise_quantize",
                              "grouped_m", "grouped_k", "quantize_grouped", "mx_gemm", "mx_quantize", "mx_permute",
                              "mx_swiglu"],

@@ -88,19 +88,21 @@ struct Params {
     const int32_t *offsets;
     int G;
     int64_t ld_T;
+    int b_trans;   // M-grouped with B in the grouped transposed layout [N][ld_T]
+    int64_t kpad;  // b_trans: column stride between experts, roundup(K, 128)
     unsigned int *err;
 };
 
 struct Tile {
     int32_t a_y, b_y;        // first TMA row of the A / B tile
-    int32_t x0;              // first K column (bytes) of both tiles
+    int32_t a_x0, b_x0;      // first K column (bytes) of the A / B tile
     int64_t sa_row, sb_row;  // first scale row of the A / B tile
-    int64_t kt0;             // first K tile in the scale layouts
+    int64_t kt0a, kt0b;      // first K tile of A's / B's scale layout
     int nkb, last_steps;
     int64_t row0, row_end, col0, col_end, c_base;
 };
 
-template <int NS>
+template <int NS, bool TMA_OUT = false>
 struct Smem {
     static constexpr int a_off = 0;
     static constexpr int b_off = NS * A_BYTES;
@@ -111,12 +113,18 @@ struct Smem {
     static constexpr int bar_off = sfb_cp_off + NS * SFB_CP;
     static constexpr int n_bars = 3 * NS + 2 + 2 + 2;
     static constexpr int slot_off = bar_off + n_bars * 8;
-    static constexpr int stage_off = (slot_off + 16 + 127) / 128 * 128;
-    static constexpr int misc_off = stage_off + 8 * 32 * 80;  // group tables
+    // epilogue staging per warp: a 32 x 32 transpose block (direct stores) or
+    // two 32-row x 64-column TMA boxes (1024-aligned for the 128-byte swizzle)
+    static constexpr int stage_warp = TMA_OUT ? 2 * 32 * 128 : 32 * 80;
+    static constexpr int stage_off = TMA_OUT ? (slot_off + 16 + 1023) / 1024 * 1024 : (slot_off + 16 + 127) / 128 * 128;
+    static constexpr int misc_off = stage_off + 8 * stage_warp;  // group tables
 };
 constexpr int STAGE_PITCH = 80;  // epilogue staging: 32 rows x 32 bf16 per warp, rows padded to 80 bytes
-constexpr int STAGE_WARP_BYTES = 32 * STAGE_PITCH;
-__host__ __device__ constexpr int ring_stages(int mode) { return mode == 0 ? STAGES : STAGES_GROUPED; }
+constexpr int BOX_BYTES = 32 * 128;  // TMA store box: 32 rows x 64 bf16
+__host__ __device__ constexpr int ring_stages(int mode, bool tma_out)
+{
+    return tma_out ? 2 : (mode == 0 ? STAGES : STAGES_GROUPED);
+}
 
 // Tile prefix [G+1] and offsets padded to FP8_MX_GROUP_ALIGN [G+1]; one warp.
 __device__ bool build_group_tables(const Params &p, int MODE, int32_t *tile_prefix, int32_t *poff,
@@ -179,10 +187,10 @@ __device__ __forceinline__ Tile tile_info(const Params &p, int64_t t, const int3
         }
         ti.a_y = mb * BM;
         ti.b_y = nb * BN;
-        ti.x0 = 0;
+        ti.a_x0 = ti.b_x0 = 0;
         ti.sa_row = (int64_t)mb * BM;
         ti.sb_row = (int64_t)nb * BN;
-        ti.kt0 = 0;
+        ti.kt0a = ti.kt0b = 0;
         ti.nkb = p.num_k_blk;
         ti.last_steps = (int)((p.K - (int64_t)(ti.nkb - 1) * BK) / UMMA_K);
         ti.row0 = (int64_t)mb * BM;
@@ -206,11 +214,22 @@ __device__ __forceinline__ Tile tile_info(const Params &p, int64_t t, const int3
             const int64_t mt = (m_e + BM - 1) / BM;
             const int64_t mb = local % mt, nb = local / mt;  // rows fastest: the expert's weight tile stays in L2
             ti.a_y = (int32_t)(p.offsets[e] + mb * BM);
-            ti.b_y = (int32_t)((int64_t)e * p.N + nb * BN);
-            ti.x0 = 0;
+            ti.a_x0 = 0;
             ti.sa_row = poff[e] + mb * BM;
-            ti.sb_row = (int64_t)e * p.N + nb * BN;
-            ti.kt0 = 0;
+            ti.kt0a = 0;
+            if (p.b_trans) {
+                // expert e's [N][K] block starts at column e * kpad of B; its
+                // scale words at K tile e * kpad / 128
+                ti.b_y = (int32_t)(nb * BN);
+                ti.b_x0 = (int32_t)(e * p.kpad);
+                ti.sb_row = nb * BN;
+                ti.kt0b = e * p.kpad / BK;
+            } else {
+                ti.b_y = (int32_t)((int64_t)e * p.N + nb * BN);
+                ti.b_x0 = 0;
+                ti.sb_row = (int64_t)e * p.N + nb * BN;
+                ti.kt0b = 0;
+            }
             ti.nkb = p.num_k_blk;
             ti.last_steps = (int)((p.K - (int64_t)(ti.nkb - 1) * BK) / UMMA_K);
             ti.row0 = p.offsets[e] + mb * BM;
@@ -224,10 +243,10 @@ __device__ __forceinline__ Tile tile_info(const Params &p, int64_t t, const int3
             const int64_t nb = local % p.num_n_blk, mb = local / p.num_n_blk;
             ti.a_y = (int32_t)(mb * BM);
             ti.b_y = (int32_t)(nb * BN);
-            ti.x0 = poff[e];
+            ti.a_x0 = ti.b_x0 = poff[e];
             ti.sa_row = mb * BM;
             ti.sb_row = nb * BN;
-            ti.kt0 = poff[e] / BK;
+            ti.kt0a = ti.kt0b = poff[e] / BK;
             ti.nkb = (int)((m_e + BK - 1) / BK);
             ti.last_steps = ti.nkb > 0 ? (int)((m_e - (int64_t)(ti.nkb - 1) * BK + UMMA_K - 1) / UMMA_K) : 0;
             ti.row0 = mb * BM;
@@ -290,13 +309,60 @@ __device__ __forceinline__ void epilogue_tile(const Params &p, const Tile &ti, u
     }
 }
 
-template <int MODE>
-__global__ void __launch_bounds__(THREADS, 1)
-    mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, Params p,
-                   uint32_t idesc)
+// The same drain for the K-grouped output through TMA stores: the warp's
+// 32 x 128 block goes to two 128-byte-swizzled 32 x 64 boxes and the warp's
+// lane 0 issues their stores; the warp first waits until its previous
+// stores have read the boxes.  Rows of the tile past N are not stored (N %
+// 32 == 0, so a quarter is all in or all out).
+__device__ __forceinline__ void epilogue_tile_tma(const Params &p, const Tile &ti, uint32_t tmem_base, int q, int cb,
+                                                  int lane, uint8_t *box, uint64_t *tempty, const CUtensorMap *tmC)
 {
-    constexpr int NS = ring_stages(MODE);
-    using L = Smem<NS>;
+    uint32_t r[4][32];
+    const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)cb;
+#pragma unroll
+    for (int u = 0; u < 4; u++) tmem_ld_32x32b_x32(taddr + 32 * u, r[u]);
+    tmem_ld_wait();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) {
+        mbar_arrive(tempty);
+        bulk_wait_group_read0();
+    }
+    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+        uint8_t *brow = box + (u >> 1) * BOX_BYTES + lane * 128;
+#pragma unroll
+        for (int g = 0; g < 4; g++) {
+            const int chunk = ((u & 1) * 4 + g) ^ (lane & 7);
+            *reinterpret_cast<uint4 *>(brow + chunk * 16) =
+                make_uint4(pack_bf16x2(__uint_as_float(r[u][8 * g]), __uint_as_float(r[u][8 * g + 1])),
+                           pack_bf16x2(__uint_as_float(r[u][8 * g + 2]), __uint_as_float(r[u][8 * g + 3])),
+                           pack_bf16x2(__uint_as_float(r[u][8 * g + 4]), __uint_as_float(r[u][8 * g + 5])),
+                           pack_bf16x2(__uint_as_float(r[u][8 * g + 6]), __uint_as_float(r[u][8 * g + 7])));
+        }
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    const int64_t qrow0 = ti.row0 + q * 32;
+    if (lane == 0 && qrow0 < ti.row_end) {
+        const int32_t y = (int32_t)(ti.c_base / p.ldc + qrow0);  // row of the [G*N][K] view of C
+#pragma unroll
+        for (int b = 0; b < 2; b++) {
+            const int64_t x = ti.col0 + cb + 64 * b;
+            if (x < ti.col_end) tma_store_2d(tmC, (int32_t)x, y, box + b * BOX_BYTES);
+        }
+        bulk_commit_group();
+    }
+}
+
+template <int MODE, bool TMA_OUT>
+__global__ void __launch_bounds__(THREADS, 1)
+    mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmC, Params p, uint32_t idesc)
+{
+    constexpr int NS = ring_stages(MODE, TMA_OUT);
+    using L = Smem<NS, TMA_OUT>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sA = smem + L::a_off;
@@ -379,12 +445,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                     ok = false;
                     break;
                 }
-                const int64_t kt = ti.kt0 + kb;
                 mbar_arrive_expect_tx(&full[stage], A_BYTES + B_BYTES + sfa_bytes + sfb_bytes);
-                tma_load_2d(sA + stage * A_BYTES, &tmA, ti.x0 + kb * BK, ti.a_y, &full[stage]);
-                tma_load_2d(sB + stage * B_BYTES, &tmB, ti.x0 + kb * BK, ti.b_y, &full[stage]);
-                bulk_load(sfa_raw + stage * SFA_RAW, p.sA + (kt * rsA + ti.sa_row) * 4, sfa_bytes, &full[stage]);
-                bulk_load(sfb_raw + stage * SFB_RAW, p.sB + (kt * p.rsB + ti.sb_row) * 4, sfb_bytes, &full[stage]);
+                tma_load_2d(sA + stage * A_BYTES, &tmA, ti.a_x0 + kb * BK, ti.a_y, &full[stage]);
+                tma_load_2d(sB + stage * B_BYTES, &tmB, ti.b_x0 + kb * BK, ti.b_y, &full[stage]);
+                bulk_load(sfa_raw + stage * SFA_RAW, p.sA + ((ti.kt0a + kb) * rsA + ti.sa_row) * 4, sfa_bytes,
+                          &full[stage]);
+                bulk_load(sfb_raw + stage * SFB_RAW, p.sB + ((ti.kt0b + kb) * p.rsB + ti.sb_row) * 4, sfb_bytes,
+                          &full[stage]);
                 issued_parity[stage] = (int)phase;
                 if (++stage == NS) {
                     stage = 0;
@@ -492,11 +559,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         // the tile
         const int q = warp & 3;
         const int cb = ((warp - 2) >> 2) * 128;
-        uint8_t *stage = smem + L::stage_off + (warp - 2) * STAGE_WARP_BYTES;
+        uint8_t *stage = smem + L::stage_off + (warp - 2) * L::stage_warp;
         uint32_t acc_phase = 0;
         for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
             const Tile ti = tile_info<MODE>(p, t, tile_prefix, poff);
-            if (ti.nkb == 0) {
+            if (ti.nkb == 0) {  // empty K-group: its block of C is zero (direct stores)
                 const int64_t gr = ti.row0 + q * 32 + lane;
                 if (gr < ti.row_end) {
                     uint16_t *crow = p.C + ti.c_base + gr * p.ldc;
@@ -507,8 +574,15 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             if (!mbar_wait_bounded(&tfull[0], acc_phase, WAIT_LIMIT_NS, p.err, ERR_EPILOGUE_WAIT)) break;
             tc_fence_after();
-            epilogue_tile(p, ti, tmem_base, q, cb, lane, stage, &tempty[0]);
+            if constexpr (TMA_OUT)
+                epilogue_tile_tma(p, ti, tmem_base, q, cb, lane, stage, &tempty[0], &tmC);
+            else
+                epilogue_tile(p, ti, tmem_base, q, cb, lane, stage, &tempty[0]);
             acc_phase ^= 1;
+        }
+        if constexpr (TMA_OUT) {
+            if (lane == 0) bulk_wait_group0();  // every store completed before the block exits
+            __syncwarp();
         }
     }
 
@@ -558,21 +632,38 @@ static bool make_map(CUtensorMap *map, const void *base, int64_t rows, int64_t c
     return r == CUDA_SUCCESS;
 }
 
-template <int MODE>
+template <int MODE, bool TMA_OUT>
 static size_t smem_bytes(int G)
 {
-    return 1024 + Smem<ring_stages(MODE)>::misc_off + (G > 0 ? 8 * (size_t)(G + 1) : 0);
+    return 1024 + Smem<ring_stages(MODE, TMA_OUT), TMA_OUT>::misc_off + (G > 0 ? 8 * (size_t)(G + 1) : 0);
 }
 
-template <int MODE>
-static fp8_status_t launch(const CUtensorMap &ma, const CUtensorMap &mb, const Params &p, int fa, int fb,
-                           int64_t grid, cudaStream_t st)
+// 2D map over the bf16 output viewed as [rows][cols] (row stride cols), box
+// {64, 32}, 128-byte swizzle: the TMA-store epilogue.
+static bool make_map_c(CUtensorMap *map, void *base, int64_t rows, int64_t cols)
 {
-    const size_t smem = smem_bytes<MODE>(MODE == MODE_DENSE ? 0 : p.G);
-    cudaError_t e = cudaFuncSetAttribute(mx_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    EncodeTiledFn enc = get_encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {64, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int MODE, bool TMA_OUT = false>
+static fp8_status_t launch(const CUtensorMap &ma, const CUtensorMap &mb, const Params &p, int fa, int fb,
+                           int64_t grid, cudaStream_t st, const CUtensorMap *mc = nullptr)
+{
+    const size_t smem = smem_bytes<MODE, TMA_OUT>(MODE == MODE_DENSE ? 0 : p.G);
+    cudaError_t e = cudaFuncSetAttribute(mx_gemm_kernel<MODE, TMA_OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
     if (e != cudaSuccess) return cuda_fail_with(e);
     const uint32_t idesc = idesc_mxf8f6f4(fa, fb, BM, BN);
-    mx_gemm_kernel<MODE><<<(unsigned)grid, THREADS, smem, st>>>(ma, mb, p, idesc);
+    mx_gemm_kernel<MODE, TMA_OUT><<<(unsigned)grid, THREADS, smem, st>>>(ma, mb, mc ? *mc : ma, p, idesc);
     return check_launch();
 }
 
@@ -630,7 +721,7 @@ extern "C" fp8_status_t fp8_mx_grouped_gemm(int mode, const uint8_t *A, int fa, 
     if (fa == FP8_E4M3FNUZ || fb == FP8_E4M3FNUZ || fa == FP8_E5M2FNUZ || fb == FP8_E5M2FNUZ)
         return FP8_ERR_UNSUPPORTED;
     if (!mx::format_ok(fa) || !mx::format_ok(fb)) return FP8_ERR_INVALID_ARG;
-    if (mode != FP8_GROUPED_M && mode != FP8_GROUPED_K) return FP8_ERR_INVALID_ARG;
+    if (mode != FP8_GROUPED_M && mode != FP8_GROUPED_K && mode != FP8_GROUPED_M_BT) return FP8_ERR_INVALID_ARG;
     if (G < 1 || G > mx::MAX_GROUPS || M_total < 0 || N < 1 || K < 1) return FP8_ERR_INVALID_ARG;
     if (M_total > INT32_MAX || N > INT32_MAX || K > INT32_MAX || (int64_t)G * N > INT32_MAX)
         return FP8_ERR_INVALID_ARG;
@@ -651,17 +742,26 @@ extern "C" fp8_status_t fp8_mx_grouped_gemm(int mode, const uint8_t *A, int fa, 
     CUtensorMap ma, mb;
     const int64_t grid = num_sms();
 
-    if (mode == FP8_GROUPED_M) {
+    if (mode == FP8_GROUPED_M || mode == FP8_GROUPED_M_BT) {
         if (K % FP8_MX_BLOCK != 0 || N % 4 != 0) return FP8_ERR_ALIGNMENT;
         p.rsA = 0;  // the padded total, known on the device from the offsets
         p.rsB = (int64_t)G * N;
+        p.kpad = (K + mx::BK - 1) / mx::BK * mx::BK;
+        if (mode == FP8_GROUPED_M_BT) {
+            if (ld_T % 16 != 0) return FP8_ERR_ALIGNMENT;
+            if (ld_T < (int64_t)G * p.kpad || ld_T > INT32_MAX) return FP8_ERR_INVALID_ARG;
+            p.b_trans = 1;
+            p.rsB = N;  // B's scale rows: the N rows of the transposed layout
+        }
         p.ldc = N;
         p.c_vec16 = N % 8 == 0 && aligned(C_bf16, 16);
         p.num_m_blk = 0;
         p.num_n_blk = (int)((N + mx::BN - 1) / mx::BN);
         p.num_k_blk = (int)((K + mx::BK - 1) / mx::BK);
         if (M_total == 0) return FP8_OK;
-        if (!mx::make_map(&ma, A, M_total, K, K, mx::BM) || !mx::make_map(&mb, B, (int64_t)G * N, K, K, mx::BN))
+        if (!mx::make_map(&ma, A, M_total, K, K, mx::BM)) return FP8_ERR_CUDA;
+        if (p.b_trans ? !mx::make_map(&mb, B, N, (int64_t)G * p.kpad, ld_T, mx::BN)
+                      : !mx::make_map(&mb, B, (int64_t)G * N, K, K, mx::BN))
             return FP8_ERR_CUDA;
         return mx::launch<mx::MODE_MGROUP>(ma, mb, p, fa, fb, grid, st);
     }
@@ -677,5 +777,11 @@ extern "C" fp8_status_t fp8_mx_grouped_gemm(int mode, const uint8_t *A, int fa, 
     p.num_k_blk = 0;
     if (!mx::make_map(&ma, A, N, ld_T, ld_T, mx::BM) || !mx::make_map(&mb, B, K, ld_T, ld_T, mx::BN))
         return FP8_ERR_CUDA;
+    if (N % 32 == 0 && K % 8 == 0 && aligned(C_bf16, 16) && (int64_t)G * N <= INT32_MAX) {
+        // the output is the whole cost of this mode: TMA-store epilogue
+        CUtensorMap mc;
+        if (!mx::make_map_c(&mc, C_bf16, (int64_t)G * N, K)) return FP8_ERR_CUDA;
+        return mx::launch<mx::MODE_KGROUP, true>(ma, mb, p, fa, fb, grid, st, &mc);
+    }
     return mx::launch<mx::MODE_KGROUP>(ma, mb, p, fa, fb, grid, st);
 }

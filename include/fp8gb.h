@@ -385,7 +385,12 @@ FP8GB_API fp8_status_t fp8_mx_gemm(const uint8_t *A, int fa, int64_t lda, const 
  *   (R = N / K, KB = P / 32 with P the padded total); C[e] = A_e . B_e^T
  *   over group e's padded columns, C bf16 [G][N][K]; an empty group's block
  *   is 0.
- * Limits: K % 32 == 0 (M mode); N % 4 == 0 (M mode); ld_T % 128 == 0
+ * FP8_GROUPED_M_BT (dgrad with the weights' transposed layout): as
+ *   FP8_GROUPED_M, but B u8 [N][ld_T] is the transposed layout of a grouped
+ *   fp8_mx_quantize of the weight stack [G*K][N] in G equal groups of K rows:
+ *   expert e's [N][K] block starts at column e * kpad, kpad = roundup(K, 128)
+ *   (ld_T >= G * kpad, ld_T % 16 == 0); sB its scales (R = N).
+ * Limits: K % 32 == 0 (M modes); N % 4 == 0 (M modes); ld_T % 128 == 0
  * (K mode); 1 <= G <= 1024; A, B, sA, sB 16-byte aligned.
  */
 FP8GB_API fp8_status_t fp8_mx_grouped_gemm(int mode, const uint8_t *A, int fa, const uint8_t *sA,

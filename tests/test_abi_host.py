@@ -249,7 +249,9 @@ def mxgg_call(lib, **kw):
 
 def test_mx_grouped_gemm_validation(lib):
     assert mxgg_call(lib, off=None) == INVALID
-    assert mxgg_call(lib, mode=2) == INVALID               # no transposed-B mode for MX
+    assert mxgg_call(lib, mode=2) == INVALID               # transposed B: ld_T shorter than G * kpad
+    assert mxgg_call(lib, mode=2, ldT=4 * 128 + 8) == ALIGN
+    assert mxgg_call(lib, mode=3) == INVALID
     assert mxgg_call(lib, G=2000) == INVALID
     assert mxgg_call(lib, fa=3) == UNSUPPORTED
     assert mxgg_call(lib, K=96 + 16) == ALIGN

@@ -244,11 +244,14 @@ def test_mx_grouped_m_small(orc):
         check_gemm(out[r0:r1], ref, bound, f"mgroup e{e}")
 
 
-def test_mx_grouped_k_small(orc):
+@pytest.mark.parametrize("NK", [(200, 300), (192, 296), (96, 520)])
+def test_mx_grouped_k_small(orc, NK):
+    """(200, 300) takes the direct-store epilogue; N % 32 == 0 with K % 8 == 0
+    the TMA-store epilogue (partial tiles, K ending inside a box)."""
     sizes = [5, 0, 200, 1, 0, 129, 64]
     G = len(sizes)
     off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
-    Mt, N, K = int(off[-1]), 200, 300
+    Mt, (N, K) = int(off[-1]), NK
     qd = orc.mx_quantize(bits(gen_x((Mt, N), seed=41)), 1, fp8.LAYOUT_COLT, offsets=off, align=128)
     qx = orc.mx_quantize(bits(gen_x((Mt, K), seed=42)), 0, fp8.LAYOUT_COLT, offsets=off, align=128)
     P = qd["q_colT"].shape[1]
@@ -265,6 +268,37 @@ def test_mx_grouped_k_small(orc):
         ref, bound = orc.mx_gemm(qd["q_colT"][:, a:b], 1, qd["s_col"][:, a // 32:b // 32],
                                  qx["q_colT"][:, a:b], 0, qx["s_col"][:, a // 32:b // 32])
         check_gemm(out[e], ref, bound, f"kgroup e{e}")
+
+
+@pytest.mark.parametrize("K", [256, 160])
+def test_mx_grouped_m_bt_small(orc, K):
+    """dgrad on the weights' transposed layout: the weight stack [G*K][N]
+    MX-quantized in G groups of K rows; expert e's block starts at column
+    e * roundup(K, 128) of the transposed layout."""
+    sizes = [5, 0, 200, 1, 0, 129, 64]
+    G = len(sizes)
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    Mt, N = int(off[-1]), 320
+    xa = gen_x((Mt, K), seed=51)
+    qa = orc.mx_quantize(bits(xa), 1, fp8.LAYOUT_ROW, offsets=off, align=128)
+    woff = (np.arange(G + 1) * K).astype(np.int32)
+    qw = orc.mx_quantize(bits(gen_x((G * K, N), seed=52)), 0, fp8.LAYOUT_COLT, offsets=woff, align=128)
+    kpad = -(-K // 128) * 128
+    P = qw["q_colT"].shape[1]
+    assert P == G * kpad
+    C = fp8.mx_grouped_gemm(fp8.GROUPED_M_BT, up(qa["q_row"]), 1, up(mx_tiled(qa["s_row"])), up(qw["q_colT"]), 0,
+                            up(mx_tiled(qw["s_col"])), up(off), Mt, N, K, ld_T=P)
+    assert fp8.fp8_sync_status() == 0
+    poff = orc.padded_offsets_align(off, 128)
+    out = C.float().cpu().numpy()
+    for e in range(G):
+        if sizes[e] == 0:
+            continue
+        r0, r1 = off[e], off[e + 1]
+        c0 = e * kpad
+        ref, bound = orc.mx_gemm(qa["q_row"][r0:r1], 1, qa["s_row"][poff[e]:poff[e] + sizes[e]],
+                                 qw["q_colT"][:, c0:c0 + K], 0, qw["s_col"][:, c0 // 32:(c0 + K) // 32])
+        check_gemm(out[r0:r1], ref, bound, f"m_bt e{e}")
 
 
 def test_mx_grouped_bad_offsets_flagged():
