@@ -516,7 +516,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
             const Tile ti = tile_info<MODE>(p, t, tile_prefix, poff);
             for (int kb = 0; kb < ti.nkb; kb++) {
-                if (!mbar_wait_bounded(&full[stage], phase, WAIT_LIMIT_NS, p.err, ERR_MMA_WAIT)) {
+                // the warp leaves together if the wait gives up in any lane
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[stage], phase, WAIT_LIMIT_NS, p.err, ERR_MMA_WAIT))) {
                     ok = false;
                     break;
                 }

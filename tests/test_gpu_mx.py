@@ -165,7 +165,7 @@ def up(a):
 
 
 MX_SMALL = [(128, 224, 128), (1, 1, 32), (100, 40, 64), (130, 300, 160), (256, 448, 512), (300, 520, 1056),
-            (129, 257, 4096)]
+            (129, 257, 4096), (257, 1, 32), (520, 264, 96)]
 
 
 @pytest.mark.parametrize("shape", MX_SMALL)
