@@ -684,6 +684,180 @@ __global__ void __launch_bounds__(QT_THREADS) cast_kernel(QArgs a)
     if constexpr (DELAYED) block_amax_atomic(fold_absmax(amax_acc), a.amax_out, red);
 }
 
+// ---------------------------------------------------------------------------
+// Cast pass of a grouped tensor (expert token rows or stacked expert weights):
+// tiles of four consecutive padded 32-row blocks (128 padded rows) x 64
+// columns.  The four blocks may belong to different groups, but they are
+// adjacent in the padded space, so each column of the tile is one contiguous
+// 128-byte run of q_colT; each thread converts row r of every block (rows r,
+// 32 + r, 64 + r, 96 + r of the tile) for 8 columns.  Scales as in the
+// plain cast pass: one tensor scale (SMODE 0) or row scales plus the
+// (group, column) scales of each block's group (SMODE 1).
+// ---------------------------------------------------------------------------
+constexpr int GT_BLOCKS = 4;   // padded 32-row blocks per tile
+constexpr int GT_COLS = 64;    // columns per tile
+constexpr int GT_ROWS = 32 * GT_BLOCKS;
+
+// tileT word (row r, word w of the row's 16): the word index is XORed with
+// the row's 8-row chunk, so the transposed read of a chunk spreads over banks
+__device__ __forceinline__ int gt_word(int r, int w) { return r * (GT_COLS / 4) + (w ^ ((r >> 3) & 15)); }
+
+template <int FMT, int SMODE, bool DELAYED, bool DO_ROW, bool DO_COLT>
+__global__ void __launch_bounds__(QT_THREADS) grouped_cast_kernel(QArgs a)
+{
+    extern __shared__ __align__(16) unsigned char dsm[];
+    int32_t *poff = reinterpret_cast<int32_t *>(dsm);
+    __shared__ uint32_t tileT[GT_ROWS * GT_COLS / 4];
+    __shared__ float srow[GT_ROWS];
+    __shared__ float scol[GT_BLOCKS][GT_COLS];
+    __shared__ RowBlock srb[GT_BLOCKS];
+    __shared__ uint32_t red[QT_THREADS / 32];
+    __shared__ int bad;
+    const float fmax = fp8_max_of(FMT);
+    compute_padded_offsets(a.offsets, a.G, a.rows, DO_COLT ? a.ld_colT : 0, poff, &bad, a.err);
+    __syncthreads();
+    if (bad) return;
+
+    float s_tensor = 1.0f;
+    if constexpr (SMODE == 0) {
+        if constexpr (DELAYED)
+            s_tensor = a.scale_in[0];
+        else
+            s_tensor = scale_from_amax(a.amax_out[0], fmax, a.margin);
+        if (blockIdx.x == 0 && threadIdx.x == 0) {
+            const float sinv = recip_rn(s_tensor);
+            if (DO_ROW) a.sinv_row[0] = sinv;
+            if (DO_COLT) a.sinv_col[0] = sinv;
+        }
+    }
+
+    const int t = threadIdx.x, cg = t & 7, roff = t >> 3;
+    const int64_t n_cchunks = (a.cols + GT_COLS - 1) / GT_COLS;
+    const int64_t n_tiles = (a.n_row_blocks + GT_BLOCKS - 1) / GT_BLOCKS * n_cchunks;
+    uint32_t amax_acc = 0;
+    for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+        const int64_t b0 = tile / n_cchunks * GT_BLOCKS;
+        const int64_t c0 = (tile % n_cchunks) * GT_COLS;
+        if (t < GT_BLOCKS) {
+            if (b0 + t < a.n_row_blocks) {
+                srb[t] = row_block<32>(a, b0 + t, poff);
+            } else {
+                srb[t].skip = true;
+                srb[t].valid = 0;
+            }
+        }
+        __syncthreads();
+        if (srb[0].skip) break;  // past the padded total: so is every later tile of this block
+        const int64_t col = c0 + cg * 8;
+        const bool col_ok = col < a.cols;
+
+        uint4 v[GT_BLOCKS];
+#pragma unroll
+        for (int i = 0; i < GT_BLOCKS; i++) {
+            const RowBlock &rb = srb[i];
+            if (!rb.skip && col_ok && roff < rb.valid)
+                v[i] = __ldg(reinterpret_cast<const uint4 *>(a.x + (rb.in_row0 + roff) * a.ld_x + col));
+            else
+                v[i] = make_uint4(0, 0, 0, 0);
+        }
+        if constexpr (SMODE == 1) {
+            if (DO_ROW && t < GT_ROWS) {
+                const RowBlock &rb = srb[t >> 5];
+                const int r = t & 31;
+                const bool ok = !rb.skip && r < rb.valid;
+                const float w = ok ? a.sinv_row[rb.in_row0 + r] : 0.0f;
+                srow[t] = a.scales_ready ? (ok ? w : 1.0f) : scale_from_amax(w, fmax, a.margin);
+            }
+            if (DO_COLT) {
+                const int i = t / GT_COLS, j = t % GT_COLS;
+                const RowBlock &rb = srb[i];
+                const bool ok = !rb.skip && c0 + j < a.cols;
+                const float w = ok ? a.sinv_col[(int64_t)rb.group * a.cols + c0 + j] : 0.0f;
+                scol[i][j] = a.scales_ready ? (ok ? w : 1.0f) : scale_from_amax(w, fmax, a.margin);
+            }
+            __syncthreads();
+        }
+
+#pragma unroll
+        for (int i = 0; i < GT_BLOCKS; i++) {
+            const RowBlock &rb = srb[i];
+            const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+            if constexpr (DELAYED) {
+#pragma unroll
+                for (int k = 0; k < 4; k++) amax_acc = absmax_bf16x2(amax_acc, w[k]);
+            }
+            uint32_t rowb0 = 0, rowb1 = 0, colb0 = 0, colb1 = 0;
+            if constexpr (SMODE == 0) {
+                const float s = s_tensor;
+                rowb0 = cvt2<FMT>(__fmul_rn(bf16lo(w[0]), s), __fmul_rn(bf16hi(w[0]), s)) |
+                        (cvt2<FMT>(__fmul_rn(bf16lo(w[1]), s), __fmul_rn(bf16hi(w[1]), s)) << 16);
+                rowb1 = cvt2<FMT>(__fmul_rn(bf16lo(w[2]), s), __fmul_rn(bf16hi(w[2]), s)) |
+                        (cvt2<FMT>(__fmul_rn(bf16lo(w[3]), s), __fmul_rn(bf16hi(w[3]), s)) << 16);
+                colb0 = rowb0;
+                colb1 = rowb1;
+            } else {
+                if constexpr (DO_ROW) {
+                    const float s = srow[i * 32 + roff];
+                    rowb0 = cvt2<FMT>(__fmul_rn(bf16lo(w[0]), s), __fmul_rn(bf16hi(w[0]), s)) |
+                            (cvt2<FMT>(__fmul_rn(bf16lo(w[1]), s), __fmul_rn(bf16hi(w[1]), s)) << 16);
+                    rowb1 = cvt2<FMT>(__fmul_rn(bf16lo(w[2]), s), __fmul_rn(bf16hi(w[2]), s)) |
+                            (cvt2<FMT>(__fmul_rn(bf16lo(w[3]), s), __fmul_rn(bf16hi(w[3]), s)) << 16);
+                }
+                if constexpr (DO_COLT) {
+                    const float *sc = &scol[i][cg * 8];
+                    colb0 = cvt2<FMT>(__fmul_rn(bf16lo(w[0]), sc[0]), __fmul_rn(bf16hi(w[0]), sc[1])) |
+                            (cvt2<FMT>(__fmul_rn(bf16lo(w[1]), sc[2]), __fmul_rn(bf16hi(w[1]), sc[3])) << 16);
+                    colb1 = cvt2<FMT>(__fmul_rn(bf16lo(w[2]), sc[4]), __fmul_rn(bf16hi(w[2]), sc[5])) |
+                            (cvt2<FMT>(__fmul_rn(bf16lo(w[3]), sc[6]), __fmul_rn(bf16hi(w[3]), sc[7])) << 16);
+                }
+            }
+            const bool ok = !rb.skip && col_ok && roff < rb.valid;
+            if constexpr (DO_ROW) {
+                if (ok)
+                    *reinterpret_cast<uint2 *>(a.q_row + (rb.in_row0 + roff) * a.cols + col) = make_uint2(rowb0, rowb1);
+            }
+            if constexpr (DO_COLT) {
+                const int r = i * 32 + roff;
+                tileT[gt_word(r, 2 * cg)] = ok ? colb0 : 0u;  // rows past a block's end become zero padding
+                tileT[gt_word(r, 2 * cg + 1)] = ok ? colb1 : 0u;
+            }
+        }
+
+        if constexpr (DO_COLT) {
+            __syncthreads();
+            // item t = (column quad qa, 8-row chunk q); the 16 chunks of a
+            // column quad are 16 adjacent lanes, so each column's 128 bytes
+            // leave as one contiguous run
+            const int q = t & 15, qa = t >> 4;
+            const RowBlock &rb = srb[q >> 2];
+            if (!rb.skip) {
+                uint32_t wv[8];
+#pragma unroll
+                for (int i = 0; i < 8; i++) wv[i] = tileT[gt_word(q * 8 + i, qa)];
+                // 8 rows x 4 columns of bytes -> 4 columns x 8 rows
+                const uint32_t a01l = __byte_perm(wv[0], wv[1], 0x5140), a01h = __byte_perm(wv[0], wv[1], 0x7362);
+                const uint32_t a23l = __byte_perm(wv[2], wv[3], 0x5140), a23h = __byte_perm(wv[2], wv[3], 0x7362);
+                const uint32_t a45l = __byte_perm(wv[4], wv[5], 0x5140), a45h = __byte_perm(wv[4], wv[5], 0x7362);
+                const uint32_t a67l = __byte_perm(wv[6], wv[7], 0x5140), a67h = __byte_perm(wv[6], wv[7], 0x7362);
+                uint2 o[4];
+                o[0] = make_uint2(__byte_perm(a01l, a23l, 0x5410), __byte_perm(a45l, a67l, 0x5410));
+                o[1] = make_uint2(__byte_perm(a01l, a23l, 0x7632), __byte_perm(a45l, a67l, 0x7632));
+                o[2] = make_uint2(__byte_perm(a01h, a23h, 0x5410), __byte_perm(a45h, a67h, 0x5410));
+                o[3] = make_uint2(__byte_perm(a01h, a23h, 0x7632), __byte_perm(a45h, a67h, 0x7632));
+                // grouped blocks always write their full 32-byte padded extent
+#pragma unroll
+                for (int jj = 0; jj < 4; jj++) {
+                    const int64_t c = c0 + qa * 4 + jj;
+                    if (c < a.cols)
+                        *reinterpret_cast<uint2 *>(a.q_colT + c * a.ld_colT + rb.out_col0 + (q & 3) * 8) = o[jj];
+                }
+            }
+        }
+        __syncthreads();
+    }
+    if constexpr (DELAYED) block_amax_atomic(fold_absmax(amax_acc), a.amax_out, red);
+}
+
 // ROWWISE scale buffers, in place: mode 0 turns the accumulated amax into
 // the scale (before the cast pass), mode 1 turns the scale into scale_inv =
 // 1 / scale (after it), mode 2 turns the amax into scale_inv directly.
@@ -721,9 +895,30 @@ static int blocks_for(K kernel, size_t dyn_smem, int64_t n_tiles, bool persisten
     return (int)g;
 }
 
+template <int FMT, int SMODE, bool DELAYED>
+static fp8_status_t launch_grouped_cast(const QArgs &a, int layouts, size_t group_smem, cudaStream_t st)
+{
+    const int64_t n_tiles = (a.n_row_blocks + GT_BLOCKS - 1) / GT_BLOCKS * ((a.cols + GT_COLS - 1) / GT_COLS);
+    if (layouts == (FP8_LAYOUT_ROW | FP8_LAYOUT_COLT)) {
+        auto k = grouped_cast_kernel<FMT, SMODE, DELAYED, true, true>;
+        k<<<blocks_for(k, group_smem, n_tiles, true), QT_THREADS, group_smem, st>>>(a);
+    } else if (layouts == FP8_LAYOUT_ROW) {
+        auto k = grouped_cast_kernel<FMT, SMODE, DELAYED, true, false>;
+        k<<<blocks_for(k, group_smem, n_tiles, true), QT_THREADS, group_smem, st>>>(a);
+    } else {
+        auto k = grouped_cast_kernel<FMT, SMODE, DELAYED, false, true>;
+        k<<<blocks_for(k, group_smem, n_tiles, true), QT_THREADS, group_smem, st>>>(a);
+    }
+    return check_launch();
+}
+
 template <int FMT, int RB, int SMODE, bool DELAYED>
 static fp8_status_t launch_cast(const QArgs &a, int layouts, size_t group_smem, cudaStream_t st)
 {
+    if (a.offsets) return launch_grouped_cast<FMT, SMODE, DELAYED>(a, layouts, group_smem, st);
+    if constexpr (RB == 32) {
+        return FP8_ERR_INVALID_ARG;  // 32-row blocks are the grouped layout's; plain tensors use 64
+    } else {
     const int64_t n_tiles = a.n_row_blocks * a.n_col_chunks;
     const size_t smem = (size_t)RB * QT_PITCH + group_smem;
     if (layouts == (FP8_LAYOUT_ROW | FP8_LAYOUT_COLT)) {
@@ -737,6 +932,7 @@ static fp8_status_t launch_cast(const QArgs &a, int layouts, size_t group_smem, 
         k<<<blocks_for(k, smem, n_tiles, a.offsets != nullptr), QT_THREADS, smem, st>>>(a);
     }
     return check_launch();
+    }
 }
 
 template <int FMT, int RB>

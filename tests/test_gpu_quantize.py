@@ -149,6 +149,18 @@ def test_quantize_grouped(orc, sizes, kind):
     assert q.ld_colT >= ref["q_colT"].shape[1]
 
 
+@pytest.mark.parametrize("layouts", [1, 2])
+@pytest.mark.parametrize("kind", [0, 1, 2])
+def test_quantize_grouped_single_layout(orc, layouts, kind):
+    """One layout at a time, every recipe, groups that straddle the cast
+    pass's 128-row tiles (sizes 0-200, 72 columns: one full and one partial
+    64-column chunk)."""
+    sizes = [5, 0, 33, 1, 0, 40, 128, 200, 97]
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    x = gen_x((int(off[-1]), 72), seed=7 + kind + layouts)
+    compare(orc, x, 0, kind, layouts=layouts, scale=96.0, offsets=off, what=f"grouped layouts {layouts} kind {kind}")
+
+
 def test_grouped_bad_offsets_reported():
     x = gen_x((40, 64), seed=1).to(DEV)
     off = torch.tensor([0, 30, 20, 40], dtype=torch.int32, device=DEV)   # decreasing: malformed
