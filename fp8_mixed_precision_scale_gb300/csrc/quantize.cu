@@ -703,7 +703,7 @@ constexpr int GT_ROWS = 32 * GT_BLOCKS;
 __device__ __forceinline__ int gt_word(int r, int w) { return r * (GT_COLS / 4) + (w ^ ((r >> 3) & 15)); }
 
 template <int FMT, int SMODE, bool DELAYED, bool DO_ROW, bool DO_COLT>
-__global__ void __launch_bounds__(QT_THREADS) grouped_cast_kernel(QArgs a)
+__global__ void __launch_bounds__(QT_THREADS, 6) grouped_cast_kernel(QArgs a)
 {
     extern __shared__ __align__(16) unsigned char dsm[];
     int32_t *poff = reinterpret_cast<int32_t *>(dsm);
