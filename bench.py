@@ -27,6 +27,8 @@ Other workloads (same JSON line, their own config):
                  and gradient blocks, 128x128 weight blocks, power-of-two scales)
   bw_quantize    the blockwise quantize of dY_gate (1x128 blocks)
   rowwise_quantize  the rowwise (current scaling) quantize of dY_gate
+  rowwise_resident  the single-launch rowwise quantize of X [8192, 4096],
+                 also timed against the two-pass path
   sweep          the delayed quantize (E4M3, both layouts) of 2^20 .. 2^30
                  elements, GB/s against size
   gemm, quantize single kernels of the default step, for profiling
@@ -373,6 +375,13 @@ class RowwiseStep:
         r, c = t.shape
         self.fp8.fp8_quantize(t, r, c, c, self.fmt[k], self.recipe, 3, None, None, q["row"], q["srow"],
                               q["colT"], r, q["scol"])
+
+    def quantize_resident(self, k):
+        """The same quantize through the single-launch entry point."""
+        t, q = self.inp[k], self.q[k]
+        r, c = t.shape
+        self.fp8.fp8_quantize_rowwise_resident(t, r, c, c, self.fmt[k], 0, 3, None, q["row"], q["srow"],
+                                               q["colT"], r, q["scol"])
 
     def gemm(self, a, al, b, bl, out):
         qa, qb = self.q[a], self.q[b]
@@ -783,7 +792,7 @@ def run_gpu(args, rank, world, local_rank):
     fp8_peak = 2.0 * bf16_sust               # FP8 dense = 2x bf16 dense (nominal 4.5 vs 2.25 PFLOP/s)
 
     if args.workload in ("gemm", "quantize", "grouped_m", "grouped_k", "quantize_grouped", "mx_gemm", "mx_quantize",
-                         "mx_permute", "mx_swiglu", "bw_quantize", "rowwise_quantize"):
+                         "mx_permute", "mx_swiglu", "bw_quantize", "rowwise_quantize", "rowwise_resident"):
         run_single_kernel(args, dev, rank)
         return
     if args.workload == "sweep":
@@ -1110,6 +1119,11 @@ def run_single_kernel(args, dev, rank):
         step = RowwiseStep(dev, 1, keys=("dy_gate",))
         fn = lambda: step.quantize("dy_gate")  # noqa: E731
         work, unit = quantize_bytes(step.inp["dy_gate"].shape) / 1e9, "GB/s (algorithmic)"
+    elif args.workload == "rowwise_resident":
+        step = RowwiseStep(dev, 1, keys=("x",))
+        fn = lambda: step.quantize_resident("x")  # noqa: E731
+        work, unit = quantize_bytes(step.inp["x"].shape) / 1e9, "GB/s (algorithmic)"
+        unfused = lambda: step.quantize("x")  # noqa: E731
     elif args.workload in ("mx_quantize", "bw_quantize"):
         step = MxStep(dev, 1, keys=("dy_gate",), outs=(), recipe="mxfp8" if args.workload == "mx_quantize" else "blockwise")
         fn = lambda: step.quantize("dy_gate")  # noqa: E731
@@ -1138,7 +1152,7 @@ def run_single_kernel(args, dev, rank):
     ms = a.elapsed_time(b) / args.steps
     line = {"workload": args.workload, "ms_per_launch": round(ms, 4), "value": round(work / (ms * 1e-3), 1),
             "unit": unit, "launches": args.steps}
-    if unfused is not None:   # the same result through the unfused chain (torch prologue, then the quantize)
+    if unfused is not None:   # the same result through the unfused chain of separate launches
         for _ in range(3):
             unfused()
         torch.cuda.synchronize()
@@ -1192,7 +1206,7 @@ def main():
     ap.add_argument("--workload", default="llama_mlp",
                     choices=["llama_mlp", "llama_rowwise", "llama_mxfp8", "llama_blockwise", "moe", "moe_mxfp8", "flux",
                              "sweep",
-                             "gemm", "quantize", "bw_quantize", "rowwise_quantize",
+                             "gemm", "quantize", "bw_quantize", "rowwise_quantize", "rowwise_resident",
                              "grouped_m", "grouped_k", "quantize_grouped", "mx_gemm", "mx_quantize", "mx_permute",
                              "mx_swiglu"],
                     help="llama_mlp: the whole fwd+bwd FP8 step of the Llama-3-8B MLP (default); see the "

@@ -40,7 +40,8 @@ LIB_PATH = os.path.join(_HERE, "libfp8gb.so")
 EXPORTED = ("fp8_quantize", "fp8_update_amax_history", "fp8_scaled_gemm", "fp8_grouped_gemm",
             "fp8_group_padded_offsets", "fp8_sync_status", "fp8_selftest_bounded_wait", "fp8_status_string",
             "fp8_last_cuda_error", "fp8_version", "fp8_mx_scale_bytes", "fp8_mx_quantize", "fp8_mx_gemm",
-            "fp8_mx_grouped_gemm", "fp8_mx_permute_quantize", "fp8_mx_swiglu_quantize", "fp8_blockwise_quantize")
+            "fp8_mx_grouped_gemm", "fp8_mx_permute_quantize", "fp8_mx_swiglu_quantize", "fp8_blockwise_quantize",
+            "fp8_quantize_rowwise_resident")
 MX_BLOCK = 32
 MX_GROUP_ALIGN = 128
 
@@ -97,6 +98,8 @@ def load_library():
             lib.fp8_quantize.restype = i32
             lib.fp8_quantize.argtypes = [P, i64, i64, i64, i32, ctypes.POINTER(fp8_recipe_t), i32, P, P, P, P, P,
                                          i64, P, P, i32, P]
+            lib.fp8_quantize_rowwise_resident.restype = i32
+            lib.fp8_quantize_rowwise_resident.argtypes = [P, i64, i64, i64, i32, i32, i32, P, P, P, P, i64, P, P]
             lib.fp8_update_amax_history.restype = i32
             lib.fp8_update_amax_history.argtypes = [P, P, P, P, i32, i32, i32, i32, P, P]
             lib.fp8_scaled_gemm.restype = i32
@@ -237,6 +240,16 @@ def fp8_mx_swiglu_quantize(gate_up, rows, F, ld, fmt, layouts, h, ld_h, q_row, s
     return rc
 
 
+def fp8_quantize_rowwise_resident(x, rows, cols, ld_x, fmt, margin, layouts, amax_out, q_row, scale_inv_row, q_colT,
+                                  ld_colT, scale_inv_col, stream=None, check=True):
+    rc = load_library().fp8_quantize_rowwise_resident(_p(x), rows, cols, ld_x, fmt, margin, layouts, _p(amax_out),
+                                                      _p(q_row), _p(scale_inv_row), _p(q_colT), ld_colT,
+                                                      _p(scale_inv_col), _stream(stream))
+    if check:
+        _check(rc, "fp8_quantize_rowwise_resident")
+    return rc
+
+
 def fp8_blockwise_quantize(x, rows, cols, ld_x, fmt, block_rows, layouts, q_row, s_row, q_colT, ld_colT, s_col,
                            stream=None, check=True):
     rc = load_library().fp8_blockwise_quantize(_p(x), rows, cols, ld_x, fmt, block_rows, layouts, _p(q_row),
@@ -313,6 +326,27 @@ def quantize(x: torch.Tensor, fmt: int, recipe: Recipe, layouts: int = LAYOUT_RO
         sc = torch.empty(nsc, dtype=torch.float32, device=dev)
     fp8_quantize(x, rows, cols, x.stride(0), fmt, recipe, layouts, scale_in, amax_out, q_row, sr, q_colT, ld_colT,
                  sc, group_offsets, G, stream)
+    return Quantized(q_row, sr, q_colT, sc, ld_colT)
+
+
+def quantize_rowwise_resident(x: torch.Tensor, fmt: int, margin: int = 0, layouts: int = LAYOUT_ROW | LAYOUT_COLT,
+                              amax_out=None, stream=None) -> Quantized:
+    """The rowwise recipe of quantize() for a plain CUDA bf16 [rows, cols]
+    tensor in one cooperative launch (same results; faster for tensors that
+    fit in L2).  Not to be run concurrently on two streams."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    rows, cols = x.shape
+    dev = x.device
+    ld_colT = max(16, (rows + 15) // 16 * 16)
+    q_row = sr = q_colT = sc = None
+    if layouts & LAYOUT_ROW:
+        q_row = torch.empty((rows, cols), dtype=torch.uint8, device=dev)
+        sr = torch.empty(max(rows, 1), dtype=torch.float32, device=dev)
+    if layouts & LAYOUT_COLT:
+        q_colT = torch.empty((cols, ld_colT), dtype=torch.uint8, device=dev)
+        sc = torch.empty(cols, dtype=torch.float32, device=dev)
+    fp8_quantize_rowwise_resident(x, rows, cols, x.stride(0), fmt, margin, layouts, amax_out, q_row, sr, q_colT,
+                                  ld_colT, sc, stream)
     return Quantized(q_row, sr, q_colT, sc, ld_colT)
 
 

@@ -26,6 +26,7 @@ enum : unsigned int {
     ERR_SELFTEST_WAIT = 16u,
     ERR_BAD_OFFSETS = 32u,
     ERR_BAD_INDEX = 64u,  // a gather index outside the source rows
+    ERR_GRID_WAIT = 128u, // a grid-wide barrier of a cooperative launch gave up
 };
 
 __device__ __forceinline__ void record_error(unsigned int *err, unsigned int bits)

@@ -278,31 +278,66 @@ __global__ void __launch_bounds__(QT_THREADS) amax_kernel(QArgs a)
 // reduced per tile (shuffles, then shared memory across the 8 warps) and
 // flushed with one relaxed atomic per column per tile.
 // ---------------------------------------------------------------------------
-template <int RB>
+// L2 eviction-priority hints for the single-launch rowwise path: the amax
+// pass marks x evict-last so the cast pass finds it in L2; the cast pass
+// reads x for the last time and writes its outputs evict-first.
+__device__ __forceinline__ uint64_t l2_policy_evict_last()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint4 ld_nc_hint(const void *ptr, uint64_t pol)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(ptr), "l"(pol));
+    return v;
+}
+
+__device__ __forceinline__ void st_hint(void *ptr, uint2 v, uint64_t pol)
+{
+    asm volatile("st.global.L2::cache_hint.v2.u32 [%0], {%1, %2}, %3;" ::"l"(ptr), "r"(v.x), "r"(v.y), "l"(pol)
+                 : "memory");
+}
+
+template <int RB, bool HINTS = false>
 __device__ __forceinline__ void dense_tile_load(const QArgs &a, int64_t tile, int cg, int roff, uint4 (&v)[RB / 16])
 {
+    uint64_t pol = 0;
+    if constexpr (HINTS) pol = l2_policy_evict_last();
     const int64_t b = tile / a.n_col_chunks;
     const int64_t col = (tile % a.n_col_chunks) * QT_COLS + cg * 8;
     const int64_t row0 = b * RB;
 #pragma unroll
     for (int i = 0; i < RB / 16; i++) {
         const int64_t r = row0 + i * 16 + roff;
-        if (col < a.cols && r < a.rows)
-            v[i] = __ldg(reinterpret_cast<const uint4 *>(a.x + r * a.ld_x + col));
-        else
+        if (col < a.cols && r < a.rows) {
+            if constexpr (HINTS)
+                v[i] = ld_nc_hint(a.x + r * a.ld_x + col, pol);
+            else
+                v[i] = __ldg(reinterpret_cast<const uint4 *>(a.x + r * a.ld_x + col));
+        } else
             v[i] = make_uint4(0, 0, 0, 0);
     }
 }
 
-template <int RB>
-__global__ void __launch_bounds__(QT_THREADS) dense_rowcol_amax_kernel(QArgs a, int64_t tiles_per_block)
+// the run of tiles [first, last) of one block
+template <int RB, bool HINTS = false>
+__device__ __forceinline__ void dense_rowcol_amax_run(const QArgs &a, int64_t first, int64_t last)
 {
     __shared__ uint32_t red[QT_THREADS / 32];
     __shared__ uint32_t colw[QT_THREADS / 32][16][4];  // per warp: 16 column groups x 4 packed words
     const int t = threadIdx.x, cg = t & 15, roff = t >> 4;
-    const int64_t n_tiles = a.n_row_blocks * a.n_col_chunks;
-    const int64_t first = (int64_t)blockIdx.x * tiles_per_block;
-    const int64_t last = first + tiles_per_block < n_tiles ? first + tiles_per_block : n_tiles;
     uint32_t tensor_acc = 0;
     uint32_t racc[RB / 16];
 #pragma unroll
@@ -323,12 +358,12 @@ __global__ void __launch_bounds__(QT_THREADS) dense_rowcol_amax_kernel(QArgs a, 
     };
 
     uint4 nv[RB / 16];
-    if (first < last) dense_tile_load<RB>(a, first, cg, roff, nv);
+    if (first < last) dense_tile_load<RB, HINTS>(a, first, cg, roff, nv);
     for (int64_t tile = first; tile < last; tile++) {
         uint4 v[RB / 16];
 #pragma unroll
         for (int i = 0; i < RB / 16; i++) v[i] = nv[i];
-        if (tile + 1 < last) dense_tile_load<RB>(a, tile + 1, cg, roff, nv);
+        if (tile + 1 < last) dense_tile_load<RB, HINTS>(a, tile + 1, cg, roff, nv);
         const int64_t b = tile / a.n_col_chunks;
         const int64_t c0 = (tile % a.n_col_chunks) * QT_COLS;
         if (b != cur_b) {  // warp-uniform: the whole block moves to the next row block
@@ -376,6 +411,15 @@ __global__ void __launch_bounds__(QT_THREADS) dense_rowcol_amax_kernel(QArgs a, 
     }
     if (cur_b >= 0) flush_rows(cur_b);
     if (a.amax_out) block_amax_atomic(tensor_acc, a.amax_out, red);
+}
+
+template <int RB>
+__global__ void __launch_bounds__(QT_THREADS) dense_rowcol_amax_kernel(QArgs a, int64_t tiles_per_block)
+{
+    const int64_t n_tiles = a.n_row_blocks * a.n_col_chunks;
+    const int64_t first = (int64_t)blockIdx.x * tiles_per_block;
+    const int64_t last = first + tiles_per_block < n_tiles ? first + tiles_per_block : n_tiles;
+    dense_rowcol_amax_run<RB>(a, first, last);
 }
 
 // ---------------------------------------------------------------------------
@@ -529,10 +573,16 @@ __global__ void __launch_bounds__(QT_THREADS) rowcol_amax_kernel(QArgs a)
 //   SMODE 1: ROWWISE -- row scales from the row amax, column scales from the
 //            (group, column) amax.
 // ---------------------------------------------------------------------------
-template <int FMT, int RB, int SMODE, bool DELAYED, bool DO_ROW, bool DO_COLT>
-__global__ void __launch_bounds__(QT_THREADS) cast_kernel(QArgs a)
+// the tiles blockIdx.x, blockIdx.x + gridDim.x, ... , or with run_last >= 0
+// the tiles run_last, run_last - 1, ..., run_first (a block's own run, newest
+// first); dsm: the block's dynamic shared memory (RB * QT_PITCH bytes, then
+// the grouped offsets)
+template <int FMT, int RB, int SMODE, bool DELAYED, bool DO_ROW, bool DO_COLT, bool HINTS = false>
+__device__ __forceinline__ void cast_run(const QArgs &a, unsigned char *dsm, int64_t run_first = 0,
+                                         int64_t run_last = -1)
 {
-    extern __shared__ __align__(16) unsigned char dsm[];
+    uint64_t pol = 0;
+    if constexpr (HINTS) pol = l2_policy_evict_first();
     uint8_t *tileT = dsm;                                                    // [RB][QT_PITCH]
     int32_t *poff = reinterpret_cast<int32_t *>(dsm + RB * QT_PITCH);       // grouped only
     __shared__ float srow[RB];
@@ -562,7 +612,9 @@ __global__ void __launch_bounds__(QT_THREADS) cast_kernel(QArgs a)
     const int t = threadIdx.x, cg = t & 15, roff = t >> 4;
     const int64_t n_tiles = a.n_row_blocks * a.n_col_chunks;
     uint32_t amax_acc = 0;
-    for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+    const bool by_run = run_last >= 0;
+    for (int64_t tile = by_run ? run_last : blockIdx.x; by_run ? tile >= run_first : tile < n_tiles;
+         tile = by_run ? tile - 1 : tile + gridDim.x) {
         const int64_t b = tile / a.n_col_chunks;
         const int64_t c0 = (tile % a.n_col_chunks) * QT_COLS;
         const RowBlock rb = row_block<RB>(a, b, poff);
@@ -574,10 +626,14 @@ __global__ void __launch_bounds__(QT_THREADS) cast_kernel(QArgs a)
 #pragma unroll
         for (int i = 0; i < RB / 16; i++) {
             const int r = i * 16 + roff;
-            if (col_ok && r < rb.valid)
-                v[i] = __ldg(reinterpret_cast<const uint4 *>(a.x + (rb.in_row0 + r) * a.ld_x + col));
-            else
+            if (col_ok && r < rb.valid) {
+                if constexpr (HINTS)
+                    v[i] = ld_nc_hint(a.x + (rb.in_row0 + r) * a.ld_x + col, pol);
+                else
+                    v[i] = __ldg(reinterpret_cast<const uint4 *>(a.x + (rb.in_row0 + r) * a.ld_x + col));
+            } else {
                 v[i] = make_uint4(0, 0, 0, 0);
+            }
         }
         if constexpr (SMODE == 1) {
             // per-tile scales from the amax accumulated by pass 1
@@ -630,8 +686,12 @@ __global__ void __launch_bounds__(QT_THREADS) cast_kernel(QArgs a)
             }
             const bool ok = col_ok && r < rb.valid;
             if constexpr (DO_ROW) {
-                if (ok)
-                    *reinterpret_cast<uint2 *>(a.q_row + (rb.in_row0 + r) * a.cols + col) = make_uint2(rowb0, rowb1);
+                if (ok) {
+                    if constexpr (HINTS)
+                        st_hint(a.q_row + (rb.in_row0 + r) * a.cols + col, make_uint2(rowb0, rowb1), pol);
+                    else
+                        *reinterpret_cast<uint2 *>(a.q_row + (rb.in_row0 + r) * a.cols + col) = make_uint2(rowb0, rowb1);
+                }
             }
             if constexpr (DO_COLT) {
                 uint32_t *dst = reinterpret_cast<uint32_t *>(tileT + r * QT_PITCH + cg * 8);
@@ -669,7 +729,10 @@ __global__ void __launch_bounds__(QT_THREADS) cast_kernel(QArgs a)
                     if (c >= a.cols) break;
                     uint8_t *dst = a.q_colT + c * a.ld_colT + rb.out_col0 + r0;
                     if (r0 + 8 <= lim) {
-                        *reinterpret_cast<uint2 *>(dst) = o[jj];
+                        if constexpr (HINTS)
+                            st_hint(dst, o[jj], pol);
+                        else
+                            *reinterpret_cast<uint2 *>(dst) = o[jj];
                     } else {
                         const uint64_t bits = ((uint64_t)o[jj].y << 32) | o[jj].x;
                         for (int k = 0; k < lim - r0; k++) dst[k] = (uint8_t)(bits >> (8 * k));
@@ -682,6 +745,13 @@ __global__ void __launch_bounds__(QT_THREADS) cast_kernel(QArgs a)
         }
     }
     if constexpr (DELAYED) block_amax_atomic(fold_absmax(amax_acc), a.amax_out, red);
+}
+
+template <int FMT, int RB, int SMODE, bool DELAYED, bool DO_ROW, bool DO_COLT>
+__global__ void __launch_bounds__(QT_THREADS) cast_kernel(QArgs a)
+{
+    extern __shared__ __align__(16) unsigned char dsm[];
+    cast_run<FMT, RB, SMODE, DELAYED, DO_ROW, DO_COLT>(a, dsm);
 }
 
 // ---------------------------------------------------------------------------
@@ -870,6 +940,88 @@ __global__ void scales_kernel(float *sinv_row, int64_t n_row, float *sinv_col, i
         const float v = *p;
         *p = mode == 0 ? scale_from_amax(v, fmax, margin)
                        : (mode == 1 ? recip_rn(v) : recip_rn(scale_from_amax(v, fmax, margin)));
+    }
+}
+
+// ---------------------------------------------------------------------------
+// The ROWWISE recipe on a plain tensor in one cooperative launch: zero the
+// amax accumulators, amax pass, cast pass, scale_inv; grid-wide barriers in
+// between.  For a tensor that fits in L2 the cast pass re-reads x from L2,
+// and the whole quantize is one launch instead of six (three clears, two
+// passes, the scale conversion).
+//
+// The barrier counter lives in a file-scope device array (no allocation):
+// the host clears it on the stream before each launch, and barrier k
+// completes when the counter reaches k * gridDim.x.  Every block of a
+// cooperative launch is resident, so every block reaches every barrier; the
+// wait is still bounded and records ERR_GRID_WAIT if it gives up.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned int g_resident_scratch[64];
+
+constexpr uint64_t GRID_WAIT_LIMIT_NS = 2000000000ull;
+
+__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int *p)
+{
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ bool grid_sync(unsigned int *count, unsigned int k, unsigned int *err)
+{
+    __shared__ int s_ok;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        atomicAdd(count, 1u);
+        const unsigned int target = k * gridDim.x;
+        const uint64_t t0 = global_timer_ns();
+        int ok = 1;
+        for (uint32_t it = 0; ld_acquire_gpu(count) < target; ++it) {
+            if ((it & 255u) == 255u && global_timer_ns() - t0 > GRID_WAIT_LIMIT_NS) {
+                record_error(err, ERR_GRID_WAIT);
+                ok = 0;
+                break;
+            }
+        }
+        __threadfence();
+        s_ok = ok;
+    }
+    __syncthreads();
+    return s_ok != 0;
+}
+
+template <int FMT, bool DO_ROW, bool DO_COLT>
+__global__ void __launch_bounds__(QT_THREADS, 4) rowwise_resident_kernel(QArgs a, int64_t tiles_per_block)
+{
+    extern __shared__ __align__(16) unsigned char dsm[];
+    unsigned int *count = g_resident_scratch;
+    const int64_t n_row = DO_ROW ? a.rows : 0, n_col = DO_COLT ? a.cols : 0;
+    const int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x, stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = i0; i < n_row + n_col; i += stride) {
+        if (i < n_row)
+            a.sinv_row[i] = 0.0f;
+        else
+            a.sinv_col[i - n_row] = 0.0f;
+    }
+    if (i0 == 0 && a.amax_out) a.amax_out[0] = 0.0f;
+    if (!grid_sync(count, 1, a.err)) return;
+
+    const int64_t n_tiles = a.n_row_blocks * a.n_col_chunks;
+    const int64_t first = (int64_t)blockIdx.x * tiles_per_block;
+    const int64_t last = first + tiles_per_block < n_tiles ? first + tiles_per_block : n_tiles;
+    dense_rowcol_amax_run<64, true>(a, first, last);
+    if (!grid_sync(count, 2, a.err)) return;
+
+    // the cast pass walks the block's own run backwards: the tiles the amax
+    // pass read last are the likeliest to still be in L2
+    cast_run<FMT, 64, 1, false, DO_ROW, DO_COLT, true>(a, dsm, first, last - 1);
+    if (!grid_sync(count, 3, a.err)) return;
+
+    const float fmax = fp8_max_of(FMT);
+    for (int64_t i = i0; i < n_row + n_col; i += stride) {
+        float *p = i < n_row ? a.sinv_row + i : a.sinv_col + (i - n_row);
+        *p = recip_rn(scale_from_amax(*p, fmax, a.margin));
     }
 }
 
@@ -1080,4 +1232,90 @@ extern "C" fp8_status_t fp8_quantize(const void *x_bf16, int64_t rows, int64_t c
     if (fmt == FP8_E4M3FNUZ) return run_quantize<FP8_E4M3FNUZ, 64>(a, recipe->kind, layouts, st);
     if (fmt == FP8_E5M2FNUZ) return run_quantize<FP8_E5M2FNUZ, 64>(a, recipe->kind, layouts, st);
     return run_quantize<FP8_E4M3FN, 64>(a, recipe->kind, layouts, st);
+}
+
+namespace fp8gb {
+
+template <int FMT, bool DO_ROW, bool DO_COLT>
+static fp8_status_t launch_resident(QArgs a, cudaStream_t st)
+{
+    auto k = rowwise_resident_kernel<FMT, DO_ROW, DO_COLT>;
+    const size_t smem = (size_t)64 * QT_PITCH;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, QT_THREADS, smem) != cudaSuccess || per_sm < 1)
+        return cuda_fail();
+    const int64_t n_tiles = a.n_row_blocks * a.n_col_chunks;
+    int64_t grid = (int64_t)num_sms() * per_sm;
+    if (grid > n_tiles) grid = n_tiles;
+    if (grid < 1) grid = 1;
+    int64_t tiles_per_block = (n_tiles + grid - 1) / grid;
+    void *scratch = nullptr;
+    if (cudaGetSymbolAddress(&scratch, g_resident_scratch) != cudaSuccess) return cuda_fail();
+    if (cudaMemsetAsync(scratch, 0, sizeof(unsigned int), st) != cudaSuccess) return cuda_fail();
+    void *args[] = {&a, &tiles_per_block};
+    const cudaError_t e = cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(k), dim3((unsigned)grid),
+                                                      dim3(QT_THREADS), args, smem, st);
+    if (e != cudaSuccess) return cuda_fail_with(e);
+    return FP8_OK;
+}
+
+template <int FMT>
+static fp8_status_t run_resident(const QArgs &a, int layouts, cudaStream_t st)
+{
+    if (layouts == (FP8_LAYOUT_ROW | FP8_LAYOUT_COLT)) return launch_resident<FMT, true, true>(a, st);
+    if (layouts == FP8_LAYOUT_ROW) return launch_resident<FMT, true, false>(a, st);
+    return launch_resident<FMT, false, true>(a, st);
+}
+
+}  // namespace fp8gb
+
+extern "C" fp8_status_t fp8_quantize_rowwise_resident(const void *x_bf16, int64_t rows, int64_t cols, int64_t ld_x,
+                                                      int fmt, int margin, int layouts, float *amax_out,
+                                                      uint8_t *q_row, float *scale_inv_row, uint8_t *q_colT,
+                                                      int64_t ld_colT, float *scale_inv_col, void *stream)
+{
+    // ---- validation (host only; nothing is launched on failure) ----
+    if (!x_bf16 && rows > 0) return FP8_ERR_INVALID_ARG;
+    if (rows < 0 || cols < 1 || ld_x < cols) return FP8_ERR_INVALID_ARG;
+    if (fmt != FP8_E4M3FN && fmt != FP8_E5M2 && fmt != FP8_E4M3FNUZ && fmt != FP8_E5M2FNUZ)
+        return FP8_ERR_INVALID_ARG;
+    if (margin < 0 || margin > 64) return FP8_ERR_INVALID_ARG;
+    if (layouts < 1 || layouts > 3) return FP8_ERR_INVALID_ARG;
+    if ((layouts & FP8_LAYOUT_ROW) && rows > 0 && (!q_row || !scale_inv_row)) return FP8_ERR_INVALID_ARG;
+    if ((layouts & FP8_LAYOUT_COLT) && (!q_colT || !scale_inv_col)) return FP8_ERR_INVALID_ARG;
+    if (cols % 8 != 0 || ld_x % 8 != 0 || !aligned(x_bf16, 16)) return FP8_ERR_ALIGNMENT;
+    if ((layouts & FP8_LAYOUT_ROW) && !aligned(q_row, 8)) return FP8_ERR_ALIGNMENT;
+    if (layouts & FP8_LAYOUT_COLT) {
+        if (!aligned(q_colT, 16) || ld_colT % 16 != 0) return FP8_ERR_ALIGNMENT;
+        if (ld_colT < rows) return FP8_ERR_INVALID_ARG;
+    }
+    if (rows > ((int64_t)1 << 40) || cols > ((int64_t)1 << 31)) return FP8_ERR_INVALID_ARG;
+    if (rows == 0) return FP8_OK;
+
+    QArgs a;
+    a.x = static_cast<const uint16_t *>(x_bf16);
+    a.rows = rows;
+    a.cols = cols;
+    a.ld_x = ld_x;
+    a.q_row = q_row;
+    a.q_colT = q_colT;
+    a.ld_colT = (layouts & FP8_LAYOUT_COLT) ? ld_colT : 0;
+    a.sinv_row = (layouts & FP8_LAYOUT_ROW) ? scale_inv_row : nullptr;
+    a.sinv_col = (layouts & FP8_LAYOUT_COLT) ? scale_inv_col : nullptr;
+    a.scale_in = nullptr;
+    a.amax_out = amax_out;
+    a.offsets = nullptr;
+    a.err = device_error_word();
+    a.G = 0;
+    a.margin = margin;
+    a.n_col_chunks = (cols + QT_COLS - 1) / QT_COLS;
+    a.n_row_blocks = (rows + 63) / 64;
+    a.scales_ready = 0;
+    a.sup_blocks = SUP_BLOCKS;
+    a.sup_chunks = SUP_CHUNKS;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (fmt == FP8_E5M2) return run_resident<FP8_E5M2>(a, layouts, st);
+    if (fmt == FP8_E4M3FNUZ) return run_resident<FP8_E4M3FNUZ>(a, layouts, st);
+    if (fmt == FP8_E5M2FNUZ) return run_resident<FP8_E5M2FNUZ>(a, layouts, st);
+    return run_resident<FP8_E4M3FN>(a, layouts, st);
 }

@@ -145,6 +145,37 @@ FP8GB_API fp8_status_t fp8_quantize(const void *x_bf16, int64_t rows, int64_t co
                           float *scale_inv_col, const int32_t *group_offsets, int num_groups, void *stream);
 
 /*
+ * fp8_quantize_rowwise_resident -- the ROWWISE recipe of fp8_quantize for a
+ * plain (ungrouped) tensor in one cooperative launch ("FP8 Training on AMD
+ * GPUs with TorchTitan and TorchAO": rowwise FP8 and the colwise-scales
+ * kernel; "How PyTorch FP8 Optimizations on AMD GPUs Reduce LLM Cost ...",
+ * What Happened: fused quantize kernels instead of chains of memory-bound
+ * launches).  The results are those of fp8_quantize with recipe kind
+ * FP8_RECIPE_ROWWISE, margin `margin` and no groups, byte for byte: q_row,
+ * q_colT, scale_inv_row [rows], scale_inv_col [cols] and the optional
+ * amax_out [1] have the meanings, layouts and alignment rules given there.
+ *
+ * One launch clears the amax accumulators, runs the row / column amax pass,
+ * the cast pass and the scale_inv conversion, with grid-wide barriers in
+ * between (all blocks of a cooperative launch are resident; each wait is
+ * bounded and a wait that gives up is reported as FP8_ERR_TIMEOUT by
+ * fp8_sync_status()).  For a tensor that fits in L2 (on GB300, up to about
+ * 96 MB of bf16) the cast pass reads x back from L2; any size is correct.
+ *
+ * The barriers count on a device-wide counter held in a static array of the
+ * library (nothing is allocated); the call clears it on `stream` before its
+ * launch.  Calls of this entry point must therefore not run concurrently on
+ * different streams of one device; calls on one stream, and concurrent
+ * calls of every other entry point, are fine.
+ *
+ * Returns FP8_ERR_CUDA if the cooperative launch is refused.
+ */
+FP8GB_API fp8_status_t fp8_quantize_rowwise_resident(const void *x_bf16, int64_t rows, int64_t cols, int64_t ld_x,
+                                                     int fmt, int margin, int layouts, float *amax_out,
+                                                     uint8_t *q_row, float *scale_inv_row, uint8_t *q_colT,
+                                                     int64_t ld_colT, float *scale_inv_col, void *stream);
+
+/*
  * fp8_update_amax_history -- delayed-scaling update for n tensors in one
  * launch ("FP8 training for Flux models": fp8_amax_history_len,
  * fp8_amax_compute_algo, fp8_margin; its verification list names a "fused
