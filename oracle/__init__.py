@@ -60,6 +60,8 @@ def _load():
             lib = ctypes.CDLL(build())
             P = ctypes.c_void_p
             i64, i32, f32, f64 = ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_double
+            lib.orc_set_threads.restype = None
+            lib.orc_set_threads.argtypes = [i32]
             lib.orc_fp8_decode.restype = f64
             lib.orc_fp8_decode.argtypes = [i32, i32]
             lib.orc_fp8_encode.restype = i32
@@ -386,3 +388,8 @@ def blockwise_quantize(x_bits, fmt, block_rows, layouts=LAYOUT_ROW | LAYOUT_COLT
     _load().orc_blockwise_quantize(_ptr(x), rows, cols, cols, fmt, block_rows, layouts, _ptr(q_row), _ptr(s_row),
                                    _ptr(q_colT), _ptr(s_col))
     return dict(q_row=q_row, s_row=s_row, q_colT=q_colT, s_col=s_col)
+
+
+def set_threads(n: int) -> None:
+    """Threads of the oracle's parallel outer loops (results do not depend on it)."""
+    _load().orc_set_threads(int(n))

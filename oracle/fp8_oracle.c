@@ -55,6 +55,20 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Threads for the parallel outer loops (the timed baseline also runs on one
+ * core); no effect on any result: every loop iteration is independent. */
+void orc_set_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
 
 #define ORC_E4M3FN 0
 #define ORC_E5M2 1
