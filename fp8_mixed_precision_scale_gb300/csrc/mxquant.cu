@@ -84,8 +84,9 @@ __device__ __forceinline__ float mx_inv_scale(uint32_t code)
 }
 
 // Exclusive prefix of roundup(m_e, FP8_MX_GROUP_ALIGN) over the groups, by
-// warp 0 into shared memory; flags malformed offsets and a padded total that
-// does not fit ld_colT.
+// warp 0 into shared memory poff[0 .. G], followed by a copy of the offsets
+// (poff[G + 1 .. 2G + 1]) so tile lookups never wait on global memory; flags
+// malformed offsets and a padded total that does not fit ld_colT.
 __device__ void mx_padded_offsets(const MxArgs &a, int32_t *poff, int *bad)
 {
     if (threadIdx.x >= 32) return;
@@ -107,14 +108,17 @@ __device__ void mx_padded_offsets(const MxArgs &a, int32_t *poff, int *bad)
         if (lane >= d) incl += v;
     }
     int64_t run = incl - local;
+    int32_t *soff = poff + G + 1;
     for (int e = g0; e < g1; e++) {
         poff[e] = (int32_t)run;
+        soff[e] = a.offsets[e];
         run += (int64_t)((max(a.offsets[e + 1] - a.offsets[e], 0) + AL - 1) / AL) * AL;
     }
     const int64_t total = __shfl_sync(0xffffffffu, incl, 31);
     badl = __any_sync(0xffffffffu, badl);
     if (lane == 0) {
         poff[G] = (int32_t)total;
+        soff[G] = a.offsets[G];
         const int b = badl || a.offsets[0] != 0 || (int64_t)a.offsets[G] != a.rows ||
                       (a.do_col && total > a.ld_colT) || total > INT32_MAX;
         *bad = b;
@@ -129,7 +133,10 @@ struct MxTile {
     int64_t rt, ct, pr0, c0, src0, nreal;
 };
 
-__device__ __forceinline__ MxTile mx_tile(const MxArgs &a, int64_t t, int64_t prows, const int32_t *poff)
+// `hint`: the group of the thread's previous tile.  A block's tiles advance
+// through the row space, so the search steps forward from there (a few
+// groups at most) before falling back to bisection.
+__device__ __forceinline__ MxTile mx_tile(const MxArgs &a, int64_t t, int64_t prows, const int32_t *poff, int &hint)
 {
     MxTile g;
     g.rt = t / a.n_col_tiles;
@@ -141,17 +148,27 @@ __device__ __forceinline__ MxTile mx_tile(const MxArgs &a, int64_t t, int64_t pr
     g.nreal = a.rows - g.pr0 < MX_ROWS ? a.rows - g.pr0 : MX_ROWS;
     if (a.offsets && g.live) {
         // the tile lies inside one group (groups are padded to 128 rows)
-        int lo = 0, hi = a.G;  // poff[lo] <= pr0 < poff[hi]
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (poff[mid] <= g.pr0)
-                lo = mid;
-            else
-                hi = mid;
+        int lo = poff[hint] <= g.pr0 ? hint : 0;  // poff[lo] <= pr0
+        int step = 0;
+        while (step < 4 && lo + 1 < a.G && poff[lo + 1] <= g.pr0) {
+            ++lo;
+            ++step;
         }
+        if (lo + 1 < a.G && poff[lo + 1] <= g.pr0) {
+            int hi = a.G;  // poff[lo] <= pr0 < poff[hi]
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (poff[mid] <= g.pr0)
+                    lo = mid;
+                else
+                    hi = mid;
+            }
+        }
+        hint = lo;
+        const int32_t *soff = poff + a.G + 1;  // the offsets, staged next to poff
         const int64_t local0 = g.pr0 - poff[lo];
-        const int64_t m_e = (int64_t)a.offsets[lo + 1] - a.offsets[lo];
-        g.src0 = a.offsets[lo] + local0;
+        const int64_t m_e = (int64_t)soff[lo + 1] - soff[lo];
+        g.src0 = soff[lo] + local0;
         g.nreal = m_e - local0 < MX_ROWS ? m_e - local0 : MX_ROWS;
     }
     if (g.nreal < 0) g.nreal = 0;
@@ -277,7 +294,7 @@ __global__ void __launch_bounds__(MX_THREADS)
     mx_quantize_kernel(MxArgs a)
 {
     __shared__ __align__(16) uint32_t tile[MX_ROWS * MX_PITCH / 2];
-    extern __shared__ int32_t poff[];  // grouped: [G + 1]
+    extern __shared__ int32_t poff[];  // grouped: padded offsets [G + 1], then the offsets [G + 1]
     __shared__ int s_bad;
 
     const int tid = threadIdx.x;
@@ -294,14 +311,15 @@ __global__ void __launch_bounds__(MX_THREADS)
 
     // persistent loop; the next tile's loads are issued before this tile's work
     int64_t t = blockIdx.x;
-    MxTile g = mx_tile(a, t, prows, poff);
+    int hint = 0;
+    MxTile g = mx_tile(a, t, prows, poff, hint);
     MxRaw<PRO> nraw;
     mx_load<PRO>(a, g, tid, nraw);
     for (; t < total; t += gridDim.x) {
         const MxTile cur = g;
         const MxRaw<PRO> raw = nraw;
         if (t + gridDim.x < total) {
-            g = mx_tile(a, t + gridDim.x, prows, poff);
+            g = mx_tile(a, t + gridDim.x, prows, poff, hint);
             mx_load<PRO>(a, g, tid, nraw);
         }
         if (!cur.live) continue;  // grouped: beyond the padded total (block-uniform)
@@ -406,7 +424,10 @@ __global__ void __launch_bounds__(MX_THREADS)
 template <int FMT, int PRO>
 static fp8_status_t launch_mx(const MxArgs &a, cudaStream_t st)
 {
-    const size_t dyn = a.offsets ? (size_t)(a.G + 1) * sizeof(int32_t) : 0;
+    const size_t dyn = a.offsets ? 2 * (size_t)(a.G + 1) * sizeof(int32_t) : 0;  // poff + offsets
+    if (dyn > 0 && cudaFuncSetAttribute(mx_quantize_kernel<FMT, PRO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)dyn) != cudaSuccess)
+        return cuda_fail();
     const int64_t total = a.n_row_tiles * a.n_col_tiles;
     // persistent: as many blocks as fit at once, each looping over tiles
     int per_sm = 0;

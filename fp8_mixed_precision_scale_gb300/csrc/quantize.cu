@@ -76,8 +76,10 @@ struct RowBlock {
 };
 
 // Exclusive prefix of roundup(m_e, 32) over groups, computed by warp 0 into
-// shared memory.  Flags malformed offsets (negative group sizes, total
-// beyond `rows`, padded total beyond ld_colT).
+// shared memory poff[0 .. G], followed by a copy of the offsets themselves
+// (poff[G + 1 .. 2G + 1]) so tile lookups never wait on global memory.
+// Flags malformed offsets (negative group sizes, total beyond `rows`, padded
+// total beyond ld_colT).
 __device__ void compute_padded_offsets(const int32_t *off, int G, int64_t rows, int64_t ld_colT, int32_t *poff,
                                        int *bad, unsigned int *err)
 {
@@ -98,8 +100,10 @@ __device__ void compute_padded_offsets(const int32_t *off, int G, int64_t rows, 
         if (lane >= d) incl += v;
     }
     int64_t run = incl - local;
+    int32_t *soff = poff + G + 1;
     for (int e = g0; e < g1; e++) {
         poff[e] = (int32_t)run;
+        soff[e] = off[e];
         int m = off[e + 1] - off[e];
         run += (int64_t)((max(m, 0) + 31) / 32) * 32;
     }
@@ -107,6 +111,7 @@ __device__ void compute_padded_offsets(const int32_t *off, int G, int64_t rows, 
     badl = __any_sync(0xffffffffu, badl);
     if (lane == 0) {
         poff[G] = (int32_t)total;
+        soff[G] = off[G];
         int b = badl || off[0] != 0 || (int64_t)off[G] != rows || (ld_colT > 0 && total > ld_colT);
         *bad = b;
         if (b) record_error(err, ERR_BAD_OFFSETS);
@@ -143,8 +148,9 @@ __device__ __forceinline__ RowBlock row_block(const QArgs &a, int64_t b, const i
         }
         const int e = lo;
         const int64_t within = p - poff[e];
-        const int64_t m = (int64_t)a.offsets[e + 1] - a.offsets[e];
-        rb.in_row0 = a.offsets[e] + within;
+        const int32_t *soff = poff + a.G + 1;  // the offsets, staged next to poff
+        const int64_t m = (int64_t)soff[e + 1] - soff[e];
+        rb.in_row0 = soff[e] + within;
         rb.out_col0 = p;
         rb.valid = (int)(m - within < RB ? (m - within > 0 ? m - within : 0) : RB);
         rb.group = e;
@@ -1090,7 +1096,7 @@ static fp8_status_t launch_cast(const QArgs &a, int layouts, size_t group_smem, 
 template <int FMT, int RB>
 static fp8_status_t run_quantize(QArgs a, int kind, int layouts, cudaStream_t st)
 {
-    const size_t group_smem = a.offsets ? sizeof(int32_t) * (size_t)(a.G + 1) : 0;
+    const size_t group_smem = a.offsets ? 2 * sizeof(int32_t) * (size_t)(a.G + 1) : 0;  // poff + offsets
     const int64_t n_tiles = a.n_row_blocks * a.n_col_chunks;
     fp8_status_t s;
     if (kind == FP8_RECIPE_DELAYED) {
