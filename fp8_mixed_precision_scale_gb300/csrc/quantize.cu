@@ -119,7 +119,10 @@ __device__ void compute_padded_offsets(const int32_t *off, int G, int64_t rows, 
 }
 
 template <int RB>
-__device__ __forceinline__ RowBlock row_block(const QArgs &a, int64_t b, const int32_t *poff)
+// `hint` (optional): the group of the caller's previous block, when blocks
+// are visited in increasing order; the search steps forward from it (a few
+// groups at most) before falling back to bisection.
+__device__ __forceinline__ RowBlock row_block(const QArgs &a, int64_t b, const int32_t *poff, int *hint = nullptr)
 {
     RowBlock rb;
     rb.skip = false;
@@ -138,14 +141,19 @@ __device__ __forceinline__ RowBlock row_block(const QArgs &a, int64_t b, const i
             rb.group = 0;
             return rb;
         }
-        int lo = 0, hi = a.G;  // invariant: poff[lo] <= p < poff[hi]
-        while (hi - lo > 1) {
-            int mid = (lo + hi) >> 1;
-            if (poff[mid] <= p)
-                lo = mid;
-            else
-                hi = mid;
+        int lo = hint && poff[*hint] <= p ? *hint : 0;  // poff[lo] <= p
+        for (int step = 0; step < 4 && lo + 1 < a.G && poff[lo + 1] <= p; ++step) ++lo;
+        if (lo + 1 < a.G && poff[lo + 1] <= p) {
+            int hi = a.G;  // invariant: poff[lo] <= p < poff[hi]
+            while (hi - lo > 1) {
+                int mid = (lo + hi) >> 1;
+                if (poff[mid] <= p)
+                    lo = mid;
+                else
+                    hi = mid;
+            }
         }
+        if (hint) *hint = lo;
         const int e = lo;
         const int64_t within = p - poff[e];
         const int32_t *soff = poff + a.G + 1;  // the offsets, staged next to poff
@@ -808,6 +816,7 @@ __global__ void __launch_bounds__(QT_THREADS, 6) grouped_cast_kernel(QArgs a)
     }
 
     const int t = threadIdx.x, cg = t & 7, roff = t >> 3;
+    int hint = 0;  // threads 0 .. GT_BLOCKS - 1: the group of their previous block
     const int64_t n_cchunks = (a.cols + GT_COLS - 1) / GT_COLS;
     const int64_t n_tiles = (a.n_row_blocks + GT_BLOCKS - 1) / GT_BLOCKS * n_cchunks;
     uint32_t amax_acc = 0;
@@ -816,7 +825,7 @@ __global__ void __launch_bounds__(QT_THREADS, 6) grouped_cast_kernel(QArgs a)
         const int64_t c0 = (tile % n_cchunks) * GT_COLS;
         if (t < GT_BLOCKS) {
             if (b0 + t < a.n_row_blocks) {
-                srb[t] = row_block<32>(a, b0 + t, poff);
+                srb[t] = row_block<32>(a, b0 + t, poff, &hint);
             } else {
                 srb[t].skip = true;
                 srb[t].valid = 0;
