@@ -332,8 +332,8 @@ def quantize(x: torch.Tensor, fmt: int, recipe: Recipe, layouts: int = LAYOUT_RO
 def quantize_rowwise_resident(x: torch.Tensor, fmt: int, margin: int = 0, layouts: int = LAYOUT_ROW | LAYOUT_COLT,
                               amax_out=None, stream=None) -> Quantized:
     """The rowwise recipe of quantize() for a plain CUDA bf16 [rows, cols]
-    tensor in one cooperative launch (same results; faster for tensors that
-    fit in L2).  Not to be run concurrently on two streams."""
+    tensor in one cooperative launch (same results; fewer launches, and the
+    second read of x comes from L2)."""
     assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
     rows, cols = x.shape
     dev = x.device

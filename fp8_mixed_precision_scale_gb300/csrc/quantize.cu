@@ -33,6 +33,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "fp8gb.h"
 #include "fp8gb_device.cuh"
 #include "fp8gb_host.h"
@@ -965,13 +967,18 @@ __global__ void scales_kernel(float *sinv_row, int64_t n_row, float *sinv_col, i
 // and the whole quantize is one launch instead of six (three clears, two
 // passes, the scale conversion).
 //
-// The barrier counter lives in a file-scope device array (no allocation):
-// the host clears it on the stream before each launch, and barrier k
-// completes when the counter reaches k * gridDim.x.  Every block of a
-// cooperative launch is resident, so every block reaches every barrier; the
-// wait is still bounded and records ERR_GRID_WAIT if it gives up.
+// The barrier counters live in a file-scope device array (no allocation):
+// RESIDENT_SLOTS counters, 128 bytes apart; each call takes the next slot in
+// turn, the host clears it on the stream before the launch, and barrier k
+// completes when the slot's counter reaches k * gridDim.x.  Calls on
+// different streams therefore use different counters as long as fewer than
+// RESIDENT_SLOTS of them are in flight at once.  Every block of a cooperative
+// launch is resident, so every block reaches every barrier; the wait is
+// still bounded and records ERR_GRID_WAIT if it gives up.
 // ---------------------------------------------------------------------------
-static __device__ __align__(256) unsigned int g_resident_scratch[64];
+constexpr int RESIDENT_SLOTS = 64;
+constexpr int RESIDENT_SLOT_WORDS = 32;  // 128 bytes per counter
+static __device__ __align__(256) unsigned int g_resident_scratch[RESIDENT_SLOTS * RESIDENT_SLOT_WORDS];
 
 constexpr uint64_t GRID_WAIT_LIMIT_NS = 2000000000ull;
 
@@ -1007,10 +1014,10 @@ __device__ __forceinline__ bool grid_sync(unsigned int *count, unsigned int k, u
 }
 
 template <int FMT, bool DO_ROW, bool DO_COLT>
-__global__ void __launch_bounds__(QT_THREADS, 4) rowwise_resident_kernel(QArgs a, int64_t tiles_per_block)
+__global__ void __launch_bounds__(QT_THREADS, 4)
+    rowwise_resident_kernel(QArgs a, int64_t tiles_per_block, unsigned int *count)
 {
     extern __shared__ __align__(16) unsigned char dsm[];
-    unsigned int *count = g_resident_scratch;
     const int64_t n_row = DO_ROW ? a.rows : 0, n_col = DO_COLT ? a.cols : 0;
     const int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x, stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = i0; i < n_row + n_col; i += stride) {
@@ -1266,8 +1273,12 @@ static fp8_status_t launch_resident(QArgs a, cudaStream_t st)
     int64_t tiles_per_block = (n_tiles + grid - 1) / grid;
     void *scratch = nullptr;
     if (cudaGetSymbolAddress(&scratch, g_resident_scratch) != cudaSuccess) return cuda_fail();
-    if (cudaMemsetAsync(scratch, 0, sizeof(unsigned int), st) != cudaSuccess) return cuda_fail();
-    void *args[] = {&a, &tiles_per_block};
+    static std::atomic<unsigned int> next_slot{0};
+    unsigned int *count = static_cast<unsigned int *>(scratch) +
+                          (size_t)(next_slot.fetch_add(1, std::memory_order_relaxed) % RESIDENT_SLOTS) *
+                              RESIDENT_SLOT_WORDS;
+    if (cudaMemsetAsync(count, 0, sizeof(unsigned int), st) != cudaSuccess) return cuda_fail();
+    void *args[] = {&a, &tiles_per_block, &count};
     const cudaError_t e = cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(k), dim3((unsigned)grid),
                                                       dim3(QT_THREADS), args, smem, st);
     if (e != cudaSuccess) return cuda_fail_with(e);

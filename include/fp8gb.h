@@ -162,11 +162,11 @@ FP8GB_API fp8_status_t fp8_quantize(const void *x_bf16, int64_t rows, int64_t co
  * fp8_sync_status()).  For a tensor that fits in L2 (on GB300, up to about
  * 96 MB of bf16) the cast pass reads x back from L2; any size is correct.
  *
- * The barriers count on a device-wide counter held in a static array of the
- * library (nothing is allocated); the call clears it on `stream` before its
- * launch.  Calls of this entry point must therefore not run concurrently on
- * different streams of one device; calls on one stream, and concurrent
- * calls of every other entry point, are fine.
+ * The barriers count on one of 64 device counters held in a static array of
+ * the library (nothing is allocated); each call takes the next counter in
+ * turn and clears it on `stream` before its launch.  Calls on different
+ * streams may overlap as long as fewer than 64 of them are in flight at
+ * once; calls of every other entry point are unaffected.
  *
  * Returns FP8_ERR_CUDA if the cooperative launch is refused.
  */

@@ -102,3 +102,27 @@ def test_resident_rejects_bad_arguments():
         assert rc in (1, 3), (b, rc)   # FP8_ERR_INVALID_ARG, FP8_ERR_ALIGNMENT
     rc = fp8.fp8_quantize_rowwise_resident(x, 0, 64, 64, 0, 0, 1, None, None, None, None, 0, None, check=False)
     assert rc == 0
+
+
+def test_resident_calls_on_two_streams():
+    """Calls on two streams, issued back to back without synchronising: each
+    takes its own barrier counter, and every result equals the two-pass
+    path's."""
+    xs = [gen_x((1000, 1032), seed=s).to(DEV) for s in (21, 22)]
+    rec = fp8.Recipe(kind=fp8.ROWWISE)
+    refs = [fp8.quantize(x, 1, rec, 3) for x in xs]
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = []
+    for _ in range(4):
+        for i, (x, st) in enumerate(zip(xs, streams)):
+            with torch.cuda.stream(st):
+                outs.append((i, fp8.quantize_rowwise_resident(x, 1, stream=st)))
+    torch.cuda.synchronize()
+    assert fp8.fp8_sync_status() == 0
+    for i, q in outs:
+        ref = refs[i]
+        assert torch.equal(q.q_row, ref.q_row)
+        assert torch.equal(q.q_colT[:, :1000], ref.q_colT[:, :1000])
+        assert torch.equal(q.scale_inv_row[:1000].view(torch.int32), ref.scale_inv_row.view(torch.int32))
+        assert torch.equal(q.scale_inv_col.view(torch.int32), ref.scale_inv_col.view(torch.int32))
