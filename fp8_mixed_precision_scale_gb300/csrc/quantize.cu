@@ -515,29 +515,46 @@ __global__ void __launch_bounds__(QT_THREADS) rowcol_amax_kernel(QArgs a)
         uint32_t rmax[SUP_BLOCKS][2];
 #pragma unroll
         for (int kb = 0; kb < SUP_BLOCKS; kb++) rmax[kb][0] = rmax[kb][1] = 0;
+        // step k: half k % 2 (row blocks 4 (k % 2) .. + 3) of column chunk k / 2;
+        // the next step's loads are issued before this step is reduced
+        auto load_step = [&](int k, uint4 (&v)[SUP_BLOCKS / 2][2]) {
+            const int jj = k >> 1, hf = k & 1;
+            const int64_t cc0 = (sc * SC + jj) * QT_COLS;
+            const int64_t col = cc0 + cg * 8;
+            const bool ok = jj < SC && hf * (SUP_BLOCKS / 2) < SB && col < a.cols;
+#pragma unroll
+            for (int kk = 0; kk < SUP_BLOCKS / 2; kk++) {
+                const RowBlock &rb = srb[hf * (SUP_BLOCKS / 2) + kk];
+#pragma unroll
+                for (int h = 0; h < 2; h++) {
+                    const int r = h * 16 + roff;
+                    if (ok && !rb.skip && r < rb.valid)
+                        v[kk][h] = __ldg(reinterpret_cast<const uint4 *>(a.x + (rb.in_row0 + r) * a.ld_x + col));
+                    else
+                        v[kk][h] = make_uint4(0, 0, 0, 0);
+                }
+            }
+        };
+        uint4 nv[SUP_BLOCKS / 2][2];
+        load_step(0, nv);
+        uint32_t cacc[4] = {0, 0, 0, 0};
+        int cur_group = -1;
         for (int j = 0; j < SC; j++) {
             const int64_t c0 = (sc * SC + j) * QT_COLS;
             if (c0 >= a.cols) break;  // uniform
-            const int64_t col = c0 + cg * 8;
-            const bool col_ok = col < a.cols;
-            uint32_t cacc[4] = {0, 0, 0, 0};
-            int cur_group = -1;
 #pragma unroll
             for (int half = 0; half < 2; half++) {
-                if (half * (SUP_BLOCKS / 2) >= SB) break;  // uniform
+                const int k = 2 * j + half;
+                if (half * (SUP_BLOCKS / 2) >= SB) continue;  // uniform: no second half
                 uint4 v[SUP_BLOCKS / 2][2];
 #pragma unroll
                 for (int kk = 0; kk < SUP_BLOCKS / 2; kk++) {
-                    const RowBlock &rb = srb[half * (SUP_BLOCKS / 2) + kk];
-#pragma unroll
-                    for (int h = 0; h < 2; h++) {
-                        const int r = h * 16 + roff;
-                        if (!rb.skip && col_ok && r < rb.valid)
-                            v[kk][h] = __ldg(reinterpret_cast<const uint4 *>(a.x + (rb.in_row0 + r) * a.ld_x + col));
-                        else
-                            v[kk][h] = make_uint4(0, 0, 0, 0);
-                    }
+                    v[kk][0] = nv[kk][0];
+                    v[kk][1] = nv[kk][1];
                 }
+                // the next step that runs: half 1 exists only when SB > SUP_BLOCKS / 2
+                const int kn = (k & 1) == 0 && SB <= SUP_BLOCKS / 2 ? k + 2 : k + 1;
+                if (kn < 2 * SC) load_step(kn, nv);
 #pragma unroll
                 for (int kk = 0; kk < SUP_BLOCKS / 2; kk++) {
                     const int kb = half * (SUP_BLOCKS / 2) + kk;
@@ -561,8 +578,12 @@ __global__ void __launch_bounds__(QT_THREADS) rowcol_amax_kernel(QArgs a)
                         rmax[kb][h] = max(rmax[kb][h], fold_absmax(racc));
                     }
                 }
+                const bool chunk_end = half == 1 || (SUP_BLOCKS / 2) >= SB;
+                if (chunk_end) {
+                    if (a.sinv_col && cur_group >= 0) flush_col_amax(a, cacc, cur_group, c0, colw);
+                    cur_group = -1;
+                }
             }
-            if (a.sinv_col && cur_group >= 0) flush_col_amax(a, cacc, cur_group, c0, colw);
         }
         // row maxima: reduce over the 16 threads sharing a row, one atomic per row
 #pragma unroll
