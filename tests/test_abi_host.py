@@ -105,6 +105,42 @@ def test_quantize_validation(lib):
     assert q_call(lib, G=3) == INVALID
 
 
+def r_call(lib, **kw):
+    args = dict(x=FAKE, rows=64, cols=64, ld_x=64, fmt=0, margin=0, layouts=3, amax_out=None, q_row=FAKE,
+                sinv_row=FAKE, q_colT=FAKE, ld_colT=64, sinv_col=FAKE)
+    args.update(kw)
+    P = ctypes.c_void_p
+    return lib.fp8_quantize_rowwise_resident(P(args["x"]), args["rows"], args["cols"], args["ld_x"], args["fmt"],
+                                             args["margin"], args["layouts"], P(args["amax_out"]), P(args["q_row"]),
+                                             P(args["sinv_row"]), P(args["q_colT"]), args["ld_colT"],
+                                             P(args["sinv_col"]), None)
+
+
+def test_resident_quantize_validation(lib):
+    """The single-launch rowwise quantize checks what fp8_quantize checks for
+    a plain rowwise tensor; an empty tensor returns OK without a launch."""
+    assert r_call(lib, x=None) == INVALID
+    assert r_call(lib, rows=-1) == INVALID
+    assert r_call(lib, cols=0) == INVALID
+    assert r_call(lib, ld_x=32) == INVALID
+    assert r_call(lib, fmt=4) == INVALID
+    assert r_call(lib, margin=-1) == INVALID
+    assert r_call(lib, margin=65) == INVALID
+    assert r_call(lib, layouts=0) == INVALID
+    assert r_call(lib, layouts=4) == INVALID
+    assert r_call(lib, q_row=None) == INVALID
+    assert r_call(lib, sinv_row=None) == INVALID
+    assert r_call(lib, q_colT=None) == INVALID
+    assert r_call(lib, sinv_col=None) == INVALID
+    assert r_call(lib, cols=60, ld_x=64) == ALIGN
+    assert r_call(lib, ld_x=68) == ALIGN
+    assert r_call(lib, x=FAKE + 8) == ALIGN
+    assert r_call(lib, q_row=FAKE + 4) == ALIGN
+    assert r_call(lib, ld_colT=72) == ALIGN
+    assert r_call(lib, ld_colT=48) == INVALID         # shorter than rows
+    assert r_call(lib, rows=0, x=None, q_row=None, sinv_row=None) == OK
+
+
 def g_call(lib, **kw):
     a = dict(A=FAKE, fa=0, lda=128, B=FAKE, fb=0, ldb=128, M=128, N=256, K=128, sa=FAKE, sam=0, sb=FAKE, sbm=0,
              C=FAKE, ldc=256)
