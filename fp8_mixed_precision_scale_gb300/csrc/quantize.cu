@@ -966,6 +966,20 @@ __global__ void __launch_bounds__(QT_THREADS, 6) grouped_cast_kernel(QArgs a)
     if constexpr (DELAYED) block_amax_atomic(fold_absmax(amax_acc), a.amax_out, red);
 }
 
+// Zero the ROWWISE amax accumulators (row, column, and the optional tensor
+// amax) before the amax pass.
+__global__ void clear_amax_kernel(float *row, int64_t n_row, float *col, int64_t n_col, float *tensor)
+{
+    const int64_t total = n_row + n_col;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        if (i < n_row)
+            row[i] = 0.0f;
+        else
+            col[i - n_row] = 0.0f;
+    }
+    if (tensor && blockIdx.x == 0 && threadIdx.x == 0) tensor[0] = 0.0f;
+}
+
 // ROWWISE scale buffers, in place: mode 0 turns the accumulated amax into
 // the scale (before the cast pass), mode 1 turns the scale into scale_inv =
 // 1 / scale (after it), mode 2 turns the amax into scale_inv directly.
@@ -1151,9 +1165,13 @@ static fp8_status_t run_quantize(QArgs a, int kind, int layouts, cudaStream_t st
     const int64_t n_col = (layouts & FP8_LAYOUT_COLT) ? a.cols * (a.offsets ? a.G : 1) : 0;
     if (!(layouts & FP8_LAYOUT_ROW)) a.sinv_row = nullptr;
     if (!(layouts & FP8_LAYOUT_COLT)) a.sinv_col = nullptr;
-    if (n_row && cudaMemsetAsync(a.sinv_row, 0, sizeof(float) * n_row, st) != cudaSuccess) return cuda_fail();
-    if (n_col && cudaMemsetAsync(a.sinv_col, 0, sizeof(float) * n_col, st) != cudaSuccess) return cuda_fail();
-    if (a.amax_out && cudaMemsetAsync(a.amax_out, 0, sizeof(float), st) != cudaSuccess) return cuda_fail();
+    // the amax accumulators start at zero: one launch clears all three
+    {
+        const int64_t n = n_row + n_col + (a.amax_out ? 1 : 0);
+        const int zgrid = (int)((n + 255) / 256 < 1024 ? ((n + 255) / 256 > 0 ? (n + 255) / 256 : 1) : 1024);
+        clear_amax_kernel<<<zgrid, 256, 0, st>>>(a.sinv_row, n_row, a.sinv_col, n_col, a.amax_out);
+        if ((s = check_launch()) != FP8_OK) return s;
+    }
     if (!a.offsets) {
         auto k = dense_rowcol_amax_kernel<RB>;
         const int64_t grid = blocks_for(k, 0, n_tiles, true);
