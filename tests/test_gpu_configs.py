@@ -126,7 +126,19 @@ class DelayedLayer:
                                     self.algo, 0)
 
 
-def run_delayed(orc, base, fmts, algo, gemms, steps=50, full_steps=(0, 30, 49), gemm_steps=(0, 1, 30, 49)):
+def checkpoint_roundtrip(tensors):
+    """Save the delayed-scaling state to the host, lose the device copy, and
+    restore it: the library keeps no state of its own, so the run must
+    continue exactly as if nothing happened."""
+    saved = [v.cpu().clone() for v in tensors]
+    for v in tensors:
+        v.fill_(float("nan"))
+    for v, h in zip(tensors, saved):
+        v.copy_(h.to(v.device))
+
+
+def run_delayed(orc, base, fmts, algo, gemms, steps=50, full_steps=(0, 30, 49), gemm_steps=(0, 1, 30, 49),
+                restore_at=25):
     L = 1024
     lay = DelayedLayer(base, fmts, L, algo)
     n = len(lay.names)
@@ -181,6 +193,9 @@ def run_delayed(orc, base, fmts, algo, gemms, steps=50, full_steps=(0, 30, 49), 
         assert_f32_bits_equal(lay.hist.cpu().numpy(), hist_o, f"hist t{t}")
         assert_f32_bits_equal(lay.scale.cpu().numpy(), scale_o, f"scale t{t}")
         assert_f32_bits_equal(lay.sinv.cpu().numpy(), sinv_o, f"scale_inv t{t}")
+        if t == restore_at:
+            checkpoint_roundtrip((lay.hist, lay.scale, lay.sinv))
+            sync_ok()
     # the spike at t = 30 must have lowered the activation scales afterwards
     return scale_o
 
