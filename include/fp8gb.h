@@ -13,6 +13,11 @@
  *                              (fprop, dgrad and wgrad are all this call);
  *   4. fp8_grouped_gemm        the same over variable-size expert groups of a
  *                              Mixture-of-Experts layer.
+ * Beyond those: fp8_quantize_rowwise_resident (the rowwise recipe in one
+ * cooperative launch), the MXFP8 recipe (fp8_mx_quantize, fp8_mx_gemm,
+ * fp8_mx_grouped_gemm, and the fused MoE prologues fp8_mx_permute_quantize
+ * and fp8_mx_swiglu_quantize), and the blockwise recipe
+ * (fp8_blockwise_quantize, whose scales feed fp8_mx_gemm).
  *
  * Method sources (page title, section):
  *   - "FP8 training for Flux models" (AMD Primus guide), Configuration >
