@@ -9,9 +9,10 @@
 // non-coalesced writes were the bottleneck; the five-kernel chain fused into
 // one; relaxed atomics).
 //
-// Design (GB300): thread blocks of 256 threads work on tiles of RB rows x 128
-// columns (RB = 64 for plain tensors, one tile per block; RB = 32 for
-// expert-grouped tensors, persistent blocks).  Each thread issues all of its 16-byte loads for a
+// Design (GB300): thread blocks of 256 threads work on tiles of 64 rows x 128
+// columns for plain tensors (one tile per block); expert-grouped tensors are
+// cast by persistent blocks on tiles of four padded 32-row blocks x 64
+// columns (grouped_cast_kernel).  Each thread issues all of its 16-byte loads for a
 // tile before touching the data, converts 8 elements at a time with
 // cvt.rn.satfinite.{e4m3,e5m2}x2, stores the row layout directly (8-byte
 // coalesced stores) and stages the bytes in shared memory; the transposed
@@ -23,12 +24,16 @@
 //
 // Kernels and passes:
 //   DELAYED    : cast (stored scale) + fused amax            -> 1 launch
-//   TENSORWISE : amax pass, cast pass                        -> 2 launches
-//   ROWWISE    : amax pass (row + column amax), cast pass, scale_inv
-//                (+ amax -> scale before the cast when grouped) -> 3 or 4 launches
+//   TENSORWISE : amax pass, cast pass                        -> 2 launches (+ a clear)
+//   ROWWISE    : clear, amax pass (row + column amax), cast pass, scale_inv
+//                (+ amax -> scale before the cast when grouped) -> 4 or 5 launches
+//   fp8_quantize_rowwise_resident: the ROWWISE passes of a plain tensor in
+//                one cooperative launch with grid-wide barriers
 // The rowwise / colwise amax values are accumulated in the scale_inv output
 // buffers themselves (as fp32 bit patterns), turned into the scales before
-// the cast pass and into scale_inv after it, so no scratch memory is needed.
+// the cast pass and into scale_inv after it, so the passes need no scratch
+// memory; only the single-launch form keeps its barrier counters in a
+// file-scope device array.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
