@@ -13,10 +13,11 @@
 //
 // Design (GB300, sm_103a): the persistent warp-specialised structure of the
 // tensor-scaled GEMM plus a scale warp, 352 threads per CTA, one CTA per SM.
-//   warp 0     producer: TMA tiles of A (128 x 128 bytes) and B (224 x 128
+//   warp 0     producer: TMA tiles of A (128 x 128 bytes) and B (256 x 128
 //              bytes), plus one bulk copy each of the tiles' scale words
 //              (one 32-bit word per row and 128-element K tile), all counted
-//              on one mbarrier per stage of a 4-stage ring.
+//              on one mbarrier per stage of the ring (4 stages dense, 3
+//              grouped, 2 with the TMA-store epilogue).
 //   warp 10    scales: rearranges each stage's scale words into the 32-lane
 //              x 16-byte blocks that tcgen05.cp 32x128b.warpx4 copies into
 //              tensor memory (word of row 32j + L at lane L, column j,
@@ -27,14 +28,15 @@
 //   warp 1     MMA: one thread waits for a stage's scales and issues its four
 //              K=32 MMAs, each selecting its byte of the scale words by the
 //              scale-factor ids of the instruction descriptor.
-//   warps 2-9  epilogue: tcgen05.ld, bf16, shared-memory transpose, whole-
-//              sector stores.
-// Tiles are 128 x 224: two 224-column accumulators (columns 0 and 256) and
-// one set of scale columns per ring stage (224 .. 239 for A, 480 .. 511 for
-// B) fit the 512 TMEM columns, so the epilogue of one tile overlaps the main
-// loop of the next and a stage's scale copies never wait for the MMAs of the
-// stage before.  Every wait is
-// bounded as in the tensor-scaled GEMM.
+//   warps 2-9  epilogue: each warp drains its 32 x 128 block of the
+//              accumulator into registers and releases it, then converts to
+//              bf16 and stores (shared-memory transpose and whole-sector
+//              stores, or 128-byte-swizzled boxes and TMA stores for the
+//              K-grouped output).
+// Tiles are 128 x 256 with one 256-column accumulator (TMEM columns 0 ..
+// 255); each ring stage has its own scale columns (A from 256, B from 288),
+// so a stage's scale copies never wait for the MMAs of the stage before.
+// Every wait is bounded as in the tensor-scaled GEMM.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
