@@ -25,6 +25,11 @@
 //              bf16, store.  Two 256-column accumulators (all 512 TMEM
 //              columns) let the epilogue of one tile overlap the main loop of
 //              the next.
+// Two more kernels share this structure (each described where it is
+// defined): fp8_gemm_pair_kernel, the dense GEMM for M > 128 on CTA pairs
+// (256 x 256 tiles from 2-SM MMAs, each CTA staging half of A and of B), and
+// fp8_gemm_kgroup_tma_kernel, the K-grouped wgrad whose epilogue writes
+// through 128-byte-swizzled boxes and TMA stores.
 // Every mbarrier wait is bounded (about 2 s of wall time); a wait that gives
 // up records the device error word, drains in-flight copies, releases TMEM
 // and returns.
