@@ -11,6 +11,7 @@ dyadic rational, so sum_k a_k b_k is computed exactly as a Fraction -- plus
 special cases (one-hot operands, K = 16, empty groups) and grouped GEMM equal
 to a loop of dense GEMMs.
 """
+import os
 from fractions import Fraction
 
 import numpy as np
@@ -261,3 +262,31 @@ def test_grouped_gemm_equals_dense_loop(orc):
             continue
         d, _ = orc.gemm(AT[:, poff[e]:poff[e] + m], 1, BT[:, poff[e]:poff[e] + m], 0, sa2[e], sb2[e])
         assert np.array_equal(ref2[e], d)
+
+
+def test_results_do_not_depend_on_thread_count(orc):
+    """The oracle parallelises only independent outer loops: one thread and
+    several give the same bytes, scales and GEMM values bit for bit."""
+    import oracle as oracle_mod
+    g = torch.Generator().manual_seed(12)
+    x = synth.bf16_bits((torch.randn((300, 264), generator=g) * 3).to(torch.bfloat16))
+    xm = synth.bf16_bits((torch.randn((320, 256), generator=g) * 3).to(torch.bfloat16))  # MX: multiples of 32
+    A = torch.randint(0, 0x7E, (40, 96), generator=g, dtype=torch.int32).to(torch.uint8).numpy()
+    B = torch.randint(0, 0x7E, (56, 96), generator=g, dtype=torch.int32).to(torch.uint8).numpy()
+    sa = (torch.rand(40, generator=g) + 0.5).numpy().astype(np.float32)
+    sb = (torch.rand(56, generator=g) + 0.5).numpy().astype(np.float32)
+    outs = []
+    try:
+        for threads in (1, 4):
+            oracle_mod.set_threads(threads)
+            q = orc.quantize(x, 0, orc.ROWWISE)
+            mxq = orc.mx_quantize(xm, 1)
+            ref, bound = orc.gemm(A, 0, B, 1, sa, sb)
+            outs.append((q, mxq, ref, bound))
+    finally:
+        oracle_mod.set_threads(os.cpu_count() or 1)
+    (q1, m1, r1, b1), (q4, m4, r4, b4) = outs
+    for d1, d4 in ((q1, q4), (m1, m4)):
+        for k in d1:
+            assert np.asarray(d1[k]).tobytes() == np.asarray(d4[k]).tobytes(), k   # bit for bit
+    assert r1.tobytes() == r4.tobytes() and b1.tobytes() == b4.tobytes()
