@@ -103,10 +103,8 @@ def _load():
             lib.orc_mx_gemm.restype = None
             lib.orc_mx_gemm.argtypes = [P, i32, i64, P, i64, P, i32, i64, P, i64, i64, i64, i64, P, P, i64,
                                         P, P]
-            lib.orc_exp_f32.restype = f32
-            lib.orc_exp_f32.argtypes = [f32]
-            lib.orc_bf16_rne.restype = ctypes.c_uint16
-            lib.orc_bf16_rne.argtypes = [f32]
+            lib.orc_bf16_from_double.restype = ctypes.c_uint16
+            lib.orc_bf16_from_double.argtypes = [ctypes.c_double]
             lib.orc_swiglu_bf16.restype = None
             lib.orc_swiglu_bf16.argtypes = [P, P, i64, P]
             lib.orc_blockwise_code.restype = i32
@@ -330,18 +328,14 @@ def mx_gemm(A, fa, sA, B, fb, sB, points=None):
 
 # --- MoE prologues: gather (permute) and SwiGLU ------------------------------
 
-def exp_f32(x: float) -> np.float32:
-    """The fixed fp32 exp (Cody-Waite reduction, degree-6 Taylor) of the
-    SwiGLU definition."""
-    return np.float32(_load().orc_exp_f32(float(np.float32(x))))
-
-
-def bf16_rne(x: float) -> int:
-    return int(_load().orc_bf16_rne(float(np.float32(x))))
+def bf16_from_double(x: float) -> int:
+    """bf16 bit pattern of x rounded once to the nearest bf16 (ties to even)."""
+    return int(_load().orc_bf16_from_double(float(x)))
 
 
 def swiglu_bf16(g_bits, u_bits) -> np.ndarray:
-    """h = bf16(silu(g) * u) element-wise on bf16 bit patterns."""
+    """h = bf16_rne(silu(g) * u) element-wise on bf16 bit patterns: the exact
+    value (evaluated in double precision) rounded once to bf16."""
     g = _c(g_bits, np.uint16)
     u = _c(u_bits, np.uint16)
     assert g.shape == u.shape

@@ -717,79 +717,77 @@ void orc_mx_gemm(const uint8_t *A, int fa, int64_t lda, const uint8_t *sA, int64
  * gate/up and down projections, SwiGLU.  Their definitions here:
  *
  *   gather : row i of the output is row src[i] of the input.
- *   SwiGLU : h = bf16_rne(silu(g) * u), silu(g) = g / (1 + exp(-g)), with
- *            every operation an IEEE fp32 operation (round to nearest even,
- *            no fused multiply-add) and exp evaluated by the fixed fp32
- *            algorithm below, so that a kernel evaluating the same steps in
- *            the same order produces the same bf16 value.
+ *   SwiGLU : h = bf16_rne(silu(g) * u) with silu(g) = g * sigma(g),
+ *            sigma(g) = 1 / (1 + e^-g): the real-valued result rounded once
+ *            to the nearest bf16 (ties to even).  Limits and IEEE
+ *            conventions: silu(+Inf) = +Inf, silu(-Inf) = -0 (the limit of
+ *            g e^g), NaN in g or u gives NaN, Inf * 0 gives NaN.
  *
- * exp_f32 (Cody-Waite argument reduction and a Taylor polynomial):
- *   n = rint(x * log2(e)), r = (x - n * C1) - n * C2, where C1 is ln 2
- *   rounded to 16 significant bits (so n * C1 is exact) and C2 = fp32(ln 2 -
- *   C1); e^r ~ 1 + r + r^2/2! + ... + r^6/6! by Horner's rule (|r| <= 0.35,
- *   truncation below 2e-7 relative); the result is scaled by 2^n in two
- *   exact power-of-two multiplies.  x > 88 gives +Inf, x < -104 gives +0,
- *   NaN gives NaN.
+ * Evaluation: P = g * u is exact in double (two 8-bit significands), sigma
+ * is evaluated in double (libm exp), h_d = P * sigma_d, an error far below
+ * half a bf16 ulp.  The one way that error can still move the rounding is
+ * h_d landing exactly on a midpoint between two bf16 values while the exact
+ * product does not; that happens when sigma_d comes out as exactly 1/2 (|g|
+ * tiny) or exactly 1 (g large), and there the side of the exact value is
+ * known: sigma(g) > 1/2 for g > 0, < 1/2 for g < 0, and < 1 always.
  */
-static float f32_mul(float a, float b) { volatile float r = a * b; return r; }
-static float f32_add(float a, float b) { volatile float r = a + b; return r; }
-static float f32_sub(float a, float b) { volatile float r = a - b; return r; }
-static float f32_div(float a, float b) { volatile float r = a / b; return r; }
 
-static float pow2_f32(int n) /* 2^n for -126 <= n <= 127 */
+/* bf16 rounding of a double (nearest; bf16's range: subnormals down to
+ * 2^-133, overflow to Inf; NaN gives the quiet NaN 0x7FC0).  An exact
+ * midpoint between two bf16 values goes to the larger magnitude when
+ * tie > 0, the smaller when tie < 0, the even code when tie == 0. */
+static uint16_t bf16_round(double v, int tie)
 {
-    uint32_t u = (uint32_t)(n + 127) << 23;
+    uint16_t sign;
+    double a, q, m, r, h;
+    int e, E;
     float f;
-    memcpy(&f, &u, 4);
-    return f;
-}
-
-float orc_exp_f32(float x)
-{
-    const float LOG2E = 1.44269502f;            /* fp32(1 / ln 2) */
-    const float C1 = 0.693145751953125f;        /* ln 2 to 16 significant bits */
-    const float C2 = 1.42860677e-06f;           /* fp32(ln 2 - C1) */
-    float n, r, p;
-    int ni;
-    if (isnan(x)) return x;
-    if (x > 88.0f) return INFINITY;
-    if (x < -104.0f) return 0.0f;
-    n = rintf(f32_mul(x, LOG2E));
-    ni = (int)n;
-    r = f32_sub(f32_sub(x, f32_mul(n, C1)), f32_mul(n, C2));
-    /* Horner: 1 + r(1 + r(1/2 + r(1/6 + r(1/24 + r(1/120 + r/720))))) */
-    p = f32_add(1.0f / 120.0f, f32_mul(r, 1.0f / 720.0f));
-    p = f32_add(1.0f / 24.0f, f32_mul(r, p));
-    p = f32_add(1.0f / 6.0f, f32_mul(r, p));
-    p = f32_add(0.5f, f32_mul(r, p));
-    p = f32_add(1.0f, f32_mul(r, p));
-    p = f32_add(1.0f, f32_mul(r, p));
-    /* 2^n in two power-of-two multiplies (n in [-150, 127]: each factor is
-     * a normal fp32 power of two) */
-    p = f32_mul(p, pow2_f32(ni / 2));
-    p = f32_mul(p, pow2_f32(ni - ni / 2));
-    return p;
-}
-
-/* bf16 bit pattern of an fp32 value, round to nearest even (NaN stays NaN). */
-uint16_t orc_bf16_rne(float f)
-{
     uint32_t u;
+    if (isnan(v)) return 0x7FC0;
+    sign = signbit(v) ? 0x8000 : 0;
+    a = fabs(v);
+    if (isinf(a)) return (uint16_t)(sign | 0x7F80);
+    if (a == 0.0) return sign;
+    (void)frexp(a, &e);          /* a = f * 2^e, f in [0.5, 1): floor(log2 a) = e - 1 */
+    E = e - 1 < -126 ? -126 : e - 1;
+    q = ldexp(1.0, E - 7);       /* the bf16 spacing at a: 8 significant bits */
+    m = a / q;                   /* exact (power-of-two scaling) */
+    if (m - floor(m) == 0.5 && tie != 0)
+        r = tie > 0 ? ceil(m) : floor(m);
+    else
+        r = nearbyint(m);        /* nearest, ties to even */
+    h = r * q;
+    if (h >= ldexp(1.0, 128)) return (uint16_t)(sign | 0x7F80);
+    f = (float)h;                /* exact: h has at most 8 significant bits */
     memcpy(&u, &f, 4);
-    if ((u & 0x7FFFFFFFu) > 0x7F800000u) return (uint16_t)((u >> 16) | 0x40u);
-    u += 0x7FFFu + ((u >> 16) & 1u);
-    return (uint16_t)(u >> 16);
+    return (uint16_t)(sign | (u >> 16));
 }
 
-/* h = bf16(silu(g) * u) for n pairs; g, u and h are bf16 bit patterns. */
+/* bf16 bit pattern of a double rounded once to the nearest bf16 value, ties
+ * to even. */
+uint16_t orc_bf16_from_double(double v) { return bf16_round(v, 0); }
+
+/* h = bf16_rne(silu(g) * u) for n pairs; g, u and h are bf16 bit patterns. */
 void orc_swiglu_bf16(const uint16_t *g, const uint16_t *u, int64_t n, uint16_t *h)
 {
 #pragma omp parallel for schedule(static)
     for (int64_t i = 0; i < n; i++) {
-        float gf = bf16_to_float(g[i]), uf = bf16_to_float(u[i]);
-        float e = orc_exp_f32(-gf);
-        float s = f32_div(gf, f32_add(1.0f, e));
-        h[i] = orc_bf16_rne(f32_mul(s, uf));
+        double gd = bf16_to_float(g[i]), ud = bf16_to_float(u[i]);
+        double sig, hd;
+        int tie = 0;
+        if (isnan(gd) || isnan(ud)) {
+            h[i] = 0x7FC0;
+            continue;
+        }
+        if (isinf(gd)) {  /* silu(+Inf) = +Inf, silu(-Inf) = -0 */
+            h[i] = bf16_round((gd > 0 ? gd : -0.0) * ud, 0);
+            continue;
+        }
+        sig = 1.0 / (1.0 + exp(-gd));
+        hd = (gd * ud) * sig;
+        if (sig == 0.5) tie = gd > 0 ? 1 : (gd < 0 ? -1 : 0);
+        if (sig == 1.0) tie = -1;
+        h[i] = bf16_round(hd, tie);
     }
 }
 
