@@ -218,30 +218,6 @@ __device__ __forceinline__ void mx_load(const MxArgs &a, const MxTile &g, int ti
     }
 }
 
-// exp in IEEE fp32 by a fixed algorithm (Cody-Waite argument reduction with
-// ln 2 split into a 16-significant-bit part and its fp32 remainder, then the
-// degree-6 Taylor polynomial of e^r by Horner's rule, then two exact
-// power-of-two scalings), every operation rounded to nearest without fused
-// multiply-add, so the result is reproducible bit for bit on any IEEE fp32
-// implementation that takes the same steps.  x > 88 -> +Inf, x < -104 -> +0.
-__device__ __forceinline__ float exp_fixed(float x)
-{
-    if (x != x) return x;
-    if (x > 88.0f) return __int_as_float(0x7F800000);
-    if (x < -104.0f) return 0.0f;
-    const float n = rintf(__fmul_rn(x, 1.44269502f));
-    const int ni = (int)n;
-    const float r = __fsub_rn(__fsub_rn(x, __fmul_rn(n, 0.693145751953125f)), __fmul_rn(n, 1.42860677e-06f));
-    float p = __fadd_rn(1.0f / 120.0f, __fmul_rn(r, 1.0f / 720.0f));
-    p = __fadd_rn(1.0f / 24.0f, __fmul_rn(r, p));
-    p = __fadd_rn(1.0f / 6.0f, __fmul_rn(r, p));
-    p = __fadd_rn(0.5f, __fmul_rn(r, p));
-    p = __fadd_rn(1.0f, __fmul_rn(r, p));
-    p = __fadd_rn(1.0f, __fmul_rn(r, p));
-    p = __fmul_rn(p, __int_as_float((ni / 2 + 127) << 23));
-    return __fmul_rn(p, __int_as_float((ni - ni / 2 + 127) << 23));
-}
-
 // fp32 -> bf16 bits, round to nearest even; NaN stays a quiet NaN.
 __device__ __forceinline__ uint32_t bf16_bits_rne(float f)
 {
@@ -251,13 +227,30 @@ __device__ __forceinline__ uint32_t bf16_bits_rne(float f)
     return u >> 16;
 }
 
-// h = bf16(silu(g) * u), silu(g) = g / (1 + exp(-g)), for a packed pair.
+// silu(g) * u in fp32, with sigma(g) = 1 / (1 + e^-g) formed from t = e^-|g|
+// (never overflows): sigma = 1 / (1 + t) for g >= 0, t / (1 + t) for g < 0.
+// For g < 0 the product is carried scaled by 2^126 (t is computed as 2^126
+// e^-|g|, a normal fp32 for |g| < 174) and unscaled by the last multiply,
+// applied to u first when |u| >= 1, so no intermediate overflows or turns
+// subnormal before the end.  __expf and __fdividef (1 + t lies in [1, 2])
+// err by far less than 2^-9 relative, so the bf16 rounding of the result is
+// within one bf16 ulp of the exact bf16_rne(silu(g) * u) for every g when
+// |u| <= 2^110 (NaN, +-Inf and the sign of zero as IEEE arithmetic gives
+// them; silu(-Inf) = -0).
+__device__ __forceinline__ float swiglu1(float g, float u)
+{
+    constexpr float LN2_X126 = 87.3365479f;  // 126 ln 2: e^(x + 126 ln 2) = 2^126 e^x
+    const float t = __expf(LN2_X126 - fabsf(g));
+    const float r = __fdividef(1.0f, fmaf(t, 0x1p-126f, 1.0f));
+    if (g >= 0.0f) return (g * r) * u;
+    const float s = t == 0.0f ? -0.0f : g * (t * r);  // 2^126 silu(g); t == 0 also for g = -Inf
+    return fabsf(u) >= 1.0f ? s * (u * 0x1p-126f) : (s * u) * 0x1p-126f;
+}
+
+// h = bf16(silu(g) * u) for a packed pair.
 __device__ __forceinline__ uint32_t swiglu2(uint32_t g2, uint32_t u2)
 {
-    const float g0 = bf16lo(g2), g1 = bf16hi(g2);
-    const float s0 = __fdiv_rn(g0, __fadd_rn(1.0f, exp_fixed(-g0)));
-    const float s1 = __fdiv_rn(g1, __fadd_rn(1.0f, exp_fixed(-g1)));
-    return bf16_bits_rne(__fmul_rn(s0, bf16lo(u2))) | (bf16_bits_rne(__fmul_rn(s1, bf16hi(u2))) << 16);
+    return bf16_bits_rne(swiglu1(bf16lo(g2), bf16lo(u2))) | (bf16_bits_rne(swiglu1(bf16hi(g2), bf16hi(u2))) << 16);
 }
 
 // The 32 bf16 the quantize sees: the raw values, or SwiGLU of gate and up

@@ -372,13 +372,11 @@ FP8GB_API fp8_status_t fp8_blockwise_quantize(const void *x_bf16, int64_t rows, 
  *     gate_up_bf16  [rows][ld] bf16: gate in columns [0, F), up in [F, 2F);
  *                   ld >= 2F, ld % 8 == 0; F % 32 == 0.
  *     h_bf16        optional [rows][ld_h] bf16 copy of h (NULL: not written).
- *   silu(g) = g / (1 + exp(-g)) is evaluated in IEEE fp32 (round to nearest,
- *   no fused multiply-add) with exp computed by a fixed algorithm:
- *   n = rint(x log2 e), r = (x - n C1) - n C2 (C1 = ln 2 to 16 significant
- *   bits, C2 = fp32(ln 2 - C1)), e^r by the degree-6 Taylor polynomial in
- *   Horner form, scaled by 2^n in two exact steps; x > 88 -> Inf, x < -104 ->
- *   0.  h is that fp32 product rounded to bf16 (nearest even), so the
- *   quantized bytes are reproducible from the definition.
+ *   h is bf16_rne(silu(g) * u), silu(g) = g / (1 + e^-g), evaluated in fp32
+ *   with the fast exponential and divide; each element of h is within one
+ *   bf16 ulp of the exact value rounded to bf16 (for |u| <= 2^110; NaN and
+ *   +-Inf follow IEEE arithmetic, silu(-Inf) = -0).  The quantized bytes and
+ *   scales are exactly fp8_mx_quantize's of that h.
  */
 FP8GB_API fp8_status_t fp8_mx_permute_quantize(const void *x_bf16, int64_t x_rows, int64_t cols, int64_t ld_x,
                                                const int32_t *src_rows, int64_t rows, int fmt, int layouts,
