@@ -39,6 +39,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <mutex>
 
 #include "fp8gb.h"
 #include "fp8gb_device.cuh"
@@ -1007,12 +1008,16 @@ __global__ void scales_kernel(float *sinv_row, int64_t n_row, float *sinv_col, i
 // and the whole quantize is one launch instead of six (three clears, two
 // passes, the scale conversion).
 //
-// The barrier counters live in a file-scope device array (no allocation):
-// RESIDENT_SLOTS counters, 128 bytes apart; each call takes the next slot in
-// turn, the host clears it on the stream before the launch, and barrier k
-// completes when the slot's counter reaches k * gridDim.x.  Calls on
-// different streams therefore use different counters as long as fewer than
-// RESIDENT_SLOTS of them are in flight at once.  Every block of a cooperative
+// The barrier counters are the kernel's only scratch memory, and they live
+// in a file-scope device array instead of an allocation: RESIDENT_SLOTS
+// counters, 128 bytes apart (8 KB in all, held by every device that loads
+// the library until the process exits).  Each call takes the next slot in
+// turn, clears that slot's counter on its stream before the launch (the
+// array keeps whatever the previous user of the slot left), and barrier k
+// completes when the counter reaches k * gridDim.x.  A call uses one counter
+// whatever the tensor size.  Calls that overlap on the GPU use different
+// counters while fewer than RESIDENT_SLOTS are in flight; past that, two
+// in-flight calls share a counter and race.  Every block of a cooperative
 // launch is resident, so every block reaches every barrier; the wait is
 // still bounded and records ERR_GRID_WAIT if it gives up.
 // ---------------------------------------------------------------------------
@@ -1302,6 +1307,35 @@ extern "C" fp8_status_t fp8_quantize(const void *x_bf16, int64_t rows, int64_t c
 
 namespace fp8gb {
 
+// Device address of g_resident_scratch on the current device.  In host code
+// the array's name denotes a host-side stand-in, not device memory, so the
+// address is looked up with cudaGetSymbolAddress: once per device, by the
+// first call made while that device is current, and kept for later calls.
+constexpr int RESIDENT_MAX_DEVICES = 64;
+static std::mutex g_resident_mu;
+static unsigned int *g_resident_ptr[RESIDENT_MAX_DEVICES];
+
+static unsigned int *resident_scratch(cudaError_t *e)
+{
+    int dev = 0;
+    if ((*e = cudaGetDevice(&dev)) != cudaSuccess) return nullptr;
+    if (dev < 0 || dev >= RESIDENT_MAX_DEVICES) {
+        *e = cudaErrorInvalidDevice;
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lk(g_resident_mu);
+    if (!g_resident_ptr[dev]) {
+        void *p = nullptr;
+        if ((*e = cudaGetSymbolAddress(&p, g_resident_scratch)) != cudaSuccess) {
+            cudaGetLastError();  // not sticky: clear it so later launch checks do not see it
+            return nullptr;
+        }
+        g_resident_ptr[dev] = static_cast<unsigned int *>(p);
+    }
+    *e = cudaSuccess;
+    return g_resident_ptr[dev];
+}
+
 template <int FMT, bool DO_ROW, bool DO_COLT>
 static fp8_status_t launch_resident(QArgs a, cudaStream_t st)
 {
@@ -1315,12 +1349,12 @@ static fp8_status_t launch_resident(QArgs a, cudaStream_t st)
     if (grid > n_tiles) grid = n_tiles;
     if (grid < 1) grid = 1;
     int64_t tiles_per_block = (n_tiles + grid - 1) / grid;
-    void *scratch = nullptr;
-    if (cudaGetSymbolAddress(&scratch, g_resident_scratch) != cudaSuccess) return cuda_fail();
+    cudaError_t se = cudaSuccess;
+    unsigned int *scratch = resident_scratch(&se);
+    if (!scratch) return cuda_fail_with(se);
     static std::atomic<unsigned int> next_slot{0};
-    unsigned int *count = static_cast<unsigned int *>(scratch) +
-                          (size_t)(next_slot.fetch_add(1, std::memory_order_relaxed) % RESIDENT_SLOTS) *
-                              RESIDENT_SLOT_WORDS;
+    unsigned int *count =
+        scratch + (size_t)(next_slot.fetch_add(1, std::memory_order_relaxed) % RESIDENT_SLOTS) * RESIDENT_SLOT_WORDS;
     if (cudaMemsetAsync(count, 0, sizeof(unsigned int), st) != cudaSuccess) return cuda_fail();
     void *args[] = {&a, &tiles_per_block, &count};
     const cudaError_t e = cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(k), dim3((unsigned)grid),
@@ -1360,7 +1394,8 @@ extern "C" fp8_status_t fp8_quantize_rowwise_resident(const void *x_bf16, int64_
         if (ld_colT < rows) return FP8_ERR_INVALID_ARG;
     }
     if (rows > ((int64_t)1 << 40) || cols > ((int64_t)1 << 31)) return FP8_ERR_INVALID_ARG;
-    if (rows == 0) return FP8_OK;
+    // rows == 0 still launches (one block, no tiles): like fp8_quantize it
+    // writes scale_inv_col = 1 and amax_out = 0 for an empty tensor
 
     QArgs a;
     a.x = static_cast<const uint16_t *>(x_bf16);

@@ -151,29 +151,50 @@ FP8GB_API fp8_status_t fp8_quantize(const void *x_bf16, int64_t rows, int64_t co
 
 /*
  * fp8_quantize_rowwise_resident -- the ROWWISE recipe of fp8_quantize for a
- * plain (ungrouped) tensor in one cooperative launch ("FP8 Training on AMD
- * GPUs with TorchTitan and TorchAO": rowwise FP8 and the colwise-scales
- * kernel; "How PyTorch FP8 Optimizations on AMD GPUs Reduce LLM Cost ...",
- * What Happened: fused quantize kernels instead of chains of memory-bound
- * launches).  The results are those of fp8_quantize with recipe kind
- * FP8_RECIPE_ROWWISE, margin `margin` and no groups, byte for byte: q_row,
- * q_colT, scale_inv_row [rows], scale_inv_col [cols] and the optional
- * amax_out [1] have the meanings, layouts and alignment rules given there.
+ * plain (ungrouped) tensor in one cooperative launch, for callers that
+ * cannot allocate device memory when they call.  The pages have no
+ * counterpart to this entry point: it is an interface choice of this
+ * library.
  *
- * One launch clears the amax accumulators, runs the row / column amax pass,
- * the cast pass and the scale_inv conversion, with grid-wide barriers in
- * between (all blocks of a cooperative launch are resident; each wait is
- * bounded and a wait that gives up is reported as FP8_ERR_TIMEOUT by
- * fp8_sync_status()).  For a tensor that fits in L2 (on GB300, up to about
- * 96 MB of bf16) the cast pass reads x back from L2; any size is correct.
+ * Results: those of fp8_quantize with recipe kind FP8_RECIPE_ROWWISE, margin
+ * `margin` and no groups, byte for byte -- q_row, q_colT, scale_inv_row
+ * [rows], scale_inv_col [cols] and the optional amax_out [1] have the
+ * meanings, layouts and alignment rules given there.  An empty tensor (rows
+ * == 0) writes scale_inv_col = 1 and amax_out = 0, as fp8_quantize does.
  *
- * The barriers count on one of 64 device counters held in a static array of
- * the library (nothing is allocated); each call takes the next counter in
- * turn and clears it on `stream` before its launch.  Calls on different
- * streams may overlap as long as fewer than 64 of them are in flight at
- * once; calls of every other entry point are unaffected.
+ * Why it exists.  One launch clears the amax accumulators, runs the row /
+ * column amax pass, the cast pass and the scale_inv conversion, with
+ * grid-wide barriers in between; for a tensor that fits in L2 (on GB300, up
+ * to about 96 MB of bf16) the cast pass reads x back from L2.  The barriers
+ * need a counter in global memory beyond the inputs and outputs.  A library
+ * would normally take that from a workspace the caller allocates or allocate
+ * it itself; this entry point does neither, because some callers cannot call
+ * cudaMalloc: a framework whose caching allocator owns all device memory
+ * (a cudaMalloc behind its back fragments its pool and can fail once the
+ * pool has taken the free memory), an engine that reserves a fixed memory
+ * budget up front, or a training step that must not stall, since cudaMalloc
+ * and cudaFree can synchronise the device.  It calls no cudaMalloc, cudaFree
+ * or allocating library routine.
  *
- * Returns FP8_ERR_CUDA if the cooperative launch is refused.
+ * Scratch.  The counters live in a file-scope device array of the library:
+ * 64 counters of 128 bytes (8 KB), present on every device that loads the
+ * library until the process exits.  A call uses one counter whatever the
+ * tensor size, so no tensor is refused for want of scratch; the size limits
+ * are those of fp8_quantize (rows <= 2^40, cols <= 2^31, else
+ * FP8_ERR_INVALID_ARG).  The first call on a device, made with that device
+ * current, looks up the array's device address (cudaGetSymbolAddress) and
+ * keeps it; make that first call before any stream capture on the device.
+ * Every call shares the array, which keeps what the last call left: each
+ * call takes the next counter in turn and clears it on `stream` before its
+ * launch.  Calls that overlap on the GPU (on different streams) use
+ * different counters while fewer than 64 are in flight at once; beyond
+ * that, two overlapping calls share a counter and race.  Calls of every
+ * other entry point are unaffected.
+ *
+ * Errors: FP8_ERR_INVALID_ARG / FP8_ERR_ALIGNMENT before any launch;
+ * FP8_ERR_CUDA if the address lookup or the cooperative launch fails; a
+ * barrier wait that gives up (about 2 s) is reported as FP8_ERR_TIMEOUT by
+ * fp8_sync_status().
  */
 FP8GB_API fp8_status_t fp8_quantize_rowwise_resident(const void *x_bf16, int64_t rows, int64_t cols, int64_t ld_x,
                                                      int fmt, int margin, int layouts, float *amax_out,

@@ -20,7 +20,7 @@ from fp8_mixed_precision_scale_gb300 import build as fp8build
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "fp8gb.h")
 
-OK, INVALID, UNSUPPORTED, ALIGN = 0, 1, 2, 3
+OK, INVALID, UNSUPPORTED, ALIGN, CUDA = 0, 1, 2, 3, 4
 
 
 @pytest.fixture(scope="module")
@@ -118,7 +118,10 @@ def r_call(lib, **kw):
 
 def test_resident_quantize_validation(lib):
     """The single-launch rowwise quantize checks what fp8_quantize checks for
-    a plain rowwise tensor; an empty tensor returns OK without a launch."""
+    a plain rowwise tensor.  An empty tensor passes validation and is
+    launched (it writes the column scales and the amax when asked for), so
+    without a GPU it gets as far as the CUDA error; the call asks for neither,
+    so on a GPU it touches no memory at all."""
     assert r_call(lib, x=None) == INVALID
     assert r_call(lib, rows=-1) == INVALID
     assert r_call(lib, cols=0) == INVALID
@@ -138,7 +141,8 @@ def test_resident_quantize_validation(lib):
     assert r_call(lib, q_row=FAKE + 4) == ALIGN
     assert r_call(lib, ld_colT=72) == ALIGN
     assert r_call(lib, ld_colT=48) == INVALID         # shorter than rows
-    assert r_call(lib, rows=0, x=None, q_row=None, sinv_row=None) == OK
+    assert r_call(lib, rows=0, x=None, layouts=1, q_row=None, sinv_row=None, q_colT=None,
+                  sinv_col=None) in (OK, CUDA)
 
 
 def g_call(lib, **kw):

@@ -1,12 +1,13 @@
 """GPU parity of fp8_quantize_rowwise_resident (the rowwise recipe in one
-cooperative launch) against the oracle, and byte-for-byte agreement with
-fp8_quantize's rowwise path."""
+cooperative launch) against the oracle, its argument checks and calls on two
+streams.  Its comparison with fp8_quantize's two-pass path (two calls in a
+row, every barrier counter reused, the empty tensor) is in
+test_zz_no_alloc.py."""
 import numpy as np
 import pytest
 import torch
 
 import fp8_mixed_precision_scale_gb300 as fp8
-import synth
 from parity import assert_codes_equal, assert_f32_bits_equal, bits
 from test_gpu_quantize import gen_x
 
@@ -68,23 +69,6 @@ def test_resident_special_values(orc):
     x[50, 9] = float("nan")
     x[77, :] = 1e-40
     check(orc, x, 1, what="specials")
-
-
-def test_resident_equals_two_pass_path():
-    """[8192, 4096] (the Llama-3-8B activation X, t4-distributed as in the
-    rowwise configuration): every byte and scale equal to fp8_quantize's
-    rowwise path, called twice in a row (the barrier counter is reused)."""
-    g = torch.Generator().manual_seed(3)
-    x = synth.student_t((8192, 4096), 4, g).to(DEV)
-    ref = fp8.quantize(x, 0, fp8.Recipe(kind=fp8.ROWWISE), 3)
-    for _ in range(2):
-        q = fp8.quantize_rowwise_resident(x, 0)
-        assert fp8.fp8_sync_status() == 0
-        assert torch.equal(q.q_row, ref.q_row)
-        assert torch.equal(q.q_colT[:, :8192], ref.q_colT[:, :8192])
-        assert torch.equal(q.scale_inv_row.view(torch.int32), ref.scale_inv_row.view(torch.int32))
-        assert torch.equal(q.scale_inv_col.view(torch.int32), ref.scale_inv_col.view(torch.int32))
-    del g
 
 
 def test_resident_rejects_bad_arguments():
