@@ -44,25 +44,32 @@ def bf16_to_f64(t: torch.Tensor) -> np.ndarray:
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
-def check_gemm(out, ref, bound, what=""):
+def check_gemm(out, ref, bound, what="", strict=False):
     """GEMM tolerance, elementwise:
 
-        |out - ref| <= 2e-3 * bound + 1e-5 + 2^-8 * max(|ref|, |out|)
+        |out - ref| <= 2e-3 * bound + 1e-5            (the stated bound)
+                       + 2^-8 * max(|ref|, |out|)     only where |ref| > bound / 16
 
-    The first two terms are the stated accumulation bound; the last is the
-    bf16 output cast (half a bf16 ulp), which no bf16 output can avoid: where
-    one product dominates a sum (|ref| close to bound, as with the tiny
-    workload's 50x outliers) half an ulp exceeds 2e-3 * bound.
-    Returns the largest err / bound seen (the strict-bound margin).
+    The last term is the bf16 output cast (half a bf16 ulp), which no bf16
+    output can avoid where one product dominates a sum (|ref| close to bound,
+    as with the tiny workload's 50x outliers: there half an ulp exceeds
+    2e-3 * bound).  Where |ref| <= bound / 16 the cast moves a value by at most
+    2^-12 * bound, which fits inside the stated bound together with the fp32
+    accumulation error, so the stated bound alone applies.  strict=True asserts
+    the stated bound on every element (random-sign data at large K, where
+    |ref| / bound is about 1 / sqrt(K)).
+    Returns the largest err / bound seen (the margin against 2e-3).
     """
     out = np.asarray(out, np.float64)
     err = np.abs(out - ref)
-    lim = TOL_REL * bound + TOL_ABS + BF16_HALF_ULP_REL * np.maximum(np.abs(ref), np.abs(out))
+    lim = TOL_REL * bound + TOL_ABS
+    if not strict:
+        lim = lim + np.where(np.abs(ref) > bound / 16, BF16_HALF_ULP_REL * np.maximum(np.abs(ref), np.abs(out)), 0.0)
     bad = ~(err <= lim)
     if bad.any():
         i = np.argwhere(bad)[:6]
-        raise AssertionError(f"{what}: {int(bad.sum())}/{bad.size} outside tolerance; first {i.tolist()}: "
-                             f"out {out[bad][:6]} ref {ref[bad][:6]} bound {bound[bad][:6]}")
+        raise AssertionError(f"{what}: {int(bad.sum())}/{bad.size} outside tolerance{' (strict)' if strict else ''}; "
+                             f"first {i.tolist()}: out {out[bad][:6]} ref {ref[bad][:6]} bound {bound[bad][:6]}")
     denom = np.where(bound > 0, bound, 1.0)
     return float((err / denom).max()) if err.size else 0.0
 

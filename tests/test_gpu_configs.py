@@ -38,8 +38,9 @@ def sync_ok():
     assert fp8.fp8_sync_status() == 0
 
 
-def sampled_gemm_check(orc, A, fa, B, fb, sa, sb, C, seed, what, n_rows=8, n_cols=8, n_rand=2048):
-    """Check C = A.B^T * sa * sb on sampled full rows, full columns and random points."""
+def sampled_gemm_check(orc, A, fa, B, fb, sa, sb, C, seed, what, n_rows=8, n_cols=8, n_rand=2048, strict=False):
+    """Check C = A.B^T * sa * sb on sampled full rows, full columns and random
+    points (strict: the stated bound alone, for random-sign data at large K)."""
     M, K = A.shape
     N = B.shape[0]
     g = torch.Generator().manual_seed(seed)
@@ -52,7 +53,7 @@ def sampled_gemm_check(orc, A, fa, B, fb, sa, sb, C, seed, what, n_rows=8, n_col
     out = C[torch.from_numpy(pm).to(DEV), torch.from_numpy(pn).to(DEV)].float().cpu().numpy()
     ref, bound = orc.gemm(A.cpu().numpy(), fa, B.cpu().numpy(), fb, sa.cpu().numpy(), sb.cpu().numpy(),
                           points=(pm, pn))
-    check_gemm(out, ref, bound, what)
+    check_gemm(out, ref, bound, what, strict=strict)
 
 
 # --------------------------------------------------------------------------------------------
@@ -185,7 +186,7 @@ def run_delayed(orc, base, fmts, algo, gemms, steps=50, full_steps=(0, 30, 49), 
                 C = fp8.scaled_gemm(A, fmts[a], B, fmts[b], sa, sb, K=K)
                 sync_ok()
                 sampled_gemm_check(orc, A[:, :K], fmts[a], B[:, :K], fmts[b], sa, sb, C, seed=t * 10 + gi,
-                                   what=f"t{t} gemm {a}.{al} x {b}.{bl}")
+                                   what=f"t{t} gemm {a}.{al} x {b}.{bl}", strict=True)
                 del C
         lay.update()
         orc.update_amax_history(hist_o, scale_o, sinv_o, fmt_np, algo, 0)
@@ -363,7 +364,7 @@ def test_config4_moe_layer(orc):
             ref, bound = orc.gemm(cpu(Arow[r0:r1]), fa, Bexp(e), fb, cpu(qa.scale_inv_row[r0:r1]), sbexp(e),
                                   points=(pm, pn))
             out = C[torch.from_numpy(pm + r0).to(DEV), torch.from_numpy(pn).to(DEV)].float().cpu().numpy()
-            check_gemm(out, ref, bound, f"{name} expert {e}")
+            check_gemm(out, ref, bound, f"{name} expert {e}", strict=True)
     # wgrad of the gate projection: dW_e = dY_e^T X_e over the group's rows
     ldT = qt["xp"].ld_colT
     scg = qt["dy_gate"].scale_inv_col.view(E, F)

@@ -61,7 +61,7 @@ def test_gemm_realistic_values(orc):
     sa, sb = scales(g, M, True), scales(g, N, True)
     C = run_gemm(A, 0, B, 1, sa, sb)
     ref, bound = orc.gemm(A.numpy(), 0, B.numpy(), 1, sa.numpy(), sb.numpy())
-    check_gemm(C.float().cpu().numpy(), ref, bound, "realistic")
+    check_gemm(C.float().cpu().numpy(), ref, bound, "realistic", strict=True)
 
 
 def test_gemm_padded_leading_dims(orc):
@@ -122,7 +122,7 @@ def _sampled(orc, M, N, K, fa, fb, seed, per_row=True):
     pm, pn = sample_points(g, M, N)
     out = C[torch.from_numpy(pm).to(DEV), torch.from_numpy(pn).to(DEV)].float().cpu().numpy()
     ref, bound = orc.gemm(A.cpu().numpy(), fa, B.cpu().numpy(), fb, sa.numpy(), sb.numpy(), points=(pm, pn))
-    return check_gemm(out, ref, bound, f"{M}x{N}x{K}")
+    return check_gemm(out, ref, bound, f"{M}x{N}x{K}", strict=True)
 
 
 def test_gemm_llama_gate_fprop_sampled(orc):

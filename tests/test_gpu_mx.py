@@ -217,7 +217,7 @@ def test_mx_gemm_llama_gate_sampled(orc):
     g = torch.Generator().manual_seed(5)
     pm, pn = sample_points(g, M, N, n_rows=16, n_cols=16, n_rand=4096)
     ref, bound = orc.mx_gemm(A, 0, sA, B, 0, sB, points=(pm, pn))
-    check_gemm(C.float().cpu().numpy()[pm, pn], ref, bound, "llama gate")
+    check_gemm(C.float().cpu().numpy()[pm, pn], ref, bound, "llama gate", strict=True)
 
 
 # --- grouped GEMM ------------------------------------------------------------
