@@ -40,6 +40,8 @@ Other workloads (same JSON line, their own config):
   mx_permute, mx_swiglu  fused MoE prologue + MX quantize at DeepSeek-V3
                  shapes (gather of 4096 x top-8 routed rows of 7168; SwiGLU
                  of [32768, 2 x 2048]), also timed against the unfused chain
+  permute, swiglu  the same prologues fused into the rowwise quantize with
+                 per-expert column scales, also timed against the unfused chain
 
 Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle on a
 bounded sample of the same workload instead.
@@ -803,7 +805,8 @@ def run_gpu(args, rank, world, local_rank):
     fp8_peak = 2.0 * bf16_sust               # FP8 dense = 2x bf16 dense (nominal 4.5 vs 2.25 PFLOP/s)
 
     if args.workload in ("gemm", "quantize", "grouped_m", "grouped_k", "quantize_grouped", "mx_gemm", "mx_quantize",
-                         "mx_permute", "mx_swiglu", "bw_quantize", "rowwise_quantize", "rowwise_resident"):
+                         "mx_permute", "mx_swiglu", "permute", "swiglu", "bw_quantize", "rowwise_quantize",
+                         "rowwise_resident"):
         run_single_kernel(args, dev, rank)
         return
     if args.workload == "sweep":
@@ -1100,7 +1103,23 @@ def moe_fused_case(kind, dev, T=4096, topk=8, E=256):
         unfused = lambda: fp8.mx_quantize(x.index_select(0, src64), 0, 3, group_offsets=off,  # noqa: E731
                                           host_offsets=off_h)
         return fused, unfused, rows * H * (2 + 2 + 2 / 32) / 1e9
+    if kind == "permute":   # rowwise recipe, per-expert column scales
+        x = _normal(g, dev, (T, H), 1.0)
+        fused = lambda: fp8.permute_quantize(x, src, 0, off, off_h)  # noqa: E731
+        src64 = src.long()
+        rec = fp8.Recipe(kind=fp8.ROWWISE)
+        unfused = lambda: fp8.quantize(x.index_select(0, src64), 0, rec, group_offsets=off,  # noqa: E731
+                                       host_offsets=off_h)
+        return fused, unfused, rows * H * 4 / 1e9
     gu = _normal(g, dev, (rows, 2 * F), 2.0)
+    if kind == "swiglu":    # rowwise recipe, per-expert column scales
+        fused = lambda: fp8.swiglu_quantize(gu, 0, off, off_h)  # noqa: E731
+        rec = fp8.Recipe(kind=fp8.ROWWISE)
+
+        def unfused_rw():
+            h = (torch.nn.functional.silu(gu[:, :F].float()) * gu[:, F:].float()).to(torch.bfloat16)
+            return fp8.quantize(h, 0, rec, group_offsets=off, host_offsets=off_h)
+        return fused, unfused_rw, rows * F * (4 + 2) / 1e9
     fused = lambda: fp8.mx_swiglu_quantize(gu, 0, 3, group_offsets=off, host_offsets=off_h)  # noqa: E731
 
     def unfused():
@@ -1113,7 +1132,7 @@ def run_single_kernel(args, dev, rank):
     """Time one kernel of the default step in isolation (profiling aid)."""
     import fp8_mixed_precision_scale_gb300 as fp8
     unfused = None
-    if args.workload in ("mx_permute", "mx_swiglu"):
+    if args.workload in ("mx_permute", "mx_swiglu", "permute", "swiglu"):
         fn, unfused, work = moe_fused_case(args.workload, dev)
         unit = "GB/s (algorithmic)"
     elif args.workload in ("grouped_m", "grouped_k"):
@@ -1228,7 +1247,7 @@ def main():
                              "sweep",
                              "gemm", "quantize", "bw_quantize", "rowwise_quantize", "rowwise_resident",
                              "grouped_m", "grouped_k", "quantize_grouped", "mx_gemm", "mx_quantize", "mx_permute",
-                             "mx_swiglu"],
+                             "mx_swiglu", "permute", "swiglu"],
                     help="llama_mlp: the whole fwd+bwd FP8 step of the Llama-3-8B MLP (default); see the "
                          "module docstring for the others")
     args = ap.parse_args()

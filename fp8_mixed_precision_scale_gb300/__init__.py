@@ -41,7 +41,7 @@ EXPORTED = ("fp8_quantize", "fp8_update_amax_history", "fp8_scaled_gemm", "fp8_g
             "fp8_group_padded_offsets", "fp8_sync_status", "fp8_selftest_bounded_wait", "fp8_status_string",
             "fp8_last_cuda_error", "fp8_version", "fp8_mx_scale_bytes", "fp8_mx_quantize", "fp8_mx_gemm",
             "fp8_mx_grouped_gemm", "fp8_mx_permute_quantize", "fp8_mx_swiglu_quantize", "fp8_blockwise_quantize",
-            "fp8_quantize_rowwise_resident")
+            "fp8_quantize_rowwise_resident", "fp8_permute_quantize", "fp8_swiglu_quantize")
 MX_BLOCK = 32
 MX_GROUP_ALIGN = 128
 
@@ -100,6 +100,11 @@ def load_library():
                                          i64, P, P, i32, P]
             lib.fp8_quantize_rowwise_resident.restype = i32
             lib.fp8_quantize_rowwise_resident.argtypes = [P, i64, i64, i64, i32, i32, i32, P, P, P, P, i64, P, P]
+            lib.fp8_permute_quantize.restype = i32
+            lib.fp8_permute_quantize.argtypes = [P, i64, i64, i64, P, i64, i32, i32, i32, P, P, P, P, i64, P, P, i32,
+                                                 P]
+            lib.fp8_swiglu_quantize.restype = i32
+            lib.fp8_swiglu_quantize.argtypes = [P, i64, i64, i64, i32, i32, i32, P, i64, P, P, P, P, i64, P, P, i32, P]
             lib.fp8_update_amax_history.restype = i32
             lib.fp8_update_amax_history.argtypes = [P, P, P, P, i32, i32, i32, i32, P, P]
             lib.fp8_scaled_gemm.restype = i32
@@ -250,6 +255,27 @@ def fp8_quantize_rowwise_resident(x, rows, cols, ld_x, fmt, margin, layouts, ama
     return rc
 
 
+def fp8_permute_quantize(x, x_rows, cols, ld_x, src_rows, rows, fmt, margin, layouts, amax_out, q_row,
+                         scale_inv_row, q_colT, ld_colT, scale_inv_col, group_offsets, num_groups, stream=None,
+                         check=True):
+    rc = load_library().fp8_permute_quantize(_p(x), x_rows, cols, ld_x, _p(src_rows), rows, fmt, margin, layouts,
+                                             _p(amax_out), _p(q_row), _p(scale_inv_row), _p(q_colT), ld_colT,
+                                             _p(scale_inv_col), _p(group_offsets), num_groups, _stream(stream))
+    if check:
+        _check(rc, "fp8_permute_quantize")
+    return rc
+
+
+def fp8_swiglu_quantize(gate_up, rows, F, ld, fmt, margin, layouts, h, ld_h, amax_out, q_row, scale_inv_row,
+                        q_colT, ld_colT, scale_inv_col, group_offsets, num_groups, stream=None, check=True):
+    rc = load_library().fp8_swiglu_quantize(_p(gate_up), rows, F, ld, fmt, margin, layouts, _p(h), ld_h,
+                                            _p(amax_out), _p(q_row), _p(scale_inv_row), _p(q_colT), ld_colT,
+                                            _p(scale_inv_col), _p(group_offsets), num_groups, _stream(stream))
+    if check:
+        _check(rc, "fp8_swiglu_quantize")
+    return rc
+
+
 def fp8_blockwise_quantize(x, rows, cols, ld_x, fmt, block_rows, layouts, q_row, s_row, q_colT, ld_colT, s_col,
                            stream=None, check=True):
     rc = load_library().fp8_blockwise_quantize(_p(x), rows, cols, ld_x, fmt, block_rows, layouts, _p(q_row),
@@ -348,6 +374,49 @@ def quantize_rowwise_resident(x: torch.Tensor, fmt: int, margin: int = 0, layout
     fp8_quantize_rowwise_resident(x, rows, cols, x.stride(0), fmt, margin, layouts, amax_out, q_row, sr, q_colT,
                                   ld_colT, sc, stream)
     return Quantized(q_row, sr, q_colT, sc, ld_colT)
+
+
+def _rowwise_outputs(rows, cols, dev, layouts, host_offsets):
+    G = len(host_offsets) - 1
+    ld_colT, _ = fp8_group_padded_offsets(host_offsets)
+    ld_colT = max(16, (ld_colT + 15) // 16 * 16)
+    q_row = sr = q_colT = sc = None
+    if layouts & LAYOUT_ROW:
+        q_row = torch.empty((rows, cols), dtype=torch.uint8, device=dev)
+        sr = torch.empty(max(rows, 1), dtype=torch.float32, device=dev)
+    if layouts & LAYOUT_COLT:
+        q_colT = torch.empty((cols, ld_colT), dtype=torch.uint8, device=dev)
+        sc = torch.empty(cols * G, dtype=torch.float32, device=dev)
+    return Quantized(q_row, sr, q_colT, sc, ld_colT)
+
+
+def permute_quantize(x: torch.Tensor, src_rows: torch.Tensor, fmt: int, group_offsets, host_offsets,
+                     layouts: int = LAYOUT_ROW | LAYOUT_COLT, margin: int = 0, amax_out=None,
+                     stream=None) -> Quantized:
+    """Gather x[src_rows] (routed token rows in expert order) and quantize it
+    with the rowwise recipe, per-expert column scales, in one pass."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1 and src_rows.dtype == torch.int32
+    rows, cols = src_rows.numel(), x.shape[1]
+    q = _rowwise_outputs(rows, cols, x.device, layouts, host_offsets)
+    fp8_permute_quantize(x, x.shape[0], cols, x.stride(0), src_rows, rows, fmt, margin, layouts, amax_out, q.q_row,
+                         q.scale_inv_row, q.q_colT, q.ld_colT, q.scale_inv_col, group_offsets,
+                         group_offsets.numel() - 1, stream)
+    return q
+
+
+def swiglu_quantize(gate_up: torch.Tensor, fmt: int, group_offsets, host_offsets,
+                    layouts: int = LAYOUT_ROW | LAYOUT_COLT, h_out=None, margin: int = 0, amax_out=None,
+                    stream=None) -> Quantized:
+    """h = bf16(silu(gate) * up) of a [rows, 2F] gate|up tensor, quantized
+    with the rowwise recipe, per-expert column scales, in one pass (h also
+    written to h_out when given)."""
+    assert gate_up.dtype == torch.bfloat16 and gate_up.dim() == 2 and gate_up.stride(1) == 1
+    rows, F = gate_up.shape[0], gate_up.shape[1] // 2
+    q = _rowwise_outputs(rows, F, gate_up.device, layouts, host_offsets)
+    fp8_swiglu_quantize(gate_up, rows, F, gate_up.stride(0), fmt, margin, layouts, h_out,
+                        h_out.stride(0) if h_out is not None else 0, amax_out, q.q_row, q.scale_inv_row, q.q_colT,
+                        q.ld_colT, q.scale_inv_col, group_offsets, group_offsets.numel() - 1, stream)
+    return q
 
 
 def scaled_gemm(A: torch.Tensor, fa: int, B: torch.Tensor, fb: int, sa: torch.Tensor, sb: torch.Tensor, K=None,

@@ -467,4 +467,43 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return r;
 }
 
+// ---------------------------------------------------------------------------
+// SwiGLU element function shared by the fused MoE prologues of the MX and
+// the rowwise quantizers.
+// ---------------------------------------------------------------------------
+// fp32 -> bf16 bits, round to nearest even; NaN stays a quiet NaN.
+__device__ __forceinline__ uint32_t bf16_bits_rne(float f)
+{
+    uint32_t u = __float_as_uint(f);
+    if ((u & 0x7FFFFFFFu) > 0x7F800000u) return (u >> 16) | 0x40u;
+    u += 0x7FFFu + ((u >> 16) & 1u);
+    return u >> 16;
+}
+
+// silu(g) * u in fp32, with sigma(g) = 1 / (1 + e^-g) formed from t = e^-|g|
+// (never overflows): sigma = 1 / (1 + t) for g >= 0, t / (1 + t) for g < 0.
+// For g < 0 the product is carried scaled by 2^126 (t is computed as 2^126
+// e^-|g|, a normal fp32 for |g| < 174) and unscaled by the last multiply,
+// applied to u first when |u| >= 1, so no intermediate overflows or turns
+// subnormal before the end.  __expf and __fdividef (1 + t lies in [1, 2])
+// err by far less than 2^-9 relative, so the bf16 rounding of the result is
+// within one bf16 ulp of the exact bf16_rne(silu(g) * u) for every g when
+// |u| <= 2^110 (NaN, +-Inf and the sign of zero as IEEE arithmetic gives
+// them; silu(-Inf) = -0).
+__device__ __forceinline__ float swiglu1(float g, float u)
+{
+    constexpr float LN2_X126 = 87.3365479f;  // 126 ln 2: e^(x + 126 ln 2) = 2^126 e^x
+    const float t = __expf(LN2_X126 - fabsf(g));
+    const float r = __fdividef(1.0f, fmaf(t, 0x1p-126f, 1.0f));
+    if (g >= 0.0f) return (g * r) * u;
+    const float s = t == 0.0f ? -0.0f : g * (t * r);  // 2^126 silu(g); t == 0 also for g = -Inf
+    return fabsf(u) >= 1.0f ? s * (u * 0x1p-126f) : (s * u) * 0x1p-126f;
+}
+
+// h = bf16(silu(g) * u) for a packed pair.
+__device__ __forceinline__ uint32_t swiglu2(uint32_t g2, uint32_t u2)
+{
+    return bf16_bits_rne(swiglu1(bf16lo(g2), bf16lo(u2))) | (bf16_bits_rne(swiglu1(bf16hi(g2), bf16hi(u2))) << 16);
+}
+
 }  // namespace fp8gb

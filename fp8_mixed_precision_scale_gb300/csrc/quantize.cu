@@ -71,7 +71,51 @@ struct QArgs {
     int scales_ready;  // rowwise cast pass: the scale buffers already hold scales (else amaxes)
     int sup_blocks;  // rowwise amax pass: 32-row blocks per super tile (1..8)
     int sup_chunks;  // rowwise amax pass: 128-column chunks per super tile (1..8)
+    // fused MoE prologues of the grouped rowwise passes (template parameter PRO)
+    const int32_t *src_rows;  // QPRO_GATHER: row r of the tensor is row src_rows[r] of x
+    int64_t x_rows;           // QPRO_GATHER: rows of x
+    int64_t up_off;           // QPRO_SWIGLU: column offset of `up` in each row of x
+    uint16_t *h_out;          // QPRO_SWIGLU: optional bf16 copy of h, [rows][ld_h]
+    int64_t ld_h;
 };
+
+// Prologues of the grouped rowwise passes: the tensor is x itself, the
+// gathered rows x[src_rows[r]], or h = bf16(silu(gate) * up) of the two
+// halves of each row of x.  Both passes apply the prologue to what they
+// read, so neither the gathered tensor nor h is ever written to memory
+// (except the optional copy of h).
+enum { QPRO_NONE = 0, QPRO_GATHER = 1, QPRO_SWIGLU = 2 };
+
+// input row of tensor row r: x's own row, or src_rows[r] (checked: an index
+// outside x is reported and reads as a zero row, -1)
+template <int PRO>
+__device__ __forceinline__ int64_t pro_src_row(const QArgs &a, int64_t r)
+{
+    if constexpr (PRO == QPRO_GATHER) {
+        const int64_t s = __ldg(a.src_rows + r);
+        if (s < 0 || s >= a.x_rows) {
+            record_error(a.err, ERR_BAD_INDEX);
+            return -1;
+        }
+        return s;
+    } else {
+        return r;
+    }
+}
+
+// eight bf16 of the tensor at input row `src` (-1: zeros), columns col .. col + 7
+template <int PRO>
+__device__ __forceinline__ uint4 pro_load8(const QArgs &a, int64_t src, int64_t col)
+{
+    if (src < 0) return make_uint4(0, 0, 0, 0);
+    const uint16_t *p = a.x + src * a.ld_x + col;
+    if constexpr (PRO == QPRO_SWIGLU) {
+        const uint4 g = __ldg(reinterpret_cast<const uint4 *>(p)), u = __ldg(reinterpret_cast<const uint4 *>(p + a.up_off));
+        return make_uint4(swiglu2(g.x, u.x), swiglu2(g.y, u.y), swiglu2(g.z, u.z), swiglu2(g.w, u.w));
+    } else {
+        return __ldg(reinterpret_cast<const uint4 *>(p));
+    }
+}
 
 // Row-block geometry: which input rows a tile covers and where they land in
 // the transposed layout.
@@ -487,6 +531,7 @@ __device__ __forceinline__ void flush_col_amax(const QArgs &a, uint32_t (&cacc)[
     for (int k = 0; k < 4; k++) cacc[k] = 0;
 }
 
+template <int PRO>
 __global__ void __launch_bounds__(QT_THREADS) rowcol_amax_kernel(QArgs a)
 {
     extern __shared__ __align__(16) unsigned char dsm[];
@@ -494,6 +539,7 @@ __global__ void __launch_bounds__(QT_THREADS) rowcol_amax_kernel(QArgs a)
     __shared__ uint32_t red[QT_THREADS / 32];
     __shared__ uint32_t colw[QT_THREADS / 32][16][4];
     __shared__ RowBlock srb[SUP_BLOCKS];
+    __shared__ int64_t ssrc[PRO == QPRO_NONE ? 1 : SUP_BLOCKS * 32];  // input row of each row of the super tile
     __shared__ int bad;
     if (a.offsets) {
         compute_padded_offsets(a.offsets, a.G, a.rows, 0, poff, &bad, a.err);
@@ -518,6 +564,14 @@ __global__ void __launch_bounds__(QT_THREADS) rowcol_amax_kernel(QArgs a)
             }
         }
         __syncthreads();
+        if constexpr (PRO != QPRO_NONE) {
+            if (t < SUP_BLOCKS * 32) {
+                const RowBlock &rb = srb[t >> 5];
+                const int r = t & 31;
+                ssrc[t] = !rb.skip && r < rb.valid ? pro_src_row<PRO>(a, rb.in_row0 + r) : -1;
+            }
+            __syncthreads();
+        }
         uint32_t rmax[SUP_BLOCKS][2];
 #pragma unroll
         for (int kb = 0; kb < SUP_BLOCKS; kb++) rmax[kb][0] = rmax[kb][1] = 0;
@@ -534,10 +588,14 @@ __global__ void __launch_bounds__(QT_THREADS) rowcol_amax_kernel(QArgs a)
 #pragma unroll
                 for (int h = 0; h < 2; h++) {
                     const int r = h * 16 + roff;
-                    if (ok && !rb.skip && r < rb.valid)
-                        v[kk][h] = __ldg(reinterpret_cast<const uint4 *>(a.x + (rb.in_row0 + r) * a.ld_x + col));
-                    else
-                        v[kk][h] = make_uint4(0, 0, 0, 0);
+                    if constexpr (PRO == QPRO_NONE) {
+                        if (ok && !rb.skip && r < rb.valid)
+                            v[kk][h] = __ldg(reinterpret_cast<const uint4 *>(a.x + (rb.in_row0 + r) * a.ld_x + col));
+                        else
+                            v[kk][h] = make_uint4(0, 0, 0, 0);
+                    } else {
+                        v[kk][h] = pro_load8<PRO>(a, ok ? ssrc[(hf * (SUP_BLOCKS / 2) + kk) * 32 + r] : -1, col);
+                    }
                 }
             }
         };
@@ -815,9 +873,10 @@ constexpr int GT_ROWS = 32 * GT_BLOCKS;
 // the row's 8-row chunk, so the transposed read of a chunk spreads over banks
 __device__ __forceinline__ int gt_word(int r, int w) { return r * (GT_COLS / 4) + (w ^ ((r >> 3) & 15)); }
 
-template <int FMT, int SMODE, bool DELAYED, bool DO_ROW, bool DO_COLT>
+template <int FMT, int SMODE, bool DELAYED, bool DO_ROW, bool DO_COLT, int PRO = QPRO_NONE>
 __global__ void __launch_bounds__(QT_THREADS, 6) grouped_cast_kernel(QArgs a)
 {
+    __shared__ int64_t ssrc[PRO == QPRO_NONE ? 1 : GT_ROWS];  // input row of each row of the tile
     extern __shared__ __align__(16) unsigned char dsm[];
     int32_t *poff = reinterpret_cast<int32_t *>(dsm);
     __shared__ uint32_t tileT[GT_ROWS * GT_COLS / 4];
@@ -864,15 +923,31 @@ __global__ void __launch_bounds__(QT_THREADS, 6) grouped_cast_kernel(QArgs a)
         if (srb[0].skip) break;  // past the padded total: so is every later tile of this block
         const int64_t col = c0 + cg * 8;
         const bool col_ok = col < a.cols;
+        if constexpr (PRO != QPRO_NONE) {
+            if (t < GT_ROWS) {
+                const RowBlock &rb = srb[t >> 5];
+                const int r = t & 31;
+                ssrc[t] = !rb.skip && r < rb.valid ? pro_src_row<PRO>(a, rb.in_row0 + r) : -1;
+            }
+            __syncthreads();
+        }
 
         uint4 v[GT_BLOCKS];
 #pragma unroll
         for (int i = 0; i < GT_BLOCKS; i++) {
             const RowBlock &rb = srb[i];
-            if (!rb.skip && col_ok && roff < rb.valid)
-                v[i] = __ldg(reinterpret_cast<const uint4 *>(a.x + (rb.in_row0 + roff) * a.ld_x + col));
-            else
-                v[i] = make_uint4(0, 0, 0, 0);
+            if constexpr (PRO == QPRO_NONE) {
+                if (!rb.skip && col_ok && roff < rb.valid)
+                    v[i] = __ldg(reinterpret_cast<const uint4 *>(a.x + (rb.in_row0 + roff) * a.ld_x + col));
+                else
+                    v[i] = make_uint4(0, 0, 0, 0);
+            } else {
+                v[i] = pro_load8<PRO>(a, col_ok ? ssrc[i * 32 + roff] : -1, col);
+                if constexpr (PRO == QPRO_SWIGLU) {
+                    if (a.h_out && !rb.skip && col_ok && roff < rb.valid)
+                        *reinterpret_cast<uint4 *>(a.h_out + (rb.in_row0 + roff) * a.ld_h + col) = v[i];
+                }
+            }
         }
         if constexpr (SMODE == 1) {
             if (DO_ROW && t < GT_ROWS) {
@@ -1114,27 +1189,27 @@ static int blocks_for(K kernel, size_t dyn_smem, int64_t n_tiles, bool persisten
     return (int)g;
 }
 
-template <int FMT, int SMODE, bool DELAYED>
+template <int FMT, int SMODE, bool DELAYED, int PRO = QPRO_NONE>
 static fp8_status_t launch_grouped_cast(const QArgs &a, int layouts, size_t group_smem, cudaStream_t st)
 {
     const int64_t n_tiles = (a.n_row_blocks + GT_BLOCKS - 1) / GT_BLOCKS * ((a.cols + GT_COLS - 1) / GT_COLS);
     if (layouts == (FP8_LAYOUT_ROW | FP8_LAYOUT_COLT)) {
-        auto k = grouped_cast_kernel<FMT, SMODE, DELAYED, true, true>;
+        auto k = grouped_cast_kernel<FMT, SMODE, DELAYED, true, true, PRO>;
         k<<<blocks_for(k, group_smem, n_tiles, true), QT_THREADS, group_smem, st>>>(a);
     } else if (layouts == FP8_LAYOUT_ROW) {
-        auto k = grouped_cast_kernel<FMT, SMODE, DELAYED, true, false>;
+        auto k = grouped_cast_kernel<FMT, SMODE, DELAYED, true, false, PRO>;
         k<<<blocks_for(k, group_smem, n_tiles, true), QT_THREADS, group_smem, st>>>(a);
     } else {
-        auto k = grouped_cast_kernel<FMT, SMODE, DELAYED, false, true>;
+        auto k = grouped_cast_kernel<FMT, SMODE, DELAYED, false, true, PRO>;
         k<<<blocks_for(k, group_smem, n_tiles, true), QT_THREADS, group_smem, st>>>(a);
     }
     return check_launch();
 }
 
-template <int FMT, int RB, int SMODE, bool DELAYED>
+template <int FMT, int RB, int SMODE, bool DELAYED, int PRO = QPRO_NONE>
 static fp8_status_t launch_cast(const QArgs &a, int layouts, size_t group_smem, cudaStream_t st)
 {
-    if (a.offsets) return launch_grouped_cast<FMT, SMODE, DELAYED>(a, layouts, group_smem, st);
+    if (a.offsets) return launch_grouped_cast<FMT, SMODE, DELAYED, PRO>(a, layouts, group_smem, st);
     if constexpr (RB == 32) {
         return FP8_ERR_INVALID_ARG;  // 32-row blocks are the grouped layout's; plain tensors use 64
     } else {
@@ -1154,7 +1229,7 @@ static fp8_status_t launch_cast(const QArgs &a, int layouts, size_t group_smem, 
     }
 }
 
-template <int FMT, int RB>
+template <int FMT, int RB, int PRO = QPRO_NONE>
 static fp8_status_t run_quantize(QArgs a, int kind, int layouts, cudaStream_t st)
 {
     const size_t group_smem = a.offsets ? 2 * sizeof(int32_t) * (size_t)(a.G + 1) : 0;  // poff + offsets
@@ -1206,7 +1281,7 @@ static fp8_status_t run_quantize(QArgs a, int kind, int layouts, cudaStream_t st
                 b.sup_blocks /= 2;
         }
         const int64_t n_super = n_super_of(b);
-        rowcol_amax_kernel<<<(unsigned)(n_super < 1 ? 1 : (n_super < INT32_MAX ? n_super : INT32_MAX)), QT_THREADS,
+        rowcol_amax_kernel<PRO><<<(unsigned)(n_super < 1 ? 1 : (n_super < INT32_MAX ? n_super : INT32_MAX)), QT_THREADS,
                              group_smem, st>>>(b);
         if ((s = check_launch()) != FP8_OK) return s;
     }
@@ -1220,7 +1295,7 @@ static fp8_status_t run_quantize(QArgs a, int kind, int layouts, cudaStream_t st
         scales_kernel<<<sgrid, 256, 0, st>>>(a.sinv_row, n_row, a.sinv_col, n_col, fp8_max_of(FMT), a.margin, 0);
         if ((s = check_launch()) != FP8_OK) return s;
     }
-    if ((s = launch_cast<FMT, RB, 1, false>(a, layouts, group_smem, st)) != FP8_OK) return s;
+    if ((s = launch_cast<FMT, RB, 1, false, PRO>(a, layouts, group_smem, st)) != FP8_OK) return s;
     if (total > 0) {
         scales_kernel<<<sgrid, 256, 0, st>>>(a.sinv_row, n_row, a.sinv_col, n_col, fp8_max_of(FMT), a.margin,
                                              a.scales_ready ? 1 : 2);
@@ -1267,7 +1342,7 @@ extern "C" fp8_status_t fp8_quantize(const void *x_bf16, int64_t rows, int64_t c
     // grouped padded offsets are int32 on the device
     if (group_offsets && (rows + 32LL * num_groups > INT32_MAX || ld_colT > INT32_MAX)) return FP8_ERR_INVALID_ARG;
 
-    QArgs a;
+    QArgs a{};
     a.x = static_cast<const uint16_t *>(x_bf16);
     a.rows = rows;
     a.cols = cols;
@@ -1397,7 +1472,7 @@ extern "C" fp8_status_t fp8_quantize_rowwise_resident(const void *x_bf16, int64_
     // rows == 0 still launches (one block, no tiles): like fp8_quantize it
     // writes scale_inv_col = 1 and amax_out = 0 for an empty tensor
 
-    QArgs a;
+    QArgs a{};
     a.x = static_cast<const uint16_t *>(x_bf16);
     a.rows = rows;
     a.cols = cols;
@@ -1423,4 +1498,105 @@ extern "C" fp8_status_t fp8_quantize_rowwise_resident(const void *x_bf16, int64_
     if (fmt == FP8_E4M3FNUZ) return run_resident<FP8_E4M3FNUZ>(a, layouts, st);
     if (fmt == FP8_E5M2FNUZ) return run_resident<FP8_E5M2FNUZ>(a, layouts, st);
     return run_resident<FP8_E4M3FN>(a, layouts, st);
+}
+
+// ---------------------------------------------------------------------------
+// Fused MoE prologues of the ROWWISE recipe (grouped tensors): the gather of
+// routed token rows into expert order, and SwiGLU of the gate|up projection
+// output, applied by both grouped passes to what they read.
+// ---------------------------------------------------------------------------
+static fp8_status_t prologue_args(QArgs &a, int fmt, int margin, int layouts, uint8_t *q_row, float *scale_inv_row,
+                                  uint8_t *q_colT, int64_t ld_colT, float *scale_inv_col, const int32_t *group_offsets,
+                                  int num_groups)
+{
+    const int64_t rows = a.rows, cols = a.cols;
+    if (rows < 0 || cols < 1) return FP8_ERR_INVALID_ARG;
+    if (fmt != FP8_E4M3FN && fmt != FP8_E5M2 && fmt != FP8_E4M3FNUZ && fmt != FP8_E5M2FNUZ)
+        return FP8_ERR_INVALID_ARG;
+    if (margin < 0 || margin > 64) return FP8_ERR_INVALID_ARG;
+    if (layouts < 1 || layouts > 3) return FP8_ERR_INVALID_ARG;
+    if (!group_offsets || num_groups < 1 || num_groups > QT_MAX_GROUPS) return FP8_ERR_INVALID_ARG;
+    if ((layouts & FP8_LAYOUT_ROW) && rows > 0 && (!q_row || !scale_inv_row)) return FP8_ERR_INVALID_ARG;
+    if ((layouts & FP8_LAYOUT_COLT) && (!q_colT || !scale_inv_col)) return FP8_ERR_INVALID_ARG;
+    if (rows > 0 && !a.x) return FP8_ERR_INVALID_ARG;
+    if (cols % 8 != 0 || a.ld_x % 8 != 0 || !aligned(a.x, 16)) return FP8_ERR_ALIGNMENT;
+    if ((layouts & FP8_LAYOUT_ROW) && !aligned(q_row, 8)) return FP8_ERR_ALIGNMENT;
+    if (layouts & FP8_LAYOUT_COLT) {
+        if (!aligned(q_colT, 16) || ld_colT % 16 != 0) return FP8_ERR_ALIGNMENT;
+        if (ld_colT < rows) return FP8_ERR_INVALID_ARG;
+    }
+    if (cols > ((int64_t)1 << 31) || rows + 32LL * num_groups > INT32_MAX || ld_colT > INT32_MAX)
+        return FP8_ERR_INVALID_ARG;
+    a.q_row = q_row;
+    a.q_colT = q_colT;
+    a.ld_colT = (layouts & FP8_LAYOUT_COLT) ? ld_colT : 0;
+    a.sinv_row = scale_inv_row;
+    a.sinv_col = scale_inv_col;
+    a.offsets = group_offsets;
+    a.G = num_groups;
+    a.margin = margin;
+    a.err = device_error_word();
+    a.n_col_chunks = (cols + QT_COLS - 1) / QT_COLS;
+    a.scales_ready = 0;
+    a.sup_blocks = SUP_BLOCKS;
+    a.sup_chunks = SUP_CHUNKS;
+    // padded space: rows + at most 31 padding rows per group
+    const int64_t padded_max = (layouts & FP8_LAYOUT_COLT) ? ld_colT : rows + 32LL * num_groups;
+    a.n_row_blocks = (padded_max + 31) / 32;
+    return FP8_OK;
+}
+
+template <int PRO>
+static fp8_status_t run_prologue(const QArgs &a, int fmt, int layouts, cudaStream_t st)
+{
+    if (fmt == FP8_E5M2) return run_quantize<FP8_E5M2, 32, PRO>(a, FP8_RECIPE_ROWWISE, layouts, st);
+    if (fmt == FP8_E4M3FNUZ) return run_quantize<FP8_E4M3FNUZ, 32, PRO>(a, FP8_RECIPE_ROWWISE, layouts, st);
+    if (fmt == FP8_E5M2FNUZ) return run_quantize<FP8_E5M2FNUZ, 32, PRO>(a, FP8_RECIPE_ROWWISE, layouts, st);
+    return run_quantize<FP8_E4M3FN, 32, PRO>(a, FP8_RECIPE_ROWWISE, layouts, st);
+}
+
+extern "C" fp8_status_t fp8_permute_quantize(const void *x_bf16, int64_t x_rows, int64_t cols, int64_t ld_x,
+                                             const int32_t *src_rows, int64_t rows, int fmt, int margin, int layouts,
+                                             float *amax_out, uint8_t *q_row, float *scale_inv_row, uint8_t *q_colT,
+                                             int64_t ld_colT, float *scale_inv_col, const int32_t *group_offsets,
+                                             int num_groups, void *stream)
+{
+    if (x_rows < 0 || ld_x < cols) return FP8_ERR_INVALID_ARG;
+    if (rows > 0 && (!src_rows || x_rows < 1)) return FP8_ERR_INVALID_ARG;
+    QArgs a{};
+    a.x = static_cast<const uint16_t *>(x_bf16);
+    a.rows = rows;
+    a.cols = cols;
+    a.ld_x = ld_x;
+    a.amax_out = amax_out;
+    a.src_rows = src_rows;
+    a.x_rows = x_rows;
+    const fp8_status_t s = prologue_args(a, fmt, margin, layouts, q_row, scale_inv_row, q_colT, ld_colT,
+                                         scale_inv_col, group_offsets, num_groups);
+    if (s != FP8_OK) return s;
+    return run_prologue<QPRO_GATHER>(a, fmt, layouts, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" fp8_status_t fp8_swiglu_quantize(const void *gate_up_bf16, int64_t rows, int64_t F, int64_t ld, int fmt,
+                                            int margin, int layouts, void *h_bf16, int64_t ld_h, float *amax_out,
+                                            uint8_t *q_row, float *scale_inv_row, uint8_t *q_colT, int64_t ld_colT,
+                                            float *scale_inv_col, const int32_t *group_offsets, int num_groups,
+                                            void *stream)
+{
+    if (F < 1 || ld < 2 * F) return FP8_ERR_INVALID_ARG;
+    if (h_bf16 && ld_h < F) return FP8_ERR_INVALID_ARG;
+    if (h_bf16 && (ld_h % 8 != 0 || !aligned(h_bf16, 16))) return FP8_ERR_ALIGNMENT;
+    QArgs a{};
+    a.x = static_cast<const uint16_t *>(gate_up_bf16);
+    a.rows = rows;
+    a.cols = F;
+    a.ld_x = ld;
+    a.amax_out = amax_out;
+    a.up_off = F;
+    a.h_out = static_cast<uint16_t *>(h_bf16);
+    a.ld_h = ld_h;
+    const fp8_status_t s = prologue_args(a, fmt, margin, layouts, q_row, scale_inv_row, q_colT, ld_colT,
+                                         scale_inv_col, group_offsets, num_groups);
+    if (s != FP8_OK) return s;
+    return run_prologue<QPRO_SWIGLU>(a, fmt, layouts, static_cast<cudaStream_t>(stream));
 }

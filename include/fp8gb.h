@@ -14,7 +14,8 @@
  *   4. fp8_grouped_gemm        the same over variable-size expert groups of a
  *                              Mixture-of-Experts layer.
  * Beyond those: fp8_quantize_rowwise_resident (the rowwise recipe in one
- * cooperative launch), the MXFP8 recipe (fp8_mx_quantize, fp8_mx_gemm,
+ * cooperative launch), the fused MoE prologues of the rowwise recipe
+ * (fp8_permute_quantize, fp8_swiglu_quantize), the MXFP8 recipe (fp8_mx_quantize, fp8_mx_gemm,
  * fp8_mx_grouped_gemm, and the fused MoE prologues fp8_mx_permute_quantize
  * and fp8_mx_swiglu_quantize), and the blockwise recipe
  * (fp8_blockwise_quantize, whose scales feed fp8_mx_gemm).
@@ -200,6 +201,50 @@ FP8GB_API fp8_status_t fp8_quantize_rowwise_resident(const void *x_bf16, int64_t
                                                      int fmt, int margin, int layouts, float *amax_out,
                                                      uint8_t *q_row, float *scale_inv_row, uint8_t *q_colT,
                                                      int64_t ld_colT, float *scale_inv_col, void *stream);
+
+/*
+ * Fused MoE prologues of the ROWWISE recipe ("FP8 Training on AMD GPUs with
+ * TorchTitan and TorchAO", the question on fused Triton kernels: the
+ * five-kernel eager chain in front of the MoE grouped GEMMs replaced by one
+ * fused kernel; "How PyTorch FP8 Optimizations on AMD GPUs ...", What
+ * Happened: rowwise FP8 with the colwise-scales kernel on the MoE path).
+ * Each writes exactly what fp8_quantize with recipe kind FP8_RECIPE_ROWWISE,
+ * margin `margin` and the given groups would write for the tensor its
+ * prologue defines: q_row, scale_inv_row [rows], q_colT in the padded
+ * grouped layout, scale_inv_col [num_groups][cols], the optional amax_out
+ * [1].  Groups are required (1 <= num_groups <= 4096); the other limits,
+ * alignments and errors are fp8_quantize's.
+ *
+ * They run the grouped rowwise passes of fp8_quantize (amax pass, cast
+ * pass) with the prologue applied to what each pass reads, so neither the
+ * gathered rows nor h is written to memory (except the optional copy of h).
+ *
+ * fp8_permute_quantize -- row r of the tensor is row src_rows[r] of x (the
+ *   routed token rows in expert order; a token routed to k experts appears
+ *   k times).
+ *     x_bf16    [x_rows][ld_x] bf16 token rows.
+ *     src_rows  device int32 [rows]; an index outside [0, x_rows) is read as
+ *               a zero row and reported (fp8_sync_status: FP8_ERR_INVALID_ARG).
+ *     rows      routed rows (= group_offsets[num_groups]).
+ *
+ * fp8_swiglu_quantize -- the tensor is h = bf16_rne(silu(g) * u), g and u
+ *   the two halves of each row of gate_up_bf16 [rows][ld] (gate in columns
+ *   [0, F), up in [F, 2F); ld >= 2F, ld % 8 == 0, F % 8 == 0), evaluated as
+ *   in fp8_mx_swiglu_quantize (each h within one bf16 ulp of the exact
+ *   value).  h_bf16: optional [rows][ld_h] bf16 copy of h (NULL: not
+ *   written; ld_h % 8 == 0, 16-byte aligned).
+ */
+FP8GB_API fp8_status_t fp8_permute_quantize(const void *x_bf16, int64_t x_rows, int64_t cols, int64_t ld_x,
+                                            const int32_t *src_rows, int64_t rows, int fmt, int margin, int layouts,
+                                            float *amax_out, uint8_t *q_row, float *scale_inv_row, uint8_t *q_colT,
+                                            int64_t ld_colT, float *scale_inv_col, const int32_t *group_offsets,
+                                            int num_groups, void *stream);
+
+FP8GB_API fp8_status_t fp8_swiglu_quantize(const void *gate_up_bf16, int64_t rows, int64_t F, int64_t ld, int fmt,
+                                           int margin, int layouts, void *h_bf16, int64_t ld_h, float *amax_out,
+                                           uint8_t *q_row, float *scale_inv_row, uint8_t *q_colT, int64_t ld_colT,
+                                           float *scale_inv_col, const int32_t *group_offsets, int num_groups,
+                                           void *stream);
 
 /*
  * fp8_update_amax_history -- delayed-scaling update for n tensors in one

@@ -362,6 +362,24 @@ def mx_swiglu_quantize(gate_up_bits, fmt, layouts=LAYOUT_ROW | LAYOUT_COLT, offs
     return out
 
 
+def permute_quantize(x_bits, src_rows, fmt, kind, offsets, margin=0, layouts=LAYOUT_ROW | LAYOUT_COLT):
+    """Gather rows x[src_rows] (routed token rows in expert order), then
+    quantize them (see quantize)."""
+    x = _c(x_bits, np.uint16)
+    return quantize(x[np.asarray(src_rows, np.int64)], fmt, kind, margin=margin, layouts=layouts, offsets=offsets)
+
+
+def swiglu_quantize(gate_up_bits, fmt, kind, offsets, margin=0, layouts=LAYOUT_ROW | LAYOUT_COLT):
+    """h = SwiGLU of a [rows, 2F] gate|up tensor, then quantize h (see
+    quantize).  Returns the quantize dict plus h."""
+    gu = _c(gate_up_bits, np.uint16)
+    F = gu.shape[1] // 2
+    h = swiglu_bf16(gu[:, :F], gu[:, F:])
+    out = quantize(h, fmt, kind, margin=margin, layouts=layouts, offsets=offsets)
+    out["h"] = h
+    return out
+
+
 # --- blockwise (1 x 128 / 128 x 128 blocks, power-of-two scales) -------------
 
 def blockwise_code(amax: float, fmt: int) -> int:

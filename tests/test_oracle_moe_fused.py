@@ -215,3 +215,29 @@ def test_swiglu_quantize_composition(orc):
     ref = orc.mx_quantize(h, 0, 3)
     for k in ("q_row", "s_row", "q_colT", "s_col"):
         assert np.array_equal(out[k], ref[k])
+
+
+def test_rowwise_prologue_compositions(orc):
+    """The rowwise prologues are compositions: the identity gather is the
+    plain grouped quantize, a repeated index repeats a row (bytes and row
+    scale), and the SwiGLU prologue quantizes the SwiGLU output."""
+    g = np.random.default_rng(4)
+    x = bf16_bits((g.standard_normal((96, 160)) * np.exp2(g.integers(-5, 5, size=(96, 1)))).astype(np.float32))
+    off = np.array([0, 30, 30, 96], np.int32)
+    ident = orc.permute_quantize(x, np.arange(96), 1, orc.ROWWISE, off)
+    plain = orc.quantize(x, 1, orc.ROWWISE, offsets=off)
+    for k in ("q_row", "scale_inv_row", "q_colT", "scale_inv_col"):
+        assert np.array_equal(ident[k], plain[k])
+    src = np.arange(96)
+    src[10:20] = 7                                        # token 7 routed to ten experts' slots
+    rep = orc.permute_quantize(x, src, 1, orc.ROWWISE, off)
+    for r in range(10, 20):
+        assert np.array_equal(rep["q_row"][r], rep["q_row"][7])
+        assert rep["scale_inv_row"][r] == rep["scale_inv_row"][7]
+    gu = bf16_bits((g.standard_normal((96, 256)) * 3).astype(np.float32))
+    out = orc.swiglu_quantize(gu, 0, orc.ROWWISE, off)
+    h = orc.swiglu_bf16(gu[:, :128], gu[:, 128:])
+    assert np.array_equal(out["h"], h)
+    ref = orc.quantize(h, 0, orc.ROWWISE, offsets=off)
+    for k in ("q_row", "scale_inv_row", "q_colT", "scale_inv_col"):
+        assert np.array_equal(out[k], ref[k])
