@@ -16,7 +16,11 @@ Other workloads (same JSON line, their own config):
                  Student-t activations (15 GEMMs, 11.13 TFLOP per step)
   moe            DeepSeek-V3-shaped MoE layer: 32768 routed rows, 256 experts,
                  hidden 7168, ffn 2048; rowwise tokens with per-expert colwise
-                 scales, rowwise / per-expert colwise weights, 9 grouped GEMMs
+                 scales, rowwise / per-expert colwise weights; the routed rows
+                 gathered and SwiGLU applied inside their quantizes; gate|up
+                 fused: 6 grouped GEMMs with the FLOPs of 9
+  moe_unfused    the same layer with the routed rows and the down projection's
+                 input given as bf16 tensors, separate gate and up (9 GEMMs)
   flux           Flux-12B linears (tokens 9216, hidden 3072, MLP 12288, QKV
                  9216), delayed scaling, all E4M3, amax algo max
   llama_mxfp8    the Llama-3-8B MLP step under the MXFP8 recipe (blocks of 32
@@ -369,7 +373,7 @@ class RowwiseStep:
             self.flops += 2.0 * M * N * K
         self.recipe = fp8.Recipe(kind=fp8.ROWWISE)
         self.q_bytes = sum(quantize_bytes(t.shape) for t in self.inp.values())
-        self.launches_per_step = 3 * len(self.inp) + len(self.GEMMS)   # amax, cast, finalise per tensor
+        self.launches_per_step = 4 * len(self.inp) + len(self.GEMMS)   # clear, amax, cast, finalise per tensor
         self.d2h = [self.out["y"]] if "y" in self.out else []
 
     def quantize(self, k):
@@ -487,11 +491,132 @@ class MxStep:
 
 
 class MoeStep:
-    """DeepSeek-V3-shaped MoE layer fwd+bwd on one GPU: routed token rows
-    grouped by expert, rowwise scales per token plus per-expert column scales;
-    expert weights with per-row scales and per-expert column scales; the
-    nine grouped GEMMs (M-grouped fprop, M-grouped dgrad on the weights'
-    transposed layout, K-grouped wgrad)."""
+    """DeepSeek-V3-shaped MoE layer fwd+bwd on one GPU under the rowwise
+    recipe: rowwise scales per routed token row plus per-expert column
+    scales, expert weights with per-row scales and per-expert column scales.
+    The fused prologues do the token-side work in the quantizes: the routed
+    rows are gathered from the 4096 token rows inside their quantize
+    (fp8_permute_quantize), and SwiGLU of the fused gate|up projection's
+    output is applied inside the quantize of the down projection's input
+    (fp8_swiglu_quantize).  Gate and up are one [E, 2F, H] weight, so six
+    grouped GEMMs carry the FLOPs of nine: M-grouped fprop (gate|up, down),
+    M-grouped dgrad on the weights' transposed layouts, K-grouped wgrad."""
+
+    def __init__(self, dev, seed):
+        import numpy as np
+
+        import fp8_mixed_precision_scale_gb300 as fp8
+        import synth
+        self.fp8 = fp8
+        E, H, F, T = synth.DSV3["E"], synth.DSV3["H"], synth.DSV3["F"], synth.DSV3["tokens"]
+        self.E, self.H, self.F = E, H, F
+        sizes = synth.moe_group_sizes().numpy()
+        self.sizes = sizes
+        self.off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+        self.off_h = torch.from_numpy(self.off)
+        self.off_d = self.off_h.to(dev)
+        self.M = M = int(self.off[-1])
+        self.tokens = T
+        self.name = "moe"
+        self.desc = ("deepseek-v3 moe layer fwd+bwd, rowwise recipe: 4096 tokens x top-8 = 32768 routed rows gathered "
+                     "into expert order inside their quantize, hidden 7168, 256 experts of ffn 2048 (gate|up fused, "
+                     "down), SwiGLU fused into the quantize of the down projection's input, group sizes multinomial "
+                     "over zipf(1.1) with 8 empty experts; rowwise + per-expert colwise scales; 6 grouped GEMMs (the "
+                     "FLOPs of 9)")
+        rng = np.random.default_rng(seed)
+        self.src = torch.from_numpy(rng.integers(0, T, size=M).astype(np.int32)).to(dev)   # routed row -> token
+        g = torch.Generator(device=dev)
+        g.manual_seed(seed)
+        self.inp = {"x": _normal(g, dev, (T, H), 1.0), "w_gu": _normal(g, dev, (E * 2 * F, H), 0.02),
+                    "w_down": _normal(g, dev, (E * H, F), 0.02), "dy": _normal(g, dev, (M, H), 1e-4),
+                    "dgu": _normal(g, dev, (M, 2 * F), 1e-4)}
+        self.fmt = {"xp": 0, "hp": 0, "w_gu": 0, "w_down": 0, "dy": 1, "dgu": 1}
+        rows_per_expert = {"w_gu": 2 * F, "w_down": H}
+        self.woff_d = {k: torch.from_numpy(np.arange(E + 1, dtype=np.int32) * r).to(dev)
+                       for k, r in rows_per_expert.items()}
+        self.recipe = fp8.Recipe(kind=fp8.ROWWISE)
+        ldT = fp8.fp8_group_padded_offsets(self.off)[0]
+        self.ldT_tok = max(16, (ldT + 15) // 16 * 16)
+        self.q_shapes = {"xp": (M, H), "w_gu": (E * 2 * F, H), "w_down": (E * H, F), "hp": (M, F), "dy": (M, H),
+                         "dgu": (M, 2 * F)}
+        self.q = {}
+        for k, (r, c) in self.q_shapes.items():
+            ld = r if k.startswith("w_") else self.ldT_tok
+            self.q[k] = dict(row=torch.empty((r, c), dtype=torch.uint8, device=dev),
+                             colT=torch.empty((c, ld), dtype=torch.uint8, device=dev), ldT=ld,
+                             srow=torch.empty(r, dtype=torch.float32, device=dev),
+                             scol=torch.empty(E * c, dtype=torch.float32, device=dev))
+        e = lambda *shape: torch.empty(shape, dtype=torch.bfloat16, device=dev)  # noqa: E731
+        self.out = {"gu": e(M, 2 * F), "y": e(M, H), "dh": e(M, F), "dx": e(M, H), "dw_down": e(E, H, F),
+                    "dw_gu": e(E, 2 * F, H)}
+        nz = int((sizes > 0).sum())
+        fl = 2.0 * M * F * H
+        self.gemm_work = {  # (flops, algorithmic bytes: A + non-empty experts' weights + C)
+            "fprop_gu": (2 * fl, M * H + 2 * nz * F * H + 4.0 * M * F),
+            "fprop_down": (fl, M * F + nz * F * H + 2.0 * M * H),
+            "dgrad_down": (fl, M * H + nz * F * H + 2.0 * M * F),
+            "dgrad_gu": (2 * fl, 2 * M * F + 2 * nz * F * H + 2.0 * M * H),
+            "wgrad_down": (fl, M * (F + H) + 2.0 * E * F * H),
+            "wgrad_gu": (2 * fl, M * (2 * F + H) + 4.0 * E * F * H)}
+        self.flops = 9 * fl
+        # algorithmic quantize bytes: 2 B read + 1 B per layout per element; SwiGLU reads gate and up
+        self.q_work = {k: quantize_bytes(sh) + (2 * sh[0] * sh[1] if k == "hp" else 0)
+                       for k, sh in self.q_shapes.items()}
+        self.q_bytes = sum(self.q_work.values())
+        self.launches_per_step = 5 * 6 + 6   # a grouped rowwise quantize is 5 launches (clear, amax, scales, cast, scales)
+        self.d2h = [self.out["y"]]
+
+    def quantize(self, k):
+        fp8, q, E = self.fp8, self.q[k], self.E
+        if k == "xp":
+            x = self.inp["x"]
+            fp8.fp8_permute_quantize(x, x.shape[0], x.shape[1], x.stride(0), self.src, self.M, 0, 0, 3, None,
+                                     q["row"], q["srow"], q["colT"], q["ldT"], q["scol"], self.off_d, E)
+        elif k == "hp":
+            gu = self.out["gu"]
+            fp8.fp8_swiglu_quantize(gu, self.M, self.F, gu.stride(0), 0, 0, 3, None, 0, None, q["row"], q["srow"],
+                                    q["colT"], q["ldT"], q["scol"], self.off_d, E)
+        else:
+            t = self.inp[k]
+            r, c = t.shape
+            off = self.woff_d[k] if k.startswith("w_") else self.off_d
+            fp8.fp8_quantize(t, r, c, c, self.fmt[k], self.recipe, 3, None, None, q["row"], q["srow"], q["colT"],
+                             q["ldT"], q["scol"], off, E)
+
+    def run(self, ev=None, world=1):
+        fp8, q, o, E, H, F, M = self.fp8, self.q, self.out, self.E, self.H, self.F, self.M
+        GM, GK, GMT = fp8.GROUPED_M, fp8.GROUPED_K, fp8.GROUPED_M_BT
+        off = self.off_d
+
+        def gg(mode, a, al, b, bl, N, K, out, ldT=0):
+            A = q[a]["row"] if al == "row" else q[a]["colT"]
+            B = q[b]["row"] if bl == "row" else q[b]["colT"]
+            sa = q[a]["srow"] if al == "row" else q[a]["scol"]
+            sb = q[b]["srow"] if bl == "row" else q[b]["scol"]
+            fp8.fp8_grouped_gemm(mode, A, self.fmt[a], B, self.fmt[b], off, E, M, N, K, sa, 1, sb, 1, o[out], ldT)
+
+        W = self.gemm_work
+        for k in ("xp", "w_gu", "w_down"):
+            _timed(ev, "q", lambda k=k: self.quantize(k), self.q_work[k])
+        _timed(ev, "g", lambda: gg(GM, "xp", "row", "w_gu", "row", 2 * F, H, "gu"), W["fprop_gu"])
+        _timed(ev, "q", lambda: self.quantize("hp"), self.q_work["hp"])
+        _timed(ev, "g", lambda: gg(GM, "hp", "row", "w_down", "row", H, F, "y"), W["fprop_down"])
+        for k in ("dy", "dgu"):
+            _timed(ev, "q", lambda k=k: self.quantize(k), self.q_work[k])
+        _timed(ev, "g", lambda: gg(GMT, "dy", "row", "w_down", "colT", F, H, "dh", q["w_down"]["ldT"]),
+               W["dgrad_down"])
+        _timed(ev, "g", lambda: gg(GMT, "dgu", "row", "w_gu", "colT", H, 2 * F, "dx", q["w_gu"]["ldT"]),
+               W["dgrad_gu"])
+        _timed(ev, "g", lambda: gg(GK, "dy", "colT", "hp", "colT", H, F, "dw_down", self.ldT_tok), W["wgrad_down"])
+        _timed(ev, "g", lambda: gg(GK, "dgu", "colT", "xp", "colT", 2 * F, H, "dw_gu", self.ldT_tok),
+               W["wgrad_gu"])
+
+
+class MoeUnfusedStep:
+    """The DeepSeek-V3-shaped MoE layer of MoeStep without the fused
+    prologues, for comparison: the routed token rows and the down
+    projection's input are given as materialised bf16 tensors, gate and up
+    are separate weights and GEMMs (the nine grouped GEMMs)."""
 
     def __init__(self, dev, seed):
         import numpy as np
@@ -507,10 +632,10 @@ class MoeStep:
         self.off_d = torch.from_numpy(self.off).to(dev)
         self.M = M = int(self.off[-1])
         self.tokens = synth.DSV3["tokens"]
-        self.name = "moe"
-        self.desc = ("deepseek-v3 moe layer fwd+bwd: 4096 tokens x top-8 = 32768 routed rows, hidden 7168, "
-                     "256 experts of ffn 2048 (gate/up/down), group sizes multinomial over zipf(1.1) with 8 empty "
-                     "experts; rowwise + per-expert colwise scales; 9 grouped GEMMs")
+        self.name = "moe_unfused"
+        self.desc = ("deepseek-v3 moe layer fwd+bwd, unfused: 4096 tokens x top-8 = 32768 routed rows (given "
+                     "permuted), hidden 7168, 256 experts of ffn 2048 (gate/up/down), group sizes multinomial over "
+                     "zipf(1.1) with 8 empty experts; rowwise + per-expert colwise scales; 9 grouped GEMMs")
         g = torch.Generator(device=dev)
         g.manual_seed(seed)
         self.tok = {"xp": _normal(g, dev, (M, H), 1.0), "hp": _normal(g, dev, (M, F), 1.0),
@@ -546,7 +671,7 @@ class MoeStep:
             "wgrad": (fl, M * (F + H) + 2.0 * E * F * H)}
         self.flops = 9 * fl
         self.q_bytes = sum(quantize_bytes(t.shape) for t in self.inp.values())
-        self.launches_per_step = 3 * len(self.inp) + 9
+        self.launches_per_step = 5 * len(self.inp) + 9   # 5 launches per grouped rowwise quantize
         self.d2h = [self.out["y"]]
 
     def quantize(self, k):
@@ -813,6 +938,7 @@ def run_gpu(args, rank, world, local_rank):
         run_sweep(args, dev, rank, hbm_gbs)
         return
     make = {"llama_mlp": llama_mlp_step, "flux": flux_step, "llama_rowwise": RowwiseStep, "moe": MoeStep,
+            "moe_unfused": MoeUnfusedStep,
             "llama_mxfp8": MxStep, "llama_blockwise": lambda dev, seed: MxStep(dev, seed, recipe="blockwise"),
             "moe_mxfp8": MoeMxStep}
     step = make[args.workload](dev, 1 + rank)
@@ -1243,7 +1369,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="llama_mlp",
-                    choices=["llama_mlp", "llama_rowwise", "llama_mxfp8", "llama_blockwise", "moe", "moe_mxfp8", "flux",
+                    choices=["llama_mlp", "llama_rowwise", "llama_mxfp8", "llama_blockwise", "moe", "moe_unfused",
+                             "moe_mxfp8", "flux",
                              "sweep",
                              "gemm", "quantize", "bw_quantize", "rowwise_quantize", "rowwise_resident",
                              "grouped_m", "grouped_k", "quantize_grouped", "mx_gemm", "mx_quantize", "mx_permute",
