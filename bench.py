@@ -70,14 +70,12 @@ METRIC = "FP8 linear fwd+bwd TFLOPS & quantize GB/s per GB300, as % of roofline"
 L_HIST = 1024
 QUANT_BYTES_PER_ELEM = 4                  # 2 B read + 1 B per layout, two layouts
 
-# DRAM bytes (read + write) of one dense GEMM launch, the gate projection
-# 8192x14336x4096, from one ncu capture (profiles/fp8_gemm_pair_kernel_llama_gate_8192x14336x4096.md).
-# Reported only while the profiled sources are unchanged.
-# DRAM bytes (read + write) of one launch of the step's dominant kernel, from
-# an ncu capture of the gate GEMM; valid only for the sources it was taken on
+# DRAM bytes (read + write) of one launch of the step's dominant kernel (the
+# gate GEMM 8192x14336x4096) from one ncu capture; reported only while the
+# sources it was taken on are unchanged (checked by hash).
 GEMM_TRAFFIC = {
-    "llama_mlp": {"bytes": 316.3e6, "kernel": "fp8_gemm_pair_kernel",
-                  "sources": {"gemm.cu": "328494e59d880345", "fp8gb_device.cuh": "d0b18901711f2f1b"}},
+    "llama_mlp": {"bytes": 318.1e6, "kernel": "fp8_gemm_pair_kernel",
+                  "sources": {"gemm.cu": "328494e59d880345", "fp8gb_device.cuh": "323e9252b7dc6212"}},
     "llama_mxfp8": {"bytes": 307.9e6, "kernel": "mx_gemm_kernel",
                     "sources": {"mxgemm.cu": "9be5e246b91c1446", "fp8gb_device.cuh": "d0b18901711f2f1b"}},
 }
@@ -407,6 +405,53 @@ class RowwiseStep:
         for k in self.BWD_Q:
             _timed(ev, "q", lambda k=k: self.quantize(k), quantize_bytes(self.inp[k].shape))
         for g in self.GEMMS[5:]:
+            _timed(ev, "g", lambda g=g: self.gemm(*g), self.gemm_work[g[4]])
+
+
+class TinyStep(RowwiseStep):
+    """The tiny FP8 linear of the benchmark set (its inputs from synth.tiny):
+    X [256, 512] ~ N(0, 1) with 0.1 % of the entries x50, W [512, 512] ~ N(0,
+    0.02), dY [256, 512] ~ N(0, 1e-3); rowwise recipe, X and W in e4m3, dY in
+    e5m2; fprop, dgrad and wgrad GEMMs.  Launch-bound: its inputs sit in L2."""
+
+    GEMMS = [("x", "row", "w", "row", "y"), ("dy", "row", "w", "colT", "dx"), ("dy", "colT", "x", "colT", "dw")]
+
+    def __init__(self, dev, seed, keys=None):
+        import fp8_mixed_precision_scale_gb300 as fp8
+        import synth
+        self.fp8 = fp8
+        self.name = "tiny"
+        self.desc = ("tiny fp8 linear fwd+bwd: X [256,512] N(0,1) with 0.1% entries x50, W [512,512] N(0,0.02), "
+                     "dY [256,512] N(0,1e-3); rowwise recipe, e4m3 X/W, e5m2 dY")
+        self.tokens = 256
+        self.inp = {k: v.to(dev) for k, v in synth.tiny().items()}
+        self.fmt = {"x": 0, "w": 0, "dy": 1}
+        self.q = {}
+        for k, t in self.inp.items():
+            r, c = t.shape
+            self.q[k] = dict(row=torch.empty((r, c), dtype=torch.uint8, device=dev),
+                             colT=torch.empty((c, r), dtype=torch.uint8, device=dev),
+                             srow=torch.empty(r, dtype=torch.float32, device=dev),
+                             scol=torch.empty(c, dtype=torch.float32, device=dev))
+        self.out, self.gemm_work = {}, {}
+        self.flops = 0.0
+        for (a, al, b, bl, o) in self.GEMMS:
+            M, K = self.inp[a].shape if al == "row" else self.inp[a].shape[::-1]
+            N = self.inp[b].shape[0] if bl == "row" else self.inp[b].shape[1]
+            self.out[o] = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            self.gemm_work[o] = (2.0 * M * N * K, M * K + N * K + 2.0 * M * N)
+            self.flops += 2.0 * M * N * K
+        self.recipe = fp8.Recipe(kind=fp8.ROWWISE)
+        self.q_bytes = sum(quantize_bytes(t.shape) for t in self.inp.values())
+        self.launches_per_step = 4 * len(self.inp) + len(self.GEMMS)
+        self.d2h = [self.out["y"]]
+
+    def run(self, ev=None, world=1):
+        for k in ("x", "w"):
+            _timed(ev, "q", lambda k=k: self.quantize(k), quantize_bytes(self.inp[k].shape))
+        _timed(ev, "g", lambda: self.gemm(*self.GEMMS[0]), self.gemm_work["y"])
+        _timed(ev, "q", lambda: self.quantize("dy"), quantize_bytes(self.inp["dy"].shape))
+        for g in self.GEMMS[1:]:
             _timed(ev, "g", lambda g=g: self.gemm(*g), self.gemm_work[g[4]])
 
 
@@ -847,46 +892,91 @@ def llama_mlp_work():
     return {"flops": flops, "q_bytes": q_bytes}
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+_CPU_INPUTS = {}
+
+
 def cpu_baseline_sample(one_core=True):
-    """The oracle on a bounded sample of the default workload, on the host
-    cores (and, with one_core, on a single core as well)."""
+    """The oracle on the default workload (the Llama-3-8B MLP block under
+    delayed scaling), on the host cores:
+      * the 8 quantizes of the step on their full tensors (synth's seed-1
+        tensors, delayed recipe, both layouts);
+      * the amax-history update of the 8 histories of length 1024;
+      * the fp64 gate-projection GEMM for a block of 256 of its 8192 output
+        rows, whose rate is extrapolated to the step's 9 GEMMs.
+    With one_core, also on a single core (X's quantize and a 16-row GEMM
+    block, extrapolated the same way)."""
     import numpy as np
 
     import oracle
     import synth
     oracle.build()
     cores = len(os.sched_getaffinity(0))
-    g = torch.Generator().manual_seed(1)
-    x = (torch.randn((2048, H_), generator=g)).to(torch.bfloat16)            # 2048 of the 8192 token rows of X
-    xb = synth.bf16_bits(x)
-    # GEMM: 8 full output rows of the gate projection (K = 4096, N = 14336)
-    A = torch.randint(0, 0x70, (8, H_), generator=g, dtype=torch.int32).to(torch.uint8).numpy()
-    B = torch.randint(0, 0x70, (F_, H_), generator=g, dtype=torch.int32).to(torch.uint8).numpy()
+    if not _CPU_INPUTS:
+        base = synth.llama_mlp_base()
+        _CPU_INPUTS["bits"] = {k: synth.bf16_bits(v) for k, v in base.items()}
+        g = torch.Generator().manual_seed(1)
+        _CPU_INPUTS["A"] = torch.randint(0, 0x70, (256, H_), generator=g, dtype=torch.int32).to(torch.uint8).numpy()
+        _CPU_INPUTS["B"] = torch.randint(0, 0x70, (F_, H_), generator=g, dtype=torch.int32).to(torch.uint8).numpy()
+    bits, A, B = _CPU_INPUTS["bits"], _CPU_INPUTS["A"], _CPU_INPUTS["B"]
     w = llama_mlp_work()
+    fmts = {k: (oracle.E5M2 if k.startswith("dy") else oracle.E4M3FN) for k in bits}
 
-    def timed(threads):
+    def timed(threads, keys, gemm_rows):
         oracle.set_threads(threads)
         t0 = time.perf_counter()
-        oracle.quantize(xb, oracle.E4M3FN, oracle.DELAYED, scale_in=np.float32(64.0), amax_io=np.float32(0.0))
+        for k in keys:
+            oracle.quantize(bits[k], fmts[k], oracle.DELAYED, scale_in=np.float32(64.0), amax_io=np.float32(0.0))
         tq = time.perf_counter() - t0
+        q_bytes = sum(QUANT_BYTES_PER_ELEM * bits[k].size for k in keys)
+        hist = np.zeros((8, L_HIST), np.float32)
+        hist[:, 0] = 1.0
+        sc, si = np.ones(8, np.float32), np.ones(8, np.float32)
         t0 = time.perf_counter()
-        oracle.gemm(A, 0, B, 0, np.float32(1.0), np.float32(1.0))
+        oracle.update_amax_history(hist, sc, si, np.array([fmts[k] for k in bits], np.uint8), oracle.MOST_RECENT, 0)
+        tu = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        oracle.gemm(A[:gemm_rows], 0, B, 0, np.float32(1.0), np.float32(1.0))
         tg = time.perf_counter() - t0
-        q_gbs = QUANT_BYTES_PER_ELEM * x.numel() / tq / 1e9
-        g_tflops = 2.0 * 8 * F_ * H_ / tg / 1e12
-        # the oracle's step time: its GEMM rate over the step's FLOPs + its quantize rate over the step's bytes
-        step_s = w["flops"] / (g_tflops * 1e12) + w["q_bytes"] / (q_gbs * 1e9)
-        return w["flops"] / step_s / 1e12, q_gbs, g_tflops, tq + tg
+        g_tflops = 2.0 * gemm_rows * F_ * H_ / tg / 1e12
+        q_gbs = q_bytes / tq / 1e9
+        # the oracle's step: the quantizes at their measured rate over the step's bytes, the update, the 9 GEMMs
+        # at the block's rate
+        step_s = w["q_bytes"] / (q_gbs * 1e9) + tu + w["flops"] / (g_tflops * 1e12)
+        return {"value": w["flops"] / step_s / 1e12, "quantize_gbs": q_gbs, "update_ms": tu * 1e3,
+                "gemm_gflops": g_tflops * 1e3, "step_s_extrapolated": step_s, "seconds": tq + tu + tg}
 
-    one = timed(1) if one_core else None
-    value, q_gbs, g_tflops, secs = timed(cores)
-    out = {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-           "sample": (f"oracle delayed quantize (both layouts) of X rows 0..2047 [2048x4096] "
-                      f"({q_gbs:.3f} GB/s) and the fp64 gate GEMM for 8 output rows [8x14336x4096] "
-                      f"({g_tflops * 1e3:.4f} GFLOP/s), extrapolated to one whole step"),
-           "quantize_gbs": q_gbs, "gemm_tflops": g_tflops, "seconds": secs + (one[3] if one else 0.0)}
+    one = timed(1, ["x"], 16) if one_core else None
+    r = timed(cores, list(bits), 256)
+    out = {"value": r["value"], "unit": "TFLOP/s", "cores": cores, "cpu": cpu_model(), "kind": "oracle",
+           "sample": (f"oracle on the step's 8 quantizes, full tensors ({r['quantize_gbs']:.3f} GB/s, timed), the "
+                      f"8 x 1024 history update ({r['update_ms']:.2f} ms, timed) and the fp64 gate GEMM for 256 of "
+                      f"its 8192 output rows [256x14336x4096] ({r['gemm_gflops']:.2f} GFLOP/s, timed), the GEMM "
+                      f"rate extrapolated to the step's 9 GEMMs: {r['step_s_extrapolated']:.1f} s per step"),
+           "quantize_gbs": r["quantize_gbs"], "update_ms": r["update_ms"], "gemm_gflops": r["gemm_gflops"],
+           "step_s_extrapolated": r["step_s_extrapolated"], "seconds": r["seconds"] + (one["seconds"] if one else 0)}
     if one:
-        out["one_core"] = {"value": one[0], "quantize_gbs": one[1], "gemm_tflops": one[2]}
+        out["one_core"] = {"value": one["value"], "quantize_gbs": one["quantize_gbs"], "gemm_gflops": one["gemm_gflops"],
+                           "sample": "X's quantize [8192x4096] and a 16-row gate GEMM block, extrapolated likewise"}
     return out
 
 
@@ -926,8 +1016,7 @@ def run_gpu(args, rank, world, local_rank):
     fp8.load_library()
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    hbm_gbs, bf16_burst, bf16_sust, peak_src = peaks()
-    fp8_peak = 2.0 * bf16_sust               # FP8 dense = 2x bf16 dense (nominal 4.5 vs 2.25 PFLOP/s)
+    hbm_gbs = peaks()[0]
 
     if args.workload in ("gemm", "quantize", "grouped_m", "grouped_k", "quantize_grouped", "mx_gemm", "mx_quantize",
                          "mx_permute", "mx_swiglu", "permute", "swiglu", "bw_quantize", "rowwise_quantize",
@@ -937,12 +1026,69 @@ def run_gpu(args, rank, world, local_rank):
     if args.workload == "sweep":
         run_sweep(args, dev, rank, hbm_gbs)
         return
-    make = {"llama_mlp": llama_mlp_step, "flux": flux_step, "llama_rowwise": RowwiseStep, "moe": MoeStep,
-            "moe_unfused": MoeUnfusedStep,
-            "llama_mxfp8": MxStep, "llama_blockwise": lambda dev, seed: MxStep(dev, seed, recipe="blockwise"),
-            "moe_mxfp8": MoeMxStep}
-    step = make[args.workload](dev, 1 + rank)
-    for _ in range(max(3, args.warmup)):
+    step = make_step(args.workload, dev, 1 + rank)
+    m = measure(step, args.steps, args.warmup, world, local_rank, dev, graph=args.workload == "tiny")
+    e2e = run_e2e(step, args, world, dev)
+    out = {
+        "metric": METRIC,
+        "value": m["value"],
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": m["ms_per_step"],
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "fp8 e4m3/e5m2 operands, fp32 accumulate, bf16 out",
+        "data": "synthetic",
+        "config": {"workload": step.desc, "name": step.name, "tokens_per_rank": step.tokens,
+                   "parallelism": f"dp{world}",
+                   "l2": "inputs larger than L2 (GBs of operands touched per step), no flush needed",
+                   "timing": "CUDA events on the launching stream, max over ranks"},
+        "tokens_per_s": m["tokens_per_s"],
+        "gemm": m["gemm"],
+        "quantize": m["quantize"],
+        "update_us": m["update_us"],
+        "roofline": m["roofline"],
+        "e2e": e2e,
+        "gpu_launches": step.launches_per_step * args.steps,
+        "clocks": m["clocks"],
+    }
+    del step
+    torch.cuda.empty_cache()
+    if args.workload == "llama_mlp" and world == 1 and not args.no_configs:
+        out["configs"] = run_configs(args, dev, local_rank, m)
+    if args.workload == "llama_mlp" and rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline_sample()
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+STEPS = {"llama_mlp": lambda dev, seed: llama_mlp_step(dev, seed), "flux": lambda dev, seed: flux_step(dev, seed),
+         "llama_rowwise": lambda dev, seed: RowwiseStep(dev, seed), "moe": lambda dev, seed: MoeStep(dev, seed),
+         "moe_unfused": lambda dev, seed: MoeUnfusedStep(dev, seed), "llama_mxfp8": lambda dev, seed: MxStep(dev, seed),
+         "llama_blockwise": lambda dev, seed: MxStep(dev, seed, recipe="blockwise"),
+         "moe_mxfp8": lambda dev, seed: MoeMxStep(dev, seed), "tiny": lambda dev, seed: TinyStep(dev, seed)}
+
+
+def make_step(name, dev, seed):
+    return STEPS[name](dev, seed)
+
+
+def measure(step, steps, warmup, world, local_rank, dev, graph=False):
+    """Warm up, then time `steps` steps with CUDA events on the launching
+    stream (barrier + synchronize on both sides, max over ranks), with the
+    clocks sampled inside the timed window; per-category kernel times from
+    events around every launch.  The FP8 tensor peak is 2 x the measured
+    bf16 peak: the burst figure, or the sustained one when the power cap
+    acted during the window (sw_power_cap among the throttle reasons).  With
+    graph, the step is also captured once in a CUDA graph and replayed, and
+    the faster of the two step times is reported (the per-category kernel
+    times stay those of the eager launches)."""
+    import fp8_mixed_precision_scale_gb300 as fp8
+    hbm_gbs, bf16_burst, bf16_sust, peak_src = peaks()
+    for _ in range(max(3, warmup)):
         step.run(world=world)
     assert fp8.fp8_sync_status() == 0
 
@@ -955,7 +1101,7 @@ def run_gpu(args, rank, world, local_rank):
     t_end = torch.cuda.Event(enable_timing=True)
     w0 = time.time()
     t_start.record()
-    for _ in range(args.steps):
+    for _ in range(steps):
         step.run(ev, world=world)
     t_end.record()
     _barrier(world)
@@ -963,8 +1109,12 @@ def run_gpu(args, rank, world, local_rank):
     clocks = sampler.stop((w0, w1))
     st = fp8.fp8_sync_status()
     assert st == 0, f"device status {st}"
-    ms_step = _max_over_ranks(t_start.elapsed_time(t_end), world, dev) / args.steps
+    ms_step = _max_over_ranks(t_start.elapsed_time(t_end), world, dev) / steps
 
+    capped = bool(clocks and "sw_power_cap" in clocks.get("reasons", []))
+    fp8_burst, fp8_sust = 2.0 * bf16_burst, 2.0 * bf16_sust
+    fp8_peak = fp8_sust if capped else fp8_burst
+    peak_name = "sustained" if capped else "burst"
     g_ms, g_work = _category(ev, "g")
     q_ms, q_work = _category(ev, "q")
     u_ms, _ = _category(ev, "u")
@@ -980,57 +1130,109 @@ def run_gpu(args, rank, world, local_rank):
         if g_roof_ms <= g_tensor_ms * 1.0001:      # tensor-bound GEMMs
             roof = {"bound": "tensor", "achieved": round(gemm_tflops, 1), "peak": round(fp8_peak, 1),
                     "unit": "TFLOP/s", "frac": round(gemm_tflops / fp8_peak, 4),
+                    "frac_burst": round(gemm_tflops / fp8_burst, 4), "frac_sustained": round(gemm_tflops / fp8_sust, 4),
                     "kernel": "mx_gemm_kernel" if isinstance(step, (MxStep, MoeMxStep)) else "fp8_gemm_pair_kernel",
                     "traffic": gemm_traffic(step.name),
-                    "peak_source": f"{peak_src}: 2 x sustained bf16 {bf16_sust} TFLOP/s (fp8/bf16 nominal ratio 2)"}
+                    "peak_source": f"{peak_src}: 2 x {peak_name} bf16 {bf16_sust if capped else bf16_burst} TFLOP/s "
+                                   f"(fp8/bf16 nominal ratio 2; {peak_name} because sw_power_cap was "
+                                   f"{'' if capped else 'not '}seen in the timed window)"}
         else:                                      # HBM-bound (grouped GEMMs at the MoE shape)
             gbs = sum(b for _, b in g_work) / (sum(g_ms) * 1e-3) / 1e9
             roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_gbs, "unit": "GB/s",
                     "frac": round(g_frac, 4), "traffic": None,
                     "kernel": "mx_gemm_kernel (grouped)" if isinstance(step, MoeMxStep) else "fp8_gemm_kernel (grouped)",
-                    "peak_source": f"{peak_src} HBM copy bandwidth; frac = roofline time max(flops / fp8 peak, "
-                                   f"bytes / HBM) over the measured time"}
+                    "peak_source": f"{peak_src} HBM copy bandwidth; frac = roofline time max(flops / fp8 {peak_name} "
+                                   f"peak, bytes / HBM) over the measured time"}
     else:
         roof = {"bound": "hbm", "achieved": round(q_gbs, 1), "peak": hbm_gbs, "unit": "GB/s",
                 "frac": round(q_gbs / hbm_gbs, 4), "traffic": None, "kernel": "quantize (amax + cast)",
                 "peak_source": f"{peak_src} HBM copy bandwidth"}
-
-    e2e = run_e2e(step, args, world, dev)
-    value = world * step.flops / (ms_step * 1e-3) / 1e12
-    out = {
-        "metric": METRIC,
-        "value": round(value, 2),
-        "unit": "TFLOP/s",
-        "n_gpus": world,
-        "steps": args.steps,
-        "warmup": args.warmup,
+    graph_ms = None
+    if graph and world == 1:
+        # the same step replayed from a CUDA graph: removes the host's launch
+        # cost, which dominates a step of microsecond kernels
+        s_cap = torch.cuda.Stream()
+        s_cap.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s_cap):
+            step.run()
+        torch.cuda.current_stream().wait_stream(s_cap)
+        torch.cuda.synchronize()
+        cg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(cg, capture_error_mode="relaxed"):
+            step.run()
+        for _ in range(3):
+            cg.replay()
+        torch.cuda.synchronize()
+        t_start.record()
+        for _ in range(steps):
+            cg.replay()
+        t_end.record()
+        torch.cuda.synchronize()
+        assert fp8.fp8_sync_status() == 0
+        graph_ms = t_start.elapsed_time(t_end) / steps
+        ms_step = min(ms_step, graph_ms)
+    return {
         "ms_per_step": round(ms_step, 4),
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "fp8 e4m3/e5m2 operands, fp32 accumulate, bf16 out",
-        "data": "synthetic",
-        "config": {"workload": step.desc, "name": step.name, "tokens_per_rank": step.tokens,
-                   "parallelism": f"dp{world}",
-                   "l2": "inputs larger than L2 (GBs of operands touched per step), no flush needed",
-                   "timing": "CUDA events on the launching stream, max over ranks"},
+        "ms_per_step_graph": round(graph_ms, 4) if graph_ms is not None else None,
+        "value": round(world * step.flops / (ms_step * 1e-3) / 1e12, 2),
         "tokens_per_s": round(world * step.tokens / (ms_step * 1e-3), 1),
-        "gemm": {"ms_per_step": round(sum(g_ms) / args.steps, 4), "tflops": round(gemm_tflops, 1),
-                 "frac_of_fp8_peak": round(gemm_tflops / fp8_peak, 4), "frac_of_roofline": round(g_frac, 4),
-                 "launches_per_step": len(g_ms) // args.steps},
-        "quantize": {"ms_per_step": round(sum(q_ms) / args.steps, 4), "gbs": round(q_gbs, 1),
+        "gemm": {"ms_per_step": round(sum(g_ms) / steps, 4), "tflops": round(gemm_tflops, 1),
+                 "frac_of_fp8_peak": round(gemm_tflops / fp8_peak, 4),
+                 "frac_of_fp8_burst": round(gemm_tflops / fp8_burst, 4),
+                 "frac_of_fp8_sustained": round(gemm_tflops / fp8_sust, 4),
+                 "frac_of_roofline": round(g_frac, 4), "launches_per_step": len(g_ms) // steps},
+        "quantize": {"ms_per_step": round(sum(q_ms) / steps, 4), "gbs": round(q_gbs, 1),
                      "frac_of_hbm": round(q_gbs / hbm_gbs, 4), "bytes_per_step": step.q_bytes,
-                     "calls_per_step": len(q_ms) // args.steps},
+                     "calls_per_step": len(q_ms) // steps},
         "update_us": round(1e3 * sum(u_ms) / len(u_ms), 2) if u_ms else None,
         "roofline": roof,
-        "e2e": e2e,
-        "gpu_launches": step.launches_per_step * args.steps,
         "clocks": clocks,
     }
-    if step.name == "llama_mlp" and rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline_sample()
-    if rank == 0:
-        print(json.dumps(out), flush=True)
+
+
+def run_configs(args, dev, local_rank, headline):
+    """Every configuration of the benchmark set, each measured like the
+    headline step on this GPU: the tiny rowwise linear, the Llama-3-8B MLP
+    block under delayed scaling (the headline itself), the Llama-3-8B
+    attention projections + MLP under the rowwise recipe, the DeepSeek-V3 MoE
+    layer, the Flux-12B linears, and the knee of the 2^20 .. 2^30-element
+    quantize sweep."""
+    hbm_gbs = peaks()[0]
+    out = {}
+    summary = lambda name, step, m: {  # noqa: E731
+        "workload": step.desc, "ms_per_step": m["ms_per_step"], "tflops": m["value"],
+        "tokens_per_s": m["tokens_per_s"], "gemm_tflops": m["gemm"]["tflops"],
+        "gemm_frac_of_roofline": m["gemm"]["frac_of_roofline"], "quantize_gbs": m["quantize"]["gbs"],
+        "quantize_frac_of_hbm": m["quantize"]["frac_of_hbm"], "update_us": m["update_us"],
+        "roofline": {k: m["roofline"][k] for k in ("bound", "achieved", "peak", "unit", "frac")},
+        "clocks": m["clocks"]}
+    for cfg, name, steps in (("1_tiny", "tiny", 200), ("3_llama_rowwise", "llama_rowwise", 20),
+                             ("4_dsv3_moe", "moe", 10), ("5_flux", "flux", 20)):
+        step = make_step(name, dev, 1)
+        m = measure(step, steps, 3, 1, local_rank, dev, graph=name == "tiny")
+        out[cfg] = summary(name, step, m)
+        if name == "tiny":
+            out[cfg]["us_per_step"] = round(m["ms_per_step"] * 1e3, 2)
+            out[cfg]["l2"] = "inputs inside L2: launch-bound, reported in us; the step replayed from a CUDA graph"
+        del step
+        torch.cuda.empty_cache()
+    out["2_llama_mlp_delayed"] = {"workload": LLAMA_MLP_DESC, "note": "the headline line itself",
+                                  "ms_per_step": headline["ms_per_step"], "tflops": headline["value"],
+                                  "tokens_per_s": headline["tokens_per_s"],
+                                  "gemm_tflops": headline["gemm"]["tflops"],
+                                  "quantize_gbs": headline["quantize"]["gbs"],
+                                  "quantize_frac_of_hbm": headline["quantize"]["frac_of_hbm"],
+                                  "roofline": {k: headline["roofline"][k]
+                                               for k in ("bound", "achieved", "peak", "unit", "frac")}}
+    pts = sweep_points(dev, hbm_gbs, max_reps=40)
+    knee = next((pt["elements"] for pt in pts if pt["frac_of_hbm"] >= 0.8), None)
+    best = max(pts, key=lambda pt: pt["gbs"])
+    out["5_quantize_sweep"] = {"workload": "delayed quantize, e4m3fn, both layouts, x ~ N(0,1) [n/4096, 4096], "
+                                           "n = 2^20 .. 2^30",
+                               "knee_elements": knee, "best_gbs": best["gbs"], "best_frac_of_hbm": best["frac_of_hbm"],
+                               "points": [{k: pt[k] for k in ("elements", "us_per_launch", "gbs", "frac_of_hbm")}
+                                          for pt in pts]}
+    return out
 
 
 def run_e2e(step, args, world, dev):
@@ -1040,10 +1242,28 @@ def run_e2e(step, args, world, dev):
     on a second stream into a second set of input buffers, so the transfer of
     step i + 1 overlaps the kernels of step i (as a training input pipeline
     would)."""
-    pinned = {k: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for k, t in step.inp.items()}
+    # pinned buffers on the NUMA node the GPU is attached to: allocated and
+    # first touched by this thread while it runs on that node's cores
+    numa = gpu_numa(dev)
+    saved = os.sched_getaffinity(0)
+    if numa.get("cpus"):
+        os.sched_setaffinity(0, numa["cpus"])
+    try:
+        pinned = {k: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for k, t in step.inp.items()}
+        for k in pinned:
+            pinned[k].copy_(step.inp[k])
+        host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in step.d2h]
+    finally:
+        os.sched_setaffinity(0, saved)
+    # the host link on its own: the step's H2D copies back to back
+    h0 = torch.cuda.Event(enable_timing=True)
+    h1 = torch.cuda.Event(enable_timing=True)
+    h0.record()
     for k in pinned:
-        pinned[k].copy_(step.inp[k])
-    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in step.d2h]
+        step.inp[k].copy_(pinned[k], non_blocking=True)
+    h1.record()
+    torch.cuda.synchronize()
+    h2d_gbs = sum(t.numel() * t.element_size() for t in pinned.values()) / (h0.elapsed_time(h1) * 1e-3) / 1e9
     h2d = sum(t.numel() * t.element_size() for t in pinned.values())
     d2h = sum(t.numel() * t.element_size() for t in host_out)
     n = 2 if step.name.startswith("moe") else max(3, min(args.steps, 10))
@@ -1090,11 +1310,36 @@ def run_e2e(step, args, world, dev):
     ms = _max_over_ranks(e0.elapsed_time(e1) / n, world, dev)
     return {"value": round(world * step.flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
-            "overlap": "H2D of step i+1 on a second stream during the kernels of step i"}
+            "overlap": "H2D of step i+1 on a second stream during the kernels of step i",
+            "h2d_gbs": round(h2d_gbs, 1), "host_link_bound_ms": round(h2d / (h2d_gbs * 1e9) * 1e3, 3),
+            "pinned_numa": {k: v for k, v in numa.items() if k != "cpus"}}
 
 
-def run_sweep(args, dev, rank, hbm_gbs):
-    """Delayed quantize (E4M3, both layouts) of 2^20 .. 2^30 elements."""
+def gpu_numa(dev):
+    """The NUMA node of the GPU's PCI function and that node's cores (those
+    this process may run on), from sysfs; empty when unknown."""
+    try:
+        p = torch.cuda.get_device_properties(dev)
+        dom, bus, slot = getattr(p, "pci_domain_id"), getattr(p, "pci_bus_id"), getattr(p, "pci_device_id")
+        addr = f"{dom:04x}:{bus:02x}:{slot:02x}.0"
+        with open(f"/sys/bus/pci/devices/{addr}/numa_node") as f:
+            node = int(f.read().strip())
+        if node < 0:
+            return {"pci": addr, "node": None}
+        cpus = set()
+        with open(f"/sys/devices/system/node/node{node}/cpulist") as f:
+            for part in f.read().strip().split(","):
+                lo, _, hi = part.partition("-")
+                cpus.update(range(int(lo), int(hi or lo) + 1))
+        cpus &= os.sched_getaffinity(0)
+        return {"pci": addr, "node": node, "cpus": cpus, "cores_on_node": len(cpus)}
+    except Exception as e:   # noqa: BLE001  (no sysfs entry, older torch): report and go on
+        return {"node": None, "error": type(e).__name__}
+
+
+def sweep_points(dev, hbm_gbs, max_reps=200):
+    """Delayed quantize (E4M3, both layouts) of 2^20 .. 2^30 elements: GB/s
+    against size, inputs rotated over buffers larger than L2."""
     import fp8_mixed_precision_scale_gb300 as fp8
     import synth
     rec = fp8.Recipe(kind=fp8.DELAYED)
@@ -1112,7 +1357,7 @@ def run_sweep(args, dev, rank, hbm_gbs):
             bufs.append((base if i == 0 else base.clone(), torch.empty((rows, cols), dtype=torch.uint8, device=dev),
                          torch.empty((cols, rows), dtype=torch.uint8, device=dev),
                          torch.empty(1, device=dev), torch.empty(1, device=dev)))
-        reps = max(nbuf, min(200, (64 << 30) // (4 * n)))
+        reps = max(nbuf, min(max_reps, (64 << 30) // (4 * n)))
 
         def launch(i):
             x, qr, qc, sr, sc = bufs[i % nbuf]
@@ -1133,6 +1378,14 @@ def run_sweep(args, dev, rank, hbm_gbs):
                        "frac_of_hbm": round(gbs / hbm_gbs, 4), "buffers": nbuf, "launches": reps})
         del bufs, base
         torch.cuda.empty_cache()
+    assert fp8.fp8_sync_status() == 0
+    return points
+
+
+def run_sweep(args, dev, rank, hbm_gbs):
+    """Delayed quantize (E4M3, both layouts) of 2^20 .. 2^30 elements."""
+    import fp8_mixed_precision_scale_gb300 as fp8
+    points = sweep_points(dev, hbm_gbs)
     assert fp8.fp8_sync_status() == 0
     knee = next((pt["elements"] for pt in points if pt["frac_of_hbm"] >= 0.8), None)
     best = max(points, key=lambda pt: pt["gbs"])
@@ -1333,28 +1586,35 @@ def run_single_kernel(args, dev, rank):
 
 
 def run_reference(args, rank, world):
-    """The oracle as it stands, timed on the host cores (rank 0 only)."""
+    """The oracle as it stands, timed on the host cores (rank 0 only): each
+    step is the bounded sample of cpu_baseline_sample (the step's quantizes
+    and update in full, one 256-row block of a GEMM); ms_per_step is that
+    sample's wall time, value the oracle's rate extrapolated to the whole
+    step."""
     if rank != 0:
         return
     t0 = time.perf_counter()
-    vals = []
+    vals, secs = [], []
     base = None
     for i in range(max(0, args.warmup) + args.steps):
+        s0 = time.perf_counter()
         b = cpu_baseline_sample(one_core=False)   # the host-core rate only: keeps the run to a few minutes
         if i >= args.warmup:
             vals.append(b["value"])
+            secs.append(time.perf_counter() - s0)
         base = b
     value = statistics.mean(vals)
     wall = time.perf_counter() - t0
-    work = llama_mlp_work()
     out = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": 1e3 * work["flops"] / (value * 1e12),
+        "warmup": args.warmup, "ms_per_step": round(1e3 * statistics.mean(secs), 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
         "data": "synthetic", "impl": "reference",
-        "config": {"workload": LLAMA_MLP_DESC, "parallelism": "host cores"},
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": base["cores"], "kind": "oracle",
-                         "sample": base["sample"]},
+        "config": {"workload": LLAMA_MLP_DESC, "parallelism": "host cores",
+                   "step": "the bounded sample described in cpu_baseline.sample"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": base["cores"], "cpu": base["cpu"],
+                         "kind": "oracle", "sample": base["sample"]},
+        "oracle_step_s_extrapolated": round(base["step_s_extrapolated"], 1),
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "wall_s": round(wall, 2),
     }
@@ -1368,9 +1628,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-configuration measurements")
     ap.add_argument("--workload", default="llama_mlp",
                     choices=["llama_mlp", "llama_rowwise", "llama_mxfp8", "llama_blockwise", "moe", "moe_unfused",
-                             "moe_mxfp8", "flux",
+                             "moe_mxfp8", "flux", "tiny",
                              "sweep",
                              "gemm", "quantize", "bw_quantize", "rowwise_quantize", "rowwise_resident",
                              "grouped_m", "grouped_k", "quantize_grouped", "mx_gemm", "mx_quantize", "mx_permute",
