@@ -13,7 +13,10 @@ Recipe (all tensors bf16, drawn in fp32 then rounded to bf16 by torch):
                           weights ~ N(0,0.02), grads ~ N(0,1e-4).  The SwiGLU
                           output H [8192,14336] is drawn directly.
   * llama_attn    seed 2  as llama_mlp plus QKV [6144,4096] and O [4096,6144]
-                          weights; activations Student-t with nu = 4.
+                          weights; activations Student-t with nu = 4.  The
+                          MLP of this (rowwise) workload: seed 102, the
+                          llama_mlp shapes with Student-t (nu = 4)
+                          activations X and H.
   * dsv3_moe      seed 3  4096 tokens x top-8 = 32768 routed rows, hidden
                           7168, 256 experts of ffn 2048.  Group sizes
                           ~ Multinomial(32768, p), p_e ~ r_e^-1.1 over a seeded
@@ -126,6 +129,24 @@ def llama_attn_extra(device="cpu", scale_down: int = 1):
         w_o=normal((H, Q), 0.02, g),
         dy_qkv=normal((T, Q), 1e-4, g),
         dy_o=normal((T, H), 1e-4, g),
+    )
+    return {k: v.to(device) for k, v in t.items()}
+
+
+def llama_rowwise_mlp(device="cpu", scale_down: int = 1):
+    """MLP tensors of the rowwise Llama-3-8B workload: the llama_mlp shapes,
+    Student-t (nu = 4) activations, N(0, 0.02) weights, N(0, 1e-4) grads."""
+    g = _gen(LLAMA["seed_attn"] + 100)
+    T, H, F = LLAMA["T"] // scale_down, LLAMA["H"] // scale_down, LLAMA["F"] // scale_down
+    t = dict(
+        x=student_t((T, H), 4, g),
+        w_gate=normal((F, H), 0.02, g),
+        w_up=normal((F, H), 0.02, g),
+        w_down=normal((H, F), 0.02, g),
+        h=student_t((T, F), 4, g),
+        dy_down=normal((T, H), 1e-4, g),
+        dy_gate=normal((T, F), 1e-4, g),
+        dy_up=normal((T, F), 1e-4, g),
     )
     return {k: v.to(device) for k, v in t.items()}
 

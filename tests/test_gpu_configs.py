@@ -229,23 +229,17 @@ def test_config5_flux_delayed_max_50_steps(orc):
 # 3. rowwise attention projections
 # --------------------------------------------------------------------------------------------
 
-def test_config3_llama_attention_rowwise(orc):
-    t = synth.llama_attn_extra()
-    fmts = {"x": 0, "w_qkv": 0, "o_in": 0, "w_o": 0, "dy_qkv": 1, "dy_o": 1}
+def rowwise_layer_check(orc, t, fmts, gemms, seed):
+    """Quantize every tensor with the rowwise recipe; check sampled rows and
+    columns (bytes and scale_inv) against the oracle, then every GEMM on
+    sampled rows, columns and points."""
     rec = fp8.Recipe(kind=fp8.ROWWISE)
     q = {k: fp8.quantize(t[k].to(DEV), fmts[k], rec) for k in fmts}
     sync_ok()
-    g = torch.Generator().manual_seed(5)
+    g = torch.Generator().manual_seed(seed)
     for k, f in fmts.items():
         xb = bits(t[k])
         R, Cn = xb.shape
-        if k == "x":
-            ref = orc.quantize(xb, f, orc.ROWWISE)
-            assert_codes_equal(q[k].q_row.cpu().numpy(), ref["q_row"], f, k)
-            assert_codes_equal(q[k].q_colT.cpu().numpy()[:, :R], ref["q_colT"], f, k)
-            assert_f32_bits_equal(q[k].scale_inv_row.cpu().numpy(), ref["scale_inv_row"], k)
-            assert_f32_bits_equal(q[k].scale_inv_col.cpu().numpy(), ref["scale_inv_col"], k)
-            continue
         for r in torch.randperm(R, generator=g)[:8].tolist():
             ref = orc.quantize(xb[r:r + 1], f, orc.ROWWISE, layouts=1)
             assert_codes_equal(q[k].q_row[r:r + 1].cpu().numpy(), ref["q_row"], f, f"{k} row {r}")
@@ -254,8 +248,6 @@ def test_config3_llama_attention_rowwise(orc):
             ref = orc.quantize(np.ascontiguousarray(xb[:, c:c + 1]), f, orc.ROWWISE, layouts=2)
             assert_codes_equal(q[k].q_colT[c:c + 1, :R].cpu().numpy(), ref["q_colT"], f, f"{k} col {c}")
             assert_f32_bits_equal(q[k].scale_inv_col[c:c + 1].cpu().numpy(), ref["scale_inv_col"], k)
-    gemms = [("x", "row", "w_qkv", "row"), ("o_in", "row", "w_o", "row"), ("dy_qkv", "row", "w_qkv", "colT"),
-             ("dy_o", "row", "w_o", "colT"), ("dy_qkv", "colT", "x", "colT"), ("dy_o", "colT", "o_in", "colT")]
     for gi, (a, al, b, bl) in enumerate(gemms):
         A = q[a].q_row if al == "row" else q[a].q_colT
         B = q[b].q_row if bl == "row" else q[b].q_colT
@@ -264,8 +256,35 @@ def test_config3_llama_attention_rowwise(orc):
         sb = q[b].scale_inv_row if bl == "row" else q[b].scale_inv_col
         C = fp8.scaled_gemm(A, fmts[a], B, fmts[b], sa, sb, K=K)
         sync_ok()
-        sampled_gemm_check(orc, A[:, :K], fmts[a], B[:, :K], fmts[b], sa, sb, C, seed=gi,
+        sampled_gemm_check(orc, A[:, :K], fmts[a], B[:, :K], fmts[b], sa, sb, C, seed=seed + gi,
                            what=f"{a}.{al} x {b}.{bl}")
+        del C
+    return q
+
+
+def test_config3_llama_attention_rowwise(orc):
+    """Config 3, attention projections: QKV and O under the rowwise recipe
+    (Student-t activations), all six GEMMs; X's bytes and scales in full."""
+    t = synth.llama_attn_extra()
+    fmts = {"x": 0, "w_qkv": 0, "o_in": 0, "w_o": 0, "dy_qkv": 1, "dy_o": 1}
+    gemms = [("x", "row", "w_qkv", "row"), ("o_in", "row", "w_o", "row"), ("dy_qkv", "row", "w_qkv", "colT"),
+             ("dy_o", "row", "w_o", "colT"), ("dy_qkv", "colT", "x", "colT"), ("dy_o", "colT", "o_in", "colT")]
+    q = rowwise_layer_check(orc, t, fmts, gemms, seed=5)
+    xb = bits(t["x"])
+    ref = orc.quantize(xb, 0, orc.ROWWISE)
+    R = xb.shape[0]
+    assert_codes_equal(q["x"].q_row.cpu().numpy(), ref["q_row"], 0, "x")
+    assert_codes_equal(q["x"].q_colT.cpu().numpy()[:, :R], ref["q_colT"], 0, "x")
+    assert_f32_bits_equal(q["x"].scale_inv_row.cpu().numpy(), ref["scale_inv_row"], "x")
+    assert_f32_bits_equal(q["x"].scale_inv_col.cpu().numpy(), ref["scale_inv_col"], "x")
+
+
+def test_config3_llama_mlp_rowwise(orc):
+    """Config 3, MLP: gate, up and down under the rowwise recipe with
+    Student-t activations, the nine GEMMs (fprop, dgrad, wgrad of each)."""
+    t = synth.llama_rowwise_mlp()
+    fmts = {k: (1 if k.startswith("dy") else 0) for k in t}
+    rowwise_layer_check(orc, t, fmts, [g for g in MLP_GEMMS], seed=50)
 
 
 # --------------------------------------------------------------------------------------------
@@ -283,11 +302,13 @@ def test_config4_moe_layer(orc):
     tok = synth.moe_tokens()
     rec = fp8.Recipe(kind=fp8.ROWWISE)
     # token side: rowwise + per-group colwise
-    tf = {"xp": 0, "hp": 0, "dy_down": 1, "dy_gate": 1}
+    tf = {"xp": 0, "hp": 0, "dy_down": 1, "dy_gate": 1, "dy_up": 1}
     qt = {k: fp8.quantize(tok[k].to(DEV), f, rec, group_offsets=off_d, host_offsets=off) for k, f in tf.items()}
     # weights: rowwise per expert row, per-expert colwise (equal groups of `rows per expert`)
-    w = {"w_gate": synth.moe_weight((E * F, H), DEV, seed=10), "w_down": synth.moe_weight((E * H, F), DEV, seed=11)}
-    woff = {"w_gate": np.arange(E + 1, dtype=np.int32) * F, "w_down": np.arange(E + 1, dtype=np.int32) * H}
+    w = {"w_gate": synth.moe_weight((E * F, H), DEV, seed=10), "w_up": synth.moe_weight((E * F, H), DEV, seed=12),
+         "w_down": synth.moe_weight((E * H, F), DEV, seed=11)}
+    woff = {"w_gate": np.arange(E + 1, dtype=np.int32) * F, "w_up": np.arange(E + 1, dtype=np.int32) * F,
+            "w_down": np.arange(E + 1, dtype=np.int32) * H}
     qw = {k: fp8.quantize(w[k], 0, rec, group_offsets=torch.from_numpy(woff[k]).to(DEV), host_offsets=woff[k])
           for k in w}
     sync_ok()
@@ -318,7 +339,7 @@ def test_config4_moe_layer(orc):
             assert_codes_equal(qt[k].q_row[r0:min(r1, r0 + 4)].cpu().numpy(), rr["q_row"], f, f"{k} rows {e}")
     # weight bytes for the sampled experts
     for k in w:
-        rows_e = F if k == "w_gate" else H
+        rows_e = H if k == "w_down" else F
         for e in sorted(experts)[:6]:
             wb = bits(w[k][e * rows_e:(e + 1) * rows_e].cpu())
             ref = orc.quantize(wb, 0, orc.ROWWISE)
@@ -326,9 +347,14 @@ def test_config4_moe_layer(orc):
             seg = qw[k].q_colT[:, e * rows_e:(e + 1) * rows_e].cpu().numpy()
             assert_codes_equal(seg, ref["q_colT"], 0, f"{k} colT {e}")
 
-    # grouped GEMMs: fprop gate (M), fprop down (M), dgrad gate (M^T), dgrad down (M^T), wgrad gate and down (K)
+    # the nine grouped GEMMs: fprop gate / up / down (M), dgrad gate / up / down (M on the weights' transposed
+    # layout), wgrad gate / up / down (K)
     Cg = fp8.grouped_gemm(fp8.GROUPED_M, qt["xp"].q_row, 0, qw["w_gate"].q_row, 0, off_d, Mt, F, H,
                           qt["xp"].scale_inv_row, qw["w_gate"].scale_inv_row)
+    Cu = fp8.grouped_gemm(fp8.GROUPED_M, qt["xp"].q_row, 0, qw["w_up"].q_row, 0, off_d, Mt, F, H,
+                          qt["xp"].scale_inv_row, qw["w_up"].scale_inv_row)
+    dXu = fp8.grouped_gemm(fp8.GROUPED_M_BT, qt["dy_up"].q_row, 1, qw["w_up"].q_colT, 0, off_d, Mt, H, F,
+                           qt["dy_up"].scale_inv_row, qw["w_up"].scale_inv_col, ld_T=qw["w_up"].ld_colT)
     Cd = fp8.grouped_gemm(fp8.GROUPED_M, qt["hp"].q_row, 0, qw["w_down"].q_row, 0, off_d, Mt, H, F,
                           qt["hp"].scale_inv_row, qw["w_down"].scale_inv_row)
     dX = fp8.grouped_gemm(fp8.GROUPED_M_BT, qt["dy_gate"].q_row, 1, qw["w_gate"].q_colT, 0, off_d, Mt, H, F,
@@ -337,6 +363,10 @@ def test_config4_moe_layer(orc):
                           qt["dy_down"].scale_inv_row, qw["w_down"].scale_inv_col, ld_T=qw["w_down"].ld_colT)
     dWg = fp8.grouped_gemm(fp8.GROUPED_K, qt["dy_gate"].q_colT, 1, qt["xp"].q_colT, 0, off_d, Mt, F, H,
                            qt["dy_gate"].scale_inv_col, qt["xp"].scale_inv_col, ld_T=qt["xp"].ld_colT)
+    dWu = fp8.grouped_gemm(fp8.GROUPED_K, qt["dy_up"].q_colT, 1, qt["xp"].q_colT, 0, off_d, Mt, F, H,
+                           qt["dy_up"].scale_inv_col, qt["xp"].scale_inv_col, ld_T=qt["xp"].ld_colT)
+    dWd = fp8.grouped_gemm(fp8.GROUPED_K, qt["dy_down"].q_colT, 1, qt["hp"].q_colT, 0, off_d, Mt, H, F,
+                           qt["dy_down"].scale_inv_col, qt["hp"].scale_inv_col, ld_T=qt["hp"].ld_colT)
     sync_ok()
 
     def cpu(t):
@@ -345,6 +375,10 @@ def test_config4_moe_layer(orc):
     checks = [  # (output, A rows source, B expert matrix source, ...)
         ("fprop gate", Cg, qt["xp"], 0, lambda e: cpu(qw["w_gate"].q_row[e * F:(e + 1) * F]),
          lambda e: cpu(qw["w_gate"].scale_inv_row[e * F:(e + 1) * F]), 0, F),
+        ("fprop up", Cu, qt["xp"], 0, lambda e: cpu(qw["w_up"].q_row[e * F:(e + 1) * F]),
+         lambda e: cpu(qw["w_up"].scale_inv_row[e * F:(e + 1) * F]), 0, F),
+        ("dgrad up", dXu, qt["dy_up"], 1, lambda e: cpu(qw["w_up"].q_colT[:, e * F:(e + 1) * F]),
+         lambda e: cpu(qw["w_up"].scale_inv_col.view(E, H)[e]), 0, H),
         ("fprop down", Cd, qt["hp"], 0, lambda e: cpu(qw["w_down"].q_row[e * H:(e + 1) * H]),
          lambda e: cpu(qw["w_down"].scale_inv_row[e * H:(e + 1) * H]), 0, H),
         ("dgrad gate", dX, qt["dy_gate"], 1, lambda e: cpu(qw["w_gate"].q_colT[:, e * F:(e + 1) * F]),
@@ -365,20 +399,23 @@ def test_config4_moe_layer(orc):
                                   points=(pm, pn))
             out = C[torch.from_numpy(pm + r0).to(DEV), torch.from_numpy(pn).to(DEV)].float().cpu().numpy()
             check_gemm(out, ref, bound, f"{name} expert {e}", strict=True)
-    # wgrad of the gate projection: dW_e = dY_e^T X_e over the group's rows
+    # wgrad of gate, up and down: dW_e = dY_e^T X_e over the group's rows
+    for name, dW, qa, qb, Nw, Kw in (("wgrad gate", dWg, qt["dy_gate"], qt["xp"], F, H),
+                                     ("wgrad up", dWu, qt["dy_up"], qt["xp"], F, H),
+                                     ("wgrad down", dWd, qt["dy_down"], qt["hp"], H, F)):
+        sca = qa.scale_inv_col.view(E, Nw)
+        scb = qb.scale_inv_col.view(E, Kw)
+        for e in sorted(experts):
+            if sizes[e] == 0:
+                assert torch.all(dW[e] == 0), f"{name} expert {e}"
+                continue
+            a = cpu(qa.q_colT[:, poff[e]:poff[e] + sizes[e]])
+            b = cpu(qb.q_colT[:, poff[e]:poff[e] + sizes[e]])
+            rows = torch.randperm(Nw, generator=g)[:4].numpy()
+            pm = np.repeat(rows, Kw).astype(np.int64)
+            pn = np.tile(np.arange(Kw), len(rows)).astype(np.int64)
+            ref, bound = orc.gemm(a, 1, b, 0, cpu(sca[e]), cpu(scb[e]), points=(pm, pn))
+            out = dW[e][torch.from_numpy(pm).to(DEV), torch.from_numpy(pn).to(DEV)].float().cpu().numpy()
+            check_gemm(out, ref, bound, f"{name} expert {e}")
     ldT = qt["xp"].ld_colT
-    scg = qt["dy_gate"].scale_inv_col.view(E, F)
-    scx = qt["xp"].scale_inv_col.view(E, H)
-    for e in sorted(experts):
-        if sizes[e] == 0:
-            assert torch.all(dWg[e] == 0)
-            continue
-        a = cpu(qt["dy_gate"].q_colT[:, poff[e]:poff[e] + sizes[e]])
-        b = cpu(qt["xp"].q_colT[:, poff[e]:poff[e] + sizes[e]])
-        rows = torch.randperm(F, generator=g)[:4].numpy()
-        pm = np.repeat(rows, H).astype(np.int64)
-        pn = np.tile(np.arange(H), len(rows)).astype(np.int64)
-        ref, bound = orc.gemm(a, 1, b, 0, cpu(scg[e]), cpu(scx[e]), points=(pm, pn))
-        out = dWg[e][torch.from_numpy(pm).to(DEV), torch.from_numpy(pn).to(DEV)].float().cpu().numpy()
-        check_gemm(out, ref, bound, f"wgrad gate expert {e}")
     assert ldT >= int(poff[-1])
