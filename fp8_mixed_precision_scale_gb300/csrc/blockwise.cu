@@ -127,11 +127,9 @@ __global__ void __launch_bounds__(BW_THREADS)
             uint32_t out[16];
 #pragma unroll
             for (int j = 0; j < 8; j++) {
-                const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-                out[2 * j] = cvt2<FMT>(bf16lo(w[0]) * s, bf16hi(w[0]) * s) |
-                             (cvt2<FMT>(bf16lo(w[1]) * s, bf16hi(w[1]) * s) << 16);
-                out[2 * j + 1] = cvt2<FMT>(bf16lo(w[2]) * s, bf16hi(w[2]) * s) |
-                                 (cvt2<FMT>(bf16lo(w[3]) * s, bf16hi(w[3]) * s) << 16);
+                const uint2 b = cvt8_scaled<FMT>(v[j], s);
+                out[2 * j] = b.x;
+                out[2 * j + 1] = b.y;
             }
             uint4 *dst = reinterpret_cast<uint4 *>(a.q_row + (r0 + r) * a.cols + c0 + 64 * half);
 #pragma unroll
@@ -163,8 +161,14 @@ __global__ void __launch_bounds__(BW_THREADS)
 #pragma unroll
         for (int i = 0; i < 8; i++) {
             const uint32_t x0 = w[4 * i], x1 = w[4 * i + 1], x2 = w[4 * i + 2], x3 = w[4 * i + 3];
-            o0[i] = cvt2<FMT>(bf16lo(x0) * s0, bf16lo(x1) * s0) | (cvt2<FMT>(bf16lo(x2) * s0, bf16lo(x3) * s0) << 16);
-            o1[i] = cvt2<FMT>(bf16hi(x0) * s1, bf16hi(x1) * s1) | (cvt2<FMT>(bf16hi(x2) * s1, bf16hi(x3) * s1) << 16);
+            float a0 = bf16lo(x0), a1 = bf16lo(x1), a2 = bf16lo(x2), a3 = bf16lo(x3);
+            float c0 = bf16hi(x0), c1 = bf16hi(x1), c2 = bf16hi(x2), c3 = bf16hi(x3);
+            mul2_rn(a0, a1, s0, s0);
+            mul2_rn(a2, a3, s0, s0);
+            mul2_rn(c0, c1, s1, s1);
+            mul2_rn(c2, c3, s1, s1);
+            o0[i] = cvt4<FMT>(a0, a1, a2, a3);
+            o1[i] = cvt4<FMT>(c0, c1, c2, c3);
         }
         const int64_t c = c0 + 2 * p;
         uint4 *d0 = reinterpret_cast<uint4 *>(a.q_colT + c * a.ld_colT + r0 + 32 * qq);

@@ -468,6 +468,66 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 }
 
 // ---------------------------------------------------------------------------
+// Scaled conversion of eight bf16 (one 16-byte word) to eight FP8 codes (two
+// words, bytes in element order): each element times its scale in IEEE fp32
+// (round to nearest), then the saturating round-to-nearest-even conversion.
+// Two products per mul.rn.f32x2 and four codes per packed word keep the
+// instruction count per element low (the cast passes run at HBM speed).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mul2_rn(float &a, float &b, float sa, float sb)
+{
+    asm("{.reg .b64 x, s, r;\n\t"
+        "mov.b64 x, {%0, %1};\n\t"
+        "mov.b64 s, {%2, %3};\n\t"
+        "mul.rn.f32x2 r, x, s;\n\t"
+        "mov.b64 {%0, %1}, r;}"
+        : "+f"(a), "+f"(b)
+        : "f"(sa), "f"(sb));
+}
+
+template <int FMT>
+__device__ __forceinline__ uint32_t cvt4(float a, float b, float c, float d)
+{
+    uint32_t r;
+    if constexpr (FMT == FP8_E4M3FN) {
+        asm("{.reg .b16 l, h;\n\t"
+            "cvt.rn.satfinite.e4m3x2.f32 l, %2, %1;\n\t"
+            "cvt.rn.satfinite.e4m3x2.f32 h, %4, %3;\n\t"
+            "mov.b32 %0, {l, h};}"
+            : "=r"(r)
+            : "f"(a), "f"(b), "f"(c), "f"(d));
+    } else if constexpr (FMT == FP8_E5M2) {
+        asm("{.reg .b16 l, h;\n\t"
+            "cvt.rn.satfinite.e5m2x2.f32 l, %2, %1;\n\t"
+            "cvt.rn.satfinite.e5m2x2.f32 h, %4, %3;\n\t"
+            "mov.b32 %0, {l, h};}"
+            : "=r"(r)
+            : "f"(a), "f"(b), "f"(c), "f"(d));
+    } else {
+        r = cvt2<FMT>(a, b) | (cvt2<FMT>(c, d) << 16);
+    }
+    return r;
+}
+
+template <int FMT>
+__device__ __forceinline__ uint2 cvt8_scaled(const uint4 &v, const float (&s)[8])
+{
+    float f[8] = {bf16lo(v.x), bf16hi(v.x), bf16lo(v.y), bf16hi(v.y),
+                  bf16lo(v.z), bf16hi(v.z), bf16lo(v.w), bf16hi(v.w)};
+#pragma unroll
+    for (int j = 0; j < 8; j += 2) mul2_rn(f[j], f[j + 1], s[j], s[j + 1]);
+    return make_uint2(cvt4<FMT>(f[0], f[1], f[2], f[3]), cvt4<FMT>(f[4], f[5], f[6], f[7]));
+}
+
+// the same with one scale for all eight
+template <int FMT>
+__device__ __forceinline__ uint2 cvt8_scaled(const uint4 &v, float s)
+{
+    const float ss[8] = {s, s, s, s, s, s, s, s};
+    return cvt8_scaled<FMT>(v, ss);
+}
+
+// ---------------------------------------------------------------------------
 // SwiGLU element function shared by the fused MoE prologues of the MX and
 // the rowwise quantizers.
 // ---------------------------------------------------------------------------

@@ -302,13 +302,9 @@ __global__ void __launch_bounds__(MX_THREADS)
                 uint32_t out[8];
 #pragma unroll
                 for (int j = 0; j < 4; j++) {
-                    const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-                    const uint32_t b01 = cvt2<FMT>(bf16lo(w[0]) * inv, bf16hi(w[0]) * inv);
-                    const uint32_t b23 = cvt2<FMT>(bf16lo(w[1]) * inv, bf16hi(w[1]) * inv);
-                    const uint32_t b45 = cvt2<FMT>(bf16lo(w[2]) * inv, bf16hi(w[2]) * inv);
-                    const uint32_t b67 = cvt2<FMT>(bf16lo(w[3]) * inv, bf16hi(w[3]) * inv);
-                    out[2 * j] = b01 | (b23 << 16);
-                    out[2 * j + 1] = b45 | (b67 << 16);
+                    const uint2 b = cvt8_scaled<FMT>(v[j], inv);
+                    out[2 * j] = b.x;
+                    out[2 * j + 1] = b.y;
                 }
                 uint4 *dst = reinterpret_cast<uint4 *>(a.q_row + (cur.src0 + lr) * a.cols + cur.c0 + 32 * blk);
                 dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
@@ -353,10 +349,14 @@ __global__ void __launch_bounds__(MX_THREADS)
 #pragma unroll
                     for (int i = 0; i < 4; i++) {
                         const uint32_t x0 = w[4 * i], x1 = w[4 * i + 1], x2 = w[4 * i + 2], x3 = w[4 * i + 3];
-                        o0[i] = cvt2<FMT>(bf16lo(x0) * inv0, bf16lo(x1) * inv0) |
-                                (cvt2<FMT>(bf16lo(x2) * inv0, bf16lo(x3) * inv0) << 16);
-                        o1[i] = cvt2<FMT>(bf16hi(x0) * inv1, bf16hi(x1) * inv1) |
-                                (cvt2<FMT>(bf16hi(x2) * inv1, bf16hi(x3) * inv1) << 16);
+                        float a0 = bf16lo(x0), a1 = bf16lo(x1), a2 = bf16lo(x2), a3 = bf16lo(x3);
+                        float c0 = bf16hi(x0), c1 = bf16hi(x1), c2 = bf16hi(x2), c3 = bf16hi(x3);
+                        mul2_rn(a0, a1, inv0, inv0);
+                        mul2_rn(a2, a3, inv0, inv0);
+                        mul2_rn(c0, c1, inv1, inv1);
+                        mul2_rn(c2, c3, inv1, inv1);
+                        o0[i] = cvt4<FMT>(a0, a1, a2, a3);
+                        o1[i] = cvt4<FMT>(c0, c1, c2, c3);
                     }
                     const int64_t r0 = cur.pr0 + 32 * h + 16 * s;
                     *reinterpret_cast<uint4 *>(a.q_colT + c * a.ld_colT + r0) = make_uint4(o0[0], o0[1], o0[2], o0[3]);

@@ -762,27 +762,21 @@ __device__ __forceinline__ void cast_run(const QArgs &a, unsigned char *dsm, int
             }
             uint32_t rowb0, rowb1, colb0, colb1;
             if constexpr (SMODE == 0) {
-                const float s = s_tensor;
-                rowb0 = cvt2<FMT>(__fmul_rn(bf16lo(w[0]), s), __fmul_rn(bf16hi(w[0]), s)) |
-                        (cvt2<FMT>(__fmul_rn(bf16lo(w[1]), s), __fmul_rn(bf16hi(w[1]), s)) << 16);
-                rowb1 = cvt2<FMT>(__fmul_rn(bf16lo(w[2]), s), __fmul_rn(bf16hi(w[2]), s)) |
-                        (cvt2<FMT>(__fmul_rn(bf16lo(w[3]), s), __fmul_rn(bf16hi(w[3]), s)) << 16);
-                colb0 = rowb0;
-                colb1 = rowb1;
+                const uint2 b = cvt8_scaled<FMT>(v[i], s_tensor);
+                rowb0 = colb0 = b.x;
+                rowb1 = colb1 = b.y;
             } else {
                 if constexpr (DO_ROW) {
-                    const float s = srow[r];
-                    rowb0 = cvt2<FMT>(__fmul_rn(bf16lo(w[0]), s), __fmul_rn(bf16hi(w[0]), s)) |
-                            (cvt2<FMT>(__fmul_rn(bf16lo(w[1]), s), __fmul_rn(bf16hi(w[1]), s)) << 16);
-                    rowb1 = cvt2<FMT>(__fmul_rn(bf16lo(w[2]), s), __fmul_rn(bf16hi(w[2]), s)) |
-                            (cvt2<FMT>(__fmul_rn(bf16lo(w[3]), s), __fmul_rn(bf16hi(w[3]), s)) << 16);
+                    const uint2 b = cvt8_scaled<FMT>(v[i], srow[r]);
+                    rowb0 = b.x;
+                    rowb1 = b.y;
                 }
                 if constexpr (DO_COLT) {
                     const float *sc = scol + cg * 8;
-                    colb0 = cvt2<FMT>(__fmul_rn(bf16lo(w[0]), sc[0]), __fmul_rn(bf16hi(w[0]), sc[1])) |
-                            (cvt2<FMT>(__fmul_rn(bf16lo(w[1]), sc[2]), __fmul_rn(bf16hi(w[1]), sc[3])) << 16);
-                    colb1 = cvt2<FMT>(__fmul_rn(bf16lo(w[2]), sc[4]), __fmul_rn(bf16hi(w[2]), sc[5])) |
-                            (cvt2<FMT>(__fmul_rn(bf16lo(w[3]), sc[6]), __fmul_rn(bf16hi(w[3]), sc[7])) << 16);
+                    const float cs[8] = {sc[0], sc[1], sc[2], sc[3], sc[4], sc[5], sc[6], sc[7]};
+                    const uint2 b = cvt8_scaled<FMT>(v[i], cs);
+                    colb0 = b.x;
+                    colb1 = b.y;
                 }
             }
             const bool ok = col_ok && r < rb.valid;
@@ -977,27 +971,21 @@ __global__ void __launch_bounds__(QT_THREADS, 6) grouped_cast_kernel(QArgs a)
             }
             uint32_t rowb0 = 0, rowb1 = 0, colb0 = 0, colb1 = 0;
             if constexpr (SMODE == 0) {
-                const float s = s_tensor;
-                rowb0 = cvt2<FMT>(__fmul_rn(bf16lo(w[0]), s), __fmul_rn(bf16hi(w[0]), s)) |
-                        (cvt2<FMT>(__fmul_rn(bf16lo(w[1]), s), __fmul_rn(bf16hi(w[1]), s)) << 16);
-                rowb1 = cvt2<FMT>(__fmul_rn(bf16lo(w[2]), s), __fmul_rn(bf16hi(w[2]), s)) |
-                        (cvt2<FMT>(__fmul_rn(bf16lo(w[3]), s), __fmul_rn(bf16hi(w[3]), s)) << 16);
-                colb0 = rowb0;
-                colb1 = rowb1;
+                const uint2 b = cvt8_scaled<FMT>(v[i], s_tensor);
+                rowb0 = colb0 = b.x;
+                rowb1 = colb1 = b.y;
             } else {
                 if constexpr (DO_ROW) {
-                    const float s = srow[i * 32 + roff];
-                    rowb0 = cvt2<FMT>(__fmul_rn(bf16lo(w[0]), s), __fmul_rn(bf16hi(w[0]), s)) |
-                            (cvt2<FMT>(__fmul_rn(bf16lo(w[1]), s), __fmul_rn(bf16hi(w[1]), s)) << 16);
-                    rowb1 = cvt2<FMT>(__fmul_rn(bf16lo(w[2]), s), __fmul_rn(bf16hi(w[2]), s)) |
-                            (cvt2<FMT>(__fmul_rn(bf16lo(w[3]), s), __fmul_rn(bf16hi(w[3]), s)) << 16);
+                    const uint2 b = cvt8_scaled<FMT>(v[i], srow[i * 32 + roff]);
+                    rowb0 = b.x;
+                    rowb1 = b.y;
                 }
                 if constexpr (DO_COLT) {
                     const float *sc = &scol[i][cg * 8];
-                    colb0 = cvt2<FMT>(__fmul_rn(bf16lo(w[0]), sc[0]), __fmul_rn(bf16hi(w[0]), sc[1])) |
-                            (cvt2<FMT>(__fmul_rn(bf16lo(w[1]), sc[2]), __fmul_rn(bf16hi(w[1]), sc[3])) << 16);
-                    colb1 = cvt2<FMT>(__fmul_rn(bf16lo(w[2]), sc[4]), __fmul_rn(bf16hi(w[2]), sc[5])) |
-                            (cvt2<FMT>(__fmul_rn(bf16lo(w[3]), sc[6]), __fmul_rn(bf16hi(w[3]), sc[7])) << 16);
+                    const float cs[8] = {sc[0], sc[1], sc[2], sc[3], sc[4], sc[5], sc[6], sc[7]};
+                    const uint2 b = cvt8_scaled<FMT>(v[i], cs);
+                    colb0 = b.x;
+                    colb1 = b.y;
                 }
             }
             const bool ok = !rb.skip && col_ok && roff < rb.valid;
