@@ -576,9 +576,6 @@ class MoeStep:
                     "w_down": _normal(g, dev, (E * H, F), 0.02), "dy": _normal(g, dev, (M, H), 1e-4),
                     "dgu": _normal(g, dev, (M, 2 * F), 1e-4)}
         self.fmt = {"xp": 0, "hp": 0, "w_gu": 0, "w_down": 0, "dy": 1, "dgu": 1}
-        rows_per_expert = {"w_gu": 2 * F, "w_down": H}
-        self.woff_d = {k: torch.from_numpy(np.arange(E + 1, dtype=np.int32) * r).to(dev)
-                       for k, r in rows_per_expert.items()}
         self.recipe = fp8.Recipe(kind=fp8.ROWWISE)
         ldT = fp8.fp8_group_padded_offsets(self.off)[0]
         self.ldT_tok = max(16, (ldT + 15) // 16 * 16)
@@ -608,7 +605,8 @@ class MoeStep:
         self.q_work = {k: quantize_bytes(sh) + (2 * sh[0] * sh[1] if k == "hp" else 0)
                        for k, sh in self.q_shapes.items()}
         self.q_bytes = sum(self.q_work.values())
-        self.launches_per_step = 5 * 6 + 6   # a grouped rowwise quantize is 5 launches (clear, amax, scales, cast, scales)
+        # a grouped rowwise quantize is 5 launches (clear, amax, scales, cast, scales), an equal-groups one 4
+        self.launches_per_step = 5 * 4 + 4 * 2 + 6
         self.d2h = [self.out["y"]]
 
     def quantize(self, k):
@@ -624,7 +622,8 @@ class MoeStep:
         else:
             t = self.inp[k]
             r, c = t.shape
-            off = self.woff_d[k] if k.startswith("w_") else self.off_d
+            # expert weights: E equal groups (no offsets needed); routed tokens: the routing offsets
+            off = None if k.startswith("w_") else self.off_d
             fp8.fp8_quantize(t, r, c, c, self.fmt[k], self.recipe, 3, None, None, q["row"], q["srow"], q["colT"],
                              q["ldT"], q["scol"], off, E)
 
@@ -690,9 +689,6 @@ class MoeUnfusedStep:
         self.w = {"w_gate": _normal(g, dev, (E * F, H), 0.02), "w_up": _normal(g, dev, (E * F, H), 0.02),
                   "w_down": _normal(g, dev, (E * H, F), 0.02)}
         self.inp = dict(self.tok, **self.w)
-        rows_per_expert = {"w_gate": F, "w_up": F, "w_down": H}
-        self.woff_d = {k: torch.from_numpy(np.arange(E + 1, dtype=np.int32) * r).to(dev)
-                       for k, r in rows_per_expert.items()}
         self.recipe = fp8.Recipe(kind=fp8.ROWWISE)
         ldT = fp8.fp8_group_padded_offsets(self.off)[0]
         self.ldT_tok = max(16, (ldT + 15) // 16 * 16)
@@ -716,13 +712,13 @@ class MoeUnfusedStep:
             "wgrad": (fl, M * (F + H) + 2.0 * E * F * H)}
         self.flops = 9 * fl
         self.q_bytes = sum(quantize_bytes(t.shape) for t in self.inp.values())
-        self.launches_per_step = 5 * len(self.inp) + 9   # 5 launches per grouped rowwise quantize
+        self.launches_per_step = 5 * len(self.tok) + 4 * len(self.w) + 9   # grouped 5, equal groups 4 launches
         self.d2h = [self.out["y"]]
 
     def quantize(self, k):
         t, q = self.inp[k], self.q[k]
         r, c = t.shape
-        off_d = self.woff_d[k] if k in self.w else self.off_d
+        off_d = None if k in self.w else self.off_d   # expert weights: E equal groups
         f = 0 if k in self.w else self.tfmt[k]
         self.fp8.fp8_quantize(t, r, c, c, f, self.recipe, 3, None, None, q["row"], q["srow"], q["colT"],
                               q["ldT"], q["scol"], off_d, self.E)

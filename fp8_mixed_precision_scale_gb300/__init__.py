@@ -326,11 +326,13 @@ class Quantized:
 
 
 def quantize(x: torch.Tensor, fmt: int, recipe: Recipe, layouts: int = LAYOUT_ROW | LAYOUT_COLT, scale_in=None,
-             amax_out=None, group_offsets=None, host_offsets=None, stream=None) -> Quantized:
+             amax_out=None, group_offsets=None, host_offsets=None, stream=None, equal_groups: int = 0) -> Quantized:
     """Quantize a CUDA bf16 [rows, cols] tensor (row stride x.stride(0)).
 
     Grouped (MoE) tensors pass the device offsets and their CPU copy
-    (host_offsets) so the padded colwise width can be sized here.
+    (host_offsets) so the padded colwise width can be sized here; a stack of
+    equal groups (expert weights) may pass equal_groups = the number of
+    groups instead (rows / equal_groups a multiple of 64).
     """
     assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
     rows, cols = x.shape
@@ -341,6 +343,7 @@ def quantize(x: torch.Tensor, fmt: int, recipe: Recipe, layouts: int = LAYOUT_RO
         ld_colT, _ = fp8_group_padded_offsets(host_offsets)
         ld_colT = max(16, (ld_colT + 15) // 16 * 16)
     else:
+        G = equal_groups
         ld_colT = max(16, (rows + 15) // 16 * 16)
     q_row = sr = q_colT = sc = None
     if layouts & LAYOUT_ROW:

@@ -71,6 +71,7 @@ struct QArgs {
     int scales_ready;  // rowwise cast pass: the scale buffers already hold scales (else amaxes)
     int sup_blocks;  // rowwise amax pass: 32-row blocks per super tile (1..8)
     int sup_chunks;  // rowwise amax pass: 128-column chunks per super tile (1..8)
+    int64_t group_rows;  // equal groups without offsets: rows per group (a multiple of 64); 0 = one group
     // fused MoE prologues of the grouped rowwise passes (template parameter PRO)
     const int32_t *src_rows;  // QPRO_GATHER: row r of the tensor is row src_rows[r] of x
     int64_t x_rows;           // QPRO_GATHER: rows of x
@@ -182,7 +183,7 @@ __device__ __forceinline__ RowBlock row_block(const QArgs &a, int64_t b, const i
         rb.in_row0 = b * RB;
         rb.out_col0 = b * RB;
         rb.valid = (int)(a.rows - rb.in_row0 < RB ? a.rows - rb.in_row0 : RB);
-        rb.group = 0;
+        rb.group = a.group_rows ? (int)(rb.in_row0 / a.group_rows) : 0;  // equal groups: a block lies in one
     } else {
         // padded block start p = b * RB (RB == 32): last group with poff <= p
         const int64_t p = b * RB;
@@ -470,7 +471,9 @@ __device__ __forceinline__ void dense_rowcol_amax_run(const QArgs &a, int64_t fi
                     m = max(m, (j & 1) ? (word >> 16) : (word & 0xFFFFu));
                 }
                 const int64_t c = c0 + t;
-                if (c < a.cols) atomicMax(reinterpret_cast<unsigned int *>(a.sinv_col) + c, m << 16);
+                // equal groups: the tile's rows lie in one group (group_rows is a multiple of RB)
+                const int64_t grp = a.group_rows ? b * RB / a.group_rows : 0;
+                if (c < a.cols) atomicMax(reinterpret_cast<unsigned int *>(a.sinv_col) + grp * a.cols + c, m << 16);
             }
             __syncthreads();
         }
@@ -1235,7 +1238,7 @@ static fp8_status_t run_quantize(QArgs a, int kind, int layouts, cudaStream_t st
     }
     // ROWWISE
     const int64_t n_row = (layouts & FP8_LAYOUT_ROW) ? a.rows : 0;
-    const int64_t n_col = (layouts & FP8_LAYOUT_COLT) ? a.cols * (a.offsets ? a.G : 1) : 0;
+    const int64_t n_col = (layouts & FP8_LAYOUT_COLT) ? a.cols * (a.offsets || a.group_rows ? a.G : 1) : 0;
     if (!(layouts & FP8_LAYOUT_ROW)) a.sinv_row = nullptr;
     if (!(layouts & FP8_LAYOUT_COLT)) a.sinv_col = nullptr;
     // the amax accumulators start at zero: one launch clears all three
@@ -1318,7 +1321,10 @@ extern "C" fp8_status_t fp8_quantize(const void *x_bf16, int64_t rows, int64_t c
     if (recipe->kind == FP8_RECIPE_DELAYED && (!scale_in || !amax_out)) return FP8_ERR_INVALID_ARG;
     if (recipe->kind == FP8_RECIPE_TENSORWISE && !amax_out) return FP8_ERR_INVALID_ARG;
     if (group_offsets && (num_groups < 1 || num_groups > QT_MAX_GROUPS)) return FP8_ERR_INVALID_ARG;
-    if (!group_offsets && num_groups != 0) return FP8_ERR_INVALID_ARG;
+    // equal groups without offsets: num_groups groups of rows / num_groups rows, a multiple of 64
+    if (!group_offsets && (num_groups < 0 || num_groups > QT_MAX_GROUPS)) return FP8_ERR_INVALID_ARG;
+    if (!group_offsets && num_groups > 0 && (rows % num_groups != 0 || (rows / num_groups) % 64 != 0))
+        return FP8_ERR_INVALID_ARG;
     if (cols % 8 != 0 || ld_x % 8 != 0 || !aligned(x_bf16, 16)) return FP8_ERR_ALIGNMENT;
     if ((layouts & FP8_LAYOUT_ROW) && !aligned(q_row, 8)) return FP8_ERR_ALIGNMENT;
     if (layouts & FP8_LAYOUT_COLT) {
@@ -1344,7 +1350,8 @@ extern "C" fp8_status_t fp8_quantize(const void *x_bf16, int64_t rows, int64_t c
     a.amax_out = amax_out;
     a.offsets = group_offsets;
     a.err = device_error_word();
-    a.G = group_offsets ? num_groups : 0;
+    a.G = num_groups;
+    a.group_rows = !group_offsets && num_groups > 0 ? rows / num_groups : 0;
     a.margin = recipe->margin;
     a.n_col_chunks = (cols + QT_COLS - 1) / QT_COLS;
     a.scales_ready = 0;

@@ -141,6 +141,13 @@ enum { FP8_GROUPED_M = 0, FP8_GROUPED_K = 1, FP8_GROUPED_M_BT = 2 };  /* grouped
  *                 non-decreasing, offsets[num_groups] = rows (the row range
  *                 of each expert group).  Not validated on the device beyond
  *                 bounds: rows outside [0, rows) are skipped.
+ *   num_groups    with group_offsets: the number of groups (1 .. 4096).
+ *                 Without (NULL): 0 for an ungrouped tensor, or num_groups
+ *                 equal groups of rows / num_groups rows each (a stack of
+ *                 expert weights), which must be a multiple of 64: the same
+ *                 results as passing the offsets e * rows / num_groups (no
+ *                 padding columns, since the groups are multiples of 32), on
+ *                 the plain tensor's kernels.
  *   Scale arithmetic (fp32, IEEE): s = fp8_max / amax, s *= 2^-margin, an
  *   overflow to Inf becomes FLT_MAX, amax == 0 or non-finite gives s = 1;
  *   scale_inv = 1 / s.  NaN in x propagates into the amax.

@@ -102,7 +102,9 @@ def test_quantize_validation(lib):
     assert q_call(lib, ld_colT=72) == ALIGN
     assert q_call(lib, ld_colT=48) == INVALID         # shorter than rows
     assert q_call(lib, offsets=FAKE, G=0) == INVALID
-    assert q_call(lib, G=3) == INVALID
+    assert q_call(lib, G=3) == INVALID                # equal groups: 64 rows do not split into 3
+    assert q_call(lib, G=2) == INVALID                # equal groups of 32 rows: not a multiple of 64
+    assert q_call(lib, G=-1) == INVALID
 
 
 def r_call(lib, **kw):

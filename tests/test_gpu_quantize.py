@@ -377,3 +377,49 @@ def test_e5m2fnuz_top_binade(orc):
         q, _ = run_gpu(pats, 3, 0, scale=scale)
         exp = orc.cast_points(bits(pats), np.float32(scale), 3).reshape(8, 128)
         assert_codes_equal(q.q_row.cpu().numpy(), exp, 3, f"top binade s{scale}")
+
+
+@pytest.mark.parametrize("layouts", [1, 2, 3])
+@pytest.mark.parametrize("fmt", [0, 1, 2])
+def test_quantize_equal_groups(orc, layouts, fmt):
+    """Equal groups without offsets (a stack of 6 expert weights of 128 rows,
+    136 columns): the same bytes and scales as the same call with the
+    offsets e * 128, and as the oracle's grouped quantize."""
+    E, m, cols = 6, 128, 136
+    x = gen_x((E * m, cols), seed=60 + fmt + 3 * layouts)
+    off = np.arange(E + 1, dtype=np.int32) * m
+    rec = fp8.Recipe(kind=fp8.ROWWISE, margin=1)
+    xd = x.to(DEV)
+    qe = fp8.quantize(xd, fmt, rec, layouts, equal_groups=E)
+    qo = fp8.quantize(xd, fmt, rec, layouts, group_offsets=torch.from_numpy(off).to(DEV), host_offsets=off)
+    assert fp8.fp8_sync_status() == 0
+    ref = orc.quantize(bits(x), fmt, orc.ROWWISE, margin=1, layouts=layouts, offsets=off)
+    rows = E * m
+    if layouts & 1:
+        assert torch.equal(qe.q_row, qo.q_row)
+        assert torch.equal(qe.scale_inv_row.view(torch.int32), qo.scale_inv_row.view(torch.int32))
+        assert_codes_equal(qe.q_row.cpu().numpy(), ref["q_row"], fmt, "equal groups q_row")
+        assert_f32_bits_equal(qe.scale_inv_row.cpu().numpy(), ref["scale_inv_row"], "equal groups sinv_row")
+    if layouts & 2:
+        assert torch.equal(qe.q_colT[:, :rows], qo.q_colT[:, :rows])
+        assert torch.equal(qe.scale_inv_col.view(torch.int32), qo.scale_inv_col.view(torch.int32))
+        assert_codes_equal(qe.q_colT.cpu().numpy()[:, :rows], ref["q_colT"], fmt, "equal groups q_colT")
+        assert_f32_bits_equal(qe.scale_inv_col.cpu().numpy().reshape(E, cols), ref["scale_inv_col"],
+                              "equal groups sinv_col")
+
+
+def test_quantize_equal_groups_moe_weight():
+    """A reduced DeepSeek-V3 gate weight stack (64 experts x 2048 rows x
+    7168): equal-groups mode byte-equal to the offsets mode."""
+    E, m, cols = 64, 2048, 7168
+    g = torch.Generator(device=DEV).manual_seed(7)
+    x = (torch.randn((E * m, cols), generator=g, device=DEV) * 0.02).to(torch.bfloat16)
+    off = np.arange(E + 1, dtype=np.int32) * m
+    rec = fp8.Recipe(kind=fp8.ROWWISE)
+    qe = fp8.quantize(x, 0, rec, equal_groups=E)
+    qo = fp8.quantize(x, 0, rec, group_offsets=torch.from_numpy(off).to(DEV), host_offsets=off)
+    assert fp8.fp8_sync_status() == 0
+    assert torch.equal(qe.q_row, qo.q_row)
+    assert torch.equal(qe.q_colT[:, :E * m], qo.q_colT[:, :E * m])
+    assert torch.equal(qe.scale_inv_row.view(torch.int32), qo.scale_inv_row.view(torch.int32))
+    assert torch.equal(qe.scale_inv_col.view(torch.int32), qo.scale_inv_col.view(torch.int32))
