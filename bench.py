@@ -795,8 +795,6 @@ class MoeMxStep:
                     "w_down": _normal(g, dev, (E * H, F), 0.02), "dy": _normal(g, dev, (M, H), 1e-4),
                     "dgu": _normal(g, dev, (M, 2 * F), 1e-4)}
         self.P, _ = fp8.fp8_group_padded_offsets(self.off_h, fp8.MX_GROUP_ALIGN)   # padded routed rows
-        woff = {"w_gu": 2 * F, "w_down": H}
-        self.woff_d = {k: torch.from_numpy(np.arange(E + 1, dtype=np.int32) * r).to(dev) for k, r in woff.items()}
 
         def bufs(rows, cols, srows):
             return dict(row=torch.empty((rows, cols), dtype=torch.uint8, device=dev),
@@ -840,9 +838,11 @@ class MoeMxStep:
         else:
             t = self.inp[k]
             r, c = t.shape
-            off = self.woff_d[k] if k.startswith("w_") else self.off_d
+            # expert weights: groups of 4096 / 7168 rows, multiples of the 128-row MX group alignment, so the
+            # grouped layout has no padding and equals the plain quantize of the whole stack
+            off, G = (None, 0) if k.startswith("w_") else (self.off_d, E)
             f = 1 if k in ("dy", "dgu") else 0
-            fp8.fp8_mx_quantize(t, r, c, c, f, 3, q["row"], q["srow"], q["colT"], q["ldT"], q["scol"], off, E)
+            fp8.fp8_mx_quantize(t, r, c, c, f, 3, q["row"], q["srow"], q["colT"], q["ldT"], q["scol"], off, G)
 
     def run(self, ev=None, world=1):
         fp8, q, o, E, H, F, M = self.fp8, self.q, self.out, self.E, self.H, self.F, self.M

@@ -310,3 +310,19 @@ def test_mx_grouped_bad_offsets_flagged():
     fp8.fp8_mx_grouped_gemm(fp8.GROUPED_M, A, 0, s, B, 0, s, off, 3, 64, 224, 128, C)
     assert fp8.fp8_sync_status() == 1
     assert (C == 3.0).all()
+
+
+def test_mx_quantize_equal_groups_is_plain():
+    """Groups of equal size that are multiples of 128 rows (a stack of expert
+    weights) have no padding, so the grouped MX quantize equals the plain
+    one on the whole stack: bytes and scale bytes."""
+    E, m, cols = 8, 256, 160
+    x = gen_x((E * m, cols), seed=31).to(DEV)
+    off = np.arange(E + 1, dtype=np.int32) * m
+    for fmt in (0, 1):
+        qg = fp8.mx_quantize(x, fmt, 3, group_offsets=torch.from_numpy(off).to(DEV), host_offsets=off)
+        qp = fp8.mx_quantize(x, fmt, 3)
+        assert fp8.fp8_sync_status() == 0
+        assert qg.scale_rows == qp.scale_rows == E * m
+        assert torch.equal(qg.q_row, qp.q_row) and torch.equal(qg.s_row, qp.s_row)
+        assert torch.equal(qg.q_colT[:, :E * m], qp.q_colT[:, :E * m]) and torch.equal(qg.s_col, qp.s_col)
