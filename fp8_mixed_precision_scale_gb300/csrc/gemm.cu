@@ -505,18 +505,21 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 // ---------------------------------------------------------------------------
 constexpr int KT_STAGES = 3;
 constexpr int KT_BOX_BYTES = 32 * 128;  // 32 rows x 64 bf16
+constexpr int KT_THREADS = 576;         // warp 0 TMA, warp 1 MMA, warps 2-9 and 10-17: two epilogue groups
 
 struct SmemLayoutKT {
     static constexpr int a_off = 0;
     static constexpr int b_off = KT_STAGES * A_STAGE_BYTES;
     static constexpr int box_off = b_off + KT_STAGES * B_STAGE_BYTES;      // 1024-aligned
-    static constexpr int bar_off = box_off + 8 * 2 * KT_BOX_BYTES;
+    static constexpr int bar_off = box_off + 16 * KT_BOX_BYTES;            // one box per epilogue warp
     static constexpr int n_bars = 2 * KT_STAGES + 2 + 2 + 1;
     static constexpr int slot_off = bar_off + n_bars * 8;
     static constexpr int misc_off = (slot_off + 16 + 127) / 128 * 128;    // group tables
 };
+static_assert(1024 + SmemLayoutKT::misc_off + 8 * (MAX_GROUPS + 1) + 1024 <= 227 * 1024,
+              "K-grouped ring, boxes and group tables fit in shared memory");
 
-__global__ void __launch_bounds__(GEMM_THREADS, 1)
+__global__ void __launch_bounds__(KT_THREADS, 1)
     fp8_gemm_kgroup_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                                const __grid_constant__ CUtensorMap tmC, GemmParams p, uint32_t idesc)
 {
@@ -640,18 +643,26 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         mbar_wait_bounded(done, 0, WAIT_LIMIT_NS, p.err, ERR_TEARDOWN_WAIT);
     } else if (warp >= 2) {
         // ---------------- epilogue: TMEM -> bf16 boxes -> TMA stores ----------------
+        // Two groups of 8 warps take alternate non-empty tiles: group g
+        // drains accumulator g, so each group has two tile periods for its
+        // drain, conversion and stores.  In a group, warp w reads TMEM lane
+        // quarter w % 4 (the quarter its id may access) and one half (128
+        // columns) of the tile, in two rounds of 64 columns through one box.
+        const int g = (warp - 2) >> 3;
         const int q = warp & 3;
-        const int half = (warp - 2) >> 2;
-        uint8_t *box = smem + L::box_off + (warp - 2) * 2 * KT_BOX_BYTES;
-        int acc = 0;
+        const int half = ((warp - 2) >> 2) & 1;
+        uint8_t *box = smem + L::box_off + (warp - 2) * KT_BOX_BYTES;
         uint32_t acc_phase = 0;
-        for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
+        int64_t nonempty = 0;
+        int64_t i = 0;
+        for (int64_t t = blockIdx.x; t < total; t += gridDim.x, ++i) {
             const TileInfo ti = tile_info<MODE>(p, t, tile_prefix, poff);
             const int64_t qrow0 = ti.row0 + q * 32;  // this warp's first row of C[e]
             const bool live = qrow0 < ti.row_end;    // N % 32 == 0: the quarter is all in or all out
             const int64_t cbeg = ti.col0 + half * (BN / 2);
             if (ti.nkb == 0) {
-                // empty group: its block of C is zero
+                // empty group: its block of C is zero (alternate tiles to alternate groups)
+                if ((i & 1) != g) continue;
                 const int64_t cend = min(cbeg + BN / 2, ti.col_end);
                 if (live) {
                     uint16_t *crow = p.C + ti.c_base + (qrow0 + lane) * p.ldc;
@@ -659,6 +670,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 }
                 continue;
             }
+            if ((nonempty++ & 1) != g) continue;  // the other group's accumulator
             // this tile's scales, loaded before the accumulator wait so their
             // latency hides behind it: the lane's row scale and, for each of
             // the four 32-column chunks, the scale of column (chunk, lane)
@@ -669,57 +681,54 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 const int64_t cc = cbeg + u * 32 + lane;
                 sbl4[u] = p.sb_per_row ? (cc < ti.col_end ? __ldg(p.sb + ti.sb_base + cc) : 0.0f) : __ldg(p.sb);
             }
-            if (!mbar_wait_bounded(&tfull[acc], acc_phase, WAIT_LIMIT_NS, p.err, ERR_EPILOGUE_WAIT)) break;
+            if (!mbar_wait_bounded(&tfull[g], acc_phase, WAIT_LIMIT_NS, p.err, ERR_EPILOGUE_WAIT)) break;
             tc_fence_after();
-            // the previous tile's stores must have read the boxes before they are refilled
-            if (lane == 0) bulk_wait_group_read0();
-            __syncwarp();
-            // the warp's whole 32 x 128 block in one round trip: four loads, one wait
-            uint32_t r[4][32];
-            const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN) +
+            const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(g * BN) +
                                    (uint32_t)(half * (BN / 2));
+            const int32_t y = (int32_t)(ti.c_base / p.ldc + qrow0);  // row of the [G*N][K] view
 #pragma unroll
-            for (int u = 0; u < 4; u++) tmem_ld_32x32b_x32(taddr + 32 * u, r[u]);
-            tmem_ld_wait();
-            // accumulator read: release it to the MMA warp before converting
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[acc]);
+            for (int rd = 0; rd < 2; rd++) {  // round rd: columns 64 rd .. 64 rd + 63 of this warp's 128
+                // the box's previous store must have read it before it is refilled
+                if (lane == 0) bulk_wait_group_read0();
+                __syncwarp();
 #pragma unroll
-            for (int cu = 0; cu < 4; cu++) {  // 32-column chunk 0..3 of this warp's 128 columns
-                uint32_t packed[16];
+                for (int cu = 0; cu < 2; cu++) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(taddr + 64 * rd + 32 * cu, r);
+                    tmem_ld_wait();
+                    if (rd == 1 && cu == 1) {
+                        // the whole block is read: release the accumulator to the MMA warp
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&tempty[g]);
+                    }
+                    uint32_t packed[16];
+                    const float sbv = sbl4[2 * rd + cu];
 #pragma unroll
-                for (int j = 0; j < 16; j++) {
-                    const float lo = __uint_as_float(r[cu][2 * j]) * sa_v * __shfl_sync(0xffffffffu, sbl4[cu], 2 * j);
-                    const float hi =
-                        __uint_as_float(r[cu][2 * j + 1]) * sa_v * __shfl_sync(0xffffffffu, sbl4[cu], 2 * j + 1);
-                    packed[j] = pack_bf16x2(lo, hi);
+                    for (int j = 0; j < 16; j++) {
+                        const float lo = __uint_as_float(r[2 * j]) * sa_v * __shfl_sync(0xffffffffu, sbv, 2 * j);
+                        const float hi = __uint_as_float(r[2 * j + 1]) * sa_v * __shfl_sync(0xffffffffu, sbv, 2 * j + 1);
+                        packed[j] = pack_bf16x2(lo, hi);
+                    }
+                    // 16-byte chunks 4 cu .. 4 cu + 3 of this lane's 128-byte row,
+                    // 128-byte swizzle: chunk index XOR (row % 8)
+                    uint8_t *brow = box + lane * 128;
+#pragma unroll
+                    for (int gg = 0; gg < 4; gg++) {
+                        const int chunk = (cu * 4 + gg) ^ (lane & 7);
+                        *reinterpret_cast<uint4 *>(brow + chunk * 16) =
+                            make_uint4(packed[4 * gg], packed[4 * gg + 1], packed[4 * gg + 2], packed[4 * gg + 3]);
+                    }
                 }
-                // box cu / 2, 16-byte chunks 4 (cu % 2) .. +3 of this lane's 128-byte row,
-                // 128-byte swizzle: chunk index XOR (row % 8)
-                uint8_t *brow = box + (cu >> 1) * KT_BOX_BYTES + lane * 128;
-#pragma unroll
-                for (int g = 0; g < 4; g++) {
-                    const int chunk = ((cu & 1) * 4 + g) ^ (lane & 7);
-                    *reinterpret_cast<uint4 *>(brow + chunk * 16) =
-                        make_uint4(packed[4 * g], packed[4 * g + 1], packed[4 * g + 2], packed[4 * g + 3]);
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0 && live) {
+                    const int64_t x = cbeg + 64 * rd;
+                    if (x < ti.col_end) tma_store_2d(&tmC, (int32_t)x, y, box);
+                    bulk_commit_group();
                 }
             }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            __syncwarp();
-            if (lane == 0 && live) {
-                const int32_t y = (int32_t)(ti.c_base / p.ldc + qrow0);  // row of the [G*N][K] view
-#pragma unroll
-                for (int b = 0; b < 2; b++) {
-                    const int64_t x = cbeg + 64 * b;
-                    if (x < ti.col_end) tma_store_2d(&tmC, (int32_t)x, y, box + b * KT_BOX_BYTES);
-                }
-                bulk_commit_group();
-            }
-            if (++acc == 2) {
-                acc = 0;
-                acc_phase ^= 1;
-            }
+            acc_phase ^= 1;
         }
         if (lane == 0) bulk_wait_group0();
         __syncwarp();
@@ -990,7 +999,7 @@ static fp8_status_t launch_kgroup_tma(const CUtensorMap &ma, const CUtensorMap &
                                          (int)smem);
     if (e != cudaSuccess) return cuda_fail_with(e);
     const uint32_t idesc = idesc_f8f6f4(fa, fb, BM, BN);
-    fp8_gemm_kgroup_tma_kernel<<<(unsigned)grid, GEMM_THREADS, smem, st>>>(ma, mb, mc, p, idesc);
+    fp8_gemm_kgroup_tma_kernel<<<(unsigned)grid, KT_THREADS, smem, st>>>(ma, mb, mc, p, idesc);
     return check_launch();
 }
 
