@@ -174,6 +174,30 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams &p, int64_t t, co
         ti.c_base = 0;
         ti.sa_base = 0;
         ti.sb_base = 0;
+    } else if constexpr (MODE == MODE_KGROUP) {
+        // K-grouped: every group owns num_m_blk x num_n_blk tiles of its
+        // [N][K] output block, so the group is a division (the tile count is
+        // below 2^31); the group's padded column count is the difference of
+        // its padded offsets.  Output block e is [N][K]; the contraction runs
+        // over the group's padded columns.
+        const int per = p.num_m_blk * p.num_n_blk;
+        const int tt = (int)t;
+        const int e = tt / per;
+        const int local = tt - e * per;
+        const int mb = local / p.num_n_blk, nb = local - mb * p.num_n_blk;
+        const int pad = poff[e + 1] - poff[e];
+        ti.a_y = mb * BM;
+        ti.b_y = nb * BN;
+        ti.a_x0 = ti.b_x0 = poff[e];
+        ti.nkb = (pad + BK - 1) / BK;
+        ti.last_steps = ti.nkb > 0 ? (pad - (ti.nkb - 1) * BK) / UMMA_K : 0;
+        ti.row0 = (int64_t)mb * BM;
+        ti.row_end = p.N;  // rows of C[e]
+        ti.col0 = (int64_t)nb * BN;
+        ti.col_end = p.K;
+        ti.c_base = (int64_t)e * p.N * p.K;
+        ti.sa_base = (int64_t)e * p.N;
+        ti.sb_base = (int64_t)e * p.K;
     } else {
         // group e: last with tile_prefix[e] <= t
         int lo = 0, hi = p.G;
@@ -211,22 +235,6 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams &p, int64_t t, co
             ti.c_base = 0;
             ti.sa_base = 0;
             ti.sb_base = (int64_t)e * p.N;
-        } else {
-            // K-grouped: output block e is [N][K]; contraction over the group's padded columns
-            const int64_t nb = local % p.num_n_blk, mb = local / p.num_n_blk;
-            const int64_t pad = (m_e + 31) / 32 * 32;
-            ti.a_y = (int32_t)(mb * BM);
-            ti.b_y = (int32_t)(nb * BN);
-            ti.a_x0 = ti.b_x0 = poff[e];
-            ti.nkb = (int)((pad + BK - 1) / BK);
-            ti.last_steps = ti.nkb > 0 ? (int)((pad - (int64_t)(ti.nkb - 1) * BK) / UMMA_K) : 0;
-            ti.row0 = mb * BM;
-            ti.row_end = p.N;  // rows of C[e]
-            ti.col0 = nb * BN;
-            ti.col_end = p.K;
-            ti.c_base = (int64_t)e * p.N * p.K;
-            ti.sa_base = (int64_t)e * p.N;
-            ti.sb_base = (int64_t)e * p.K;
         }
     }
     return ti;
@@ -603,15 +611,19 @@ __global__ void __launch_bounds__(KT_THREADS, 1)
                 mbar_wait_bounded(&full[s], (uint32_t)issued_parity[s], WAIT_LIMIT_NS, p.err, ERR_TEARDOWN_WAIT);
     } else if (warp == 1 && lane == 0) {
         // ---------------- MMA issuer ----------------
+        // the CTA's i-th tile goes to accumulator i % 2 (drained by epilogue
+        // group i % 2); bit a of acc_phase is the phase of accumulator a
         int stage = 0;
         uint32_t phase = 0;
-        int acc = 0;
         uint32_t acc_phase = 0;
         bool ok = true;
-        for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        int64_t i = 0;
+        for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x, ++i) {
             const TileInfo ti = tile_info<MODE>(p, t, tile_prefix, poff);
             if (ti.nkb == 0) continue;
-            if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1, WAIT_LIMIT_NS, p.err, ERR_MMA_WAIT)) break;
+            const int acc = (int)(i & 1);
+            if (!mbar_wait_bounded(&tempty[acc], ((acc_phase >> acc) & 1u) ^ 1u, WAIT_LIMIT_NS, p.err, ERR_MMA_WAIT))
+                break;
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
             for (int kb = 0; kb < ti.nkb; kb++) {
@@ -634,35 +646,29 @@ __global__ void __launch_bounds__(KT_THREADS, 1)
             }
             if (!ok) break;
             mma_commit(&tfull[acc]);
-            if (++acc == 2) {
-                acc = 0;
-                acc_phase ^= 1;
-            }
+            acc_phase ^= 1u << acc;
         }
         mma_commit(done);
         mbar_wait_bounded(done, 0, WAIT_LIMIT_NS, p.err, ERR_TEARDOWN_WAIT);
     } else if (warp >= 2) {
         // ---------------- epilogue: TMEM -> bf16 boxes -> TMA stores ----------------
-        // Two groups of 8 warps take alternate non-empty tiles: group g
+        // Two groups of 8 warps take alternate tiles of the CTA: group g
         // drains accumulator g, so each group has two tile periods for its
-        // drain, conversion and stores.  In a group, warp w reads TMEM lane
-        // quarter w % 4 (the quarter its id may access) and one half (128
-        // columns) of the tile, in two rounds of 64 columns through one box.
+        // drain, conversion and stores, and looks up only its own tiles.  In
+        // a group, warp w reads TMEM lane quarter w % 4 (the quarter its id
+        // may access) and one half (128 columns) of the tile, in two rounds
+        // of 64 columns through one box.  An empty group's tiles are zeros.
         const int g = (warp - 2) >> 3;
         const int q = warp & 3;
         const int half = ((warp - 2) >> 2) & 1;
         uint8_t *box = smem + L::box_off + (warp - 2) * KT_BOX_BYTES;
         uint32_t acc_phase = 0;
-        int64_t nonempty = 0;
-        int64_t i = 0;
-        for (int64_t t = blockIdx.x; t < total; t += gridDim.x, ++i) {
+        for (int64_t t = blockIdx.x + (int64_t)g * gridDim.x; t < total; t += 2 * (int64_t)gridDim.x) {
             const TileInfo ti = tile_info<MODE>(p, t, tile_prefix, poff);
             const int64_t qrow0 = ti.row0 + q * 32;  // this warp's first row of C[e]
             const bool live = qrow0 < ti.row_end;    // N % 32 == 0: the quarter is all in or all out
             const int64_t cbeg = ti.col0 + half * (BN / 2);
             if (ti.nkb == 0) {
-                // empty group: its block of C is zero (alternate tiles to alternate groups)
-                if ((i & 1) != g) continue;
                 const int64_t cend = min(cbeg + BN / 2, ti.col_end);
                 if (live) {
                     uint16_t *crow = p.C + ti.c_base + (qrow0 + lane) * p.ldc;
@@ -670,7 +676,6 @@ __global__ void __launch_bounds__(KT_THREADS, 1)
                 }
                 continue;
             }
-            if ((nonempty++ & 1) != g) continue;  // the other group's accumulator
             // this tile's scales, loaded before the accumulator wait so their
             // latency hides behind it: the lane's row scale and, for each of
             // the four 32-column chunks, the scale of column (chunk, lane)
