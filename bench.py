@@ -38,6 +38,7 @@ Other workloads (same JSON line, their own config):
   gemm, quantize single kernels of the default step, for profiling
   grouped_m, grouped_k  one M-grouped / K-grouped expert GEMM of a reduced
                  MoE layer (64 experts, 8192 routed rows), for profiling
+  mx_grouped_k   the MXFP8 K-grouped wgrad of that layer, for profiling
   quantize_grouped  the rowwise quantize of one reduced MoE weight (64
                  experts x 2048 rows x 7168), for profiling
   mx_gemm, mx_quantize  the MXFP8 gate GEMM / the MX quantize of dY_gate
@@ -1014,8 +1015,8 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.set_device(dev)
     hbm_gbs = peaks()[0]
 
-    if args.workload in ("gemm", "quantize", "grouped_m", "grouped_k", "quantize_grouped", "mx_gemm", "mx_quantize",
-                         "mx_permute", "mx_swiglu", "permute", "swiglu", "bw_quantize", "rowwise_quantize",
+    if args.workload in ("gemm", "quantize", "grouped_m", "grouped_k", "mx_grouped_k", "quantize_grouped", "mx_gemm",
+                         "mx_quantize", "mx_permute", "mx_swiglu", "permute", "swiglu", "bw_quantize", "rowwise_quantize",
                          "rowwise_resident"):
         run_single_kernel(args, dev, rank)
         return
@@ -1417,6 +1418,18 @@ def grouped_case(kind, dev, E=64, rows=8192):
                                           s_ef, 1, C, 0)
         wbytes = int((sizes > 0).sum()) * F * H
         return fn, (rows * H + wbytes + 2.0 * rows * F) / 1e9, "GB/s (algorithmic)"
+    if kind == "mx_grouped_k":    # MXFP8 wgrad of the gate projection from grouped MX quantizes
+        gb = torch.Generator(device=dev)
+        gb.manual_seed(8)
+        dy = torch.randn((rows, F), generator=gb, device=dev).to(torch.bfloat16)
+        x = torch.randn((rows, H), generator=gb, device=dev).to(torch.bfloat16)
+        off_h = torch.from_numpy(off)
+        qa = fp8.mx_quantize(dy, 0, fp8.LAYOUT_COLT, group_offsets=off_d, host_offsets=off_h)
+        qb = fp8.mx_quantize(x, 0, fp8.LAYOUT_COLT, group_offsets=off_d, host_offsets=off_h)
+        C = torch.empty((E, F, H), dtype=torch.bfloat16, device=dev)
+        fn = lambda: fp8.fp8_mx_grouped_gemm(fp8.GROUPED_K, qa.q_colT, 0, qa.s_col, qb.q_colT, 0, qb.s_col,  # noqa
+                                             off_d, E, rows, F, H, C, qa.ld_colT)
+        return fn, (rows * (F + H) + 2.0 * E * F * H) / 1e9, "GB/s (algorithmic)"
     ldT = int(fp8.fp8_group_padded_offsets(off)[0])
     ldT = (ldT + 15) // 16 * 16
     A, B = codes(F, ldT), codes(H, ldT)   # wgrad of the gate projection: dW_e = dY_e^T X_e
@@ -1510,7 +1523,7 @@ def run_single_kernel(args, dev, rank):
     if args.workload in ("mx_permute", "mx_swiglu", "permute", "swiglu"):
         fn, unfused, work = moe_fused_case(args.workload, dev)
         unit = "GB/s (algorithmic)"
-    elif args.workload in ("grouped_m", "grouped_k"):
+    elif args.workload in ("grouped_m", "grouped_k", "mx_grouped_k"):
         fn, work, unit = grouped_case(args.workload, dev)
     elif args.workload == "quantize_grouped":
         fn, work, unit = grouped_weight_quantize_case(dev)
@@ -1630,7 +1643,8 @@ def main():
                              "moe_mxfp8", "flux", "tiny",
                              "sweep",
                              "gemm", "quantize", "bw_quantize", "rowwise_quantize", "rowwise_resident",
-                             "grouped_m", "grouped_k", "quantize_grouped", "mx_gemm", "mx_quantize", "mx_permute",
+                             "grouped_m", "grouped_k", "mx_grouped_k", "quantize_grouped", "mx_gemm", "mx_quantize",
+                             "mx_permute",
                              "mx_swiglu", "permute", "swiglu"],
                     help="llama_mlp: the whole fwd+bwd FP8 step of the Llama-3-8B MLP (default); see the "
                          "module docstring for the others")

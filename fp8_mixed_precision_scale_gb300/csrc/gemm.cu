@@ -669,10 +669,21 @@ __global__ void __launch_bounds__(KT_THREADS, 1)
             const bool live = qrow0 < ti.row_end;    // N % 32 == 0: the quarter is all in or all out
             const int64_t cbeg = ti.col0 + half * (BN / 2);
             if (ti.nkb == 0) {
-                const int64_t cend = min(cbeg + BN / 2, ti.col_end);
-                if (live) {
-                    uint16_t *crow = p.C + ti.c_base + (qrow0 + lane) * p.ldc;
-                    for (int64_t c = cbeg; c < cend; c += 8) *reinterpret_cast<uint4 *>(crow + c) = make_uint4(0, 0, 0, 0);
+                // empty group: the warp's box filled with zeros, stored over
+                // its two 64-column chunks by TMA
+                if (lane == 0) bulk_wait_group_read0();
+                __syncwarp();
+                for (int k = lane; k < KT_BOX_BYTES / 16; k += 32)
+                    reinterpret_cast<uint4 *>(box)[k] = make_uint4(0, 0, 0, 0);
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0 && live) {
+                    const int32_t y = (int32_t)(ti.c_base / p.ldc + qrow0);
+                    for (int rd = 0; rd < 2; rd++) {
+                        const int64_t x = cbeg + 64 * rd;
+                        if (x < ti.col_end) tma_store_2d(&tmC, (int32_t)x, y, box);
+                    }
+                    bulk_commit_group();
                 }
                 continue;
             }

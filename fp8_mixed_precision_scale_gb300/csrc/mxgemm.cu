@@ -116,17 +116,22 @@ struct Smem {
     static constexpr int n_bars = 3 * NS + 2 + 2 + 2;
     static constexpr int slot_off = bar_off + n_bars * 8;
     // epilogue staging per warp: a 32 x 32 transpose block (direct stores) or
-    // two 32-row x 64-column TMA boxes (1024-aligned for the 128-byte swizzle)
-    static constexpr int stage_warp = TMA_OUT ? 2 * 32 * 128 : 32 * 80;
+    // one 32-row x 64-column TMA box, filled twice per tile (1024-aligned for
+    // the 128-byte swizzle)
+    static constexpr int stage_warp = TMA_OUT ? 32 * 128 : 32 * 80;
     static constexpr int stage_off = TMA_OUT ? (slot_off + 16 + 1023) / 1024 * 1024 : (slot_off + 16 + 127) / 128 * 128;
     static constexpr int misc_off = stage_off + 8 * stage_warp;  // group tables
 };
 constexpr int STAGE_PITCH = 80;  // epilogue staging: 32 rows x 32 bf16 per warp, rows padded to 80 bytes
-constexpr int BOX_BYTES = 32 * 128;  // TMA store box: 32 rows x 64 bf16
 __host__ __device__ constexpr int ring_stages(int mode, bool tma_out)
 {
-    return tma_out ? 2 : (mode == 0 ? STAGES : STAGES_GROUPED);
+    return tma_out ? STAGES_GROUPED : (mode == 0 ? STAGES : STAGES_GROUPED);
 }
+// dynamic (ring, staging, group tables, 1024 alignment slack) plus the static
+// block fit the 227 KB a block may use
+static_assert(1024 + Smem<STAGES_GROUPED, true>::misc_off + 8 * (MAX_GROUPS + 1) + 1024 <= 227 * 1024, "smem");
+static_assert(1024 + Smem<STAGES_GROUPED, false>::misc_off + 8 * (MAX_GROUPS + 1) + 1024 <= 227 * 1024, "smem");
+static_assert(1024 + Smem<STAGES, false>::misc_off + 1024 <= 227 * 1024, "smem");
 
 // Tile prefix [G+1] and offsets padded to FP8_MX_GROUP_ALIGN [G+1]; one warp.
 __device__ bool build_group_tables(const Params &p, int MODE, int32_t *tile_prefix, int32_t *poff,
@@ -200,6 +205,30 @@ __device__ __forceinline__ Tile tile_info(const Params &p, int64_t t, const int3
         ti.col0 = (int64_t)nb * BN;
         ti.col_end = p.N;
         ti.c_base = 0;
+    } else if constexpr (MODE == MODE_KGROUP) {
+        // K-grouped: every group owns num_m_blk x num_n_blk tiles of its
+        // [N][K] output block, so the group is a division (the tile count is
+        // below 2^31).  The contraction runs over group e's columns, which
+        // start at poff[e] (a multiple of 128).
+        const int per = p.num_m_blk * p.num_n_blk;
+        const int tt = (int)t;
+        const int e = tt / per;
+        const int local = tt - e * per;
+        const int mb = local / p.num_n_blk, nb = local - mb * p.num_n_blk;
+        const int m_e = __ldg(p.offsets + e + 1) - __ldg(p.offsets + e);
+        ti.a_y = mb * BM;
+        ti.b_y = nb * BN;
+        ti.a_x0 = ti.b_x0 = poff[e];
+        ti.sa_row = (int64_t)mb * BM;
+        ti.sb_row = (int64_t)nb * BN;
+        ti.kt0a = ti.kt0b = poff[e] / BK;
+        ti.nkb = (m_e + BK - 1) / BK;
+        ti.last_steps = ti.nkb > 0 ? (m_e - (ti.nkb - 1) * BK + UMMA_K - 1) / UMMA_K : 0;
+        ti.row0 = (int64_t)mb * BM;
+        ti.row_end = p.N;
+        ti.col0 = (int64_t)nb * BN;
+        ti.col_end = p.K;
+        ti.c_base = (int64_t)e * p.N * p.K;
     } else {
         int lo = 0, hi = p.G;  // group e: last with tile_prefix[e] <= t
         while (hi - lo > 1) {
@@ -239,23 +268,6 @@ __device__ __forceinline__ Tile tile_info(const Params &p, int64_t t, const int3
             ti.col0 = nb * BN;
             ti.col_end = p.N;
             ti.c_base = 0;
-        } else {
-            // K-grouped: output block e is [N][K]; the contraction runs over
-            // group e's columns, which start at poff[e] (a multiple of 128)
-            const int64_t nb = local % p.num_n_blk, mb = local / p.num_n_blk;
-            ti.a_y = (int32_t)(mb * BM);
-            ti.b_y = (int32_t)(nb * BN);
-            ti.a_x0 = ti.b_x0 = poff[e];
-            ti.sa_row = mb * BM;
-            ti.sb_row = nb * BN;
-            ti.kt0a = ti.kt0b = poff[e] / BK;
-            ti.nkb = (int)((m_e + BK - 1) / BK);
-            ti.last_steps = ti.nkb > 0 ? (int)((m_e - (int64_t)(ti.nkb - 1) * BK + UMMA_K - 1) / UMMA_K) : 0;
-            ti.row0 = mb * BM;
-            ti.row_end = p.N;
-            ti.col0 = nb * BN;
-            ti.col_end = p.K;
-            ti.c_base = (int64_t)e * p.N * p.K;
         }
     }
     return ti;
@@ -326,33 +338,58 @@ __device__ __forceinline__ void epilogue_tile_tma(const Params &p, const Tile &t
     tmem_ld_wait();
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) {
-        mbar_arrive(tempty);
-        bulk_wait_group_read0();
-    }
-    __syncwarp();
+    if (lane == 0) mbar_arrive(tempty);
+    const int64_t qrow0 = ti.row0 + q * 32;
+    const int32_t y = (int32_t)(ti.c_base / p.ldc + qrow0);  // row of the [G*N][K] view of C
+    // two rounds of 64 columns through the warp's one box
 #pragma unroll
-    for (int u = 0; u < 4; u++) {
-        uint8_t *brow = box + (u >> 1) * BOX_BYTES + lane * 128;
+    for (int b = 0; b < 2; b++) {
+        // the box's previous store must have read it before it is refilled
+        if (lane == 0) bulk_wait_group_read0();
+        __syncwarp();
+        uint8_t *brow = box + lane * 128;
 #pragma unroll
-        for (int g = 0; g < 4; g++) {
-            const int chunk = ((u & 1) * 4 + g) ^ (lane & 7);
-            *reinterpret_cast<uint4 *>(brow + chunk * 16) =
-                make_uint4(pack_bf16x2(__uint_as_float(r[u][8 * g]), __uint_as_float(r[u][8 * g + 1])),
-                           pack_bf16x2(__uint_as_float(r[u][8 * g + 2]), __uint_as_float(r[u][8 * g + 3])),
-                           pack_bf16x2(__uint_as_float(r[u][8 * g + 4]), __uint_as_float(r[u][8 * g + 5])),
-                           pack_bf16x2(__uint_as_float(r[u][8 * g + 6]), __uint_as_float(r[u][8 * g + 7])));
+        for (int h = 0; h < 2; h++) {
+            const int u = 2 * b + h;
+#pragma unroll
+            for (int g = 0; g < 4; g++) {
+                const int chunk = (h * 4 + g) ^ (lane & 7);
+                *reinterpret_cast<uint4 *>(brow + chunk * 16) =
+                    make_uint4(pack_bf16x2(__uint_as_float(r[u][8 * g]), __uint_as_float(r[u][8 * g + 1])),
+                               pack_bf16x2(__uint_as_float(r[u][8 * g + 2]), __uint_as_float(r[u][8 * g + 3])),
+                               pack_bf16x2(__uint_as_float(r[u][8 * g + 4]), __uint_as_float(r[u][8 * g + 5])),
+                               pack_bf16x2(__uint_as_float(r[u][8 * g + 6]), __uint_as_float(r[u][8 * g + 7])));
+            }
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0 && qrow0 < ti.row_end) {
+            const int64_t x = ti.col0 + cb + 64 * b;
+            if (x < ti.col_end) tma_store_2d(tmC, (int32_t)x, y, box);
+            bulk_commit_group();
         }
     }
+}
+
+// An empty K-group's block of C for one epilogue warp (rows q*32 .. q*32+31
+// of the tile, columns [cb, cb + 128)): the warp's box filled with zeros and
+// stored over its two 64-column chunks by TMA.  Out of line: it is off the
+// hot path and would otherwise take registers from the epilogue.
+__device__ __noinline__ void zero_block_tma(const Params &p, const Tile &ti, int q, int cb, int lane, uint8_t *box,
+                                            const CUtensorMap *tmC)
+{
+    if (lane == 0) bulk_wait_group_read0();
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < 32 * 128 / 16 / 32; k++) reinterpret_cast<uint4 *>(box)[k * 32 + lane] = make_uint4(0, 0, 0, 0);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncwarp();
     const int64_t qrow0 = ti.row0 + q * 32;
     if (lane == 0 && qrow0 < ti.row_end) {
-        const int32_t y = (int32_t)(ti.c_base / p.ldc + qrow0);  // row of the [G*N][K] view of C
-#pragma unroll
+        const int32_t y = (int32_t)(ti.c_base / p.ldc + qrow0);
         for (int b = 0; b < 2; b++) {
             const int64_t x = ti.col0 + cb + 64 * b;
-            if (x < ti.col_end) tma_store_2d(tmC, (int32_t)x, y, box + b * BOX_BYTES);
+            if (x < ti.col_end) tma_store_2d(tmC, (int32_t)x, y, box);
         }
         bulk_commit_group();
     }
@@ -566,12 +603,16 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t acc_phase = 0;
         for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
             const Tile ti = tile_info<MODE>(p, t, tile_prefix, poff);
-            if (ti.nkb == 0) {  // empty K-group: its block of C is zero (direct stores)
-                const int64_t gr = ti.row0 + q * 32 + lane;
-                if (gr < ti.row_end) {
-                    uint16_t *crow = p.C + ti.c_base + gr * p.ldc;
-                    const int64_t c1 = ti.col0 + cb + 128 < ti.col_end ? ti.col0 + cb + 128 : ti.col_end;
-                    for (int64_t c = ti.col0 + cb; c < c1; c++) crow[c] = 0;
+            if (ti.nkb == 0) {  // empty K-group: its block of C is zero
+                if constexpr (TMA_OUT) {
+                    zero_block_tma(p, ti, q, cb, lane, stage, &tmC);
+                } else {
+                    const int64_t gr = ti.row0 + q * 32 + lane;
+                    if (gr < ti.row_end) {
+                        uint16_t *crow = p.C + ti.c_base + gr * p.ldc;
+                        const int64_t c1 = ti.col0 + cb + 128 < ti.col_end ? ti.col0 + cb + 128 : ti.col_end;
+                        for (int64_t c = ti.col0 + cb; c < c1; c++) crow[c] = 0;
+                    }
                 }
                 continue;
             }

@@ -255,8 +255,10 @@ def test_mx_grouped_k_small(orc, NK):
     qd = orc.mx_quantize(bits(gen_x((Mt, N), seed=41)), 1, fp8.LAYOUT_COLT, offsets=off, align=128)
     qx = orc.mx_quantize(bits(gen_x((Mt, K), seed=42)), 0, fp8.LAYOUT_COLT, offsets=off, align=128)
     P = qd["q_colT"].shape[1]
+    # a NaN sentinel in every element: the empty groups' zeros are written, not left over
+    sentinel = torch.full((G, N, K), float("nan"), dtype=torch.bfloat16, device=DEV)
     C = fp8.mx_grouped_gemm(fp8.GROUPED_K, up(qd["q_colT"]), 1, up(mx_tiled(qd["s_col"])), up(qx["q_colT"]), 0,
-                            up(mx_tiled(qx["s_col"])), up(off), Mt, N, K, ld_T=P)
+                            up(mx_tiled(qx["s_col"])), up(off), Mt, N, K, ld_T=P, out=sentinel)
     assert fp8.fp8_sync_status() == 0
     poff = orc.padded_offsets_align(off, 128)
     out = C.float().cpu().numpy()
