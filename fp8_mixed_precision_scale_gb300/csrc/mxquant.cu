@@ -34,7 +34,7 @@ namespace fp8gb {
 constexpr int MX_THREADS = 256;
 constexpr int MX_ROWS = 64;             // rows per tile
 constexpr int MX_COLS = 128;            // columns per tile: four blocks of a row
-constexpr int MX_PITCH = MX_COLS + 8;   // bf16 per shared-memory row (16-byte pad)
+constexpr int MX_PITCH_W = 72;          // 32-bit words per shared-memory row (64 + two 4-word pads)
 constexpr int MX_MAX_GROUPS = 4096;
 
 struct MxArgs {
@@ -48,6 +48,7 @@ struct MxArgs {
     const int32_t *offsets;
     int G;
     int do_row, do_col;
+    int ld32;  // every row block of the input starts on a 32-byte boundary: 32-byte loads
     unsigned int *err;
     // prologues (template parameter PRO of the kernel)
     const int32_t *src_rows;  // PRO_GATHER: output row r reads input row src_rows[r]
@@ -177,6 +178,15 @@ __device__ __forceinline__ MxTile mx_tile(const MxArgs &a, int64_t t, int64_t pr
 
 // Raw input registers of one thread for one tile: the 32 bf16 of its row
 // block, and for SwiGLU the 32 gate and 32 up values.
+// 32 bytes (16 bf16) from a 32-byte-aligned address through the read-only
+// path, as two 16-byte halves.
+__device__ __forceinline__ void ld_nc_32b(const uint16_t *p, uint4 &lo, uint4 &hi)
+{
+    asm volatile("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(lo.x), "=r"(lo.y), "=r"(lo.z), "=r"(lo.w), "=r"(hi.x), "=r"(hi.y), "=r"(hi.z), "=r"(hi.w)
+                 : "l"(p));
+}
+
 template <int PRO>
 struct MxRaw {
     uint4 v[PRO == PRO_SWIGLU ? 8 : 4];
@@ -204,13 +214,23 @@ __device__ __forceinline__ void mx_load(const MxArgs &a, const MxTile &g, int ti
         if (r >= 0) row = a.x + r * a.ld_x + g.c0 + 32 * blk;
     }
     if (row) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(row);
+        if (a.ld32) {
+            // whole 32-byte sectors per load
+            ld_nc_32b(row, raw.v[0], raw.v[1]);
+            ld_nc_32b(row + 16, raw.v[2], raw.v[3]);
+            if constexpr (PRO == PRO_SWIGLU) {
+                ld_nc_32b(row + a.up_off, raw.v[4], raw.v[5]);
+                ld_nc_32b(row + a.up_off + 16, raw.v[6], raw.v[7]);
+            }
+        } else {
+            const uint4 *src = reinterpret_cast<const uint4 *>(row);
 #pragma unroll
-        for (int j = 0; j < 4; j++) raw.v[j] = __ldg(src + j);
-        if constexpr (PRO == PRO_SWIGLU) {
-            const uint4 *up = reinterpret_cast<const uint4 *>(row + a.up_off);
+            for (int j = 0; j < 4; j++) raw.v[j] = __ldg(src + j);
+            if constexpr (PRO == PRO_SWIGLU) {
+                const uint4 *up = reinterpret_cast<const uint4 *>(row + a.up_off);
 #pragma unroll
-            for (int j = 0; j < 4; j++) raw.v[4 + j] = __ldg(up + j);
+                for (int j = 0; j < 4; j++) raw.v[4 + j] = __ldg(up + j);
+            }
         }
     } else {
 #pragma unroll
@@ -242,16 +262,23 @@ __device__ __forceinline__ void mx_prologue(const MxArgs &a, const MxTile &g, in
     }
 }
 
-// Shared tile: 64 rows of MX_PITCH / 2 words; the 32-bit word (column pair)
+// Shared tile: 64 rows of MX_PITCH_W words.  The 32-bit word (column pair)
 // index is XOR-swizzled by 16 in rows 16-31 of every 32, so the transposed
-// phase's column-pair reads (rows r and r + 16 in one warp) hit all 32 banks.
-__device__ __forceinline__ int mx_word(int row, int pair) { return row * (MX_PITCH / 2) + (pair ^ ((row & 16))); }
+// phase's column-pair reads (rows r and r + 16 in one warp) hit all 32 banks;
+// a 4-word gap after the first 32 words of a row and the row pitch of 72
+// words (8 banks mod 32) make the row phase's 16-byte stores (two rows x four
+// 32-column blocks per quarter warp) hit 32 distinct banks too.
+__device__ __forceinline__ int mx_word(int row, int pair)
+{
+    const int pp = pair ^ (row & 16);
+    return row * MX_PITCH_W + pp + 4 * (pp >> 5);
+}
 
 template <int FMT, int PRO>
 __global__ void __launch_bounds__(MX_THREADS)
     mx_quantize_kernel(MxArgs a)
 {
-    __shared__ __align__(16) uint32_t tile[MX_ROWS * MX_PITCH / 2];
+    __shared__ __align__(16) uint32_t tile[MX_ROWS * MX_PITCH_W];
     extern __shared__ int32_t poff[];  // grouped: padded offsets [G + 1], then the offsets [G + 1]
     __shared__ int s_bad;
 
@@ -428,6 +455,9 @@ static fp8_status_t mx_run(MxArgs a, int fmt, int layouts, int pro, cudaStream_t
     }
     a.do_row = do_row;
     a.do_col = do_col;
+    // row blocks start at x + r * ld_x + 32 k (+ up_off): 32-byte aligned
+    // when the base is and the strides are multiples of 16 elements
+    a.ld32 = aligned(a.x, 32) && a.ld_x % 16 == 0 && a.up_off % 16 == 0;
     a.rs_row = (rows + 3) / 4 * 4;
     a.n_col_tiles = (cols + MX_COLS - 1) / MX_COLS;
     a.err = device_error_word();
