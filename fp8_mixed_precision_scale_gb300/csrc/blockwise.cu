@@ -36,7 +36,7 @@ struct BwArgs {
     int64_t rows, cols, ld_x;
     uint8_t *q_row, *s_row, *q_colT, *s_col;
     int64_t ld_colT;
-    int64_t rs_row;  // scale rows of s_row (rows rounded up to 4)
+    int64_t rs_row;  // scale rows of s_row (rows rounded up to 128)
     int64_t n_col_tiles;
     int do_row, do_col;
 };
@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(BW_THREADS)
         }
         // one scale word per row and 128-column tile: the code in all four slots
         if (half == 0 && r0 + r < a.rs_row)
-            *reinterpret_cast<uint32_t *>(a.s_row + (ct * a.rs_row + r0 + r) * 4) =
+            *reinterpret_cast<uint32_t *>(a.s_row + mx_scale_word(ct, r0 + r, a.rs_row) * 4) =
                 row_real ? code * 0x01010101u : 0u;
     }
 
@@ -177,10 +177,9 @@ __global__ void __launch_bounds__(BW_THREADS)
         d0[1] = make_uint4(o0[4], o0[5], o0[6], o0[7]);
         d1[0] = make_uint4(o1[0], o1[1], o1[2], o1[3]);
         d1[1] = make_uint4(o1[4], o1[5], o1[6], o1[7]);
-        if (qq == 0) {
-            uint32_t *sc = reinterpret_cast<uint32_t *>(a.s_col + (rt * a.cols + c) * 4);
-            sc[0] = code0 * 0x01010101u;
-            sc[1] = code1 * 0x01010101u;
+        if (qq == 0) {  // scale rows c and c + 1 of s_col (cols is a multiple of 128)
+            *reinterpret_cast<uint32_t *>(a.s_col + mx_scale_word(rt, c, a.cols) * 4) = code0 * 0x01010101u;
+            *reinterpret_cast<uint32_t *>(a.s_col + mx_scale_word(rt, c + 1, a.cols) * 4) = code1 * 0x01010101u;
         }
     }
 }
@@ -213,7 +212,7 @@ extern "C" fp8_status_t fp8_blockwise_quantize(const void *x_bf16, int64_t rows,
     if ((do_col || block_rows == BW_TILE) && rows % BW_TILE != 0) return FP8_ERR_ALIGNMENT;
     if (do_row && (!aligned(q_row, 16) || !aligned(s_row, 4))) return FP8_ERR_ALIGNMENT;
     if (do_col) {
-        if (ld_colT % 16 != 0 || !aligned(q_colT, 16) || !aligned(s_col, 8)) return FP8_ERR_ALIGNMENT;
+        if (ld_colT % 16 != 0 || !aligned(q_colT, 16) || !aligned(s_col, 4)) return FP8_ERR_ALIGNMENT;
         if (ld_colT < rows) return FP8_ERR_INVALID_ARG;
     }
     BwArgs a{};
@@ -226,7 +225,7 @@ extern "C" fp8_status_t fp8_blockwise_quantize(const void *x_bf16, int64_t rows,
     a.q_colT = q_colT;
     a.s_col = s_col;
     a.ld_colT = ld_colT;
-    a.rs_row = (rows + 3) / 4 * 4;
+    a.rs_row = round_up_128(rows);
     a.n_col_tiles = cols / BW_TILE;
     a.do_row = do_row;
     a.do_col = do_col;

@@ -566,4 +566,17 @@ __device__ __forceinline__ uint32_t swiglu2(uint32_t g2, uint32_t u2)
     return bf16_bits_rne(swiglu1(bf16lo(g2), bf16lo(u2))) | (bf16_bits_rne(swiglu1(bf16hi(g2), bf16hi(u2))) << 16);
 }
 
+// ---------------------------------------------------------------------------
+// MX scale layout: word (four E8M0 codes, one per 32-element block of a
+// 128-element K tile) of scale row r in K tile kt, for R128 scale rows per K
+// tile (a multiple of 128).  Each 128-row block is 512 contiguous bytes in the
+// order a tcgen05.cp 32x128b copy reads them: row 32 j + L at lane L, word j.
+// ---------------------------------------------------------------------------
+__host__ __device__ __forceinline__ int64_t mx_scale_word(int64_t kt, int64_t r, int64_t R128)
+{
+    return kt * R128 + (r & ~(int64_t)127) + ((r & 31) << 2) + ((r >> 5) & 3);
+}
+
+__host__ __device__ __forceinline__ int64_t round_up_128(int64_t v) { return (v + 127) / 128 * 128; }
+
 }  // namespace fp8gb

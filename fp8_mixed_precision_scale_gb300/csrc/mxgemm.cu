@@ -12,22 +12,24 @@
 // TorchTitan and TorchAO"), with the OCP Microscaling block rule.
 //
 // Design (GB300, sm_103a): the persistent warp-specialised structure of the
-// tensor-scaled GEMM plus a scale warp, 352 threads per CTA, one CTA per SM.
+// tensor-scaled GEMM plus a scale-copy warp, 352 threads per CTA, one CTA
+// per SM.
 //   warp 0     producer: TMA tiles of A (128 x 128 bytes) and B (256 x 128
-//              bytes), plus one bulk copy each of the tiles' scale words
-//              (one 32-bit word per row and 128-element K tile), all counted
-//              on one mbarrier per stage of the ring (4 stages dense, 3
-//              grouped, 2 with the TMA-store epilogue).
-//   warp 10    scales: rearranges each stage's scale words into the 32-lane
-//              x 16-byte blocks that tcgen05.cp 32x128b.warpx4 copies into
-//              tensor memory (word of row 32j + L at lane L, column j,
-//              replicated into every lane quarter: the column and lane the
-//              block-scaled MMA reads for that row), issues the three copies
-//              into the stage's own scale columns and commits them to a
-//              per-stage barrier -- off the MMA thread's critical path.
-//   warp 1     MMA: one thread waits for a stage's scales and issues its four
-//              K=32 MMAs, each selecting its byte of the scale words by the
-//              scale-factor ids of the instruction descriptor.
+//              bytes), plus one bulk copy each of the tiles' scale blocks,
+//              all counted on one mbarrier per stage of the ring (4 stages
+//              dense, 3 grouped and with the TMA-store epilogue).  The MX
+//              scale layout stores every 128 scale rows of a K tile as the
+//              512-byte block tcgen05.cp 32x128b.warpx4 reads (word of row
+//              32j + L at lane L, column j, replicated into every lane
+//              quarter: the column and lane the block-scaled MMA reads for
+//              that row), so the copies land ready to use.
+//   warp 10    scale copies: one thread waits for each stage's loads, issues
+//              the three copies of its scale blocks into the stage's own
+//              TMEM scale columns and commits them to a per-stage barrier,
+//              running ahead of the MMA thread by up to the ring.
+//   warp 1     MMA: one thread waits for a stage's scales and issues its
+//              four K=32 MMAs, each selecting its byte of the scale words by
+//              the scale-factor ids of the instruction descriptor.
 //   warps 2-9  epilogue: each warp drains its 32 x 128 block of the
 //              accumulator into registers and releases it, then converts to
 //              bf16 and stores (shared-memory transpose and whole-sector
@@ -56,13 +58,11 @@ constexpr int BK = 128;
 constexpr int UMMA_K = 32;
 constexpr int STAGES = 4;         // dense; grouped kernels keep 3 (room for the group tables)
 constexpr int STAGES_GROUPED = 3;
-constexpr int THREADS = 352;  // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue, warp 10 scales
+constexpr int THREADS = 352;  // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue, warp 10 scale copies
 constexpr int A_BYTES = BM * BK;
 constexpr int B_BYTES = BN * BK;
 constexpr int SFA_RAW = BM * 4;   // one scale word per A row
 constexpr int SFB_RAW = 256 * 4;  // BN words used; room for two 128-row blocks
-constexpr int SFA_CP = 512;       // [32 lanes][4 words]
-constexpr int SFB_CP = 1024;      // two such blocks (rows 0-127, 128-255)
 constexpr uint32_t TMEM_COLS = 512;
 // one 256-column accumulator at column 0; scale columns, one set per ring
 // stage so a stage's copies never overwrite scales that MMAs of an earlier
@@ -80,7 +80,7 @@ enum { MODE_DENSE = 0, MODE_MGROUP = 1, MODE_KGROUP = 2 };
 struct Params {
     int64_t M, N, K;
     const uint8_t *sA, *sB;
-    int64_t rsA, rsB;  // scale rows of the A / B scale layouts (multiples of 4)
+    int64_t rsA, rsB;  // scale rows of the A / B scale layouts (multiples of 128)
     uint16_t *C;
     int64_t ldc;
     int c_vec16;
@@ -110,9 +110,7 @@ struct Smem {
     static constexpr int b_off = NS * A_BYTES;
     static constexpr int sfa_raw_off = b_off + NS * B_BYTES;
     static constexpr int sfb_raw_off = sfa_raw_off + NS * SFA_RAW;
-    static constexpr int sfa_cp_off = sfb_raw_off + NS * SFB_RAW;
-    static constexpr int sfb_cp_off = sfa_cp_off + NS * SFA_CP;
-    static constexpr int bar_off = sfb_cp_off + NS * SFB_CP;
+    static constexpr int bar_off = sfb_raw_off + NS * SFB_RAW;
     static constexpr int n_bars = 3 * NS + 2 + 2 + 2;
     static constexpr int slot_off = bar_off + n_bars * 8;
     // epilogue staging per warp: a 32 x 32 transpose block (direct stores) or
@@ -408,8 +406,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint8_t *sB = smem + L::b_off;
     uint8_t *sfa_raw = smem + L::sfa_raw_off;
     uint8_t *sfb_raw = smem + L::sfb_raw_off;
-    uint8_t *sfa_cp = smem + L::sfa_cp_off;
-    uint8_t *sfb_cp = smem + L::sfb_cp_off;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::bar_off);
     uint64_t *full = bars;
     uint64_t *empty = bars + NS;
@@ -543,44 +539,27 @@ __global__ void __launch_bounds__(THREADS, 1)
         // all issued MMAs complete before TMEM is released
         mma_commit(done);
         mbar_wait_bounded(done, 0, WAIT_LIMIT_NS, p.err, ERR_TEARDOWN_WAIT);
-    } else if (warp == 10) {
-        // ---------------- scale factors ----------------
-        // For every stage: rearrange the scale words (row r's word at r) into
-        // the copy blocks (row 32j + L at lane L, word j), copy them into the
-        // stage's TMEM scale columns, and signal sf_full[stage] when the
-        // copies have landed.  Runs ahead of the MMA thread by up to the ring.
+    } else if (warp == 10 && lane == 0) {
+        // ---------------- scale copies ----------------
+        // the scale blocks arrive in copy order: each stage's three copies go
+        // out as soon as its loads have landed
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
         for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
             const Tile ti = tile_info<MODE>(p, t, tile_prefix, poff);
             for (int kb = 0; kb < ti.nkb; kb++) {
-                // the warp leaves together if the wait gives up in any lane
-                if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[stage], phase, WAIT_LIMIT_NS, p.err, ERR_MMA_WAIT))) {
+                if (!mbar_wait_bounded(&full[stage], phase, WAIT_LIMIT_NS, p.err, ERR_MMA_WAIT)) {
                     ok = false;
                     break;
                 }
-                const uint32_t *ra = reinterpret_cast<const uint32_t *>(sfa_raw + stage * SFA_RAW);
-                const uint32_t *rb = reinterpret_cast<const uint32_t *>(sfb_raw + stage * SFB_RAW);
-                uint8_t *ca = sfa_cp + stage * SFA_CP;
-                uint8_t *cb = sfb_cp + stage * SFB_CP;
-                *reinterpret_cast<uint4 *>(ca + lane * 16) =
-                    make_uint4(ra[lane], ra[32 + lane], ra[64 + lane], ra[96 + lane]);
-                *reinterpret_cast<uint4 *>(cb + lane * 16) =
-                    make_uint4(rb[lane], rb[32 + lane], rb[64 + lane], rb[96 + lane]);
-                *reinterpret_cast<uint4 *>(cb + 512 + lane * 16) =
-                    make_uint4(rb[128 + lane], rb[160 + lane], rb[192 + lane], rb[224 + lane]);
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                __syncwarp();
-                if (lane == 0) {
-                    tc_fence_after();
-                    const uint32_t sfa = tmem_base + SFA_COL + 4 * stage, sfb = tmem_base + SFB_COL + 8 * stage;
-                    tmem_cp_32x128b_x4(sfa, smem_desc_sf(smem_u32(ca)));
-                    tmem_cp_32x128b_x4(sfb, smem_desc_sf(smem_u32(cb)));
-                    tmem_cp_32x128b_x4(sfb + 4, smem_desc_sf(smem_u32(cb + 512)));
-                    mma_commit(&sf_full[stage]);
-                }
-                __syncwarp();
+                tc_fence_after();
+                const uint32_t sfa = tmem_base + SFA_COL + 4 * stage, sfb = tmem_base + SFB_COL + 8 * stage;
+                const uint32_t ra = smem_u32(sfa_raw + stage * SFA_RAW), rb = smem_u32(sfb_raw + stage * SFB_RAW);
+                tmem_cp_32x128b_x4(sfa, smem_desc_sf(ra));
+                tmem_cp_32x128b_x4(sfb, smem_desc_sf(rb));
+                tmem_cp_32x128b_x4(sfb + 4, smem_desc_sf(rb + 512));
+                mma_commit(&sf_full[stage]);
                 if (++stage == NS) {
                     stage = 0;
                     phase ^= 1;
@@ -588,11 +567,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
         }
         // every issued copy lands before TMEM is released
-        if (lane == 0) {
-            mma_commit(sf_done);
-            mbar_wait_bounded(sf_done, 0, WAIT_LIMIT_NS, p.err, ERR_TEARDOWN_WAIT);
-        }
-        __syncwarp();
+        mma_commit(sf_done);
+        mbar_wait_bounded(sf_done, 0, WAIT_LIMIT_NS, p.err, ERR_TEARDOWN_WAIT);
     } else if (warp >= 2 && warp < 10) {
         // ---------------- epilogue ----------------
         // warp w reads TMEM lane quarter w % 4 and one half (128 columns) of
@@ -738,8 +714,8 @@ extern "C" fp8_status_t fp8_mx_gemm(const uint8_t *A, int fa, int64_t lda, const
     p.K = K;
     p.sA = sA;
     p.sB = sB;
-    p.rsA = (M + 3) / 4 * 4;
-    p.rsB = (N + 3) / 4 * 4;
+    p.rsA = round_up_128(M);
+    p.rsB = round_up_128(N);
     p.C = static_cast<uint16_t *>(C_bf16);
     p.ldc = ldc;
     p.c_vec16 = ldc % 8 == 0 && aligned(C_bf16, 16);
@@ -771,6 +747,9 @@ extern "C" fp8_status_t fp8_mx_grouped_gemm(int mode, const uint8_t *A, int fa, 
         return FP8_ERR_INVALID_ARG;
     if (!aligned(A, 16) || !aligned(B, 16) || !aligned(sA, 16) || !aligned(sB, 16) || !aligned(C_bf16, 2))
         return FP8_ERR_ALIGNMENT;
+    // M-grouped: expert e's weight rows start at scale row e * N, which must
+    // start a 128-row block of the MX scale layout
+    if (mode == FP8_GROUPED_M && N % 128 != 0) return FP8_ERR_ALIGNMENT;
 
     mx::Params p{};
     p.M = M_total;
@@ -795,7 +774,7 @@ extern "C" fp8_status_t fp8_mx_grouped_gemm(int mode, const uint8_t *A, int fa, 
             if (ld_T % 16 != 0) return FP8_ERR_ALIGNMENT;
             if (ld_T < (int64_t)G * p.kpad || ld_T > INT32_MAX) return FP8_ERR_INVALID_ARG;
             p.b_trans = 1;
-            p.rsB = N;  // B's scale rows: the N rows of the transposed layout
+            p.rsB = round_up_128(N);  // B's scale rows: the N rows of the transposed layout
         }
         p.ldc = N;
         p.c_vec16 = N % 8 == 0 && aligned(C_bf16, 16);
@@ -811,8 +790,8 @@ extern "C" fp8_status_t fp8_mx_grouped_gemm(int mode, const uint8_t *A, int fa, 
     }
     // K-grouped (wgrad): C[e] = A_e [N][m_e] . B_e [K][m_e]^T
     if (ld_T < 128 || ld_T % 128 != 0 || N % 4 != 0 || K % 4 != 0) return FP8_ERR_ALIGNMENT;
-    p.rsA = N;
-    p.rsB = K;
+    p.rsA = round_up_128(N);
+    p.rsB = round_up_128(K);
     p.ldc = K;
     p.c_vec16 = K % 8 == 0 && aligned(C_bf16, 16);
     p.ld_T = ld_T;

@@ -42,7 +42,8 @@ struct MxArgs {
     int64_t rows, cols, ld_x;
     uint8_t *q_row, *s_row, *q_colT, *s_col;
     int64_t ld_colT;
-    int64_t rs_row;       // scale rows of s_row rounded up to 4 (ungrouped)
+    int64_t rs_row;       // scale rows of s_row, rows rounded up to 128 (ungrouped)
+    int64_t cols128;      // scale rows of s_col, cols rounded up to 128
     int64_t n_row_tiles;  // grouped: an upper bound (tiles past the padded total exit)
     int64_t n_col_tiles;
     const int32_t *offsets;
@@ -144,7 +145,9 @@ __device__ __forceinline__ MxTile mx_tile(const MxArgs &a, int64_t t, int64_t pr
     g.ct = t % a.n_col_tiles;
     g.pr0 = g.rt * MX_ROWS;
     g.c0 = g.ct * MX_COLS;
-    g.live = g.pr0 < prows;
+    // ungrouped: the row tiles run to the scale rows (rows rounded up to 128),
+    // so the padding rows' scale words are written too (as 0)
+    g.live = g.pr0 < (a.offsets ? prows : a.rs_row);
     g.src0 = g.pr0;
     g.nreal = a.rows - g.pr0 < MX_ROWS ? a.rows - g.pr0 : MX_ROWS;
     if (a.offsets && g.live) {
@@ -342,9 +345,9 @@ __global__ void __launch_bounds__(MX_THREADS)
             word |= __shfl_xor_sync(0xffffffffu, word, 1);
             word |= __shfl_xor_sync(0xffffffffu, word, 2);
             const int64_t srow = cur.pr0 + lr;  // scale row (padded row space)
-            const int64_t srows = a.offsets ? prows : a.rs_row;
+            const int64_t srows = a.offsets ? prows : a.rs_row;  // a multiple of 128 either way
             if (blk == 0 && srow < srows)
-                *reinterpret_cast<uint32_t *>(a.s_row + (cur.ct * srows + srow) * 4) = word;
+                *reinterpret_cast<uint32_t *>(a.s_row + mx_scale_word(cur.ct, srow, srows) * 4) = word;
         }
 
         // ---- transposed layout ----
@@ -367,38 +370,39 @@ __global__ void __launch_bounds__(MX_THREADS)
                 am = absmax_bf16x2(am, w[i]);
             }
             am = __vmaxu2(am, __shfl_xor_sync(0xffffffffu, am, 1));
-            if (c < a.cols) {
-                const uint32_t code0 = blk_valid ? mx_code<FMT>(am << 16) : 0u;
-                const uint32_t code1 = blk_valid ? mx_code<FMT>(am & 0xFFFF0000u) : 0u;
-                if (blk_valid) {
-                    const float inv0 = mx_inv_scale(code0), inv1 = mx_inv_scale(code1);
-                    uint32_t o0[4], o1[4];
+            const bool real = c < a.cols && blk_valid;  // columns past cols: padding scale rows
+            const uint32_t code0 = real ? mx_code<FMT>(am << 16) : 0u;
+            const uint32_t code1 = real ? mx_code<FMT>(am & 0xFFFF0000u) : 0u;
+            if (real) {
+                const float inv0 = mx_inv_scale(code0), inv1 = mx_inv_scale(code1);
+                uint32_t o0[4], o1[4];
 #pragma unroll
-                    for (int i = 0; i < 4; i++) {
-                        const uint32_t x0 = w[4 * i], x1 = w[4 * i + 1], x2 = w[4 * i + 2], x3 = w[4 * i + 3];
-                        float a0 = bf16lo(x0), a1 = bf16lo(x1), a2 = bf16lo(x2), a3 = bf16lo(x3);
-                        float c0 = bf16hi(x0), c1 = bf16hi(x1), c2 = bf16hi(x2), c3 = bf16hi(x3);
-                        mul2_rn(a0, a1, inv0, inv0);
-                        mul2_rn(a2, a3, inv0, inv0);
-                        mul2_rn(c0, c1, inv1, inv1);
-                        mul2_rn(c2, c3, inv1, inv1);
-                        o0[i] = cvt4<FMT>(a0, a1, a2, a3);
-                        o1[i] = cvt4<FMT>(c0, c1, c2, c3);
-                    }
-                    const int64_t r0 = cur.pr0 + 32 * h + 16 * s;
-                    *reinterpret_cast<uint4 *>(a.q_colT + c * a.ld_colT + r0) = make_uint4(o0[0], o0[1], o0[2], o0[3]);
-                    *reinterpret_cast<uint4 *>(a.q_colT + (c + 1) * a.ld_colT + r0) =
-                        make_uint4(o1[0], o1[1], o1[2], o1[3]);
+                for (int i = 0; i < 4; i++) {
+                    const uint32_t x0 = w[4 * i], x1 = w[4 * i + 1], x2 = w[4 * i + 2], x3 = w[4 * i + 3];
+                    float a0 = bf16lo(x0), a1 = bf16lo(x1), a2 = bf16lo(x2), a3 = bf16lo(x3);
+                    float c0 = bf16hi(x0), c1 = bf16hi(x1), c2 = bf16hi(x2), c3 = bf16hi(x3);
+                    mul2_rn(a0, a1, inv0, inv0);
+                    mul2_rn(a2, a3, inv0, inv0);
+                    mul2_rn(c0, c1, inv1, inv1);
+                    mul2_rn(c2, c3, inv1, inv1);
+                    o0[i] = cvt4<FMT>(a0, a1, a2, a3);
+                    o1[i] = cvt4<FMT>(c0, c1, c2, c3);
                 }
-                if (s == 0) {
-                    uint8_t *sc = a.s_col + ((kb >> 2) * a.cols + c) * 4 + (kb & 3);
-                    sc[0] = (uint8_t)code0;
-                    sc[4] = (uint8_t)code1;
-                    // the last word's blocks past the data are written as 0
-                    if (cur.rt == last_rt && (kb & 3) < 2) {
-                        sc[2] = 0;
-                        sc[6] = 0;
-                    }
+                const int64_t r0 = cur.pr0 + 32 * h + 16 * s;
+                *reinterpret_cast<uint4 *>(a.q_colT + c * a.ld_colT + r0) = make_uint4(o0[0], o0[1], o0[2], o0[3]);
+                *reinterpret_cast<uint4 *>(a.q_colT + (c + 1) * a.ld_colT + r0) =
+                    make_uint4(o1[0], o1[1], o1[2], o1[3]);
+            }
+            if (s == 0 && c < a.cols128) {
+                // columns c and c + 1 are scale rows c and c + 1 of s_col
+                uint8_t *sc0 = a.s_col + mx_scale_word(kb >> 2, c, a.cols128) * 4 + (kb & 3);
+                uint8_t *sc1 = a.s_col + mx_scale_word(kb >> 2, c + 1, a.cols128) * 4 + (kb & 3);
+                sc0[0] = (uint8_t)code0;
+                sc1[0] = (uint8_t)code1;
+                // the last word's blocks past the data are written as 0
+                if (cur.rt == last_rt && (kb & 3) < 2) {
+                    sc0[2] = 0;
+                    sc1[2] = 0;
                 }
             }
             __syncthreads();  // the tile is rewritten by the next iteration
@@ -458,7 +462,8 @@ static fp8_status_t mx_run(MxArgs a, int fmt, int layouts, int pro, cudaStream_t
     // row blocks start at x + r * ld_x + 32 k (+ up_off): 32-byte aligned
     // when the base is and the strides are multiples of 16 elements
     a.ld32 = aligned(a.x, 32) && a.ld_x % 16 == 0 && a.up_off % 16 == 0;
-    a.rs_row = (rows + 3) / 4 * 4;
+    a.rs_row = round_up_128(rows);
+    a.cols128 = round_up_128(cols);
     a.n_col_tiles = (cols + MX_COLS - 1) / MX_COLS;
     a.err = device_error_word();
     if (a.offsets) {
@@ -501,7 +506,7 @@ using namespace fp8gb;
 extern "C" int64_t fp8_mx_scale_bytes(int64_t scale_rows, int64_t blocks)
 {
     if (scale_rows < 0 || blocks < 0) return -1;
-    return (blocks + 3) / 4 * ((scale_rows + 3) / 4 * 4) * 4;
+    return (blocks + 3) / 4 * round_up_128(scale_rows) * 4;
 }
 
 extern "C" fp8_status_t fp8_mx_quantize(const void *x_bf16, int64_t rows, int64_t cols, int64_t ld_x, int fmt,

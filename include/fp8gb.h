@@ -350,14 +350,17 @@ FP8GB_API int64_t fp8_group_padded_offsets(const int32_t *host_offsets, int G, i
  * holding a NaN or Inf has code 255 and NaN elements.
  *
  * MX scale layout.  The E8M0 codes of an operand with R scale rows and KB
- * blocks per row are bytes [ceil(KB / 4)][roundup(R, 4)][4]: the scale of
- * block b of row r is at byte ((b / 4) * roundup(R, 4) + r) * 4 + b % 4.  A
- * row's four blocks of one 128-element K tile form one 32-bit word and the
- * words of consecutive rows are contiguous, so the scales of a GEMM tile are
- * a single contiguous copy.  Bytes of blocks past KB and of rows past R are
- * written as 0.  Grouped MX layouts pad every group to FP8_MX_GROUP_ALIGN
- * rows (fp8_group_padded_offsets with that align gives the padded offsets
- * and the total P).
+ * blocks per row are bytes [ceil(KB / 4)][R128][4] with R128 = roundup(R,
+ * 128): a row's four blocks of one 128-element K tile form one 32-bit word,
+ * and every 128 rows of a K tile are one 512-byte block in which row
+ * 128 i + 32 j + L has word 4 L + j -- the order in which the tensor cores'
+ * shared-to-tensor-memory copy (tcgen05.cp 32x128b) reads a 128-row block.
+ * The scale of block b of row r is at byte 4 * ((b / 4) * R128 + 128 (r /
+ * 128) + 4 (r % 32) + (r / 32) % 4) + b % 4, so the scales of a GEMM tile
+ * are one contiguous copy that the GEMM uses as it lands.  Bytes of blocks
+ * past KB and of rows past R are written as 0.  Grouped MX layouts pad every
+ * group to FP8_MX_GROUP_ALIGN rows (fp8_group_padded_offsets with that align
+ * gives the padded offsets and the total P).
  * ------------------------------------------------------------------------ */
 #define FP8_MX_BLOCK 32
 #define FP8_MX_GROUP_ALIGN 128
@@ -487,6 +490,8 @@ FP8GB_API fp8_status_t fp8_mx_gemm(const uint8_t *A, int fa, int64_t lda, const 
  * FP8_GROUPED_M: A u8 [M_total][K] (group rows stacked), sA the row-layout
  *   scales of a grouped fp8_mx_quantize (R = P, KB = K / 32); B u8 [G][N][K],
  *   sB its scales as one [G*N][K] operand (R = G * N); C bf16 [M_total][N].
+ *   N % 128 == 0 (expert e's scale rows start at row e * N, which must begin
+ *   a 128-row block of the MX scale layout), else FP8_ERR_ALIGNMENT.
  * FP8_GROUPED_K: A u8 [N][ld_T], B u8 [K][ld_T] the transposed layouts of
  *   grouped fp8_mx_quantize calls (ld_T their ld_colT), sA / sB their scales
  *   (R = N / K, KB = P / 32 with P the padded total); C[e] = A_e . B_e^T

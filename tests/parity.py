@@ -110,12 +110,14 @@ def bits(t: torch.Tensor) -> np.ndarray:
 
 
 def mx_tiled(plain: np.ndarray) -> np.ndarray:
-    """Plain E8M0 codes [R][KB] -> the bytes of the MX scale layout
-    [ceil(KB/4)][roundup(R, 4)][4] (scale of block b of row r at
-    ((b // 4) * roundup(R, 4) + r) * 4 + b % 4; pad bytes 0)."""
+    """Plain E8M0 codes [R][KB] -> the bytes of the MX scale layout: K tiles
+    of four blocks, [ceil(KB/4)][roundup(R, 128)][4], each 128-row block of
+    a K tile stored as [32 lanes][4 row groups][4 blocks] (row 32 j + L at
+    lane L, word j); pad bytes 0."""
     R, KB = plain.shape
     KT = -(-KB // 4)
-    Rs = -(-R // 4) * 4
+    Rs = -(-R // 128) * 128
     padded = np.zeros((Rs, KT * 4), np.uint8)
     padded[:R, :KB] = plain
-    return np.ascontiguousarray(padded.reshape(Rs, KT, 4).transpose(1, 0, 2)).reshape(-1)
+    t = padded.reshape(Rs // 128, 4, 32, KT, 4)          # [row block][j][L][kt][block]
+    return np.ascontiguousarray(t.transpose(3, 0, 2, 1, 4)).reshape(-1)

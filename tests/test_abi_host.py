@@ -226,8 +226,9 @@ def test_format_roles():
 
 
 def test_mx_scale_bytes(lib):
-    assert lib.fp8_mx_scale_bytes(5, 5) == 2 * 8 * 4      # ceil(5/4) K tiles x roundup(5,4) rows x 4
+    assert lib.fp8_mx_scale_bytes(5, 5) == 2 * 128 * 4    # ceil(5/4) K tiles x roundup(5,128) rows x 4
     assert lib.fp8_mx_scale_bytes(128, 128) == 32 * 128 * 4
+    assert lib.fp8_mx_scale_bytes(129, 4) == 1 * 256 * 4
     assert lib.fp8_mx_scale_bytes(0, 4) == 0
     assert lib.fp8_mx_scale_bytes(-1, 4) == -1
 
@@ -298,6 +299,7 @@ def test_mx_grouped_gemm_validation(lib):
     assert mxgg_call(lib, fa=3) == UNSUPPORTED
     assert mxgg_call(lib, K=96 + 16) == ALIGN
     assert mxgg_call(lib, N=254) == ALIGN                  # scale rows of a tile start on a word boundary
+    assert mxgg_call(lib, N=320) == ALIGN                  # M-grouped: experts' scale rows start 128-row blocks
     assert mxgg_call(lib, mode=1, ldT=192) == ALIGN        # groups padded to 128 columns
     assert mxgg_call(lib, mode=1, ldT=256, K=130) == ALIGN
 

@@ -226,7 +226,7 @@ def test_mx_grouped_m_small(orc):
     sizes = [5, 0, 200, 1, 0, 129, 64]
     G = len(sizes)
     off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
-    Mt, N, K = int(off[-1]), 300, 256
+    Mt, N, K = int(off[-1]), 384, 256     # N % 128 == 0: each expert's scale rows start a 128-row block
     xa = gen_x((Mt, K), seed=31)
     qa = orc.mx_quantize(bits(xa), 0, fp8.LAYOUT_ROW, offsets=off, align=128)
     B, sB = mx_operand(orc, G * N, K, 0, seed=32)
@@ -306,10 +306,10 @@ def test_mx_grouped_m_bt_small(orc, K):
 def test_mx_grouped_bad_offsets_flagged():
     off = torch.tensor([0, 50, 20, 64], dtype=torch.int32, device=DEV)
     A = torch.zeros((64, 128), dtype=torch.uint8, device=DEV)
-    B = torch.zeros((3 * 224, 128), dtype=torch.uint8, device=DEV)
+    B = torch.zeros((3 * 256, 128), dtype=torch.uint8, device=DEV)
     s = torch.zeros(1 << 16, dtype=torch.uint8, device=DEV)
-    C = torch.full((64, 224), 3.0, dtype=torch.bfloat16, device=DEV)
-    fp8.fp8_mx_grouped_gemm(fp8.GROUPED_M, A, 0, s, B, 0, s, off, 3, 64, 224, 128, C)
+    C = torch.full((64, 256), 3.0, dtype=torch.bfloat16, device=DEV)
+    fp8.fp8_mx_grouped_gemm(fp8.GROUPED_M, A, 0, s, B, 0, s, off, 3, 64, 256, 128, C)
     assert fp8.fp8_sync_status() == 1
     assert (C == 3.0).all()
 
