@@ -423,3 +423,24 @@ def test_quantize_equal_groups_moe_weight():
     assert torch.equal(qe.q_colT[:, :E * m], qo.q_colT[:, :E * m])
     assert torch.equal(qe.scale_inv_row.view(torch.int32), qo.scale_inv_row.view(torch.int32))
     assert torch.equal(qe.scale_inv_col.view(torch.int32), qo.scale_inv_col.view(torch.int32))
+
+
+@pytest.mark.parametrize("groups", [0, 40])
+def test_quantize_rowwise_tall(orc, groups):
+    """A tall tensor (163840 x 160, the last column chunk ragged): every
+    block's run of tiles in the amax pass spans several row blocks, and with
+    40 equal groups of 4096 rows many runs cross a group boundary; bytes and
+    scales bit-exact against the oracle."""
+    rows, cols, fmt = 163840, 160, 1
+    x = gen_x((rows, cols), seed=71 + groups)
+    off = np.arange(groups + 1, dtype=np.int32) * (rows // groups) if groups else None
+    rec = fp8.Recipe(kind=fp8.ROWWISE)
+    q = fp8.quantize(x.to(DEV), fmt, rec, 3, equal_groups=groups)
+    assert fp8.fp8_sync_status() == 0
+    ref = orc.quantize(bits(x), fmt, orc.ROWWISE, layouts=3, offsets=off)
+    what = f"tall, {groups} groups"
+    assert_codes_equal(q.q_row.cpu().numpy(), ref["q_row"], fmt, f"{what} q_row")
+    assert_f32_bits_equal(q.scale_inv_row.cpu().numpy(), ref["scale_inv_row"], f"{what} sinv_row")
+    assert_codes_equal(q.q_colT.cpu().numpy()[:, :rows], ref["q_colT"], fmt, f"{what} q_colT")
+    sc = q.scale_inv_col.cpu().numpy()
+    assert_f32_bits_equal(sc.reshape(groups, cols) if groups else sc, ref["scale_inv_col"], f"{what} sinv_col")
