@@ -141,8 +141,11 @@ struct MxTile {
 __device__ __forceinline__ MxTile mx_tile(const MxArgs &a, int64_t t, int64_t prows, const int32_t *poff, int &hint)
 {
     MxTile g;
-    g.rt = t / a.n_col_tiles;
-    g.ct = t % a.n_col_tiles;
+    // tile counts stay far below 2^32 (rows and columns are at most 2^31):
+    // a 32-bit division instead of a 64-bit one in every thread
+    const uint32_t tt = (uint32_t)t, nct = (uint32_t)a.n_col_tiles;
+    g.rt = tt / nct;
+    g.ct = tt - (uint32_t)g.rt * nct;
     g.pr0 = g.rt * MX_ROWS;
     g.c0 = g.ct * MX_COLS;
     // ungrouped: the row tiles run to the scale rows (rows rounded up to 128),
@@ -474,6 +477,7 @@ static fp8_status_t mx_run(MxArgs a, int fmt, int layouts, int pro, cudaStream_t
     } else {
         a.n_row_tiles = (a.rs_row + MX_ROWS - 1) / MX_ROWS;
     }
+    if (a.n_row_tiles * a.n_col_tiles >= (1LL << 32)) return FP8_ERR_INVALID_ARG;  // tile indices are 32-bit
     if (pro == PRO_GATHER) return fmt == FP8_E5M2 ? launch_mx<FP8_E5M2, PRO_GATHER>(a, st)
                                                   : launch_mx<FP8_E4M3FN, PRO_GATHER>(a, st);
     if (pro == PRO_SWIGLU) return fmt == FP8_E5M2 ? launch_mx<FP8_E5M2, PRO_SWIGLU>(a, st)
