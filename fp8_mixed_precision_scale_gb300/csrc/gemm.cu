@@ -28,8 +28,9 @@
 // Two more kernels share this structure (each described where it is
 // defined): fp8_gemm_pair_kernel, the dense GEMM for M > 128 on CTA pairs
 // (256 x 256 tiles from 2-SM MMAs, each CTA staging half of A and of B), and
-// fp8_gemm_kgroup_tma_kernel, the K-grouped wgrad whose epilogue writes
-// through 128-byte-swizzled boxes and TMA stores.
+// fp8_gemm_kgroup_tma_kernel, the K-grouped wgrad (576 threads: two groups
+// of eight epilogue warps on alternate tiles and accumulators, writing
+// through 128-byte-swizzled boxes and TMA stores).
 // Every mbarrier wait is bounded (about 2 s of wall time); a wait that gives
 // up records the device error word, drains in-flight copies, releases TMEM
 // and returns.
@@ -501,15 +502,18 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 // K-grouped GEMM (MoE wgrad) with a TMA-store epilogue.
 //
 // Each output tile of dW_e is written once and its contraction is short (one
-// expert's tokens), so the kernel is bound by writing C.  Here each epilogue
-// warp converts its 32 x 128 block to bf16 into two 32-row x 64-column boxes
-// in shared memory (128-byte swizzle: conflict-free 16-byte writes) and
-// issues their TMA stores itself; the copy drains asynchronously while the
-// warp reads the next accumulator, and the warp only waits for its previous
-// stores to finish reading shared memory before refilling its boxes.  A
-// 3-stage operand ring leaves room for the 64 KB of boxes.  Used when N is a
-// multiple of 32 (a 32-row quarter never straddles two experts' blocks), K
-// a multiple of 8 and C 16-byte aligned.
+// expert's tokens), so the kernel is bound by writing C.  Two groups of eight
+// epilogue warps take the CTA's tiles alternately, each group draining its
+// own TMEM accumulator, so a group has two tile periods for its drain,
+// conversion and stores while the MMAs of the next tile fill the other
+// accumulator.  Each epilogue warp converts its 32 x 128 block to bf16 in
+// two rounds of 64 columns through one 32-row x 64-column box in shared
+// memory (128-byte swizzle: conflict-free 16-byte writes) and issues the TMA
+// stores itself; it waits only for the box's previous store to finish
+// reading shared memory before refilling it.  An empty group's blocks are
+// stored from a zeroed box.  A 3-stage operand ring leaves room for the 64
+// KB of boxes.  Used when N is a multiple of 32 (a 32-row quarter never
+// straddles two experts' blocks), K a multiple of 8 and C 16-byte aligned.
 // ---------------------------------------------------------------------------
 constexpr int KT_STAGES = 3;
 constexpr int KT_BOX_BYTES = 32 * 128;  // 32 rows x 64 bf16
