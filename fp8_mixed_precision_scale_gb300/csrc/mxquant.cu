@@ -10,7 +10,9 @@
 // Design (GB300): persistent 256-thread blocks looping over tiles of 64 rows
 // x 128 columns; each block issues the next tile's loads before working on
 // the current one.
-//   Row layout: thread (row, block) loads its 32 bf16 (4 x 16-byte loads),
+//   Row layout: thread (row, block) loads its 32 bf16 (two 32-byte loads,
+//     whole sectors, when the row blocks are 32-byte aligned; else four
+//     16-byte loads),
 //     takes the packed |bf16| maximum, derives the E8M0 code from the fp32
 //     exponent bits, multiplies by 2^(127 - code) (exact) and converts with
 //     cvt.rn.satfinite; the four blocks of a row combine their codes into one
