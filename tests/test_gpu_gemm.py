@@ -197,6 +197,42 @@ def test_grouped_k_small(orc, sizes, NK):
             assert torch.all(C[e] == 0)
 
 
+def test_grouped_k_many_tiles_per_cta(orc):
+    """300 small groups with runs of empty ones at N = 256, K = 512: 1200
+    output tiles, so every CTA takes several in turn and both epilogue
+    groups, both accumulators and their phases are exercised; sampled
+    against the oracle, and every empty group's block is zero (over a NaN
+    sentinel)."""
+    rng = np.random.default_rng(300)
+    g = torch.Generator().manual_seed(300)
+    sizes = rng.integers(1, 80, size=300)
+    sizes[[0, 1, 2, 57, 150, 151, 299]] = 0
+    off = offsets_of(sizes)
+    poff = orc.padded_offsets(off)
+    ldT = max(16, int(poff[-1]))
+    G, N, K = len(sizes), 256, 512
+    AT = torch.zeros((N, ldT), dtype=torch.uint8)
+    BT = torch.zeros((K, ldT), dtype=torch.uint8)
+    for e, m in enumerate(sizes):
+        if m:
+            AT[:, poff[e]:poff[e] + m] = finite_codes(g, (N, int(m)), 1)
+            BT[:, poff[e]:poff[e] + m] = finite_codes(g, (K, int(m)), 0)
+    sa = scales(g, G * N, True)
+    sb = scales(g, G * K, True)
+    sentinel = torch.full((G, N, K), float("nan"), dtype=torch.bfloat16, device=DEV)
+    C = fp8.grouped_gemm(fp8.GROUPED_K, AT.to(DEV), 1, BT.to(DEV), 0, torch.from_numpy(off).to(DEV),
+                         int(off[-1]), N, K, sa.to(DEV), sb.to(DEV), ld_T=ldT, out=sentinel)
+    assert fp8.fp8_sync_status() == 0
+    pg = rng.integers(0, G, size=20000)
+    pn = rng.integers(0, N, size=20000)
+    pk = rng.integers(0, K, size=20000)
+    ref, bound = orc.grouped_gemm(1, AT.numpy(), 1, BT.numpy(), 0, off, N, K, sa.numpy(), sb.numpy(), pg, pn, pk)
+    out = C.float().cpu().numpy()
+    check_gemm(out[pg, pn, pk], ref, bound, "grouped K, 300 groups")
+    for e in np.flatnonzero(sizes == 0):
+        assert (out[e] == 0).all(), f"empty group {e}"
+
+
 def test_grouped_m_moe_shape_sampled(orc):
     """DeepSeek-V3 gate projection: 32768 routed rows, 256 experts, 7168 -> 2048."""
     sizes = synth.moe_group_sizes().numpy()

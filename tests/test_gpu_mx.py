@@ -272,6 +272,37 @@ def test_mx_grouped_k_small(orc, NK):
         check_gemm(out[e], ref, bound, f"kgroup e{e}")
 
 
+def test_mx_grouped_k_many_tiles_per_cta(orc):
+    """300 small groups with runs of empty ones at N = 256, K = 512: 1200
+    output tiles, several per CTA (the single accumulator handed between
+    tiles many times); 64 oracle points per non-empty group, empty groups'
+    blocks zero over a NaN sentinel."""
+    rng = np.random.default_rng(301)
+    sizes = rng.integers(1, 80, size=300)
+    sizes[[0, 1, 2, 57, 150, 151, 299]] = 0
+    G, N, K = len(sizes), 256, 512
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    Mt = int(off[-1])
+    qd = orc.mx_quantize(bits(gen_x((Mt, N), seed=43)), 1, fp8.LAYOUT_COLT, offsets=off, align=128)
+    qx = orc.mx_quantize(bits(gen_x((Mt, K), seed=44)), 0, fp8.LAYOUT_COLT, offsets=off, align=128)
+    P = qd["q_colT"].shape[1]
+    sentinel = torch.full((G, N, K), float("nan"), dtype=torch.bfloat16, device=DEV)
+    C = fp8.mx_grouped_gemm(fp8.GROUPED_K, up(qd["q_colT"]), 1, up(mx_tiled(qd["s_col"])), up(qx["q_colT"]), 0,
+                            up(mx_tiled(qx["s_col"])), up(off), Mt, N, K, ld_T=P, out=sentinel)
+    assert fp8.fp8_sync_status() == 0
+    poff = orc.padded_offsets_align(off, 128)
+    out = C.float().cpu().numpy()
+    for e in range(G):
+        if sizes[e] == 0:
+            assert (out[e] == 0).all(), f"empty group {e}"
+            continue
+        a, b = int(poff[e]), int(poff[e + 1])
+        pn, pk = rng.integers(0, N, size=64), rng.integers(0, K, size=64)
+        ref, bound = orc.mx_gemm(qd["q_colT"][:, a:b], 1, qd["s_col"][:, a // 32:b // 32],
+                                 qx["q_colT"][:, a:b], 0, qx["s_col"][:, a // 32:b // 32], points=(pn, pk))
+        check_gemm(out[e][pn, pk], ref, bound, f"kgroup many e{e}")
+
+
 @pytest.mark.parametrize("K", [256, 160])
 def test_mx_grouped_m_bt_small(orc, K):
     """dgrad on the weights' transposed layout: the weight stack [G*K][N]
