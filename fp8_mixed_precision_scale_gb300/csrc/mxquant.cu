@@ -15,7 +15,8 @@
 //     16-byte loads),
 //     takes the packed |bf16| maximum, derives the E8M0 code from the fp32
 //     exponent bits, multiplies by 2^(127 - code) (exact) and converts with
-//     cvt.rn.satfinite; the four blocks of a row combine their codes into one
+//     cvt.rn.satfinite, writing its 32 codes with one 32-byte store (q_row
+//     32-byte aligned); the four blocks of a row combine their codes into one
 //     32-bit word of the scale layout by two shuffles.
 //   Transposed layout: the tile is staged in shared memory (column pairs as
 //     32-bit words, swizzled); a thread reads two columns x 16 rows, takes
@@ -52,6 +53,7 @@ struct MxArgs {
     int G;
     int do_row, do_col;
     int ld32;  // every row block of the input starts on a 32-byte boundary: 32-byte loads
+    int st32;  // q_row is 32-byte aligned: each row block's 32 codes in one 32-byte store
     unsigned int *err;
     // prologues (template parameter PRO of the kernel)
     const int32_t *src_rows;  // PRO_GATHER: output row r reads input row src_rows[r]
@@ -193,6 +195,14 @@ __device__ __forceinline__ void ld_nc_32b(const uint16_t *p, uint4 &lo, uint4 &h
     asm volatile("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
                  : "=r"(lo.x), "=r"(lo.y), "=r"(lo.z), "=r"(lo.w), "=r"(hi.x), "=r"(hi.y), "=r"(hi.z), "=r"(hi.w)
                  : "l"(p));
+}
+
+// 32 bytes to a 32-byte-aligned address
+__device__ __forceinline__ void st_32b(void *p, const uint32_t (&o)[8])
+{
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(o[0]), "r"(o[1]),
+                 "r"(o[2]), "r"(o[3]), "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7])
+                 : "memory");
 }
 
 template <int PRO>
@@ -341,9 +351,13 @@ __global__ void __launch_bounds__(MX_THREADS)
                     out[2 * j] = b.x;
                     out[2 * j + 1] = b.y;
                 }
-                uint4 *dst = reinterpret_cast<uint4 *>(a.q_row + (cur.src0 + lr) * a.cols + cur.c0 + 32 * blk);
-                dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
-                dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
+                uint8_t *dst = a.q_row + (cur.src0 + lr) * a.cols + cur.c0 + 32 * blk;
+                if (a.st32) {
+                    st_32b(dst, out);
+                } else {
+                    reinterpret_cast<uint4 *>(dst)[0] = make_uint4(out[0], out[1], out[2], out[3]);
+                    reinterpret_cast<uint4 *>(dst)[1] = make_uint4(out[4], out[5], out[6], out[7]);
+                }
             }
             // the four blocks of the row (lanes 4i .. 4i+3) form one scale word
             uint32_t word = code << (8 * blk);
@@ -467,6 +481,7 @@ static fp8_status_t mx_run(MxArgs a, int fmt, int layouts, int pro, cudaStream_t
     // row blocks start at x + r * ld_x + 32 k (+ up_off): 32-byte aligned
     // when the base is and the strides are multiples of 16 elements
     a.ld32 = aligned(a.x, 32) && a.ld_x % 16 == 0 && a.up_off % 16 == 0;
+    a.st32 = a.q_row && aligned(a.q_row, 32);
     a.rs_row = round_up_128(rows);
     a.cols128 = round_up_128(cols);
     a.n_col_tiles = (cols + MX_COLS - 1) / MX_COLS;

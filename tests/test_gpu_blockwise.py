@@ -28,9 +28,10 @@ def gen_x(shape, seed, spread=8):
     return x.to(torch.bfloat16)
 
 
-def compare_bw(orc, x, fmt, block_rows, layouts=3, what=""):
+def compare_bw(orc, x, fmt, block_rows, layouts=3, what="", xd=None):
+    """xd: the device copy of x to quantize (default x.to(DEV)), e.g. a strided view"""
     ref = orc.blockwise_quantize(bits(x), fmt, block_rows, layouts)
-    q = fp8.blockwise_quantize(x.to(DEV), fmt, block_rows, layouts)
+    q = fp8.blockwise_quantize(x.to(DEV) if xd is None else xd, fmt, block_rows, layouts)
     torch.cuda.synchronize()
     assert fp8.fp8_sync_status() == 0
     rows = x.shape[0]
@@ -75,6 +76,61 @@ def test_blockwise_every_bf16_pattern(orc, fmt):
     perm = torch.randperm(65536, generator=torch.Generator().manual_seed(2))
     for block_rows in (1, 128):
         compare_bw(orc, pats[perm].reshape(256, 256), fmt, block_rows, what=f"patterns f{fmt} b{block_rows}")
+
+
+@pytest.mark.parametrize("block_rows", [1, 128])
+def test_blockwise_many_tiles_per_block(orc, block_rows):
+    """512 tiles of 128 x 128, more than the persistent grid holds: blocks
+    convert one tile while the next one's loads are in flight."""
+    compare_bw(orc, gen_x((4096, 2048), seed=11 + block_rows), 1, block_rows, what=f"4096x2048 b{block_rows}")
+
+
+@pytest.mark.parametrize("block_rows", [1, 128])
+def test_blockwise_rows_not_32_byte_aligned(orc, block_rows):
+    """Row pitch cols + 8 (rows 16-byte but not 32-byte aligned): the 16-byte load path."""
+    x = gen_x((384, 384), seed=21)
+    pad = torch.zeros((384, 392), dtype=torch.bfloat16)
+    pad[:, :384] = x
+    compare_bw(orc, x, 0, block_rows, what=f"ld 392 b{block_rows}", xd=pad.to(DEV)[:, :384])
+
+
+def test_blockwise_row_output_16_byte_aligned(orc):
+    """q_row 16-byte but not 32-byte aligned: the row layout's 16-byte stores."""
+    x = gen_x((256, 384), seed=23)
+    ref = orc.blockwise_quantize(bits(x), 0, 1, 1)
+    rows, cols = x.shape
+    buf = torch.zeros(rows * cols + 48, dtype=torch.uint8, device=DEV)
+    off = 16 if buf.data_ptr() % 32 == 0 else 0  # a 16-byte but not 32-byte aligned start
+    q_row = buf[off:off + rows * cols]
+    s_row = torch.zeros(fp8.fp8_mx_scale_bytes(rows, cols // 32), dtype=torch.uint8, device=DEV)
+    xd = x.to(DEV)
+    fp8.fp8_blockwise_quantize(xd, rows, cols, cols, 0, 1, 1, q_row, s_row, None, 0, None)
+    torch.cuda.synchronize()
+    assert fp8.fp8_sync_status() == 0
+    assert_codes_equal(q_row.cpu().numpy().reshape(rows, cols), ref["q_row"], 0, "q_row at +16")
+    e = mx_tiled(ref["s_row"])
+    assert np.array_equal(s_row.cpu().numpy()[:e.size], e)
+    assert (buf[:off].cpu().numpy() == 0).all() and (buf[off + rows * cols:].cpu().numpy() == 0).all()
+
+
+@pytest.mark.parametrize("block_rows", [1, 128])
+def test_blockwise_colT_pitch_16_not_32(orc, block_rows):
+    """Transposed layout at a row pitch of rows + 16 (16-byte but not 32-byte
+    aligned rows); the pitch's padding bytes stay untouched."""
+    x = gen_x((256, 256), seed=41)
+    ref = orc.blockwise_quantize(bits(x), 1, block_rows, 2)
+    rows, cols = x.shape
+    ld = rows + 16
+    q_colT = torch.zeros((cols, ld), dtype=torch.uint8, device=DEV)
+    s_col = torch.zeros(fp8.fp8_mx_scale_bytes(cols, rows // 32), dtype=torch.uint8, device=DEV)
+    fp8.fp8_blockwise_quantize(x.to(DEV), rows, cols, cols, 1, block_rows, 2, None, None, q_colT, ld, s_col)
+    torch.cuda.synchronize()
+    assert fp8.fp8_sync_status() == 0
+    got = q_colT.cpu().numpy()
+    assert_codes_equal(got[:, :rows], ref["q_colT"], 1, f"q_colT pitch {ld} b{block_rows}")
+    assert (got[:, rows:] == 0).all()
+    e = mx_tiled(ref["s_col"])
+    assert np.array_equal(s_col.cpu().numpy()[:e.size], e)
 
 
 def test_blockwise_llama_weight_full(orc):

@@ -144,6 +144,43 @@ def test_mx_quantize_llama_activation_full(orc):
     compare_mx(orc, x, 0, 3, what="llama X")
 
 
+def test_mx_quantize_row_output_16_byte_aligned(orc):
+    """q_row 16-byte but not 32-byte aligned: the row layout's 16-byte stores."""
+    x = gen_x((96, 160), seed=31)
+    ref = orc.mx_quantize(bits(x), 1, fp8.LAYOUT_ROW, offsets=None, align=fp8.MX_GROUP_ALIGN)
+    rows, cols = x.shape
+    buf = torch.zeros(rows * cols + 48, dtype=torch.uint8, device=DEV)
+    off = 16 if buf.data_ptr() % 32 == 0 else 0  # a 16-byte but not 32-byte aligned start
+    q_row = buf[off:off + rows * cols]
+    s_row = torch.zeros(fp8.fp8_mx_scale_bytes(rows, cols // 32), dtype=torch.uint8, device=DEV)
+    fp8.fp8_mx_quantize(x.to(DEV), rows, cols, cols, 1, fp8.LAYOUT_ROW, q_row, s_row, None, 0, None)
+    torch.cuda.synchronize()
+    assert fp8.fp8_sync_status() == 0
+    assert_codes_equal(q_row.cpu().numpy().reshape(rows, cols), ref["q_row"], 1, "q_row at +16")
+    exp = mx_tiled(ref["s_row"])
+    assert np.array_equal(s_row.cpu().numpy()[:exp.size], exp)
+    assert (buf[:off].cpu().numpy() == 0).all() and (buf[off + rows * cols:].cpu().numpy() == 0).all()
+
+
+def test_mx_quantize_colT_pitch_16_not_32(orc):
+    """Transposed layout at a row pitch of rows + 16 (16-byte but not 32-byte
+    aligned rows); the pitch's padding bytes stay untouched."""
+    x = gen_x((64, 160), seed=37)
+    ref = orc.mx_quantize(bits(x), 0, fp8.LAYOUT_COLT, offsets=None, align=fp8.MX_GROUP_ALIGN)
+    rows, cols = x.shape
+    ld = rows + 16
+    q_colT = torch.zeros((cols, ld), dtype=torch.uint8, device=DEV)
+    s_col = torch.zeros(fp8.fp8_mx_scale_bytes(cols, rows // 32), dtype=torch.uint8, device=DEV)
+    fp8.fp8_mx_quantize(x.to(DEV), rows, cols, cols, 0, fp8.LAYOUT_COLT, None, None, q_colT, ld, s_col)
+    torch.cuda.synchronize()
+    assert fp8.fp8_sync_status() == 0
+    got = q_colT.cpu().numpy()
+    assert_codes_equal(got[:, :rows], ref["q_colT"], 0, "q_colT pitch 80")
+    assert (got[:, rows:] == 0).all()
+    exp = mx_tiled(ref["s_col"])
+    assert np.array_equal(s_col.cpu().numpy()[:exp.size], exp)
+
+
 def test_mx_quantize_deterministic():
     x = gen_x((256, 512), seed=5).to(DEV)
     a = fp8.mx_quantize(x, 0)
