@@ -34,7 +34,7 @@ namespace fp8gb {
 
 constexpr int BW_THREADS = 512;
 constexpr int BW_TILE = 128;
-constexpr int BW_PITCH_W = BW_TILE / 2 + 4;  // 32-bit words (column pairs) per shared row, padded
+constexpr int BW_PITCH_W = BW_TILE / 2 + 8;  // 32-bit words per shared row: 64 column pairs + two 4-word pads
 
 struct BwArgs {
     const uint16_t *x;
@@ -68,12 +68,17 @@ __device__ __forceinline__ float bw_scale(uint32_t code)  // s = 2^(127 - code),
     return __uint_as_float((254u - code) << 23);
 }
 
-// Shared tile word of (row, column pair).  Rows are 68 words apart (4 banks
-// mod 32) and the pair index is XORed with 4 x the row's 16-row group: the
-// row phase's 16-byte stores (eight rows x four 32-column slices per warp)
-// and the transposed phase's word reads (eight 16-row slices x four column
-// pairs per warp) each reach all 32 banks.
-__device__ __forceinline__ int bw_word(int row, int pair) { return row * BW_PITCH_W + (pair ^ (((row >> 4) & 7) << 2)); }
+// Shared tile word of (row, column pair).  The pair index is XORed with 4 x
+// the row's 16-row group, rows are 72 words apart (8 banks mod 32) and a
+// 4-word gap follows the first 32 pairs of a row: each quarter warp of the
+// row phase's 16-byte stores (two rows x four 32-column slices) reaches all
+// 32 banks, and so does each warp of the transposed phase's word reads
+// (eight 16-row slices x four column pairs).
+__device__ __forceinline__ int bw_word(int row, int pair)
+{
+    const int pp = pair ^ (((row >> 4) & 7) << 2);
+    return row * BW_PITCH_W + pp + 4 * (pp >> 5);
+}
 
 // 32 bytes (16 bf16) from a 32-byte-aligned address through the read-only
 // path, as two 16-byte halves
