@@ -8,8 +8,8 @@
 // v1.0 one: X = 2^(floor(log2 amax) - emax_elem), element = sat_rne(v / X).
 //
 // Design (GB300): persistent 256-thread blocks looping over tiles of 64 rows
-// x 128 columns; each block issues the next tile's loads before working on
-// the current one.
+// x 128 columns (row-major; tall tensors in bands of eight column tiles);
+// each block issues the next tile's loads before working on the current one.
 //   Row layout: thread (row, block) loads its 32 bf16 (two 32-byte loads,
 //     whole sectors, when the row blocks are 32-byte aligned; else four
 //     16-byte loads),
@@ -39,6 +39,8 @@ constexpr int MX_ROWS = 64;             // rows per tile
 constexpr int MX_COLS = 128;            // columns per tile: four blocks of a row
 constexpr int MX_PITCH_W = 72;          // 32-bit words per shared-memory row (64 + two 4-word pads)
 constexpr int MX_MAX_GROUPS = 4096;
+constexpr int MX_BAND_TILES = 8;           // column tiles per band of the ungrouped tile walk
+constexpr int64_t MX_BAND_MIN_ROWS = 65536;  // ... used from this many rows on
 
 struct MxArgs {
     const uint16_t *x;
@@ -49,6 +51,7 @@ struct MxArgs {
     int64_t cols128;      // scale rows of s_col, cols rounded up to 128
     int64_t n_row_tiles;  // grouped: an upper bound (tiles past the padded total exit)
     int64_t n_col_tiles;
+    int band;  // ungrouped: tiles walked in bands of `band` column tiles (0: row-major)
     const int32_t *offsets;
     int G;
     int do_row, do_col;
@@ -148,8 +151,18 @@ __device__ __forceinline__ MxTile mx_tile(const MxArgs &a, int64_t t, int64_t pr
     // tile counts stay far below 2^32 (rows and columns are at most 2^31):
     // a 32-bit division instead of a 64-bit one in every thread
     const uint32_t tt = (uint32_t)t, nct = (uint32_t)a.n_col_tiles;
-    g.rt = tt / nct;
-    g.ct = tt - (uint32_t)g.rt * nct;
+    if (a.band) {
+        // row-major inside bands of `band` column tiles (the last band narrower)
+        const uint32_t per = (uint32_t)a.band * (uint32_t)a.n_row_tiles;
+        const uint32_t bnd = tt / per, r = tt - bnd * per, c_lo = bnd * (uint32_t)a.band;
+        const uint32_t w = nct - c_lo < (uint32_t)a.band ? nct - c_lo : (uint32_t)a.band;
+        const uint32_t rt = r / w;
+        g.rt = rt;
+        g.ct = c_lo + (r - rt * w);
+    } else {
+        g.rt = tt / nct;
+        g.ct = tt - (uint32_t)g.rt * nct;
+    }
     g.pr0 = g.rt * MX_ROWS;
     g.c0 = g.ct * MX_COLS;
     // ungrouped: the row tiles run to the scale rows (rows rounded up to 128),
@@ -495,6 +508,12 @@ static fp8_status_t mx_run(MxArgs a, int fmt, int layouts, int pro, cudaStream_t
         a.n_row_tiles = (a.rs_row + MX_ROWS - 1) / MX_ROWS;
     }
     if (a.n_row_tiles * a.n_col_tiles >= (1LL << 32)) return FP8_ERR_INVALID_ARG;  // tile indices are 32-bit
+    // Tall tensors (q_colT rows of 64 KB and more) walk their tiles in column
+    // bands, so the tiles in flight write runs of a few KB into a few
+    // thousand q_colT rows rather than 512-byte pieces into all of them:
+    // measured 9 % faster on a [1048576, 7168] expert-weight stack, 2 % slower
+    // on [8192, 14336], where row-major order stays.
+    a.band = !a.offsets && rows >= MX_BAND_MIN_ROWS && a.n_col_tiles > MX_BAND_TILES ? MX_BAND_TILES : 0;
     if (pro == PRO_GATHER) return fmt == FP8_E5M2 ? launch_mx<FP8_E5M2, PRO_GATHER>(a, st)
                                                   : launch_mx<FP8_E4M3FN, PRO_GATHER>(a, st);
     if (pro == PRO_SWIGLU) return fmt == FP8_E5M2 ? launch_mx<FP8_E5M2, PRO_SWIGLU>(a, st)

@@ -137,6 +137,13 @@ def test_mx_quantize_bad_offsets_flagged():
     assert fp8.fp8_sync_status() == 0
 
 
+def test_mx_quantize_tall_band_walk(orc):
+    """A tall tensor (65600 rows: tiles walked in bands of eight column tiles)
+    with nine column tiles (a last band one tile wide) and a padding row tile
+    past the data (rows rounded up to 128), both layouts in full."""
+    compare_mx(orc, gen_x((65600, 1152), seed=43), 1, 3, what="65600x1152")
+
+
 def test_mx_quantize_llama_activation_full(orc):
     """Llama-3-8B MLP input [8192, 4096], both layouts, compared in full."""
     g = torch.Generator().manual_seed(1)
