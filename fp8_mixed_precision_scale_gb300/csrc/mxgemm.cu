@@ -393,12 +393,14 @@ __device__ __noinline__ void zero_block_tma(const Params &p, const Tile &ti, int
     }
 }
 
-template <int MODE, bool TMA_OUT>
+// NS_: ring stages (0: ring_stages(MODE, TMA_OUT)); the M-grouped modes run
+// a four-stage ring when the group tables leave room for it
+template <int MODE, bool TMA_OUT, int NS_ = 0>
 __global__ void __launch_bounds__(THREADS, 1)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, Params p, uint32_t idesc)
 {
-    constexpr int NS = ring_stages(MODE, TMA_OUT);
+    constexpr int NS = NS_ ? NS_ : ring_stages(MODE, TMA_OUT);
     using L = Smem<NS, TMA_OUT>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -652,10 +654,11 @@ static bool make_map(CUtensorMap *map, const void *base, int64_t rows, int64_t c
     return r == CUDA_SUCCESS;
 }
 
-template <int MODE, bool TMA_OUT>
+template <int MODE, bool TMA_OUT, int NS_ = 0>
 static size_t smem_bytes(int G)
 {
-    return 1024 + Smem<ring_stages(MODE, TMA_OUT), TMA_OUT>::misc_off + (G > 0 ? 8 * (size_t)(G + 1) : 0);
+    constexpr int NS = NS_ ? NS_ : ring_stages(MODE, TMA_OUT);
+    return 1024 + Smem<NS, TMA_OUT>::misc_off + (G > 0 ? 8 * (size_t)(G + 1) : 0);
 }
 
 // 2D map over the bf16 output viewed as [rows][cols] (row stride cols), box
@@ -674,17 +677,30 @@ static bool make_map_c(CUtensorMap *map, void *base, int64_t rows, int64_t cols)
     return r == CUDA_SUCCESS;
 }
 
+template <int MODE, bool TMA_OUT, int NS_>
+static fp8_status_t launch_ns(const CUtensorMap &ma, const CUtensorMap &mb, const Params &p, int fa, int fb,
+                              int64_t grid, cudaStream_t st, const CUtensorMap *mc)
+{
+    const size_t smem = smem_bytes<MODE, TMA_OUT, NS_>(MODE == MODE_DENSE ? 0 : p.G);
+    cudaError_t e = cudaFuncSetAttribute(mx_gemm_kernel<MODE, TMA_OUT, NS_>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return cuda_fail_with(e);
+    const uint32_t idesc = idesc_mxf8f6f4(fa, fb, BM, BN);
+    mx_gemm_kernel<MODE, TMA_OUT, NS_><<<(unsigned)grid, THREADS, smem, st>>>(ma, mb, mc ? *mc : ma, p, idesc);
+    return check_launch();
+}
+
 template <int MODE, bool TMA_OUT = false>
 static fp8_status_t launch(const CUtensorMap &ma, const CUtensorMap &mb, const Params &p, int fa, int fb,
                            int64_t grid, cudaStream_t st, const CUtensorMap *mc = nullptr)
 {
-    const size_t smem = smem_bytes<MODE, TMA_OUT>(MODE == MODE_DENSE ? 0 : p.G);
-    cudaError_t e = cudaFuncSetAttribute(mx_gemm_kernel<MODE, TMA_OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return cuda_fail_with(e);
-    const uint32_t idesc = idesc_mxf8f6f4(fa, fb, BM, BN);
-    mx_gemm_kernel<MODE, TMA_OUT><<<(unsigned)grid, THREADS, smem, st>>>(ma, mb, mc ? *mc : ma, p, idesc);
-    return check_launch();
+    // grouped modes with direct stores: four stages when the group tables fit
+    // beside them (up to about 800 groups), else three
+    if constexpr (MODE != MODE_DENSE && !TMA_OUT) {
+        if (smem_bytes<MODE, false, STAGES>(p.G) <= 227 * 1024)
+            return launch_ns<MODE, false, STAGES>(ma, mb, p, fa, fb, grid, st, mc);
+    }
+    return launch_ns<MODE, TMA_OUT, 0>(ma, mb, p, fa, fb, grid, st, mc);
 }
 
 static bool format_ok(int f) { return f == FP8_E4M3FN || f == FP8_E5M2; }

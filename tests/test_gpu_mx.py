@@ -288,6 +288,41 @@ def test_mx_grouped_m_small(orc):
         check_gemm(out[r0:r1], ref, bound, f"mgroup e{e}")
 
 
+def _mx_grouped_m_check(orc, sizes, N, K, seed, every=1):
+    G = len(sizes)
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    Mt = int(off[-1])
+    xa = gen_x((Mt, K), seed=seed)
+    qa = orc.mx_quantize(bits(xa), 0, fp8.LAYOUT_ROW, offsets=off, align=128)
+    B, sB = mx_operand(orc, G * N, K, 0, seed=seed + 1)
+    C = fp8.mx_grouped_gemm(fp8.GROUPED_M, up(qa["q_row"]), 0, up(mx_tiled(qa["s_row"])), up(B), 0,
+                            up(mx_tiled(sB)), up(off), Mt, N, K)
+    assert fp8.fp8_sync_status() == 0
+    poff = orc.padded_offsets_align(off, 128)
+    out = C.float().cpu().numpy()
+    live = [e for e in range(G) if sizes[e] > 0]
+    for e in live[::every] + live[-1:]:
+        r0, r1 = off[e], off[e + 1]
+        ref, bound = orc.mx_gemm(qa["q_row"][r0:r1], 0, qa["s_row"][poff[e]:poff[e] + sizes[e]],
+                                 B[e * N:(e + 1) * N], 0, sB[e * N:(e + 1) * N])
+        check_gemm(out[r0:r1], ref, bound, f"mgroup G{G} e{e}")
+
+
+def test_mx_grouped_m_deep_k(orc):
+    """Ten k-blocks per tile: the (four-stage) ring wraps inside every tile
+    and across a CTA's tiles."""
+    _mx_grouped_m_check(orc, [300, 0, 129, 64, 1, 256], 256, 1280, seed=61)
+
+
+def test_mx_grouped_m_1000_groups(orc):
+    """1000 groups: their tables leave no room for a fourth ring stage, so
+    the M-grouped kernel runs its three-stage form (every 25th non-empty
+    group and the last one checked in full)."""
+    g = np.random.default_rng(63)
+    sizes = [int(v) for v in g.integers(0, 5, size=1000)]
+    _mx_grouped_m_check(orc, sizes, 128, 384, seed=63, every=25)
+
+
 @pytest.mark.parametrize("NK", [(200, 300), (192, 296), (96, 520)])
 def test_mx_grouped_k_small(orc, NK):
     """(200, 300) takes the direct-store epilogue; N % 32 == 0 with K % 8 == 0
