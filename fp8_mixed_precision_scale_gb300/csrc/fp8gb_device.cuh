@@ -531,14 +531,6 @@ __device__ __forceinline__ uint2 cvt8_scaled(const uint4 &v, float s)
 // SwiGLU element function shared by the fused MoE prologues of the MX and
 // the rowwise quantizers.
 // ---------------------------------------------------------------------------
-// fp32 -> bf16 bits, round to nearest even; NaN stays a quiet NaN.
-__device__ __forceinline__ uint32_t bf16_bits_rne(float f)
-{
-    uint32_t u = __float_as_uint(f);
-    if ((u & 0x7FFFFFFFu) > 0x7F800000u) return (u >> 16) | 0x40u;
-    u += 0x7FFFu + ((u >> 16) & 1u);
-    return u >> 16;
-}
 
 // silu(g) * u in fp32, with sigma(g) = 1 / (1 + e^-g) formed from t = e^-|g|
 // (never overflows): sigma = 1 / (1 + t) for g >= 0, t / (1 + t) for g < 0.
@@ -560,10 +552,11 @@ __device__ __forceinline__ float swiglu1(float g, float u)
     return fabsf(u) >= 1.0f ? s * (u * 0x1p-126f) : (s * u) * 0x1p-126f;
 }
 
-// h = bf16(silu(g) * u) for a packed pair.
+// h = bf16(silu(g) * u) for a packed pair: one round-to-nearest-even
+// conversion of both products (a NaN product becomes the canonical NaN).
 __device__ __forceinline__ uint32_t swiglu2(uint32_t g2, uint32_t u2)
 {
-    return bf16_bits_rne(swiglu1(bf16lo(g2), bf16lo(u2))) | (bf16_bits_rne(swiglu1(bf16hi(g2), bf16hi(u2))) << 16);
+    return pack_bf16x2(swiglu1(bf16lo(g2), bf16lo(u2)), swiglu1(bf16hi(g2), bf16hi(u2)));
 }
 
 // ---------------------------------------------------------------------------
