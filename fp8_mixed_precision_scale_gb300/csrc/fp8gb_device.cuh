@@ -547,9 +547,12 @@ __device__ __forceinline__ float swiglu1(float g, float u)
     constexpr float LN2_X126 = 87.3365479f;  // 126 ln 2: e^(x + 126 ln 2) = 2^126 e^x
     const float t = __expf(LN2_X126 - fabsf(g));
     const float r = __fdividef(1.0f, fmaf(t, 0x1p-126f, 1.0f));
-    if (g >= 0.0f) return (g * r) * u;
+    // both signs' forms are evaluated and one is selected: the signs of a
+    // warp's elements differ, and a branch per element diverges
+    const float pos = (g * r) * u;
     const float s = t == 0.0f ? -0.0f : g * (t * r);  // 2^126 silu(g); t == 0 also for g = -Inf
-    return fabsf(u) >= 1.0f ? s * (u * 0x1p-126f) : (s * u) * 0x1p-126f;
+    const float neg = fabsf(u) >= 1.0f ? s * (u * 0x1p-126f) : (s * u) * 0x1p-126f;
+    return g >= 0.0f ? pos : neg;
 }
 
 // h = bf16(silu(g) * u) for a packed pair: one round-to-nearest-even
