@@ -372,7 +372,10 @@ __global__ void __launch_bounds__(QT_THREADS) amax_kernel(QArgs a)
 // Persistent blocks, each owning a contiguous run of tiles in row-major tile
 // order, so consecutive tiles mostly belong to the same row block: the row
 // maxima stay in registers across the run and are flushed (one relaxed
-// atomic per row) only when the row block changes or the run ends.  The next
+// atomic per row) only when the row block changes or the run ends.  The
+// tile coordinates are stepped along the run (one division per run, none
+// per tile), and an equal-groups tensor's group is looked up only when the
+// row block changes.  The next
 // tile's 16-byte loads are issued before the current tile is reduced, so
 // every thread keeps loads in flight while it reduces.  Column maxima are
 // reduced per tile (shuffles, then shared memory across the 8 warps) and
