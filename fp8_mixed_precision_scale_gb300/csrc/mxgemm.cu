@@ -114,20 +114,20 @@ struct Smem {
     static constexpr int n_bars = 3 * NS + 2 + 2 + 2;
     static constexpr int slot_off = bar_off + n_bars * 8;
     // epilogue staging per warp: a 32 x 32 transpose block (direct stores) or
-    // one 32-row x 64-column TMA box, filled twice per tile (1024-aligned for
-    // the 128-byte swizzle)
-    static constexpr int stage_warp = TMA_OUT ? 32 * 128 : 32 * 80;
+    // one 32-row x 32-column TMA box (64-byte rows, 64-byte swizzle), filled
+    // four times per tile; 2 KB a warp leaves room for a four-stage ring
+    static constexpr int stage_warp = TMA_OUT ? 32 * 64 : 32 * 80;
     static constexpr int stage_off = TMA_OUT ? (slot_off + 16 + 1023) / 1024 * 1024 : (slot_off + 16 + 127) / 128 * 128;
     static constexpr int misc_off = stage_off + 8 * stage_warp;  // group tables
 };
 constexpr int STAGE_PITCH = 80;  // epilogue staging: 32 rows x 32 bf16 per warp, rows padded to 80 bytes
 __host__ __device__ constexpr int ring_stages(int mode, bool tma_out)
 {
-    return tma_out ? STAGES_GROUPED : (mode == 0 ? STAGES : STAGES_GROUPED);
+    return tma_out ? STAGES : (mode == 0 ? STAGES : STAGES_GROUPED);
 }
 // dynamic (ring, staging, group tables, 1024 alignment slack) plus the static
 // block fit the 227 KB a block may use
-static_assert(1024 + Smem<STAGES_GROUPED, true>::misc_off + 8 * (MAX_GROUPS + 1) + 1024 <= 227 * 1024, "smem");
+static_assert(1024 + Smem<STAGES, true>::misc_off + 8 * (MAX_GROUPS + 1) + 1024 <= 227 * 1024, "smem");
 static_assert(1024 + Smem<STAGES_GROUPED, false>::misc_off + 8 * (MAX_GROUPS + 1) + 1024 <= 227 * 1024, "smem");
 static_assert(1024 + Smem<STAGES, false>::misc_off + 1024 <= 227 * 1024, "smem");
 
@@ -339,30 +339,27 @@ __device__ __forceinline__ void epilogue_tile_tma(const Params &p, const Tile &t
     if (lane == 0) mbar_arrive(tempty);
     const int64_t qrow0 = ti.row0 + q * 32;
     const int32_t y = (int32_t)(ti.c_base / p.ldc + qrow0);  // row of the [G*N][K] view of C
-    // two rounds of 64 columns through the warp's one box
+    // four rounds of 32 columns through the warp's one box
 #pragma unroll
-    for (int b = 0; b < 2; b++) {
+    for (int b = 0; b < 4; b++) {
         // the box's previous store must have read it before it is refilled
         if (lane == 0) bulk_wait_group_read0();
         __syncwarp();
-        uint8_t *brow = box + lane * 128;
+        uint8_t *brow = box + lane * 64;
 #pragma unroll
-        for (int h = 0; h < 2; h++) {
-            const int u = 2 * b + h;
-#pragma unroll
-            for (int g = 0; g < 4; g++) {
-                const int chunk = (h * 4 + g) ^ (lane & 7);
-                *reinterpret_cast<uint4 *>(brow + chunk * 16) =
-                    make_uint4(pack_bf16x2(__uint_as_float(r[u][8 * g]), __uint_as_float(r[u][8 * g + 1])),
-                               pack_bf16x2(__uint_as_float(r[u][8 * g + 2]), __uint_as_float(r[u][8 * g + 3])),
-                               pack_bf16x2(__uint_as_float(r[u][8 * g + 4]), __uint_as_float(r[u][8 * g + 5])),
-                               pack_bf16x2(__uint_as_float(r[u][8 * g + 6]), __uint_as_float(r[u][8 * g + 7])));
-            }
+        for (int g = 0; g < 4; g++) {
+            // 64-byte swizzle: 16-byte chunk g of row `lane` at chunk g ^ ((lane >> 1) & 3)
+            const int chunk = g ^ ((lane >> 1) & 3);
+            *reinterpret_cast<uint4 *>(brow + chunk * 16) =
+                make_uint4(pack_bf16x2(__uint_as_float(r[b][8 * g]), __uint_as_float(r[b][8 * g + 1])),
+                           pack_bf16x2(__uint_as_float(r[b][8 * g + 2]), __uint_as_float(r[b][8 * g + 3])),
+                           pack_bf16x2(__uint_as_float(r[b][8 * g + 4]), __uint_as_float(r[b][8 * g + 5])),
+                           pack_bf16x2(__uint_as_float(r[b][8 * g + 6]), __uint_as_float(r[b][8 * g + 7])));
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
         if (lane == 0 && qrow0 < ti.row_end) {
-            const int64_t x = ti.col0 + cb + 64 * b;
+            const int64_t x = ti.col0 + cb + 32 * b;
             if (x < ti.col_end) tma_store_2d(tmC, (int32_t)x, y, box);
             bulk_commit_group();
         }
@@ -379,14 +376,14 @@ __device__ __noinline__ void zero_block_tma(const Params &p, const Tile &ti, int
     if (lane == 0) bulk_wait_group_read0();
     __syncwarp();
 #pragma unroll
-    for (int k = 0; k < 32 * 128 / 16 / 32; k++) reinterpret_cast<uint4 *>(box)[k * 32 + lane] = make_uint4(0, 0, 0, 0);
+    for (int k = 0; k < 32 * 64 / 16 / 32; k++) reinterpret_cast<uint4 *>(box)[k * 32 + lane] = make_uint4(0, 0, 0, 0);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncwarp();
     const int64_t qrow0 = ti.row0 + q * 32;
     if (lane == 0 && qrow0 < ti.row_end) {
         const int32_t y = (int32_t)(ti.c_base / p.ldc + qrow0);
-        for (int b = 0; b < 2; b++) {
-            const int64_t x = ti.col0 + cb + 64 * b;
+        for (int b = 0; b < 4; b++) {
+            const int64_t x = ti.col0 + cb + 32 * b;
             if (x < ti.col_end) tma_store_2d(tmC, (int32_t)x, y, box);
         }
         bulk_commit_group();
@@ -662,17 +659,17 @@ static size_t smem_bytes(int G)
 }
 
 // 2D map over the bf16 output viewed as [rows][cols] (row stride cols), box
-// {64, 32}, 128-byte swizzle: the TMA-store epilogue.
+// {32, 32}, 64-byte swizzle: the TMA-store epilogue.
 static bool make_map_c(CUtensorMap *map, void *base, int64_t rows, int64_t cols)
 {
     EncodeTiledFn enc = get_encode_fn();
     if (!enc) return false;
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-    cuuint32_t box[2] = {64, 32};
+    cuuint32_t box[2] = {32, 32};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
