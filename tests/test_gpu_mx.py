@@ -144,6 +144,12 @@ def test_mx_quantize_tall_band_walk(orc):
     compare_mx(orc, gen_x((65600, 1152), seed=43), 1, 3, what="65600x1152")
 
 
+def test_mx_quantize_band_threshold_ragged_cols(orc):
+    """Exactly the row count from which tiles are walked in column bands
+    (65536), with ten column tiles the last of which is a quarter full."""
+    compare_mx(orc, gen_x((65536, 1184), seed=47), 0, 3, what="65536x1184")
+
+
 def test_mx_quantize_llama_activation_full(orc):
     """Llama-3-8B MLP input [8192, 4096], both layouts, compared in full."""
     g = torch.Generator().manual_seed(1)

@@ -425,12 +425,13 @@ def test_quantize_equal_groups_moe_weight():
     assert torch.equal(qe.scale_inv_col.view(torch.int32), qo.scale_inv_col.view(torch.int32))
 
 
-@pytest.mark.parametrize("groups", [0, 40])
+@pytest.mark.parametrize("groups", [0, 40, 2560])
 def test_quantize_rowwise_tall(orc, groups):
     """A tall tensor (163840 x 160, the last column chunk ragged): every
     block's run of tiles in the amax pass spans several row blocks, and with
-    40 equal groups of 4096 rows many runs cross a group boundary; bytes and
-    scales bit-exact against the oracle."""
+    40 equal groups of 4096 rows many runs cross a group boundary (2560 groups
+    of 64 rows: every row block starts a group); bytes and scales bit-exact
+    against the oracle."""
     rows, cols, fmt = 163840, 160, 1
     x = gen_x((rows, cols), seed=71 + groups)
     off = np.arange(groups + 1, dtype=np.int32) * (rows // groups) if groups else None
