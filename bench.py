@@ -41,6 +41,10 @@ Other workloads (same JSON line, their own config):
   mx_grouped_k   the MXFP8 K-grouped wgrad of that layer, for profiling
   quantize_grouped  the rowwise quantize of one reduced MoE weight (64
                  experts x 2048 rows x 7168), for profiling
+  stack_quantize, mx_stack_quantize  the rowwise (256 equal groups) / MX
+                 quantize of a whole DeepSeek-V3 expert-weight stack, as the
+                 MoE steps run it: gate|up [256 x 4096, 7168], or with
+                 --stack down [256 x 7168, 2048]
   mx_gemm, mx_quantize  the MXFP8 gate GEMM / the MX quantize of dY_gate
   mx_permute, mx_swiglu  fused MoE prologue + MX quantize at DeepSeek-V3
                  shapes (gather of 4096 x top-8 routed rows of 7168; SwiGLU
@@ -1020,7 +1024,7 @@ def run_gpu(args, rank, world, local_rank):
 
     if args.workload in ("gemm", "quantize", "grouped_m", "grouped_k", "mx_grouped_k", "quantize_grouped", "mx_gemm",
                          "mx_quantize", "mx_permute", "mx_swiglu", "permute", "swiglu", "bw_quantize", "rowwise_quantize",
-                         "rowwise_resident"):
+                         "rowwise_resident", "stack_quantize", "mx_stack_quantize"):
         run_single_kernel(args, dev, rank)
         return
     if args.workload == "sweep":
@@ -1474,6 +1478,33 @@ def grouped_weight_quantize_case(dev, E=64):
     return fn, quantize_bytes((rows, H)) / 1e9, "GB/s (algorithmic)"
 
 
+def weight_stack_case(kind, stack, dev):
+    """Quantize of a whole DeepSeek-V3 expert-weight stack (256 experts,
+    gate|up fused: [256 x 4096, 7168]; down: [256 x 7168, 2048]), both
+    layouts, as the MoE steps quantize their weights: rowwise with 256 equal
+    groups (`stack_quantize`) or MX (`mx_stack_quantize`)."""
+    import fp8_mixed_precision_scale_gb300 as fp8
+    import synth
+    E, H, F = synth.DSV3["E"], synth.DSV3["H"], synth.DSV3["F"]
+    rows, cols = (E * 2 * F, H) if stack == "gateup" else (E * H, F)
+    g = torch.Generator(device=dev)
+    g.manual_seed(11)
+    w = _normal(g, dev, (rows, cols), 0.02)
+    if kind == "mx_stack_quantize":
+        q = fp8.mx_quantize(w, 0)
+        fn = lambda: fp8.fp8_mx_quantize(w, rows, cols, cols, 0, 3, q.q_row, q.s_row, q.q_colT,  # noqa: E731
+                                         q.ld_colT, q.s_col)
+        return fn, rows * cols * (2 + 2 + 2 / 32) / 1e9, "GB/s (algorithmic)"
+    q_row = torch.empty((rows, cols), dtype=torch.uint8, device=dev)
+    q_colT = torch.empty((cols, rows), dtype=torch.uint8, device=dev)
+    sr = torch.empty(rows, device=dev)
+    sc = torch.empty(E * cols, device=dev)
+    rec = fp8.Recipe(kind=fp8.ROWWISE)
+    fn = lambda: fp8.fp8_quantize(w, rows, cols, cols, 0, rec, 3, None, None, q_row, sr, q_colT, rows, sc,  # noqa: E731
+                                  None, E)
+    return fn, quantize_bytes((rows, cols)) / 1e9, "GB/s (algorithmic)"
+
+
 def moe_fused_case(kind, dev, T=4096, topk=8, E=256):
     """DeepSeek-V3-shaped fused MoE prologue + MX quantize (both layouts,
     per-expert grouping): `mx_permute` gathers 4096 tokens x top-8 routed
@@ -1539,6 +1570,8 @@ def run_single_kernel(args, dev, rank):
         fn, work, unit = grouped_case(args.workload, dev)
     elif args.workload == "quantize_grouped":
         fn, work, unit = grouped_weight_quantize_case(dev)
+    elif args.workload in ("stack_quantize", "mx_stack_quantize"):
+        fn, work, unit = weight_stack_case(args.workload, args.stack, dev)
     elif args.workload == "mx_gemm":
         step = MxStep(dev, 1, keys=("x", "w_gate"), outs=("gate",))
         for k in ("x", "w_gate"):
@@ -1650,6 +1683,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-configuration measurements")
+    ap.add_argument("--stack", default="gateup", choices=["gateup", "down"],
+                    help="stack_quantize / mx_stack_quantize: which DeepSeek-V3 expert-weight stack")
     ap.add_argument("--workload", default="llama_mlp",
                     choices=["llama_mlp", "llama_rowwise", "llama_mxfp8", "llama_blockwise", "moe", "moe_unfused",
                              "moe_mxfp8", "flux", "tiny",
@@ -1657,7 +1692,7 @@ def main():
                              "gemm", "quantize", "bw_quantize", "rowwise_quantize", "rowwise_resident",
                              "grouped_m", "grouped_k", "mx_grouped_k", "quantize_grouped", "mx_gemm", "mx_quantize",
                              "mx_permute",
-                             "mx_swiglu", "permute", "swiglu"],
+                             "mx_swiglu", "permute", "swiglu", "stack_quantize", "mx_stack_quantize"],
                     help="llama_mlp: the whole fwd+bwd FP8 step of the Llama-3-8B MLP (default); see the "
                          "module docstring for the others")
     args = ap.parse_args()
