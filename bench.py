@@ -38,7 +38,8 @@ Other workloads (same JSON line, their own config):
   gemm, quantize single kernels of the default step, for profiling
   grouped_m, grouped_k  one M-grouped / K-grouped expert GEMM of a reduced
                  MoE layer (64 experts, 8192 routed rows), for profiling
-  mx_grouped_k   the MXFP8 K-grouped wgrad of that layer, for profiling
+  mx_grouped_m, mx_grouped_k  the MXFP8 M-grouped fprop / K-grouped wgrad of
+                 that layer, for profiling
   quantize_grouped  the rowwise quantize of one reduced MoE weight (64
                  experts x 2048 rows x 7168), for profiling
   stack_quantize, mx_stack_quantize  the rowwise (256 equal groups) / MX
@@ -1022,9 +1023,9 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.set_device(dev)
     hbm_gbs = peaks()[0]
 
-    if args.workload in ("gemm", "quantize", "grouped_m", "grouped_k", "mx_grouped_k", "quantize_grouped", "mx_gemm",
-                         "mx_quantize", "mx_permute", "mx_swiglu", "permute", "swiglu", "bw_quantize", "rowwise_quantize",
-                         "rowwise_resident", "stack_quantize", "mx_stack_quantize"):
+    if args.workload in ("gemm", "quantize", "grouped_m", "grouped_k", "mx_grouped_m", "mx_grouped_k",
+                         "quantize_grouped", "mx_gemm", "mx_quantize", "mx_permute", "mx_swiglu", "permute", "swiglu",
+                         "bw_quantize", "rowwise_quantize", "rowwise_resident", "stack_quantize", "mx_stack_quantize"):
         run_single_kernel(args, dev, rank)
         return
     if args.workload == "sweep":
@@ -1436,6 +1437,18 @@ def grouped_case(kind, dev, E=64, rows=8192):
                                           s_ef, 1, C, 0)
         wbytes = int((sizes > 0).sum()) * F * H
         return fn, (rows * H + wbytes + 2.0 * rows * F) / 1e9, "GB/s (algorithmic)"
+    if kind == "mx_grouped_m":    # MXFP8 fprop of the gate projection (MX-quantized routed rows and weights)
+        gb = torch.Generator(device=dev)
+        gb.manual_seed(9)
+        x = torch.randn((rows, H), generator=gb, device=dev).to(torch.bfloat16)
+        w = (torch.randn((E * F, H), generator=gb, device=dev) * 0.02).to(torch.bfloat16)
+        qa = fp8.mx_quantize(x, 0, fp8.LAYOUT_ROW, group_offsets=off_d, host_offsets=torch.from_numpy(off))
+        qw = fp8.mx_quantize(w, 0, fp8.LAYOUT_ROW)
+        C = torch.empty((rows, F), dtype=torch.bfloat16, device=dev)
+        fn = lambda: fp8.fp8_mx_grouped_gemm(fp8.GROUPED_M, qa.q_row, 0, qa.s_row, qw.q_row, 0, qw.s_row,  # noqa
+                                             off_d, E, rows, F, H, C, 0)
+        wbytes = int((sizes > 0).sum()) * F * H
+        return fn, (rows * H + wbytes + 2.0 * rows * F) / 1e9, "GB/s (algorithmic)"
     if kind == "mx_grouped_k":    # MXFP8 wgrad of the gate projection from grouped MX quantizes
         gb = torch.Generator(device=dev)
         gb.manual_seed(8)
@@ -1566,7 +1579,7 @@ def run_single_kernel(args, dev, rank):
     if args.workload in ("mx_permute", "mx_swiglu", "permute", "swiglu"):
         fn, unfused, work = moe_fused_case(args.workload, dev)
         unit = "GB/s (algorithmic)"
-    elif args.workload in ("grouped_m", "grouped_k", "mx_grouped_k"):
+    elif args.workload in ("grouped_m", "grouped_k", "mx_grouped_m", "mx_grouped_k"):
         fn, work, unit = grouped_case(args.workload, dev)
     elif args.workload == "quantize_grouped":
         fn, work, unit = grouped_weight_quantize_case(dev)
@@ -1690,7 +1703,8 @@ def main():
                              "moe_mxfp8", "flux", "tiny",
                              "sweep",
                              "gemm", "quantize", "bw_quantize", "rowwise_quantize", "rowwise_resident",
-                             "grouped_m", "grouped_k", "mx_grouped_k", "quantize_grouped", "mx_gemm", "mx_quantize",
+                             "grouped_m", "grouped_k", "mx_grouped_m", "mx_grouped_k", "quantize_grouped", "mx_gemm",
+                             "mx_quantize",
                              "mx_permute",
                              "mx_swiglu", "permute", "swiglu", "stack_quantize", "mx_stack_quantize"],
                     help="llama_mlp: the whole fwd+bwd FP8 step of the Llama-3-8B MLP (default); see the "
